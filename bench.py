@@ -1,0 +1,359 @@
+"""Benchmark of the routed NVFP4 MoE decode layer-step on GB300.
+
+Default workload: one layer at serving width -- b = 8 rows (one request
+verifying 1 + 7 tokens), hidden 7168, 256 experts, top-8, expert intermediate
+2048, NVFP4 experts -- plus the final boundary, replayed as one CUDA graph.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+
+Prints one JSON line.  value = microseconds per layer-step (lower is better),
+timed with CUDA events around K graph replays on device-resident inputs; the
+weights of the ~57 activated experts (~1.4 GB per step) exceed L2 (129 MB)
+many times over and each step uses a different input draw.  `roofline` is
+the gate/up expert kernel (the largest share of the bytes), timed with CUDA
+events around its own launches; `e2e` is the same step through the host-buffer
+entry point (pinned H2D of the step inputs, D2H of its outputs, inside the
+timed region); `cpu_baseline` is the CPU oracle on a bounded sample.
+Multi-GPU (torchrun): one independent replica per GPU (the step has no
+exchange on one GPU's worth of experts), max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE decode layer-step µs at b=8 and weight-stream HBM GB/s vs GB300 peak"
+UNIT = "µs"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _algorithmic_bytes(w: synth.Workload, n_active: int, rows: int):
+    """Bytes one layer-step must move at minimum (weights read once)."""
+    H, I, E, k = w.hidden, w.inter, w.n_experts, w.top_k
+    gate_up = n_active * 2 * I * (H // 2 + H // 16) + n_active * 8
+    down = n_active * H * (I // 2 + I // 16) + n_active * 4
+    router = 2 * E * H + (4 * E if w.zipf_bias else 0)
+    acts = rows * H * (4 + 4 + 2)                 # stream read + write, branch / gathered y
+    return dict(gate_up=gate_up + rows * H // 2 + rows * k * I * 4, down=down, router=router,
+                total=gate_up + down + router + acts)
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        mx = max(mx, float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+        finally:
+            os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(x: float, ws: int, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_baseline(w: synth.Workload, n_sample_experts: int = 4):
+    """The CPU oracle, as it stands, on a bounded sample of one layer-step:
+    the boundary, router and routing of every row, and the experts of
+    `n_sample_experts` activated experts (all their pairs); the expert time is
+    scaled to the step's activated experts.  -> (us per layer-step, info)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from helpers import oracle_weights
+
+    stream, branch = synth.step_inputs(w)
+    br = oracle.bf16_to_f64(branch)
+    w_post, w_pre = synth.norm_weights(w, 0)
+    rw = synth.router_weights(w, 0)
+    bias = synth.router_bias(w, 0)
+    t0 = time.perf_counter()
+    s1, x, _ = oracle.boundary(br, stream, w_post, w_pre, w.eps)
+    r = oracle.route(x, rw, bias, w.top_k)
+    pl = oracle.pool(r["ids"], w.n_experts)
+    xc, xs, xg, _ = oracle.nvfp4_quantize(oracle.bf16_to_f64(x).astype(np.float32))
+    t_front = time.perf_counter() - t0
+    act = list(pl["active"])
+    rs = np.random.RandomState(0)
+    sample = sorted(int(e) for e in rs.choice(act, size=min(n_sample_experts, len(act)), replace=False))
+    ow = oracle_weights(w, 0, experts=sample)          # input preparation, not timed
+    from helpers import expert_subproblem
+    t_exp = 0.0
+    for e in sample:
+        p0, p1 = pl["offset"][e], pl["offset"][e + 1]
+        pairs = pl["pair_order"][p0:p1]
+        n = p1 - p0
+        sub = expert_subproblem(ow, e)
+        zi, off, order = np.zeros((n, 1), np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32)
+        t1 = time.perf_counter()
+        h = oracle.gate_up(sub, 1, xc[pairs // w.top_k], xs[pairs // w.top_k], xg, zi, off, order)
+        hq = oracle.h_quant(1, w.inter, off, h)
+        oracle.down(sub, 1, zi, off, order, hq["h_codes"], hq["h_sf"], hq["h_sg"])
+        t_exp += time.perf_counter() - t1
+    t_step = t_front + t_exp * len(act) / len(sample)
+    info = {"kind": "oracle", "cores": oracle.num_threads(),
+            "sample": f"boundary+router+routing of all {w.rows} rows; experts of {len(sample)} of "
+                      f"{len(act)} activated experts (all their pairs), scaled to {len(act)}"}
+    return t_step * 1e6, info
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    times = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        us, info = cpu_baseline(w, n_sample_experts=2)
+        if i >= args.warmup:
+            times.append(us)
+    v = float(np.mean(times))
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(v / 1000.0 * w.n_layers, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden,
+                       "n_experts": w.n_experts, "top_k": w.top_k, "inter": w.inter,
+                       "n_layers": w.n_layers},
+            "cpu_baseline": dict(info, value=round(v, 1), unit=UNIT),
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args, w):
+    import torch
+
+    import speculative_decode_routed_gb300 as moe
+    import synth.gpu as sgpu
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    dec = sgpu.build(w, device=device)
+    V = 4                                             # distinct input draws, cycled
+    bufs = []
+    for v in range(V):
+        s, b = sgpu.step_tensors(w, variant=v, device=device)
+        bufs.append((s, b, torch.empty_like(b)))
+    rows = w.rows
+    cs = torch.cuda.current_stream(device)
+
+    # active experts of each draw (for the byte count): one eager layer per draw
+    n_active = []
+    for s, b, o in bufs:
+        st = s.clone()
+        dec.layer(0, rows, b, st)
+        torch.cuda.synchronize(device)
+        n_active.append(int(torch.as_tensor(
+            _Cai(dec.debug().n_active, (1,), "<i4"), device=device).item()))
+    dec.check()
+
+    for i in range(args.warmup):
+        s, b, o = bufs[i % V]
+        dec.step_graph(rows, b, s, o)
+    torch.cuda.synchronize(device)
+    _barrier(ws)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+        ev0.record(cs)
+        for i in range(args.steps):
+            s, b, o = bufs[i % V]
+            dec.step_graph(rows, b, s, o)
+        ev1.record(cs)
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+    dec.check()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = _max_over_ranks(ms, ws, device)
+    us_layer = ms * 1000.0 / w.n_layers
+    clocks = clk.summary()
+
+    # per-kernel durations (events on the launching stream around each kernel)
+    prof = []
+    for i in range(max(3, min(args.steps, 20))):
+        s, b, o = bufs[i % V]
+        prof.append(dec.layer_profile(0, rows, b, s))
+    prof = np.array(prof)
+    k_ms = prof.mean(0)
+    na = float(np.mean(n_active))
+    byt = _algorithmic_bytes(w, int(round(na)), rows)
+    peak, peak_kind = _peaks()
+    gu_gbs = byt["gate_up"] / (k_ms[2] * 1e-3) / 1e9
+    dn_gbs = byt["down"] / (k_ms[3] * 1e-3) / 1e9
+    step_gbs = byt["total"] * w.n_layers / (ms * 1e-3) / 1e9 * ws
+
+    # end to end through the host-buffer entry point
+    s_h, b_h = synth.step_inputs(w)
+    sh = torch.from_numpy(s_h).pin_memory()
+    bh = torch.from_numpy(b_h).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(bh).pin_memory()
+    for _ in range(3):
+        dec.step_host(rows, bh, sh, oh)
+    _barrier(ws)
+    t0 = time.perf_counter()
+    n_e2e = max(args.steps, 5)
+    for _ in range(n_e2e):
+        dec.step_host(rows, bh, sh, oh)
+    e2e_ms = (time.perf_counter() - t0) * 1000.0 / n_e2e
+    e2e_ms = _max_over_ranks(e2e_ms, ws, device)
+
+    if rank != 0:
+        dec.close()
+        return
+    line = {
+        "metric": METRIC, "value": round(us_layer, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1",
+        "data": "synthetic (seeded Philox / Irwin-Hall normals, NVFP4-packed on device)",
+        "config": {"workload": w.name, "rows": rows, "hidden": w.hidden, "n_experts": w.n_experts,
+                   "top_k": w.top_k, "inter": w.inter, "n_layers": w.n_layers,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "graph": "one CUDA graph per step (layers + final boundary)",
+                   "l2": "inputs larger than L2: ~%.2f GB of expert weights per step, 4 input draws cycled" % (byt["total"] / 1e9)},
+        "weight_stream_gbs": round(step_gbs, 1),
+        "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
+        "bytes_per_layer_step": int(byt["total"]), "n_active_mean": na,
+        "roofline": {"kernel": "experts gate/up", "bound": "hbm", "achieved": round(gu_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gu_gbs / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind,
+                     "launch_us": round(k_ms[2] * 1000, 2),
+                     "algorithmic_bytes": int(byt["gate_up"])},
+        "kernels_us": {"boundary": round(k_ms[0] * 1000, 2), "router": round(k_ms[1] * 1000, 2),
+                       "gate_up": round(k_ms[2] * 1000, 2), "down": round(k_ms[3] * 1000, 2),
+                       "down_gbs": round(dn_gbs, 1)},
+        "e2e": {"value": round(e2e_ms * 1000.0 / w.n_layers, 2), "unit": UNIT,
+                "h2d_bytes_per_step": rows * w.hidden * (2 + 4),
+                "d2h_bytes_per_step": rows * w.hidden * (4 + 2)},
+        "gpu_launches": moe.moe_decode_step_kernel_count(dec.handle) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        us, info = cpu_baseline(w)
+        line["cpu_baseline"] = dict(info, value=round(us, 1), unit=UNIT)
+    print(json.dumps(line), flush=True)
+    dec.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+class _Cai:
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="serving", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.rows:
+        w = w.with_rows(args.rows)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_native(args, w)
+
+
+if __name__ == "__main__":
+    main()

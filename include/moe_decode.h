@@ -1,0 +1,200 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) routed NVFP4 mixture-of-experts
+ * decode layer-step.
+ *
+ * What one layer-step computes (the specialized decode executor page,
+ * vllm.models.muse_spark.nvidia.specialized_decode.runtime.decode, module
+ * docstring "One step of b rows" -- one request verifying 1 + 7 tokens, b
+ * rows; the attention boundary "all-reduce + the dual norm into the stream
+ * and the MoE input"; the MoE "router -> routing -> pooler -> routed experts
+ * -> tail -> unpooler"; "final: the last gather + dual norm"; the dual norm's
+ * form is MuseSparkDSparkDecoderLayer.forward on the DSpark page,
+ * vllm.models.muse_spark.common.dspark):
+ *
+ *   stream' = stream + rmsnorm(branch) * w_post            fp32 stream
+ *   x       = bf16(rmsnorm(stream') * w_pre)               MoE input
+ *   logit   = x Wr^T (+ bias);  p = softmax(logit)
+ *   ids     = top-k of p (ties to the lower id), slots by descending p
+ *   gates   = p[ids] / sum p[ids]
+ *   xq      = NVFP4(x)                 one tensor over all rows
+ *   h       = silu(Wg xq) * (Wu xq)    per (row, slot), fp32
+ *   hq      = NVFP4(h)                 one tensor per expert (its rows)
+ *   o       = Wd hq                    per (row, slot), fp32
+ *   y[r]    = sum_s gates[r][s] o[r][s]   -> the next layer's branch, or
+ *   final:  stream' = stream + rmsnorm(y) * w_post_final;
+ *           out = bf16(rmsnorm(stream') * w_final)
+ *
+ * NVFP4 (every expert weight and activation operand): element = e2m1 code
+ * (4 bits) * e4m3 block scale (one per 16 consecutive elements along the
+ * reduction dimension) * fp32 tensor scale; tensor scale = amax / (6 * 448);
+ * block scale = e4m3(amax_blk / 6 / tensor scale), round to nearest even,
+ * saturating; code = e2m1(v / (block scale * tensor scale)).
+ *
+ * Conventions
+ *  - Every pointer is a DEVICE pointer unless the name ends in _host.  The
+ *    caller owns all of them; weights must stay valid until destroy.  The
+ *    library owns only its workspace, sized at create (no allocation later).
+ *  - Layouts (row-major, K-major weights):
+ *      router_w  bf16 [E][H]
+ *      w13       e2m1x2 [E][2I][H/2]  rows 0..I-1 gate, I..2I-1 up;
+ *                element 2j in the low nibble of byte j
+ *      w13_sf    e4m3 [E][2I][H/16]
+ *      w2        e2m1x2 [E][H][I/2],  w2_sf e4m3 [E][H][I/16]
+ *      w_gscale  fp32 [E][3]          tensor scales of gate, up, down
+ *      stream    fp32 [rows][H];  branch / out bf16 [rows][H]
+ *  - Alignment: w13, w13_sf, w2, w2_sf, router_w 16 bytes; fp32 arrays and
+ *    stream 16 bytes; branch and out 8 bytes.
+ *  - Errors: functions return MOE_OK (0) or a negative MOE_E* code, checked
+ *    before anything is launched; moe_decode_error_message() gives the reason
+ *    of the last failure on this thread.  Faults detected on the device
+ *    (a bounded wait that gave up, an out-of-range routing value) latch a
+ *    flag read by moe_decode_last_error().  Nothing here traps on the device.
+ *  - Asynchrony: layer / final / step calls are asynchronous on the given CUDA
+ *    stream (a cudaStream_t passed as void*; NULL = the legacy default
+ *    stream), allocate nothing and never synchronize, so they can be
+ *    captured into a CUDA graph.  A handle serves one stream at a time.
+ *  - Supported shapes: H and I multiples of 128, at most 8192;
+ *    1 <= top_k <= min(E, 16); E <= 1024; 1 <= rows <= max_rows <= 128.
+ *    The device must be of the SM 10.x family (built for sm_103a).
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,        /* a null / misaligned pointer or an out-of-range argument */
+  MOE_EUNSUPPORTED = -2,  /* a shape or device this library does not serve */
+  MOE_ECUDA = -3,         /* a CUDA runtime call failed */
+  MOE_ENOMEM = -4,        /* the workspace could not be allocated */
+  MOE_EDEVICE = -5        /* a device-side check latched an error */
+};
+
+typedef struct moe_decode_s moe_decode_t;
+
+typedef struct {
+  int hidden;     /* H */
+  int n_experts;  /* E */
+  int top_k;      /* k */
+  int inter;      /* I: expert intermediate width */
+  int max_rows;   /* largest b any call will use */
+  int n_layers;   /* L */
+  float eps;      /* RMSNorm epsilon */
+} moe_decode_dims;
+
+typedef struct {
+  const float* w_post;        /* [H]  norm weight of the incoming branch */
+  const float* w_pre;         /* [H]  norm weight of the stream -> MoE input */
+  const uint16_t* router_w;   /* bf16 [E][H] */
+  const float* router_bias;   /* [E] additive logit bias, or NULL */
+  const uint8_t* w13;         /* e2m1x2 [E][2I][H/2] */
+  const uint8_t* w13_sf;      /* e4m3 [E][2I][H/16] */
+  const uint8_t* w2;          /* e2m1x2 [E][H][I/2] */
+  const uint8_t* w2_sf;       /* e4m3 [E][H][I/16] */
+  const float* w_gscale;      /* [E][3] */
+} moe_layer_weights;
+
+/* Device pointers into the workspace, holding the last layer run's
+ * intermediates (for staged checks).  Scalars are device pointers too. */
+typedef struct {
+  const uint16_t* x;          /* bf16 [rows][H]: MoE input */
+  const uint8_t* x_codes;     /* [rows][H/2] */
+  const uint8_t* x_sf;        /* [rows][H/16] */
+  const float* x_sg;          /* [1] */
+  const float* logits;        /* [rows][E] */
+  const int32_t* ids;         /* [rows][k] */
+  const float* gates;         /* [rows][k] */
+  const uint8_t* flags;       /* [rows] */
+  const int32_t* count;       /* [E] */
+  const int32_t* offset;      /* [E+1] */
+  const int32_t* pair_order;  /* [rows*k]: pair id r*k+s at each pooled position */
+  const int32_t* pos_of_pair; /* [rows*k] */
+  const int32_t* active;      /* [E] (n_active used) */
+  const int32_t* n_active;    /* [1] */
+  const float* h;             /* [rows*k][I], pooled order */
+  const float* h_sg;          /* [E] */
+  const uint8_t* h_codes;     /* [rows*k][I/2], pooled order */
+  const uint8_t* h_sf;        /* [rows*k][I/16] */
+  const float* o;             /* [rows*k][H], pair-id order */
+} moe_decode_debug_view;
+
+/* Validates the shapes, the device and every pointer, plans the kernels and
+ * allocates the workspace.  `layers` points to dims->n_layers entries (copied).
+ * w_post_final / w_final: [H] norm weights of the final boundary (may be
+ * NULL if moe_decode_final / _step are never called). */
+int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* layers,
+                      const float* w_post_final, const float* w_final, moe_decode_t** out);
+
+/* One layer-step (boundary .. down) for `rows` rows.  branch: bf16 [rows][H],
+ * or NULL to use the unpooled output of the previous layer call on this
+ * handle (same rows) as the branch.  stream: fp32 [rows][H], updated in place. */
+int moe_decode_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, float* stream,
+                     void* cuda_stream);
+
+/* Final boundary: gathers the last layer's unpooled output into the stream
+ * and writes out = bf16(rmsnorm(stream) * w_final). */
+int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, void* cuda_stream);
+
+/* Every layer (layer 0 takes `branch`, later ones chain) and the final
+ * boundary. */
+int moe_decode_step(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
+                    uint16_t* out, void* cuda_stream);
+
+/* As moe_decode_step, replayed from a CUDA graph the library captures on the
+ * first call for this (rows, branch, stream, out) and caches in the handle.
+ * The first call for a new key must not itself be under stream capture. */
+int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
+                          uint16_t* out, void* cuda_stream);
+
+/* End-to-end step on HOST buffers: copies branch and stream in (H2D), replays
+ * the step graph, copies stream and out back (D2H) and synchronizes the
+ * stream.  Pinned host memory gives asynchronous copies. */
+int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
+                         float* stream_host, uint16_t* out_host, void* cuda_stream);
+
+/* One layer-step with a CUDA event recorded on `cuda_stream` around each of
+ * its four kernels (boundary, router, experts gate/up, experts down), launched
+ * without programmatic overlap so each duration is that kernel's alone.
+ * Synchronizes, then writes the four durations (ms) to kernel_ms_host[4].
+ * For measurement only; not capturable. */
+int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_t* branch,
+                             float* stream, void* cuda_stream, float* kernel_ms_host);
+
+/* Workspace pointers of the last layer run (see moe_decode_debug_view). */
+int moe_decode_debug(moe_decode_t* h, moe_decode_debug_view* out);
+
+/* Synchronizes the device, then returns MOE_EDEVICE if a device-side check
+ * latched an error since create (and clears it), MOE_ECUDA on a CUDA error,
+ * else MOE_OK. */
+int moe_decode_last_error(moe_decode_t* h);
+
+/* Bytes of device workspace the handle holds. */
+size_t moe_decode_workspace_bytes(const moe_decode_t* h);
+
+/* Number of kernels one moe_decode_step launches for `rows` rows. */
+int moe_decode_step_kernel_count(const moe_decode_t* h);
+
+void moe_decode_destroy(moe_decode_t* h);
+
+const char* moe_decode_strerror(int code);
+
+/* Reason of the last failing call on this thread ("" if none). */
+const char* moe_decode_error_message(void);
+
+/* NVFP4 quantizer (the scheme above) for one fp32 tensor v[rows][cols],
+ * cols % 16 == 0: writes codes [rows][cols/2], sf [rows][cols/16], the tensor
+ * scale *sg and *amax (device scalars).  v 16-byte aligned, codes 8-byte
+ * aligned.  Asynchronous on cuda_stream. */
+int moe_nvfp4_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
+                       float* sg, float* amax, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,259 @@
+"""GB300 (sm_103a) routed NVFP4 mixture-of-experts decode layer-step.
+
+A thin ctypes binding over ``libmoe_decode.so`` (see ``include/moe_decode.h``
+for the contract of every entry point).  The functions below keep the C
+names and only marshal arguments: device pointers come from torch tensors'
+``data_ptr()``, the CUDA stream from ``torch.cuda.current_stream()``.  Every
+step of the computation runs in the library's kernels; there is no other
+code path, and loading fails loudly if the library was not built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
+
+MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOMEM, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
+
+# Every symbol include/moe_decode.h declares.
+EXPORTS = (
+    "moe_decode_create", "moe_decode_layer", "moe_decode_final", "moe_decode_step",
+    "moe_decode_step_graph", "moe_decode_step_host", "moe_decode_layer_profile", "moe_decode_debug",
+    "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_step_kernel_count",
+    "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
+    "moe_nvfp4_quantize",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib().moe_decode_error_message().decode()
+        super().__init__(f"{where}: {_lib().moe_decode_strerror(code).decode()} ({code}): {msg}")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("inter", ctypes.c_int), ("max_rows", ctypes.c_int), ("n_layers", ctypes.c_int),
+                ("eps", ctypes.c_float)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_post", "w_pre", "router_w", "router_bias", "w13", "w13_sf", "w2", "w2_sf", "w_gscale")]
+
+
+class DebugView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "x", "x_codes", "x_sf", "x_sg", "logits", "ids", "gates", "flags", "count", "offset",
+        "pair_order", "pos_of_pair", "active", "n_active", "h", "h_sg", "h_codes", "h_sf", "o")]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        sig = {
+            "moe_decode_create": (i32, [ctypes.POINTER(Dims), ctypes.POINTER(LayerWeights), vp, vp,
+                                        ctypes.POINTER(vp)]),
+            "moe_decode_layer": (i32, [vp, i32, i32, vp, vp, vp]),
+            "moe_decode_final": (i32, [vp, i32, vp, vp, vp]),
+            "moe_decode_step": (i32, [vp, i32, vp, vp, vp, vp]),
+            "moe_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp]),
+            "moe_decode_step_host": (i32, [vp, i32, vp, vp, vp, vp]),
+            "moe_decode_layer_profile": (i32, [vp, i32, i32, vp, vp, vp, vp]),
+            "moe_decode_debug": (i32, [vp, ctypes.POINTER(DebugView)]),
+            "moe_decode_last_error": (i32, [vp]),
+            "moe_decode_workspace_bytes": (ctypes.c_size_t, [vp]),
+            "moe_decode_step_kernel_count": (i32, [vp]),
+            "moe_decode_destroy": (None, [vp]),
+            "moe_decode_strerror": (ctypes.c_char_p, [i32]),
+            "moe_decode_error_message": (ctypes.c_char_p, []),
+            "moe_nvfp4_quantize": (i32, [vp, i64, i64, vp, vp, vp, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def lib():
+    """The loaded library (raises ImportError if it was not built)."""
+    return _lib()
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ C names
+
+
+def moe_decode_create(dims: Dims, layers, w_post_final, w_final) -> ctypes.c_void_p:
+    arr = (LayerWeights * len(layers))(*layers)
+    h = ctypes.c_void_p()
+    _check(_lib().moe_decode_create(ctypes.byref(dims), arr, _ptr(w_post_final), _ptr(w_final),
+                                    ctypes.byref(h)), "moe_decode_create")
+    return h
+
+
+def moe_decode_layer(h, layer, rows, branch, stream_buf, stream=None):
+    _check(_lib().moe_decode_layer(h, layer, rows, _ptr(branch), _ptr(stream_buf),
+                                   _stream(stream)), "moe_decode_layer")
+
+
+def moe_decode_final(h, rows, stream_buf, out, stream=None):
+    _check(_lib().moe_decode_final(h, rows, _ptr(stream_buf), _ptr(out), _stream(stream)),
+           "moe_decode_final")
+
+
+def moe_decode_step(h, rows, branch, stream_buf, out, stream=None):
+    _check(_lib().moe_decode_step(h, rows, _ptr(branch), _ptr(stream_buf), _ptr(out),
+                                  _stream(stream)), "moe_decode_step")
+
+
+def moe_decode_step_graph(h, rows, branch, stream_buf, out, stream=None):
+    _check(_lib().moe_decode_step_graph(h, rows, _ptr(branch), _ptr(stream_buf), _ptr(out),
+                                        _stream(stream)), "moe_decode_step_graph")
+
+
+def moe_decode_step_host(h, rows, branch_host, stream_host, out_host, stream=None):
+    """Host (CPU) tensors, ideally pinned; stream_host is updated in place."""
+    _check(_lib().moe_decode_step_host(h, rows, _ptr(branch_host), _ptr(stream_host),
+                                       _ptr(out_host), _stream(stream)), "moe_decode_step_host")
+
+
+def moe_decode_layer_profile(h, layer, rows, branch, stream_buf, stream=None):
+    """-> [boundary, router, gate/up, down] kernel durations in ms."""
+    ms = (ctypes.c_float * 4)()
+    _check(_lib().moe_decode_layer_profile(h, layer, rows, _ptr(branch), _ptr(stream_buf),
+                                           _stream(stream), ms), "moe_decode_layer_profile")
+    return list(ms)
+
+
+def moe_decode_debug(h) -> DebugView:
+    v = DebugView()
+    _check(_lib().moe_decode_debug(h, ctypes.byref(v)), "moe_decode_debug")
+    return v
+
+
+def moe_decode_last_error(h) -> int:
+    return _lib().moe_decode_last_error(h)
+
+
+def moe_decode_workspace_bytes(h) -> int:
+    return _lib().moe_decode_workspace_bytes(h)
+
+
+def moe_decode_step_kernel_count(h) -> int:
+    return _lib().moe_decode_step_kernel_count(h)
+
+
+def moe_decode_destroy(h):
+    _lib().moe_decode_destroy(h)
+
+
+def moe_nvfp4_quantize(v, codes, sf, sg, amax, stream=None):
+    """v fp32 [rows, cols] -> codes u8 [rows, cols/2], sf u8 [rows, cols/16], sg / amax fp32 [1]
+    (all CUDA tensors)."""
+    rows, cols = v.shape
+    _check(_lib().moe_nvfp4_quantize(_ptr(v), rows, cols, _ptr(codes), _ptr(sf), _ptr(sg),
+                                     _ptr(amax), _stream(stream)), "moe_nvfp4_quantize")
+
+
+# --------------------------------------------------------- torch convenience
+
+
+@dataclass
+class LayerTensors:
+    """One layer's device tensors (kept alive by the handle)."""
+    w_post: object
+    w_pre: object
+    router_w: object          # bf16 [E, H]
+    router_bias: object       # fp32 [E] or None
+    w13: object               # u8 [E, 2I, H/2]
+    w13_sf: object            # u8 [E, 2I, H/16]
+    w2: object                # u8 [E, H, I/2]
+    w2_sf: object             # u8 [E, H, I/16]
+    w_gscale: object          # fp32 [E, 3]
+
+    def struct(self) -> LayerWeights:
+        return LayerWeights(*[None if t is None else t.data_ptr() for t in (
+            self.w_post, self.w_pre, self.router_w, self.router_bias, self.w13, self.w13_sf,
+            self.w2, self.w2_sf, self.w_gscale)])
+
+
+class MoEDecode:
+    """Owns a handle over caller-owned device weights (torch tensors)."""
+
+    def __init__(self, hidden, n_experts, top_k, inter, max_rows, layers, w_post_final=None,
+                 w_final=None, eps=1e-6):
+        self.dims = Dims(hidden, n_experts, top_k, inter, max_rows, len(layers), eps)
+        self.layers = list(layers)
+        self.w_post_final, self.w_final = w_post_final, w_final
+        self.handle = moe_decode_create(self.dims, [l.struct() for l in self.layers],
+                                        w_post_final, w_final)
+
+    def layer(self, layer, rows, branch, stream_buf, stream=None):
+        moe_decode_layer(self.handle, layer, rows, branch, stream_buf, stream)
+
+    def final(self, rows, stream_buf, out, stream=None):
+        moe_decode_final(self.handle, rows, stream_buf, out, stream)
+
+    def step(self, rows, branch, stream_buf, out, stream=None):
+        moe_decode_step(self.handle, rows, branch, stream_buf, out, stream)
+
+    def step_graph(self, rows, branch, stream_buf, out, stream=None):
+        moe_decode_step_graph(self.handle, rows, branch, stream_buf, out, stream)
+
+    def step_host(self, rows, branch_host, stream_host, out_host, stream=None):
+        moe_decode_step_host(self.handle, rows, branch_host, stream_host, out_host, stream)
+
+    def layer_profile(self, layer, rows, branch, stream_buf, stream=None):
+        return moe_decode_layer_profile(self.handle, layer, rows, branch, stream_buf, stream)
+
+    def debug(self) -> DebugView:
+        return moe_decode_debug(self.handle)
+
+    def last_error(self) -> int:
+        return moe_decode_last_error(self.handle)
+
+    def check(self):
+        rc = self.last_error()
+        if rc != MOE_OK:
+            raise MoeError(rc, "device")
+
+    def close(self):
+        if self.handle:
+            moe_decode_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

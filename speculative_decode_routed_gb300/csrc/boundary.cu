@@ -1,0 +1,151 @@
+// Dual-norm boundary (and the unpooler gather feeding it), one kernel.
+//
+// Page: vllm.models.muse_spark.nvidia.specialized_decode.runtime.decode,
+// module docstring "One step of b rows": the input boundary of later layers
+// gathers the previous MoE's unpooler blocks and applies the dual norm into
+// the stream; the attention boundary applies the dual norm into the stream
+// and the MoE input; "final" is the last gather + dual norm.  The norm pair
+// follows MuseSparkDSparkDecoderLayer.forward on the DSpark page:
+//   stream' = stream + rmsnorm(branch) * w_post        (fp32 stream)
+//   x       = bf16(rmsnorm(stream') * w_pre)
+// where branch is either a bf16 tensor or the gathered expert outputs
+//   y[r] = sum_s gates[r][s] * o[r*k + s]               (slot order).
+//
+// GB300 layout: one thread-block cluster per row; each CTA owns H / cluster
+// columns (four per thread, 128-bit accesses), and the two row sums of
+// squares are reduced across the cluster through distributed shared memory,
+// in a fixed order, so every CTA sees the same bit-exact total.  One atomicMax
+// per CTA folds max|x| into the MoE input's NVFP4 global-scale accumulator.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace moe {
+namespace {
+
+// Block-wide sum of v (fixed order) into *slot, written by thread 0.
+__device__ __forceinline__ void block_sum_to_slot(float v, float* warp_red, float* slot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) warp_red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += warp_red[w];
+    *slot = t;
+  }
+}
+
+__global__ void boundary_kernel(BoundaryParams p) {
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float warp_red[32];
+  __shared__ float part[2];
+  __shared__ float amax_red[32];
+
+  const int r = blockIdx.y;
+  const int col = blockIdx.x * p.cols_per_cta + threadIdx.x * 4;
+  const bool live = (int)threadIdx.x * 4 < p.cols_per_cta;
+
+  // Norm weights do not depend on the previous kernel: fetch them first.
+  float4 wpost = make_float4(0.f, 0.f, 0.f, 0.f), wpre = wpost;
+  if (live) {
+    wpost = __ldg(reinterpret_cast<const float4*>(p.w_post + col));
+    wpre = __ldg(reinterpret_cast<const float4*>(p.w_pre + col));
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (live) {
+    if (p.branch) {
+      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(p.branch + (size_t)r * p.H + col));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      y = make_float4(a.x, a.y, b.x, b.y);
+    } else {
+      for (int s = 0; s < p.k; ++s) {
+        const float g = __ldcg(p.gates + r * p.k + s);
+        const float4 o =
+            __ldcg(reinterpret_cast<const float4*>(p.o + ((size_t)r * p.k + s) * p.H + col));
+        y.x = fmaf(g, o.x, y.x);
+        y.y = fmaf(g, o.y, y.y);
+        y.z = fmaf(g, o.z, y.z);
+        y.w = fmaf(g, o.w, y.w);
+      }
+    }
+  }
+
+  // rms of the branch over the whole row (cluster-wide)
+  block_sum_to_slot(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, warp_red, &part[0]);
+  cluster.sync();
+  float ss = 0.0f;
+  for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss += *cluster.map_shared_rank(&part[0], q);
+  const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
+
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  float* srow = p.stream + (size_t)r * p.H + col;
+  if (live) {
+    s = __ldcg(reinterpret_cast<const float4*>(srow));
+    s.x += y.x * inv1 * wpost.x;
+    s.y += y.y * inv1 * wpost.y;
+    s.z += y.z * inv1 * wpost.z;
+    s.w += y.w * inv1 * wpost.w;
+    *reinterpret_cast<float4*>(srow) = s;
+  }
+
+  // rms of the updated stream
+  block_sum_to_slot(s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w, warp_red, &part[1]);
+  cluster.sync();
+  float ss2 = 0.0f;
+  for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss2 += *cluster.map_shared_rank(&part[1], q);
+  const float inv2 = rsqrtf(ss2 / (float)p.H + p.eps);
+
+  float m = 0.0f;
+  if (live) {
+    const __nv_bfloat162 x01 = __floats2bfloat162_rn(s.x * inv2 * wpre.x, s.y * inv2 * wpre.y);
+    const __nv_bfloat162 x23 = __floats2bfloat162_rn(s.z * inv2 * wpre.z, s.w * inv2 * wpre.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&x01);
+    packed.y = *reinterpret_cast<const uint32_t*>(&x23);
+    *reinterpret_cast<uint2*>(p.x_out + (size_t)r * p.H + col) = packed;
+    const float2 f01 = __bfloat1622float2(x01), f23 = __bfloat1622float2(x23);
+    m = fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y)));
+  }
+  if (p.x_amax) {
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) amax_red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = fmaxf(t, amax_red[w]);
+      atomic_max_nonneg(p.x_amax, t);
+    }
+  }
+  // keep this CTA's shared memory alive until every peer has read it
+  cluster.sync();
+}
+
+}  // namespace
+
+cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl) {
+  const int threads = ((p.cols_per_cta / 4 + 31) / 32) * 32;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster, p.rows, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, boundary_kernel, p);
+}
+
+}  // namespace moe

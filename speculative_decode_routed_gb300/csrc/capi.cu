@@ -1,0 +1,565 @@
+// C ABI of the routed NVFP4 MoE decode step: argument validation, the launch
+// plan (tile sizes, pipeline depth, cluster shape), the workspace, the kernel
+// sequence of a layer / step, and the library-owned CUDA graphs.
+//
+// Page: vllm.models.muse_spark.nvidia.specialized_decode.runtime (the
+// deployment gate `unsupported`: the first reason a configuration cannot
+// run, checked up front -- mirrored by moe_decode_create's validation and
+// moe_decode_error_message) and ...runtime.decode (SpecializedDecode.run: per
+// layer boundary.run -> attention -> attention_boundary.run -> moe.run, then
+// final.run, replayed inside a FULL CUDA graph).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/moe_decode.h"
+#include "moe_decode_internal.h"
+
+namespace moe {
+size_t router_smem_bytes(int E, int rows);
+cudaError_t router_set_smem(size_t bytes);
+cudaError_t expert_set_smem(size_t bytes);
+}  // namespace moe
+
+namespace {
+
+thread_local std::string g_msg;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct GraphEntry {
+  int rows;
+  const void* branch;
+  const float* stream;
+  const void* out;
+  cudaGraphExec_t exec;
+};
+
+}  // namespace
+
+struct moe_decode_s {
+  moe_decode_dims d;
+  std::vector<moe_layer_weights> layers;
+  const float* w_post_final = nullptr;
+  const float* w_final = nullptr;
+  int device = 0;
+  int num_sms = 0;
+  void* ws_mem = nullptr;
+  size_t ws_bytes = 0;
+  moe::Workspace ws{};
+  int cluster = 1;
+  int S = 1, EG = 8, n_eg = 1;
+  moe::ExpertParams gu{}, dn{};
+  cudaStream_t cap_stream = nullptr;
+  std::vector<GraphEntry> graphs;
+  uint16_t* io_branch = nullptr;
+  float* io_stream = nullptr;
+  uint16_t* io_out = nullptr;
+};
+
+namespace {
+
+// Tile plan of one expert projection (see experts.cu).
+int plan_experts(moe::ExpertParams& p, int mode, const moe_decode_dims& d) {
+  p = moe::ExpertParams{};
+  p.mode = mode;
+  p.H = d.hidden;
+  p.I = d.inter;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.K = (mode == moe::kGateUp) ? d.hidden : d.inter;
+  p.KB = p.K / 2;
+  p.KS = p.K / 16;
+  p.CH = p.K / 32;
+  p.TPG = ((p.CH + 31) / 32) * 32;
+  if (p.TPG > 256) return fail(MOE_EUNSUPPORTED, "reduction length %d > 8192", p.K);
+  p.G = 256 / p.TPG;
+  p.TW = moe::kTW;
+  p.T = moe::kTW * p.G;
+  if (mode == moe::kGateUp) {
+    p.TJ = p.T / 2;
+    if (d.inter % p.TJ)
+      return fail(MOE_EUNSUPPORTED, "inter %d not a multiple of the gate/up tile %d", d.inter, p.TJ);
+    p.tiles = d.inter / p.TJ;
+    p.RE = 2 * d.inter;
+  } else {
+    p.TJ = p.T;
+    if (d.hidden % p.T)
+      return fail(MOE_EUNSUPPORTED, "hidden %d not a multiple of the down tile %d", d.hidden, p.T);
+    p.tiles = d.hidden / p.T;
+    p.RE = d.hidden;
+  }
+  p.stage_bytes = (uint32_t)(p.T * (p.KB + p.KS));
+  p.stage_stride = (p.stage_bytes + 127u) / 128u * 128u;
+  const size_t ctrl = 16 * 1024;  // upper bound of the control area
+  int ns = (int)((moe::kSmemBudget - ctrl) / p.stage_stride);
+  if (ns > 16) ns = 16;
+  if (ns < 2) return fail(MOE_EUNSUPPORTED, "expert stage of %u bytes too large", p.stage_bytes);
+  p.NS = ns;
+  p.ws_pairs = d.max_rows * d.top_k;
+  return MOE_OK;
+}
+
+int check_layer(const moe_layer_weights& w, int i) {
+  if (!w.w_post || !w.w_pre || !w.router_w || !w.w13 || !w.w13_sf || !w.w2 || !w.w2_sf ||
+      !w.w_gscale)
+    return fail(MOE_EINVAL, "layer %d: a required weight pointer is NULL", i);
+  const void* a16[] = {w.w_post, w.w_pre, w.router_w, w.w13, w.w13_sf, w.w2, w.w2_sf};
+  for (const void* q : a16)
+    if (!aligned(q, 16)) return fail(MOE_EINVAL, "layer %d: weight pointer not 16-byte aligned", i);
+  if (!aligned(w.w_gscale, 4) || (w.router_bias && !aligned(w.router_bias, 4)))
+    return fail(MOE_EINVAL, "layer %d: fp32 pointer not 4-byte aligned", i);
+  return MOE_OK;
+}
+
+template <typename T>
+T* carve(uint8_t*& cur, size_t count) {
+  T* p = reinterpret_cast<T*>(cur);
+  cur += (count * sizeof(T) + 255) / 256 * 256;
+  return p;
+}
+
+size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims& d, int S) {
+  const size_t R = d.max_rows, H = d.hidden, E = d.n_experts, k = d.top_k, I = d.inter;
+  uint8_t* cur = base;
+  ws.x = carve<__nv_bfloat16>(cur, R * H);
+  ws.x_codes = carve<uint8_t>(cur, R * H / 2);
+  ws.x_sf = carve<uint8_t>(cur, R * H / 16);
+  ws.x_sg = carve<float>(cur, 1);
+  ws.x_amax = carve<unsigned>(cur, 1);
+  ws.logit_part = carve<float>(cur, (size_t)S * R * E);
+  ws.logits = carve<float>(cur, R * E);
+  ws.ids = carve<int>(cur, R * k);
+  ws.gates = carve<float>(cur, R * k);
+  ws.flags = carve<uint8_t>(cur, R);
+  ws.count = carve<int>(cur, E);
+  ws.offset = carve<int>(cur, E + 1);
+  ws.pair_order = carve<int>(cur, R * k);
+  ws.pos_of_pair = carve<int>(cur, R * k);
+  ws.active = carve<int>(cur, E);
+  ws.n_active = carve<int>(cur, 1);
+  ws.h = carve<float>(cur, R * k * I);
+  ws.h_amax = carve<unsigned>(cur, E);
+  ws.h_sg = carve<float>(cur, E);
+  ws.h_codes = carve<uint8_t>(cur, R * k * I / 2);
+  ws.h_sf = carve<uint8_t>(cur, R * k * I / 16);
+  ws.done = carve<unsigned>(cur, E);
+  ws.o = carve<float>(cur, R * k * H);
+  ws.counters = carve<unsigned>(cur, 4);
+  ws.err = carve<unsigned>(cur, 1);
+  return (size_t)(cur - base);
+}
+
+int check_rows(const moe_decode_t* h, int rows) {
+  if (rows < 1 || rows > h->d.max_rows)
+    return fail(MOE_EINVAL, "rows %d outside [1, max_rows=%d]", rows, h->d.max_rows);
+  return MOE_OK;
+}
+
+int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, float* stream,
+                 cudaStream_t s, cudaEvent_t* ev = nullptr) {
+  const bool pdl = (ev == nullptr);
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  mark(0);
+  const moe_decode_dims& d = h->d;
+  const moe_layer_weights& w = h->layers[layer];
+  moe::BoundaryParams bp{};
+  bp.H = d.hidden;
+  bp.k = d.top_k;
+  bp.rows = rows;
+  bp.cols_per_cta = d.hidden / h->cluster;
+  bp.eps = d.eps;
+  bp.branch = reinterpret_cast<const __nv_bfloat16*>(branch);
+  bp.o = h->ws.o;
+  bp.gates = h->ws.gates;
+  bp.stream = stream;
+  bp.w_post = w.w_post;
+  bp.w_pre = w.w_pre;
+  bp.x_out = h->ws.x;
+  bp.x_amax = h->ws.x_amax;
+  cudaError_t e = moe::launch_boundary(bp, h->cluster, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "boundary launch");
+  mark(1);
+
+  moe::RouterParams rp{};
+  rp.H = d.hidden;
+  rp.E = d.n_experts;
+  rp.k = d.top_k;
+  rp.rows = rows;
+  rp.S = h->S;
+  rp.EG = h->EG;
+  rp.n_eg = h->n_eg;
+  rp.x = h->ws.x;
+  rp.wr = reinterpret_cast<const __nv_bfloat16*>(w.router_w);
+  rp.bias = w.router_bias;
+  rp.ws = h->ws;
+  e = moe::launch_router(rp, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  mark(2);
+
+  moe::ExpertParams gu = h->gu;
+  gu.w = w.w13;
+  gu.w_sf = w.w13_sf;
+  gu.gscale = w.w_gscale;
+  gu.ws = h->ws;
+  e = moe::launch_experts(gu, h->num_sms, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
+  mark(3);
+
+  moe::ExpertParams dn = h->dn;
+  dn.w = w.w2;
+  dn.w_sf = w.w2_sf;
+  dn.gscale = w.w_gscale;
+  dn.ws = h->ws;
+  e = moe::launch_experts(dn, h->num_sms, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  mark(4);
+  return MOE_OK;
+}
+
+int launch_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, cudaStream_t s) {
+  const moe_decode_dims& d = h->d;
+  moe::BoundaryParams bp{};
+  bp.H = d.hidden;
+  bp.k = d.top_k;
+  bp.rows = rows;
+  bp.cols_per_cta = d.hidden / h->cluster;
+  bp.eps = d.eps;
+  bp.branch = nullptr;
+  bp.o = h->ws.o;
+  bp.gates = h->ws.gates;
+  bp.stream = stream;
+  bp.w_post = h->w_post_final;
+  bp.w_pre = h->w_final;
+  bp.x_out = reinterpret_cast<__nv_bfloat16*>(out);
+  bp.x_amax = nullptr;
+  const cudaError_t e = moe::launch_boundary(bp, h->cluster, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "final boundary launch");
+  return MOE_OK;
+}
+
+int check_step_args(moe_decode_t* h, int rows, const void* branch, const float* stream,
+                    const void* out) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!branch || !stream || !out) return fail(MOE_EINVAL, "branch, stream and out are required");
+  if (!aligned(stream, 16) || !aligned(branch, 8) || !aligned(out, 8))
+    return fail(MOE_EINVAL, "stream must be 16-byte, branch and out 8-byte aligned");
+  if (!h->w_post_final || !h->w_final)
+    return fail(MOE_EINVAL, "the handle was created without final norm weights");
+  return MOE_OK;
+}
+
+int enqueue_step(moe_decode_t* h, int rows, const uint16_t* branch, float* stream, uint16_t* out,
+                 cudaStream_t s) {
+  for (int l = 0; l < h->d.n_layers; ++l) {
+    const int rc = launch_layer(h, l, rows, l == 0 ? branch : nullptr, stream, s);
+    if (rc) return rc;
+  }
+  return launch_final(h, rows, stream, out, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_decode_error_message(void) { return g_msg.c_str(); }
+
+const char* moe_decode_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument";
+    case MOE_EUNSUPPORTED: return "unsupported shape or device";
+    case MOE_ECUDA: return "CUDA runtime error";
+    case MOE_ENOMEM: return "out of device memory";
+    case MOE_EDEVICE: return "device-side check failed";
+    default: return "unknown error";
+  }
+}
+
+int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* layers,
+                      const float* w_post_final, const float* w_final, moe_decode_t** out) {
+  g_msg.clear();
+  if (!dims || !layers || !out) return fail(MOE_EINVAL, "dims, layers and out are required");
+  *out = nullptr;
+  const moe_decode_dims d = *dims;
+  if (d.hidden < 128 || d.hidden % 128 || d.hidden > 8192)
+    return fail(MOE_EUNSUPPORTED, "hidden %d: need a multiple of 128 in [128, 8192]", d.hidden);
+  if (d.inter < 128 || d.inter % 128 || d.inter > 8192)
+    return fail(MOE_EUNSUPPORTED, "inter %d: need a multiple of 128 in [128, 8192]", d.inter);
+  if (d.n_experts < 1 || d.n_experts > 1024)
+    return fail(MOE_EUNSUPPORTED, "n_experts %d outside [1, 1024]", d.n_experts);
+  if (d.top_k < 1 || d.top_k > d.n_experts || d.top_k > 16)
+    return fail(MOE_EUNSUPPORTED, "top_k %d outside [1, min(E, 16)]", d.top_k);
+  if (d.max_rows < 1 || d.max_rows > 128)
+    return fail(MOE_EUNSUPPORTED, "max_rows %d outside [1, 128]", d.max_rows);
+  if (d.n_layers < 1 || d.n_layers > 256)
+    return fail(MOE_EUNSUPPORTED, "n_layers %d outside [1, 256]", d.n_layers);
+  if (!(d.eps >= 0.0f)) return fail(MOE_EINVAL, "eps must be >= 0");
+  for (int i = 0; i < d.n_layers; ++i) {
+    const int rc = check_layer(layers[i], i);
+    if (rc) return rc;
+  }
+  if ((w_post_final && !aligned(w_post_final, 16)) || (w_final && !aligned(w_final, 16)))
+    return fail(MOE_EINVAL, "final norm weights must be 16-byte aligned");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major != 10)
+    return fail(MOE_EUNSUPPORTED, "device %s is sm_%d%d; the library is built for the SM 10.x "
+                "family (sm_103a)", prop.name, prop.major, prop.minor);
+
+  moe_decode_t* h = new moe_decode_s();
+  h->d = d;
+  h->layers.assign(layers, layers + d.n_layers);
+  h->w_post_final = w_post_final;
+  h->w_final = w_final;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  // boundary: the largest cluster (<= 8) whose CTAs get whole 128-column slabs
+  h->cluster = 1;
+  for (int c = 8; c >= 1; c >>= 1)
+    if (d.hidden % (c * 128) == 0) {
+      h->cluster = c;
+      break;
+    }
+  // router: one warp per expert, H split into slices of at most 1024
+  h->EG = 8;
+  h->n_eg = (d.n_experts + h->EG - 1) / h->EG;
+  h->S = (d.hidden / 8 + 127) / 128;
+  int rc = plan_experts(h->gu, moe::kGateUp, d);
+  if (!rc) rc = plan_experts(h->dn, moe::kDown, d);
+  if (rc) {
+    delete h;
+    return rc;
+  }
+  e = moe::expert_set_smem(std::max(moe::expert_smem_bytes(h->gu), moe::expert_smem_bytes(h->dn)));
+  if (e == cudaSuccess) e = moe::router_set_smem(moe::router_smem_bytes(d.n_experts, d.max_rows));
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "kernel attribute");
+  }
+  moe::Workspace probe{};
+  alignas(256) static uint8_t fake_base[256];  // sizes only: nothing is written through it
+  h->ws_bytes = layout_workspace(probe, fake_base, d, h->S);
+  e = cudaMalloc(&h->ws_mem, h->ws_bytes);
+  if (e != cudaSuccess) {
+    const size_t want = h->ws_bytes;
+    delete h;
+    return fail(MOE_ENOMEM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
+  }
+  layout_workspace(h->ws, static_cast<uint8_t*>(h->ws_mem), d, h->S);
+  const size_t io = (size_t)d.max_rows * d.hidden;
+  e = cudaMemset(h->ws_mem, 0, h->ws_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->io_branch, io * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->io_stream, io * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h->io_out, io * 2);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    moe_decode_destroy(h);
+    return cuda_fail(e, "workspace setup");
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_decode_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, float* stream,
+                     void* cuda_stream) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  if (layer < 0 || layer >= h->d.n_layers)
+    return fail(MOE_EINVAL, "layer %d outside [0, %d)", layer, h->d.n_layers);
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!stream || !aligned(stream, 16)) return fail(MOE_EINVAL, "stream must be 16-byte aligned");
+  if (branch && !aligned(branch, 8)) return fail(MOE_EINVAL, "branch must be 8-byte aligned");
+  return launch_layer(h, layer, rows, branch, stream, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, void* cuda_stream) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!stream || !out || !aligned(stream, 16) || !aligned(out, 8))
+    return fail(MOE_EINVAL, "stream (16-byte) and out (8-byte) must be aligned device pointers");
+  if (!h->w_post_final || !h->w_final)
+    return fail(MOE_EINVAL, "the handle was created without final norm weights");
+  return launch_final(h, rows, stream, out, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int moe_decode_step(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
+                    uint16_t* out, void* cuda_stream) {
+  const int rc = check_step_args(h, rows, branch, stream, out);
+  if (rc) return rc;
+  return enqueue_step(h, rows, branch, stream, out, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
+                          uint16_t* out, void* cuda_stream) {
+  int rc = check_step_args(h, rows, branch, stream, out);
+  if (rc) return rc;
+  cudaGraphExec_t exec = nullptr;
+  for (const GraphEntry& g : h->graphs)
+    if (g.rows == rows && g.branch == branch && g.stream == stream && g.out == out) exec = g.exec;
+  if (!exec) {
+    cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "begin capture");
+    rc = enqueue_step(h, rows, branch, stream, out, h->cap_stream);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "end capture");
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
+    h->graphs.push_back(GraphEntry{rows, branch, stream, out, exec});
+  }
+  const cudaError_t e = cudaGraphLaunch(exec, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  return MOE_OK;
+}
+
+int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
+                         float* stream_host, uint16_t* out_host, void* cuda_stream) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!branch_host || !stream_host || !out_host)
+    return fail(MOE_EINVAL, "branch_host, stream_host and out_host are required");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const size_t n = (size_t)rows * h->d.hidden;
+  cudaError_t e = cudaMemcpyAsync(h->io_branch, branch_host, n * 2, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "input copy");
+  rc = moe_decode_step_graph(h, rows, h->io_branch, h->io_stream, h->io_out, cuda_stream);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(stream_host, h->io_stream, n * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, h->io_out, n * 2, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "output copy");
+  return MOE_OK;
+}
+
+int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_t* branch,
+                             float* stream, void* cuda_stream, float* kernel_ms_host) {
+  if (!h || !kernel_ms_host) return fail(MOE_EINVAL, "handle and kernel_ms_host are required");
+  if (layer < 0 || layer >= h->d.n_layers)
+    return fail(MOE_EINVAL, "layer %d outside [0, %d)", layer, h->d.n_layers);
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!stream || !aligned(stream, 16)) return fail(MOE_EINVAL, "stream must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaEvent_t ev[5] = {};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  if (e == cudaSuccess) {
+    rc = launch_layer(h, layer, rows, branch, stream, s, ev);
+    if (!rc) e = cudaEventSynchronize(ev[4]);
+    for (int i = 0; i < 4 && !rc && e == cudaSuccess; ++i)
+      e = cudaEventElapsedTime(&kernel_ms_host[i], ev[i], ev[i + 1]);
+  }
+  for (int i = 0; i < 5; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  if (rc) return rc;
+  if (e != cudaSuccess) return cuda_fail(e, "profile events");
+  return MOE_OK;
+}
+
+int moe_decode_debug(moe_decode_t* h, moe_decode_debug_view* v) {
+  if (!h || !v) return fail(MOE_EINVAL, "handle and view are required");
+  const moe::Workspace& w = h->ws;
+  v->x = reinterpret_cast<const uint16_t*>(w.x);
+  v->x_codes = w.x_codes;
+  v->x_sf = w.x_sf;
+  v->x_sg = w.x_sg;
+  v->logits = w.logits;
+  v->ids = w.ids;
+  v->gates = w.gates;
+  v->flags = w.flags;
+  v->count = w.count;
+  v->offset = w.offset;
+  v->pair_order = w.pair_order;
+  v->pos_of_pair = w.pos_of_pair;
+  v->active = w.active;
+  v->n_active = w.n_active;
+  v->h = w.h;
+  v->h_sg = w.h_sg;
+  v->h_codes = w.h_codes;
+  v->h_sf = w.h_sf;
+  v->o = w.o;
+  return MOE_OK;
+}
+
+int moe_decode_last_error(moe_decode_t* h) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  unsigned flag = 0;
+  e = cudaMemcpy(&flag, h->ws.err, sizeof(flag), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error flag read");
+  if (flag) {
+    cudaMemset(h->ws.err, 0, sizeof(unsigned));
+    return fail(MOE_EDEVICE, "device-side error %u (1 = bounded wait gave up, 2 = bad routing)",
+                flag);
+  }
+  return MOE_OK;
+}
+
+size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
+
+int moe_decode_step_kernel_count(const moe_decode_t* h) {
+  return h ? 4 * h->d.n_layers + 1 : 0;
+}
+
+void moe_decode_destroy(moe_decode_t* h) {
+  if (!h) return;
+  for (GraphEntry& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  cudaFree(h->io_branch);
+  cudaFree(h->io_stream);
+  cudaFree(h->io_out);
+  cudaFree(h->ws_mem);
+  delete h;
+}
+
+int moe_nvfp4_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
+                       float* sg, float* amax, void* cuda_stream) {
+  if (!v || !codes || !sf || !sg || !amax) return fail(MOE_EINVAL, "null pointer");
+  if (rows < 0 || cols < 0 || cols % 16) return fail(MOE_EINVAL, "cols must be a multiple of 16");
+  if (!aligned(v, 16) || !aligned(codes, 8) || !aligned(sg, 4) || !aligned(amax, 4))
+    return fail(MOE_EINVAL, "v must be 16-byte and codes 8-byte aligned");
+  const cudaError_t e = moe::launch_quantize(v, rows, cols, codes, sf, sg, amax,
+                                             static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// Internal interfaces of the routed NVFP4 MoE decode library: the device
+// workspace layout and the parameter blocks of its kernels.  Not part of the
+// public C ABI (include/moe_decode.h).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace moe {
+
+// Device-side error codes latched into the workspace error word.
+enum DeviceError : unsigned {
+  kDevOk = 0,
+  kDevWaitTimeout = 1,    // a bounded mbarrier wait gave up
+  kDevBadRouting = 2,     // routing produced an out-of-range id / count
+};
+
+// Library-owned scratch, sized at create for max_rows rows.
+struct Workspace {
+  __nv_bfloat16* x;      // [R][H]      MoE input (bf16)
+  uint8_t* x_codes;      // [R][H/2]    NVFP4 codes of x (one tensor)
+  uint8_t* x_sf;         // [R][H/16]   e4m3 block scales of x
+  float* x_sg;           // [1]         global scale of x
+  unsigned* x_amax;      // [1]         max |x| (float bits), reset by the router
+  float* logit_part;     // [S][R][E]   router partial sums per H-slice
+  float* logits;         // [R][E]      router logits (bias included)
+  int* ids;              // [R][k]      expert of each (row, slot)
+  float* gates;          // [R][k]      renormalised gates
+  uint8_t* flags;        // [R]         1 if the k-th / (k+1)-th gap < 1e-6
+  int* count;            // [E]         pairs per expert
+  int* offset;           // [E+1]       exclusive prefix of count
+  int* pair_order;       // [R*k]       pair id (r*k+s) at each pooled position
+  int* pos_of_pair;      // [R*k]       pooled position of each pair id
+  int* active;           // [E]         experts with pairs, ascending
+  int* n_active;         // [1]
+  float* h;              // [R*k][I]    silu(G)*U, pooled order
+  unsigned* h_amax;      // [E]         per-expert max |h| (float bits)
+  float* h_sg;           // [E]         per-expert global scale of h
+  uint8_t* h_codes;      // [R*k][I/2]
+  uint8_t* h_sf;         // [R*k][I/16]
+  unsigned* done;        // [E]         finished gate/up tiles per expert
+  float* o;              // [R*k][H]    expert outputs, pair-id order
+  unsigned* counters;    // [4]         [0] router CTA arrivals
+  unsigned* err;         // [1]         latched DeviceError
+};
+
+// ----------------------------------------------------------- boundary (K1)
+struct BoundaryParams {
+  int H, k, rows;
+  int cols_per_cta;             // H / cluster size
+  float eps;
+  const __nv_bfloat16* branch;  // [rows][H] or null: gather sum_s g * o instead
+  const float* o;               // [rows*k][H]
+  const float* gates;           // [rows][k]
+  float* stream;                // [rows][H] in/out
+  const float* w_post;          // [H]
+  const float* w_pre;           // [H]
+  __nv_bfloat16* x_out;         // [rows][H]
+  unsigned* x_amax;             // max |x| accumulator, or null (final boundary)
+};
+
+// ------------------------------------------------------------- router (K2)
+struct RouterParams {
+  int H, E, k, rows;
+  int S;                        // H slices (split-K)
+  int EG;                       // experts per CTA (one warp each)
+  int n_eg;                     // expert groups: ceil(E / EG)
+  const __nv_bfloat16* x;       // [rows][H]
+  const __nv_bfloat16* wr;      // [E][H]
+  const float* bias;            // [E] or null
+  Workspace ws;
+};
+
+// ------------------------------------------------------ experts (K3 / K4)
+enum ExpertMode : int { kGateUp = 0, kDown = 1 };
+
+struct ExpertParams {
+  int mode;
+  int H, I, E, k;
+  int K, KB, KS;                // reduction length, code / scale bytes per weight row
+  int T;                        // weight rows per item (gate/up: TJ gate + TJ up)
+  int TJ;                       // gate/up: output columns per item; down: T
+  int tiles;                    // items per expert
+  int RE;                       // weight rows per expert (2I or H)
+  int CH, TPG, G, TW;           // chunks/row, threads/row-group, row-groups, rows/thread
+  int NS;                       // pipeline stages
+  int ws_pairs;                 // rows * k of the workspace (bounds of pooled positions)
+  uint32_t stage_bytes;         // bytes of one stage (codes + scales)
+  uint32_t stage_stride;        // stage_bytes rounded up to 128
+  const uint8_t* w;             // codes [E][RE][KB]
+  const uint8_t* w_sf;          // scales [E][RE][KS]
+  const float* gscale;          // [E][3]
+  Workspace ws;
+};
+
+constexpr int kMaxRB = 8;         // activation rows held in registers
+constexpr int kTW = 8;            // weight rows per thread per item
+constexpr int kSmemBudget = 200 * 1024;
+
+// Host-side launchers (one per kernel family).
+cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl);
+cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes,
+                            uint8_t* sf, float* sg, float* amax, cudaStream_t s);
+
+size_t expert_smem_bytes(const ExpertParams& p);
+
+}  // namespace moe

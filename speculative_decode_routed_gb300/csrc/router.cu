@@ -1,0 +1,291 @@
+// Router GEMV, softmax top-k routing, pooler and the MoE input's NVFP4
+// quantization, one kernel.
+//
+// Page: vllm.models.muse_spark.nvidia.specialized_decode.runtime.decode,
+// module docstring "One step of b rows", MoE: "router -> routing -> pooler ->
+// routed experts"; SpecializedDecode.build builds one Pooler for all layers
+// and batches.  Routing is softmax over all experts, top-k by probability
+// (ties to the lower expert id), gates renormalised over the selected k; the
+// pooler groups the (row, slot) pairs by expert, experts ascending and rows
+// ascending within an expert.
+//
+// GB300 layout: split-K GEMV.  CTA (g, s) owns EG experts (one warp each)
+// and one H-slice; the warp holds its expert's slice of the router weights in
+// registers (fetched before the programmatic-dependency wait, since the
+// weights do not depend on the previous kernel) and writes one fp32 partial
+// per (row, expert).  Every CTA also quantizes a share of the MoE input's
+// 16-element blocks.  The last CTA to arrive (threadfence + counter, no spin)
+// sums the partials in slice order, selects the top-k per row (one warp per
+// row), and builds the pooler's arrays in shared memory.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouterThreads = 256;
+constexpr int kRouterWarps = kRouterThreads / 32;
+constexpr int kRouterChunks = 4;   // 8-element chunks per lane per slice: slices <= 1024 wide
+constexpr int kMaxTopK = 16;
+
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
+  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
+// Routing + pooler, run by the last CTA.
+__device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
+  const Workspace& ws = p.ws;
+  const int E = p.E, k = p.k, rows = p.rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* lg = reinterpret_cast<float*>(smem);                       // [warps][E]
+  int* cnt = reinterpret_cast<int*>(lg + kRouterWarps * E);          // [E]
+  int* off = cnt + E;                                                // [E+1]
+  const int RW = (rows + 31) / 32;
+  unsigned* mask = reinterpret_cast<unsigned*>(off + E + 1);        // [E][RW]
+
+  // ---- routing: one warp per row
+  for (int r = warp; r < rows; r += kRouterWarps) {
+    float* l = lg + warp * E;
+    float m = -INFINITY;
+    for (int e = lane; e < E; e += 32) {
+      float v = 0.0f;
+      for (int s = 0; s < p.S; ++s) v += __ldcg(ws.logit_part + ((size_t)s * rows + r) * E + e);
+      if (p.bias) v += __ldg(p.bias + e);
+      l[e] = v;
+      ws.logits[(size_t)r * E + e] = v;
+      m = fmaxf(m, v);
+    }
+    m = warp_max(m);
+    float z = 0.0f;
+    for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
+    z = warp_sum(z);
+    __syncwarp();
+    // top-(k+1) by logit (monotone in probability), ties to the lower id
+    const int nsel = (k < E) ? k + 1 : k;
+    int sel_id = -1;      // lane t keeps the t-th selection
+    float sel_v = 0.0f;
+    for (int t = 0; t < nsel; ++t) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int e = lane; e < E; e += 32) {
+        const float v = l[e];
+        if (v > bv || (v == bv && e < bi)) {
+          bv = v;
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane == t) {
+        sel_id = bi;
+        sel_v = bv;
+      }
+      __syncwarp();
+      if (lane == 0) l[bi] = -INFINITY;  // taken
+      __syncwarp();
+    }
+    // gates: exp(l_s - m) renormalised over the k selected, slot order
+    const float ex = (lane < nsel) ? expf(sel_v - m) : 0.0f;
+    float den = 0.0f;
+    for (int t = 0; t < k; ++t) den += __shfl_sync(0xffffffffu, ex, t);
+    const float ek = __shfl_sync(0xffffffffu, ex, k - 1);
+    const float ek1 = __shfl_sync(0xffffffffu, ex, (nsel > k) ? k : 0);
+    if (lane < k) {
+      ws.ids[r * k + lane] = sel_id;
+      ws.gates[r * k + lane] = ex / den;
+      if (sel_id < 0 || sel_id >= E) latch_error(ws.err, kDevBadRouting);
+    }
+    if (lane == 0) ws.flags[r] = (nsel > k) ? (uint8_t)((ek - ek1) / z < 1e-6f) : (uint8_t)0;
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // ---- pooler
+  for (int e = tid; e < E; e += kRouterThreads) {
+    cnt[e] = 0;
+    for (int w = 0; w < RW; ++w) mask[e * RW + w] = 0u;
+  }
+  __syncthreads();
+  const int npairs = rows * k;
+  for (int q = tid; q < npairs; q += kRouterThreads) {
+    const int e = ws.ids[q];
+    if (e < 0 || e >= E) continue;
+    const int r = q / k;
+    atomicAdd(&cnt[e], 1);
+    atomicOr(&mask[e * RW + (r >> 5)], 1u << (r & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the counts and of the active flags; lane owns a range
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per, e1 = min(E, e0 + per);
+    int csum = 0, asum = 0;
+    for (int e = e0; e < e1; ++e) {
+      csum += cnt[e];
+      asum += cnt[e] > 0;
+    }
+    int cex = csum, aex = asum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int tc = __shfl_up_sync(0xffffffffu, cex, o);
+      const int ta = __shfl_up_sync(0xffffffffu, aex, o);
+      if (lane >= o) {
+        cex += tc;
+        aex += ta;
+      }
+    }
+    cex -= csum;
+    aex -= asum;
+    for (int e = e0; e < e1; ++e) {
+      off[e] = cex;
+      ws.offset[e] = cex;
+      ws.count[e] = cnt[e];
+      cex += cnt[e];
+      if (cnt[e] > 0) ws.active[aex++] = e;
+    }
+    if (lane == 31) {
+      off[E] = cex;
+      ws.offset[E] = cex;
+      ws.n_active[0] = aex;
+    }
+  }
+  __syncthreads();
+  for (int q = tid; q < npairs; q += kRouterThreads) {
+    const int e = ws.ids[q];
+    if (e < 0 || e >= E) continue;
+    const int r = q / k;
+    int rank = 0;
+    for (int w = 0; w < (r >> 5); ++w) rank += __popc(mask[e * RW + w]);
+    rank += __popc(mask[e * RW + (r >> 5)] & ((1u << (r & 31)) - 1u));
+    const int pos = off[e] + rank;
+    ws.pair_order[pos] = q;
+    ws.pos_of_pair[q] = pos;
+  }
+  // ready for the next layer
+  if (tid == 0) {
+    ws.counters[0] = 0u;
+    ws.x_amax[0] = 0u;
+  }
+}
+
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+  const Workspace& ws = p.ws;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * p.EG + warp;
+  const int sl = blockIdx.y;
+  const int nch = p.H / 8;
+  const int c0 = sl * nch / p.S, c1 = (sl + 1) * nch / p.S;
+
+  // the expert's slice of the router weights (static): before the wait
+  uint4 wv[kRouterChunks];
+#pragma unroll
+  for (int i = 0; i < kRouterChunks; ++i) {
+    const int c = c0 + lane + 32 * i;
+    wv[i] = (warp < p.EG && e < p.E && c < c1)
+                ? __ldg(reinterpret_cast<const uint4*>(p.wr + (size_t)e * p.H) + c)
+                : make_uint4(0u, 0u, 0u, 0u);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (warp < p.EG && e < p.E) {
+    for (int r = 0; r < p.rows; ++r) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kRouterChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < c1) {
+          const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)r * p.H) + c);
+          acc = dot8_bf16(xv, wv[i], acc);
+        }
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) ws.logit_part[((size_t)sl * p.rows + r) * p.E + e] = acc;
+    }
+  }
+
+  // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks
+  const int ncta = gridDim.x * gridDim.y;
+  const int cta = blockIdx.y * gridDim.x + blockIdx.x;
+  const float sg = __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f);
+  const int nblk = p.rows * (p.H / 16);
+  const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
+  for (int b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
+    const uint4 q0 = __ldcg(src), q1 = __ldcg(src + 1);
+    float v[16];
+    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
+    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f0 = __bfloat1622float2(h0[i]), f1 = __bfloat1622float2(h1[i]);
+      v[2 * i] = f0.x;
+      v[2 * i + 1] = f0.y;
+      v[8 + 2 * i] = f1.x;
+      v[8 + 2 * i + 1] = f1.y;
+    }
+    uint32_t lo, hi, sb;
+    quant_block16(v, sg, lo, hi, sb);
+    *reinterpret_cast<uint2*>(ws.x_codes + (size_t)b * 8) = make_uint2(lo, hi);
+    ws.x_sf[b] = (uint8_t)sb;
+  }
+  if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
+
+  // last CTA: routing and pooling over every row
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(ws.counters, 1u);
+    s_last = (old == (unsigned)ncta - 1u);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  route_and_pool(p, smem);
+}
+
+}  // namespace
+
+size_t router_smem_bytes(int E, int rows) {
+  const int RW = (rows + 31) / 32;
+  return (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 + (size_t)E * RW * 4;
+}
+
+cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
+  const size_t smem = router_smem_bytes(p.E, p.rows);
+  static_assert(kMaxTopK <= 32, "one lane per selected expert");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_eg, p.S, 1);
+  cfg.blockDim = dim3(kRouterThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_kernel, p);
+}
+
+cudaError_t router_set_smem(size_t bytes) {
+  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)bytes);
+}
+
+}  // namespace moe

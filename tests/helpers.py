@@ -43,3 +43,73 @@ def oracle_weights(w, layer, experts=None):
 
 def silu(z):
     return z / (1.0 + np.exp(-z))
+
+
+# --------------------------------------------------------------- GPU side
+
+
+class _CudaArray:
+    """Zero-copy view of raw device memory for torch.as_tensor."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def dev_array(ptr, shape, dtype):
+    """Copy `shape` elements of numpy `dtype` at device address `ptr` to the host."""
+    import torch
+    dt = np.dtype(dtype)
+    t = torch.as_tensor(_CudaArray(ptr, shape, dt.str), device="cuda")
+    return t.cpu().numpy().copy()
+
+
+def read_debug(dec, rows):
+    """The workspace intermediates of the last layer run, as numpy arrays."""
+    v = dec.debug()
+    d = dec.dims
+    H, E, k, I = d.hidden, d.n_experts, d.top_k, d.inter
+    n = rows * k
+    out = dict(
+        x=dev_array(v.x, (rows, H), np.uint16),
+        x_codes=dev_array(v.x_codes, (rows, H // 2), np.uint8),
+        x_sf=dev_array(v.x_sf, (rows, H // 16), np.uint8),
+        x_sg=dev_array(v.x_sg, (1,), np.float32)[0],
+        logits=dev_array(v.logits, (rows, E), np.float32),
+        ids=dev_array(v.ids, (rows, k), np.int32),
+        gates=dev_array(v.gates, (rows, k), np.float32),
+        flags=dev_array(v.flags, (rows,), np.uint8),
+        count=dev_array(v.count, (E,), np.int32),
+        offset=dev_array(v.offset, (E + 1,), np.int32),
+        pair_order=dev_array(v.pair_order, (n,), np.int32),
+        pos_of_pair=dev_array(v.pos_of_pair, (n,), np.int32),
+        n_active=int(dev_array(v.n_active, (1,), np.int32)[0]),
+        h=dev_array(v.h, (n, I), np.float32),
+        h_sg=dev_array(v.h_sg, (E,), np.float32),
+        h_codes=dev_array(v.h_codes, (n, I // 2), np.uint8),
+        h_sf=dev_array(v.h_sf, (n, I // 16), np.uint8),
+        o=dev_array(v.o, (n, H), np.float32),
+    )
+    out["active"] = dev_array(v.active, (E,), np.int32)[: out["n_active"]]
+    return out
+
+
+def bf16_near_tie(exact, rel=1e-5):
+    """True where the fp64 value sits within `rel` (relative) of a bf16 rounding
+    midpoint, so fp32 and fp64 evaluations may round it differently."""
+    a = np.abs(np.asarray(exact, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    q = np.exp2(e - 7)                      # bf16 quantum in this binade
+    frac = a / q - np.floor(a / q)
+    return np.abs(frac - 0.5) * q <= rel * a
+
+
+def expert_subproblem(ow, e):
+    """A one-expert oracle.LayerWeights holding expert e of `ow` as expert 0."""
+    import oracle
+    g = np.zeros((1, 3), np.float32)
+    g[0] = ow.gscale[e]
+    return oracle.LayerWeights(1, ow.H, ow.I, ow.w_post, ow.w_pre, ow.router_w[:1], None,
+                               {0: ow.w13[e]}, {0: ow.w13_sf[e]}, {0: ow.w2[e]},
+                               {0: ow.w2_sf[e]}, g)

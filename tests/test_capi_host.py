@@ -1,0 +1,82 @@
+"""The C ABI library without a GPU: it loads, exports every symbol the public
+header declares, and rejects invalid arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decode_routed_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe_decode.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_symbols_are_exported():
+    lib = moe.lib()
+    names = _declared()
+    assert "moe_decode_create" in names and "moe_nvfp4_quantize" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe.EXPORTS) == names
+
+
+def _dims(**kw):
+    d = dict(hidden=256, n_experts=8, top_k=2, inter=128, max_rows=8, n_layers=1, eps=1e-6)
+    d.update(kw)
+    return moe.Dims(**d)
+
+
+def _fake_layer(align=256):
+    # non-null, aligned fake addresses: validation runs before any CUDA call
+    base = 1 << 20
+    return moe.LayerWeights(*(base + i * align for i in range(3)), None,
+                           *(base + (4 + i) * align for i in range(5)))
+
+
+def _create(dims, layers):
+    h = ctypes.c_void_p()
+    arr = (moe.LayerWeights * len(layers))(*layers)
+    rc = moe.lib().moe_decode_create(ctypes.byref(dims), arr, None, None, ctypes.byref(h))
+    return rc, moe.lib().moe_decode_error_message().decode()
+
+
+@pytest.mark.parametrize("kw", [dict(hidden=200), dict(hidden=16384), dict(inter=100),
+                                dict(n_experts=0), dict(n_experts=2000), dict(top_k=0),
+                                dict(top_k=9), dict(top_k=17, n_experts=32), dict(max_rows=0),
+                                dict(max_rows=129), dict(n_layers=0)])
+def test_unsupported_shapes(kw):
+    rc, msg = _create(_dims(**kw), [_fake_layer()])
+    assert rc == moe.MOE_EUNSUPPORTED, (kw, rc, msg)
+    assert msg
+
+
+def test_null_and_misaligned_pointers():
+    lay = _fake_layer()
+    lay.w13 = None
+    rc, msg = _create(_dims(), [lay])
+    assert rc == moe.MOE_EINVAL and "NULL" in msg
+    lay = _fake_layer()
+    lay.w2 = lay.w2 + 4
+    rc, msg = _create(_dims(), [lay])
+    assert rc == moe.MOE_EINVAL and "aligned" in msg
+    rc = moe.lib().moe_decode_create(None, None, None, None, None)
+    assert rc == moe.MOE_EINVAL
+
+
+def test_calls_on_a_null_handle_fail_cleanly():
+    L = moe.lib()
+    assert L.moe_decode_layer(None, 0, 1, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_decode_step(None, 1, None, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_decode_final(None, 1, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_decode_last_error(None) == moe.MOE_EINVAL
+    assert L.moe_decode_workspace_bytes(None) == 0
+    L.moe_decode_destroy(None)
+    assert L.moe_decode_strerror(moe.MOE_EDEVICE).decode() == "device-side check failed"
+    assert L.moe_nvfp4_quantize(None, 1, 16, None, None, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_nvfp4_quantize(1 << 20, 1, 17, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None) == moe.MOE_EINVAL

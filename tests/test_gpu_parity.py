@@ -1,0 +1,370 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Staged checks feed each oracle stage the GPU's own output of the stage before
+(the ids, the MoE input's codes, h), so every integer decision is compared bit
+for bit and every floating-point stage against a tight tolerance; the
+end-to-end checks run the oracle independently and apply the workload's
+stream tolerance max|err| <= 2e-3 * rms(stream).  Rows whose k-th/(k+1)-th
+router-probability gap is below 1e-6 are flagged and excluded from id checks.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (bf16_near_tie, dev_array, expert_subproblem, oracle_weights, read_debug)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+STREAM_TOL = 2e-3          # end-to-end: max|err| <= STREAM_TOL * rms(stream)
+STAGE_TOL = 1e-4           # staged floats: max|err| <= STAGE_TOL * rms(reference)
+
+
+def _rms(a):
+    return float(np.sqrt(np.mean(np.asarray(a, np.float64) ** 2)))
+
+
+def _close(got, ref, tol, what):
+    err = float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64)))) if np.size(ref) else 0.0
+    bound = tol * max(_rms(ref), 1e-30)
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e}"
+    return err
+
+
+def _bf16_f32(bits):
+    return oracle.bf16_to_f64(bits).astype(np.float32)
+
+
+def _sgpu():
+    import synth.gpu as sgpu
+    return sgpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import speculative_decode_routed_gb300 as moe
+    moe.lib()
+    yield
+
+
+# ----------------------------------------------------------------- pieces
+
+
+@pytest.mark.parametrize("shape,scale", [((1, 16), 1.0), ((3, 48), 1e-3), ((64, 256), 0.02),
+                                         ((7, 7168), 3.0), ((128, 2048), 1e4)])
+def test_quantizer_bit_exact(shape, scale):
+    import speculative_decode_routed_gb300 as moe
+    rs = np.random.RandomState(sum(shape))
+    v = (rs.standard_normal(shape) * scale).astype(np.float32)
+    v[0, :16] = 0.0                                     # a zero block
+    if shape[1] >= 32:
+        v[-1, 16:32] = np.float32(scale) * np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25] * 2)
+    codes, sf, sg, amax = oracle.nvfp4_quantize(v)
+    tv = torch.from_numpy(v).cuda()
+    tc = torch.empty(shape[0], shape[1] // 2, dtype=torch.uint8, device="cuda")
+    ts = torch.empty(shape[0], shape[1] // 16, dtype=torch.uint8, device="cuda")
+    tg = torch.empty(1, device="cuda")
+    ta = torch.empty(1, device="cuda")
+    moe.moe_nvfp4_quantize(tv, tc, ts, tg, ta)
+    torch.cuda.synchronize()
+    assert ta.item() == amax and tg.item() == sg
+    assert np.array_equal(ts.cpu().numpy(), sf)
+    assert np.array_equal(tc.cpu().numpy(), codes)
+
+
+def test_quantizer_zero_tensor():
+    import speculative_decode_routed_gb300 as moe
+    tv = torch.zeros(4, 64, device="cuda")
+    tc = torch.full((4, 32), 0xAB, dtype=torch.uint8, device="cuda")
+    ts = torch.full((4, 4), 0xAB, dtype=torch.uint8, device="cuda")
+    tg = torch.full((1,), 7.0, device="cuda")
+    ta = torch.full((1,), 7.0, device="cuda")
+    moe.moe_nvfp4_quantize(tv, tc, ts, tg, ta)
+    torch.cuda.synchronize()
+    assert tg.item() == 0.0 and ta.item() == 0.0
+    assert not tc.any().item() and not ts.any().item()
+
+
+def test_device_generator_bit_exact():
+    for tg, (mu, sd), n in ((synth.tag(synth.KIND_GATE, 2, 17), (0.0, 0.02), 100003),
+                            (synth.tag(synth.KIND_W_PRE, 0), (1.0, 0.1), 4096)):
+        t = torch.empty(n, device="cuda")
+        synth.dev_normal_f32(t, 0, tg, mu, sd)
+        assert np.array_equal(t.cpu().numpy(), synth.normal_f32((n,), 0, tg, mu, sd))
+    b = torch.empty(5000, dtype=torch.bfloat16, device="cuda")
+    synth.dev_normal_bf16(b, 3, 9)
+    assert np.array_equal(b.view(torch.uint16).cpu().numpy(), synth.normal_bf16((5000,), 3, 9))
+
+
+# -------------------------------------------------------- staged layer check
+
+
+def _check_weights(dec, ow, layer, experts):
+    t = dec.layers[layer]
+    for e in experts:
+        assert np.array_equal(t.w13[e].cpu().numpy(), ow.w13[e]), f"w13 codes of expert {e}"
+        assert np.array_equal(t.w13_sf[e].cpu().numpy(), ow.w13_sf[e])
+        assert np.array_equal(t.w2[e].cpu().numpy(), ow.w2[e])
+        assert np.array_equal(t.w2_sf[e].cpu().numpy(), ow.w2_sf[e])
+        assert np.array_equal(t.w_gscale[e].cpu().numpy(), ow.gscale[e])
+
+
+def staged_layer(w, dec, ow, layer, rows, branch, stream, experts="all", prev=None):
+    """Run one layer on the GPU and check every stage.  branch: bf16 CUDA tensor,
+    or None (chained: the previous layer's unpooled output, from `prev`)."""
+    k, E, I = w.top_k, w.n_experts, w.inter
+    s_in = stream.cpu().numpy().copy()
+    dec.layer(layer, rows, branch, stream)
+    torch.cuda.synchronize()
+    dec.check()
+    d = read_debug(dec, rows)
+
+    # A: dual-norm boundary
+    if branch is not None:
+        br = oracle.bf16_to_f64(branch.view(torch.uint16).cpu().numpy())
+    else:
+        br = oracle.gather(prev["gates"].astype(np.float64), prev["o"], k)
+    s_ref, x_ref, xe = oracle.boundary(br, s_in, ow.w_post, ow.w_pre, w.eps)
+    _close(stream.cpu().numpy(), s_ref, 1e-5, "stream after the boundary")
+    diff = d["x"] != x_ref
+    assert not np.any(diff & ~bf16_near_tie(xe)), "MoE input differs away from bf16 near-ties"
+
+    # B: router, routing, pooler, activation quantization (from the GPU's x)
+    r = oracle.route(d["x"], ow.router_w, ow.router_bias, k)
+    ok_rows = r["flags"] == 0
+    assert np.array_equal(d["ids"][ok_rows], r["ids"][ok_rows]), "expert ids"
+    np.testing.assert_allclose(d["gates"][ok_rows], r["gates"][ok_rows], atol=1e-5)
+    np.testing.assert_allclose(d["gates"].sum(1), 1.0, atol=1e-6)
+    _close(d["logits"], r["logits"], 1e-5, "router logits")
+    pl = oracle.pool(d["ids"], E)
+    for key in ("count", "offset", "pair_order"):
+        assert np.array_equal(d[key], pl[key]), key
+    assert d["n_active"] == pl["n_active"] and np.array_equal(d["active"], pl["active"])
+    xc, xs, xg, _ = oracle.nvfp4_quantize(_bf16_f32(d["x"]))
+    assert d["x_sg"] == xg and np.array_equal(d["x_sf"], xs) and np.array_equal(d["x_codes"], xc)
+
+    # C-E: experts, per expert, on the GPU's own stage inputs
+    active = list(d["active"]) if experts == "all" else [e for e in experts if d["count"][e] > 0]
+    for e in active:
+        p0, p1 = d["offset"][e], d["offset"][e + 1]
+        pairs = d["pair_order"][p0:p1]
+        n = p1 - p0
+        sub = expert_subproblem(ow, e)
+        zi, off, order = np.zeros((n, 1), np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32)
+        rws = pairs // k
+        h_ref = oracle.gate_up(sub, 1, d["x_codes"][rws], d["x_sf"][rws], d["x_sg"], zi, off, order)
+        _close(d["h"][p0:p1], h_ref, STAGE_TOL, f"h of expert {e}")
+        hq = oracle.h_quant(1, I, off, d["h"][p0:p1])
+        assert d["h_sg"][e] == hq["h_sg"][0], f"h scale of expert {e}"
+        assert np.array_equal(d["h_sf"][p0:p1], hq["h_sf"]), f"h block scales of expert {e}"
+        assert np.array_equal(d["h_codes"][p0:p1], hq["h_codes"]), f"h codes of expert {e}"
+        o_ref = oracle.down(sub, 1, zi, off, order, d["h_codes"][p0:p1], d["h_sf"][p0:p1],
+                            np.array([d["h_sg"][e]], np.float32))
+        _close(d["o"][pairs], o_ref, STAGE_TOL, f"o of expert {e}")
+    d["stream"] = stream.cpu().numpy().copy()
+    return d
+
+
+def _final_check(w, dec, d, rows, stream):
+    wpf, wf = synth.final_norm_weights(w)
+    out = torch.empty(rows, w.hidden, dtype=torch.bfloat16, device="cuda")
+    s_in = stream.cpu().numpy().copy()
+    dec.final(rows, stream, out)
+    torch.cuda.synchronize()
+    y = oracle.gather(d["gates"].astype(np.float64), d["o"], w.top_k)
+    s_ref, out_ref, oe = oracle.boundary(y, s_in, wpf, wf, w.eps)
+    _close(stream.cpu().numpy(), s_ref, 1e-5, "stream after the final boundary")
+    got = out.view(torch.uint16).cpu().numpy()
+    assert not np.any((got != out_ref) & ~bf16_near_tie(oe)), "final output away from near-ties"
+
+
+def test_tiny_layer_staged():
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    ow = oracle_weights(w, 0)
+    _check_weights(dec, ow, 0, range(w.n_experts))
+    stream, branch = sgpu.step_tensors(w)
+    d = staged_layer(w, dec, ow, 0, w.rows, branch, stream)
+    _final_check(w, dec, d, w.rows, stream)
+    dec.close()
+
+
+def _oracle_step(w, variant=0, experts_needed=None):
+    stream, branch = synth.step_inputs(w, variant)
+    s = stream
+    br = oracle.bf16_to_f64(branch)
+    outs = []
+    for l in range(w.n_layers):
+        ow = oracle_weights(w, l)
+        o = oracle.layer_step(ow, w.top_k, w.eps, br, s)
+        outs.append(o)
+        s = o["stream"]
+        br = oracle.gather(o["gates"], o["o"], w.top_k)
+    wpf, wf = synth.final_norm_weights(w)
+    s, out, _ = oracle.boundary(br, s, wpf, wf, w.eps)
+    return s, out, outs
+
+
+def test_tiny_step_end_to_end_graph_and_host():
+    import speculative_decode_routed_gb300 as moe
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    s_ref, out_ref, outs = _oracle_step(w)
+    # eager
+    stream, branch = sgpu.step_tensors(w)
+    out = torch.empty_like(branch)
+    dec.step(w.rows, branch, stream, out)
+    torch.cuda.synchronize()
+    dec.check()
+    ids = dev_array(dec.debug().ids, (w.rows, w.top_k), np.int32)
+    ok = outs[-1]["flags"] == 0
+    assert np.array_equal(ids[ok], outs[-1]["ids"][ok])
+    eager_stream, eager_out = stream.cpu().numpy(), out.view(torch.uint16).cpu().numpy()
+    err = np.abs(eager_stream - s_ref).max()
+    assert err <= STREAM_TOL * _rms(s_ref), f"end-to-end stream max|err| {err:.3e}"
+    assert np.mean(eager_out != out_ref) < 0.02
+    # graph replay is bitwise the eager result, twice in a row
+    for _ in range(2):
+        stream2, branch2 = sgpu.step_tensors(w)
+        out2 = torch.empty_like(branch2)
+        dec.step_graph(w.rows, branch2, stream2, out2)
+        torch.cuda.synchronize()
+        assert np.array_equal(stream2.cpu().numpy(), eager_stream)
+        assert np.array_equal(out2.view(torch.uint16).cpu().numpy(), eager_out)
+    # host-buffer path
+    s_h, b_h = synth.step_inputs(w)
+    sh = torch.from_numpy(s_h).pin_memory()
+    bh = torch.from_numpy(b_h).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(bh).pin_memory()
+    dec.step_host(w.rows, bh, sh, oh)
+    assert np.array_equal(sh.numpy(), eager_stream)
+    assert np.array_equal(oh.view(torch.uint16).numpy(), eager_out)
+    assert moe.moe_decode_step_kernel_count(dec.handle) == 4 * w.n_layers + 1
+    dec.close()
+
+
+ODD_SHAPES = [
+    # (rows, H, E, k, I): a ragged H (cluster of 1, 12 chunks/row), a single
+    # expert, k == E, a row count with many rows per expert (> 8: the
+    # multi-group path), one row
+    (5, 384, 6, 3, 384),
+    (3, 128, 1, 1, 128),
+    (3, 1024, 16, 16, 256),
+    (128, 256, 8, 2, 128),
+    (1, 512, 32, 4, 640),
+]
+
+
+@pytest.mark.parametrize("rows,H,E,k,I", ODD_SHAPES)
+def test_odd_shapes_staged(rows, H, E, k, I):
+    w = synth.Workload(f"odd{H}", rows=rows, hidden=H, n_experts=E, top_k=k, inter=I)
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    ow = oracle_weights(w, 0)
+    stream, branch = sgpu.step_tensors(w)
+    d = staged_layer(w, dec, ow, 0, rows, branch, stream)
+    _final_check(w, dec, d, rows, stream)
+    dec.close()
+
+
+def test_zero_branch_keeps_stream_and_rows_below_max():
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w, max_rows=16)
+    ow = oracle_weights(w, 0)
+    stream, branch = sgpu.step_tensors(w)
+    s0 = stream.cpu().numpy().copy()
+    zero = torch.zeros_like(branch)
+    dec.layer(0, w.rows, zero, stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(stream.cpu().numpy(), s0)
+    # fewer rows than max_rows
+    stream, branch = sgpu.step_tensors(w)
+    staged_layer(w, dec, ow, 0, 3, branch[:3], stream[:3].clone())
+    dec.close()
+
+
+# ------------------------------------------------------------- full sizes
+
+
+def _sample_experts(d, n_extra=2, seed=0):
+    """The expert with the most pairs plus a few seeded picks among the active."""
+    act = list(d["active"])
+    hot = int(max(act, key=lambda e: d["count"][e]))
+    rs = np.random.RandomState(seed)
+    pick = [int(e) for e in rs.choice(act, size=min(n_extra, len(act)), replace=False)]
+    return sorted(set([hot] + pick))
+
+
+def _staged_full(w, dec, layer, rows, branch, stream, n_extra=2, prev=None):
+    """Staged check at full size: routing / pooler / act quant for every row,
+    experts on a sample (weights quantized by the oracle only for those)."""
+    s_before = stream.clone()
+    dec.layer(layer, rows, branch, stream)
+    torch.cuda.synchronize()
+    d0 = read_debug(dec, rows)
+    sample = _sample_experts(d0, n_extra, seed=layer)
+    ow = oracle_weights(w, layer, experts=sample)
+    _check_weights(dec, ow, layer, sample)
+    stream.copy_(s_before)
+    return staged_layer(w, dec, ow, layer, rows, branch, stream, experts=sample, prev=prev)
+
+
+@pytest.mark.slow
+def test_serving_width_layer_sampled():
+    """One layer at serving width (H 7168, 256 experts, top-8, I 2048, b 8): the
+    bench's configuration and launch path."""
+    w = synth.WORKLOADS["serving"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    d = _staged_full(w, dec, 0, w.rows, branch, stream)
+    _final_check(w, dec, d, w.rows, stream)
+    # the graph-replayed step matches the eager step bit for bit
+    s1, b1 = sgpu.step_tensors(w, variant=1)
+    o1 = torch.empty_like(b1)
+    dec.step(w.rows, b1, s1, o1)
+    s2, b2 = sgpu.step_tensors(w, variant=1)
+    o2 = torch.empty_like(b2)
+    dec.step_graph(w.rows, b2, s2, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2) and torch.equal(o1, o2)
+    dec.close()
+
+
+@pytest.mark.slow
+def test_chained_layers_sampled():
+    """Eight chained layers (H 5120, 128 experts, top-8, I 1536): each layer's
+    stages checked on a sample, the chained gather included, then the graph."""
+    w = synth.WORKLOADS["chained8"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    prev = None
+    for l in range(w.n_layers):
+        prev = _staged_full(w, dec, l, w.rows, branch if l == 0 else None, stream, n_extra=1,
+                            prev=prev)
+    _final_check(w, dec, prev, w.rows, stream)
+    eager_stream = stream.clone()
+    s2, b2 = sgpu.step_tensors(w)
+    o2 = torch.empty_like(b2)
+    dec.step_graph(w.rows, b2, s2, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(s2, eager_stream)
+    dec.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("rows", synth.SWEEP_ROWS)
+def test_batch_skew_sweep_sampled(rows):
+    """H 7168, 256 experts, top-8, I 2048 with a Zipf(1.1) logit bias, b in
+    {1, 8, 32, 64, 128}; the hottest expert (most rows) is always checked."""
+    w = synth.WORKLOADS["sweep"].with_rows(rows)
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    _staged_full(w, dec, 0, rows, branch, stream, n_extra=1)
+    dec.close()
