@@ -19,10 +19,11 @@
 //  - One persistent CTA per SM.  Work item = (active expert, tile of weight
 //    rows); each CTA takes a contiguous run of items, so it streams a long
 //    contiguous stretch of each expert's weights.
-//  - A producer warp moves each item's packed codes and e4m3 scales
-//    global -> shared with bulk async copies (evict-first in L2) into a ring
-//    of stages tracked by mbarriers (full: complete_tx; empty: consumer
-//    warps), so ~200 KB per SM is in flight ahead of the math.
+//  - Each item's packed codes and e4m3 scales move global -> shared with
+//    bulk async copies (evict-first in L2) into a ring of stages tracked by
+//    mbarriers (complete_tx); thread 0 refills a stage as soon as the
+//    per-item barrier shows every thread is done with it, so the copies of
+//    the next NS-1 items (~130-190 KB per SM) are in flight ahead of the math.
 //  - Consumer threads own a fixed 16-byte column chunk (32 elements, two
 //    16-blocks) of every weight row; the expert's activation rows for that
 //    chunk stay in registers as signed bytes (2 x e2m1 value, exact).  A
@@ -45,18 +46,18 @@ namespace {
 
 constexpr int kRedFloats = 8 * kTW * kMaxRB;  // one reduction buffer: 8 warps x 64 values
 constexpr int kMaxPairs = 128;                 // pairs of one expert <= rows <= 128
-constexpr int kCtrlBytes = 512 + 2 * kRedFloats * 4 + kMaxPairs * 4 + 64;
+constexpr int kExpertTable = 64;               // experts of one CTA's run kept in smem
+constexpr int kCtrlBytes = 512 + kExpertTable * 16 + 2 * kRedFloats * 4 + kMaxPairs * 4 + 64;
 
 // Shared memory: [barriers + stage metadata | 2 reduction buffers | pair ids
 // of the current expert | flags] then the stage ring.
 struct Smem {
   uint64_t* full;
-  uint64_t* empty;
   int4* meta;       // per stage: expert, tile, first pooled position, pairs
+  int4* etab;       // this CTA's experts in run order: expert, first position, pairs
   float* red;       // [2][kRedFloats]
   int* pairs;       // [kMaxPairs] pair ids of the current expert (down)
   int* flag;        // last-CTA verdict of finish_expert
-  int* abort;
   int* ok;          // stage verdict of the current item
   uint8_t* stages;
 };
@@ -64,13 +65,12 @@ struct Smem {
 __device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
   s.full = reinterpret_cast<uint64_t*>(base);        // 16 x 8 B
-  s.empty = s.full + 16;                             // 16 x 8 B
   s.meta = reinterpret_cast<int4*>(base + 256);      // 16 x 16 B
-  s.red = reinterpret_cast<float*>(base + 512);
-  s.pairs = reinterpret_cast<int*>(base + 512 + 2 * kRedFloats * 4);
+  s.etab = reinterpret_cast<int4*>(base + 512);      // kExpertTable x 16 B
+  s.red = reinterpret_cast<float*>(base + 512 + kExpertTable * 16);
+  s.pairs = reinterpret_cast<int*>(base + 512 + kExpertTable * 16 + 2 * kRedFloats * 4);
   s.flag = s.pairs + kMaxPairs;
-  s.abort = s.flag + 1;
-  s.ok = s.flag + 2;
+  s.ok = s.flag + 1;
   s.stages = base + ((kCtrlBytes + 1023) / 1024) * 1024;
   return s;
 }
@@ -277,101 +277,106 @@ __device__ void finish_expert(const ExpertParams& p, const Smem& sm, int e, int 
   named_bar(1, NC);
 }
 
+// Issue the bulk copies of item `n` of this CTA's run into its stage
+// (thread 0 only).  Stage metadata (expert, tile, first pooled position,
+// pairs) rides along in shared memory.
+__device__ __forceinline__ bool issue_item(const ExpertParams& p, const Smem& sm, bool gate_up,
+                                           int it, int n, int ai_first, uint64_t pol) {
+  const Workspace& ws = p.ws;
+  const int s = n % p.NS;
+  const int ai = it / p.tiles, tile = it % p.tiles;
+  const int q = ai - ai_first;
+  int4 et;
+  if (q < kExpertTable) {
+    et = sm.etab[q];
+  } else {  // long runs over many experts: read the routing directly
+    const int e = __ldcg(ws.active + ai);
+    const int pos0 = (e >= 0 && e < p.E) ? __ldcg(ws.offset + e) : 0;
+    const int ne = (e >= 0 && e < p.E) ? __ldcg(ws.offset + e + 1) - pos0 : 0;
+    et = make_int4(e, pos0, ne, 0);
+  }
+  const int e = et.x, pos0 = et.y, ne = et.z;
+  if (e < 0 || e >= p.E || pos0 < 0 || ne < 1 || ne > kMaxPairs || pos0 + ne > p.ws_pairs) {
+    latch_error(ws.err, kDevBadRouting);
+    return false;
+  }
+  sm.meta[s] = make_int4(e, tile, pos0, ne);
+  uint8_t* dst = sm.stages + (size_t)s * p.stage_stride;
+  // the stage was last read through the generic proxy; order that before the
+  // async-proxy writes that refill it
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_expect_tx(&sm.full[s], p.stage_bytes);
+  if (gate_up) {
+    const size_t rg = (size_t)e * p.RE + (size_t)tile * p.TJ;  // gate rows
+    const size_t ru = rg + p.I;                                 // up rows
+    const uint32_t cb = (uint32_t)(p.TJ * p.KB), sb = (uint32_t)(p.TJ * p.KS);
+    bulk_g2s(dst, p.w + rg * p.KB, cb, &sm.full[s], pol);
+    bulk_g2s(dst + cb, p.w + ru * p.KB, cb, &sm.full[s], pol);
+    bulk_g2s(dst + 2 * cb, p.w_sf + rg * p.KS, sb, &sm.full[s], pol);
+    bulk_g2s(dst + 2 * cb + sb, p.w_sf + ru * p.KS, sb, &sm.full[s], pol);
+  } else {
+    const size_t r0 = (size_t)e * p.RE + (size_t)tile * p.T;
+    bulk_g2s(dst, p.w + r0 * p.KB, (uint32_t)(p.T * p.KB), &sm.full[s], pol);
+    bulk_g2s(dst + (size_t)p.T * p.KB, p.w_sf + r0 * p.KS, (uint32_t)(p.T * p.KS), &sm.full[s],
+             pol);
+  }
+  return true;
+}
+
+// One CTA per SM by design (about 200 KB of shared memory), at most 8 warps:
+// two warps per SM sub-partition leave room for up to 224 registers per
+// thread, which keeps the RB = 8 path free of spills.
 template <bool kGU>
-// One CTA per SM by design (about 200 KB of shared memory): 9 warps may use
-// up to 224 registers each, which keeps the RB = 8 path free of spills.
 __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const Workspace& ws = p.ws;
   const int tid = threadIdx.x;
-  const int NC = p.G * p.TPG;  // consumer threads
-  const int ncw = NC / 32;
+  const int NC = p.G * p.TPG;  // every thread computes; thread 0 also feeds the ring
 
   if (tid == 0) {
-    for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], ncw);
-    }
-    *sm.abort = 0;
+    for (int s = 0; s < p.NS; ++s) mbar_init(&sm.full[s], 1);
     mbar_fence_init();
   }
-  __syncthreads();
 
   // Gate/up needs the routing of the kernel before it; down's weights and
   // work list depend only on that routing (final before the gate/up kernel
-  // started), so its producer may run ahead of the wait.
+  // started), so its first copies may be issued ahead of the wait.
   if (kGU) {
     grid_dep_wait();
     grid_dep_launch();
   }
   const int na = __ldcg(ws.n_active);
-  if (na < 0 || na > p.E) {
+  const bool na_ok = na >= 0 && na <= p.E;
+  const int n_items = na_ok ? na * p.tiles : 0;
+  const int it0 = (int)((long long)blockIdx.x * n_items / gridDim.x);
+  const int it1 = (int)((long long)(blockIdx.x + 1) * n_items / gridDim.x);
+  const int count = it1 - it0;
+  const int ai_first = count > 0 ? it0 / p.tiles : 0;
+  const int nai = count > 0 ? (it1 - 1) / p.tiles - ai_first + 1 : 0;
+  for (int q = tid; q < nai && q < kExpertTable; q += NC) {
+    const int e = __ldcg(ws.active + ai_first + q);
+    const bool ok = e >= 0 && e < p.E;
+    const int pos0 = ok ? __ldcg(ws.offset + e) : 0;
+    sm.etab[q] = make_int4(e, pos0, ok ? __ldcg(ws.offset + e + 1) - pos0 : 0, 0);
+  }
+  __syncthreads();
+  if (!na_ok) {
     if (tid == 0) latch_error(ws.err, kDevBadRouting);
     return;
   }
-  const int n_items = na * p.tiles;
-  const int it0 = (int)((long long)blockIdx.x * n_items / gridDim.x);
-  const int it1 = (int)((long long)(blockIdx.x + 1) * n_items / gridDim.x);
 
-  if (tid >= NC) {
-    // ---------------------------------------------------------- producer
-    if (tid == NC) {
-      const uint64_t pol = l2_evict_first_policy();
-      int cur_ai = -1, e = 0, pos0 = 0, ne = 0;
-      int n = 0;
-      for (int it = it0; it < it1; ++it, ++n) {
-        const int s = n % p.NS;
-        if (n >= p.NS && !mbar_wait(&sm.empty[s], ((n / p.NS) - 1) & 1)) {
-          latch_error(ws.err, kDevWaitTimeout);
-          break;
-        }
-        if (*reinterpret_cast<volatile int*>(sm.abort)) break;
-        const int ai = it / p.tiles, tile = it % p.tiles;
-        if (ai != cur_ai) {
-          cur_ai = ai;
-          e = __ldcg(ws.active + ai);
-          const bool e_ok = e >= 0 && e < p.E;
-          pos0 = e_ok ? __ldcg(ws.offset + e) : 0;
-          ne = e_ok ? __ldcg(ws.offset + e + 1) - pos0 : 0;
-          if (!e_ok || pos0 < 0 || ne < 1 || ne > kMaxPairs || pos0 + ne > p.ws_pairs) {
-            latch_error(ws.err, kDevBadRouting);
-            *reinterpret_cast<volatile int*>(sm.abort) = 1;
-            break;
-          }
-        }
-        sm.meta[s] = make_int4(e, tile, pos0, ne);
-        uint8_t* dst = sm.stages + (size_t)s * p.stage_stride;
-        mbar_arrive_expect_tx(&sm.full[s], p.stage_bytes);
-        if (kGU) {
-          const size_t rg = (size_t)e * p.RE + (size_t)tile * p.TJ;  // gate rows
-          const size_t ru = rg + p.I;                                 // up rows
-          const uint32_t cb = (uint32_t)(p.TJ * p.KB), sb = (uint32_t)(p.TJ * p.KS);
-          bulk_g2s(dst, p.w + rg * p.KB, cb, &sm.full[s], pol);
-          bulk_g2s(dst + cb, p.w + ru * p.KB, cb, &sm.full[s], pol);
-          bulk_g2s(dst + 2 * cb, p.w_sf + rg * p.KS, sb, &sm.full[s], pol);
-          bulk_g2s(dst + 2 * cb + sb, p.w_sf + ru * p.KS, sb, &sm.full[s], pol);
-        } else {
-          const size_t r0 = (size_t)e * p.RE + (size_t)tile * p.T;
-          bulk_g2s(dst, p.w + r0 * p.KB, (uint32_t)(p.T * p.KB), &sm.full[s], pol);
-          bulk_g2s(dst + (size_t)p.T * p.KB, p.w_sf + r0 * p.KS, (uint32_t)(p.T * p.KS),
-                   &sm.full[s], pol);
-        }
-      }
-      // every issued copy lands before the CTA may exit
-      for (int s = 0; s < p.NS && s < n; ++s) {
-        const int last = s + p.NS * ((n - 1 - s) / p.NS);
-        if (!mbar_wait(&sm.full[s], (last / p.NS) & 1)) latch_error(ws.err, kDevWaitTimeout);
-      }
-    }
-    return;
+  const uint64_t pol = l2_evict_first_policy();
+  int issued = 0;  // thread 0: items whose copies are in flight or landed
+  if (tid == 0) {
+    for (; issued < count && issued < p.NS; ++issued)
+      if (!issue_item(p, sm, kGU, it0 + issued, issued, ai_first, pol)) break;
   }
-
-  // ------------------------------------------------------------ consumers
   if (!kGU) {
     grid_dep_wait();  // h codes and scales come from the gate/up kernel
     grid_dep_launch();
   }
+
   const int cc = tid % p.TPG;
   const bool live = cc < p.CH;
   const int lane = tid & 31;
@@ -382,27 +387,27 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
   float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
   int gi = 0;
 
-  for (int it = it0, n = 0; it < it1; ++it, ++n) {
+  for (int n = 0; n < count; ++n) {
     const int s = n % p.NS;
-    // One thread waits (bounded) for the stage; the barrier hands its
-    // acquire and its verdict to every consumer, so all of them take the
-    // same path and none can be left behind at a later barrier.
+    // Thread 0 waits (bounded) for the stage; the barrier hands its acquire
+    // and its verdict to every thread, so all take the same path and none is
+    // left behind at a later barrier.  Passing the barrier also proves every
+    // thread is done with item n-1, so its stage is refilled right after.
     if (tid == 0) {
-      const bool got = mbar_wait(&sm.full[s], (n / p.NS) & 1);
-      if (!got) {
-        latch_error(ws.err, kDevWaitTimeout);
-        *reinterpret_cast<volatile int*>(sm.abort) = 1;
-      }
+      bool got = n < issued && mbar_wait(&sm.full[s], (n / p.NS) & 1);
+      if (!got) latch_error(ws.err, kDevWaitTimeout);
       *sm.ok = got ? 1 : 0;
     }
     named_bar(1, NC);
     if (*reinterpret_cast<volatile int*>(sm.ok) == 0) break;
+    if (tid == 0 && n >= 1 && issued < count && issued == n - 1 + p.NS) {
+      if (issue_item(p, sm, kGU, it0 + issued, issued, ai_first, pol)) ++issued;
+    }
     const int4 m = sm.meta[s];
     const int e = m.x, tile = m.y, pos0 = m.z, ne = m.w;
     if (e != cur_e) {
-      // (the item barrier above already ordered every read of the previous
-      // expert's pair ids before these writes)
-      if (kGU && cur_e >= 0) finish_expert(p, sm, cur_e, cur_tiles, cur_pos0, cur_ne, cur_amax, tid, NC);
+      if (kGU && cur_e >= 0)
+        finish_expert(p, sm, cur_e, cur_tiles, cur_pos0, cur_ne, cur_amax, tid, NC);
       cur_e = e;
       cur_pos0 = pos0;
       cur_ne = ne;
@@ -412,8 +417,10 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
         sc0 = __ldg(p.gscale + 3 * e + 0) * x_sg * 0.25f;
         sc1 = __ldg(p.gscale + 3 * e + 1) * x_sg * 0.25f;
       } else {
+        // (the item barrier above ordered every read of the previous
+        // expert's pair ids before these writes)
         sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e) * 0.25f;
-        for (int q = tid; q < ne && q < kMaxPairs; q += NC) sm.pairs[q] = __ldcg(ws.pair_order + pos0 + q);
+        for (int q = tid; q < ne; q += NC) sm.pairs[q] = __ldcg(ws.pair_order + pos0 + q);
       }
       const int rb = min(kMaxRB, ne);
       if (ne <= kMaxRB) {
@@ -439,11 +446,16 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
         run_group<8, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, xa, sx, sc0, sc1, cur_amax);
     }
     ++cur_tiles;
-    // the stage is free again (every read of it happened before the group barrier)
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
   if (kGU && cur_e >= 0) finish_expert(p, sm, cur_e, cur_tiles, cur_pos0, cur_ne, cur_amax, tid, NC);
+  // every issued copy has landed before the CTA may exit (normally all were
+  // consumed already; after an early stop this drains the ring)
+  if (tid == 0) {
+    for (int s = 0; s < p.NS && s < issued; ++s) {
+      const int last = s + p.NS * ((issued - 1 - s) / p.NS);
+      (void)mbar_wait(&sm.full[s], (last / p.NS) & 1);
+    }
+  }
 }
 
 }  // namespace
@@ -463,7 +475,7 @@ cudaError_t expert_set_smem(size_t bytes) {
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(p.G * p.TPG + 32, 1, 1);
+  cfg.blockDim = dim3(p.G * p.TPG, 1, 1);
   cfg.dynamicSmemBytes = expert_smem_bytes(p);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -94,15 +94,19 @@ def read_debug(dec, rows):
     return out
 
 
-def bf16_near_tie(exact, rel=1e-5):
-    """True where the fp64 value sits within `rel` (relative) of a bf16 rounding
-    midpoint, so fp32 and fp64 evaluations may round it differently."""
-    a = np.abs(np.asarray(exact, np.float64))
+def bf16_near_tie(exact, rel=1e-5, abs_frac=1e-5):
+    """True where the fp64 value sits within rel * |value| + abs_frac * rms(values)
+    of a bf16 rounding midpoint, so an fp32 evaluation may round it the other
+    way.  The absolute term covers values left small by cancellation, whose
+    fp32 relative error is large although their absolute error is not."""
+    x = np.asarray(exact, np.float64)
+    a = np.abs(x)
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    q = np.exp2(e - 7)                      # bf16 quantum in this binade
+    q = np.exp2(np.maximum(e, -126) - 7)        # bf16 quantum in this binade
     frac = a / q - np.floor(a / q)
-    return np.abs(frac - 0.5) * q <= rel * a
+    tol = rel * a + abs_frac * np.sqrt(np.mean(x ** 2))
+    return np.abs(frac - 0.5) * q <= tol
 
 
 def expert_subproblem(ow, e):
