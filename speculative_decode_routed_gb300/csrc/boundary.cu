@@ -65,14 +65,24 @@ __global__ void boundary_kernel(BoundaryParams p) {
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
       y = make_float4(a.x, a.y, b.x, b.y);
     } else {
-      for (int s = 0; s < p.k; ++s) {
-        const float g = __ldcg(p.gates + r * p.k + s);
-        const float4 o =
-            __ldcg(reinterpret_cast<const float4*>(p.o + ((size_t)r * p.k + s) * p.H + col));
-        y.x = fmaf(g, o.x, y.x);
-        y.y = fmaf(g, o.y, y.y);
-        y.z = fmaf(g, o.z, y.z);
-        y.w = fmaf(g, o.w, y.w);
+      // all slots' loads in flight at once (k <= 16), summed in slot order
+      float g[16];
+      float4 o[16];
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        if (s < p.k) {
+          g[s] = __ldcg(p.gates + r * p.k + s);
+          o[s] = __ldcg(reinterpret_cast<const float4*>(p.o + ((size_t)r * p.k + s) * p.H + col));
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        if (s < p.k) {
+          y.x = fmaf(g[s], o[s].x, y.x);
+          y.y = fmaf(g[s], o[s].y, y.y);
+          y.z = fmaf(g[s], o[s].z, y.z);
+          y.w = fmaf(g[s], o[s].w, y.w);
+        }
       }
     }
   }

@@ -89,26 +89,34 @@ int plan_experts(moe::ExpertParams& p, int mode, const moe_decode_dims& d) {
   p.KS = p.K / 16;
   p.CH = p.K / 32;
   p.TPG = ((p.CH + 31) / 32) * 32;
-  if (p.TPG > 256) return fail(MOE_EUNSUPPORTED, "reduction length %d > 8192", p.K);
-  p.G = 256 / p.TPG;
-  p.TW = moe::kTW;
-  p.T = moe::kTW * p.G;
+  if (p.TPG > moe::kMaxCTAThreads) return fail(MOE_EUNSUPPORTED, "reduction length %d > 16384", p.K);
+  p.TW = (mode == moe::kGateUp) ? moe::kTWGateUp : moe::kTWDown;
+  // as many row-groups as fit in a CTA whose item still tiles the output
+  p.G = 0;
+  for (int g = moe::kMaxCTAThreads / p.TPG; g >= 1; --g) {
+    const int T = p.TW * g;
+    const bool fits = (mode == moe::kGateUp) ? (T % 2 == 0 && d.inter % (T / 2) == 0)
+                                             : (d.hidden % T == 0);
+    if (fits) {
+      p.G = g;
+      break;
+    }
+  }
+  if (p.G == 0)
+    return fail(MOE_EUNSUPPORTED, "no expert tile divides %s", mode == moe::kGateUp ? "inter" : "hidden");
+  p.T = p.TW * p.G;
   if (mode == moe::kGateUp) {
     p.TJ = p.T / 2;
-    if (d.inter % p.TJ)
-      return fail(MOE_EUNSUPPORTED, "inter %d not a multiple of the gate/up tile %d", d.inter, p.TJ);
     p.tiles = d.inter / p.TJ;
     p.RE = 2 * d.inter;
   } else {
     p.TJ = p.T;
-    if (d.hidden % p.T)
-      return fail(MOE_EUNSUPPORTED, "hidden %d not a multiple of the down tile %d", d.hidden, p.T);
     p.tiles = d.hidden / p.T;
     p.RE = d.hidden;
   }
   p.stage_bytes = (uint32_t)(p.T * (p.KB + p.KS));
   p.stage_stride = (p.stage_bytes + 127u) / 128u * 128u;
-  const size_t ctrl = 16 * 1024;  // upper bound of the control area
+  const size_t ctrl = moe::expert_ctrl_bytes();
   int ns = (int)((moe::kSmemBudget - ctrl) / p.stage_stride);
   if (ns > 16) ns = 16;
   if (ns < 2) return fail(MOE_EUNSUPPORTED, "expert stage of %u bytes too large", p.stage_bytes);

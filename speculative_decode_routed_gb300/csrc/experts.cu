@@ -24,13 +24,21 @@
 //    mbarriers (complete_tx); thread 0 refills a stage as soon as the
 //    per-item barrier shows every thread is done with it, so the copies of
 //    the next NS-1 items (~130-190 KB per SM) are in flight ahead of the math.
-//  - Consumer threads own a fixed 16-byte column chunk (32 elements, two
-//    16-blocks) of every weight row; the expert's activation rows for that
-//    chunk stay in registers as signed bytes (2 x e2m1 value, exact).  A
-//    weight chunk is expanded to signed bytes with byte-permute table
-//    lookups and each 16-block dot product is an exact int32 sum of four
-//    dp4a; the block result is scaled by the exact fp32 product of the two
-//    e4m3 scales and accumulated in fp32.
+//  - Sixteen warps per SM (at most 128 registers a thread).  Each thread
+//    owns a fixed 16-byte column chunk (32 elements, two 16-blocks) of every
+//    weight row; the expert's activation rows for that chunk stay in
+//    registers.  Two exact ways to form a 16-block dot product, chosen per
+//    expert by its number of rows:
+//      1-2 rows: the hardware e2m1x2 -> f16x2 conversion and f16x2 fused
+//        multiply-adds.  e2m1 products are multiples of 1/4 below 36, so
+//        four-term partial sums (< 144) and their pairwise sums (< 288) are
+//        exact in f16, and so is their fp32 total.
+//      3+ rows (groups of 4): byte-permute table lookups turn codes into
+//        signed bytes (2 x value) and four dp4a give the exact int32 sum.
+//    The block result is scaled by the exact fp32 product of the two e4m3
+//    scales and accumulated in fp32.  (Measured on GB300 from shared memory:
+//    ~57 weight elements/cycle/SM for the f16 path at 1 row and 16 warps,
+//    ~39 for dp4a; 29 vs 20 at 4 rows.)
 //  - Partial sums are reduced across the row's threads with a warp
 //    reduce-scatter (one value per lane, not one reduction per value) and a
 //    fixed-order sum across warps: deterministic, no float atomics.
@@ -44,13 +52,16 @@
 namespace moe {
 namespace {
 
-constexpr int kRedFloats = 8 * kTW * kMaxRB;  // one reduction buffer: 8 warps x 64 values
-constexpr int kMaxPairs = 128;                 // pairs of one expert <= rows <= 128
-constexpr int kExpertTable = 64;               // experts of one CTA's run kept in smem
+constexpr int kMaxThreads = 512;
+constexpr int kMaxWarps = kMaxThreads / 32;
+constexpr int kRedFloats = kMaxWarps * 32;   // one reduction buffer: 16 warps x 32 values
+constexpr int kMaxPairs = 128;               // pairs of one expert <= rows <= 128
+constexpr int kExpertTable = 64;             // experts of one CTA's run kept in smem
 constexpr int kCtrlBytes = 512 + kExpertTable * 16 + 2 * kRedFloats * 4 + kMaxPairs * 4 + 64;
+constexpr int kCtrlRounded = (kCtrlBytes + 1023) / 1024 * 1024;
 
-// Shared memory: [barriers + stage metadata | 2 reduction buffers | pair ids
-// of the current expert | flags] then the stage ring.
+// Shared memory: [barriers + stage metadata | expert table | 2 reduction
+// buffers | pair ids of the current expert | flags] then the stage ring.
 struct Smem {
   uint64_t* full;
   int4* meta;       // per stage: expert, tile, first pooled position, pairs
@@ -71,15 +82,16 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.pairs = reinterpret_cast<int*>(base + 512 + kExpertTable * 16 + 2 * kRedFloats * 4);
   s.flag = s.pairs + kMaxPairs;
   s.ok = s.flag + 1;
-  s.stages = base + ((kCtrlBytes + 1023) / 1024) * 1024;
+  s.stages = base + kCtrlRounded;
   return s;
 }
 
-// Reduce-scatter of V values (V a power of two) across the 32 lanes; lane
-// results land in dst[index] (lanes holding the same index write once).
+// Reduce-scatter of V values (V a power of two <= 32) across the 32 lanes;
+// lane results land in dst[index] (lanes holding the same index write once).
 template <int V>
 __device__ __forceinline__ void warp_reduce_scatter_store(float (&v)[V], int lane, float* dst) {
-  constexpr int kSteps = (V >= 32) ? 5 : (V == 16 ? 4 : (V == 8 ? 3 : (V == 4 ? 2 : (V == 2 ? 1 : 0))));
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V: a power of two <= 32");
+  constexpr int kSteps = (V == 32) ? 5 : (V == 16 ? 4 : (V == 8 ? 3 : (V == 4 ? 2 : (V == 2 ? 1 : 0))));
   int base = 0;
 #pragma unroll
   for (int st = 0; st < kSteps; ++st) {
@@ -94,35 +106,55 @@ __device__ __forceinline__ void warp_reduce_scatter_store(float (&v)[V], int lan
     }
     if (upper) base += n / 2;
   }
-  constexpr int kLeft = V >> kSteps;  // values per lane now (1, or V/32)
 #pragma unroll
   for (int st = kSteps; st < 5; ++st) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16 >> st);
   const int low_bits = (1 << (5 - kSteps)) - 1;
-  if ((lane & low_bits) == 0) {
-#pragma unroll
-    for (int i = 0; i < kLeft; ++i) dst[base + i] = v[i];
-  }
+  if ((lane & low_bits) == 0) dst[base] = v[0];
 }
 
-// The expert's activation rows [pos0, pos0 + rb) for this thread's chunk, as
-// signed bytes (2 x e2m1 value) and two fp32 block scales.
-template <int RB>
+// e2m1 pair in the low byte -> f16x2 (exact).
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte_in_low) {
+  uint32_t r;
+  const unsigned short in = static_cast<unsigned short>(byte_in_low);
+  asm("{\n\t.reg .b8 t, z;\n\tmov.b16 {t, z}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "h"(in));
+  return r;
+}
+
+__device__ __forceinline__ void chunk_to_f16(const uint4 c, uint32_t* h) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 16; ++q) h[q] = cvt_e2m1x2_f16x2(w[q >> 2] >> (8 * (q & 3)));
+}
+
+__device__ __forceinline__ void chunk_to_s8(const uint4 c, uint32_t* v) {
+  e2m1x8_to_s8x8(c.x, v[0], v[1]);
+  e2m1x8_to_s8x8(c.y, v[2], v[3]);
+  e2m1x8_to_s8x8(c.z, v[4], v[5]);
+  e2m1x8_to_s8x8(c.w, v[6], v[7]);
+}
+
+// Activation rows [pos0, pos0 + rb) of the expert for this thread's chunk:
+// F16 layout av[a*16 + q] (f16x2 of byte q) or signed-byte layout av[a*8 + q].
+template <int RB, bool kF16>
 __device__ __forceinline__ void load_act(const ExpertParams& p, bool gate_up, int pos0, int rb,
-                                         int cc, bool live, uint32_t (&xa)[kMaxRB][8],
-                                         float (&sx)[kMaxRB][2]) {
+                                         int cc, bool live, uint32_t (&av)[32],
+                                         float (&sx)[4][2]) {
   const Workspace& ws = p.ws;
   const uint8_t* codes = gate_up ? ws.x_codes : ws.h_codes;
   const uint8_t* sf = gate_up ? ws.x_sf : ws.h_sf;
+  constexpr int W = kF16 ? 16 : 8;
 #pragma unroll
   for (int a = 0; a < RB; ++a) {
     if (a < rb && live) {
       const int pos = pos0 + a;
       const int row = gate_up ? __ldcg(ws.pair_order + pos) / p.k : pos;
       const uint4 c = __ldcg(reinterpret_cast<const uint4*>(codes + (size_t)row * p.KB) + cc);
-      e2m1x8_to_s8x8(c.x, xa[a][0], xa[a][1]);
-      e2m1x8_to_s8x8(c.y, xa[a][2], xa[a][3]);
-      e2m1x8_to_s8x8(c.z, xa[a][4], xa[a][5]);
-      e2m1x8_to_s8x8(c.w, xa[a][6], xa[a][7]);
+      if (kF16)
+        chunk_to_f16(c, av + a * W);
+      else
+        chunk_to_s8(c, av + a * W);
       const unsigned short s2 =
           __ldcg(reinterpret_cast<const unsigned short*>(sf + (size_t)row * p.KS) + cc);
       const float2 f = e4m3x2_to_f32x2(s2);
@@ -130,48 +162,75 @@ __device__ __forceinline__ void load_act(const ExpertParams& p, bool gate_up, in
       sx[a][1] = f.y;
     } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) xa[a][q] = 0u;
+      for (int q = 0; q < W; ++q) av[a * W + q] = 0u;
       sx[a][0] = sx[a][1] = 0.0f;
     }
   }
 }
 
-// Dot products of this thread's chunk of the group's kTW weight rows with the
+__device__ __forceinline__ __half2 h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Dot products of this thread's chunk of the group's TW weight rows with the
 // RB activation rows held in registers.
-template <int RB>
+template <int TW, int RB, bool kF16>
 __device__ __forceinline__ void gemv_chunk(const ExpertParams& p, const uint8_t* stage, int g,
-                                           int cc, bool live, const uint32_t (&xa)[kMaxRB][8],
-                                           const float (&sx)[kMaxRB][2],
-                                           float (&acc)[kTW * RB]) {
+                                           int cc, bool live, const uint32_t (&av)[32],
+                                           const float (&sx)[4][2], float (&acc)[TW * RB]) {
 #pragma unroll
-  for (int i = 0; i < kTW * RB; ++i) acc[i] = 0.0f;
+  for (int i = 0; i < TW * RB; ++i) acc[i] = 0.0f;
   if (!live) return;
-  const uint8_t* sc = stage + (size_t)cc * 16 + (size_t)g * kTW * p.KB;
-  const uint8_t* ss = stage + (size_t)p.T * p.KB + (size_t)cc * 2 + (size_t)g * kTW * p.KS;
+  const uint8_t* sc = stage + (size_t)cc * 16 + (size_t)g * TW * p.KB;
+  const uint8_t* ss = stage + (size_t)p.T * p.KB + (size_t)cc * 2 + (size_t)g * TW * p.KS;
 #pragma unroll
-  for (int t = 0; t < kTW; ++t) {
+  for (int t = 0; t < TW; ++t) {
     const uint4 c = *reinterpret_cast<const uint4*>(sc + (size_t)t * p.KB);
     const unsigned short s2 = *reinterpret_cast<const unsigned short*>(ss + (size_t)t * p.KS);
     const float2 sw = e4m3x2_to_f32x2(s2);
-    uint32_t wv[8];
-    e2m1x8_to_s8x8(c.x, wv[0], wv[1]);
-    e2m1x8_to_s8x8(c.y, wv[2], wv[3]);
-    e2m1x8_to_s8x8(c.z, wv[4], wv[5]);
-    e2m1x8_to_s8x8(c.w, wv[6], wv[7]);
+    if (kF16) {
+      uint32_t wh[16];
+      chunk_to_f16(c, wh);
 #pragma unroll
-    for (int a = 0; a < RB; ++a) {
-      int d0 = __dp4a((int)wv[0], (int)xa[a][0], 0);
-      d0 = __dp4a((int)wv[1], (int)xa[a][1], d0);
-      d0 = __dp4a((int)wv[2], (int)xa[a][2], d0);
-      d0 = __dp4a((int)wv[3], (int)xa[a][3], d0);
-      int d1 = __dp4a((int)wv[4], (int)xa[a][4], 0);
-      d1 = __dp4a((int)wv[5], (int)xa[a][5], d1);
-      d1 = __dp4a((int)wv[6], (int)xa[a][6], d1);
-      d1 = __dp4a((int)wv[7], (int)xa[a][7], d1);
-      float acc_v = acc[t * RB + a];
-      acc_v = fmaf((float)d0, sw.x * sx[a][0], acc_v);
-      acc_v = fmaf((float)d1, sw.y * sx[a][1], acc_v);
-      acc[t * RB + a] = acc_v;
+      for (int a = 0; a < RB; ++a) {
+        const uint32_t* x = av + a * 16;
+        // four-term exact partials, then exact pairwise sums per 16-block
+        __half2 pa = __hmul2(h2(wh[0]), h2(x[0]));
+        __half2 pb = __hmul2(h2(wh[4]), h2(x[4]));
+        __half2 pc = __hmul2(h2(wh[8]), h2(x[8]));
+        __half2 pd = __hmul2(h2(wh[12]), h2(x[12]));
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+          pa = __hfma2(h2(wh[q]), h2(x[q]), pa);
+          pb = __hfma2(h2(wh[4 + q]), h2(x[4 + q]), pb);
+          pc = __hfma2(h2(wh[8 + q]), h2(x[8 + q]), pc);
+          pd = __hfma2(h2(wh[12 + q]), h2(x[12 + q]), pd);
+        }
+        const float2 f0 = __half22float2(__hadd2(pa, pb));
+        const float2 f1 = __half22float2(__hadd2(pc, pd));
+        float acc_v = acc[t * RB + a];
+        acc_v = fmaf(f0.x + f0.y, sw.x * sx[a][0], acc_v);
+        acc_v = fmaf(f1.x + f1.y, sw.y * sx[a][1], acc_v);
+        acc[t * RB + a] = acc_v;
+      }
+    } else {
+      uint32_t wv[8];
+      chunk_to_s8(c, wv);
+#pragma unroll
+      for (int a = 0; a < RB; ++a) {
+        const uint32_t* x = av + a * 8;
+        int d0 = __dp4a((int)wv[0], (int)x[0], 0);
+        d0 = __dp4a((int)wv[1], (int)x[1], d0);
+        d0 = __dp4a((int)wv[2], (int)x[2], d0);
+        d0 = __dp4a((int)wv[3], (int)x[3], d0);
+        int d1 = __dp4a((int)wv[4], (int)x[4], 0);
+        d1 = __dp4a((int)wv[5], (int)x[5], d1);
+        d1 = __dp4a((int)wv[6], (int)x[6], d1);
+        d1 = __dp4a((int)wv[7], (int)x[7], d1);
+        float acc_v = acc[t * RB + a];
+        // signed bytes carry 2 x value: the block sum is 4 x sum(w x)
+        acc_v = fmaf((float)d0 * 0.25f, sw.x * sx[a][0], acc_v);
+        acc_v = fmaf((float)d1 * 0.25f, sw.y * sx[a][1], acc_v);
+        acc[t * RB + a] = acc_v;
+      }
     }
   }
 }
@@ -181,18 +240,18 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // One activation-row group (RB rows) of one item: dot products, reduction,
 // epilogue (h for gate/up, o for down).  `red` alternates between the two
 // reduction buffers, so one barrier per group suffices.
-template <int RB, bool kGU>
+template <int TW, int RB, bool kF16, bool kGU>
 __device__ __forceinline__ void run_group(const ExpertParams& p, const Smem& sm, float* red,
                                           const uint8_t* stage, int tile, int pos0, int a0, int rb,
-                                          int tid, int NC, const uint32_t (&xa)[kMaxRB][8],
-                                          const float (&sx)[kMaxRB][2], float sc0, float sc1,
+                                          int tid, int NC, const uint32_t (&av)[32],
+                                          const float (&sx)[4][2], float sc0, float sc1,
                                           float& amax_out) {
   const int g = tid / p.TPG, cc = tid % p.TPG;
   const bool live = cc < p.CH;
   const int lane = tid & 31, warp = tid >> 5;
-  constexpr int V = kTW * RB;
+  constexpr int V = TW * RB;
   float acc[V];
-  gemv_chunk<RB>(p, stage, g, cc, live, xa, sx, acc);
+  gemv_chunk<TW, RB, kF16>(p, stage, g, cc, live, av, sx, acc);
   warp_reduce_scatter_store<V>(acc, lane, red + warp * V);
   named_bar(1, NC);
   const int wpg = p.TPG / 32;
@@ -203,8 +262,8 @@ __device__ __forceinline__ void run_group(const ExpertParams& p, const Smem& sm,
       const int j = q % p.TJ, a = q / p.TJ;
       const int wg = j, wu = p.TJ + j;  // stage rows of gate j and up j
       float G = 0.0f, U = 0.0f;
-      for (int i = 0; i < wpg; ++i) G += red[((wg / kTW) * wpg + i) * V + (wg % kTW) * RB + a];
-      for (int i = 0; i < wpg; ++i) U += red[((wu / kTW) * wpg + i) * V + (wu % kTW) * RB + a];
+      for (int i = 0; i < wpg; ++i) G += red[((wg / TW) * wpg + i) * V + (wg % TW) * RB + a];
+      for (int i = 0; i < wpg; ++i) U += red[((wu / TW) * wpg + i) * V + (wu % TW) * RB + a];
       const float hv = silu(G * sc0) * (U * sc1);
       ws.h[(size_t)(pos0 + a0 + a) * p.I + tile * p.TJ + j] = hv;
       m = fmaxf(m, fabsf(hv));
@@ -214,7 +273,7 @@ __device__ __forceinline__ void run_group(const ExpertParams& p, const Smem& sm,
     for (int q = tid; q < p.T * rb; q += NC) {
       const int w = q % p.T, a = q / p.T;
       float acc_o = 0.0f;
-      for (int i = 0; i < wpg; ++i) acc_o += red[((w / kTW) * wpg + i) * V + (w % kTW) * RB + a];
+      for (int i = 0; i < wpg; ++i) acc_o += red[((w / TW) * wpg + i) * V + (w % TW) * RB + a];
       const int pair = sm.pairs[a0 + a];
       ws.o[(size_t)pair * p.H + tile * p.T + w] = acc_o * sc0;
     }
@@ -323,11 +382,11 @@ __device__ __forceinline__ bool issue_item(const ExpertParams& p, const Smem& sm
   return true;
 }
 
-// One CTA per SM by design (about 200 KB of shared memory), at most 8 warps:
-// two warps per SM sub-partition leave room for up to 224 registers per
-// thread, which keeps the RB = 8 path free of spills.
+// One CTA per SM (about 200 KB of shared memory), up to 16 warps.
+// Gate/up runs 8 weight rows per thread per item, down 4.
 template <bool kGU>
-__global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
+__global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(ExpertParams p) {
+  constexpr int TW = kGU ? 8 : 4;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const Workspace& ws = p.ws;
@@ -379,10 +438,9 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
 
   const int cc = tid % p.TPG;
   const bool live = cc < p.CH;
-  const int lane = tid & 31;
   const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
-  uint32_t xa[kMaxRB][8];
-  float sx[kMaxRB][2];
+  uint32_t av[32];
+  float sx[4][2];
   int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0;
   float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
   int gi = 0;
@@ -414,36 +472,34 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
       cur_tiles = 0;
       cur_amax = 0.0f;
       if (kGU) {
-        sc0 = __ldg(p.gscale + 3 * e + 0) * x_sg * 0.25f;
-        sc1 = __ldg(p.gscale + 3 * e + 1) * x_sg * 0.25f;
+        sc0 = __ldg(p.gscale + 3 * e + 0) * x_sg;
+        sc1 = __ldg(p.gscale + 3 * e + 1) * x_sg;
       } else {
         // (the item barrier above ordered every read of the previous
         // expert's pair ids before these writes)
-        sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e) * 0.25f;
+        sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e);
         for (int q = tid; q < ne; q += NC) sm.pairs[q] = __ldcg(ws.pair_order + pos0 + q);
       }
-      const int rb = min(kMaxRB, ne);
-      if (ne <= kMaxRB) {
-        if (rb == 1) load_act<1>(p, kGU, pos0, rb, cc, live, xa, sx);
-        else if (rb == 2) load_act<2>(p, kGU, pos0, rb, cc, live, xa, sx);
-        else if (rb <= 4) load_act<4>(p, kGU, pos0, rb, cc, live, xa, sx);
-        else load_act<8>(p, kGU, pos0, rb, cc, live, xa, sx);
-      }
+      if (ne == 1) load_act<1, true>(p, kGU, pos0, 1, cc, live, av, sx);
+      else if (ne == 2) load_act<2, true>(p, kGU, pos0, 2, cc, live, av, sx);
+      else if (ne <= 4) load_act<4, false>(p, kGU, pos0, ne, cc, live, av, sx);
     }
     const uint8_t* stage = sm.stages + (size_t)s * p.stage_stride;
-    for (int a0 = 0; a0 < ne; a0 += kMaxRB) {
-      const int rb = min(kMaxRB, ne - a0);
-      float* red = sm.red + (gi & 1) * kRedFloats;
+    float* red = sm.red + (gi & 1) * kRedFloats;
+    if (ne == 1) {
       ++gi;
-      if (ne > kMaxRB) load_act<kMaxRB>(p, kGU, pos0 + a0, rb, cc, live, xa, sx);
-      if (rb == 1)
-        run_group<1, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, xa, sx, sc0, sc1, cur_amax);
-      else if (rb == 2)
-        run_group<2, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, xa, sx, sc0, sc1, cur_amax);
-      else if (rb <= 4)
-        run_group<4, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, xa, sx, sc0, sc1, cur_amax);
-      else
-        run_group<8, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, xa, sx, sc0, sc1, cur_amax);
+      run_group<TW, 1, true, kGU>(p, sm, red, stage, tile, pos0, 0, 1, tid, NC, av, sx, sc0, sc1, cur_amax);
+    } else if (ne == 2) {
+      ++gi;
+      run_group<TW, 2, true, kGU>(p, sm, red, stage, tile, pos0, 0, 2, tid, NC, av, sx, sc0, sc1, cur_amax);
+    } else {
+      for (int a0 = 0; a0 < ne; a0 += 4) {
+        const int rb = min(4, ne - a0);
+        red = sm.red + (gi & 1) * kRedFloats;
+        ++gi;
+        if (ne > 4) load_act<4, false>(p, kGU, pos0 + a0, rb, cc, live, av, sx);
+        run_group<TW, 4, false, kGU>(p, sm, red, stage, tile, pos0, a0, rb, tid, NC, av, sx, sc0, sc1, cur_amax);
+      }
     }
     ++cur_tiles;
   }
@@ -460,8 +516,10 @@ __global__ void __maxnreg__(224) expert_kernel(ExpertParams p) {
 
 }  // namespace
 
+size_t expert_ctrl_bytes() { return (size_t)kCtrlRounded; }
+
 size_t expert_smem_bytes(const ExpertParams& p) {
-  return (size_t)((kCtrlBytes + 1023) / 1024) * 1024 + (size_t)p.NS * p.stage_stride;
+  return (size_t)kCtrlRounded + (size_t)p.NS * p.stage_stride;
 }
 
 cudaError_t expert_set_smem(size_t bytes) {

@@ -93,9 +93,10 @@ struct ExpertParams {
   Workspace ws;
 };
 
-constexpr int kMaxRB = 8;         // activation rows held in registers
-constexpr int kTW = 8;            // weight rows per thread per item
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kTWGateUp = 8;      // weight rows per thread per item (gate/up)
+constexpr int kTWDown = 4;        // weight rows per thread per item (down)
+constexpr int kMaxCTAThreads = 512;
+constexpr int kSmemBudget = 226 * 1024;  // of the 227 KB a CTA may use
 
 // Host-side launchers (one per kernel family).
 cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl);
@@ -105,5 +106,6 @@ cudaError_t launch_quantize(const float* v, int64_t rows, int64_t cols, uint8_t*
                             uint8_t* sf, float* sg, float* amax, cudaStream_t s);
 
 size_t expert_smem_bytes(const ExpertParams& p);
+size_t expert_ctrl_bytes();
 
 }  // namespace moe

@@ -26,6 +26,7 @@ constexpr int kRouterThreads = 256;
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kRouterChunks = 4;   // 8-element chunks per lane per slice: slices <= 1024 wide
 constexpr int kMaxTopK = 16;
+constexpr int kRowBlock = 8;       // rows whose x slice is staged at once
 
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -54,13 +55,30 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
   for (int r = warp; r < rows; r += kRouterWarps) {
     float* l = lg + warp * E;
     float m = -INFINITY;
-    for (int e = lane; e < E; e += 32) {
-      float v = 0.0f;
-      for (int s = 0; s < p.S; ++s) v += __ldcg(ws.logit_part + ((size_t)s * rows + r) * E + e);
-      if (p.bias) v += __ldg(p.bias + e);
-      l[e] = v;
-      ws.logits[(size_t)r * E + e] = v;
-      m = fmaxf(m, v);
+    // the lane's experts e = lane + 32 i, in groups of 8 so that the loads of
+    // a slice are all in flight together; slices are summed in order
+    for (int i0 = 0; i0 * 32 < E; i0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      for (int s = 0; s < p.S; ++s) {
+        const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane + 32 * (i0 + i);
+          if (e < E) v[i] += __ldcg(src + e);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * (i0 + i);
+        if (e < E) {
+          const float vb = p.bias ? v[i] + __ldg(p.bias + e) : v[i];
+          l[e] = vb;
+          ws.logits[(size_t)r * E + e] = vb;
+          m = fmaxf(m, vb);
+        }
+      }
     }
     m = warp_max(m);
     float z = 0.0f;
@@ -204,21 +222,44 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   grid_dep_wait();
   grid_dep_launch();
 
-  if (warp < p.EG && e < p.E) {
-    for (int r = 0; r < p.rows; ++r) {
-      float acc = 0.0f;
+  // rows in blocks of kRowBlock: the block's x slice is staged in shared
+  // memory with every load in flight at once, then each warp forms its
+  // expert's kRowBlock partial dot products from registers and smem
+  uint4* xs = reinterpret_cast<uint4*>(smem);  // [kRowBlock][kRouterChunks * 32]
+  const int nc = c1 - c0;
+  for (int r0 = 0; r0 < p.rows; r0 += kRowBlock) {
+    const int nr = min(kRowBlock, p.rows - r0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr * nc; i += kRouterThreads) {
+      const int rr = i / nc, c = i % nc;
+      xs[rr * (kRouterChunks * 32) + c] =
+          __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)(r0 + rr) * p.H) + c0 + c);
+    }
+    __syncthreads();
+    if (warp < p.EG && e < p.E) {
+      float acc[kRowBlock];
 #pragma unroll
-      for (int i = 0; i < kRouterChunks; ++i) {
-        const int c = c0 + lane + 32 * i;
-        if (c < c1) {
-          const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)r * p.H) + c);
-          acc = dot8_bf16(xv, wv[i], acc);
+      for (int rr = 0; rr < kRowBlock; ++rr) {
+        acc[rr] = 0.0f;
+        if (rr < nr) {
+#pragma unroll
+          for (int i = 0; i < kRouterChunks; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nc) acc[rr] = dot8_bf16(xs[rr * (kRouterChunks * 32) + c], wv[i], acc[rr]);
+          }
         }
       }
-      acc = warp_sum(acc);
-      if (lane == 0) ws.logit_part[((size_t)sl * p.rows + r) * p.E + e] = acc;
+#pragma unroll
+      for (int rr = 0; rr < kRowBlock; ++rr) acc[rr] = warp_sum(acc[rr]);
+      if (lane < nr) {
+        float v = acc[0];
+#pragma unroll
+        for (int rr = 1; rr < kRowBlock; ++rr) v = (lane == rr) ? acc[rr] : v;
+        ws.logit_part[((size_t)sl * p.rows + r0 + lane) * p.E + e] = v;
+      }
     }
   }
+  __syncthreads();
 
   // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks
   const int ncta = gridDim.x * gridDim.y;
@@ -264,7 +305,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 
 size_t router_smem_bytes(int E, int rows) {
   const int RW = (rows + 31) / 32;
-  return (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 + (size_t)E * RW * 4;
+  const size_t route = (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 +
+                       (size_t)E * RW * 4;
+  const size_t xslice = (size_t)kRowBlock * kRouterChunks * 32 * 16;
+  return route > xslice ? route : xslice;
 }
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {

@@ -112,13 +112,17 @@ def _check_weights(dec, ow, layer, experts):
 
 def staged_layer(w, dec, ow, layer, rows, branch, stream, experts="all", prev=None):
     """Run one layer on the GPU and check every stage.  branch: bf16 CUDA tensor,
-    or None (chained: the previous layer's unpooled output, from `prev`)."""
+    or None (chained: the previous layer's unpooled output, from `prev`).
+    `ow` is oracle.LayerWeights, or a function of the GPU's debug data that
+    returns (LayerWeights, experts to check) -- for sampling at full size."""
     k, E, I = w.top_k, w.n_experts, w.inter
     s_in = stream.cpu().numpy().copy()
     dec.layer(layer, rows, branch, stream)
     torch.cuda.synchronize()
     dec.check()
     d = read_debug(dec, rows)
+    if callable(ow):
+        ow, experts = ow(d)
 
     # A: dual-norm boundary
     if branch is not None:
@@ -304,15 +308,12 @@ def _sample_experts(d, n_extra=2, seed=0):
 def _staged_full(w, dec, layer, rows, branch, stream, n_extra=2, prev=None):
     """Staged check at full size: routing / pooler / act quant for every row,
     experts on a sample (weights quantized by the oracle only for those)."""
-    s_before = stream.clone()
-    dec.layer(layer, rows, branch, stream)
-    torch.cuda.synchronize()
-    d0 = read_debug(dec, rows)
-    sample = _sample_experts(d0, n_extra, seed=layer)
-    ow = oracle_weights(w, layer, experts=sample)
-    _check_weights(dec, ow, layer, sample)
-    stream.copy_(s_before)
-    return staged_layer(w, dec, ow, layer, rows, branch, stream, experts=sample, prev=prev)
+    def pick(d):
+        sample = _sample_experts(d, n_extra, seed=layer)
+        ow = oracle_weights(w, layer, experts=sample)
+        _check_weights(dec, ow, layer, sample)
+        return ow, sample
+    return staged_layer(w, dec, pick, layer, rows, branch, stream, prev=prev)
 
 
 @pytest.mark.slow
