@@ -269,8 +269,8 @@ def run_native(args, w):
     na = float(np.mean(n_active))
     byt = _algorithmic_bytes(w, int(round(na)), rows)
     peak, peak_kind = _peaks()
-    gu_gbs = byt["gate_up"] / (k_ms[2] * 1e-3) / 1e9
-    dn_gbs = byt["down"] / (k_ms[3] * 1e-3) / 1e9
+    gu_gbs = byt["gate_up"] / (k_ms[3] * 1e-3) / 1e9
+    dn_gbs = byt["down"] / (k_ms[4] * 1e-3) / 1e9
     step_gbs = byt["total"] * w.n_layers / (ms * 1e-3) / 1e9 * ws
 
     # end to end through the host-buffer entry point
@@ -307,11 +307,11 @@ def run_native(args, w):
         "roofline": {"kernel": "experts gate/up", "bound": "hbm", "achieved": round(gu_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(gu_gbs / peak, 4),
                      "traffic": None, "peak_kind": peak_kind,
-                     "launch_us": round(k_ms[2] * 1000, 2),
+                     "launch_us": round(k_ms[3] * 1000, 2),
                      "algorithmic_bytes": int(byt["gate_up"])},
         "kernels_us": {"boundary": round(k_ms[0] * 1000, 2), "router": round(k_ms[1] * 1000, 2),
-                       "gate_up": round(k_ms[2] * 1000, 2), "down": round(k_ms[3] * 1000, 2),
-                       "down_gbs": round(dn_gbs, 1)},
+                       "pool": round(k_ms[2] * 1000, 2), "gate_up": round(k_ms[3] * 1000, 2),
+                       "down": round(k_ms[4] * 1000, 2), "down_gbs": round(dn_gbs, 1)},
         "e2e": {"value": round(e2e_ms * 1000.0 / w.n_layers, 2), "unit": UNIT,
                 "h2d_bytes_per_step": rows * w.hidden * (2 + 4),
                 "d2h_bytes_per_step": rows * w.hidden * (4 + 2)},

@@ -148,8 +148,8 @@ def moe_decode_step_host(h, rows, branch_host, stream_host, out_host, stream=Non
 
 
 def moe_decode_layer_profile(h, layer, rows, branch, stream_buf, stream=None):
-    """-> [boundary, router, gate/up, down] kernel durations in ms."""
-    ms = (ctypes.c_float * 4)()
+    """-> [boundary, router, pool, gate/up, down] kernel durations in ms."""
+    ms = (ctypes.c_float * 5)()
     _check(_lib().moe_decode_layer_profile(h, layer, rows, _ptr(branch), _ptr(stream_buf),
                                            _stream(stream), ms), "moe_decode_layer_profile")
     return list(ms)

@@ -15,8 +15,20 @@
 #include <string>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/moe_decode.h"
 #include "moe_decode_internal.h"
+#include "tc_internal.h"
+
+// The expert path is chosen when the library is built: the tcgen05
+// block-scaled tensor-core kernels by default, the CUDA-core kernels with
+// -DMOE_EXPERT_FMA (kept for measurement against each other).
+#ifndef MOE_EXPERT_FMA
+#define MOE_EXPERT_TC 1
+#else
+#define MOE_EXPERT_TC 0
+#endif
 
 namespace moe {
 size_t router_smem_bytes(int E, int rows);
@@ -72,6 +84,11 @@ struct moe_decode_s {
   uint16_t* io_branch = nullptr;
   float* io_stream = nullptr;
   uint16_t* io_out = nullptr;
+  // tensor-core path
+  moe::TcParams tgu{}, tdn{};
+  std::vector<CUtensorMap> tm_w13, tm_w2;
+  std::vector<uint8_t*> sfa13, sfa2;   // weight scale atoms per layer (library-owned)
+  CUtensorMap tm_xpool{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
 };
 
 namespace {
@@ -125,6 +142,97 @@ int plan_experts(moe::ExpertParams& p, int mode, const moe_decode_dims& d) {
   return MOE_OK;
 }
 
+// Tile plan of the tensor-core path (see experts_tc.cu).
+int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
+  p = moe::TcParams{};
+  const bool gu = (mode == moe::kGateUp);
+  p.mode = mode;
+  p.H = d.hidden;
+  p.I = d.inter;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.K = gu ? d.hidden : d.inter;
+  p.KBLK = (p.K + 255) / 256;
+  p.tiles = gu ? d.inter / 128 : d.hidden / 128;
+  p.RE = gu ? 2 * d.inter : d.hidden;
+  p.row_tiles = p.RE / 128;
+  const int maxn = d.max_rows < 128 ? d.max_rows : 128;
+  p.nt_max = (maxn + 31) / 32;
+  p.a_bytes = gu ? 32768u : 16384u;
+  p.sfa_bytes = gu ? 4096u : 2048u;
+  p.off_b = p.a_bytes;
+  p.off_sfa = p.off_b + 4096u * (uint32_t)p.nt_max;
+  p.off_sfb = p.off_sfa + p.sfa_bytes;
+  const uint32_t stage = p.off_sfb + 2048u * (uint32_t)p.nt_max;
+  p.stage_stride = (stage + 1023u) / 1024u * 1024u;
+  const int ns_smem = (int)((227 * 1024 - 1024 - moe::tc_ctrl_bytes()) / p.stage_stride);
+  const uint32_t acc_cols = (gu ? 64u : 32u) * (uint32_t)p.nt_max;
+  p.sf_slot = (gu ? 32u : 16u) + 16u * (uint32_t)p.nt_max;
+  int ns = 0;
+  for (int dbl = 1; dbl >= 0; --dbl) {
+    const uint32_t dcols = (dbl ? 2u : 1u) * acc_cols;
+    const int ns_tmem = dcols < 512u ? (int)((512u - dcols) / p.sf_slot) : 0;
+    ns = ns_smem < ns_tmem ? ns_smem : ns_tmem;
+    if (ns > 8) ns = 8;
+    if (ns >= 3 || (dbl == 0 && ns >= 2)) {
+      p.d_double = dbl;
+      p.tm_d = 0;
+      p.tm_sf = dcols;
+      break;
+    }
+    ns = 0;
+  }
+  if (ns < 2) return fail(MOE_EUNSUPPORTED, "tensor-core plan does not fit (max_rows %d)", d.max_rows);
+  p.NS = ns;
+  p.ws_pairs = d.max_rows * d.top_k;
+  return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major bytes [rows][inner]: boxes of 128 bytes x box_rows, 128B swizzle.
+int encode_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "tensor map encode failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+// Scale lines [groups][rows][16 B]: boxes of 16 B x 32 rows x 4 groups.
+int encode_lines(CUtensorMap* m, const void* base, uint64_t rows, uint64_t groups) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {16, rows, groups};
+  const cuuint64_t strides[2] = {16, rows * 16};
+  const cuuint32_t box[3] = {16, 32, 4};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "tensor map encode failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 int check_layer(const moe_layer_weights& w, int i) {
   if (!w.w_post || !w.w_pre || !w.router_w || !w.w13 || !w.w13_sf || !w.w2 || !w.w2_sf ||
       !w.w_gscale)
@@ -170,6 +278,9 @@ size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims
   ws.h_sf = carve<uint8_t>(cur, R * k * I / 16);
   ws.done = carve<unsigned>(cur, E);
   ws.o = carve<float>(cur, R * k * H);
+  ws.x_pool = carve<uint8_t>(cur, R * k * H / 2);
+  ws.x_lines = carve<uint8_t>(cur, R * k * (H / 64) * 16);
+  ws.h_lines = carve<uint8_t>(cur, R * k * (I / 64) * 16);
   ws.counters = carve<unsigned>(cur, 4);
   ws.err = carve<unsigned>(cur, 1);
   return (size_t)(cur - base);
@@ -224,6 +335,35 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   mark(2);
 
+#if MOE_EXPERT_TC
+  moe::PoolParams pp{};
+  pp.H = d.hidden;
+  pp.k = d.top_k;
+  pp.rows = rows;
+  pp.ws_pairs = d.max_rows * d.top_k;
+  pp.ws = h->ws;
+  e = moe::launch_pool_gather(pp, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+  mark(3);
+
+  moe::TcParams tg = h->tgu;
+  tg.sfa = h->sfa13[layer];
+  tg.gscale = w.w_gscale;
+  tg.ws = h->ws;
+  e = moe::launch_tc_experts(tg, h->tm_w13[layer], h->tm_xpool, h->tm_xlines, h->num_sms, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
+  mark(4);
+
+  moe::TcParams td = h->tdn;
+  td.sfa = h->sfa2[layer];
+  td.gscale = w.w_gscale;
+  td.ws = h->ws;
+  e = moe::launch_tc_experts(td, h->tm_w2[layer], h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  mark(5);
+  return MOE_OK;
+#else
+  mark(3);
   moe::ExpertParams gu = h->gu;
   gu.w = w.w13;
   gu.w_sf = w.w13_sf;
@@ -231,7 +371,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   gu.ws = h->ws;
   e = moe::launch_experts(gu, h->num_sms, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
-  mark(3);
+  mark(4);
 
   moe::ExpertParams dn = h->dn;
   dn.w = w.w2;
@@ -240,8 +380,9 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   dn.ws = h->ws;
   e = moe::launch_experts(dn, h->num_sms, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
-  mark(4);
+  mark(5);
   return MOE_OK;
+#endif
 }
 
 int launch_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, cudaStream_t s) {
@@ -361,11 +502,19 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
   h->S = (d.hidden / 8 + 127) / 128;
   int rc = plan_experts(h->gu, moe::kGateUp, d);
   if (!rc) rc = plan_experts(h->dn, moe::kDown, d);
+#if MOE_EXPERT_TC
+  if (!rc) rc = plan_tc(h->tgu, moe::kGateUp, d);
+  if (!rc) rc = plan_tc(h->tdn, moe::kDown, d);
+#endif
   if (rc) {
     delete h;
     return rc;
   }
+#if MOE_EXPERT_TC
+  e = moe::tc_set_smem(std::max(moe::tc_smem_bytes(h->tgu), moe::tc_smem_bytes(h->tdn)));
+#else
   e = moe::expert_set_smem(std::max(moe::expert_smem_bytes(h->gu), moe::expert_smem_bytes(h->dn)));
+#endif
   if (e == cudaSuccess) e = moe::router_set_smem(moe::router_smem_bytes(d.n_experts, d.max_rows));
   if (e != cudaSuccess) {
     delete h;
@@ -392,6 +541,39 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     moe_decode_destroy(h);
     return cuda_fail(e, "workspace setup");
   }
+#if MOE_EXPERT_TC
+  {
+    const uint64_t R = (uint64_t)d.max_rows * d.top_k;
+    const uint64_t H = d.hidden, I = d.inter, E = d.n_experts;
+    rc = encode_rows(&h->tm_xpool, h->ws.x_pool, H / 2, R, 32);
+    if (!rc) rc = encode_lines(&h->tm_xlines, h->ws.x_lines, R, H / 64);
+    if (!rc) rc = encode_rows(&h->tm_hcodes, h->ws.h_codes, I / 2, R, 32);
+    if (!rc) rc = encode_lines(&h->tm_hlines, h->ws.h_lines, R, I / 64);
+    h->tm_w13.resize(d.n_layers);
+    h->tm_w2.resize(d.n_layers);
+    h->sfa13.assign(d.n_layers, nullptr);
+    h->sfa2.assign(d.n_layers, nullptr);
+    for (int l = 0; l < d.n_layers && !rc; ++l) {
+      rc = encode_rows(&h->tm_w13[l], layers[l].w13, H / 2, E * 2 * I, 128);
+      if (!rc) rc = encode_rows(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128);
+      const size_t b13 = (size_t)E * h->tgu.row_tiles * h->tgu.KBLK * 2048;
+      const size_t b2 = (size_t)E * h->tdn.row_tiles * h->tdn.KBLK * 2048;
+      if (!rc && cudaMalloc(&h->sfa13[l], b13) != cudaSuccess) rc = fail(MOE_ENOMEM, "scale atoms");
+      if (!rc && cudaMalloc(&h->sfa2[l], b2) != cudaSuccess) rc = fail(MOE_ENOMEM, "scale atoms");
+      if (!rc && moe::launch_sf_atoms(layers[l].w13_sf, (int64_t)E * 2 * I, (int)(H / 16),
+                                      h->tgu.KBLK, h->sfa13[l], nullptr) != cudaSuccess)
+        rc = fail(MOE_ECUDA, "scale atoms launch");
+      if (!rc && moe::launch_sf_atoms(layers[l].w2_sf, (int64_t)E * H, (int)(I / 16), h->tdn.KBLK,
+                                      h->sfa2[l], nullptr) != cudaSuccess)
+        rc = fail(MOE_ECUDA, "scale atoms launch");
+    }
+    if (!rc && cudaDeviceSynchronize() != cudaSuccess) rc = fail(MOE_ECUDA, "scale atoms");
+    if (rc) {
+      moe_decode_destroy(h);
+      return rc;
+    }
+  }
+#endif
   *out = h;
   return MOE_OK;
 }
@@ -485,16 +667,16 @@ int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_
   if (rc) return rc;
   if (!stream || !aligned(stream, 16)) return fail(MOE_EINVAL, "stream must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  cudaEvent_t ev[5] = {};
+  cudaEvent_t ev[6] = {};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
   if (e == cudaSuccess) {
     rc = launch_layer(h, layer, rows, branch, stream, s, ev);
-    if (!rc) e = cudaEventSynchronize(ev[4]);
-    for (int i = 0; i < 4 && !rc && e == cudaSuccess; ++i)
+    if (!rc) e = cudaEventSynchronize(ev[5]);
+    for (int i = 0; i < 5 && !rc && e == cudaSuccess; ++i)
       e = cudaEventElapsedTime(&kernel_ms_host[i], ev[i], ev[i + 1]);
   }
-  for (int i = 0; i < 5; ++i)
+  for (int i = 0; i < 6; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);
   if (rc) return rc;
   if (e != cudaSuccess) return cuda_fail(e, "profile events");
@@ -544,7 +726,7 @@ int moe_decode_last_error(moe_decode_t* h) {
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
 
 int moe_decode_step_kernel_count(const moe_decode_t* h) {
-  return h ? 4 * h->d.n_layers + 1 : 0;
+  return h ? (MOE_EXPERT_TC ? 5 : 4) * h->d.n_layers + 1 : 0;
 }
 
 void moe_decode_destroy(moe_decode_t* h) {
@@ -555,6 +737,8 @@ void moe_decode_destroy(moe_decode_t* h) {
   cudaFree(h->io_stream);
   cudaFree(h->io_out);
   cudaFree(h->ws_mem);
+  for (uint8_t* p : h->sfa13) cudaFree(p);
+  for (uint8_t* p : h->sfa2) cudaFree(p);
   delete h;
 }
 

@@ -40,6 +40,9 @@ struct Workspace {
   uint8_t* h_sf;         // [R*k][I/16]
   unsigned* done;        // [E]         finished gate/up tiles per expert
   float* o;              // [R*k][H]    expert outputs, pair-id order
+  uint8_t* x_pool;       // [R*k][H/2]  MoE input codes in pooled order (tensor-core B operand)
+  uint8_t* x_lines;      // [H/64][R*k][16]  its scales, one 16-byte line per row and MMA of 64
+  uint8_t* h_lines;      // [I/64][R*k][16]  the same lines for h
   unsigned* counters;    // [4]         [0] router CTA arrivals
   unsigned* err;         // [1]         latched DeviceError
 };

@@ -1,0 +1,46 @@
+// Internal interfaces of the tensor-core (tcgen05) expert path.
+#pragma once
+#include <cuda.h>
+
+#include "moe_decode_internal.h"
+
+namespace moe {
+
+struct TcParams {
+  int mode;                 // kGateUp or kDown
+  int H, I, E, k;
+  int K;                    // reduction length (H or I)
+  int KBLK;                 // 256-wide K-blocks (the last may be half: zero filled)
+  int tiles;                // 128-row output tiles per expert (I/128 or H/128)
+  int RE;                   // weight rows per expert (2I or H)
+  int row_tiles;            // RE / 128
+  int nt_max;               // 32-row activation tiles per MMA group (max pairs / 32)
+  int NS;                   // pipeline stages
+  int d_double;             // accumulators double buffered in TMEM
+  uint32_t stage_stride;    // bytes per stage (multiple of 1024)
+  uint32_t a_bytes;         // weight tile bytes per stage (16 or 32 KB)
+  uint32_t sfa_bytes;       // weight scale atoms per stage (2 or 4 KB)
+  uint32_t off_sfa, off_b, off_sfb;  // offsets within a stage
+  uint32_t tm_d, tm_sf, sf_slot;     // TMEM column plan
+  int ws_pairs;             // rows * k of the workspace
+  const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
+  const float* gscale;      // [E][3]
+  Workspace ws;
+};
+
+struct PoolParams {
+  int H, k, rows;
+  int ws_pairs;             // rows * k of the workspace (line stride)
+  Workspace ws;
+};
+
+cudaError_t launch_tc_experts(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b,
+                              const CUtensorMap& sfb, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_pool_gather(const PoolParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_sf_atoms(const uint8_t* sf, int64_t rows, int ks, int kblk, uint8_t* out,
+                            cudaStream_t s);
+cudaError_t tc_set_smem(size_t bytes);
+size_t tc_smem_bytes(const TcParams& p);
+size_t tc_ctrl_bytes();
+
+}  // namespace moe
