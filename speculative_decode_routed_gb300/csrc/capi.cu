@@ -165,25 +165,34 @@ int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
   p.off_sfb = p.off_sfa + p.sfa_bytes;
   const uint32_t stage = p.off_sfb + 2048u * (uint32_t)p.nt_max;
   p.stage_stride = (stage + 1023u) / 1024u * 1024u;
-  const int ns_smem = (int)((227 * 1024 - 1024 - moe::tc_ctrl_bytes()) / p.stage_stride);
-  const uint32_t acc_cols = (gu ? 64u : 32u) * (uint32_t)p.nt_max;
-  p.sf_slot = (gu ? 32u : 16u) + 16u * (uint32_t)p.nt_max;
-  int ns = 0;
-  for (int dbl = 1; dbl >= 0; --dbl) {
-    const uint32_t dcols = (dbl ? 2u : 1u) * acc_cols;
-    const int ns_tmem = dcols < 512u ? (int)((512u - dcols) / p.sf_slot) : 0;
-    ns = ns_smem < ns_tmem ? ns_smem : ns_tmem;
-    if (ns > 8) ns = 8;
-    if (ns >= 3 || (dbl == 0 && ns >= 2)) {
-      p.d_double = dbl;
-      p.tm_d = 0;
-      p.tm_sf = dcols;
-      break;
-    }
-    ns = 0;
-  }
-  if (ns < 2) return fail(MOE_EUNSUPPORTED, "tensor-core plan does not fit (max_rows %d)", d.max_rows);
+  int ns = (int)((227 * 1024 - 1024 - moe::tc_ctrl_bytes()) / p.stage_stride);
+  if (ns > 8) ns = 8;
+  if (ns < 2) return fail(MOE_EUNSUPPORTED, "tensor-core stage too large (max_rows %d)", d.max_rows);
   p.NS = ns;
+  // TMEM (512 columns): as many independent MMA issuers as fit, each with its
+  // own accumulators and scale slots (issue latency, not the tensor core,
+  // bounds one issuer; issuers overlap).
+  p.T = gu ? 2 : 1;
+  p.acc_cols = 32u * (uint32_t)p.nt_max;
+  p.sf_cols = 16u + 16u * (uint32_t)p.nt_max;
+  p.P = 0;
+  const int qs_gu[2] = {2, 1}, qs_dn[3] = {4, 2, 1};
+  const int* qs = gu ? qs_gu : qs_dn;
+  const int nq = gu ? 2 : 3;
+  const int modes[3][2] = {{2, 2}, {1, 2}, {1, 1}};
+  for (int qi = 0; qi < nq && !p.P; ++qi)
+    for (int mi = 0; mi < 3 && !p.P; ++mi) {
+      const uint32_t cols = (uint32_t)modes[mi][0] * p.acc_cols + (uint32_t)modes[mi][1] * p.sf_cols;
+      const int P = p.T * qs[qi];
+      if ((uint32_t)P * cols <= 512u) {
+        p.Q = qs[qi];
+        p.P = P;
+        p.dbuf = modes[mi][0];
+        p.sfslots = modes[mi][1];
+        p.issuer_cols = cols;
+      }
+    }
+  if (!p.P) return fail(MOE_EUNSUPPORTED, "tensor-core plan does not fit TMEM (max_rows %d)", d.max_rows);
   p.ws_pairs = d.max_rows * d.top_k;
   return MOE_OK;
 }

@@ -31,7 +31,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTcThreads = 192;           // producer, MMA, 4 epilogue warps
+constexpr int kTcMaxThreads = 32 * (1 + 4 + 4);  // producer, up to 4 MMA issuers, 4 epilogue warps
 constexpr int kEpiThreads = 128;
 constexpr int kExpertTableTc = 64;
 constexpr int kMaxPairsTc = 128;
@@ -134,16 +134,27 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------ shared memory
 
 struct TcSmem {
-  uint64_t* full;       // [NS]  TMA bytes landed
-  uint64_t* empty;      // [NS]  MMAs reading the stage done
-  uint64_t* acc_full;   // [2]   accumulator ready for the epilogue
-  uint64_t* acc_empty;  // [2]   epilogue done reading the accumulator
-  uint64_t* drain;      // [1]   every MMA of this CTA done
+  uint64_t* full;       // [NS]      TMA bytes landed
+  uint64_t* empty;      // [NS]      every issuer that reads the stage is done (T arrivals)
+  uint64_t* acc_full;   // [2]       accumulators ready for the epilogue (P arrivals)
+  uint64_t* acc_empty;  // [2]       epilogue done reading them (4 arrivals)
+  uint64_t* slot_free;  // [4][2]    an issuer's scale slot may be overwritten
+  uint64_t* drain;      // [4]       every MMA of an issuer done
   int4* etab;           // [kExpertTableTc]
   int* pairs;           // [kMaxPairsTc]
   int* flag;
@@ -157,7 +168,8 @@ __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
   s.empty = s.full + 16;
   s.acc_full = s.empty + 16;
   s.acc_empty = s.acc_full + 2;
-  s.drain = s.acc_empty + 2;
+  s.slot_free = s.acc_empty + 2;
+  s.drain = s.slot_free + 8;
   s.etab = reinterpret_cast<int4*>(base + 512);
   s.pairs = reinterpret_cast<int*>(base + 512 + kExpertTableTc * 16);
   s.flag = s.pairs + kMaxPairsTc;
@@ -227,9 +239,11 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
 }  // namespace
 
 // ======================================================================
-// The expert kernel.
+// The expert kernel.  Warp 0: TMA producer.  Warps 1..P: MMA issuers (issuer
+// i = type ty * Q + phase q: accumulator type ty -- gate or up -- and the
+// K-blocks kb = q mod Q).  Warps P+1..P+4: epilogue.
 template <bool kGU>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcMaxThreads, 1)
     tc_expert_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_sfb) {
@@ -241,17 +255,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const TcSmem sm = tc_carve(smem_base);
   const Workspace& ws = p.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = p.P;
 
   if (tid == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], p.T);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_full[b], P);
       mbar_init(&sm.acc_empty[b], kEpiThreads / 32);
     }
-    mbar_init(sm.drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&sm.slot_free[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&sm.drain[i], 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int it1 = (int)((long long)(blockIdx.x + 1) * n_items / gridDim.x);
   const int ai_first = it1 > it0 ? it0 / p.tiles : 0;
   const int nai = it1 > it0 ? (it1 - 1) / p.tiles - ai_first + 1 : 0;
-  for (int q = tid; q < nai && q < kExpertTableTc; q += kTcThreads) {
+  for (int q = tid; q < nai && q < kExpertTableTc; q += blockDim.x) {
     const int e = __ldcg(ws.active + ai_first + q);
     const bool ok = e >= 0 && e < p.E;
     const int pos0 = ok ? __ldcg(ws.offset + e) : 0;
@@ -286,20 +302,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (!na_ok && tid == 0) latch_error(ws.err, kDevBadRouting);
 
   const int KB = p.KBLK;
-  const uint32_t acc_cols = (kGU ? 64u : 32u) * (uint32_t)p.nt_max;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int g = 0;  // global stage counter
+      int g = 0;  // global stage counter = item * KB + kb
       bool ok = true;
       bool waited = kGU;
       for (int it = it0; it < it1 && ok; ++it) {
         const int4 et = tc_item_expert(p, sm, it, ai_first);
         if (!tc_item_ok(p, et)) {
           latch_error(ws.err, kDevBadRouting);
-          ok = false;
           break;
         }
         const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
@@ -314,10 +328,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
           const uint32_t bytes = p.a_bytes + p.sfa_bytes + (uint32_t)nt * (4096u + 2048u);
           mbar_arrive_expect_tx(&sm.full[s], bytes);
-          const int rt = tile;  // gate rows (gate/up) or output rows (down)
-          tma_2d(st, &tm_a, kb * 128, e * p.RE + rt * 128, &sm.full[s], pol);
-          bulk_g2s_plain(st + p.off_sfa, p.sfa + (((size_t)e * p.row_tiles + rt) * KB + kb) * 2048u,
-                         2048u, &sm.full[s]);
+          // gate rows (gate/up) or output rows (down) of this tile
+          tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, &sm.full[s], pol);
+          bulk_g2s_plain(st + p.off_sfa,
+                         p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, 2048u,
+                         &sm.full[s]);
           if (kGU) {
             const int ru = p.I / 128 + tile;  // up rows follow the gate rows
             tma_2d(st + 16384, &tm_a, kb * 128, e * p.RE + ru * 128, &sm.full[s], pol);
@@ -346,67 +361,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(&sm.full[s], (last / p.NS) & 1)) latch_error(ws.err, kDevWaitTimeout);
       }
     }
-  } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer
+  } else if (warp <= P) {
+    // --------------------------------------------------------- MMA issuers
     if (!kGU) {
       grid_dep_wait();
       grid_dep_launch();
     }
+    const int i = warp - 1;
+    const int ty = i / p.Q, q = i % p.Q;
     if (lane == 0) {
-      int g = 0, item = 0;
+      const uint32_t ibase = tmem + (uint32_t)i * p.issuer_cols;
+      int c = 0, item = 0;  // stages handled, items seen
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it, ++item) {
         const int4 et = tc_item_expert(p, sm, it, ai_first);
         if (!tc_item_ok(p, et)) break;
         const int nt = (et.z + 31) / 32;
-        const int ab = p.d_double ? (item & 1) : 0;
-        const int use = p.d_double ? (item >> 1) : item;  // uses of this accumulator so far
+        const int ab = (p.dbuf == 2) ? (item & 1) : 0;
+        const int use = (p.dbuf == 2) ? (item >> 1) : item;
         if (use >= 1 && !mbar_wait(&sm.acc_empty[ab], (use - 1) & 1)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
         }
         tc_fence_after();
-        const uint32_t dcol = tmem + p.tm_d + (uint32_t)ab * acc_cols;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+        const uint32_t dcol = ibase + (uint32_t)ab * p.acc_cols;
+        bool first = true;
+        for (int kb = q; kb < KB; kb += p.Q, ++c) {
+          const int g = item * KB + kb;
           const int s = g % p.NS;
           if (!mbar_wait(&sm.full[s], (g / p.NS) & 1)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;
           }
+          const int slot = c % p.sfslots;
+          if (c >= p.sfslots &&
+              !mbar_wait(&sm.slot_free[i * 2 + slot], ((c / p.sfslots) - 1) & 1)) {
+            latch_error(ws.err, kDevWaitTimeout);
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
-          const uint32_t sf = tmem + p.tm_sf + (uint32_t)s * p.sf_slot;
-          // scales into TMEM: A (gate, up) then B per N-tile, 4 columns per MMA
+          const uint32_t sf = ibase + (uint32_t)p.dbuf * p.acc_cols + (uint32_t)slot * p.sf_cols;
+          // scales into TMEM, 4 columns per MMA: A (this issuer's weight tile)
+          // at sf, B per N-tile at sf + 16 + 16 t
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            tc_cp_sf(sf + 4 * k, st + p.off_sfa + k * 512);
-            if (kGU) tc_cp_sf(sf + 16 + 4 * k, st + p.off_sfa + 2048 + k * 512);
-          }
-          const uint32_t sfb0 = sf + (kGU ? 32u : 16u);
+          for (int k = 0; k < 4; ++k) tc_cp_sf(sf + 4 * k, st + p.off_sfa + ty * 2048 + k * 512);
           for (int t = 0; t < nt; ++t)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) tc_cp_sf(sfb0 + 16 * t + 4 * k, st + p.off_sfb + t * 2048 + k * 512);
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + p.off_b);
+            for (int k = 0; k < 4; ++k)
+              tc_cp_sf(sf + 16 + 16 * t + 4 * k, st + p.off_sfb + t * 2048 + k * 512);
+          const uint32_t a0 = smem_u32(st) + (uint32_t)ty * 16384u, b0 = smem_u32(st + p.off_b);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const bool acc = (kb > 0) || (k > 0);
-            for (int t = 0; t < nt; ++t) {
-              const uint64_t bd = smem_desc(b0 + t * 4096 + 32 * k, 16, 1024, 2);
-              tc_mma(dcol + 32 * t, smem_desc(a0 + 32 * k, 16, 1024, 2), bd, sf + 4 * k,
-                     sfb0 + 16 * t + 4 * k, acc);
-              if (kGU)
-                tc_mma(dcol + 32 * (p.nt_max + t), smem_desc(a0 + 16384 + 32 * k, 16, 1024, 2), bd,
-                       sf + 16 + 4 * k, sfb0 + 16 * t + 4 * k, acc);
-            }
+            const uint64_t ad = smem_desc(a0 + 32 * k, 16, 1024, 2);
+            for (int t = 0; t < nt; ++t)
+              tc_mma(dcol + 32 * t, ad, smem_desc(b0 + t * 4096 + 32 * k, 16, 1024, 2), sf + 4 * k,
+                     sf + 16 + 16 * t + 4 * k, !(first && k == 0));
           }
+          first = false;
           tc_commit(&sm.empty[s]);
+          tc_commit(&sm.slot_free[i * 2 + slot]);
         }
-        if (ok) tc_commit(&sm.acc_full[ab]);
+        if (ok) tc_commit(&sm.acc_full[ab]);  // also when this phase had no K-block
       }
       // everything this thread issued completes before TMEM is released
-      tc_commit(sm.drain);
-      if (!mbar_wait(sm.drain, 0)) latch_error(ws.err, kDevWaitTimeout);
+      tc_commit(&sm.drain[i]);
+      if (!mbar_wait(&sm.drain[i], 0)) latch_error(ws.err, kDevWaitTimeout);
     }
   } else {
     // ----------------------------------------------------------- epilogue
@@ -414,9 +436,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       grid_dep_wait();
       grid_dep_launch();
     }
-    const int t = tid - 64;             // 0..127
-    const int q = warp & 3;             // TMEM lane quadrant of this warp
-    const int m = 32 * q + lane;        // weight row within the tile
+    const int t = tid - 32 * (P + 1);   // 0..127
+    const int qd = warp & 3;            // TMEM lane quadrant of this warp
+    const int m = 32 * qd + lane;       // weight row within the tile
+    const int nparts = KB < p.Q ? KB : p.Q;  // K-phase partial accumulators that exist
     const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
     int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0, item = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
@@ -449,7 +472,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (!kGU) {
           tc_named_sync();  // nobody still reads the previous expert's pair ids
-          for (int i = t; i < ne; i += kEpiThreads) sm.pairs[i] = __ldcg(ws.pair_order + pos0 + i);
+          for (int j = t; j < ne; j += kEpiThreads) sm.pairs[j] = __ldcg(ws.pair_order + pos0 + j);
           tc_named_sync();
         }
         cur_e = e;
@@ -464,8 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e);
         }
       }
-      const int ab = p.d_double ? (item & 1) : 0;
-      const int use = p.d_double ? (item >> 1) : item;
+      const int ab = (p.dbuf == 2) ? (item & 1) : 0;
+      const int use = (p.dbuf == 2) ? (item >> 1) : item;
       // one thread waits (bounded); the barrier hands its verdict to all four
       // epilogue warps so none is left behind at a later barrier
       if (t == 0) *sm.flag = mbar_wait(&sm.acc_full[ab], use & 1) ? 1 : 0;
@@ -477,33 +500,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t dcol = tmem + p.tm_d + (uint32_t)ab * acc_cols + ((uint32_t)(32 * q) << 16);
+      const uint32_t lanes = (uint32_t)(32 * qd) << 16;
       const int nt = (ne + 31) / 32;
       for (int tt = 0; tt < nt; ++tt) {
-        uint32_t g[32];
-        tc_ld32(dcol + 32 * tt, g);
-        if (kGU) {
-          uint32_t u[32];
-          tc_ld32(dcol + 32 * (p.nt_max + tt), u);
-          tc_wait_ld();
-          const int cnt = min(32, ne - 32 * tt);
-          float* hrow = ws.h + (size_t)(pos0 + 32 * tt) * p.I + (size_t)tile * 128 + m;
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = 32 * tt + 16 * half;  // first pair column of this half
+          const int cnt = min(16, ne - c0);
+          if (cnt <= 0) break;
+          // sum the K-phase partials (fixed order) of each accumulator type
+          float acc0[16], acc1[16];
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (n < cnt) {
-              const float hv = silu_f(__uint_as_float(g[n]) * sc0) * (__uint_as_float(u[n]) * sc1);
-              hrow[(size_t)n * p.I] = hv;
-              cur_amax = fmaxf(cur_amax, fabsf(hv));
+          for (int n = 0; n < 16; ++n) acc0[n] = acc1[n] = 0.0f;
+          for (int qq = 0; qq < nparts; ++qq) {
+            uint32_t r[16];
+            tc_ld16(tmem + lanes + (uint32_t)qq * p.issuer_cols + (uint32_t)ab * p.acc_cols + c0, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int n = 0; n < 16; ++n) acc0[n] += __uint_as_float(r[n]);
+            if (kGU) {
+              tc_ld16(tmem + lanes + (uint32_t)(p.Q + qq) * p.issuer_cols +
+                          (uint32_t)ab * p.acc_cols + c0,
+                      r);
+              tc_wait_ld();
+#pragma unroll
+              for (int n = 0; n < 16; ++n) acc1[n] += __uint_as_float(r[n]);
             }
           }
-        } else {
-          tc_wait_ld();
-          const int cnt = min(32, ne - 32 * tt);
+          if (kGU) {
+            float* hrow = ws.h + (size_t)(pos0 + c0) * p.I + (size_t)tile * 128 + m;
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (n < cnt) {
-              const int pair = sm.pairs[32 * tt + n];
-              ws.o[(size_t)pair * p.H + (size_t)tile * 128 + m] = __uint_as_float(g[n]) * sc0;
+            for (int n = 0; n < 16; ++n) {
+              if (n < cnt) {
+                const float hv = silu_f(acc0[n] * sc0) * (acc1[n] * sc1);
+                hrow[(size_t)n * p.I] = hv;
+                cur_amax = fmaxf(cur_amax, fabsf(hv));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+              if (n < cnt) {
+                const int pair = sm.pairs[c0 + n];
+                ws.o[(size_t)pair * p.H + (size_t)tile * 128 + m] = acc0[n] * sc0;
+              }
             }
           }
         }
@@ -587,7 +626,7 @@ cudaError_t launch_tc_experts(const TcParams& p, const CUtensorMap& a, const CUt
                               const CUtensorMap& sfb, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(32 * (1 + p.P + 4), 1, 1);
   cfg.dynamicSmemBytes = tc_smem_bytes(p);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

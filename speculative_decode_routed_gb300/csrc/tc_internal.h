@@ -16,12 +16,18 @@ struct TcParams {
   int row_tiles;            // RE / 128
   int nt_max;               // 32-row activation tiles per MMA group (max pairs / 32)
   int NS;                   // pipeline stages
-  int d_double;             // accumulators double buffered in TMEM
+  int T;                    // accumulator types: 2 (gate, up) or 1 (down)
+  int Q;                    // K phases: issuer q takes the K-blocks kb = q (mod Q)
+  int P;                    // MMA issuer warps = T * Q, each with its own accumulators
+  int dbuf;                 // accumulator buffers per issuer (2: epilogue overlaps)
+  int sfslots;              // TMEM scale slots per issuer
+  uint32_t acc_cols;        // TMEM columns of one accumulator (32 per N-tile)
+  uint32_t sf_cols;         // TMEM columns of one scale slot (A: 16, B: 16 per N-tile)
+  uint32_t issuer_cols;     // TMEM columns per issuer
   uint32_t stage_stride;    // bytes per stage (multiple of 1024)
   uint32_t a_bytes;         // weight tile bytes per stage (16 or 32 KB)
   uint32_t sfa_bytes;       // weight scale atoms per stage (2 or 4 KB)
   uint32_t off_sfa, off_b, off_sfb;  // offsets within a stage
-  uint32_t tm_d, tm_sf, sf_slot;     // TMEM column plan
   int ws_pairs;             // rows * k of the workspace
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
