@@ -149,7 +149,7 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 // ------------------------------------------------------------ shared memory
 
 struct TcSmem {
-  uint64_t* full;       // [NS]      TMA bytes landed
+  uint64_t* full;       // [NS][Q]   TMA bytes landed, one barrier per stage and K-phase group
   uint64_t* empty;      // [NS]      every issuer that reads the stage is done (T arrivals)
   uint64_t* acc_full;   // [2]       accumulators ready for the epilogue (P arrivals)
   uint64_t* acc_empty;  // [2]       epilogue done reading them (4 arrivals)
@@ -165,7 +165,7 @@ struct TcSmem {
 __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
   TcSmem s;
   s.full = reinterpret_cast<uint64_t*>(base);
-  s.empty = s.full + 16;
+  s.empty = s.full + 32;
   s.acc_full = s.empty + 16;
   s.acc_empty = s.acc_full + 2;
   s.slot_free = s.acc_empty + 2;
@@ -257,9 +257,15 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.P;
 
+  // A stage is read by the issuers of K-phase group q = kb mod Q.  When NS is
+  // not a multiple of Q the group changes from one fill of a stage to the
+  // next, and a parity wait by an issuer that skipped a phase would match the
+  // stale parity of the fill before.  So each (stage, group) has its own
+  // full barrier: every phase of it is consumed by the same issuers, and each
+  // waiter tracks that barrier's parity itself.
   if (tid == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&sm.full[s], 1);
+      for (int q = 0; q < p.Q; ++q) mbar_init(&sm.full[s * p.Q + q], 1);
       mbar_init(&sm.empty[s], p.T);
     }
     for (int b = 0; b < 2; ++b) {
@@ -308,6 +314,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       int g = 0;  // global stage counter = item * KB + kb
+      uint32_t fbits = 0;  // per (stage, group) full barrier: parity of fills issued
       bool ok = true;
       bool waited = kGU;
       for (int it = it0; it < it1 && ok; ++it) {
@@ -326,19 +333,22 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
             break;
           }
           uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
+          const int fb = s * p.Q + kb % p.Q;
+          uint64_t* full = &sm.full[fb];
+          fbits ^= 1u << fb;
           const uint32_t bytes = p.a_bytes + p.sfa_bytes + (uint32_t)nt * (4096u + 2048u);
-          mbar_arrive_expect_tx(&sm.full[s], bytes);
+          mbar_arrive_expect_tx(full, bytes);
           // gate rows (gate/up) or output rows (down) of this tile
-          tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, &sm.full[s], pol);
+          tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
           bulk_g2s_plain(st + p.off_sfa,
                          p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, 2048u,
-                         &sm.full[s]);
+                         full);
           if (kGU) {
             const int ru = p.I / 128 + tile;  // up rows follow the gate rows
-            tma_2d(st + 16384, &tm_a, kb * 128, e * p.RE + ru * 128, &sm.full[s], pol);
+            tma_2d(st + 16384, &tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
             bulk_g2s_plain(st + p.off_sfa + 2048,
                            p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
-                           &sm.full[s]);
+                           full);
           }
           if (!waited) {  // down: h and its scales come from the gate/up kernel
             grid_dep_wait();
@@ -346,8 +356,8 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
             waited = true;
           }
           for (int t = 0; t < nt; ++t) {
-            tma_2d_plain(st + p.off_b + t * 4096, &tm_b, kb * 128, pos0 + 32 * t, &sm.full[s]);
-            tma_3d(st + p.off_sfb + t * 2048, &tm_sfb, 0, pos0 + 32 * t, kb * 4, &sm.full[s]);
+            tma_2d_plain(st + p.off_b + t * 4096, &tm_b, kb * 128, pos0 + 32 * t, full);
+            tma_3d(st + p.off_sfb + t * 2048, &tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
           }
         }
       }
@@ -355,10 +365,12 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         grid_dep_wait();
         grid_dep_launch();
       }
-      // every issued copy lands before the CTA may exit
+      // every issued copy lands before the CTA may exit: the last fill of a
+      // stage was issued only after every earlier fill of it had been consumed
       for (int s = 0; s < p.NS && s < g; ++s) {
         const int last = s + p.NS * ((g - 1 - s) / p.NS);
-        if (!mbar_wait(&sm.full[s], (last / p.NS) & 1)) latch_error(ws.err, kDevWaitTimeout);
+        const int fb = s * p.Q + (last % KB) % p.Q;
+        if (!mbar_wait(&sm.full[fb], ((fbits >> fb) & 1u) ^ 1u)) latch_error(ws.err, kDevWaitTimeout);
       }
     }
   } else if (warp <= P) {
@@ -372,6 +384,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
     if (lane == 0) {
       const uint32_t ibase = tmem + (uint32_t)i * p.issuer_cols;
       int c = 0, item = 0;  // stages handled, items seen
+      uint32_t fpar = 0;    // bit s: parity of this group's next phase of full[s][q]
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it, ++item) {
         const int4 et = tc_item_expert(p, sm, it, ai_first);
@@ -389,7 +402,9 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         for (int kb = q; kb < KB; kb += p.Q, ++c) {
           const int g = item * KB + kb;
           const int s = g % p.NS;
-          if (!mbar_wait(&sm.full[s], (g / p.NS) & 1)) {
+          const uint32_t par = (fpar >> s) & 1u;
+          fpar ^= 1u << s;
+          if (!mbar_wait(&sm.full[s * p.Q + q], par)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;

@@ -253,6 +253,33 @@ def test_tiny_step_end_to_end_graph_and_host():
     dec.close()
 
 
+def test_repeated_replays_bitwise():
+    """Many graph replays of one input give the eager result bit for bit with
+    no device-side error.  The shape makes the gate/up kernel's stage ring
+    (5 stages) not a multiple of its K-phase groups (2), with tens of stage
+    fills per CTA, so a stage-barrier phase mix-up between the groups would
+    show as a timeout or a changed result."""
+    w = synth.Workload("replay", rows=8, hidden=4096, n_experts=64, top_k=8, inter=1024)
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    s0 = stream.clone()
+    out = torch.empty_like(branch)
+    dec.step(w.rows, branch, stream, out)
+    torch.cuda.synchronize()
+    dec.check()
+    ref_s, ref_o = stream.clone(), out.clone()
+    bad = 0
+    for _ in range(400):
+        stream.copy_(s0)
+        dec.step_graph(w.rows, branch, stream, out)
+        bad += int(not torch.equal(stream, ref_s)) + int(not torch.equal(out, ref_o))
+    torch.cuda.synchronize()
+    dec.check()
+    assert bad == 0, f"{bad} replays differ from the eager result"
+    dec.close()
+
+
 ODD_SHAPES = [
     # (rows, H, E, k, I): a ragged H (cluster of 1, 12 chunks/row), a single
     # expert, k == E, a row count with many rows per expert (> 8: the
