@@ -195,6 +195,32 @@ const char* moe_decode_error_message(void);
 int moe_nvfp4_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
                        float* sg, float* amax, void* cuda_stream);
 
+/* The same quantizer for callers that cannot allocate device memory: code
+ * that runs inside another runtime which hands it only its input and output
+ * buffers and keeps every allocation to itself, or a latency-critical loop
+ * that cannot afford cudaMalloc / cudaFree (they may synchronize the whole
+ * device).  The pages this library follows have no counterpart: it is a
+ * deployment convenience, not part of the method.
+ *
+ * Same arguments and results as moe_nvfp4_quantize (codes, sf and *sg bit for
+ * bit equal), minus the amax scalar: the reduction's scratch is a fixed array
+ * inside the library (about 64 KB on every GPU that loads the library, held
+ * until the process exits).  It allocates nothing and calls no allocating
+ * routine.
+ *   - At most 2^30 elements (rows * cols); larger tensors are rejected with
+ *     MOE_EUNSUPPORTED before anything is launched.
+ *   - The first call on each device looks up the scratch's device address
+ *     (with that device current); make that first call before any stream
+ *     capture on the device.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents (the call clears what must start at zero).  Calls
+ *     that can overlap on the GPU -- on different streams, or from host
+ *     threads without ordering between them -- race on it and may produce a
+ *     wrong tensor scale: issue them on one stream.
+ * Asynchronous on cuda_stream. */
+int moe_nvfp4_quantize_noalloc(const float* v, int64_t rows, int64_t cols, uint8_t* codes,
+                               uint8_t* sf, float* sg, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ EXPORTS = (
     "moe_decode_step_graph", "moe_decode_step_host", "moe_decode_layer_profile", "moe_decode_debug",
     "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_step_kernel_count",
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
-    "moe_nvfp4_quantize",
+    "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
 )
 
 
@@ -81,6 +81,7 @@ def _lib():
             "moe_decode_strerror": (ctypes.c_char_p, [i32]),
             "moe_decode_error_message": (ctypes.c_char_p, []),
             "moe_nvfp4_quantize": (i32, [vp, i64, i64, vp, vp, vp, vp, vp]),
+            "moe_nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -183,6 +184,15 @@ def moe_nvfp4_quantize(v, codes, sf, sg, amax, stream=None):
     rows, cols = v.shape
     _check(_lib().moe_nvfp4_quantize(_ptr(v), rows, cols, _ptr(codes), _ptr(sf), _ptr(sg),
                                      _ptr(amax), _stream(stream)), "moe_nvfp4_quantize")
+
+
+def moe_nvfp4_quantize_noalloc(v, codes, sf, sg, stream=None):
+    """As moe_nvfp4_quantize, for callers that cannot allocate device memory:
+    the max |v| reduction uses a fixed scratch array inside the library
+    (at most 2**30 elements; calls that overlap on the GPU race on it)."""
+    rows, cols = v.shape
+    _check(_lib().moe_nvfp4_quantize_noalloc(_ptr(v), rows, cols, _ptr(codes), _ptr(sf), _ptr(sg),
+                                             _stream(stream)), "moe_nvfp4_quantize_noalloc")
 
 
 # --------------------------------------------------------- torch convenience

@@ -66,6 +66,12 @@ struct GraphEntry {
 
 }  // namespace
 
+namespace moe {
+// Records the reason of a failing call for moe_decode_error_message (entry
+// points defined outside this file).
+int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace moe
+
 struct moe_decode_s {
   moe_decode_dims d;
   std::vector<moe_layer_weights> layers;

@@ -107,6 +107,12 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes,
                             uint8_t* sf, float* sg, float* amax, cudaStream_t s);
+// The quantizer's encode pass alone, given the tensor's max |v| (float bits)
+// in device memory.
+cudaError_t launch_nvfp4_encode(const float* v, int64_t nblocks, uint8_t* codes, uint8_t* sf,
+                                const unsigned* amax, float* sg, cudaStream_t s);
+// Sets the calling thread's moe_decode_error_message; returns code.
+int api_fail(int code, const char* msg);
 
 size_t expert_smem_bytes(const ExpertParams& p);
 size_t expert_ctrl_bytes();

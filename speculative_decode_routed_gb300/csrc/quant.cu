@@ -75,4 +75,16 @@ cudaError_t launch_quantize(const float* v, int64_t rows, int64_t cols, uint8_t*
   return cudaGetLastError();
 }
 
+cudaError_t launch_nvfp4_encode(const float* v, int64_t nblocks, uint8_t* codes, uint8_t* sf,
+                                const unsigned* amax, float* sg, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int threads = 256;
+  const int64_t want = (nblocks + threads - 1) / threads;
+  const int grid = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+  encode_kernel<<<grid, threads, 0, s>>>(v, nblocks, codes, sf, amax, sg);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
