@@ -164,41 +164,52 @@ int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
   p.row_tiles = p.RE / 128;
   const int maxn = d.max_rows < 128 ? d.max_rows : 128;
   p.nt_max = (maxn + 31) / 32;
-  p.a_bytes = gu ? 32768u : 16384u;
-  p.sfa_bytes = gu ? 4096u : 2048u;
+  p.T = gu ? 2 : 1;
+  p.acc_cols = 32u * (uint32_t)p.nt_max;
+  // TMEM (512 columns): as many independent MMA issuers as fit, each with its
+  // own accumulators and scale slots (issue latency, not the tensor core,
+  // bounds one issuer; issuers overlap).  The single TMA-issuing thread costs
+  // about the same per copy whatever its size, so down, whose weight tile per
+  // K-block is half of gate/up's, moves two K-blocks per stage (one 3D copy
+  // per operand) when its rows are whole K-blocks and TMEM still holds four
+  // issuers.
+  p.P = 0;
+  const int qs_gu[2] = {2, 1}, qs_dn[3] = {4, 2, 1};
+  const int* qs = gu ? qs_gu : qs_dn;
+  const int nq = gu ? 2 : 3;
+  const int kps_opts[2] = {2, 1};
+  const int kps_first = (!gu && d.inter % 256 == 0) ? 0 : 1;
+  const int modes[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
+  for (int qi = 0; qi < nq && !p.P; ++qi)
+    for (int ki = kps_first; ki < 2 && !p.P; ++ki)
+      for (int mi = 0; mi < 4 && !p.P; ++mi) {
+        const int kps = kps_opts[ki];
+        const uint32_t sfc = 16u * (uint32_t)kps * (1u + (uint32_t)p.nt_max);
+        const uint32_t cols = (uint32_t)modes[mi][0] * p.acc_cols + (uint32_t)modes[mi][1] * sfc;
+        const int P = p.T * qs[qi];
+        if ((uint32_t)P * cols <= 512u) {
+          p.Q = qs[qi];
+          p.P = P;
+          p.KPS = kps;
+          p.dbuf = modes[mi][0];
+          p.sfslots = modes[mi][1];
+          p.sf_cols = sfc;
+          p.issuer_cols = cols;
+        }
+      }
+  if (!p.P) return fail(MOE_EUNSUPPORTED, "tensor-core plan does not fit TMEM (max_rows %d)", d.max_rows);
+  p.KSTEPS = (p.KBLK + p.KPS - 1) / p.KPS;
+  p.a_bytes = 16384u * (uint32_t)(p.KPS * p.T);
+  p.sfa_bytes = 2048u * (uint32_t)(p.KPS * p.T);
   p.off_b = p.a_bytes;
-  p.off_sfa = p.off_b + 4096u * (uint32_t)p.nt_max;
+  p.off_sfa = p.off_b + 4096u * (uint32_t)(p.KPS * p.nt_max);
   p.off_sfb = p.off_sfa + p.sfa_bytes;
-  const uint32_t stage = p.off_sfb + 2048u * (uint32_t)p.nt_max;
+  const uint32_t stage = p.off_sfb + 2048u * (uint32_t)(p.KPS * p.nt_max);
   p.stage_stride = (stage + 1023u) / 1024u * 1024u;
   int ns = (int)((227 * 1024 - 1024 - moe::tc_ctrl_bytes()) / p.stage_stride);
   if (ns > 8) ns = 8;
   if (ns < 2) return fail(MOE_EUNSUPPORTED, "tensor-core stage too large (max_rows %d)", d.max_rows);
   p.NS = ns;
-  // TMEM (512 columns): as many independent MMA issuers as fit, each with its
-  // own accumulators and scale slots (issue latency, not the tensor core,
-  // bounds one issuer; issuers overlap).
-  p.T = gu ? 2 : 1;
-  p.acc_cols = 32u * (uint32_t)p.nt_max;
-  p.sf_cols = 16u + 16u * (uint32_t)p.nt_max;
-  p.P = 0;
-  const int qs_gu[2] = {2, 1}, qs_dn[3] = {4, 2, 1};
-  const int* qs = gu ? qs_gu : qs_dn;
-  const int nq = gu ? 2 : 3;
-  const int modes[3][2] = {{2, 2}, {1, 2}, {1, 1}};
-  for (int qi = 0; qi < nq && !p.P; ++qi)
-    for (int mi = 0; mi < 3 && !p.P; ++mi) {
-      const uint32_t cols = (uint32_t)modes[mi][0] * p.acc_cols + (uint32_t)modes[mi][1] * p.sf_cols;
-      const int P = p.T * qs[qi];
-      if ((uint32_t)P * cols <= 512u) {
-        p.Q = qs[qi];
-        p.P = P;
-        p.dbuf = modes[mi][0];
-        p.sfslots = modes[mi][1];
-        p.issuer_cols = cols;
-      }
-    }
-  if (!p.P) return fail(MOE_EUNSUPPORTED, "tensor-core plan does not fit TMEM (max_rows %d)", d.max_rows);
   p.ws_pairs = d.max_rows * d.top_k;
   return MOE_OK;
 }
@@ -232,13 +243,35 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
   return MOE_OK;
 }
 
-// Scale lines [groups][rows][16 B]: boxes of 16 B x 32 rows x 4 groups.
-int encode_lines(CUtensorMap* m, const void* base, uint64_t rows, uint64_t groups) {
+// Row-major bytes [rows][inner], inner a multiple of 128, viewed as
+// [inner / 128 K-blocks][rows][128 B]: boxes of 128 bytes x box_rows x kblocks,
+// landing as kblocks consecutive 128B-swizzled tiles.
+int encode_rows_kb(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                   uint32_t box_rows, uint32_t kblocks) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
+  if (inner % 128) return fail(MOE_EUNSUPPORTED, "rows of %llu bytes are not whole K-blocks",
+                               (unsigned long long)inner);
+  const cuuint64_t dims[3] = {128, rows, inner / 128};
+  const cuuint64_t strides[2] = {inner, 128};
+  const cuuint32_t box[3] = {128, box_rows, kblocks};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "tensor map encode failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+// Scale lines [groups][rows][16 B]: boxes of 16 B x 32 rows x box_groups.
+int encode_lines(CUtensorMap* m, const void* base, uint64_t rows, uint64_t groups,
+                 uint32_t box_groups = 4) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
   const cuuint64_t dims[3] = {16, rows, groups};
   const cuuint64_t strides[2] = {16, rows * 16};
-  const cuuint32_t box[3] = {16, 32, 4};
+  const cuuint32_t box[3] = {16, 32, box_groups};
   const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -562,15 +595,18 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     const uint64_t H = d.hidden, I = d.inter, E = d.n_experts;
     rc = encode_rows(&h->tm_xpool, h->ws.x_pool, H / 2, R, 32);
     if (!rc) rc = encode_lines(&h->tm_xlines, h->ws.x_lines, R, H / 64);
-    if (!rc) rc = encode_rows(&h->tm_hcodes, h->ws.h_codes, I / 2, R, 32);
-    if (!rc) rc = encode_lines(&h->tm_hlines, h->ws.h_lines, R, I / 64);
+    const uint32_t kps = (uint32_t)h->tdn.KPS;
+    if (!rc) rc = kps == 1 ? encode_rows(&h->tm_hcodes, h->ws.h_codes, I / 2, R, 32)
+                           : encode_rows_kb(&h->tm_hcodes, h->ws.h_codes, I / 2, R, 32, kps);
+    if (!rc) rc = encode_lines(&h->tm_hlines, h->ws.h_lines, R, I / 64, 4 * kps);
     h->tm_w13.resize(d.n_layers);
     h->tm_w2.resize(d.n_layers);
     h->sfa13.assign(d.n_layers, nullptr);
     h->sfa2.assign(d.n_layers, nullptr);
     for (int l = 0; l < d.n_layers && !rc; ++l) {
       rc = encode_rows(&h->tm_w13[l], layers[l].w13, H / 2, E * 2 * I, 128);
-      if (!rc) rc = encode_rows(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128);
+      if (!rc) rc = kps == 1 ? encode_rows(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128)
+                             : encode_rows_kb(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128, kps);
       const size_t b13 = (size_t)E * h->tgu.row_tiles * h->tgu.KBLK * 2048;
       const size_t b2 = (size_t)E * h->tdn.row_tiles * h->tdn.KBLK * 2048;
       if (!rc && cudaMalloc(&h->sfa13[l], b13) != cudaSuccess) rc = fail(MOE_ENOMEM, "scale atoms");

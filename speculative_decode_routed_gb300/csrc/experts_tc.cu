@@ -11,17 +11,21 @@
 // Swap-AB: the expert's weight rows fill the MMA's M = 128 (operand A,
 // streamed from HBM), the expert's pairs fill N (operand B, 32 rows per MMA,
 // from L2).  One persistent CTA per SM, warp-specialized:
-//   warp 0  TMA producer: per 256-wide K-block, the weight tiles (2D tensor
-//           map, 128B swizzle), their scale atoms (one bulk copy, laid out
-//           for tcgen05.cp at create time), the pooled activation tile and
-//           its scale lines (2D / 3D tensor maps) into a ring of stages;
-//   warp 1  MMA issuer: tcgen05.cp of the scales into TMEM, then 4 MMAs
-//           (K = 64 each) per tile per K-block, accumulating in TMEM;
-//           tcgen05.commit frees the stage / publishes the accumulator;
-//   warps 2-5 epilogue: tcgen05.ld of the accumulators (one TMEM lane per
-//           weight row), scale by the two fp32 tensor scales, SiLU * up or
-//           the down output, coalesced stores.  Accumulators are double
-//           buffered in TMEM so the epilogue of item i overlaps item i+1.
+//   warp 0  TMA producer: per stage (KPS K-blocks of 256), the weight tiles
+//           (tensor map, 128B swizzle), their scale atoms (one bulk copy,
+//           laid out for tcgen05.cp at create time), the pooled activation
+//           tiles and their scale lines (tensor maps) into a ring of stages;
+//   warps 1..P  MMA issuers: issuer (type, q) -- gate or up accumulator, and
+//           the stages ks = q (mod Q) of every item -- copies the stage's
+//           scales into its own TMEM slot (tcgen05.cp) and issues 4 MMAs
+//           (K = 64) per K-block into its own accumulator; tcgen05.commit
+//           frees the stage and publishes the accumulator.  One thread's MMA
+//           issue is latency-bound; independent issuers overlap.
+//   4 warps epilogue: tcgen05.ld of the K-phase partial accumulators (one
+//           TMEM lane per weight row) summed in a fixed order, scaled by the
+//           two fp32 tensor scales, SiLU * up or the down output, coalesced
+//           stores.  Accumulators are double buffered in TMEM so the epilogue
+//           of item i overlaps item i+1.
 // Every wait is bounded (a latched error instead of a hang).
 #include <cuda.h>
 
@@ -63,6 +67,15 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x,
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_3d_hint(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -307,13 +320,15 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   const uint32_t tmem = *sm.tmem_base;
   if (!na_ok && tid == 0) latch_error(ws.err, kDevBadRouting);
 
-  const int KB = p.KBLK;
+  const int KB = p.KBLK;      // K-blocks of 256 per item
+  const int KPS = p.KPS;      // K-blocks per stage
+  const int KS = p.KSTEPS;    // stages per item
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int g = 0;  // global stage counter = item * KB + kb
+      int g = 0;  // global stage counter = item * KS + ks
       uint32_t fbits = 0;  // per (stage, group) full barrier: parity of fills issued
       bool ok = true;
       bool waited = kGU;
@@ -325,7 +340,9 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         }
         const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
         const int nt = (ne + 31) / 32;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int kb = ks * KPS;  // first K-block of this stage
+          const int nkb = min(KPS, KB - kb);
           const int s = g % p.NS;
           if (g >= p.NS && !mbar_wait(&sm.empty[s], ((g / p.NS) - 1) & 1)) {
             latch_error(ws.err, kDevWaitTimeout);
@@ -333,17 +350,25 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
             break;
           }
           uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
-          const int fb = s * p.Q + kb % p.Q;
+          const int fb = s * p.Q + ks % p.Q;
           uint64_t* full = &sm.full[fb];
           fbits ^= 1u << fb;
-          const uint32_t bytes = p.a_bytes + p.sfa_bytes + (uint32_t)nt * (4096u + 2048u);
+          // weight tiles (a missing second K-block of a stage is zero filled
+          // and counts in full), the present K-blocks' scale atoms, and per
+          // N-tile the activation tiles and scale lines
+          const uint32_t sfa_b = 2048u * (uint32_t)nkb;
+          const uint32_t bytes = p.a_bytes + sfa_b * (uint32_t)p.T +
+                                 (uint32_t)(nt * KPS) * (4096u + 2048u);
           mbar_arrive_expect_tx(full, bytes);
           // gate rows (gate/up) or output rows (down) of this tile
-          tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
+          if (KPS == 1)
+            tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
+          else
+            tma_3d_hint(st, &tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
           bulk_g2s_plain(st + p.off_sfa,
-                         p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, 2048u,
+                         p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, sfa_b,
                          full);
-          if (kGU) {
+          if (kGU) {  // gate/up stages hold one K-block
             const int ru = p.I / 128 + tile;  // up rows follow the gate rows
             tma_2d(st + 16384, &tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
             bulk_g2s_plain(st + p.off_sfa + 2048,
@@ -356,8 +381,11 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
             waited = true;
           }
           for (int t = 0; t < nt; ++t) {
-            tma_2d_plain(st + p.off_b + t * 4096, &tm_b, kb * 128, pos0 + 32 * t, full);
-            tma_3d(st + p.off_sfb + t * 2048, &tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
+            if (KPS == 1)
+              tma_2d_plain(st + p.off_b + t * 4096, &tm_b, kb * 128, pos0 + 32 * t, full);
+            else
+              tma_3d(st + p.off_b + t * 4096 * KPS, &tm_b, 0, pos0 + 32 * t, kb, full);
+            tma_3d(st + p.off_sfb + t * 2048 * KPS, &tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
           }
         }
       }
@@ -369,7 +397,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
       // stage was issued only after every earlier fill of it had been consumed
       for (int s = 0; s < p.NS && s < g; ++s) {
         const int last = s + p.NS * ((g - 1 - s) / p.NS);
-        const int fb = s * p.Q + (last % KB) % p.Q;
+        const int fb = s * p.Q + (last % KS) % p.Q;
         if (!mbar_wait(&sm.full[fb], ((fbits >> fb) & 1u) ^ 1u)) latch_error(ws.err, kDevWaitTimeout);
       }
     }
@@ -399,8 +427,9 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         tc_fence_after();
         const uint32_t dcol = ibase + (uint32_t)ab * p.acc_cols;
         bool first = true;
-        for (int kb = q; kb < KB; kb += p.Q, ++c) {
-          const int g = item * KB + kb;
+        for (int ks = q; ks < KS; ks += p.Q, ++c) {
+          const int g = item * KS + ks;
+          const int nkb = min(KPS, KB - ks * KPS);
           const int s = g % p.NS;
           const uint32_t par = (fpar >> s) & 1u;
           fpar ^= 1u << s;
@@ -419,21 +448,23 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
           tc_fence_after();
           const uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
           const uint32_t sf = ibase + (uint32_t)p.dbuf * p.acc_cols + (uint32_t)slot * p.sf_cols;
-          // scales into TMEM, 4 columns per MMA: A (this issuer's weight tile)
-          // at sf, B per N-tile at sf + 16 + 16 t
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tc_cp_sf(sf + 4 * k, st + p.off_sfa + ty * 2048 + k * 512);
+          // scales into TMEM, 4 columns per MMA (m = 4 j + k for K-block j of
+          // the stage): A (this issuer's weight tile) at sf, B per N-tile at
+          // sf + 16 KPS (1 + t)
+          const uint32_t sfb0 = sf + 16u * (uint32_t)KPS;
+          for (int m = 0; m < 4 * nkb; ++m)
+            tc_cp_sf(sf + 4 * m, st + p.off_sfa + ty * 2048 * KPS + m * 512);
           for (int t = 0; t < nt; ++t)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc_cp_sf(sf + 16 + 16 * t + 4 * k, st + p.off_sfb + t * 2048 + k * 512);
-          const uint32_t a0 = smem_u32(st) + (uint32_t)ty * 16384u, b0 = smem_u32(st + p.off_b);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = smem_desc(a0 + 32 * k, 16, 1024, 2);
+            for (int m = 0; m < 4 * nkb; ++m)
+              tc_cp_sf(sfb0 + 16 * KPS * t + 4 * m, st + p.off_sfb + t * 2048 * KPS + m * 512);
+          const uint32_t a0 = smem_u32(st) + (uint32_t)(ty * 16384 * KPS), b0 = smem_u32(st + p.off_b);
+          for (int m = 0; m < 4 * nkb; ++m) {
+            const uint32_t kofs = (uint32_t)((m >> 2) * 16384 + 32 * (m & 3));
+            const uint64_t ad = smem_desc(a0 + kofs, 16, 1024, 2);
             for (int t = 0; t < nt; ++t)
-              tc_mma(dcol + 32 * t, ad, smem_desc(b0 + t * 4096 + 32 * k, 16, 1024, 2), sf + 4 * k,
-                     sf + 16 + 16 * t + 4 * k, !(first && k == 0));
+              tc_mma(dcol + 32 * t, ad,
+                     smem_desc(b0 + t * 4096 * KPS + (m >> 2) * 4096 + 32 * (m & 3), 16, 1024, 2),
+                     sf + 4 * m, sfb0 + 16 * KPS * t + 4 * m, !(first && m == 0));
           }
           first = false;
           tc_commit(&sm.empty[s]);
@@ -454,7 +485,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
     const int t = tid - 32 * (P + 1);   // 0..127
     const int qd = warp & 3;            // TMEM lane quadrant of this warp
     const int m = 32 * qd + lane;       // weight row within the tile
-    const int nparts = KB < p.Q ? KB : p.Q;  // K-phase partial accumulators that exist
+    const int nparts = KS < p.Q ? KS : p.Q;  // K-phase partial accumulators that exist
     const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
     int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0, item = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;

@@ -11,6 +11,8 @@ struct TcParams {
   int H, I, E, k;
   int K;                    // reduction length (H or I)
   int KBLK;                 // 256-wide K-blocks (the last may be half: zero filled)
+  int KPS;                  // K-blocks per pipeline stage (1, or 2 when rows are whole K-blocks)
+  int KSTEPS;               // stages per item: ceil(KBLK / KPS)
   int tiles;                // 128-row output tiles per expert (I/128 or H/128)
   int RE;                   // weight rows per expert (2I or H)
   int row_tiles;            // RE / 128
