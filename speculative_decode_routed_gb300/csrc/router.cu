@@ -40,6 +40,197 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   return acc;
 }
 
+// Comparator of the routing order: higher logit first, ties to the lower id.
+__device__ __forceinline__ bool route_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Shared tail of one row's routing (lane t < nsel holds the t-th selection):
+// renormalised gates in slot order, the near-tie flag, ids to global and to
+// shared memory for the pooler.
+__device__ __forceinline__ void route_finish(const RouterParams& p, int r, int nsel, int sel_id,
+                                             float sel_v, float m, float z, int* sids) {
+  const Workspace& ws = p.ws;
+  const int k = p.k, lane = threadIdx.x & 31;
+  const float ex = (lane < nsel) ? expf(sel_v - m) : 0.0f;
+  float den = 0.0f;
+  for (int t = 0; t < k; ++t) den += __shfl_sync(0xffffffffu, ex, t);
+  const float ek = __shfl_sync(0xffffffffu, ex, k - 1);
+  const float ek1 = __shfl_sync(0xffffffffu, ex, (nsel > k) ? k : 0);
+  if (lane < k) {
+    ws.ids[r * k + lane] = sel_id;
+    sids[r * k + lane] = sel_id;
+    ws.gates[r * k + lane] = ex / den;
+    if (sel_id < 0 || sel_id >= p.E) latch_error(ws.err, kDevBadRouting);
+  }
+  if (lane == 0) ws.flags[r] = (nsel > k) ? (uint8_t)((ek - ek1) / z < 1e-6f) : (uint8_t)0;
+}
+
+// One row's routing for E <= 256: lane owns experts e = lane + 32 i (i < 8),
+// their logits in registers.  The slices' partial sums are all loaded at
+// once and added in slice order; the lane's 8 candidates are sorted once
+// (Batcher's odd-even merge network, 19 comparators) and each of the k + 1
+// selections is one warp arg-max of the lanes' heads, after which the
+// winning lane shifts its list.
+__device__ void route_row_small(const RouterParams& p, int r, int* sids) {
+  const Workspace& ws = p.ws;
+  const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
+  float v[8];
+  int id[8];
+  float part[8][8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      part[s][i] = (s < p.S && e < E) ? __ldcg(src + e) : 0.0f;
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    float acc = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < p.S) acc += part[s][i];
+    if (e < E) {
+      if (p.bias) acc += __ldg(p.bias + e);
+      ws.logits[(size_t)r * E + e] = acc;
+      m = fmaxf(m, acc);
+      v[i] = acc;
+      id[i] = e;
+    } else {
+      v[i] = -INFINITY;
+      id[i] = 0x7fffffff;
+    }
+  }
+  m = warp_max(m);
+  float z = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (lane + 32 * i < E) z += expf(v[i] - m);
+  z = warp_sum(z);
+  constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                               {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                               {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const int a = kNet[c][0], b = kNet[c][1];
+    if (route_before(v[b], id[b], v[a], id[a])) {
+      const float tv = v[a];
+      v[a] = v[b];
+      v[b] = tv;
+      const int ti = id[a];
+      id[a] = id[b];
+      id[b] = ti;
+    }
+  }
+  const int nsel = (k < E) ? k + 1 : k;
+  int sel_id = -1;
+  float sel_v = 0.0f;
+  for (int t = 0; t < nsel; ++t) {
+    float bv = v[0];
+    int bi = id[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (route_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == t) {
+      sel_id = bi;
+      sel_v = bv;
+    }
+    const bool won = (id[0] == bi);
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      v[i] = won ? v[i + 1] : v[i];
+      id[i] = won ? id[i + 1] : id[i];
+    }
+    if (won) {
+      v[7] = -INFINITY;
+      id[7] = 0x7fffffff;
+    }
+  }
+  route_finish(p, r, nsel, sel_id, sel_v, m, z, sids);
+}
+
+// One row's routing for any E (up to 1024): logits staged in shared memory,
+// each selection a scan of the lane's experts and a warp arg-max.
+__device__ void route_row_any(const RouterParams& p, int r, float* l, int* sids) {
+  const Workspace& ws = p.ws;
+  const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  // the lane's experts e = lane + 32 i, in groups of 8 so that the loads of
+  // a slice are all in flight together; slices are summed in order
+  for (int i0 = 0; i0 * 32 < E; i0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    for (int s = 0; s < p.S; ++s) {
+      const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * (i0 + i);
+        if (e < E) v[i] += __ldcg(src + e);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * (i0 + i);
+      if (e < E) {
+        const float vb = p.bias ? v[i] + __ldg(p.bias + e) : v[i];
+        l[e] = vb;
+        ws.logits[(size_t)r * E + e] = vb;
+        m = fmaxf(m, vb);
+      }
+    }
+  }
+  m = warp_max(m);
+  float z = 0.0f;
+  for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
+  z = warp_sum(z);
+  __syncwarp();
+  // top-(k+1) by logit (monotone in probability), ties to the lower id
+  const int nsel = (k < E) ? k + 1 : k;
+  int sel_id = -1;      // lane t keeps the t-th selection
+  float sel_v = 0.0f;
+  for (int t = 0; t < nsel; ++t) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = l[e];
+      if (route_before(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (route_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == t) {
+      sel_id = bi;
+      sel_v = bv;
+    }
+    __syncwarp();
+    if (lane == 0) l[bi] = -INFINITY;  // taken
+    __syncwarp();
+  }
+  route_finish(p, r, nsel, sel_id, sel_v, m, z, sids);
+  __syncwarp();
+}
+
 // Routing + pooler, run by the last CTA.
 __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
   const Workspace& ws = p.ws;
@@ -50,85 +241,15 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
   int* off = cnt + E;                                                // [E+1]
   const int RW = (rows + 31) / 32;
   unsigned* mask = reinterpret_cast<unsigned*>(off + E + 1);        // [E][RW]
+  int* sids = reinterpret_cast<int*>(mask + E * RW);                 // [rows * k]
+  int* wtot = sids + rows * k;                                       // [2][warps]
 
   // ---- routing: one warp per row
   for (int r = warp; r < rows; r += kRouterWarps) {
-    float* l = lg + warp * E;
-    float m = -INFINITY;
-    // the lane's experts e = lane + 32 i, in groups of 8 so that the loads of
-    // a slice are all in flight together; slices are summed in order
-    for (int i0 = 0; i0 * 32 < E; i0 += 8) {
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      for (int s = 0; s < p.S; ++s) {
-        const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * (i0 + i);
-          if (e < E) v[i] += __ldcg(src + e);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * (i0 + i);
-        if (e < E) {
-          const float vb = p.bias ? v[i] + __ldg(p.bias + e) : v[i];
-          l[e] = vb;
-          ws.logits[(size_t)r * E + e] = vb;
-          m = fmaxf(m, vb);
-        }
-      }
-    }
-    m = warp_max(m);
-    float z = 0.0f;
-    for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
-    z = warp_sum(z);
-    __syncwarp();
-    // top-(k+1) by logit (monotone in probability), ties to the lower id
-    const int nsel = (k < E) ? k + 1 : k;
-    int sel_id = -1;      // lane t keeps the t-th selection
-    float sel_v = 0.0f;
-    for (int t = 0; t < nsel; ++t) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int e = lane; e < E; e += 32) {
-        const float v = l[e];
-        if (v > bv || (v == bv && e < bi)) {
-          bv = v;
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (lane == t) {
-        sel_id = bi;
-        sel_v = bv;
-      }
-      __syncwarp();
-      if (lane == 0) l[bi] = -INFINITY;  // taken
-      __syncwarp();
-    }
-    // gates: exp(l_s - m) renormalised over the k selected, slot order
-    const float ex = (lane < nsel) ? expf(sel_v - m) : 0.0f;
-    float den = 0.0f;
-    for (int t = 0; t < k; ++t) den += __shfl_sync(0xffffffffu, ex, t);
-    const float ek = __shfl_sync(0xffffffffu, ex, k - 1);
-    const float ek1 = __shfl_sync(0xffffffffu, ex, (nsel > k) ? k : 0);
-    if (lane < k) {
-      ws.ids[r * k + lane] = sel_id;
-      ws.gates[r * k + lane] = ex / den;
-      if (sel_id < 0 || sel_id >= E) latch_error(ws.err, kDevBadRouting);
-    }
-    if (lane == 0) ws.flags[r] = (nsel > k) ? (uint8_t)((ek - ek1) / z < 1e-6f) : (uint8_t)0;
-    __syncwarp();
+    if (E <= 256)
+      route_row_small(p, r, sids);
+    else
+      route_row_any(p, r, lg + warp * E, sids);
   }
   __syncthreads();
 
@@ -140,34 +261,43 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
   __syncthreads();
   const int npairs = rows * k;
   for (int q = tid; q < npairs; q += kRouterThreads) {
-    const int e = ws.ids[q];
+    const int e = sids[q];
     if (e < 0 || e >= E) continue;
     const int r = q / k;
     atomicAdd(&cnt[e], 1);
     atomicOr(&mask[e * RW + (r >> 5)], 1u << (r & 31));
   }
   __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the counts and of the active flags; lane owns a range
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per, e1 = min(E, e0 + per);
+  {
+    // block-wide exclusive scan of the counts and of the active flags; each
+    // thread owns a range of experts
+    const int per = (E + kRouterThreads - 1) / kRouterThreads;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     int csum = 0, asum = 0;
     for (int e = e0; e < e1; ++e) {
       csum += cnt[e];
       asum += cnt[e] > 0;
     }
-    int cex = csum, aex = asum;
+    int ci = csum, ai = asum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int tc = __shfl_up_sync(0xffffffffu, cex, o);
-      const int ta = __shfl_up_sync(0xffffffffu, aex, o);
+      const int tc = __shfl_up_sync(0xffffffffu, ci, o);
+      const int ta = __shfl_up_sync(0xffffffffu, ai, o);
       if (lane >= o) {
-        cex += tc;
-        aex += ta;
+        ci += tc;
+        ai += ta;
       }
     }
-    cex -= csum;
-    aex -= asum;
+    if (lane == 31) {
+      wtot[warp] = ci;
+      wtot[kRouterWarps + warp] = ai;
+    }
+    __syncthreads();
+    int cex = ci - csum, aex = ai - asum;
+    for (int w = 0; w < warp; ++w) {
+      cex += wtot[w];
+      aex += wtot[kRouterWarps + w];
+    }
     for (int e = e0; e < e1; ++e) {
       off[e] = cex;
       ws.offset[e] = cex;
@@ -175,7 +305,7 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
       cex += cnt[e];
       if (cnt[e] > 0) ws.active[aex++] = e;
     }
-    if (lane == 31) {
+    if (tid == kRouterThreads - 1) {
       off[E] = cex;
       ws.offset[E] = cex;
       ws.n_active[0] = aex;
@@ -183,7 +313,7 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
   }
   __syncthreads();
   for (int q = tid; q < npairs; q += kRouterThreads) {
-    const int e = ws.ids[q];
+    const int e = sids[q];
     if (e < 0 || e >= E) continue;
     const int r = q / k;
     int rank = 0;
@@ -306,7 +436,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 size_t router_smem_bytes(int E, int rows) {
   const int RW = (rows + 31) / 32;
   const size_t route = (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 +
-                       (size_t)E * RW * 4;
+                       (size_t)E * RW * 4 + (size_t)rows * kMaxTopK * 4 + 2 * kRouterWarps * 4;
   const size_t xslice = (size_t)kRowBlock * kRouterChunks * 32 * 16;
   return route > xslice ? route : xslice;
 }
