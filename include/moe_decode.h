@@ -159,11 +159,13 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
                          float* stream_host, uint16_t* out_host, void* cuda_stream);
 
 /* One layer-step with a CUDA event recorded on `cuda_stream` around each of
- * its kernels (boundary, router, pooler gather, experts gate/up, experts
- * down), launched without programmatic overlap so each duration is that
- * kernel's alone.  Synchronizes, then writes the five durations (ms) to
- * kernel_ms_host[5] (the pooler gather is 0 when the build has no such
- * kernel).  For measurement only; not capturable. */
+ * its kernels, launched without programmatic overlap so each duration is
+ * that kernel's alone.  Synchronizes, then writes five durations (ms) to
+ * kernel_ms_host[5]: boundary, router, pooler gather, routed experts, and a
+ * fifth slot.  The tensor-core build runs gate/up and down in one kernel
+ * (slot 3 holds both, slot 4 is 0); the CUDA-core build has no pooler
+ * gather (slot 2 is 0) and times gate/up (slot 3) and down (slot 4)
+ * separately.  For measurement only; not capturable. */
 int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_t* branch,
                              float* stream, void* cuda_stream, float* kernel_ms_host);
 

@@ -329,6 +329,8 @@ size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims
   ws.x_pool = carve<uint8_t>(cur, R * k * H / 2);
   ws.x_lines = carve<uint8_t>(cur, R * k * (H / 64) * 16);
   ws.h_lines = carve<uint8_t>(cur, R * k * (I / 64) * 16);
+  ws.act_info = carve<unsigned>(cur, E);
+  ws.ready_info = carve<unsigned>(cur, E);
   ws.counters = carve<unsigned>(cur, 4);
   ws.err = carve<unsigned>(cur, 1);
   return (size_t)(cur - base);
@@ -394,20 +396,19 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   if (e != cudaSuccess) return cuda_fail(e, "pool launch");
   mark(3);
 
+  // gate/up and down in one persistent launch
   moe::TcParams tg = h->tgu;
   tg.sfa = h->sfa13[layer];
   tg.gscale = w.w_gscale;
   tg.ws = h->ws;
-  e = moe::launch_tc_experts(tg, h->tm_w13[layer], h->tm_xpool, h->tm_xlines, h->num_sms, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
-  mark(4);
-
   moe::TcParams td = h->tdn;
   td.sfa = h->sfa2[layer];
   td.gscale = w.w_gscale;
   td.ws = h->ws;
-  e = moe::launch_tc_experts(td, h->tm_w2[layer], h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  e = moe::launch_tc_moe(tg, h->tm_w13[layer], h->tm_xpool, h->tm_xlines, td, h->tm_w2[layer],
+                         h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "experts launch");
+  mark(4);
   mark(5);
   return MOE_OK;
 #else
@@ -559,7 +560,7 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     return rc;
   }
 #if MOE_EXPERT_TC
-  e = moe::tc_set_smem(std::max(moe::tc_smem_bytes(h->tgu), moe::tc_smem_bytes(h->tdn)));
+  e = moe::tc_set_smem(moe::tc_moe_smem_bytes(h->tgu, h->tdn));
 #else
   e = moe::expert_set_smem(std::max(moe::expert_smem_bytes(h->gu), moe::expert_smem_bytes(h->dn)));
 #endif
@@ -726,6 +727,7 @@ int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_
     if (!rc) e = cudaEventSynchronize(ev[5]);
     for (int i = 0; i < 5 && !rc && e == cudaSuccess; ++i)
       e = cudaEventElapsedTime(&kernel_ms_host[i], ev[i], ev[i + 1]);
+    if (MOE_EXPERT_TC && !rc) kernel_ms_host[4] = 0.0f;  // gate/up and down share slot 3
   }
   for (int i = 0; i < 6; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);
@@ -777,7 +779,7 @@ int moe_decode_last_error(moe_decode_t* h) {
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
 
 int moe_decode_step_kernel_count(const moe_decode_t* h) {
-  return h ? (MOE_EXPERT_TC ? 5 : 4) * h->d.n_layers + 1 : 0;
+  return h ? 4 * h->d.n_layers + 1 : 0;
 }
 
 void moe_decode_destroy(moe_decode_t* h) {

@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kTcMaxThreads = 32 * (1 + 4 + 4);  // producer, up to 4 MMA issuers, 4 epilogue warps
 constexpr int kEpiThreads = 128;
-constexpr int kExpertTableTc = 64;
 constexpr int kMaxPairsTc = 128;
 constexpr int kTcCtrl = 4096;             // barriers, tables, flags
 
@@ -134,19 +133,6 @@ __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
@@ -161,15 +147,19 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 
 // ------------------------------------------------------------ shared memory
 
+constexpr int kItemRing = 4;  // items published ahead by the producer
+
 struct TcSmem {
-  uint64_t* full;       // [NS][Q]   TMA bytes landed, one barrier per stage and K-phase group
-  uint64_t* empty;      // [NS]      every issuer that reads the stage is done (T arrivals)
-  uint64_t* acc_full;   // [2]       accumulators ready for the epilogue (P arrivals)
-  uint64_t* acc_empty;  // [2]       epilogue done reading them (4 arrivals)
-  uint64_t* slot_free;  // [4][2]    an issuer's scale slot may be overwritten
-  uint64_t* drain;      // [4]       every MMA of an issuer done
-  int4* etab;           // [kExpertTableTc]
-  int* pairs;           // [kMaxPairsTc]
+  uint64_t* full;        // [NS][Q]   TMA bytes landed, one barrier per stage and K-phase group
+  uint64_t* empty;       // [NS]      every issuer that reads the stage is done (T arrivals)
+  uint64_t* acc_full;    // [2]       accumulators ready for the epilogue (P arrivals)
+  uint64_t* acc_empty;   // [2]       epilogue done reading them (4 arrivals)
+  uint64_t* slot_free;   // [4][2]    an issuer's scale slot may be overwritten
+  uint64_t* drain;       // [4]       every MMA of an issuer done
+  uint64_t* item_full;   // [kItemRing]  an item published by the producer
+  uint64_t* item_empty;  // [kItemRing]  read by every issuer and the epilogue (P + 1 arrivals)
+  int4* items;           // [kItemRing]  (item, expert, first pooled position, pairs); item < 0: end
+  int* pairs;            // [kMaxPairsTc]
   int* flag;
   uint32_t* tmem_base;
   uint8_t* stages;
@@ -182,23 +172,66 @@ __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
   s.acc_full = s.empty + 16;
   s.acc_empty = s.acc_full + 2;
   s.slot_free = s.acc_empty + 2;
-  s.drain = s.slot_free + 8;
-  s.etab = reinterpret_cast<int4*>(base + 512);
-  s.pairs = reinterpret_cast<int*>(base + 512 + kExpertTableTc * 16);
+  s.drain = s.slot_free + 8;                 // 64 barriers: 512 bytes
+  s.item_full = reinterpret_cast<uint64_t*>(base + 512);
+  s.item_empty = s.item_full + kItemRing;
+  s.items = reinterpret_cast<int4*>(base + 576);
+  s.pairs = reinterpret_cast<int*>(base + 640);
   s.flag = s.pairs + kMaxPairsTc;
   s.tmem_base = reinterpret_cast<uint32_t*>(s.flag + 4);
   s.stages = base + kTcCtrl;
   return s;
 }
 
-__device__ __forceinline__ int4 tc_item_expert(const TcParams& p, const TcSmem& sm, int it,
-                                               int ai_first) {
-  const int ai = it / p.tiles, q = ai - ai_first;
-  if (q < kExpertTableTc) return sm.etab[q];
-  const int e = __ldcg(p.ws.active + ai);
-  const bool ok = e >= 0 && e < p.E;
-  const int pos0 = ok ? __ldcg(p.ws.offset + e) : 0;
-  return make_int4(e, pos0, ok ? __ldcg(p.ws.offset + e + 1) - pos0 : 0, 0);
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Every barrier of one projection's pipeline (init, or inval before the
+// shared memory takes the other projection's layout).
+__device__ void tc_barriers(const TcParams& p, const TcSmem& sm, bool init) {
+  auto one = [&](uint64_t* b, uint32_t count) {
+    if (init)
+      mbar_init(b, count);
+    else
+      mbar_inval(b);
+  };
+  for (int s = 0; s < p.NS; ++s) {
+    for (int q = 0; q < p.Q; ++q) one(&sm.full[s * p.Q + q], 1);
+    one(&sm.empty[s], (uint32_t)p.T);
+  }
+  for (int b = 0; b < 2; ++b) {
+    one(&sm.acc_full[b], (uint32_t)p.P);
+    one(&sm.acc_empty[b], kEpiThreads / 32);
+  }
+  for (int i = 0; i < 8; ++i) one(&sm.slot_free[i], 1);
+  for (int i = 0; i < 4; ++i) one(&sm.drain[i], 1);
+  for (int r = 0; r < kItemRing; ++r) {
+    one(&sm.item_full[r], 1);
+    one(&sm.item_empty[r], (uint32_t)p.P + 1);
+  }
+  if (init) mbar_fence_init();
+}
+
+__device__ __forceinline__ int4 unpack_expert(unsigned w) {
+  const unsigned v = w - 1u;
+  return make_int4((int)(v & 1023u), (int)((v >> 10) & 4095u), (int)(v >> 22), 0);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* ptr, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy global writes before later async-proxy
+// (TMA) accesses that synchronize with them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ bool tc_item_ok(const TcParams& p, int4 et) {
@@ -206,14 +239,58 @@ __device__ __forceinline__ bool tc_item_ok(const TcParams& p, int4 et) {
          et.y + et.z <= p.ws_pairs;
 }
 
+// Gate/up item it: tile it % tiles of active expert it / tiles.
+__device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, int it) {
+  const unsigned w = __ldcg(p.ws.act_info + it / p.tiles);
+  return w ? unpack_expert(w) : make_int4(-1, 0, 0, 0);
+}
+
+// Down item it: tile it % tiles of the (it / tiles)-th expert whose h became
+// ready.  Waits (bounded) until that expert is published; the acquire and the
+// proxy fence make its h codes and scale lines visible to the TMA.
+__device__ __forceinline__ bool tc_resolve_down(const TcParams& p, int it, int4& et) {
+  const unsigned* slot = p.ws.ready_info + it / p.tiles;
+  unsigned w = ld_acquire_u32(slot);
+  if (!w) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+      w = ld_acquire_u32(slot);
+      if (w) break;
+      if ((i & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+  fence_proxy_async_global();
+  et = unpack_expert(w);
+  return true;
+}
+
+// Producer side of the item ring: publish item j (bounded wait for the slot).
+__device__ __forceinline__ bool ring_put(const TcSmem& sm, int j, int4 v) {
+  const int r = j % kItemRing;
+  if (j >= kItemRing && !mbar_wait(&sm.item_empty[r], (uint32_t)((j / kItemRing) - 1) & 1u))
+    return false;
+  sm.items[r] = v;
+  mbar_arrive(&sm.item_full[r]);
+  return true;
+}
+
+// One consumer thread's read of item j.
+__device__ __forceinline__ bool ring_get(const TcSmem& sm, int j, int4& v) {
+  const int r = j % kItemRing;
+  if (!mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u)) return false;
+  v = sm.items[r];
+  mbar_arrive(&sm.item_empty[r]);
+  return true;
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// Barrier over the four epilogue warps only (threads 64..191).
+// Barrier over the four epilogue warps only.
 __device__ __forceinline__ void tc_named_sync() { named_bar(2, kEpiThreads); }
 
 // The last CTA to finish an expert's gate/up tiles quantizes its h rows (one
 // NVFP4 tensor per expert): codes, block scales and the per-MMA scale lines
-// the down kernel streams as its B-operand scales.
+// the down projection streams as its B-operand scales.
 __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne, int t) {
   const Workspace& ws = p.ws;
   const float amax = __uint_as_float(__ldcg(ws.h_amax + e));
@@ -249,77 +326,49 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
   if (t == 0) ws.h_sg[e] = sg;
 }
 
-}  // namespace
+// Gate/up epilogue: this CTA has finished `tiles` tiles of expert e.  Adds
+// its max |h| and tile count; the CTA that completes the expert quantizes h
+// and publishes the expert to the down projection.
+__device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int pos0, int ne,
+                                 int tiles, float amax_part, int t) {
+  const Workspace& ws = p.ws;
+  const float am = warp_max(amax_part);
+  if ((t & 31) == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + e, am);
+  __threadfence();
+  tc_named_sync();
+  if (t == 0) {
+    const unsigned old = atomicAdd(ws.done + e, (unsigned)tiles);
+    *sm.flag = (old + (unsigned)tiles == (unsigned)p.tiles);
+  }
+  tc_named_sync();
+  if (*reinterpret_cast<volatile int*>(sm.flag)) {
+    __threadfence();
+    tc_quantize_expert_h(p, e, pos0, ne, t);
+    fence_proxy_async_global();
+    __threadfence();
+    tc_named_sync();
+    if (t == 0) {
+      ws.done[e] = 0u;
+      ws.h_amax[e] = 0u;
+      const unsigned slot = atomicAdd(ws.counters + 3, 1u);
+      if (slot < (unsigned)p.E) st_release_u32(ws.ready_info + slot, pack_expert(e, pos0, ne));
+    }
+  }
+  tc_named_sync();
+}
 
 // ======================================================================
-// The expert kernel.  Warp 0: TMA producer.  Warps 1..P: MMA issuers (issuer
-// i = type ty * Q + phase q: accumulator type ty -- gate or up -- and the
-// K-blocks kb = q mod Q).  Warps P+1..P+4: epilogue.
+// One projection's pipeline over dynamically claimed items.  Warp 0:
+// producer (claims items, streams their stages); warps 1..P: MMA issuers
+// (issuer i = type ty * Q + phase q: accumulator type ty -- gate or up --
+// and the stages ks = q mod Q); warps epi0..epi0+3: epilogue.  Issuer warps
+// beyond this projection's P sit the projection out.
 template <bool kGU>
-__global__ void __launch_bounds__(kTcMaxThreads, 1)
-    tc_expert_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_a,
-                     const __grid_constant__ CUtensorMap tm_b,
-                     const __grid_constant__ CUtensorMap tm_sfb) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 128B-swizzled TMA tiles need 1024-byte aligned destinations: align the
-  // base explicitly (the launch adds 1 KB of slack for this)
-  uint8_t* smem_base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const TcSmem sm = tc_carve(smem_base);
+__device__ void tc_phase(const TcParams& p, const CUtensorMap* tm_a, const CUtensorMap* tm_b,
+                         const CUtensorMap* tm_sfb, const TcSmem& sm, uint32_t tmem, int n_items,
+                         int epi0) {
   const Workspace& ws = p.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int P = p.P;
-
-  // A stage is read by the issuers of K-phase group q = kb mod Q.  When NS is
-  // not a multiple of Q the group changes from one fill of a stage to the
-  // next, and a parity wait by an issuer that skipped a phase would match the
-  // stale parity of the fill before.  So each (stage, group) has its own
-  // full barrier: every phase of it is consumed by the same issuers, and each
-  // waiter tracks that barrier's parity itself.
-  if (tid == 0) {
-    for (int s = 0; s < p.NS; ++s) {
-      for (int q = 0; q < p.Q; ++q) mbar_init(&sm.full[s * p.Q + q], 1);
-      mbar_init(&sm.empty[s], p.T);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.acc_full[b], P);
-      mbar_init(&sm.acc_empty[b], kEpiThreads / 32);
-    }
-    for (int i = 0; i < 8; ++i) mbar_init(&sm.slot_free[i], 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&sm.drain[i], 1);
-    mbar_fence_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(sm.tmem_base)),
-                 "r"(512));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // Gate/up waits for the routing and the pooled MoE input before anything;
-  // down's producer issues its first weight tiles before waiting.
-  if (kGU) {
-    grid_dep_wait();
-    grid_dep_launch();
-  }
-  const int na = __ldcg(ws.n_active);
-  const bool na_ok = na >= 0 && na <= p.E;
-  const int n_items = na_ok ? na * p.tiles : 0;
-  const int it0 = (int)((long long)blockIdx.x * n_items / gridDim.x);
-  const int it1 = (int)((long long)(blockIdx.x + 1) * n_items / gridDim.x);
-  const int ai_first = it1 > it0 ? it0 / p.tiles : 0;
-  const int nai = it1 > it0 ? (it1 - 1) / p.tiles - ai_first + 1 : 0;
-  for (int q = tid; q < nai && q < kExpertTableTc; q += blockDim.x) {
-    const int e = __ldcg(ws.active + ai_first + q);
-    const bool ok = e >= 0 && e < p.E;
-    const int pos0 = ok ? __ldcg(ws.offset + e) : 0;
-    sm.etab[q] = make_int4(e, pos0, ok ? __ldcg(ws.offset + e + 1) - pos0 : 0, 0);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *sm.tmem_base;
-  if (!na_ok && tid == 0) latch_error(ws.err, kDevBadRouting);
-
   const int KB = p.KBLK;      // K-blocks of 256 per item
   const int KPS = p.KPS;      // K-blocks per stage
   const int KS = p.KSTEPS;    // stages per item
@@ -328,16 +377,32 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int g = 0;  // global stage counter = item * KS + ks
+      unsigned* claim = ws.counters + (kGU ? 1 : 2);
+      int g = 0;           // stages issued = item * KS + ks
       uint32_t fbits = 0;  // per (stage, group) full barrier: parity of fills issued
       bool ok = true;
-      bool waited = kGU;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const int4 et = tc_item_expert(p, sm, it, ai_first);
-        if (!tc_item_ok(p, et)) {
-          latch_error(ws.err, kDevBadRouting);
+      int it = (int)atomicAdd(claim, 1u);
+      for (int j = 0;; ++j) {
+        int4 et = make_int4(-1, 0, 0, 0);
+        bool live = ok && it < n_items;
+        if (live) {
+          if (kGU) {
+            et = tc_resolve_gate_up(p, it);
+          } else if (!tc_resolve_down(p, it, et)) {
+            latch_error(ws.err, kDevWaitTimeout);
+            live = ok = false;
+          }
+          if (live && !tc_item_ok(p, et)) {
+            latch_error(ws.err, kDevBadRouting);
+            live = ok = false;
+          }
+        }
+        if (!ring_put(sm, j, live ? make_int4(it, et.x, et.y, et.z) : make_int4(-1, 0, 0, 0))) {
+          latch_error(ws.err, kDevWaitTimeout);
           break;
         }
+        if (!live) break;
+        const int nxt = (int)atomicAdd(claim, 1u);  // its latency hides under this item
         const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
         const int nt = (ne + 31) / 32;
         for (int ks = 0; ks < KS; ++ks, ++g) {
@@ -362,64 +427,63 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
           mbar_arrive_expect_tx(full, bytes);
           // gate rows (gate/up) or output rows (down) of this tile
           if (KPS == 1)
-            tma_2d(st, &tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
+            tma_2d(st, tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
           else
-            tma_3d_hint(st, &tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
+            tma_3d_hint(st, tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
           bulk_g2s_plain(st + p.off_sfa,
                          p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, sfa_b,
                          full);
           if (kGU) {  // gate/up stages hold one K-block
             const int ru = p.I / 128 + tile;  // up rows follow the gate rows
-            tma_2d(st + 16384, &tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
+            tma_2d(st + 16384, tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
             bulk_g2s_plain(st + p.off_sfa + 2048,
                            p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
                            full);
           }
-          if (!waited) {  // down: h and its scales come from the gate/up kernel
-            grid_dep_wait();
-            grid_dep_launch();
-            waited = true;
-          }
           for (int t = 0; t < nt; ++t) {
             if (KPS == 1)
-              tma_2d_plain(st + p.off_b + t * 4096, &tm_b, kb * 128, pos0 + 32 * t, full);
+              tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, pos0 + 32 * t, full);
             else
-              tma_3d(st + p.off_b + t * 4096 * KPS, &tm_b, 0, pos0 + 32 * t, kb, full);
-            tma_3d(st + p.off_sfb + t * 2048 * KPS, &tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
+              tma_3d(st + p.off_b + t * 4096 * KPS, tm_b, 0, pos0 + 32 * t, kb, full);
+            tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
           }
         }
+        it = nxt;
       }
-      if (!waited) {
-        grid_dep_wait();
-        grid_dep_launch();
-      }
-      // every issued copy lands before the CTA may exit: the last fill of a
-      // stage was issued only after every earlier fill of it had been consumed
+      // every issued copy lands before the pipeline is torn down: the last
+      // fill of a stage was issued only after every earlier fill of it had
+      // been consumed
       for (int s = 0; s < p.NS && s < g; ++s) {
         const int last = s + p.NS * ((g - 1 - s) / p.NS);
         const int fb = s * p.Q + (last % KS) % p.Q;
         if (!mbar_wait(&sm.full[fb], ((fbits >> fb) & 1u) ^ 1u)) latch_error(ws.err, kDevWaitTimeout);
       }
+      // and the issuers' releases of every stage have arrived (no commit may
+      // land on a barrier after it is re-initialised for the next projection)
+      if (ok)
+        for (int s = 0; s < p.NS && s < g; ++s)
+          if (!mbar_wait(&sm.empty[s], (uint32_t)((g - 1 - s) / p.NS) & 1u))
+            latch_error(ws.err, kDevWaitTimeout);
     }
-  } else if (warp <= P) {
+  } else if (warp <= p.P) {
     // --------------------------------------------------------- MMA issuers
-    if (!kGU) {
-      grid_dep_wait();
-      grid_dep_launch();
-    }
     const int i = warp - 1;
     const int ty = i / p.Q, q = i % p.Q;
     if (lane == 0) {
       const uint32_t ibase = tmem + (uint32_t)i * p.issuer_cols;
-      int c = 0, item = 0;  // stages handled, items seen
-      uint32_t fpar = 0;    // bit s: parity of this group's next phase of full[s][q]
+      int c = 0;          // stages handled
+      uint32_t fpar = 0;  // bit s: parity of this group's next phase of full[s][q]
       bool ok = true;
-      for (int it = it0; it < it1 && ok; ++it, ++item) {
-        const int4 et = tc_item_expert(p, sm, it, ai_first);
-        if (!tc_item_ok(p, et)) break;
-        const int nt = (et.z + 31) / 32;
-        const int ab = (p.dbuf == 2) ? (item & 1) : 0;
-        const int use = (p.dbuf == 2) ? (item >> 1) : item;
+      for (int j = 0; ok; ++j) {
+        int4 v;
+        if (!ring_get(sm, j, v)) {
+          latch_error(ws.err, kDevWaitTimeout);
+          break;
+        }
+        if (v.x < 0) break;
+        const int nt = (v.w + 31) / 32;
+        const int ab = (p.dbuf == 2) ? (j & 1) : 0;
+        const int use = (p.dbuf == 2) ? (j >> 1) : j;
         if (use >= 1 && !mbar_wait(&sm.acc_empty[ab], (use - 1) & 1)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
@@ -428,7 +492,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         const uint32_t dcol = ibase + (uint32_t)ab * p.acc_cols;
         bool first = true;
         for (int ks = q; ks < KS; ks += p.Q, ++c) {
-          const int g = item * KS + ks;
+          const int g = j * KS + ks;
           const int nkb = min(KPS, KB - ks * KPS);
           const int s = g % p.NS;
           const uint32_t par = (fpar >> s) & 1u;
@@ -472,53 +536,45 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
         }
         if (ok) tc_commit(&sm.acc_full[ab]);  // also when this phase had no K-block
       }
-      // everything this thread issued completes before TMEM is released
+      // everything this thread issued completes before the pipeline is torn
+      // down, and the commits to its scale slots have arrived
       tc_commit(&sm.drain[i]);
       if (!mbar_wait(&sm.drain[i], 0)) latch_error(ws.err, kDevWaitTimeout);
+      if (ok)
+        for (int sl = 0; sl < p.sfslots && sl < c; ++sl)
+          if (!mbar_wait(&sm.slot_free[i * 2 + sl], (uint32_t)((c - 1 - sl) / p.sfslots) & 1u))
+            latch_error(ws.err, kDevWaitTimeout);
     }
-  } else {
+  } else if (warp >= epi0) {
     // ----------------------------------------------------------- epilogue
-    if (!kGU) {
-      grid_dep_wait();
-      grid_dep_launch();
-    }
-    const int t = tid - 32 * (P + 1);   // 0..127
+    const int t = tid - 32 * epi0;      // 0..127
     const int qd = warp & 3;            // TMEM lane quadrant of this warp
     const int m = 32 * qd + lane;       // weight row within the tile
     const int nparts = KS < p.Q ? KS : p.Q;  // K-phase partial accumulators that exist
     const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
-    int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0, item = 0;
+    int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
-    for (int it = it0; it < it1; ++it, ++item) {
-      const int4 et = tc_item_expert(p, sm, it, ai_first);
-      if (!tc_item_ok(p, et)) break;
-      const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
+    for (int j = 0;; ++j) {
+      // the next item (one thread waits, bounded; the barrier hands the slot
+      // and the verdict to all four warps)
+      const int r = j % kItemRing;
+      if (t == 0) *sm.flag = mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u) ? 1 : 0;
+      tc_named_sync();
+      const bool have = *reinterpret_cast<volatile int*>(sm.flag) != 0;
+      const int4 v = have ? sm.items[r] : make_int4(-1, 0, 0, 0);
+      tc_named_sync();
+      if (!have) {
+        if (t == 0) latch_error(ws.err, kDevWaitTimeout);
+        break;
+      }
+      if (t == 0) mbar_arrive(&sm.item_empty[r]);
+      if (v.x < 0) break;
+      const int e = v.y, tile = v.x % p.tiles, pos0 = v.z, ne = v.w;
       if (e != cur_e) {
-        if (kGU && cur_e >= 0) {
-          // publish this CTA's share of the finished expert
-          float am = warp_max(cur_amax);
-          if (lane == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + cur_e, am);
-          __threadfence();
-          tc_named_sync();
-          if (t == 0) {
-            const unsigned old = atomicAdd(ws.done + cur_e, (unsigned)cur_tiles);
-            *sm.flag = (old + (unsigned)cur_tiles == (unsigned)p.tiles);
-          }
-          tc_named_sync();
-          if (*sm.flag) {
-            __threadfence();
-            tc_quantize_expert_h(p, cur_e, cur_pos0, cur_ne, t);
-            tc_named_sync();
-            if (t == 0) {
-              ws.done[cur_e] = 0u;
-              ws.h_amax[cur_e] = 0u;
-            }
-          }
-          tc_named_sync();
-        }
+        if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_pos0, cur_ne, cur_tiles, cur_amax, t);
         if (!kGU) {
           tc_named_sync();  // nobody still reads the previous expert's pair ids
-          for (int j = t; j < ne; j += kEpiThreads) sm.pairs[j] = __ldcg(ws.pair_order + pos0 + j);
+          for (int jj = t; jj < ne; jj += kEpiThreads) sm.pairs[jj] = __ldcg(ws.pair_order + pos0 + jj);
           tc_named_sync();
         }
         cur_e = e;
@@ -533,10 +589,8 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
           sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e);
         }
       }
-      const int ab = (p.dbuf == 2) ? (item & 1) : 0;
-      const int use = (p.dbuf == 2) ? (item >> 1) : item;
-      // one thread waits (bounded); the barrier hands its verdict to all four
-      // epilogue warps so none is left behind at a later barrier
+      const int ab = (p.dbuf == 2) ? (j & 1) : 0;
+      const int use = (p.dbuf == 2) ? (j >> 1) : j;
       if (t == 0) *sm.flag = mbar_wait(&sm.acc_full[ab], use & 1) ? 1 : 0;
       tc_named_sync();
       const bool got = *reinterpret_cast<volatile int*>(sm.flag) != 0;
@@ -558,18 +612,18 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
 #pragma unroll
           for (int n = 0; n < 16; ++n) acc0[n] = acc1[n] = 0.0f;
           for (int qq = 0; qq < nparts; ++qq) {
-            uint32_t r[16];
-            tc_ld16(tmem + lanes + (uint32_t)qq * p.issuer_cols + (uint32_t)ab * p.acc_cols + c0, r);
+            uint32_t rr[16];
+            tc_ld16(tmem + lanes + (uint32_t)qq * p.issuer_cols + (uint32_t)ab * p.acc_cols + c0, rr);
             tc_wait_ld();
 #pragma unroll
-            for (int n = 0; n < 16; ++n) acc0[n] += __uint_as_float(r[n]);
+            for (int n = 0; n < 16; ++n) acc0[n] += __uint_as_float(rr[n]);
             if (kGU) {
               tc_ld16(tmem + lanes + (uint32_t)(p.Q + qq) * p.issuer_cols +
                           (uint32_t)ab * p.acc_cols + c0,
-                      r);
+                      rr);
               tc_wait_ld();
 #pragma unroll
-              for (int n = 0; n < 16; ++n) acc1[n] += __uint_as_float(r[n]);
+              for (int n = 0; n < 16; ++n) acc1[n] += __uint_as_float(rr[n]);
             }
           }
           if (kGU) {
@@ -598,27 +652,74 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
       if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
       ++cur_tiles;
     }
-    if (kGU && cur_e >= 0) {
-      float am = warp_max(cur_amax);
-      if (lane == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + cur_e, am);
-      __threadfence();
-      tc_named_sync();
-      if (t == 0) {
-        const unsigned old = atomicAdd(ws.done + cur_e, (unsigned)cur_tiles);
-        *sm.flag = (old + (unsigned)cur_tiles == (unsigned)p.tiles);
-      }
-      tc_named_sync();
-      if (*sm.flag) {
-        __threadfence();
-        tc_quantize_expert_h(p, cur_e, cur_pos0, cur_ne, t);
-        tc_named_sync();
-        if (t == 0) {
-          ws.done[cur_e] = 0u;
-          ws.h_amax[cur_e] = 0u;
-        }
-      }
-    }
+    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_pos0, cur_ne, cur_tiles, cur_amax, t);
   }
+}
+
+}  // namespace
+
+// ======================================================================
+// Routed experts of one layer in one persistent launch: every CTA claims
+// gate/up items until they run out, then down items.  An expert's down items
+// are handed out in the order experts' h became ready, so CTAs that finish
+// gate/up early stream down weights instead of idling.  A CTA only ever
+// waits for gate/up work that running CTAs have already claimed, and gate/up
+// work waits for nothing, so the launch needs no co-residency guarantee.
+__global__ void __launch_bounds__(kTcMaxThreads, 1)
+    tc_moe_kernel(const __grid_constant__ TcParams pg, const __grid_constant__ CUtensorMap g_a,
+                  const __grid_constant__ CUtensorMap g_b, const __grid_constant__ CUtensorMap g_sfb,
+                  const __grid_constant__ TcParams pd, const __grid_constant__ CUtensorMap d_a,
+                  const __grid_constant__ CUtensorMap d_b, const __grid_constant__ CUtensorMap d_sfb) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128B-swizzled TMA tiles need 1024-byte aligned destinations: align the
+  // base explicitly (the launch adds 1 KB of slack for this)
+  uint8_t* smem_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const TcSmem sm = tc_carve(smem_base);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int epi0 = 1 + (pg.P > pd.P ? pg.P : pd.P);
+
+  // A stage is read by the issuers of K-phase group q = ks mod Q.  When NS is
+  // not a multiple of Q the group changes from one fill of a stage to the
+  // next, and a parity wait by an issuer that skipped a phase would match the
+  // stale parity of the fill before.  So each (stage, group) has its own
+  // full barrier: every phase of it is consumed by the same issuers, and each
+  // waiter tracks that barrier's parity itself.
+  if (tid == 0) tc_barriers(pg, sm, true);
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(sm.tmem_base)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // the routing, the pooled MoE input and the item counters come from the
+  // kernels before
+  grid_dep_wait();
+  grid_dep_launch();
+  const int na = __ldcg(pg.ws.n_active);
+  const bool na_ok = na >= 0 && na <= pg.E;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_base;
+  if (!na_ok && tid == 0) latch_error(pg.ws.err, kDevBadRouting);
+  const int n_act = na_ok ? na : 0;
+
+  tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0);
+
+  // this CTA's gate/up copies have landed, its MMAs completed and its
+  // accumulators been read: the shared memory takes the down layout
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    tc_barriers(pg, sm, false);
+    tc_barriers(pd, sm, true);
+  }
+  __syncthreads();
+
+  tc_phase<false>(pd, &d_a, &d_b, &d_sfb, sm, tmem, n_act * pd.tiles, epi0);
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -668,32 +769,35 @@ __global__ void sf_atoms_kernel(const uint8_t* __restrict__ sf, int64_t rows, in
   }
 }
 
-cudaError_t launch_tc_experts(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b,
-                              const CUtensorMap& sfb, int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_tc_moe(const TcParams& gu, const CUtensorMap& gu_a, const CUtensorMap& gu_b,
+                          const CUtensorMap& gu_sfb, const TcParams& dn, const CUtensorMap& dn_a,
+                          const CUtensorMap& dn_b, const CUtensorMap& dn_sfb, int grid,
+                          cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(32 * (1 + p.P + 4), 1, 1);
-  cfg.dynamicSmemBytes = tc_smem_bytes(p);
+  cfg.blockDim = dim3(32 * (1 + (gu.P > dn.P ? gu.P : dn.P) + 4), 1, 1);
+  cfg.dynamicSmemBytes = tc_moe_smem_bytes(gu, dn);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.mode == kGateUp) return cudaLaunchKernelEx(&cfg, tc_expert_kernel<true>, p, a, b, sfb);
-  return cudaLaunchKernelEx(&cfg, tc_expert_kernel<false>, p, a, b, sfb);
+  return cudaLaunchKernelEx(&cfg, tc_moe_kernel, gu, gu_a, gu_b, gu_sfb, dn, dn_a, dn_b, dn_sfb);
 }
 
 cudaError_t tc_set_smem(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc_moe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)bytes);
 }
 
 size_t tc_smem_bytes(const TcParams& p) {
   return 1024 + (size_t)kTcCtrl + (size_t)p.NS * p.stage_stride;  // + alignment slack
+}
+
+size_t tc_moe_smem_bytes(const TcParams& gu, const TcParams& dn) {
+  const size_t a = tc_smem_bytes(gu), b = tc_smem_bytes(dn);
+  return a > b ? a : b;
 }
 
 size_t tc_ctrl_bytes() { return (size_t)kTcCtrl; }

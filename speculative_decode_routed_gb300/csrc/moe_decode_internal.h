@@ -8,6 +8,13 @@
 
 namespace moe {
 
+// One expert's routing summary in a word: 1 + (expert | first pooled
+// position << 10 | pairs << 22); 0 means "not published".  Experts < 1024,
+// pooled positions < 4096, pairs < 256.
+__host__ __device__ inline unsigned pack_expert(int e, int pos0, int ne) {
+  return 1u + ((unsigned)e | ((unsigned)pos0 << 10) | ((unsigned)ne << 22));
+}
+
 // Device-side error codes latched into the workspace error word.
 enum DeviceError : unsigned {
   kDevOk = 0,
@@ -43,7 +50,10 @@ struct Workspace {
   uint8_t* x_pool;       // [R*k][H/2]  MoE input codes in pooled order (tensor-core B operand)
   uint8_t* x_lines;      // [H/64][R*k][16]  its scales, one 16-byte line per row and MMA of 64
   uint8_t* h_lines;      // [I/64][R*k][16]  the same lines for h
-  unsigned* counters;    // [4]         [0] router CTA arrivals
+  unsigned* act_info;    // [E]         per active expert: packed (expert, first pooled position, pairs)
+  unsigned* ready_info;  // [E]         the same words in the order experts' h became ready (0: not yet)
+  unsigned* counters;    // [4]         [0] router CTA arrivals, [1] gate/up item claims,
+                         //             [2] down item claims, [3] experts ready
   unsigned* err;         // [1]         latched DeviceError
 };
 

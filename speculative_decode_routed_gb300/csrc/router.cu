@@ -302,8 +302,12 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
       off[e] = cex;
       ws.offset[e] = cex;
       ws.count[e] = cnt[e];
+      ws.ready_info[e] = 0u;  // the expert kernel publishes ready experts here
+      if (cnt[e] > 0) {
+        ws.act_info[aex] = pack_expert(e, cex, cnt[e]);
+        ws.active[aex++] = e;
+      }
       cex += cnt[e];
-      if (cnt[e] > 0) ws.active[aex++] = e;
     }
     if (tid == kRouterThreads - 1) {
       off[E] = cex;
@@ -323,9 +327,12 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
     ws.pair_order[pos] = q;
     ws.pos_of_pair[q] = pos;
   }
-  // ready for the next layer
+  // ready for the next layer; the expert kernel's item counters start at 0
   if (tid == 0) {
     ws.counters[0] = 0u;
+    ws.counters[1] = 0u;
+    ws.counters[2] = 0u;
+    ws.counters[3] = 0u;
     ws.x_amax[0] = 0u;
   }
 }

@@ -42,12 +42,17 @@ struct PoolParams {
   Workspace ws;
 };
 
-cudaError_t launch_tc_experts(const TcParams& p, const CUtensorMap& a, const CUtensorMap& b,
-                              const CUtensorMap& sfb, int grid, cudaStream_t s, bool pdl);
+// Gate/up and down of one layer in one persistent launch (maps: weights,
+// activation codes, activation scale lines of each projection).
+cudaError_t launch_tc_moe(const TcParams& gu, const CUtensorMap& gu_a, const CUtensorMap& gu_b,
+                          const CUtensorMap& gu_sfb, const TcParams& dn, const CUtensorMap& dn_a,
+                          const CUtensorMap& dn_b, const CUtensorMap& dn_sfb, int grid,
+                          cudaStream_t s, bool pdl);
+size_t tc_moe_smem_bytes(const TcParams& gu, const TcParams& dn);
 cudaError_t launch_pool_gather(const PoolParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_sf_atoms(const uint8_t* sf, int64_t rows, int ks, int kblk, uint8_t* out,
                             cudaStream_t s);
-cudaError_t tc_set_smem(size_t bytes);
+cudaError_t tc_set_smem(size_t bytes);  // the fused kernel's dynamic shared memory
 size_t tc_smem_bytes(const TcParams& p);
 size_t tc_ctrl_bytes();
 
