@@ -364,9 +364,9 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
 // and the stages ks = q mod Q); warps epi0..epi0+3: epilogue.  Issuer warps
 // beyond this projection's P sit the projection out.
 template <bool kGU>
-__device__ void tc_phase(const TcParams& p, const CUtensorMap* tm_a, const CUtensorMap* tm_b,
-                         const CUtensorMap* tm_sfb, const TcSmem& sm, uint32_t tmem, int n_items,
-                         int epi0) {
+__device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* tm_a,
+                                         const CUtensorMap* tm_b, const CUtensorMap* tm_sfb,
+                                         const TcSmem& sm, uint32_t tmem, int n_items, int epi0) {
   const Workspace& ws = p.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KB = p.KBLK;      // K-blocks of 256 per item
@@ -685,7 +685,13 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   // stale parity of the fill before.  So each (stage, group) has its own
   // full barrier: every phase of it is consumed by the same issuers, and each
   // waiter tracks that barrier's parity itself.
-  if (tid == 0) tc_barriers(pg, sm, true);
+  if (tid == 0) {
+    tc_barriers(pg, sm, true);
+    // every descriptor this launch will use, into the TMA unit's cache
+    const CUtensorMap* maps[6] = {&g_a, &g_b, &g_sfb, &d_a, &d_b, &d_sfb};
+    for (int i = 0; i < 6; ++i)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i])) : "memory");
+  }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(sm.tmem_base)),
