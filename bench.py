@@ -48,6 +48,29 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+# DRAM traffic (read + write) of the experts kernel per active expert, from
+# one ncu capture at serving widths with 64 experts; valid only for the
+# kernel source it was taken on (profiles/expert_kernel_tc_fused_E64.md).
+EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu",
+                   "sha256_prefix": "4cc8fc3c6dcb2366", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": 1077044056 / 43}
+
+
+def _experts_traffic(w: synth.Workload, n_active: float):
+    """Bytes per launch of the experts kernel scaled from the ncu capture, or
+    None if the kernel changed since or the widths differ."""
+    import hashlib
+    t = EXPERTS_TRAFFIC
+    try:
+        with open(os.path.join(ROOT, t["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if not digest.startswith(t["sha256_prefix"]) or (w.hidden, w.inter) != (t["hidden"], t["inter"]):
+        return None
+    return int(round(t["bytes_per_active_expert"] * n_active))
+
+
 def _algorithmic_bytes(w: synth.Workload, n_active: int, rows: int):
     """Bytes one layer-step must move at minimum (weights read once)."""
     H, I, E, k = w.hidden, w.inter, w.n_experts, w.top_k
@@ -311,7 +334,8 @@ def run_native(args, w):
         "roofline": {"kernel": "routed experts (gate/up and down, one kernel)" if fused
                      else "experts gate/up", "bound": "hbm", "achieved": round(exp_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(exp_gbs / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": _experts_traffic(w, float(np.mean([n_active[i % V] for i in range(len(prof))])))
+                     if fused else None, "peak_kind": peak_kind,
                      "launch_us": round(k_ms[3] * 1000, 2),
                      "algorithmic_bytes": int(exp_bytes.mean())},
         "kernels_us": dict({"boundary": round(k_ms[0] * 1000, 2), "router": round(k_ms[1] * 1000, 2),

@@ -187,6 +187,10 @@ WORKLOADS = {
                       zipf_bias=True),
     "stack16": Workload("stack16", rows=8, hidden=7168, n_experts=256, top_k=8, inter=2048,
                         n_layers=16),
+    # serving widths with 64 experts (~1.6 GB of weights): small enough for
+    # multi-pass profiler captures, still far larger than L2
+    "serving_e64": Workload("serving_e64", rows=8, hidden=7168, n_experts=64, top_k=8,
+                            inter=2048),
 }
 SWEEP_ROWS = (1, 8, 32, 64, 128)
 
