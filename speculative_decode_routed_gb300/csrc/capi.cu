@@ -162,8 +162,8 @@ int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
   p.tiles = gu ? d.inter / 128 : d.hidden / 128;
   p.RE = gu ? 2 * d.inter : d.hidden;
   p.row_tiles = p.RE / 128;
-  const int maxn = d.max_rows < 128 ? d.max_rows : 128;
-  p.nt_max = (maxn + 31) / 32;
+  // work items cover at most kVirtualPairs (32) pairs: one N-tile
+  p.nt_max = 1;
   p.T = gu ? 2 : 1;
   p.acc_cols = 32u * (uint32_t)p.nt_max;
   // TMEM (512 columns): as many independent MMA issuers as fit, each with its
@@ -329,8 +329,11 @@ size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims
   ws.x_pool = carve<uint8_t>(cur, R * k * H / 2);
   ws.x_lines = carve<uint8_t>(cur, R * k * (H / 64) * 16);
   ws.h_lines = carve<uint8_t>(cur, R * k * (I / 64) * 16);
-  ws.act_info = carve<unsigned>(cur, E);
-  ws.ready_info = carve<unsigned>(cur, E);
+  const size_t V = (size_t)moe::virtual_slots((int)E, (int)(R * k));
+  ws.act_info = carve<unsigned>(cur, V);
+  ws.ready_info = carve<unsigned>(cur, V);
+  ws.n_virtual = carve<int>(cur, 1);
+  ws.rg_count = carve<unsigned>(cur, 16);
   ws.counters = carve<unsigned>(cur, 4);
   ws.err = carve<unsigned>(cur, 1);
   return (size_t)(cur - base);

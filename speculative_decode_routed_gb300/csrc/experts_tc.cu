@@ -235,18 +235,19 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 __device__ __forceinline__ bool tc_item_ok(const TcParams& p, int4 et) {
-  return et.x >= 0 && et.x < p.E && et.y >= 0 && et.z >= 1 && et.z <= kMaxPairsTc &&
+  return et.x >= 0 && et.x < p.E && et.y >= 0 && et.z >= 1 && et.z <= kVirtualPairs &&
          et.y + et.z <= p.ws_pairs;
 }
 
-// Gate/up item it: tile it % tiles of active expert it / tiles.
+// Gate/up item it: tile it % tiles of virtual expert it / tiles (an active
+// expert's pairs in groups of at most 32).
 __device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, int it) {
   const unsigned w = __ldcg(p.ws.act_info + it / p.tiles);
   return w ? unpack_expert(w) : make_int4(-1, 0, 0, 0);
 }
 
-// Down item it: tile it % tiles of the (it / tiles)-th expert whose h became
-// ready.  Waits (bounded) until that expert is published; the acquire and the
+// Down item it: tile it % tiles of the (it / tiles)-th virtual expert whose h
+// became ready.  Waits (bounded) until that expert is published; the acquire and the
 // proxy fence make its h codes and scale lines visible to the TMA.
 __device__ __forceinline__ bool tc_resolve_down(const TcParams& p, int it, int4& et) {
   const unsigned* slot = p.ws.ready_info + it / p.tiles;
@@ -326,19 +327,22 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
   if (t == 0) ws.h_sg[e] = sg;
 }
 
-// Gate/up epilogue: this CTA has finished `tiles` tiles of expert e.  Adds
-// its max |h| and tile count; the CTA that completes the expert quantizes h
-// and publishes the expert to the down projection.
-__device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int pos0, int ne,
-                                 int tiles, float amax_part, int t) {
+// Gate/up epilogue: this CTA has finished `tiles` tiles of expert e (over
+// any of its virtual parts).  Adds its max |h| and tile count; the CTA that
+// completes the expert -- every tile of every part -- quantizes all of the
+// expert's h rows and publishes its parts to the down projection.
+__device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int tiles,
+                                 float amax_part, int t) {
   const Workspace& ws = p.ws;
+  const int pos0 = __ldcg(ws.offset + e), ne = __ldcg(ws.offset + e + 1) - pos0;
+  const int parts = (ne + kVirtualPairs - 1) / kVirtualPairs;
   const float am = warp_max(amax_part);
   if ((t & 31) == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + e, am);
   __threadfence();
   tc_named_sync();
   if (t == 0) {
     const unsigned old = atomicAdd(ws.done + e, (unsigned)tiles);
-    *sm.flag = (old + (unsigned)tiles == (unsigned)p.tiles);
+    *sm.flag = (old + (unsigned)tiles == (unsigned)(p.tiles * parts));
   }
   tc_named_sync();
   if (*reinterpret_cast<volatile int*>(sm.flag)) {
@@ -350,8 +354,12 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
     if (t == 0) {
       ws.done[e] = 0u;
       ws.h_amax[e] = 0u;
-      const unsigned slot = atomicAdd(ws.counters + 3, 1u);
-      if (slot < (unsigned)p.E) st_release_u32(ws.ready_info + slot, pack_expert(e, pos0, ne));
+      const unsigned slot = atomicAdd(ws.counters + 3, (unsigned)parts);
+      const unsigned cap = (unsigned)virtual_slots(p.E, p.ws_pairs);
+      for (int g = 0; g < parts; ++g)
+        if (slot + g < cap)
+          st_release_u32(ws.ready_info + slot + g,
+                         pack_expert(e, pos0 + kVirtualPairs * g, min(kVirtualPairs, ne - kVirtualPairs * g)));
     }
   }
   tc_named_sync();
@@ -552,7 +560,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
     const int m = 32 * qd + lane;       // weight row within the tile
     const int nparts = KS < p.Q ? KS : p.Q;  // K-phase partial accumulators that exist
     const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
-    int cur_e = -1, cur_pos0 = 0, cur_ne = 0, cur_tiles = 0;
+    int cur_e = -1, cur_pos0 = -1, cur_tiles = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
     for (int j = 0;; ++j) {
       // the next item (one thread waits, bounded; the barrier hands the slot
@@ -570,16 +578,17 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (t == 0) mbar_arrive(&sm.item_empty[r]);
       if (v.x < 0) break;
       const int e = v.y, tile = v.x % p.tiles, pos0 = v.z, ne = v.w;
-      if (e != cur_e) {
-        if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_pos0, cur_ne, cur_tiles, cur_amax, t);
+      // gate/up accumulates per expert (over its virtual parts); down keeps
+      // the pair ids of the current virtual part
+      if (e != cur_e || (!kGU && pos0 != cur_pos0)) {
+        if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
         if (!kGU) {
-          tc_named_sync();  // nobody still reads the previous expert's pair ids
+          tc_named_sync();  // nobody still reads the previous part's pair ids
           for (int jj = t; jj < ne; jj += kEpiThreads) sm.pairs[jj] = __ldcg(ws.pair_order + pos0 + jj);
           tc_named_sync();
         }
         cur_e = e;
         cur_pos0 = pos0;
-        cur_ne = ne;
         cur_tiles = 0;
         cur_amax = 0.0f;
         if (kGU) {
@@ -652,7 +661,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
       ++cur_tiles;
     }
-    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_pos0, cur_ne, cur_tiles, cur_amax, t);
+    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
   }
 }
 
@@ -702,8 +711,8 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   // kernels before
   grid_dep_wait();
   grid_dep_launch();
-  const int na = __ldcg(pg.ws.n_active);
-  const bool na_ok = na >= 0 && na <= pg.E;
+  const int na = __ldcg(pg.ws.n_virtual);
+  const bool na_ok = na >= 0 && na <= virtual_slots(pg.E, pg.ws_pairs);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -8,6 +8,14 @@
 
 namespace moe {
 
+// Pairs of one virtual expert: an active expert's pooled pairs in groups of
+// at most this many, so that one 32-wide MMA N-tile covers each work item.
+constexpr int kVirtualPairs = 32;
+
+__host__ __device__ inline int virtual_slots(int E, int max_pairs) {
+  return E + max_pairs / kVirtualPairs + 1;
+}
+
 // One expert's routing summary in a word: 1 + (expert | first pooled
 // position << 10 | pairs << 22); 0 means "not published".  Experts < 1024,
 // pooled positions < 4096, pairs < 256.
@@ -50,9 +58,12 @@ struct Workspace {
   uint8_t* x_pool;       // [R*k][H/2]  MoE input codes in pooled order (tensor-core B operand)
   uint8_t* x_lines;      // [H/64][R*k][16]  its scales, one 16-byte line per row and MMA of 64
   uint8_t* h_lines;      // [I/64][R*k][16]  the same lines for h
-  unsigned* act_info;    // [E]         per active expert: packed (expert, first pooled position, pairs)
-  unsigned* ready_info;  // [E]         the same words in the order experts' h became ready (0: not yet)
-  unsigned* counters;    // [4]         [0] router CTA arrivals, [1] gate/up item claims,
+  unsigned* act_info;    // [V]         per virtual expert (an active expert's pairs in groups of
+                         //             at most 32): packed (expert, first pooled position, pairs)
+  unsigned* ready_info;  // [V]         the same words in the order experts' h became ready (0: not yet)
+  int* n_virtual;        // [1]         virtual experts of the step (V = E + rows*k/32 + 1 slots)
+  unsigned* rg_count;    // [16]        router CTA arrivals per block of 8 rows
+  unsigned* counters;    // [4]         [0] router row blocks routed, [1] gate/up item claims,
                          //             [2] down item claims, [3] experts ready
   unsigned* err;         // [1]         latched DeviceError
 };

@@ -9,14 +9,15 @@
 // pooler groups the (row, slot) pairs by expert, experts ascending and rows
 // ascending within an expert.
 //
-// GB300 layout: split-K GEMV.  CTA (g, s) owns EG experts (one warp each)
-// and one H-slice; the warp holds its expert's slice of the router weights in
+// GB300 layout: split-K GEMV.  CTA (g, s, r) owns EG experts (one warp each),
+// one H-slice and one block of 8 rows; the warp holds its expert's slice of the router weights in
 // registers (fetched before the programmatic-dependency wait, since the
 // weights do not depend on the previous kernel) and writes one fp32 partial
 // per (row, expert).  Every CTA also quantizes a share of the MoE input's
-// 16-element blocks.  The last CTA to arrive (threadfence + counter, no spin)
-// sums the partials in slice order, selects the top-k per row (one warp per
-// row), and builds the pooler's arrays in shared memory.
+// 16-element blocks.  The last CTA of a row block to arrive (threadfence +
+// counter, no spin) sums its rows' partials in slice order and selects their
+// top-k (one warp per row); the last row block to finish builds the pooler's
+// arrays over every row.
 #include "common.cuh"
 
 namespace moe {
@@ -231,29 +232,55 @@ __device__ void route_row_any(const RouterParams& p, int r, float* l, int* sids)
   __syncwarp();
 }
 
-// Routing + pooler, run by the last CTA.
-__device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
+// Shared-memory carve of the routing and pooler tails.
+struct RouteSmem {
+  float* lg;        // [warps][E]
+  int* cnt;         // [E]
+  int* off;         // [E+1]
+  unsigned* mask;   // [E][RW]
+  int* sids;        // [rows * k]
+  int* wtot;        // [3][warps]
+};
+
+__device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t* smem) {
+  RouteSmem r;
+  const int RW = (p.rows + 31) / 32;
+  r.lg = reinterpret_cast<float*>(smem);
+  r.cnt = reinterpret_cast<int*>(r.lg + kRouterWarps * p.E);
+  r.off = r.cnt + p.E;
+  r.mask = reinterpret_cast<unsigned*>(r.off + p.E + 1);
+  r.sids = reinterpret_cast<int*>(r.mask + p.E * RW);
+  r.wtot = r.sids + p.rows * p.k;
+  return r;
+}
+
+// Routing of rows [r0, r0 + nr): one warp per row (nr <= warps).
+__device__ void route_rows(const RouterParams& p, const RouteSmem& rs, int r0, int nr) {
+  const int warp = threadIdx.x >> 5;
+  if (warp < nr) {
+    if (p.E <= 256)
+      route_row_small(p, r0 + warp, rs.sids);
+    else
+      route_row_any(p, r0 + warp, rs.lg + warp * p.E, rs.sids);
+  }
+}
+
+// Pooler over every row, run by the last CTA to finish routing.  The ids are
+// in shared memory when one CTA routed every row, else read back.
+__device__ void pool_all(const RouterParams& p, uint8_t* smem, bool ids_in_smem) {
   const Workspace& ws = p.ws;
   const int E = p.E, k = p.k, rows = p.rows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* lg = reinterpret_cast<float*>(smem);                       // [warps][E]
-  int* cnt = reinterpret_cast<int*>(lg + kRouterWarps * E);          // [E]
-  int* off = cnt + E;                                                // [E+1]
+  const RouteSmem rs = route_carve(p, smem);
+  int* cnt = rs.cnt;
+  int* off = rs.off;
   const int RW = (rows + 31) / 32;
-  unsigned* mask = reinterpret_cast<unsigned*>(off + E + 1);        // [E][RW]
-  int* sids = reinterpret_cast<int*>(mask + E * RW);                 // [rows * k]
-  int* wtot = sids + rows * k;                                       // [2][warps]
+  unsigned* mask = rs.mask;
+  int* sids = rs.sids;
+  int* wtot = rs.wtot;
+  if (!ids_in_smem)
+    for (int q = tid; q < rows * k; q += kRouterThreads) sids[q] = __ldcg(ws.ids + q);
 
-  // ---- routing: one warp per row
-  for (int r = warp; r < rows; r += kRouterWarps) {
-    if (E <= 256)
-      route_row_small(p, r, sids);
-    else
-      route_row_any(p, r, lg + warp * E, sids);
-  }
-  __syncthreads();
-
-  // ---- pooler
   for (int e = tid; e < E; e += kRouterThreads) {
     cnt[e] = 0;
     for (int w = 0; w < RW; ++w) mask[e * RW + w] = 0u;
@@ -273,47 +300,55 @@ __device__ void route_and_pool(const RouterParams& p, uint8_t* smem) {
     // thread owns a range of experts
     const int per = (E + kRouterThreads - 1) / kRouterThreads;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    int csum = 0, asum = 0;
+    int csum = 0, asum = 0, vsum = 0;
     for (int e = e0; e < e1; ++e) {
       csum += cnt[e];
       asum += cnt[e] > 0;
+      vsum += (cnt[e] + kVirtualPairs - 1) / kVirtualPairs;
     }
-    int ci = csum, ai = asum;
+    int ci = csum, ai = asum, vi = vsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int tc = __shfl_up_sync(0xffffffffu, ci, o);
       const int ta = __shfl_up_sync(0xffffffffu, ai, o);
+      const int tv = __shfl_up_sync(0xffffffffu, vi, o);
       if (lane >= o) {
         ci += tc;
         ai += ta;
+        vi += tv;
       }
     }
     if (lane == 31) {
       wtot[warp] = ci;
       wtot[kRouterWarps + warp] = ai;
+      wtot[2 * kRouterWarps + warp] = vi;
     }
     __syncthreads();
-    int cex = ci - csum, aex = ai - asum;
+    int cex = ci - csum, aex = ai - asum, vex = vi - vsum;
     for (int w = 0; w < warp; ++w) {
       cex += wtot[w];
       aex += wtot[kRouterWarps + w];
+      vex += wtot[2 * kRouterWarps + w];
     }
     for (int e = e0; e < e1; ++e) {
       off[e] = cex;
       ws.offset[e] = cex;
       ws.count[e] = cnt[e];
-      ws.ready_info[e] = 0u;  // the expert kernel publishes ready experts here
-      if (cnt[e] > 0) {
-        ws.act_info[aex] = pack_expert(e, cex, cnt[e]);
-        ws.active[aex++] = e;
-      }
+      if (cnt[e] > 0) ws.active[aex++] = e;
+      // the expert's work items: its pairs in groups of at most kVirtualPairs
+      for (int g0 = 0; g0 < cnt[e]; g0 += kVirtualPairs)
+        ws.act_info[vex++] = pack_expert(e, cex + g0, min(kVirtualPairs, cnt[e] - g0));
       cex += cnt[e];
     }
     if (tid == kRouterThreads - 1) {
       off[E] = cex;
       ws.offset[E] = cex;
       ws.n_active[0] = aex;
+      ws.n_virtual[0] = vex;
     }
+    // the expert kernel publishes ready experts here
+    const int V = virtual_slots(E, rows * k);
+    for (int v = tid; v < V; v += kRouterThreads) ws.ready_info[v] = 0u;
   }
   __syncthreads();
   for (int q = tid; q < npairs; q += kRouterThreads) {
@@ -344,6 +379,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * p.EG + warp;
   const int sl = blockIdx.y;
+  const int rg = blockIdx.z;  // row group: rows [r0, r0 + nr)
+  const int r0 = rg * kRowBlock, nr = min(kRowBlock, p.rows - r0);
   const int nch = p.H / 8;
   const int c0 = sl * nch / p.S, c1 = (sl + 1) * nch / p.S;
 
@@ -359,14 +396,12 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   grid_dep_wait();
   grid_dep_launch();
 
-  // rows in blocks of kRowBlock: the block's x slice is staged in shared
-  // memory with every load in flight at once, then each warp forms its
-  // expert's kRowBlock partial dot products from registers and smem
+  // this CTA's block of rows: the x slice is staged in shared memory with
+  // every load in flight at once, then each warp forms its expert's partial
+  // dot products from registers and smem
   uint4* xs = reinterpret_cast<uint4*>(smem);  // [kRowBlock][kRouterChunks * 32]
   const int nc = c1 - c0;
-  for (int r0 = 0; r0 < p.rows; r0 += kRowBlock) {
-    const int nr = min(kRowBlock, p.rows - r0);
-    __syncthreads();
+  {
     for (int i = threadIdx.x; i < nr * nc; i += kRouterThreads) {
       const int rr = i / nc, c = i % nc;
       xs[rr * (kRouterChunks * 32) + c] =
@@ -399,8 +434,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   __syncthreads();
 
   // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks
-  const int ncta = gridDim.x * gridDim.y;
-  const int cta = blockIdx.y * gridDim.x + blockIdx.x;
+  const int ncta = gridDim.x * gridDim.y * gridDim.z;
+  const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   const float sg = __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f);
   const int nblk = p.rows * (p.H / 16);
   const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
@@ -425,17 +460,32 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   }
   if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
 
-  // last CTA: routing and pooling over every row
+  // the last CTA of this row group routes its rows; the last group to finish
+  // builds the pooler over every row
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned old = atomicAdd(ws.counters, 1u);
-    s_last = (old == (unsigned)ncta - 1u);
+    const unsigned old = atomicAdd(ws.rg_count + rg, 1u);
+    s_last = (old == gridDim.x * gridDim.y - 1u);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  route_and_pool(p, smem);
+  const RouteSmem rs = route_carve(p, smem);
+  route_rows(p, rs, r0, nr);
+  __syncthreads();
+  if (threadIdx.x == 0) ws.rg_count[rg] = 0u;  // every CTA of the block has arrived
+  if (gridDim.z > 1) {  // with one row block this CTA is already the last
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned old = atomicAdd(ws.counters, 1u);
+      s_last = (old == gridDim.z - 1u);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
+  pool_all(p, smem, gridDim.z == 1);
 }
 
 }  // namespace
@@ -443,7 +493,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 size_t router_smem_bytes(int E, int rows) {
   const int RW = (rows + 31) / 32;
   const size_t route = (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 +
-                       (size_t)E * RW * 4 + (size_t)rows * kMaxTopK * 4 + 2 * kRouterWarps * 4;
+                       (size_t)E * RW * 4 + (size_t)rows * kMaxTopK * 4 + 3 * kRouterWarps * 4;
   const size_t xslice = (size_t)kRowBlock * kRouterChunks * 32 * 16;
   return route > xslice ? route : xslice;
 }
@@ -452,7 +502,7 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   const size_t smem = router_smem_bytes(p.E, p.rows);
   static_assert(kMaxTopK <= 32, "one lane per selected expert");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_eg, p.S, 1);
+  cfg.gridDim = dim3(p.n_eg, p.S, (p.rows + kRowBlock - 1) / kRowBlock);
   cfg.blockDim = dim3(kRouterThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -284,12 +284,15 @@ def test_repeated_replays_bitwise():
 ODD_SHAPES = [
     # (rows, H, E, k, I): a ragged H (cluster of 1, 12 chunks/row), a single
     # expert, k == E, a row count with many rows per expert (> 8: the
-    # multi-group path), one row
+    # multi-group path, 16 router row blocks), one row
     (5, 384, 6, 3, 384),
     (3, 128, 1, 1, 128),
     (3, 1024, 16, 16, 256),
     (128, 256, 8, 2, 128),
     (1, 512, 32, 4, 640),
+    # two experts for 128 rows: ~64 pairs each, so every expert's work is
+    # split into several 32-pair parts whose h is quantized as one tensor
+    (128, 256, 2, 1, 256),
 ]
 
 
