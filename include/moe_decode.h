@@ -163,9 +163,10 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
  * that kernel's alone.  Synchronizes, then writes five durations (ms) to
  * kernel_ms_host[5]: boundary, router, pooler gather, routed experts, and a
  * fifth slot.  The tensor-core build runs gate/up and down in one kernel
- * (slot 3 holds both, slot 4 is 0); the CUDA-core build has no pooler
- * gather (slot 2 is 0) and times gate/up (slot 3) and down (slot 4)
- * separately.  For measurement only; not capturable. */
+ * (slot 3 holds both, slot 4 is 0) and gathers a pooled copy of the MoE
+ * input only above 32 rows (slot 2 is 0 otherwise); the CUDA-core build has
+ * no pooler gather (slot 2 is 0) and times gate/up (slot 3) and down
+ * (slot 4) separately.  For measurement only; not capturable. */
 int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_t* branch,
                              float* stream, void* cuda_stream, float* kernel_ms_host);
 
@@ -180,7 +181,7 @@ int moe_decode_last_error(moe_decode_t* h);
 /* Bytes of device workspace the handle holds. */
 size_t moe_decode_workspace_bytes(const moe_decode_t* h);
 
-/* Number of kernels one moe_decode_step launches for `rows` rows. */
+/* Number of kernels one moe_decode_step of max_rows rows launches. */
 int moe_decode_step_kernel_count(const moe_decode_t* h);
 
 void moe_decode_destroy(moe_decode_t* h);

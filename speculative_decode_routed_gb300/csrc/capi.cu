@@ -94,7 +94,7 @@ struct moe_decode_s {
   moe::TcParams tgu{}, tdn{};
   std::vector<CUtensorMap> tm_w13, tm_w2;
   std::vector<uint8_t*> sfa13, sfa2;   // weight scale atoms per layer (library-owned)
-  CUtensorMap tm_xpool{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
+  CUtensorMap tm_xpool{}, tm_xcodes{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
 };
 
 namespace {
@@ -383,20 +383,26 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   rp.x = h->ws.x;
   rp.wr = reinterpret_cast<const __nv_bfloat16*>(w.router_w);
   rp.bias = w.router_bias;
+  rp.line_rows = d.max_rows * d.top_k;
   rp.ws = h->ws;
   e = moe::launch_router(rp, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   mark(2);
 
 #if MOE_EXPERT_TC
-  moe::PoolParams pp{};
-  pp.H = d.hidden;
-  pp.k = d.top_k;
-  pp.rows = rows;
-  pp.ws_pairs = d.max_rows * d.top_k;
-  pp.ws = h->ws;
-  e = moe::launch_pool_gather(pp, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+  // up to 32 rows the gate/up MMA's N holds the rows themselves: no pooled
+  // copy of the MoE input is needed
+  const bool direct = rows <= 32;
+  if (!direct) {
+    moe::PoolParams pp{};
+    pp.H = d.hidden;
+    pp.k = d.top_k;
+    pp.rows = rows;
+    pp.ws_pairs = d.max_rows * d.top_k;
+    pp.ws = h->ws;
+    e = moe::launch_pool_gather(pp, s, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+  }
   mark(3);
 
   // gate/up and down in one persistent launch
@@ -404,11 +410,13 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   tg.sfa = h->sfa13[layer];
   tg.gscale = w.w_gscale;
   tg.ws = h->ws;
+  tg.direct = direct ? 1 : 0;
   moe::TcParams td = h->tdn;
   td.sfa = h->sfa2[layer];
   td.gscale = w.w_gscale;
   td.ws = h->ws;
-  e = moe::launch_tc_moe(tg, h->tm_w13[layer], h->tm_xpool, h->tm_xlines, td, h->tm_w2[layer],
+  e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
+                         td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "experts launch");
   mark(4);
@@ -598,6 +606,7 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     const uint64_t R = (uint64_t)d.max_rows * d.top_k;
     const uint64_t H = d.hidden, I = d.inter, E = d.n_experts;
     rc = encode_rows(&h->tm_xpool, h->ws.x_pool, H / 2, R, 32);
+    if (!rc) rc = encode_rows(&h->tm_xcodes, h->ws.x_codes, H / 2, (uint64_t)d.max_rows, 32);
     if (!rc) rc = encode_lines(&h->tm_xlines, h->ws.x_lines, R, H / 64);
     const uint32_t kps = (uint32_t)h->tdn.KPS;
     if (!rc) rc = kps == 1 ? encode_rows(&h->tm_hcodes, h->ws.h_codes, I / 2, R, 32)
@@ -730,7 +739,10 @@ int moe_decode_layer_profile(moe_decode_t* h, int layer, int rows, const uint16_
     if (!rc) e = cudaEventSynchronize(ev[5]);
     for (int i = 0; i < 5 && !rc && e == cudaSuccess; ++i)
       e = cudaEventElapsedTime(&kernel_ms_host[i], ev[i], ev[i + 1]);
-    if (MOE_EXPERT_TC && !rc) kernel_ms_host[4] = 0.0f;  // gate/up and down share slot 3
+    if (MOE_EXPERT_TC && !rc) {
+      kernel_ms_host[4] = 0.0f;                  // gate/up and down share slot 3
+      if (rows <= 32) kernel_ms_host[2] = 0.0f;  // no pooler gather
+    }
   }
   for (int i = 0; i < 6; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);
@@ -782,7 +794,9 @@ int moe_decode_last_error(moe_decode_t* h) {
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
 
 int moe_decode_step_kernel_count(const moe_decode_t* h) {
-  return h ? 4 * h->d.n_layers + 1 : 0;
+  // the tensor-core build skips the pooler gather up to 32 rows
+  const int per_layer = (MOE_EXPERT_TC && h && h->d.max_rows <= 32) ? 3 : 4;
+  return h ? per_layer * h->d.n_layers + 1 : 0;
 }
 
 void moe_decode_destroy(moe_decode_t* h) {

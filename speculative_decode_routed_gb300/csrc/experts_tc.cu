@@ -143,6 +143,10 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tc_ld1(uint32_t taddr, uint32_t& r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------ shared memory
@@ -413,6 +417,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
         const int nxt = (int)atomicAdd(claim, 1u);  // its latency hides under this item
         const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
         const int nt = (ne + 31) / 32;
+        const int brow = (kGU && p.direct) ? 0 : pos0;  // first B row
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int kb = ks * KPS;  // first K-block of this stage
           const int nkb = min(KPS, KB - kb);
@@ -450,10 +455,10 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           }
           for (int t = 0; t < nt; ++t) {
             if (KPS == 1)
-              tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, pos0 + 32 * t, full);
+              tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, brow + 32 * t, full);
             else
-              tma_3d(st + p.off_b + t * 4096 * KPS, tm_b, 0, pos0 + 32 * t, kb, full);
-            tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, pos0 + 32 * t, kb * 4, full);
+              tma_3d(st + p.off_b + t * 4096 * KPS, tm_b, 0, brow + 32 * t, kb, full);
+            tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, brow + 32 * t, kb * 4, full);
           }
         }
         it = nxt;
@@ -578,17 +583,18 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (t == 0) mbar_arrive(&sm.item_empty[r]);
       if (v.x < 0) break;
       const int e = v.y, tile = v.x % p.tiles, pos0 = v.z, ne = v.w;
-      // gate/up accumulates per expert (over its virtual parts); down keeps
-      // the pair ids of the current virtual part
-      if (e != cur_e || (!kGU && pos0 != cur_pos0)) {
-        if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
-        if (!kGU) {
-          tc_named_sync();  // nobody still reads the previous part's pair ids
-          for (int jj = t; jj < ne; jj += kEpiThreads) sm.pairs[jj] = __ldcg(ws.pair_order + pos0 + jj);
-          tc_named_sync();
-        }
+      // gate/up accumulates per expert (over its virtual parts); down and
+      // direct gate/up keep the pair ids of the current virtual part
+      const bool new_e = (e != cur_e), new_part = new_e || pos0 != cur_pos0;
+      if (new_e && kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
+      if (new_part && (!kGU || p.direct)) {
+        tc_named_sync();  // nobody still reads the previous part's pair ids
+        for (int jj = t; jj < ne; jj += kEpiThreads) sm.pairs[jj] = __ldcg(ws.pair_order + pos0 + jj);
+        tc_named_sync();
+      }
+      cur_pos0 = pos0;
+      if (new_e) {
         cur_e = e;
-        cur_pos0 = pos0;
         cur_tiles = 0;
         cur_amax = 0.0f;
         if (kGU) {
@@ -610,7 +616,26 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       }
       tc_fence_after();
       const uint32_t lanes = (uint32_t)(32 * qd) << 16;
-      const int nt = (ne + 31) / 32;
+      const int nt = (kGU && p.direct) ? 0 : (ne + 31) / 32;
+      if (kGU && p.direct) {
+        // the B columns are the rows: pair jj reads the column of its row
+        for (int jj = 0; jj < ne; ++jj) {
+          const uint32_t col = (uint32_t)(sm.pairs[jj] / p.k);
+          float g = 0.0f, u = 0.0f;
+          for (int qq = 0; qq < nparts; ++qq) {
+            uint32_t ra, rb;
+            tc_ld1(tmem + lanes + (uint32_t)qq * p.issuer_cols + (uint32_t)ab * p.acc_cols + col, ra);
+            tc_ld1(tmem + lanes + (uint32_t)(p.Q + qq) * p.issuer_cols + (uint32_t)ab * p.acc_cols + col,
+                   rb);
+            tc_wait_ld();
+            g += __uint_as_float(ra);
+            u += __uint_as_float(rb);
+          }
+          const float hv = silu_f(g * sc0) * (u * sc1);
+          ws.h[(size_t)(pos0 + jj) * p.I + (size_t)tile * 128 + m] = hv;
+          cur_amax = fmaxf(cur_amax, fabsf(hv));
+        }
+      }
       for (int tt = 0; tt < nt; ++tt) {
         for (int half = 0; half < 2; ++half) {
           const int c0 = 32 * tt + 16 * half;  // first pair column of this half

@@ -56,7 +56,8 @@ struct Workspace {
   unsigned* done;        // [E]         finished gate/up tiles per expert
   float* o;              // [R*k][H]    expert outputs, pair-id order
   uint8_t* x_pool;       // [R*k][H/2]  MoE input codes in pooled order (tensor-core B operand)
-  uint8_t* x_lines;      // [H/64][R*k][16]  its scales, one 16-byte line per row and MMA of 64
+  uint8_t* x_lines;      // [H/64][R*k][16]  its scales, one 16-byte line per MMA of 64 and row
+                         //             (router; rows <= 32) or pooled position (pooler gather)
   uint8_t* h_lines;      // [I/64][R*k][16]  the same lines for h
   unsigned* act_info;    // [V]         per virtual expert (an active expert's pairs in groups of
                          //             at most 32): packed (expert, first pooled position, pairs)
@@ -92,6 +93,7 @@ struct RouterParams {
   const __nv_bfloat16* x;       // [rows][H]
   const __nv_bfloat16* wr;      // [E][H]
   const float* bias;            // [E] or null
+  int line_rows;                // row stride of the scale lines (max_rows * k)
   Workspace ws;
 };
 

@@ -433,11 +433,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   }
   __syncthreads();
 
-  // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks
+  // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks,
+  // one per thread.  Each block's scale also goes into its 16-byte scale
+  // line ([H/64][line_rows][16]: bytes 0-3 the four scales of 64 elements,
+  // the rest zero) that the tensor-core experts read when the rows
+  // themselves are the MMA's N.
   const int ncta = gridDim.x * gridDim.y * gridDim.z;
   const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   const float sg = __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f);
-  const int nblk = p.rows * (p.H / 16);
+  const int bpr = p.H / 16;
+  const int nblk = p.rows * bpr;
   const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
   for (int b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
@@ -457,6 +462,14 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
     quant_block16(v, sg, lo, hi, sb);
     *reinterpret_cast<uint2*>(ws.x_codes + (size_t)b * 8) = make_uint2(lo, hi);
     ws.x_sf[b] = (uint8_t)sb;
+    const int row = b / bpr, blk = b % bpr;
+    uint8_t* line = ws.x_lines + ((size_t)(blk / 4) * p.line_rows + row) * 16;
+    line[blk % 4] = (uint8_t)sb;
+    if (blk % 4 == 0) {
+      reinterpret_cast<uint32_t*>(line)[1] = 0u;
+      reinterpret_cast<uint32_t*>(line)[2] = 0u;
+      reinterpret_cast<uint32_t*>(line)[3] = 0u;
+    }
   }
   if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
 

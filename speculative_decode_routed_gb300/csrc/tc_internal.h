@@ -31,6 +31,8 @@ struct TcParams {
   uint32_t sfa_bytes;       // weight scale atoms per stage (2 or 4 KB)
   uint32_t off_sfa, off_b, off_sfb;  // offsets within a stage
   int ws_pairs;             // rows * k of the workspace
+  int direct;               // gate/up: B is the MoE input's rows themselves (rows <= 32), not
+                            // its pooled copy; each pair reads the accumulator column of its row
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
   Workspace ws;

@@ -248,9 +248,10 @@ def test_tiny_step_end_to_end_graph_and_host():
     dec.step_host(w.rows, bh, sh, oh)
     assert np.array_equal(sh.numpy(), eager_stream)
     assert np.array_equal(oh.view(torch.uint16).numpy(), eager_out)
-    # four kernels per layer (boundary, router, pooler gather and the experts;
-    # or boundary, router, gate/up and down), plus the final boundary
-    assert moe.moe_decode_step_kernel_count(dec.handle) == 4 * w.n_layers + 1
+    # per layer: boundary, router and the experts (tensor cores, up to 32
+    # rows: no pooler gather), or boundary, router, gate/up and down; plus
+    # the final boundary
+    assert moe.moe_decode_step_kernel_count(dec.handle) in (3 * w.n_layers + 1, 4 * w.n_layers + 1)
     dec.close()
 
 
