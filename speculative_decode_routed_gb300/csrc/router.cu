@@ -240,6 +240,7 @@ struct RouteSmem {
   unsigned* mask;   // [E][RW]
   int* sids;        // [rows * k]
   int* wtot;        // [3][warps]
+  int* pk;          // [rows * k + 4]  pair's (expert | rank << 16), 16-byte aligned
 };
 
 __device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t* smem) {
@@ -251,6 +252,8 @@ __device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t*
   r.mask = reinterpret_cast<unsigned*>(r.off + p.E + 1);
   r.sids = reinterpret_cast<int*>(r.mask + p.E * RW);
   r.wtot = r.sids + p.rows * p.k;
+  r.pk = reinterpret_cast<int*>(
+      (reinterpret_cast<uintptr_t>(r.wtot + 3 * kRouterWarps) + 15) & ~static_cast<uintptr_t>(15));
   return r;
 }
 
@@ -263,6 +266,84 @@ __device__ void route_rows(const RouterParams& p, const RouteSmem& rs, int r0, i
     else
       route_row_any(p, r0 + warp, rs.lg + warp * p.E, rs.sids);
   }
+}
+
+// After the pooler: the expert kernel's ready list and item counters start
+// empty, and the router's counters are ready for the next layer.
+__device__ void pool_reset(const RouterParams& p) {
+  const Workspace& ws = p.ws;
+  const int V = virtual_slots(p.E, p.rows * p.k);
+  for (int v = threadIdx.x; v < V; v += kRouterThreads) ws.ready_info[v] = 0u;
+  if (threadIdx.x == 0) {
+    ws.counters[0] = 0u;
+    ws.counters[1] = 0u;
+    ws.counters[2] = 0u;
+    ws.counters[3] = 0u;
+    ws.x_amax[0] = 0u;
+  }
+}
+
+// Pooler for at most kRouterThreads pairs, without scans: each pair's rank
+// among its expert's pairs, then per expert one pass over the pairs (packed
+// as expert | rank << 16, four per load) for its offset, count, active index
+// and first virtual part (a part starts at every pair whose rank is a
+// multiple of kVirtualPairs).  The results equal the scanning pooler's.
+__device__ void pool_small(const RouterParams& p, uint8_t* smem, bool ids_in_smem) {
+  const Workspace& ws = p.ws;
+  const int E = p.E, npairs = p.rows * p.k, tid = threadIdx.x;
+  const RouteSmem rs = route_carve(p, smem);
+  int* sids = rs.sids;
+  int* pk = rs.pk;
+  int* off = rs.off;
+  if (!ids_in_smem) {
+    for (int q = tid; q < npairs; q += kRouterThreads) sids[q] = __ldcg(ws.ids + q);
+    __syncthreads();
+  }
+  // pairs are in (row, slot) order, so within an expert they rank by row
+  const int eq = (tid < npairs) ? sids[tid] : -1;
+  const bool valid = eq >= 0 && eq < E;
+  int rank = 0;
+  if (valid)
+    for (int q = 0; q < tid; ++q) rank += (sids[q] == eq);
+  if (tid < ((npairs + 3) & ~3)) pk[tid] = valid ? (eq | (rank << 16)) : -1;  // -1: no expert
+  const int n_valid = __syncthreads_count(valid);
+  const int n_act = __syncthreads_count(valid && rank == 0);
+  const int n_virt = __syncthreads_count(valid && (rank % kVirtualPairs) == 0);
+  const int4* pk4 = reinterpret_cast<const int4*>(pk);
+  for (int e = tid; e < E; e += kRouterThreads) {
+    int o = 0, c = 0, a = 0, v = 0;
+    for (int q4 = 0; q4 < (npairs + 3) / 4; ++q4) {
+      const int4 w = pk4[q4];
+      const int ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ex = ws4[i] & 0xFFFF, rq = ws4[i] >> 16;  // no expert: ex 0xFFFF
+        const int lt = ex < e;
+        o += lt;
+        a += lt & (rq == 0);
+        v += lt & ((rq & (kVirtualPairs - 1)) == 0);
+        c += (ex == e);
+      }
+    }
+    off[e] = o;
+    ws.offset[e] = o;
+    ws.count[e] = c;
+    if (c > 0) ws.active[a] = e;
+    for (int g0 = 0; g0 < c; g0 += kVirtualPairs)
+      ws.act_info[v++] = pack_expert(e, o + g0, min(kVirtualPairs, c - g0));
+  }
+  if (tid == 0) {
+    ws.offset[E] = n_valid;
+    ws.n_active[0] = n_act;
+    ws.n_virtual[0] = n_virt;
+  }
+  __syncthreads();
+  if (valid) {
+    const int pos = off[eq] + rank;
+    ws.pair_order[pos] = tid;
+    ws.pos_of_pair[tid] = pos;
+  }
+  pool_reset(p);
 }
 
 // Pooler over every row, run by the last CTA to finish routing.  The ids are
@@ -346,9 +427,6 @@ __device__ void pool_all(const RouterParams& p, uint8_t* smem, bool ids_in_smem)
       ws.n_active[0] = aex;
       ws.n_virtual[0] = vex;
     }
-    // the expert kernel publishes ready experts here
-    const int V = virtual_slots(E, rows * k);
-    for (int v = tid; v < V; v += kRouterThreads) ws.ready_info[v] = 0u;
   }
   __syncthreads();
   for (int q = tid; q < npairs; q += kRouterThreads) {
@@ -362,14 +440,51 @@ __device__ void pool_all(const RouterParams& p, uint8_t* smem, bool ids_in_smem)
     ws.pair_order[pos] = q;
     ws.pos_of_pair[q] = pos;
   }
-  // ready for the next layer; the expert kernel's item counters start at 0
-  if (tid == 0) {
-    ws.counters[0] = 0u;
-    ws.counters[1] = 0u;
-    ws.counters[2] = 0u;
-    ws.counters[3] = 0u;
-    ws.x_amax[0] = 0u;
+  pool_reset(p);
+}
+
+// This CTA's share of the MoE input's NVFP4 quantization (sg: its tensor
+// scale).
+__device__ void quantize_share(const RouterParams& p, float sg) {
+  // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks,
+  // one per thread.  Each block's scale also goes into its 16-byte scale
+  // line ([H/64][line_rows][16]: bytes 0-3 the four scales of 64 elements,
+  // the rest zero) that the tensor-core experts read when the rows
+  // themselves are the MMA's N.
+  const Workspace& ws = p.ws;
+  const int ncta = gridDim.x * gridDim.y * gridDim.z;
+  const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  const int bpr = p.H / 16;
+  const int nblk = p.rows * bpr;
+  const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
+  for (int b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
+    const uint4 q0 = __ldcg(src), q1 = __ldcg(src + 1);
+    float v[16];
+    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
+    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f0 = __bfloat1622float2(h0[i]), f1 = __bfloat1622float2(h1[i]);
+      v[2 * i] = f0.x;
+      v[2 * i + 1] = f0.y;
+      v[8 + 2 * i] = f1.x;
+      v[8 + 2 * i + 1] = f1.y;
+    }
+    uint32_t lo, hi, sb;
+    quant_block16(v, sg, lo, hi, sb);
+    *reinterpret_cast<uint2*>(ws.x_codes + (size_t)b * 8) = make_uint2(lo, hi);
+    ws.x_sf[b] = (uint8_t)sb;
+    const int row = b / bpr, blk = b % bpr;
+    uint8_t* line = ws.x_lines + ((size_t)(blk / 4) * p.line_rows + row) * 16;
+    line[blk % 4] = (uint8_t)sb;
+    if (blk % 4 == 0) {
+      reinterpret_cast<uint32_t*>(line)[1] = 0u;
+      reinterpret_cast<uint32_t*>(line)[2] = 0u;
+      reinterpret_cast<uint32_t*>(line)[3] = 0u;
+    }
   }
+  if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) {
@@ -433,45 +548,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   }
   __syncthreads();
 
-  // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks,
-  // one per thread.  Each block's scale also goes into its 16-byte scale
-  // line ([H/64][line_rows][16]: bytes 0-3 the four scales of 64 elements,
-  // the rest zero) that the tensor-core experts read when the rows
-  // themselves are the MMA's N.
-  const int ncta = gridDim.x * gridDim.y * gridDim.z;
-  const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-  const float sg = __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f);
-  const int bpr = p.H / 16;
-  const int nblk = p.rows * bpr;
-  const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
-  for (int b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
-    const uint4 q0 = __ldcg(src), q1 = __ldcg(src + 1);
-    float v[16];
-    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
-    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f0 = __bfloat1622float2(h0[i]), f1 = __bfloat1622float2(h1[i]);
-      v[2 * i] = f0.x;
-      v[2 * i + 1] = f0.y;
-      v[8 + 2 * i] = f1.x;
-      v[8 + 2 * i + 1] = f1.y;
-    }
-    uint32_t lo, hi, sb;
-    quant_block16(v, sg, lo, hi, sb);
-    *reinterpret_cast<uint2*>(ws.x_codes + (size_t)b * 8) = make_uint2(lo, hi);
-    ws.x_sf[b] = (uint8_t)sb;
-    const int row = b / bpr, blk = b % bpr;
-    uint8_t* line = ws.x_lines + ((size_t)(blk / 4) * p.line_rows + row) * 16;
-    line[blk % 4] = (uint8_t)sb;
-    if (blk % 4 == 0) {
-      reinterpret_cast<uint32_t*>(line)[1] = 0u;
-      reinterpret_cast<uint32_t*>(line)[2] = 0u;
-      reinterpret_cast<uint32_t*>(line)[3] = 0u;
-    }
-  }
-  if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
+  // this CTA's share of the MoE input's quantization, before it arrives (the
+  // pooler resets max |x| for the next layer once every CTA has arrived)
+  quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
 
   // the last CTA of this row group routes its rows; the last group to finish
   // builds the pooler over every row
@@ -498,7 +577,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
     if (!s_last) return;
     __threadfence();
   }
-  pool_all(p, smem, gridDim.z == 1);
+  if (p.rows * p.k <= kRouterThreads)
+    pool_small(p, smem, gridDim.z == 1);
+  else
+    pool_all(p, smem, gridDim.z == 1);
 }
 
 }  // namespace
@@ -506,7 +588,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 size_t router_smem_bytes(int E, int rows) {
   const int RW = (rows + 31) / 32;
   const size_t route = (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 +
-                       (size_t)E * RW * 4 + (size_t)rows * kMaxTopK * 4 + 3 * kRouterWarps * 4;
+                       (size_t)E * RW * 4 + 2 * (size_t)rows * kMaxTopK * 4 + 3 * kRouterWarps * 4 + 48;
   const size_t xslice = (size_t)kRowBlock * kRouterChunks * 32 * 16;
   return route > xslice ? route : xslice;
 }
