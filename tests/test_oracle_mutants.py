@@ -1,0 +1,119 @@
+"""The oracle's pins catch plausible mistakes (no GPU).
+
+Each case plants one mistake in a copy of oracle/oracle.c, builds it into a
+temporary library, points the oracle binding at it and runs the pins that
+should notice; at least one of them must fail.  A mistake no pin notices
+would mean the oracle is pinned to itself only.  The real oracle is restored
+after every case.
+"""
+import importlib
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+
+ORACLE_DIR = os.path.dirname(os.path.abspath(oracle.__file__))
+
+# (name, text in oracle.c, planted mistake, pins: (module, test, kwargs))
+MUTANTS = [
+    ("e2m1 ties round to odd",
+     "(d == bd && (c & 1) == 0)", "(d == bd && (c & 1) == 1)",
+     [("test_oracle_formats", "test_e2m1_encode_golden", {}),
+      ("test_oracle_formats", "test_e2m1_encode_is_nearest_even_on_a_dense_grid", {})]),
+    ("bf16 truncates",
+     "double val = nearbyint(a / q) * q;", "double val = floor(a / q) * q;",
+     [("test_oracle_formats", "test_bf16_rounding_matches_torch_on_fp32_values", {}),
+      ("test_oracle_formats", "test_bf16_rounds_once_from_fp64", {})]),
+    ("tensor scale amax / 448",
+     "float sg = amax / 2688.0f;", "float sg = amax / 448.0f;",
+     [("test_oracle_quant", "test_equal_block_at_tensor_max_gives_six_and_448", {}),
+      ("test_oracle_quant", "test_codes_and_scales_are_nearest_by_brute_force", {})]),
+    ("block scale ab / 4",
+     "float q = ab / 6.0f;", "float q = ab / 4.0f;",
+     [("test_oracle_quant", "test_equal_block_at_tensor_max_gives_six_and_448", {}),
+      ("test_oracle_quant", "test_codes_and_scales_are_nearest_by_brute_force", {})]),
+    ("nibbles swapped when packing",
+     "out[i] = (uint8_t)(lo | (hi << 4));", "out[i] = (uint8_t)(hi | (lo << 4));",
+     [("test_oracle_quant", "test_low_nibble_holds_the_even_element", {})]),
+    ("nibbles swapped when unpacking",
+     "uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);",
+     "uint8_t code = (c & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4);",
+     [("test_oracle_quant", "test_dequantize_matches_format_tables", {}),
+      ("test_oracle_quant", "test_dequantization_error_bound", {})]),
+    ("branch norm without eps",
+     "double inv = 1.0 / sqrt(ms + eps);", "double inv = 1.0 / sqrt(ms);",
+     [("test_oracle_step", "test_constant_rows_closed_form", {}),
+      ("test_oracle_step", "test_norm_is_scale_free_without_eps", {})]),
+    ("post-norm weight dropped",
+     "s[h] = (float)((double)s[h] + br[h] * inv * (double)w_post[h]);",
+     "s[h] = (float)((double)s[h] + br[h] * inv);",
+     [("test_oracle_step", "test_constant_rows_closed_form", {}),
+      ("test_oracle_step", "test_norm_is_scale_free_without_eps", {})]),
+    ("top-k ties to the higher id",
+     "if (best < 0 || p[e] > p[best]) best = e;", "if (best < 0 || p[e] >= p[best]) best = e;",
+     [("test_oracle_step", "test_ties_go_to_the_lower_expert_and_are_flagged", {}),
+      ("test_oracle_step", "test_topk_brute_force_subsets", {"k": 2})]),
+    ("gates not renormalised",
+     "gates[r * k + s] = p[sel[s]] / sum;", "gates[r * k + s] = p[sel[s]];",
+     [("test_oracle_step", "test_tiny_layer_statistics", {}),
+      ("test_oracle_step", "test_topk_brute_force_subsets", {"k": 2})]),
+    ("near-tie flag threshold 1e-3",
+     "flags[r] = (uint8_t)(g < 1e-6);", "flags[r] = (uint8_t)(g < 1e-3);",
+     [("test_oracle_step", "test_ties_go_to_the_lower_expert_and_are_flagged", {}),
+      ("test_oracle_step", "test_near_tie_flag_is_the_gap_below_1e6", {})]),
+    ("silu on up instead of gate",
+     "h[(int64_t)pos * I + j] = (float)(silu(G) * U);", "h[(int64_t)pos * I + j] = (float)(G * silu(U));",
+     [("test_oracle_step", "test_single_expert_with_gate_one_is_a_dense_gated_mlp", {}),
+      ("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {})]),
+    ("down uses the up projection's scale",
+     "float sg_down = w->gscale[3 * e + 2];", "float sg_down = w->gscale[3 * e + 1];",
+     [("test_oracle_step", "test_single_expert_with_gate_one_is_a_dense_gated_mlp", {}),
+      ("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {})]),
+    ("gather without gates",
+     "acc += gates[r * k + s] * (double)o[((int64_t)r * k + s) * H + hh];",
+     "acc += (double)o[((int64_t)r * k + s) * H + hh];",
+     [("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {})]),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_libs(tmp_path_factory):
+    """Builds every mutant in parallel: name -> library path."""
+    src = open(os.path.join(ORACLE_DIR, "oracle.c")).read()
+    root = tmp_path_factory.mktemp("oracle_mutants")
+    shutil.copy(os.path.join(ORACLE_DIR, "oracle.h"), root / "oracle.h")
+    procs, libs = [], {}
+    for i, (name, old, new, _) in enumerate(MUTANTS):
+        assert src.count(old) == 1, f"mutation site of '{name}' not found once in oracle.c"
+        c = root / f"m{i}.c"
+        c.write_text(src.replace(old, new))
+        so = root / f"libm{i}.so"
+        procs.append(subprocess.Popen(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-ffp-contract=off",
+             "-I", str(root), "-o", str(so), str(c), "-lm"], stderr=subprocess.PIPE))
+        libs[name] = str(so)
+    for p in procs:
+        _, err = p.communicate()
+        assert p.returncode == 0, err.decode()
+    return libs
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_a_pin_catches_the_planted_mistake(name, mutant_libs):
+    pins = next(m[3] for m in MUTANTS if m[0] == name)
+    saved = (oracle.LIB, oracle._lib)
+    oracle.LIB, oracle._lib = mutant_libs[name], None
+    caught = []
+    try:
+        for module, test, kwargs in pins:
+            fn = getattr(importlib.import_module(module), test)
+            try:
+                fn(**kwargs)
+            except AssertionError:
+                caught.append(test)
+    finally:
+        oracle.LIB, oracle._lib = saved
+    assert caught, f"no pin notices '{name}'"

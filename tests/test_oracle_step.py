@@ -122,6 +122,25 @@ def test_ties_go_to_the_lower_expert_and_are_flagged():
     assert list(r["ids"][0])[1] == 1 and r["flags"][0] == 1 and r["gap"][0] == 0.0
 
 
+def test_near_tie_flag_is_the_gap_below_1e6():
+    """With x = 0 the logits are the biases exactly; experts 0 and 1 lead,
+    the rest are negligible.  The k-th/(k+1)-th probability gap is then the
+    closed-form softmax gap, and the row is flagged exactly when it is below
+    1e-6 (gaps of about 1e-5, 2e-6 and 5e-7)."""
+    E, k, H = 4, 1, 16
+    x = np.zeros((3, H), np.uint16)                  # bf16 +0
+    wr = np.zeros((E, H), np.uint16)
+    for delta, flagged in ((2e-5, 0), (4e-6, 0), (1e-6, 1)):
+        bias = np.array([0.0, -delta, -40.0, -40.0], np.float32)
+        r = oracle.route(x[:1], wr, bias, k)
+        lg = bias.astype(np.float64)
+        p = np.exp(lg - lg.max())
+        p /= p.sum()
+        assert list(r["ids"][0]) == [0]
+        assert r["gap"][0] == pytest.approx(p[0] - p[1], rel=1e-9)
+        assert int(r["flags"][0]) == flagged, (delta, r["gap"][0])
+
+
 # ------------------------------------------------------------------- pooler
 
 
