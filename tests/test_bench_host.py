@@ -1,0 +1,63 @@
+"""bench.py's multi-process bookkeeping without a GPU: the max over ranks and
+the barrier on a two-rank gloo group, and the reference arm's rank-0-only
+output under a two-rank launch."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, values, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    bench._barrier(world)
+    out[rank] = bench._max_over_ranks(values[rank], world, "cpu")
+    bench._barrier(world)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_on_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    values = [0.25, 1.75]
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, values, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 1.75, 1: 1.75}
+
+
+def test_reference_arm_prints_once_under_two_ranks():
+    lines = {}
+    for rank in (1, 0):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2")
+        r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                            "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines[rank] = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert lines[1] == []
+    assert len(lines[0]) == 1
+    rec = json.loads(lines[0][0])
+    assert rec["impl"] == "reference" and rec["unit"] == "µs" and rec["higher_is_better"] is False
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
