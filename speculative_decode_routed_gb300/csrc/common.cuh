@@ -93,6 +93,18 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// fp32 store that asks L2 to keep the line (results read back soon while
+// streamed weights pass through L2 marked evict-first).
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+
 // Contiguous global -> shared copy completed on `bar` (complete_tx).  Both
 // addresses 16-byte aligned, `bytes` a multiple of 16.  The weights are
 // streamed once per step, so they are marked evict-first in L2.

@@ -192,27 +192,39 @@ __device__ __forceinline__ void mbar_inval(uint64_t* bar) {
 }
 
 // Every barrier of one projection's pipeline (init, or inval before the
-// shared memory takes the other projection's layout).
-__device__ void tc_barriers(const TcParams& p, const TcSmem& sm, bool init) {
-  auto one = [&](uint64_t* b, uint32_t count) {
+// shared memory takes the other projection's layout), spread over the lanes
+// of one warp: lane l takes the barriers j = l mod 32 of the list below.
+__device__ void tc_barriers(const TcParams& p, const TcSmem& sm, bool init, int lane) {
+  const int nfull = p.NS * p.Q, nb = nfull + p.NS + 4 + 8 + 4 + 2 * kItemRing;
+  for (int j = lane; j < nb; j += 32) {
+    uint64_t* b;
+    uint32_t count = 1;
+    int i = j;
+    if (i < nfull) {
+      b = &sm.full[i];
+    } else if ((i -= nfull) < p.NS) {
+      b = &sm.empty[i];
+      count = (uint32_t)p.T;
+    } else if ((i -= p.NS) < 2) {
+      b = &sm.acc_full[i];
+      count = (uint32_t)p.P;
+    } else if ((i -= 2) < 2) {
+      b = &sm.acc_empty[i];
+      count = kEpiThreads / 32;
+    } else if ((i -= 2) < 8) {
+      b = &sm.slot_free[i];
+    } else if ((i -= 8) < 4) {
+      b = &sm.drain[i];
+    } else if ((i -= 4) < kItemRing) {
+      b = &sm.item_full[i];
+    } else {
+      b = &sm.item_empty[i - kItemRing];
+      count = (uint32_t)p.P + 1;
+    }
     if (init)
       mbar_init(b, count);
     else
       mbar_inval(b);
-  };
-  for (int s = 0; s < p.NS; ++s) {
-    for (int q = 0; q < p.Q; ++q) one(&sm.full[s * p.Q + q], 1);
-    one(&sm.empty[s], (uint32_t)p.T);
-  }
-  for (int b = 0; b < 2; ++b) {
-    one(&sm.acc_full[b], (uint32_t)p.P);
-    one(&sm.acc_empty[b], kEpiThreads / 32);
-  }
-  for (int i = 0; i < 8; ++i) one(&sm.slot_free[i], 1);
-  for (int i = 0; i < 4; ++i) one(&sm.drain[i], 1);
-  for (int r = 0; r < kItemRing; ++r) {
-    one(&sm.item_full[r], 1);
-    one(&sm.item_empty[r], (uint32_t)p.P + 1);
   }
   if (init) mbar_fence_init();
 }
@@ -565,6 +577,9 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
     const int m = 32 * qd + lane;       // weight row within the tile
     const int nparts = KS < p.Q ? KS : p.Q;  // K-phase partial accumulators that exist
     const float x_sg = kGU ? __ldcg(ws.x_sg) : 0.0f;
+    // h and o are read back soon (the h quantization and the next boundary's
+    // gather): keep them in L2 while the weights stream through it
+    const uint64_t keep = l2_evict_last_policy();
     int cur_e = -1, cur_pos0 = -1, cur_tiles = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
     for (int j = 0;; ++j) {
@@ -632,7 +647,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             u += __uint_as_float(rb);
           }
           const float hv = silu_f(g * sc0) * (u * sc1);
-          ws.h[(size_t)(pos0 + jj) * p.I + (size_t)tile * 128 + m] = hv;
+          st_keep(ws.h + (size_t)(pos0 + jj) * p.I + (size_t)tile * 128 + m, hv, keep);
           cur_amax = fmaxf(cur_amax, fabsf(hv));
         }
       }
@@ -666,7 +681,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             for (int n = 0; n < 16; ++n) {
               if (n < cnt) {
                 const float hv = silu_f(acc0[n] * sc0) * (acc1[n] * sc1);
-                hrow[(size_t)n * p.I] = hv;
+                st_keep(hrow + (size_t)n * p.I, hv, keep);
                 cur_amax = fmaxf(cur_amax, fabsf(hv));
               }
             }
@@ -675,7 +690,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             for (int n = 0; n < 16; ++n) {
               if (n < cnt) {
                 const int pair = sm.pairs[c0 + n];
-                ws.o[(size_t)pair * p.H + (size_t)tile * 128 + m] = acc0[n] * sc0;
+                st_keep(ws.o + (size_t)pair * p.H + (size_t)tile * 128 + m, acc0[n] * sc0, keep);
               }
             }
           }
@@ -719,8 +734,8 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   // stale parity of the fill before.  So each (stage, group) has its own
   // full barrier: every phase of it is consumed by the same issuers, and each
   // waiter tracks that barrier's parity itself.
+  if (warp == 0) tc_barriers(pg, sm, true, tid);
   if (tid == 0) {
-    tc_barriers(pg, sm, true);
     // every descriptor this launch will use, into the TMA unit's cache
     const CUtensorMap* maps[6] = {&g_a, &g_b, &g_sfb, &d_a, &d_b, &d_sfb};
     for (int i = 0; i < 6; ++i)
@@ -752,9 +767,10 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {
-    tc_barriers(pg, sm, false);
-    tc_barriers(pd, sm, true);
+  if (warp == 0) {
+    tc_barriers(pg, sm, false, tid);
+    __syncwarp();
+    tc_barriers(pd, sm, true, tid);
   }
   __syncthreads();
 
