@@ -301,6 +301,24 @@ def run_native(args, w):
     dn_gbs = None if fused else (sum(pb["down"] for pb in prof_bytes) / (prof[:, 4].sum() * 1e-3) / 1e9)
     step_gbs = byt["total"] * w.n_layers / (ms * 1e-3) / 1e9 * ws
 
+    # the first layer's front (embedded tokens -> stream + input norm), timed
+    # alone: CUDA events around 50 launches on the launching stream
+    emb_bits, wn = synth.front_inputs(w)
+    emb = torch.from_numpy(emb_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    wn_t = torch.from_numpy(wn).to(device)
+    st_f = torch.empty(rows, w.hidden, dtype=torch.float32, device=device)
+    ai_f = torch.empty(rows, w.hidden, dtype=torch.bfloat16, device=device)
+    for _ in range(5):
+        dec.front(rows, emb, wn_t, st_f, ai_f)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(cs)
+    for _ in range(50):
+        dec.front(rows, emb, wn_t, st_f, ai_f)
+    f1.record(cs)
+    torch.cuda.synchronize(device)
+    dec.check()
+    front_us = f0.elapsed_time(f1) * 1000.0 / 50
+
     # end to end through the host-buffer entry point
     s_h, b_h = synth.step_inputs(w)
     sh = torch.from_numpy(s_h).pin_memory()
@@ -340,7 +358,7 @@ def run_native(args, w):
                      "launch_us": round(k_ms[3] * 1000, 2),
                      "algorithmic_bytes": int(exp_bytes.mean())},
         "kernels_us": dict({"boundary": round(k_ms[0] * 1000, 2), "router": round(k_ms[1] * 1000, 2),
-                            "pool": round(k_ms[2] * 1000, 2)},
+                            "pool": round(k_ms[2] * 1000, 2), "front": round(front_us, 2)},
                            **({"experts": round(k_ms[3] * 1000, 2)} if fused else
                               {"gate_up": round(k_ms[3] * 1000, 2), "down": round(k_ms[4] * 1000, 2),
                                "down_gbs": round(dn_gbs, 1)})),

@@ -138,8 +138,25 @@ int moe_decode_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branc
                      void* cuda_stream);
 
 /* Final boundary: gathers the last layer's unpooled output into the stream
- * and writes out = bf16(rmsnorm(stream) * w_final). */
-int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, void* cuda_stream);
+ * and writes out = bf16(rmsnorm(stream) * w_final).  aux: fp32 [rows][H]
+ * receiving a copy of the updated stream (the drafter's final aux hidden
+ * state; decode page, SpecializedDecode.run: final.run(final_slot, stream,
+ * output, final_aux)), or NULL.  stream and aux 16-byte, out 8-byte aligned. */
+int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, float* aux,
+                     void* cuda_stream);
+
+/* The first layer's front (decode page, module docstring "One step of b
+ * rows": "the embedded tokens into the stream (fp32) and its
+ * pre_qkv_proj_norm into the attention input, one kernel"):
+ *   stream     = fp32(embedded)                          [rows][H], written
+ *   attn_input = bf16(rmsnorm(stream) * w_norm)          [rows][H]
+ *   aux        = stream (a copy for the drafter), or NULL
+ * embedded: bf16 [rows][H] (the embedding's output); w_norm: fp32 [H], the
+ * first layer's input norm weight (caller-owned); eps is the handle's.
+ * w_norm, stream and aux 16-byte, embedded and attn_input 8-byte aligned.
+ * Asynchronous on cuda_stream. */
+int moe_decode_front(moe_decode_t* h, int rows, const uint16_t* embedded, const float* w_norm,
+                     float* stream, uint16_t* attn_input, float* aux, void* cuda_stream);
 
 /* Every layer (layer 0 takes `branch`, later ones chain) and the final
  * boundary. */

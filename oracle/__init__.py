@@ -53,6 +53,7 @@ def lib():
             "oracle_nvfp4_quantize": (None, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
             "oracle_nvfp4_dequantize": (None, [_vp, _vp, _f32, _i64, _i64, _vp]),
             "oracle_boundary": (None, [ctypes.c_int, ctypes.c_int, _f64, _vp, _vp, _vp, _vp, _vp, _vp]),
+            "oracle_front": (None, [ctypes.c_int, ctypes.c_int, _f64, _vp, _vp, _vp, _vp, _vp]),
             "oracle_route": (None, [ctypes.c_int] * 4 + [_vp] * 9),
             "oracle_pool": (None, [ctypes.c_int] * 3 + [_vp] * 6),
             "oracle_gate_up": (ctypes.c_int, [ctypes.c_int] * 5 + [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp]),
@@ -143,6 +144,19 @@ def boundary(branch, stream, w_post, w_pre, eps):
     lib().oracle_boundary(rows, H, eps, _p(branch), _p(s), _p(_c(w_post, np.float32)),
                           _p(_c(w_pre, np.float32)), _p(x), _p(xe))
     return s, x, xe
+
+
+def front(embedded, w, eps):
+    """The first layer's front: embedded bf16 bits [rows, H] -> (stream fp32,
+    out bf16 bits, out before rounding fp64)."""
+    embedded = _c(embedded, np.uint16)
+    rows, H = embedded.shape
+    w = _c(w, np.float32)
+    stream = np.zeros((rows, H), np.float32)
+    out = np.zeros((rows, H), np.uint16)
+    exact = np.zeros((rows, H))
+    lib().oracle_front(rows, H, eps, _p(embedded), _p(w), _p(stream), _p(out), _p(exact))
+    return stream, out, exact
 
 
 def route(x, router_w, bias, k):

@@ -203,6 +203,29 @@ void oracle_boundary(int rows, int H, double eps, const double* branch, float* s
   }
 }
 
+/* The first layer's front (decode page, module docstring "One step of b
+ * rows": the embedded tokens into the stream (fp32) and its
+ * pre_qkv_proj_norm into the attention input): stream = the embedded bf16
+ * values, exactly; out = bf16(stream / sqrt(mean(stream^2) + eps) * w). */
+void oracle_front(int rows, int H, double eps, const uint16_t* embedded, const float* w,
+                  float* stream, uint16_t* out, double* out_exact) {
+  for (int r = 0; r < rows; ++r) {
+    float* s = stream + (int64_t)r * H;
+    double ms = 0.0;
+    for (int h = 0; h < H; ++h) {
+      s[h] = (float)oracle_bf16_decode(embedded[(int64_t)r * H + h]);
+      ms += (double)s[h] * (double)s[h];
+    }
+    ms /= H;
+    double inv_front = 1.0 / sqrt(ms + eps);
+    for (int h = 0; h < H; ++h) {
+      double xe = (double)s[h] * inv_front * (double)w[h];
+      if (out_exact) out_exact[(int64_t)r * H + h] = xe;
+      out[(int64_t)r * H + h] = oracle_bf16_from_double(xe);
+    }
+  }
+}
+
 /* ------------------------------------------------------------------ routing */
 
 static void softmax_row(int E, const double* logit, double* p) {

@@ -66,6 +66,11 @@ void oracle_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, float sg, 
 void oracle_boundary(int rows, int H, double eps, const double* branch, float* stream,
                      const float* w_post, const float* w_pre, uint16_t* x, double* x_exact);
 
+/* The first layer's front: stream fp32 [rows][H] = embedded (bf16 bits),
+ * exactly; out bf16 bits = bf16(rmsnorm(stream) * w); out_exact (optional)
+ * the value before rounding. */
+void oracle_front(int rows, int H, double eps, const uint16_t* embedded, const float* w,
+                  float* stream, uint16_t* out, double* out_exact);
 /* Router + routing.  x bf16 [rows][H]; router_w bf16 [E][H]; bias fp32 [E] or
  * NULL.  Outputs: logits fp64 [rows][E] (optional), probs fp64 [rows][E]
  * (optional), ids int32 [rows][k] (slot order: descending p), gates fp64

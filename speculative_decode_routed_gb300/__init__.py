@@ -20,7 +20,7 @@ MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOMEM, MOE_EDEVICE = 0, -1
 
 # Every symbol include/moe_decode.h declares.
 EXPORTS = (
-    "moe_decode_create", "moe_decode_layer", "moe_decode_final", "moe_decode_step",
+    "moe_decode_create", "moe_decode_layer", "moe_decode_final", "moe_decode_front", "moe_decode_step",
     "moe_decode_step_graph", "moe_decode_step_host", "moe_decode_layer_profile", "moe_decode_debug",
     "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_step_kernel_count",
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
@@ -68,7 +68,8 @@ def _lib():
             "moe_decode_create": (i32, [ctypes.POINTER(Dims), ctypes.POINTER(LayerWeights), vp, vp,
                                         ctypes.POINTER(vp)]),
             "moe_decode_layer": (i32, [vp, i32, i32, vp, vp, vp]),
-            "moe_decode_final": (i32, [vp, i32, vp, vp, vp]),
+            "moe_decode_final": (i32, [vp, i32, vp, vp, vp, vp]),
+            "moe_decode_front": (i32, [vp, i32, vp, vp, vp, vp, vp, vp]),
             "moe_decode_step": (i32, [vp, i32, vp, vp, vp, vp]),
             "moe_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp]),
             "moe_decode_step_host": (i32, [vp, i32, vp, vp, vp, vp]),
@@ -127,9 +128,14 @@ def moe_decode_layer(h, layer, rows, branch, stream_buf, stream=None):
                                    _stream(stream)), "moe_decode_layer")
 
 
-def moe_decode_final(h, rows, stream_buf, out, stream=None):
-    _check(_lib().moe_decode_final(h, rows, _ptr(stream_buf), _ptr(out), _stream(stream)),
+def moe_decode_final(h, rows, stream_buf, out, aux=None, stream=None):
+    _check(_lib().moe_decode_final(h, rows, _ptr(stream_buf), _ptr(out), _ptr(aux), _stream(stream)),
            "moe_decode_final")
+
+
+def moe_decode_front(h, rows, embedded, w_norm, stream_buf, attn_input, aux=None, stream=None):
+    _check(_lib().moe_decode_front(h, rows, _ptr(embedded), _ptr(w_norm), _ptr(stream_buf),
+                                   _ptr(attn_input), _ptr(aux), _stream(stream)), "moe_decode_front")
 
 
 def moe_decode_step(h, rows, branch, stream_buf, out, stream=None):
@@ -231,8 +237,11 @@ class MoEDecode:
     def layer(self, layer, rows, branch, stream_buf, stream=None):
         moe_decode_layer(self.handle, layer, rows, branch, stream_buf, stream)
 
-    def final(self, rows, stream_buf, out, stream=None):
-        moe_decode_final(self.handle, rows, stream_buf, out, stream)
+    def final(self, rows, stream_buf, out, aux=None, stream=None):
+        moe_decode_final(self.handle, rows, stream_buf, out, aux, stream)
+
+    def front(self, rows, embedded, w_norm, stream_buf, attn_input, aux=None, stream=None):
+        moe_decode_front(self.handle, rows, embedded, w_norm, stream_buf, attn_input, aux, stream)
 
     def step(self, rows, branch, stream_buf, out, stream=None):
         moe_decode_step(self.handle, rows, branch, stream_buf, out, stream)

@@ -10,6 +10,12 @@
 //   x       = bf16(rmsnorm(stream') * w_pre)
 // where branch is either a bf16 tensor or the gathered expert outputs
 //   y[r] = sum_s gates[r][s] * o[r*k + s]               (slot order).
+// The first layer's front (same page: "the embedded tokens into the stream
+// (fp32) and its pre_qkv_proj_norm into the attention input, one kernel") is
+// the same kernel with one norm:  stream' = fp32(embedded), x = bf16(
+// rmsnorm(stream') * w).  Boundaries that feed the drafter also copy stream'
+// into an aux buffer (SpecializedDecode.build: aux buffers of the aux
+// layers, and the final boundary's).
 //
 // GB300 layout: one thread-block cluster per row; each CTA owns H / cluster
 // columns (four per thread, 128-bit accesses), and the two row sums of
@@ -51,7 +57,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
   // Norm weights do not depend on the previous kernel: fetch them first.
   float4 wpost = make_float4(0.f, 0.f, 0.f, 0.f), wpre = wpost;
   if (live) {
-    wpost = __ldg(reinterpret_cast<const float4*>(p.w_post + col));
+    if (!p.front) wpost = __ldg(reinterpret_cast<const float4*>(p.w_post + col));
     wpre = __ldg(reinterpret_cast<const float4*>(p.w_pre + col));
   }
   grid_dep_wait();
@@ -87,22 +93,29 @@ __global__ void boundary_kernel(BoundaryParams p) {
     }
   }
 
-  // rms of the branch over the whole row (cluster-wide)
-  block_sum_to_slot(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, warp_red, &part[0]);
-  cluster.sync();
-  float ss = 0.0f;
-  for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss += *cluster.map_shared_rank(&part[0], q);
-  const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
-
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   float* srow = p.stream + (size_t)r * p.H + col;
+  if (p.front) {
+    // the first layer's front: the embedded tokens are the stream
+    s = y;
+  } else {
+    // rms of the branch over the whole row (cluster-wide)
+    block_sum_to_slot(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, warp_red, &part[0]);
+    cluster.sync();
+    float ss = 0.0f;
+    for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss += *cluster.map_shared_rank(&part[0], q);
+    const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
+    if (live) {
+      s = __ldcg(reinterpret_cast<const float4*>(srow));
+      s.x += y.x * inv1 * wpost.x;
+      s.y += y.y * inv1 * wpost.y;
+      s.z += y.z * inv1 * wpost.z;
+      s.w += y.w * inv1 * wpost.w;
+    }
+  }
   if (live) {
-    s = __ldcg(reinterpret_cast<const float4*>(srow));
-    s.x += y.x * inv1 * wpost.x;
-    s.y += y.y * inv1 * wpost.y;
-    s.z += y.z * inv1 * wpost.z;
-    s.w += y.w * inv1 * wpost.w;
     *reinterpret_cast<float4*>(srow) = s;
+    if (p.aux) *reinterpret_cast<float4*>(p.aux + (size_t)r * p.H + col) = s;
   }
 
   // rms of the updated stream

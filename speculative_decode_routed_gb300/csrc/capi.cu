@@ -445,7 +445,8 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
 #endif
 }
 
-int launch_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, cudaStream_t s) {
+int launch_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, cudaStream_t s,
+                 float* aux = nullptr) {
   const moe_decode_dims& d = h->d;
   moe::BoundaryParams bp{};
   bp.H = d.hidden;
@@ -461,6 +462,7 @@ int launch_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, cudaSt
   bp.w_pre = h->w_final;
   bp.x_out = reinterpret_cast<__nv_bfloat16*>(out);
   bp.x_amax = nullptr;
+  bp.aux = aux;
   const cudaError_t e = moe::launch_boundary(bp, h->cluster, s, true);
   if (e != cudaSuccess) return cuda_fail(e, "final boundary launch");
   return MOE_OK;
@@ -654,15 +656,44 @@ int moe_decode_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branc
   return launch_layer(h, layer, rows, branch, stream, static_cast<cudaStream_t>(cuda_stream));
 }
 
-int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, void* cuda_stream) {
+int moe_decode_final(moe_decode_t* h, int rows, float* stream, uint16_t* out, float* aux,
+                     void* cuda_stream) {
   if (!h) return fail(MOE_EINVAL, "null handle");
   int rc = check_rows(h, rows);
   if (rc) return rc;
-  if (!stream || !out || !aligned(stream, 16) || !aligned(out, 8))
-    return fail(MOE_EINVAL, "stream (16-byte) and out (8-byte) must be aligned device pointers");
+  if (!stream || !out || !aligned(stream, 16) || !aligned(out, 8) || !aligned(aux, 16))
+    return fail(MOE_EINVAL, "stream and aux (16-byte) and out (8-byte) must be aligned device pointers");
   if (!h->w_post_final || !h->w_final)
     return fail(MOE_EINVAL, "the handle was created without final norm weights");
-  return launch_final(h, rows, stream, out, static_cast<cudaStream_t>(cuda_stream));
+  return launch_final(h, rows, stream, out, static_cast<cudaStream_t>(cuda_stream), aux);
+}
+
+int moe_decode_front(moe_decode_t* h, int rows, const uint16_t* embedded, const float* w_norm,
+                     float* stream, uint16_t* attn_input, float* aux, void* cuda_stream) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!embedded || !w_norm || !stream || !attn_input)
+    return fail(MOE_EINVAL, "embedded, w_norm, stream and attn_input are required");
+  if (!aligned(embedded, 8) || !aligned(w_norm, 16) || !aligned(stream, 16) ||
+      !aligned(attn_input, 8) || !aligned(aux, 16))
+    return fail(MOE_EINVAL, "w_norm, stream and aux must be 16-byte, embedded and attn_input 8-byte aligned");
+  const moe_decode_dims& d = h->d;
+  moe::BoundaryParams bp{};
+  bp.H = d.hidden;
+  bp.k = d.top_k;
+  bp.rows = rows;
+  bp.cols_per_cta = d.hidden / h->cluster;
+  bp.eps = d.eps;
+  bp.branch = reinterpret_cast<const __nv_bfloat16*>(embedded);
+  bp.stream = stream;
+  bp.w_pre = w_norm;
+  bp.x_out = reinterpret_cast<__nv_bfloat16*>(attn_input);
+  bp.front = 1;
+  bp.aux = aux;
+  const cudaError_t e = moe::launch_boundary(bp, h->cluster, static_cast<cudaStream_t>(cuda_stream), false);
+  if (e != cudaSuccess) return cuda_fail(e, "front launch");
+  return MOE_OK;
 }
 
 int moe_decode_step(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,

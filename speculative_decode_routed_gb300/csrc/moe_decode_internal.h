@@ -82,6 +82,9 @@ struct BoundaryParams {
   const float* w_pre;           // [H]
   __nv_bfloat16* x_out;         // [rows][H]
   unsigned* x_amax;             // max |x| accumulator, or null (final boundary)
+  int front;                    // 1: the first layer's front -- the stream is the branch (the
+                                //    embedded tokens) itself, one norm (w_pre) into x_out
+  float* aux;                   // [rows][H] copy of the updated stream, or null
 };
 
 // ------------------------------------------------------------- router (K2)

@@ -37,6 +37,8 @@ KIND_DOWN = 8
 KIND_W_POST_FINAL = 9
 KIND_W_FINAL = 10
 KIND_ZIPF_PERM = 11
+KIND_EMBED = 12
+KIND_W_FRONT = 13
 
 
 def tag(kind: int, layer: int = 0, index: int = 0) -> int:
@@ -215,6 +217,14 @@ def final_norm_weights(w: Workload):
     h = w.hidden
     return (normal_f32((h,), w.seed, tag(KIND_W_POST_FINAL), *w.norm_dist),
             normal_f32((h,), w.seed, tag(KIND_W_FINAL), *w.norm_dist))
+
+
+def front_inputs(w: Workload, variant: int = 0):
+    """The first layer's front: (embedded tokens bf16 bits [b, H] ~ N(0, 1),
+    its input norm weight fp32 [H] = 1 + 0.1 N(0, 1))."""
+    emb = normal_bf16((w.rows, w.hidden), w.seed, tag(KIND_EMBED, 0, variant), *w.branch_dist)
+    wn = normal_f32((w.hidden,), w.seed, tag(KIND_W_FRONT), *w.norm_dist)
+    return emb, wn
 
 
 def router_weights(w: Workload, layer: int) -> np.ndarray:

@@ -73,7 +73,8 @@ def test_calls_on_a_null_handle_fail_cleanly():
     L = moe.lib()
     assert L.moe_decode_layer(None, 0, 1, None, None, None) == moe.MOE_EINVAL
     assert L.moe_decode_step(None, 1, None, None, None, None) == moe.MOE_EINVAL
-    assert L.moe_decode_final(None, 1, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_decode_final(None, 1, None, None, None, None) == moe.MOE_EINVAL
+    assert L.moe_decode_front(None, 1, None, None, None, None, None, None) == moe.MOE_EINVAL
     assert L.moe_decode_last_error(None) == moe.MOE_EINVAL
     assert L.moe_decode_workspace_bytes(None) == 0
     L.moe_decode_destroy(None)

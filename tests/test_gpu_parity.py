@@ -282,6 +282,40 @@ def test_repeated_replays_bitwise():
     dec.close()
 
 
+@pytest.mark.parametrize("H", [256, 7168])
+def test_front_and_aux_copies(H):
+    """The first layer's front against the oracle (stream bit-exact, the
+    attention input exact away from bf16 near-ties), its aux copy, and the
+    final boundary's aux copy of the stream."""
+    w = synth.Workload(f"front{H}", rows=8, hidden=H, n_experts=8, top_k=2, inter=128)
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    emb_bits, wn = synth.front_inputs(w)
+    emb = torch.from_numpy(emb_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    stream = torch.empty(w.rows, H, dtype=torch.float32, device="cuda")
+    attn = torch.empty(w.rows, H, dtype=torch.bfloat16, device="cuda")
+    aux = torch.full_like(stream, float("nan"))
+    dec.front(w.rows, emb, torch.from_numpy(wn).cuda(), stream, attn, aux)
+    torch.cuda.synchronize()
+    dec.check()
+    s_ref, out_ref, exact = oracle.front(emb_bits, wn, w.eps)
+    assert np.array_equal(stream.cpu().numpy(), s_ref)
+    assert torch.equal(aux, stream)
+    got = attn.view(torch.uint16).cpu().numpy()
+    assert not np.any((got != out_ref) & ~bf16_near_tie(exact)), "attention input away from near-ties"
+    assert np.mean(got != out_ref) < 1e-3
+    # a layer on that stream, then the final boundary with its aux copy
+    _, branch = sgpu.step_tensors(w)
+    dec.layer(0, w.rows, branch, stream)
+    out = torch.empty_like(attn)
+    aux2 = torch.full_like(stream, float("nan"))
+    dec.final(w.rows, stream, out, aux2)
+    torch.cuda.synchronize()
+    dec.check()
+    assert torch.equal(aux2, stream)
+    dec.close()
+
+
 ODD_SHAPES = [
     # (rows, H, E, k, I): a ragged H (cluster of 1, 12 chunks/row), a single
     # expert, k == E, a row count with many rows per expert (> 8: the

@@ -52,6 +52,13 @@ MUTANTS = [
      "s[h] = (float)((double)s[h] + br[h] * inv);",
      [("test_oracle_step", "test_constant_rows_closed_form", {}),
       ("test_oracle_step", "test_norm_is_scale_free_without_eps", {})]),
+    ("front norm without eps",
+     "double inv_front = 1.0 / sqrt(ms + eps);", "double inv_front = 1.0 / sqrt(ms);",
+     [("test_oracle_step", "test_front_constant_rows_closed_form", {})]),
+    ("front stream rounded to bf16 twice",
+     "s[h] = (float)oracle_bf16_decode(embedded[(int64_t)r * H + h]);",
+     "s[h] = (float)oracle_bf16_decode(oracle_bf16_from_double(0.5 * oracle_bf16_decode(embedded[(int64_t)r * H + h])));",
+     [("test_oracle_step", "test_front_stream_is_the_embedding_exactly", {})]),
     ("top-k ties to the higher id",
      "if (best < 0 || p[e] > p[best]) best = e;", "if (best < 0 || p[e] >= p[best]) best = e;",
      [("test_oracle_step", "test_ties_go_to_the_lower_expert_and_are_flagged", {}),

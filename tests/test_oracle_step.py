@@ -122,6 +122,48 @@ def test_ties_go_to_the_lower_expert_and_are_flagged():
     assert list(r["ids"][0])[1] == 1 and r["flags"][0] == 1 and r["gap"][0] == 0.0
 
 
+def _bf16_f64(bits):
+    import torch
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_front_stream_is_the_embedding_exactly():
+    rs = np.random.RandomState(3)
+    emb = _bf16_bits(rs.standard_normal((5, 96)) * 3.0)
+    w = (1.0 + 0.1 * rs.standard_normal(96)).astype(np.float32)
+    stream, out, _ = oracle.front(emb, w, 1e-6)
+    np.testing.assert_array_equal(stream.astype(np.float64), _bf16_f64(emb))
+
+
+def test_front_constant_rows_closed_form():
+    """A row of constant c: rms = |c|, so out = bf16(sign(c) * w / sqrt(1 + eps/c^2));
+    c = 1e-3 makes eps/c^2 = 1 (the eps term matters)."""
+    H, eps = 64, 1e-6
+    rs = np.random.RandomState(4)
+    w = (1.0 + 0.1 * rs.standard_normal(H)).astype(np.float32)
+    cs = [1e-3, -2.5, 7.0]
+    emb = _bf16_bits(np.array([[c] * H for c in cs]))
+    _, out, exact = oracle.front(emb, w, eps)
+    for i in range(len(cs)):
+        c = _bf16_f64(emb[i, :1])[0]
+        want = np.sign(c) * w.astype(np.float64) / np.sqrt(1.0 + eps / (c * c))
+        np.testing.assert_allclose(exact[i], want, rtol=1e-12)
+        np.testing.assert_array_equal(out[i], _bf16_bits(want.astype(np.float32)))
+
+
+def test_front_is_scale_free_without_eps():
+    """Doubling the input (exact in bf16) leaves the normalised output bit
+    for bit unchanged when eps = 0."""
+    rs = np.random.RandomState(5)
+    emb = _bf16_bits(rs.standard_normal((4, 128)))
+    emb2 = _bf16_bits(_bf16_f64(emb) * 2.0)
+    w = (1.0 + 0.1 * rs.standard_normal(128)).astype(np.float32)
+    s1, out1, _ = oracle.front(emb, w, 0.0)
+    s2, out2, _ = oracle.front(emb2, w, 0.0)
+    np.testing.assert_array_equal(s2, 2.0 * s1)
+    np.testing.assert_array_equal(out1, out2)
+
+
 def test_near_tie_flag_is_the_gap_below_1e6():
     """With x = 0 the logits are the biases exactly; experts 0 and 1 lead,
     the rest are negligible.  The k-th/(k+1)-th probability gap is then the
