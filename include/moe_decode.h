@@ -171,7 +171,10 @@ int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, flo
 
 /* End-to-end step on HOST buffers: copies branch and stream in (H2D), replays
  * the step graph, copies stream and out back (D2H) and synchronizes the
- * stream.  Pinned host memory gives asynchronous copies. */
+ * stream.  When all three buffers are page-locked, the copies and the step
+ * are one library-owned graph (cached per rows and buffers, captured on the
+ * first call), launched once per call; pageable buffers take separate copies
+ * around the step graph. */
 int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
                          float* stream_host, uint16_t* out_host, void* cuda_stream);
 

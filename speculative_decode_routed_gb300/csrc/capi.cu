@@ -56,6 +56,17 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Page-locked (or registered) host memory, which a graph's copy nodes can
+// move asynchronously.
+bool host_pinned(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // pageable memory may report an error on older drivers
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
 struct GraphEntry {
   int rows;
   const void* branch;
@@ -87,6 +98,7 @@ struct moe_decode_s {
   moe::ExpertParams gu{}, dn{};
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
+  std::vector<GraphEntry> host_graphs;  // copies in, step, copies out (pinned host buffers)
   uint16_t* io_branch = nullptr;
   float* io_stream = nullptr;
   uint16_t* io_out = nullptr;
@@ -740,6 +752,43 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
     return fail(MOE_EINVAL, "branch_host, stream_host and out_host are required");
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const size_t n = (size_t)rows * h->d.hidden;
+  // Pinned host buffers: the copies in, the step and the copies out as one
+  // cached graph, so a call is one launch and one synchronization.
+  if (host_pinned(branch_host) && host_pinned(stream_host) && host_pinned(out_host)) {
+    cudaGraphExec_t exec = nullptr;
+    for (const GraphEntry& g : h->host_graphs)
+      if (g.rows == rows && g.branch == branch_host && g.stream == stream_host && g.out == out_host)
+        exec = g.exec;
+    if (!exec) {
+      cudaStream_t c = h->cap_stream;
+      cudaError_t e = cudaStreamBeginCapture(c, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) return cuda_fail(e, "begin capture");
+      e = cudaMemcpyAsync(h->io_branch, branch_host, n * 2, cudaMemcpyHostToDevice, c);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, c);
+      int erc = (e == cudaSuccess) ? enqueue_step(h, rows, h->io_branch, h->io_stream, h->io_out, c)
+                                   : cuda_fail(e, "input copy");
+      if (!erc) {
+        e = cudaMemcpyAsync(stream_host, h->io_stream, n * 4, cudaMemcpyDeviceToHost, c);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, h->io_out, n * 2, cudaMemcpyDeviceToHost, c);
+        if (e != cudaSuccess) erc = cuda_fail(e, "output copy");
+      }
+      cudaGraph_t graph = nullptr;
+      e = cudaStreamEndCapture(c, &graph);
+      if (erc) {
+        if (graph) cudaGraphDestroy(graph);
+        return erc;
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "end capture");
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
+      h->host_graphs.push_back(GraphEntry{rows, branch_host, stream_host, out_host, exec});
+    }
+    cudaError_t e = cudaGraphLaunch(exec, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-buffer step");
+    return MOE_OK;
+  }
   cudaError_t e = cudaMemcpyAsync(h->io_branch, branch_host, n * 2, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, s);
@@ -833,6 +882,7 @@ int moe_decode_step_kernel_count(const moe_decode_t* h) {
 void moe_decode_destroy(moe_decode_t* h) {
   if (!h) return;
   for (GraphEntry& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  for (GraphEntry& g : h->host_graphs) cudaGraphExecDestroy(g.exec);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   cudaFree(h->io_branch);
   cudaFree(h->io_stream);

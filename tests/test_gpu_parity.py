@@ -245,9 +245,17 @@ def test_tiny_step_end_to_end_graph_and_host():
     sh = torch.from_numpy(s_h).pin_memory()
     bh = torch.from_numpy(b_h).view(torch.bfloat16).pin_memory()
     oh = torch.empty_like(bh).pin_memory()
-    dec.step_host(w.rows, bh, sh, oh)
-    assert np.array_equal(sh.numpy(), eager_stream)
-    assert np.array_equal(oh.view(torch.uint16).numpy(), eager_out)
+    for _ in range(2):                      # captured on the first call, replayed on the second
+        sh.copy_(torch.from_numpy(s_h))
+        dec.step_host(w.rows, bh, sh, oh)
+        assert np.array_equal(sh.numpy(), eager_stream)
+        assert np.array_equal(oh.view(torch.uint16).numpy(), eager_out)
+    # pageable host buffers take the separate copies
+    sp = torch.from_numpy(s_h.copy())
+    op = torch.empty_like(oh, device="cpu")
+    dec.step_host(w.rows, torch.from_numpy(b_h.copy()).view(torch.bfloat16), sp, op)
+    assert np.array_equal(sp.numpy(), eager_stream)
+    assert np.array_equal(op.view(torch.uint16).numpy(), eager_out)
     # per layer: boundary, router and the experts (tensor cores, up to 32
     # rows: no pooler gather), or boundary, router, gate/up and down; plus
     # the final boundary
