@@ -204,9 +204,54 @@ def cpu_baseline(w: synth.Workload, n_sample_experts: int = 4):
     return t_step * 1e6, info
 
 
+DENSE_METRIC = "dense draft layer µs at b=8 and weight-stream HBM GB/s vs GB300 peak"
+
+
+def _dense_bytes(w: synth.Workload, rows: int):
+    """Bytes one dense layer must move at minimum: each bf16 weight once, the
+    activations of every stage once each way."""
+    H, I = w.hidden, w.inter
+    w13, w2 = 2 * I * H * 2, H * I * 2
+    gate_up = w13 + rows * H * 2 + rows * 2 * I * 2
+    down = w2 + rows * I * 2 + rows * H * 2
+    norms = 3 * H * 4 + 2 * rows * H * (2 + 4 + 4) + rows * H * 2 + rows * 2 * I * 2 + rows * I * 2
+    return dict(gate_up=gate_up, down=down, total=gate_up + down + norms)
+
+
+def dense_cpu_baseline(w: synth.Workload):
+    """The CPU oracle's dense layer, as it stands, on the whole step (all rows,
+    both projections); weight generation is not timed.  -> (us, info)."""
+    import oracle
+    stream, attn = synth.step_inputs(w)
+    na, npre, npost = synth.dense_norm_weights(w, 0)
+    w13, w2 = synth.dense_weights(w, 0)
+    t0 = time.perf_counter()
+    oracle.dense_layer(attn, stream, na, npre, w13, w2, npost, w.eps)
+    us = (time.perf_counter() - t0) * 1e6
+    return us, {"kind": "oracle", "cores": oracle.num_threads(),
+                "sample": f"the whole dense layer on all {w.rows} rows (no sampling)"}
+
+
 def run_reference(args, w):
     ws, rank, _ = _dist()
     if rank != 0:
+        return
+    if w.n_experts == 0:
+        times, info = [], None
+        for i in range(args.warmup + args.steps):
+            us, info = dense_cpu_baseline(w)
+            if i >= args.warmup:
+                times.append(us)
+        v = float(np.mean(times))
+        line = {"impl": "reference", "metric": DENSE_METRIC, "value": round(v, 1), "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(v / 1000.0, 3), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "inter": w.inter},
+                "cpu_baseline": dict(info, value=round(v, 1), unit=UNIT),
+                "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     times = []
     info = None
@@ -378,6 +423,133 @@ def run_native(args, w):
         dist.destroy_process_group()
 
 
+def run_dense(args, w):
+    """One dense draft layer (boundary, gate/up GEMM, SiLU * mul, down GEMM,
+    boundary) per step, replayed as a CUDA graph per input draw."""
+    import torch
+
+    import speculative_decode_routed_gb300 as moe
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    H, I, rows = w.hidden, w.inter, w.rows
+    w13 = torch.empty(2 * I, H, dtype=torch.bfloat16, device=device)
+    w2 = torch.empty(H, I, dtype=torch.bfloat16, device=device)
+    synth.dev_dense_weights(w13, w2, w, 0)
+    norms = [torch.from_numpy(n).to(device) for n in synth.dense_norm_weights(w, 0)]
+    dl = moe.DenseLayer(H, I, rows, norms[0], norms[1], w13, w2, norms[2], eps=w.eps)
+    V = 4
+    bufs = []
+    for v in range(V):
+        s, a = synth.step_inputs(w, v)
+        bufs.append((torch.from_numpy(s).to(device),
+                     torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)))
+    cs = torch.cuda.current_stream(device)
+    for s, a in bufs:                                 # eager first calls set cuBLAS up
+        dl.layer(rows, a, s.clone())
+    torch.cuda.synchronize(device)
+    graphs = []
+    side = torch.cuda.Stream(device)
+    side.wait_stream(cs)
+    for s, a in bufs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            dl.layer(rows, a, s, stream=side)
+        graphs.append(g)
+    cs.wait_stream(side)
+    for i in range(args.warmup):
+        graphs[i % V].replay()
+    torch.cuda.synchronize(device)
+    _barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+        ev0.record(cs)
+        for i in range(args.steps):
+            graphs[i % V].replay()
+        ev1.record(cs)
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = _max_over_ranks(ms, ws, device)
+    clocks = clk.summary()
+
+    # per-launch durations: events on the launching stream around each launch
+    prof = np.array([dl.layer_profile(rows, *bufs[i % V][::-1]) for i in range(max(4, min(args.steps, 20)))])
+    k_ms = prof.mean(0)
+    byt = _dense_bytes(w, rows)
+    peak, peak_kind = _peaks()
+    gu_gbs = byt["gate_up"] / (k_ms[1] * 1e-3) / 1e9
+    dn_gbs = byt["down"] / (k_ms[3] * 1e-3) / 1e9
+    step_gbs = byt["total"] / (ms * 1e-3) / 1e9 * ws
+
+    # end to end: pinned host inputs copied in, the layer, the stream copied out
+    s_h, a_h = synth.step_inputs(w)
+    sh = torch.from_numpy(s_h).pin_memory()
+    ah = torch.from_numpy(a_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(sh).pin_memory()
+    sd, ad = torch.empty_like(sh, device=device), torch.empty_like(ah, device=device)
+
+    def host_step():
+        sd.copy_(sh, non_blocking=True)
+        ad.copy_(ah, non_blocking=True)
+        dl.layer(rows, ad, sd)
+        oh.copy_(sd, non_blocking=True)
+        torch.cuda.synchronize(device)
+
+    for _ in range(3):
+        host_step()
+    _barrier(ws)
+    t0 = time.perf_counter()
+    n_e2e = max(args.steps, 5)
+    for _ in range(n_e2e):
+        host_step()
+    e2e_ms = (time.perf_counter() - t0) * 1000.0 / n_e2e
+    e2e_ms = _max_over_ranks(e2e_ms, ws, device)
+    if rank != 0:
+        dl.close()
+        return
+    line = {
+        "metric": DENSE_METRIC, "value": round(ms * 1000.0, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox / Irwin-Hall normals generated on device)",
+        "config": {"workload": w.name, "rows": rows, "hidden": H, "inter": I,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "graph": "one CUDA graph per input draw (the whole layer)",
+                   "l2": "inputs larger than L2: %.2f GB of bf16 weights per step, 4 input draws cycled"
+                         % ((byt["gate_up"] + byt["down"]) / 1e9)},
+        "weight_stream_gbs": round(step_gbs, 1),
+        "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
+        "bytes_per_layer_step": int(byt["total"]),
+        "roofline": {"kernel": "gate/up projection (cuBLAS bf16 GEMM)", "bound": "hbm",
+                     "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gu_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gate_up"])},
+        "kernels_us": {"boundary_attn": round(k_ms[0] * 1000, 2), "gate_up": round(k_ms[1] * 1000, 2),
+                       "silu_mul": round(k_ms[2] * 1000, 2), "down": round(k_ms[3] * 1000, 2),
+                       "boundary_ffn": round(k_ms[4] * 1000, 2), "down_gbs": round(dn_gbs, 1)},
+        "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT,
+                "h2d_bytes_per_step": rows * H * (4 + 2), "d2h_bytes_per_step": rows * H * 4},
+        "gpu_launches": 3 * args.steps,
+        "library_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        us, info = dense_cpu_baseline(w)
+        line["cpu_baseline"] = dict(info, value=round(us, 1), unit=UNIT)
+    print(json.dumps(line), flush=True)
+    dl.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 class _Cai:
     def __init__(self, ptr, shape, typestr):
         self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr,
@@ -390,17 +562,20 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="serving", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="serving",
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.DENSE_WORKLOADS))
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS.get(args.workload) or synth.DENSE_WORKLOADS[args.workload]
     if args.rows:
         w = w.with_rows(args.rows)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.n_experts == 0:
+        run_dense(args, w)
     else:
         run_native(args, w)
 

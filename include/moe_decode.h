@@ -244,6 +244,63 @@ int moe_nvfp4_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* code
 int moe_nvfp4_quantize_noalloc(const float* v, int64_t rows, int64_t cols, uint8_t* codes,
                                uint8_t* sf, float* sg, void* cuda_stream);
 
+/* ------------------------------------------------------------------------
+ * Dense draft layer (the DSpark page, vllm.models.muse_spark.common.dspark,
+ * MuseSparkDSparkDecoderLayer.forward): the MLP block of one dense layer at
+ * decode, after its attention.
+ *   s1 = s + rmsnorm(attn_out) * w_post_attn               (fp32 stream)
+ *   x  = bf16(rmsnorm(bf16(s1)) * w_pre_ffn)   (the stream is cast to bf16,
+ *                                                the draft's compute type,
+ *                                                before the input norm)
+ *   g, u = bf16(W_gate x), bf16(W_up x)         gate_up_proj shards 0 / 1
+ *   a  = bf16(silu(g) * u);  f = bf16(W_down a)
+ *   s2 = s1 + rmsnorm(f) * w_post_ffn                      (fp32 stream)
+ * The projections are plain bf16 GEMMs (cuBLAS, fp32 accumulation).
+ * ---------------------------------------------------------------------- */
+typedef struct moe_dense_s moe_dense_t;
+
+typedef struct {
+  int hidden;    /* H, multiple of 128, <= 16384 */
+  int inter;     /* I, multiple of 8 */
+  int max_rows;  /* 1..128 */
+  float eps;
+} moe_dense_dims;
+
+typedef struct {                 /* device pointers, caller-owned, 16-byte aligned */
+  const float* w_post_attn;      /* [H] */
+  const float* w_pre_ffn;        /* [H] */
+  const uint16_t* w13;           /* bf16 [2I][H]: gate rows, then up rows */
+  const uint16_t* w2;            /* bf16 [H][I] */
+  const float* w_post_ffn;       /* [H] */
+} moe_dense_weights;
+
+typedef struct {                 /* device pointers into the handle's workspace */
+  void* x;                       /* bf16 [rows][H]  the feed-forward input */
+  void* gu;                      /* bf16 [rows][2I] gate and up projections */
+  void* a;                       /* bf16 [rows][I]  silu(gate) * up */
+  void* f;                       /* bf16 [rows][H]  the feed-forward output */
+} moe_dense_debug_view;
+
+/* Validates the shapes, allocates the workspace and a cuBLAS handle. */
+int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe_dense_t** out);
+
+/* One layer's MLP block for `rows` rows: attn_out bf16 [rows][H] (8-byte
+ * aligned), stream fp32 [rows][H] (16-byte aligned) updated in place.
+ * Asynchronous on cuda_stream; a handle is used by one stream at a time. */
+int moe_dense_layer(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
+                    void* cuda_stream);
+
+/* The same with a CUDA event around each launch (pre-ffn boundary, gate/up
+ * GEMM, SiLU * mul, down GEMM, post-ffn boundary); synchronizes and writes
+ * the five durations (ms) to ms_host[5].  For measurement. */
+int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
+                            void* cuda_stream, float* ms_host);
+
+/* Workspace pointers of the last layer call (see moe_dense_debug_view). */
+int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
+
+void moe_dense_destroy(moe_dense_t* h);
+
 #ifdef __cplusplus
 }
 #endif

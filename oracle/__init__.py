@@ -54,6 +54,9 @@ def lib():
             "oracle_nvfp4_dequantize": (None, [_vp, _vp, _f32, _i64, _i64, _vp]),
             "oracle_boundary": (None, [ctypes.c_int, ctypes.c_int, _f64, _vp, _vp, _vp, _vp, _vp, _vp]),
             "oracle_front": (None, [ctypes.c_int, ctypes.c_int, _f64, _vp, _vp, _vp, _vp, _vp]),
+            "oracle_dense_layer": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64] + [_vp] * 12),
+            "oracle_bf16_linear": (None, [ctypes.c_int] * 3 + [_vp] * 4),
+            "oracle_silu_mul": (None, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
             "oracle_route": (None, [ctypes.c_int] * 4 + [_vp] * 9),
             "oracle_pool": (None, [ctypes.c_int] * 3 + [_vp] * 6),
             "oracle_gate_up": (ctypes.c_int, [ctypes.c_int] * 5 + [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp]),
@@ -157,6 +160,44 @@ def front(embedded, w, eps):
     exact = np.zeros((rows, H))
     lib().oracle_front(rows, H, eps, _p(embedded), _p(w), _p(stream), _p(out), _p(exact))
     return stream, out, exact
+
+
+def dense_layer(attn_out, stream, w_post_attn, w_pre_ffn, w13, w2, w_post_ffn, eps):
+    """One dense draft layer's MLP block -> dict(stream, x, gu, a, f, x_exact):
+    bf16 bits for the intermediates, fp64 for x before its rounding."""
+    attn_out = _c(attn_out, np.uint16)
+    rows, H = attn_out.shape
+    w13, w2 = _c(w13, np.uint16), _c(w2, np.uint16)
+    I = w2.shape[1]
+    s = np.array(stream, dtype=np.float32, copy=True, order="C")
+    out = dict(stream=s, x=np.zeros((rows, H), np.uint16), gu=np.zeros((rows, 2 * I), np.uint16),
+               a=np.zeros((rows, I), np.uint16), f=np.zeros((rows, H), np.uint16),
+               x_exact=np.zeros((rows, H), np.float64))
+    lib().oracle_dense_layer(rows, H, I, eps, _p(attn_out), _p(s), _p(_c(w_post_attn, np.float32)),
+                             _p(_c(w_pre_ffn, np.float32)), _p(w13), _p(w2),
+                             _p(_c(w_post_ffn, np.float32)), _p(out["x"]), _p(out["gu"]),
+                             _p(out["a"]), _p(out["f"]), _p(out["x_exact"]))
+    return out
+
+
+def bf16_linear(a, b):
+    """(bf16 bits of a . b^T, its fp64 value before rounding) for bf16-bit
+    operands a [M, K] and b [N, K]."""
+    a, b = _c(a, np.uint16), _c(b, np.uint16)
+    M, K = a.shape
+    N = b.shape[0]
+    out, exact = np.zeros((M, N), np.uint16), np.zeros((M, N), np.float64)
+    lib().oracle_bf16_linear(M, N, K, _p(a), _p(b), _p(out), _p(exact))
+    return out, exact
+
+
+def silu_mul(gu):
+    """(bf16 bits of silu(gate) * up, its fp64 value) from bf16 bits gu [rows, 2I]."""
+    gu = _c(gu, np.uint16)
+    rows, I = gu.shape[0], gu.shape[1] // 2
+    out, exact = np.zeros((rows, I), np.uint16), np.zeros((rows, I), np.float64)
+    lib().oracle_silu_mul(rows, I, _p(gu), _p(out), _p(exact))
+    return out, exact
 
 
 def route(x, router_w, bias, k):

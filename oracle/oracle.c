@@ -226,6 +226,94 @@ void oracle_front(int rows, int H, double eps, const uint16_t* embedded, const f
   }
 }
 
+/* out[m][n] = bf16(sum_k A[m][k] B[n][k]) over bf16 operands (a projection
+ * y = W x with W [N][K] row-major and x [M][K]), summed in fp64; the sum
+ * before its rounding goes to exact[m][n] when exact is not NULL. */
+void oracle_bf16_linear(int M, int N, int K, const uint16_t* A, const uint16_t* B, uint16_t* out,
+                        double* exact) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int m = 0; m < M; ++m) {
+    for (int n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k)
+        acc += oracle_bf16_decode(A[(int64_t)m * K + k]) * oracle_bf16_decode(B[(int64_t)n * K + k]);
+      out[(int64_t)m * N + n] = oracle_bf16_from_double(acc);
+      if (exact) exact[(int64_t)m * N + n] = acc;
+    }
+  }
+}
+
+/* a[r][j] = bf16(silu(g) * u) with g = gu[r][j] and u = gu[r][I + j] (the
+ * gate half, then the up half of one gate_up_proj output row). */
+void oracle_silu_mul(int rows, int I, const uint16_t* gu, uint16_t* a, double* exact) {
+  for (int r = 0; r < rows; ++r)
+    for (int j = 0; j < I; ++j) {
+      double g = oracle_bf16_decode(gu[(int64_t)r * 2 * I + j]);
+      double u = oracle_bf16_decode(gu[(int64_t)r * 2 * I + I + j]);
+      double v = g / (1.0 + exp(-g)) * u;
+      a[(int64_t)r * I + j] = oracle_bf16_from_double(v);
+      if (exact) exact[(int64_t)r * I + j] = v;
+    }
+}
+
+/* One dense draft layer's MLP block (the DSpark page,
+ * MuseSparkDSparkDecoderLayer.forward): the attention output through
+ * post_attn_norm into the fp32 stream; the feed-forward input is
+ * pre_ffn_norm of the stream after a cast to bf16, the draft's compute type
+ * (the layer casts the stream before every input norm); the gated MLP (gate_proj /
+ * up_proj as shards 0 / 1 of gate_up_proj) in bf16: each projection's
+ * output rounded to bf16, silu(gate) * up rounded to bf16, the down
+ * projection rounded to bf16; its output through post_ffn_norm into the
+ * stream.  Sums in fp64 over the exact bf16 operands.  x_exact (nullable)
+ * receives the MLP input before its bf16 rounding. */
+void oracle_dense_layer(int rows, int H, int I, double eps, const uint16_t* attn_out,
+                        float* stream, const float* w_post_attn, const float* w_pre_ffn,
+                        const uint16_t* w13, const uint16_t* w2, const float* w_post_ffn,
+                        uint16_t* x, uint16_t* gu, uint16_t* a, uint16_t* f, double* x_exact) {
+  double* br = (double*)malloc(sizeof(double) * H);
+  double* t = (double*)malloc(sizeof(double) * H);
+  for (int r = 0; r < rows; ++r) {
+    float* s = stream + (int64_t)r * H;
+    /* s1 = s + rmsnorm(attn_out) * w_post_attn */
+    double ms = 0.0;
+    for (int h = 0; h < H; ++h) {
+      br[h] = oracle_bf16_decode(attn_out[(int64_t)r * H + h]);
+      ms += br[h] * br[h];
+    }
+    double inv_attn = 1.0 / sqrt(ms / H + eps);
+    for (int h = 0; h < H; ++h) s[h] = (float)((double)s[h] + br[h] * inv_attn * (double)w_post_attn[h]);
+    /* x = bf16(rmsnorm(bf16(s1)) * w_pre_ffn) */
+    double ms_ffn = 0.0;
+    for (int h = 0; h < H; ++h) {
+      t[h] = oracle_bf16_decode(oracle_bf16_from_double((double)s[h]));
+      ms_ffn += t[h] * t[h];
+    }
+    double inv_ffn = 1.0 / sqrt(ms_ffn / H + eps);
+    for (int h = 0; h < H; ++h) {
+      double v = t[h] * inv_ffn * (double)w_pre_ffn[h];
+      x[(int64_t)r * H + h] = oracle_bf16_from_double(v);
+      if (x_exact) x_exact[(int64_t)r * H + h] = v;
+    }
+  }
+  /* the gated MLP */
+  oracle_bf16_linear(rows, 2 * I, H, x, w13, gu, NULL);
+  oracle_silu_mul(rows, I, gu, a, NULL);
+  oracle_bf16_linear(rows, H, I, a, w2, f, NULL);
+  /* s2 = s1 + rmsnorm(f) * w_post_ffn */
+  for (int r = 0; r < rows; ++r) {
+    float* s = stream + (int64_t)r * H;
+    double ms = 0.0;
+    for (int h = 0; h < H; ++h) {
+      br[h] = oracle_bf16_decode(f[(int64_t)r * H + h]);
+      ms += br[h] * br[h];
+    }
+    double inv_out = 1.0 / sqrt(ms / H + eps);
+    for (int h = 0; h < H; ++h) s[h] = (float)((double)s[h] + br[h] * inv_out * (double)w_post_ffn[h]);
+  }
+  free(br);
+  free(t);
+}
+
 /* ------------------------------------------------------------------ routing */
 
 static void softmax_row(int E, const double* logit, double* p) {

@@ -71,6 +71,21 @@ void oracle_boundary(int rows, int H, double eps, const double* branch, float* s
  * the value before rounding. */
 void oracle_front(int rows, int H, double eps, const uint16_t* embedded, const float* w,
                   float* stream, uint16_t* out, double* out_exact);
+/* Dense draft layer pieces.  oracle_bf16_linear: out [M][N] = bf16(A [M][K]
+ * . B [N][K]^T), bf16 bits in and out, fp64 sums (exact [M][N], nullable).
+ * oracle_silu_mul: a [rows][I] = bf16(silu(gate) * up) from gu [rows][2I]
+ * (gate columns, then up columns; exact [rows][I], nullable). */
+void oracle_bf16_linear(int M, int N, int K, const uint16_t* A, const uint16_t* B, uint16_t* out,
+                        double* exact);
+void oracle_silu_mul(int rows, int I, const uint16_t* gu, uint16_t* a, double* exact);
+/* One dense draft layer's MLP block: attn_out bf16 bits [rows][H]; stream
+ * fp32 [rows][H] in/out; w13 bf16 bits [2I][H] (gate rows, then up rows);
+ * w2 bf16 bits [H][I].  Intermediates (bf16 bits): x [rows][H], gu
+ * [rows][2I], a [rows][I], f [rows][H]; x_exact fp64 [rows][H] (nullable). */
+void oracle_dense_layer(int rows, int H, int I, double eps, const uint16_t* attn_out,
+                        float* stream, const float* w_post_attn, const float* w_pre_ffn,
+                        const uint16_t* w13, const uint16_t* w2, const float* w_post_ffn,
+                        uint16_t* x, uint16_t* gu, uint16_t* a, uint16_t* f, double* x_exact);
 /* Router + routing.  x bf16 [rows][H]; router_w bf16 [E][H]; bias fp32 [E] or
  * NULL.  Outputs: logits fp64 [rows][E] (optional), probs fp64 [rows][E]
  * (optional), ids int32 [rows][k] (slot order: descending p), gates fp64

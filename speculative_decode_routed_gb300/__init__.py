@@ -25,6 +25,8 @@ EXPORTS = (
     "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_step_kernel_count",
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
+    "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
+    "moe_dense_destroy",
 )
 
 
@@ -44,6 +46,19 @@ class Dims(ctypes.Structure):
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_post", "w_pre", "router_w", "router_bias", "w13", "w13_sf", "w2", "w2_sf", "w_gscale")]
+
+
+class DenseDims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("max_rows", ctypes.c_int),
+                ("eps", ctypes.c_float)]
+
+
+class DenseWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_post_attn", "w_pre_ffn", "w13", "w2", "w_post_ffn")]
+
+
+class DenseDebugView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "gu", "a", "f")]
 
 
 class DebugView(ctypes.Structure):
@@ -83,6 +98,12 @@ def _lib():
             "moe_decode_error_message": (ctypes.c_char_p, []),
             "moe_nvfp4_quantize": (i32, [vp, i64, i64, vp, vp, vp, vp, vp]),
             "moe_nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
+            "moe_dense_create": (i32, [ctypes.POINTER(DenseDims), ctypes.POINTER(DenseWeights),
+                                       ctypes.POINTER(vp)]),
+            "moe_dense_layer": (i32, [vp, i32, vp, vp, vp]),
+            "moe_dense_layer_profile": (i32, [vp, i32, vp, vp, vp, vp]),
+            "moe_dense_debug": (i32, [vp, ctypes.POINTER(DenseDebugView)]),
+            "moe_dense_destroy": (None, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -269,6 +290,51 @@ class MoEDecode:
     def close(self):
         if self.handle:
             moe_decode_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------- dense draft layer
+
+
+class DenseLayer:
+    """One dense draft layer's MLP block (moe_dense_*) over caller-owned
+    device tensors: w_post_attn, w_pre_ffn, w_post_ffn fp32 [H]; w13 bf16
+    [2I, H] (gate rows, then up rows); w2 bf16 [H, I]."""
+
+    def __init__(self, hidden, inter, max_rows, w_post_attn, w_pre_ffn, w13, w2, w_post_ffn,
+                 eps=1e-6):
+        dims = DenseDims(hidden, inter, max_rows, eps)
+        self._keep = (w_post_attn, w_pre_ffn, w13, w2, w_post_ffn)
+        wts = DenseWeights(*[t.data_ptr() for t in self._keep])
+        out = ctypes.c_void_p()
+        _check(_lib().moe_dense_create(ctypes.byref(dims), ctypes.byref(wts), ctypes.byref(out)),
+               "moe_dense_create")
+        self.handle = out
+
+    def layer(self, rows, attn_out, stream_buf, stream=None):
+        _check(_lib().moe_dense_layer(self.handle, rows, _ptr(attn_out), _ptr(stream_buf),
+                                      _stream(stream)), "moe_dense_layer")
+
+    def layer_profile(self, rows, attn_out, stream_buf, stream=None):
+        ms = (ctypes.c_float * 5)()
+        _check(_lib().moe_dense_layer_profile(self.handle, rows, _ptr(attn_out), _ptr(stream_buf),
+                                              _stream(stream), ms), "moe_dense_layer_profile")
+        return list(ms)
+
+    def debug(self) -> DenseDebugView:
+        v = DenseDebugView()
+        _check(_lib().moe_dense_debug(self.handle, ctypes.byref(v)), "moe_dense_debug")
+        return v
+
+    def close(self):
+        if self.handle:
+            _lib().moe_dense_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -118,7 +118,14 @@ __global__ void boundary_kernel(BoundaryParams p) {
     if (p.aux) *reinterpret_cast<float4*>(p.aux + (size_t)r * p.H + col) = s;
   }
 
-  // rms of the updated stream
+  // rms of the updated stream (the dense draft layer rounds the stream to
+  // bf16 before its trained input norms)
+  if (p.round_norm) {
+    s.x = __bfloat162float(__float2bfloat16_rn(s.x));
+    s.y = __bfloat162float(__float2bfloat16_rn(s.y));
+    s.z = __bfloat162float(__float2bfloat16_rn(s.z));
+    s.w = __bfloat162float(__float2bfloat16_rn(s.w));
+  }
   block_sum_to_slot(s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w, warp_red, &part[1]);
   cluster.sync();
   float ss2 = 0.0f;
@@ -126,7 +133,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
   const float inv2 = rsqrtf(ss2 / (float)p.H + p.eps);
 
   float m = 0.0f;
-  if (live) {
+  if (live && p.x_out) {
     const __nv_bfloat162 x01 = __floats2bfloat162_rn(s.x * inv2 * wpre.x, s.y * inv2 * wpre.y);
     const __nv_bfloat162 x23 = __floats2bfloat162_rn(s.z * inv2 * wpre.z, s.w * inv2 * wpre.w);
     uint2 packed;
@@ -151,6 +158,12 @@ __global__ void boundary_kernel(BoundaryParams p) {
 }
 
 }  // namespace
+
+int boundary_cluster(int H) {
+  for (int c = 8; c >= 1; c >>= 1)
+    if (H % (c * 128) == 0) return H / c <= 4096 ? c : 8;
+  return 8;
+}
 
 cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl) {
   const int threads = ((p.cols_per_cta / 4 + 31) / 32) * 32;

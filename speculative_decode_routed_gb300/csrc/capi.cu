@@ -563,13 +563,7 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
   h->w_final = w_final;
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
-  // boundary: the largest cluster (<= 8) whose CTAs get whole 128-column slabs
-  h->cluster = 1;
-  for (int c = 8; c >= 1; c >>= 1)
-    if (d.hidden % (c * 128) == 0) {
-      h->cluster = c;
-      break;
-    }
+  h->cluster = moe::boundary_cluster(d.hidden);
   // router: one warp per expert, H split into slices of at most 1024
   h->EG = 8;
   h->n_eg = (d.n_experts + h->EG - 1) / h->EG;

@@ -1,0 +1,244 @@
+// One dense draft layer's MLP block at decode (after its attention, which is
+// not part of this library).
+//
+// Page: vllm.models.muse_spark.common.dspark, MuseSparkDSparkDecoderLayer
+// .forward: the stream is fp32 (a plain add of each normalised branch, as
+// in the routed layers); the attention output enters through post_attn_norm;
+// the feed-forward reads pre_ffn_norm of the stream cast to the draft's
+// compute dtype (bf16), a cast the layer makes before every input norm; its
+// output enters through post_ffn_norm.  The
+// feed-forward is the dense gated MLP (gate_proj / up_proj stacked as shards
+// 0 / 1 of gate_up_proj, the same page's weight mapping) in bf16:
+//   s1 = s + rmsnorm(attn_out) * w_post_attn                 (fp32)
+//   x  = bf16(rmsnorm(bf16(s1)) * w_pre_ffn)
+//   g, u = bf16(W_gate x), bf16(W_up x)                      (fp32 accumulation)
+//   a  = bf16(silu(g) * u)
+//   f  = bf16(W_down a)
+//   s2 = s1 + rmsnorm(f) * w_post_ffn                        (fp32)
+//
+// GB300 layout: the norms run in the boundary kernel (cluster per row); the
+// two projections are plain bf16 GEMMs of a few rows (cuBLAS, fp32 compute,
+// bf16 out, weights streamed once); SiLU * mul is one elementwise kernel.
+#include <cublas_v2.h>
+
+#include <cstdio>
+
+#include "../../include/moe_decode.h"
+#include "common.cuh"
+#include "moe_decode_internal.h"
+
+namespace moe {
+namespace {
+
+__global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int I, int n,
+                                __nv_bfloat16* __restrict__ a) {
+  // gu: [rows][2I] (gate columns, then up columns); a: [rows][I]; n = rows * I
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int r = i / I, j = i % I;
+    const float g = __bfloat162float(gu[(size_t)r * 2 * I + j]);
+    const float u = __bfloat162float(gu[(size_t)r * 2 * I + I + j]);
+    a[i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+struct moe_dense_s {
+  moe_dense_dims d;
+  moe_dense_weights w;
+  int cluster;
+  cublasHandle_t blas;
+  void* blas_ws;
+  size_t blas_ws_bytes;
+  __nv_bfloat16 *x, *gu, *a, *f;  // [R][H], [R][2I], [R][I], [R][H]
+};
+
+namespace {
+
+constexpr size_t kBlasWorkspace = 8u << 20;
+
+bool dense_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int blas_fail(cublasStatus_t st, const char* what) {
+  char buf[160];
+  snprintf(buf, sizeof(buf), "%s: cuBLAS status %d", what, (int)st);
+  return moe::api_fail(MOE_ECUDA, buf);
+}
+
+int cuda_err(cudaError_t e, const char* what) {
+  char buf[200];
+  snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
+  return moe::api_fail(MOE_ECUDA, buf);
+}
+
+// The dense layer's launches on s; with ev, an event before each and after
+// the last (boundary, gate/up, SiLU * mul, down, boundary).
+int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
+                  cudaStream_t s, cudaEvent_t* ev) {
+  const moe_dense_dims& d = h->d;
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  mark(0);
+  moe::BoundaryParams bp{};
+  bp.H = d.hidden;
+  bp.k = 1;
+  bp.rows = rows;
+  bp.cols_per_cta = d.hidden / h->cluster;
+  bp.eps = d.eps;
+  bp.branch = reinterpret_cast<const __nv_bfloat16*>(attn_out);
+  bp.stream = stream;
+  bp.w_post = h->w.w_post_attn;
+  bp.w_pre = h->w.w_pre_ffn;
+  bp.x_out = h->x;
+  bp.round_norm = 1;
+  cudaError_t e = moe::launch_boundary(bp, h->cluster, s, false);
+  if (e != cudaSuccess) return cuda_err(e, "pre-ffn boundary launch");
+  mark(1);
+  cublasStatus_t st = cublasSetStream(h->blas, s);
+  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "cublasSetStream");
+  const float one = 1.0f, zero = 0.0f;
+  // gu [rows][2I] = x [rows][H] . W13^T  (column-major: W13 is H x 2I)
+  st = cublasGemmEx(h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * d.inter, rows, d.hidden, &one,
+                    h->w.w13, CUDA_R_16BF, d.hidden, h->x, CUDA_R_16BF, d.hidden, &zero, h->gu,
+                    CUDA_R_16BF, 2 * d.inter, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "gate/up GEMM");
+  mark(2);
+  const int n = rows * d.inter;
+  moe::silu_mul_kernel<<<(n + 255) / 256, 256, 0, s>>>(h->gu, d.inter, n, h->a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_err(e, "SiLU * mul launch");
+  mark(3);
+  // f [rows][H] = a [rows][I] . W2^T  (column-major: W2 is I x H)
+  st = cublasGemmEx(h->blas, CUBLAS_OP_T, CUBLAS_OP_N, d.hidden, rows, d.inter, &one, h->w.w2,
+                    CUDA_R_16BF, d.inter, h->a, CUDA_R_16BF, d.inter, &zero, h->f, CUDA_R_16BF,
+                    d.hidden, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "down GEMM");
+  mark(4);
+  bp.branch = h->f;
+  bp.w_post = h->w.w_post_ffn;
+  bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
+  bp.x_out = nullptr;
+  bp.round_norm = 0;
+  e = moe::launch_boundary(bp, h->cluster, s, false);
+  if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
+  mark(5);
+  return MOE_OK;
+}
+
+int check_rows_dense(const moe_dense_t* h, int rows) {
+  if (rows < 1 || rows > h->d.max_rows) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "rows %d outside [1, max_rows=%d]", rows, h->d.max_rows);
+    return moe::api_fail(MOE_EINVAL, buf);
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe_dense_t** out) {
+  if (!dims || !w || !out) return moe::api_fail(MOE_EINVAL, "dims, weights and out are required");
+  *out = nullptr;
+  const moe_dense_dims d = *dims;
+  if (d.hidden <= 0 || d.hidden % 128 || d.hidden > 16384)
+    return moe::api_fail(MOE_EUNSUPPORTED, "hidden must be a positive multiple of 128, at most 16384");
+  if (d.inter <= 0 || d.inter % 8)
+    return moe::api_fail(MOE_EUNSUPPORTED, "inter must be a positive multiple of 8");
+  if (d.max_rows < 1 || d.max_rows > 128) return moe::api_fail(MOE_EUNSUPPORTED, "max_rows must be in [1, 128]");
+  if (!(d.eps > 0.0f)) return moe::api_fail(MOE_EINVAL, "eps must be positive");
+  if (!w->w_post_attn || !w->w_pre_ffn || !w->w13 || !w->w2 || !w->w_post_ffn)
+    return moe::api_fail(MOE_EINVAL, "a required weight pointer is NULL");
+  if (!dense_aligned(w->w_post_attn, 16) || !dense_aligned(w->w_pre_ffn, 16) ||
+      !dense_aligned(w->w_post_ffn, 16) || !dense_aligned(w->w13, 16) || !dense_aligned(w->w2, 16))
+    return moe::api_fail(MOE_EINVAL, "weight pointers must be 16-byte aligned");
+  int dev = 0, major = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e != cudaSuccess) return cuda_err(e, "device query");
+  if (major != 10) return moe::api_fail(MOE_EUNSUPPORTED, "needs an SM 10.x GPU");
+  moe_dense_t* h = new moe_dense_t{};
+  h->d = d;
+  h->w = *w;
+  h->cluster = moe::boundary_cluster(d.hidden);
+  const size_t R = (size_t)d.max_rows, H = (size_t)d.hidden, I = (size_t)d.inter;
+  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H);
+  uint8_t* base = nullptr;
+  e = cudaMalloc(&base, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kBlasWorkspace);
+  if (e != cudaSuccess) {
+    moe_dense_destroy(h);
+    cudaFree(base);
+    return moe::api_fail(MOE_ENOMEM, "dense layer workspace");
+  }
+  h->blas_ws_bytes = kBlasWorkspace;
+  h->x = reinterpret_cast<__nv_bfloat16*>(base);
+  h->gu = h->x + R * H;
+  h->a = h->gu + R * 2 * I;
+  h->f = h->a + R * I;
+  cublasStatus_t st = cublasCreate(&h->blas);
+  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, h->blas_ws_bytes);
+  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);
+  if (st != CUBLAS_STATUS_SUCCESS) {
+    moe_dense_destroy(h);
+    return blas_fail(st, "cuBLAS set-up");
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_dense_layer(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
+                    void* cuda_stream) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  int rc = check_rows_dense(h, rows);
+  if (rc) return rc;
+  if (!attn_out || !stream || !dense_aligned(attn_out, 8) || !dense_aligned(stream, 16))
+    return moe::api_fail(MOE_EINVAL, "attn_out (8-byte) and stream (16-byte) must be aligned device pointers");
+  return dense_enqueue(h, rows, attn_out, stream, static_cast<cudaStream_t>(cuda_stream), nullptr);
+}
+
+int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
+                            void* cuda_stream, float* ms_host) {
+  if (!h || !ms_host) return moe::api_fail(MOE_EINVAL, "handle and ms_host are required");
+  int rc = check_rows_dense(h, rows);
+  if (rc) return rc;
+  if (!attn_out || !stream || !dense_aligned(attn_out, 8) || !dense_aligned(stream, 16))
+    return moe::api_fail(MOE_EINVAL, "attn_out (8-byte) and stream (16-byte) must be aligned device pointers");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaEvent_t ev[6] = {};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  if (e == cudaSuccess) {
+    rc = dense_enqueue(h, rows, attn_out, stream, s, ev);
+    if (!rc) e = cudaEventSynchronize(ev[5]);
+    for (int i = 0; i < 5 && !rc && e == cudaSuccess; ++i)
+      e = cudaEventElapsedTime(&ms_host[i], ev[i], ev[i + 1]);
+  }
+  for (int i = 0; i < 6; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  if (rc) return rc;
+  if (e != cudaSuccess) return cuda_err(e, "profile events");
+  return MOE_OK;
+}
+
+int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* v) {
+  if (!h || !v) return moe::api_fail(MOE_EINVAL, "handle and view are required");
+  v->x = h->x;
+  v->gu = h->gu;
+  v->a = h->a;
+  v->f = h->f;
+  return MOE_OK;
+}
+
+void moe_dense_destroy(moe_dense_t* h) {
+  if (!h) return;
+  if (h->blas) cublasDestroy(h->blas);
+  cudaFree(h->blas_ws);
+  cudaFree(h->x);
+  delete h;
+}
+
+}  // extern "C"

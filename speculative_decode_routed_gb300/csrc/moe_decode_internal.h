@@ -85,7 +85,8 @@ struct BoundaryParams {
   int front;                    // 1: the first layer's front -- the stream is the branch (the
                                 //    embedded tokens) itself, one norm (w_pre) into x_out
   float* aux;                   // [rows][H] copy of the updated stream, or null
-};
+  int round_norm;               // 1: the second norm reads the stream rounded to bf16
+};                              // (x_out may be null: no normalised output)
 
 // ------------------------------------------------------------- router (K2)
 struct RouterParams {
@@ -128,6 +129,10 @@ constexpr int kMaxCTAThreads = 512;
 constexpr int kSmemBudget = 226 * 1024;  // of the 227 KB a CTA may use
 
 // Host-side launchers (one per kernel family).
+// Cluster size of the boundary kernel for a row of H columns (H a multiple
+// of 32): the largest cluster (<= 8) whose CTAs get whole 128-column slabs,
+// unless that leaves a CTA more than 4096 columns (1024 threads of 4), then 8.
+int boundary_cluster(int H);
 cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s, bool pdl);

@@ -39,6 +39,9 @@ KIND_W_FINAL = 10
 KIND_ZIPF_PERM = 11
 KIND_EMBED = 12
 KIND_W_FRONT = 13
+KIND_DENSE_W13 = 14
+KIND_DENSE_W2 = 15
+KIND_W_POST_FFN = 16
 
 
 def tag(kind: int, layer: int = 0, index: int = 0) -> int:
@@ -196,6 +199,16 @@ WORKLOADS = {
 }
 SWEEP_ROWS = (1, 8, 32, 64, 128)
 
+# Dense draft layers (no experts: n_experts and top_k are 0).  The pages give
+# no draft widths; hidden follows the target and the MLP is four times as wide,
+# so one layer's bf16 weights (1.41 GB) dwarf the L2.
+DENSE_WORKLOADS = {
+    "draft_dense": Workload("draft_dense", rows=8, hidden=7168, n_experts=0, top_k=0,
+                            inter=28672),
+    "draft_dense_small": Workload("draft_dense_small", rows=8, hidden=256, n_experts=0, top_k=0,
+                                  inter=384),
+}
+
 
 def step_inputs(w: Workload, variant: int = 0):
     """(stream fp32 [b,H], branch bf16-bits [b,H]) of one step; `variant` selects
@@ -256,3 +269,29 @@ def dev_expert_raw(out, w: Workload, layer: int, expert: int, which: str, stream
     """Device twin of expert_raw, into the fp32 CUDA tensor `out`."""
     kind = {"gate": KIND_GATE, "up": KIND_UP, "down": KIND_DOWN}[which]
     return dev_normal_f32(out, w.seed, tag(kind, layer, expert), *w.expert_dist, stream=stream)
+
+
+# ----------------------------------------------------------------------------- dense draft layer
+
+
+def dense_norm_weights(w: Workload, layer: int):
+    """(w_post_attn, w_pre_ffn, w_post_ffn) fp32 [H] of one dense layer, each
+    1 + 0.1 N(0, 1); the first two are the routed layers' (w_post, w_pre)."""
+    post_attn, pre_ffn = norm_weights(w, layer)
+    post_ffn = normal_f32((w.hidden,), w.seed, tag(KIND_W_POST_FFN, layer), *w.norm_dist)
+    return post_attn, pre_ffn, post_ffn
+
+
+def dense_weights(w: Workload, layer: int):
+    """(w13 bf16 bits [2I, H]: gate rows then up rows, w2 bf16 bits [H, I]),
+    every entry N(0, 0.02)."""
+    w13 = normal_bf16((2 * w.inter, w.hidden), w.seed, tag(KIND_DENSE_W13, layer), *w.expert_dist)
+    w2 = normal_bf16((w.hidden, w.inter), w.seed, tag(KIND_DENSE_W2, layer), *w.expert_dist)
+    return w13, w2
+
+
+def dev_dense_weights(w13, w2, w: Workload, layer: int, stream=None):
+    """Device twin of dense_weights, into bf16 CUDA tensors [2I, H] and [H, I]."""
+    dev_normal_bf16(w13, w.seed, tag(KIND_DENSE_W13, layer), *w.expert_dist, stream=stream)
+    dev_normal_bf16(w2, w.seed, tag(KIND_DENSE_W2, layer), *w.expert_dist, stream=stream)
+    return w13, w2

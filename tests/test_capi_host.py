@@ -81,3 +81,42 @@ def test_calls_on_a_null_handle_fail_cleanly():
     assert L.moe_decode_strerror(moe.MOE_EDEVICE).decode() == "device-side check failed"
     assert L.moe_nvfp4_quantize(None, 1, 16, None, None, None, None, None) == moe.MOE_EINVAL
     assert L.moe_nvfp4_quantize(1 << 20, 1, 17, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None) == moe.MOE_EINVAL
+
+
+def _dense_create(hidden=256, inter=128, max_rows=8, eps=1e-6, null=None, shift=None):
+    dims = moe.DenseDims(hidden, inter, max_rows, eps)
+    ptrs = [(1 << 20) + i * 256 for i in range(5)]
+    if null is not None:
+        ptrs[null] = None
+    if shift is not None:
+        ptrs[shift] += 4
+    w = moe.DenseWeights(*ptrs)
+    h = ctypes.c_void_p()
+    rc = moe.lib().moe_dense_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(h))
+    return rc, moe.lib().moe_decode_error_message().decode()
+
+
+@pytest.mark.parametrize("kw", [dict(hidden=200), dict(hidden=16512), dict(hidden=0),
+                                dict(inter=100), dict(inter=0), dict(max_rows=0),
+                                dict(max_rows=129)])
+def test_dense_unsupported_shapes(kw):
+    rc, msg = _dense_create(**kw)
+    assert rc == moe.MOE_EUNSUPPORTED, (kw, rc, msg)
+    assert msg
+
+
+def test_dense_invalid_arguments():
+    for i in range(5):
+        rc, msg = _dense_create(null=i)
+        assert rc == moe.MOE_EINVAL and "NULL" in msg
+        rc, msg = _dense_create(shift=i)
+        assert rc == moe.MOE_EINVAL and "aligned" in msg
+    rc, msg = _dense_create(eps=0.0)
+    assert rc == moe.MOE_EINVAL and "eps" in msg
+    L = moe.lib()
+    assert L.moe_dense_create(None, None, None) == moe.MOE_EINVAL
+    assert L.moe_dense_layer(None, 1, None, None, None) == moe.MOE_EINVAL
+    ms = (ctypes.c_float * 5)()
+    assert L.moe_dense_layer_profile(None, 1, None, None, None, ms) == moe.MOE_EINVAL
+    assert L.moe_dense_debug(None, None) == moe.MOE_EINVAL
+    L.moe_dense_destroy(None)

@@ -83,6 +83,28 @@ MUTANTS = [
      "acc += gates[r * k + s] * (double)o[((int64_t)r * k + s) * H + hh];",
      "acc += (double)o[((int64_t)r * k + s) * H + hh];",
      [("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {})]),
+    ("dense: MLP input normalises the uncast stream",
+     "t[h] = oracle_bf16_decode(oracle_bf16_from_double((double)s[h]));", "t[h] = (double)s[h];",
+     [("test_oracle_dense", "test_mlp_input_normalises_the_stream_cast_to_bf16", {})]),
+    ("dense: post-attention norm without eps",
+     "double inv_attn = 1.0 / sqrt(ms / H + eps);", "double inv_attn = 1.0 / sqrt(ms / H);",
+     [("test_oracle_dense", "test_post_attention_norm_of_constant_rows_closed_form", {})]),
+    ("dense: silu on up instead of gate",
+     "double v = g / (1.0 + exp(-g)) * u;", "double v = u / (1.0 + exp(-u)) * g;",
+     [("test_oracle_dense", "test_single_entry_weights_name_each_product", {})]),
+    ("dense: projection weight read transposed",
+     "* oracle_bf16_decode(B[(int64_t)n * K + k]);", "* oracle_bf16_decode(B[(int64_t)k * N + n]);",
+     [("test_oracle_dense", "test_projections_are_library_matmuls_over_exact_sums", {}),
+      ("test_oracle_dense", "test_single_entry_weights_name_each_product", {})]),
+    ("dense: output norm weight dropped",
+     "s[h] = (float)((double)s[h] + br[h] * inv_out * (double)w_post_ffn[h]);",
+     "s[h] = (float)((double)s[h] + br[h] * inv_out);",
+     [("test_oracle_dense", "test_output_norm_of_a_constant_down_projection", {}),
+      ("test_oracle_dense", "test_scale_free_without_eps", {})]),
+    ("dense: output branch added without its norm",
+     "double inv_out = 1.0 / sqrt(ms / H + eps);", "double inv_out = 1.0;",
+     [("test_oracle_dense", "test_output_norm_of_a_constant_down_projection", {}),
+      ("test_oracle_dense", "test_scale_free_without_eps", {})]),
 ]
 
 
