@@ -314,6 +314,93 @@ void oracle_dense_layer(int rows, int H, int I, double eps, const uint16_t* attn
   free(t);
 }
 
+/* The draft's context-KV projection (the DSpark page, _project_muse_context_kv
+ * and precompute_and_store_context_kv).
+ *
+ * Norms: fc = bf16(rmsnorm(ctx) * w_hidden) (hidden_norm), then each layer's
+ * pre_qkv_proj_norm of fc: u[l] = bf16(rmsnorm(fc) * w_pre[l]).  The weights
+ * are the effective ones (a zero-centred gamma is passed as 1 + gamma). */
+void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, const float* w_hidden,
+                      const float* w_pre, uint16_t* fc, uint16_t* u, double* u_exact) {
+  for (int r = 0; r < n; ++r) {
+    const uint16_t* c = ctx + (int64_t)r * H;
+    uint16_t* f = fc + (int64_t)r * H;
+    double ms = 0.0;
+    for (int h = 0; h < H; ++h) ms += oracle_bf16_decode(c[h]) * oracle_bf16_decode(c[h]);
+    double inv_hidden = 1.0 / sqrt(ms / H + eps);
+    for (int h = 0; h < H; ++h)
+      f[h] = oracle_bf16_from_double(oracle_bf16_decode(c[h]) * inv_hidden * (double)w_hidden[h]);
+    double ms_fc = 0.0;
+    for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(f[h]) * oracle_bf16_decode(f[h]);
+    double inv_pre = 1.0 / sqrt(ms_fc / H + eps);
+    for (int l = 0; l < L; ++l)
+      for (int h = 0; h < H; ++h) {
+        double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_pre[(int64_t)l * H + h];
+        int64_t o = ((int64_t)l * n + r) * H + h;
+        u[o] = oracle_bf16_from_double(v);
+        if (u_exact) u_exact[o] = v;
+      }
+  }
+}
+
+/* The keys' RMSNorm and rotary embedding.  kv [L][n][2*KVH*D] holds each
+ * layer's projection (the K heads, then the V heads).  Each K head of D
+ * values is normalised in fp32 without a weight, k = bf16(k / sqrt(mean(k^2)
+ * + qk_eps)), then rotated by its row's position: the rotary embedding of
+ * RoFormer (Su et al., 2021) with the dimensions paired as (j, j + D/2) and
+ * angle pos * theta^(-2j/D), each output rounded to bf16 once.  theta = 0
+ * leaves the keys unrotated.  V passes through.  k_exact (nullable) gets the
+ * rotated keys before their rounding. */
+void oracle_k_norm_rope(int L, int n, int KVH, int D, double qk_eps, double theta,
+                        const int64_t* positions, const uint16_t* kv, uint16_t* k_out,
+                        uint16_t* v_out, double* k_exact) {
+  const int KD = KVH * D, half = D / 2;
+  double* kn = (double*)malloc(sizeof(double) * D);
+  for (int l = 0; l < L; ++l)
+    for (int r = 0; r < n; ++r) {
+      const uint16_t* row = kv + ((int64_t)l * n + r) * 2 * KD;
+      for (int hd = 0; hd < KVH; ++hd) {
+        const uint16_t* k = row + hd * D;
+        int64_t o = (((int64_t)l * n + r) * KVH + hd) * D;
+        double ms = 0.0;
+        for (int i = 0; i < D; ++i) ms += oracle_bf16_decode(k[i]) * oracle_bf16_decode(k[i]);
+        double inv = 1.0 / sqrt(ms / D + qk_eps);
+        for (int i = 0; i < D; ++i) kn[i] = oracle_bf16_decode(oracle_bf16_from_double(oracle_bf16_decode(k[i]) * inv));
+        for (int j = 0; j < half; ++j) {
+          double x1 = kn[j], x2 = kn[j + half], y1 = x1, y2 = x2;
+          if (theta > 0.0) {
+            double ang = (double)positions[r] * pow(theta, -2.0 * j / D);
+            y1 = x1 * cos(ang) - x2 * sin(ang);
+            y2 = x2 * cos(ang) + x1 * sin(ang);
+          }
+          k_out[o + j] = oracle_bf16_from_double(y1);
+          k_out[o + j + half] = oracle_bf16_from_double(y2);
+          if (k_exact) {
+            k_exact[o + j] = y1;
+            k_exact[o + j + half] = y2;
+          }
+        }
+        memcpy(v_out + o, row + KD + hd * D, sizeof(uint16_t) * D);
+      }
+    }
+  free(kn);
+}
+
+/* The cache update: layer l's rows go to cache[l][slot][KVH][D] for slot =
+ * slots[l * layer_stride + r]; a negative slot writes nothing. */
+void oracle_kv_cache_write(int L, int n, int KVH, int D, const int64_t* slots, int layer_stride,
+                           int64_t n_slots, const uint16_t* k, const uint16_t* v, uint16_t* k_cache,
+                           uint16_t* v_cache) {
+  const int64_t KD = (int64_t)KVH * D;
+  for (int l = 0; l < L; ++l)
+    for (int r = 0; r < n; ++r) {
+      int64_t slot = slots[(int64_t)l * layer_stride + r];
+      if (slot < 0 || slot >= n_slots) continue;
+      memcpy(k_cache + ((int64_t)l * n_slots + slot) * KD, k + ((int64_t)l * n + r) * KD, sizeof(uint16_t) * KD);
+      memcpy(v_cache + ((int64_t)l * n_slots + slot) * KD, v + ((int64_t)l * n + r) * KD, sizeof(uint16_t) * KD);
+    }
+}
+
 /* ------------------------------------------------------------------ routing */
 
 static void softmax_row(int E, const double* logit, double* p) {

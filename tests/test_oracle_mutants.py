@@ -105,6 +105,30 @@ MUTANTS = [
      "double inv_out = 1.0 / sqrt(ms / H + eps);", "double inv_out = 1.0;",
      [("test_oracle_dense", "test_output_norm_of_a_constant_down_projection", {}),
       ("test_oracle_dense", "test_scale_free_without_eps", {})]),
+    ("context KV: rotation with the sine's sign flipped",
+     "y1 = x1 * cos(ang) - x2 * sin(ang);", "y1 = x1 * cos(ang) + x2 * sin(ang);",
+     [("test_oracle_ctxkv", "test_one_hot_key_rotates_into_its_partner_dimension", {})]),
+    ("context KV: rotation angle exponent -j/D",
+     "pow(theta, -2.0 * j / D)", "pow(theta, -1.0 * j / D)",
+     [("test_oracle_ctxkv", "test_one_hot_key_rotates_into_its_partner_dimension", {})]),
+    ("context KV: key norm without eps",
+     "double inv = 1.0 / sqrt(ms / D + qk_eps);", "double inv = 1.0 / sqrt(ms / D);",
+     [("test_oracle_ctxkv", "test_key_norm_of_constant_heads_and_values_pass_through", {})]),
+    ("context KV: keys rotated before their bf16 cast",
+     "kn[i] = oracle_bf16_decode(oracle_bf16_from_double(oracle_bf16_decode(k[i]) * inv));",
+     "kn[i] = oracle_bf16_decode(k[i]) * inv;",
+     [("test_oracle_ctxkv", "test_one_hot_key_rotates_into_its_partner_dimension", {})]),
+    ("context KV: layer norms weighted by the hidden norm's weight",
+     "double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_pre[(int64_t)l * H + h];",
+     "double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_hidden[h];",
+     [("test_oracle_ctxkv", "test_constant_rows_closed_form", {})]),
+    ("context KV: layer norms over the raw context",
+     "for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(f[h]) * oracle_bf16_decode(f[h]);",
+     "for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(c[h]) * oracle_bf16_decode(c[h]);",
+     [("test_oracle_ctxkv", "test_constant_rows_closed_form", {})]),
+    ("context KV: every layer's keys written to layer 0's cache",
+     "memcpy(k_cache + ((int64_t)l * n_slots + slot) * KD,", "memcpy(k_cache + (slot) * KD,",
+     [("test_oracle_ctxkv", "test_cache_scatter_by_brute_force", {})]),
 ]
 
 
