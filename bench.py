@@ -232,9 +232,58 @@ def dense_cpu_baseline(w: synth.Workload):
                 "sample": f"the whole dense layer on all {w.rows} rows (no sampling)"}
 
 
+CTXKV_METRIC = "draft context-KV projection µs at 8 context rows and weight-stream HBM GB/s vs GB300 peak"
+
+
+def _ctxkv_bytes(w, n: int):
+    """Bytes one projection must move at minimum: the stacked K/V weights once,
+    the context, the layer inputs and projections once each way, the keys and
+    values into the cache."""
+    L, H, KD = w.n_layers, w.hidden, w.n_kv_heads * w.head_dim
+    weights = L * 2 * KD * H * 2
+    gemm = weights + L * n * H * 2 + L * n * 2 * KD * 2
+    rest = n * H * 2 + (H + L * H) * 4 + n * H * 2 + L * n * H * 2 + L * n * 2 * KD * 2 * 3 + n * 16
+    return dict(gemm=gemm, total=gemm + rest)
+
+
+def ctxkv_cpu_baseline(w):
+    """The CPU oracle's whole projection (all rows, all layers, the cache write);
+    weight generation is not timed.  -> (us, info)."""
+    import oracle
+    ctx, pos, slots = synth.ctxkv_inputs(w)
+    wh, wp = synth.ctxkv_norm_weights(w)
+    wkv = synth.ctxkv_weights(w)
+    shape = (w.n_layers, w.n_slots, w.n_kv_heads, w.head_dim)
+    kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    t0 = time.perf_counter()
+    o = oracle.context_kv(ctx, pos, wh, wp, wkv, w.n_kv_heads, w.head_dim, w.eps, w.qk_eps, w.rope_theta)
+    oracle.kv_cache_write(o["k"], o["v"], slots, w.n_slots, kc, vc)
+    us = (time.perf_counter() - t0) * 1e6
+    return us, {"kind": "oracle", "cores": oracle.num_threads(),
+                "sample": f"the whole projection of all {w.n_ctx} rows into {w.n_layers} layers (no sampling)"}
+
+
 def run_reference(args, w):
     ws, rank, _ = _dist()
     if rank != 0:
+        return
+    if isinstance(w, synth.CtxKvWorkload):
+        times, info = [], None
+        for i in range(args.warmup + args.steps):
+            us, info = ctxkv_cpu_baseline(w)
+            if i >= args.warmup:
+                times.append(us)
+        v = float(np.mean(times))
+        line = {"impl": "reference", "metric": CTXKV_METRIC, "value": round(v, 1), "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(v / 1000.0, 3), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "n_ctx": w.n_ctx, "hidden": w.hidden,
+                           "n_layers": w.n_layers, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim},
+                "cpu_baseline": dict(info, value=round(v, 1), unit=UNIT),
+                "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     if w.n_experts == 0:
         times, info = [], None
@@ -550,6 +599,151 @@ def run_dense(args, w):
         dist.destroy_process_group()
 
 
+def run_ctxkv(args, w):
+    """The draft context-KV projection of n_ctx rows into every draft layer and the
+    cache, replayed as a CUDA graph per input draw.  The stacked weights fit in
+    L2, so a buffer larger than L2 is written before every timed step, outside
+    the events that time it."""
+    import torch
+
+    import speculative_decode_routed_gb300 as moe
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    L, H, KVH, D, n = w.n_layers, w.hidden, w.n_kv_heads, w.head_dim, w.n_ctx
+    wkv = torch.empty(L, 2 * KVH * D, H, dtype=torch.bfloat16, device=device)
+    synth.dev_ctxkv_weights(wkv, w)
+    wh, wp = (torch.from_numpy(a).to(device) for a in synth.ctxkv_norm_weights(w))
+    op = moe.ContextKV(H, L, KVH, D, n, wh, wp, wkv, eps=w.eps, qk_eps=w.qk_eps,
+                       rope_theta=w.rope_theta, max_position=w.max_position)
+    kc = torch.zeros(L, w.n_slots, KVH, D, dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    V = 4
+    bufs = []
+    for v in range(V):
+        ctx, pos, slots = synth.ctxkv_inputs(w, v)
+        bufs.append((torch.from_numpy(ctx.view(np.int16)).view(torch.bfloat16).to(device),
+                     torch.from_numpy(pos).to(device), torch.from_numpy(slots).to(device)))
+    cs = torch.cuda.current_stream(device)
+    for c, p, s_ in bufs:
+        op.project(n, c, p, s_, kc, vc)
+    torch.cuda.synchronize(device)
+    op.check()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(cs)
+    graphs = []
+    for c, p, s_ in bufs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            op.project(n, c, p, s_, kc, vc, stream=side)
+        graphs.append(g)
+    cs.wait_stream(side)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)     # twice the L2
+    for i in range(args.warmup):
+        flush.zero_()
+        graphs[i % V].replay()
+    torch.cuda.synchronize(device)
+    _barrier(ws)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(cs)
+            graphs[i % V].replay()
+            evs[i][1].record(cs)
+        torch.cuda.synchronize(device)
+        _barrier(ws)
+    op.check()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    ms = _max_over_ranks(ms, ws, device)
+    clocks = clk.summary()
+
+    prof = []
+    for i in range(max(4, min(args.steps, 20))):
+        c, p, s_ = bufs[i % V]
+        flush.zero_()
+        prof.append(op.profile(n, c, p, s_, kc, vc))
+    k_ms = np.array(prof).mean(0)
+    byt = _ctxkv_bytes(w, n)
+    peak, peak_kind = _peaks()
+    gemm_gbs = byt["gemm"] / (k_ms[1] * 1e-3) / 1e9
+    step_gbs = byt["total"] / (ms * 1e-3) / 1e9 * ws
+
+    # end to end: pinned context, positions and slots in; the keys and values out
+    ctx_h, pos_h, slots_h = synth.ctxkv_inputs(w)
+    ch = torch.from_numpy(ctx_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ph, sh = torch.from_numpy(pos_h).pin_memory(), torch.from_numpy(slots_h).pin_memory()
+    kh = torch.empty(L, n, KVH, D, dtype=torch.bfloat16).pin_memory()
+    vh = torch.empty_like(kh).pin_memory()
+    cd, pd, sd = (torch.empty_like(t, device=device) for t in (ch, ph, sh))
+    kd, vd = torch.empty_like(kh, device=device), torch.empty_like(vh, device=device)
+
+    def host_step():
+        cd.copy_(ch, non_blocking=True)
+        pd.copy_(ph, non_blocking=True)
+        sd.copy_(sh, non_blocking=True)
+        op.project(n, cd, pd, sd, kc, vc, k_out=kd, v_out=vd)
+        kh.copy_(kd, non_blocking=True)
+        vh.copy_(vd, non_blocking=True)
+        torch.cuda.synchronize(device)
+
+    for _ in range(3):
+        host_step()
+    _barrier(ws)
+    t0 = time.perf_counter()
+    n_e2e = max(args.steps, 5)
+    for _ in range(n_e2e):
+        host_step()
+    e2e_ms = (time.perf_counter() - t0) * 1000.0 / n_e2e
+    e2e_ms = _max_over_ranks(e2e_ms, ws, device)
+    op.check()
+    if rank != 0:
+        op.close()
+        return
+    line = {
+        "metric": CTXKV_METRIC, "value": round(ms * 1000.0, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox / Irwin-Hall normals generated on device)",
+        "config": {"workload": w.name, "n_ctx": n, "hidden": H, "n_layers": L, "n_kv_heads": KVH,
+                   "head_dim": D, "rope_theta": w.rope_theta,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "graph": "one CUDA graph per input draw",
+                   "l2": "flushed before every timed step (a 256 MB write outside the events); "
+                         "%.1f MB of K/V weights per step" % (L * 2 * KVH * D * H * 2 / 1e6)},
+        "weight_stream_gbs": round(step_gbs, 1),
+        "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
+        "bytes_per_step": int(byt["total"]),
+        "roofline": {"kernel": "K/V projection (cuBLAS strided-batched bf16 GEMM)", "bound": "hbm",
+                     "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gemm_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gemm"])},
+        "kernels_us": {"norms": round(k_ms[0] * 1000, 2), "projection": round(k_ms[1] * 1000, 2),
+                       "key_norm_rope_cache": round(k_ms[2] * 1000, 2)},
+        "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT,
+                "h2d_bytes_per_step": n * H * 2 + n * 8 * 2,
+                "d2h_bytes_per_step": 2 * L * n * KVH * D * 2},
+        "gpu_launches": 2 * args.steps,
+        "library_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        us, info = ctxkv_cpu_baseline(w)
+        line["cpu_baseline"] = dict(info, value=round(us, 1), unit=UNIT)
+    print(json.dumps(line), flush=True)
+    op.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 class _Cai:
     def __init__(self, ptr, shape, typestr):
         self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr,
@@ -563,17 +757,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="serving",
-                    choices=sorted(synth.WORKLOADS) + sorted(synth.DENSE_WORKLOADS))
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.DENSE_WORKLOADS)
+                    + sorted(synth.CTXKV_WORKLOADS))
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    w = synth.WORKLOADS.get(args.workload) or synth.DENSE_WORKLOADS[args.workload]
+    w = (synth.WORKLOADS.get(args.workload) or synth.DENSE_WORKLOADS.get(args.workload)
+         or synth.CTXKV_WORKLOADS[args.workload])
     if args.rows:
-        w = w.with_rows(args.rows)
+        w = w.with_ctx(args.rows) if isinstance(w, synth.CtxKvWorkload) else w.with_rows(args.rows)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args, w)
+    elif isinstance(w, synth.CtxKvWorkload):
+        run_ctxkv(args, w)
     elif w.n_experts == 0:
         run_dense(args, w)
     else:

@@ -301,6 +301,87 @@ int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
 
 void moe_dense_destroy(moe_dense_t* h);
 
+/* ------------------------------------------------------------------------
+ * Draft context-KV projection (the DSpark page,
+ * vllm.models.muse_spark.common.dspark, _project_muse_context_kv and
+ * precompute_and_store_context_kv): context rows into every draft layer's
+ * keys and values, and into the KV cache.
+ *   fc   = bf16(rmsnorm(ctx) * w_hidden)                  hidden_norm
+ *   u[l] = bf16(rmsnorm(fc) * w_pre[l])                   pre_qkv_proj_norm
+ *   kv[l] = bf16(u[l] . W_kv[l]^T)      W_kv[l]: qkv_proj's K rows, then V rows
+ *   k = bf16(k / sqrt(mean(k^2) + qk_eps)) per head (fp32, no weight)
+ *   k = bf16(rotate(k, pos)): dimensions paired (j, j + D/2), angle
+ *       pos * theta^(-2j/D) (RoFormer's rotary embedding); theta 0: none
+ *   cache[l][slot] = k, v for every row with slot >= 0
+ * Norm weights are the effective ones: a zero-centred gamma is passed as
+ * 1 + gamma, a norm without a weight as ones.
+ * ---------------------------------------------------------------------- */
+typedef struct moe_ctxkv_s moe_ctxkv_t;
+
+typedef struct {
+  int hidden;        /* H: a multiple of 8, at most 8192 */
+  int n_layers;      /* L: draft layers, 1..256 */
+  int n_kv_heads;    /* KVH >= 1, KVH * D <= 32768 */
+  int head_dim;      /* D: 64, 128 or 256 */
+  int max_ctx;       /* most context rows per call, 1..65536 */
+  int max_position;  /* rotary table rows: positions must lie in [0, max_position) */
+  float eps;         /* hidden_norm and pre_qkv_proj_norm eps, > 0 */
+  float qk_eps;      /* the key norm's eps, > 0 */
+  double rope_theta; /* rotary base; 0 = no rotary embedding */
+} moe_ctxkv_dims;
+
+typedef struct {
+  const float* w_hidden; /* fp32 [H] */
+  const float* w_pre;    /* fp32 [L][H] */
+  const uint16_t* w_kv;  /* bf16 [L][2 * KVH * D][H], K-major */
+} moe_ctxkv_weights;
+
+typedef struct {
+  void* fc; /* bf16 [n][H] */
+  void* u;  /* bf16 [L][n][H] */
+  void* kv; /* bf16 [L][n][2 * KVH * D] */
+  void* k;  /* bf16 [L][n][KVH][D] (when no k_out was given) */
+  void* v;  /* bf16 [L][n][KVH][D] (when no v_out was given) */
+} moe_ctxkv_debug_view;
+
+/* Validates, allocates the workspace (about 2 * (1 + 2L) * max_ctx * H bytes
+ * plus the projections) and builds the rotary table (max_position * D/2
+ * cos/sin pairs, computed in fp64, stored fp32).  The caller keeps the
+ * weights alive until destroy.  16-byte aligned weight pointers. */
+int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe_ctxkv_t** out);
+
+/* One projection of n_ctx rows, asynchronous on cuda_stream, capturable.
+ *   context    bf16 [n_ctx][H], 16-byte aligned
+ *   positions  int64 [n_ctx] (required with a rotary embedding)
+ *   slots      int64 [L][slot_stride] (slot_stride 0: one map [n_ctx] for
+ *              every layer), or NULL: no cache write.  A negative slot
+ *              writes nothing; a slot >= n_slots writes nothing and latches
+ *              error 4 (moe_ctxkv_last_error).
+ *   k_cache, v_cache  bf16 [L][n_slots][KVH][D] (the paged cache with its
+ *              blocks of 16 slots flattened), 16-byte aligned
+ *   k_out, v_out  bf16 [L][n_ctx][KVH][D] or NULL (then the workspace)
+ * A position outside [0, max_position) latches error 3 and leaves that row's
+ * outputs unwritten.  Errors: MOE_EINVAL before any launch. */
+int moe_ctxkv_project(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
+                      const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
+                      int64_t n_slots, uint16_t* k_out, uint16_t* v_out, void* cuda_stream);
+
+/* The same projection with CUDA events around its three launches (norms,
+ * projection GEMM, key norm + rotation + cache write); synchronizes and
+ * writes their durations (ms) to ms_host[0..2].  For measurement. */
+int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
+                      const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
+                      int64_t n_slots, void* cuda_stream, float* ms_host);
+
+/* Workspace views of the last projection (device pointers). */
+int moe_ctxkv_debug(moe_ctxkv_t* h, moe_ctxkv_debug_view* view);
+
+/* Synchronizes the device and returns MOE_EDEVICE if a projection latched a
+ * device-side error since the last call (and clears it), else MOE_OK. */
+int moe_ctxkv_last_error(moe_ctxkv_t* h);
+
+void moe_ctxkv_destroy(moe_ctxkv_t* h);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,8 +57,9 @@ def lib():
             "oracle_dense_layer": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64] + [_vp] * 12),
             "oracle_bf16_linear": (None, [ctypes.c_int] * 3 + [_vp] * 4),
             "oracle_silu_mul": (None, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
-            "oracle_ctx_norms": (None, [ctypes.c_int] * 3 + [_f64] + [_vp] * 6),
-            "oracle_k_norm_rope": (None, [ctypes.c_int] * 4 + [_f64, _f64] + [_vp] * 5),
+            "oracle_ctx_norms": (None, [ctypes.c_int] * 3 + [_f64] + [_vp] * 7),
+            "oracle_layer_norms": (None, [ctypes.c_int] * 3 + [_f64] + [_vp] * 4),
+            "oracle_k_norm_rope": (None, [ctypes.c_int] * 4 + [_f64, _f64] + [_vp] * 6),
             "oracle_kv_cache_write": (None, [ctypes.c_int] * 4 + [_vp, ctypes.c_int, _i64] + [_vp] * 4),
             "oracle_route": (None, [ctypes.c_int] * 4 + [_vp] * 9),
             "oracle_pool": (None, [ctypes.c_int] * 3 + [_vp] * 6),
@@ -204,7 +205,7 @@ def silu_mul(gu):
 
 
 def context_kv(ctx, positions, w_hidden, w_pre, w_kv, n_kv_heads, head_dim, eps, qk_eps, theta):
-    """The draft's context-KV projection -> dict(fc, u, u_exact, kv, k, v, k_exact).
+    """The draft's context-KV projection -> dict(fc, u, fc_exact, u_exact, kv, k, v, k_exact).
     ctx bf16 bits [n, H]; w_pre fp32 [L, H]; w_kv bf16 bits [L, 2*KVH*D, H]
     (K rows, then V rows); k and v bf16 bits [L, n, KVH, D]."""
     ctx = _c(ctx, np.uint16)
@@ -215,28 +216,42 @@ def context_kv(ctx, positions, w_hidden, w_pre, w_kv, n_kv_heads, head_dim, eps,
     w_kv = _c(w_kv, np.uint16).reshape(L, 2 * KD, H)
     pos = _c(positions, np.int64)
     out = dict(fc=np.zeros((n, H), np.uint16), u=np.zeros((L, n, H), np.uint16),
-               u_exact=np.zeros((L, n, H), np.float64), kv=np.zeros((L, n, 2 * KD), np.uint16),
+               fc_exact=np.zeros((n, H), np.float64), u_exact=np.zeros((L, n, H), np.float64),
+               kv=np.zeros((L, n, 2 * KD), np.uint16),
                k=np.zeros((L, n, n_kv_heads, head_dim), np.uint16),
                v=np.zeros((L, n, n_kv_heads, head_dim), np.uint16),
                k_exact=np.zeros((L, n, n_kv_heads, head_dim), np.float64))
     lib().oracle_ctx_norms(n, H, L, eps, _p(ctx), _p(_c(w_hidden, np.float32)), _p(w_pre),
-                           _p(out["fc"]), _p(out["u"]), _p(out["u_exact"]))
+                           _p(out["fc"]), _p(out["u"]), _p(out["fc_exact"]), _p(out["u_exact"]))
     for l in range(L):
         out["kv"][l] = bf16_linear(out["u"][l], w_kv[l])[0]
     lib().oracle_k_norm_rope(L, n, n_kv_heads, head_dim, qk_eps, theta, _p(pos), _p(out["kv"]),
-                             _p(out["k"]), _p(out["v"]), _p(out["k_exact"]))
+                             _p(out["k"]), _p(out["v"]), _p(out["k_exact"]), None)
     return out
 
 
-def k_norm_rope(kv, positions, n_kv_heads, head_dim, qk_eps, theta):
-    """(k, v, k_exact) from bf16 bits kv [L, n, 2*KVH*D] (the GPU's own, staged)."""
+def layer_norms(fc, w_pre, eps):
+    """(u bf16 bits [L, n, H], u before rounding) from bf16 bits fc [n, H] (the
+    GPU's own, staged): each layer's pre_qkv_proj_norm."""
+    fc, w_pre = _c(fc, np.uint16), _c(w_pre, np.float32)
+    n, H = fc.shape
+    L = w_pre.shape[0]
+    u, ue = np.zeros((L, n, H), np.uint16), np.zeros((L, n, H), np.float64)
+    lib().oracle_layer_norms(n, H, L, eps, _p(fc), _p(w_pre), _p(u), _p(ue))
+    return u, ue
+
+
+def k_norm_rope(kv, positions, n_kv_heads, head_dim, qk_eps, theta, with_norm=False):
+    """(k, v, k_exact[, kn_exact]) from bf16 bits kv [L, n, 2*KVH*D] (the GPU's
+    own, staged); kn_exact: the normalised keys before their bf16 cast."""
     kv = _c(kv, np.uint16)
     L, n = kv.shape[:2]
     shape = (L, n, n_kv_heads, head_dim)
     k, v, ke = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16), np.zeros(shape, np.float64)
+    kne = np.zeros(shape, np.float64)
     lib().oracle_k_norm_rope(L, n, n_kv_heads, head_dim, qk_eps, theta, _p(_c(positions, np.int64)),
-                             _p(kv), _p(k), _p(v), _p(ke))
-    return k, v, ke
+                             _p(kv), _p(k), _p(v), _p(ke), _p(kne))
+    return (k, v, ke, kne) if with_norm else (k, v, ke)
 
 
 def kv_cache_write(k, v, slots, n_slots, k_cache, v_cache):

@@ -320,16 +320,10 @@ void oracle_dense_layer(int rows, int H, int I, double eps, const uint16_t* attn
  * Norms: fc = bf16(rmsnorm(ctx) * w_hidden) (hidden_norm), then each layer's
  * pre_qkv_proj_norm of fc: u[l] = bf16(rmsnorm(fc) * w_pre[l]).  The weights
  * are the effective ones (a zero-centred gamma is passed as 1 + gamma). */
-void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, const float* w_hidden,
-                      const float* w_pre, uint16_t* fc, uint16_t* u, double* u_exact) {
+void oracle_layer_norms(int n, int H, int L, double eps, const uint16_t* fc, const float* w_pre,
+                        uint16_t* u, double* u_exact) {
   for (int r = 0; r < n; ++r) {
-    const uint16_t* c = ctx + (int64_t)r * H;
-    uint16_t* f = fc + (int64_t)r * H;
-    double ms = 0.0;
-    for (int h = 0; h < H; ++h) ms += oracle_bf16_decode(c[h]) * oracle_bf16_decode(c[h]);
-    double inv_hidden = 1.0 / sqrt(ms / H + eps);
-    for (int h = 0; h < H; ++h)
-      f[h] = oracle_bf16_from_double(oracle_bf16_decode(c[h]) * inv_hidden * (double)w_hidden[h]);
+    const uint16_t* f = fc + (int64_t)r * H;
     double ms_fc = 0.0;
     for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(f[h]) * oracle_bf16_decode(f[h]);
     double inv_pre = 1.0 / sqrt(ms_fc / H + eps);
@@ -343,6 +337,22 @@ void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, cons
   }
 }
 
+void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, const float* w_hidden,
+                      const float* w_pre, uint16_t* fc, uint16_t* u, double* fc_exact, double* u_exact) {
+  for (int r = 0; r < n; ++r) {
+    const uint16_t* c = ctx + (int64_t)r * H;
+    double ms = 0.0;
+    for (int h = 0; h < H; ++h) ms += oracle_bf16_decode(c[h]) * oracle_bf16_decode(c[h]);
+    double inv_hidden = 1.0 / sqrt(ms / H + eps);
+    for (int h = 0; h < H; ++h) {
+      double v = oracle_bf16_decode(c[h]) * inv_hidden * (double)w_hidden[h];
+      fc[(int64_t)r * H + h] = oracle_bf16_from_double(v);
+      if (fc_exact) fc_exact[(int64_t)r * H + h] = v;
+    }
+  }
+  oracle_layer_norms(n, H, L, eps, fc, w_pre, u, u_exact);
+}
+
 /* The keys' RMSNorm and rotary embedding.  kv [L][n][2*KVH*D] holds each
  * layer's projection (the K heads, then the V heads).  Each K head of D
  * values is normalised in fp32 without a weight, k = bf16(k / sqrt(mean(k^2)
@@ -350,10 +360,11 @@ void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, cons
  * RoFormer (Su et al., 2021) with the dimensions paired as (j, j + D/2) and
  * angle pos * theta^(-2j/D), each output rounded to bf16 once.  theta = 0
  * leaves the keys unrotated.  V passes through.  k_exact (nullable) gets the
- * rotated keys before their rounding. */
+ * rotated keys before their rounding, kn_exact (nullable) the normalised keys
+ * before theirs. */
 void oracle_k_norm_rope(int L, int n, int KVH, int D, double qk_eps, double theta,
                         const int64_t* positions, const uint16_t* kv, uint16_t* k_out,
-                        uint16_t* v_out, double* k_exact) {
+                        uint16_t* v_out, double* k_exact, double* kn_exact) {
   const int KD = KVH * D, half = D / 2;
   double* kn = (double*)malloc(sizeof(double) * D);
   for (int l = 0; l < L; ++l)
@@ -366,6 +377,8 @@ void oracle_k_norm_rope(int L, int n, int KVH, int D, double qk_eps, double thet
         for (int i = 0; i < D; ++i) ms += oracle_bf16_decode(k[i]) * oracle_bf16_decode(k[i]);
         double inv = 1.0 / sqrt(ms / D + qk_eps);
         for (int i = 0; i < D; ++i) kn[i] = oracle_bf16_decode(oracle_bf16_from_double(oracle_bf16_decode(k[i]) * inv));
+        if (kn_exact)
+          for (int i = 0; i < D; ++i) kn_exact[o + i] = oracle_bf16_decode(k[i]) * inv;
         for (int j = 0; j < half; ++j) {
           double x1 = kn[j], x2 = kn[j + half], y1 = x1, y2 = x2;
           if (theta > 0.0) {

@@ -87,16 +87,20 @@ void oracle_dense_layer(int rows, int H, int I, double eps, const uint16_t* attn
                         const uint16_t* w13, const uint16_t* w2, const float* w_post_ffn,
                         uint16_t* x, uint16_t* gu, uint16_t* a, uint16_t* f, double* x_exact);
 /* Draft context-KV projection pieces.  ctx bf16 bits [n][H]; w_pre fp32
- * [L][H]; fc bf16 bits [n][H]; u bf16 bits [L][n][H] (u_exact nullable).
+ * [L][H]; fc bf16 bits [n][H]; u bf16 bits [L][n][H] (fc_exact, u_exact
+ * nullable: the values before their rounding).
  * kv bf16 bits [L][n][2*KVH*D] (K heads, then V heads); k_out, v_out bf16
- * bits [L][n][KVH][D] (k_exact nullable); positions [n]; theta 0 = no rotary
+ * bits [L][n][KVH][D] (k_exact, kn_exact nullable: the rotated and the
+ * normalised keys before their rounding); positions [n]; theta 0 = no rotary
  * embedding.  Caches [L][n_slots][KVH][D]; slots [L][layer_stride] (stride 0:
  * one mapping for every layer). */
+void oracle_layer_norms(int n, int H, int L, double eps, const uint16_t* fc, const float* w_pre,
+                        uint16_t* u, double* u_exact);
 void oracle_ctx_norms(int n, int H, int L, double eps, const uint16_t* ctx, const float* w_hidden,
-                      const float* w_pre, uint16_t* fc, uint16_t* u, double* u_exact);
+                      const float* w_pre, uint16_t* fc, uint16_t* u, double* fc_exact, double* u_exact);
 void oracle_k_norm_rope(int L, int n, int KVH, int D, double qk_eps, double theta,
                         const int64_t* positions, const uint16_t* kv, uint16_t* k_out,
-                        uint16_t* v_out, double* k_exact);
+                        uint16_t* v_out, double* k_exact, double* kn_exact);
 void oracle_kv_cache_write(int L, int n, int KVH, int D, const int64_t* slots, int layer_stride,
                            int64_t n_slots, const uint16_t* k, const uint16_t* v, uint16_t* k_cache,
                            uint16_t* v_cache);

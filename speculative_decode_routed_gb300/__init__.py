@@ -27,6 +27,8 @@ EXPORTS = (
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
     "moe_dense_destroy",
+    "moe_ctxkv_create", "moe_ctxkv_project", "moe_ctxkv_profile", "moe_ctxkv_debug",
+    "moe_ctxkv_last_error", "moe_ctxkv_destroy",
 )
 
 
@@ -59,6 +61,20 @@ class DenseWeights(ctypes.Structure):
 
 class DenseDebugView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("x", "gu", "a", "f")]
+
+
+class CtxKvDims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_layers", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_ctx", ctypes.c_int), ("max_position", ctypes.c_int),
+                ("eps", ctypes.c_float), ("qk_eps", ctypes.c_float), ("rope_theta", ctypes.c_double)]
+
+
+class CtxKvWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_hidden", "w_pre", "w_kv")]
+
+
+class CtxKvDebugView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("fc", "u", "kv", "k", "v")]
 
 
 class DebugView(ctypes.Structure):
@@ -104,6 +120,13 @@ def _lib():
             "moe_dense_layer_profile": (i32, [vp, i32, vp, vp, vp, vp]),
             "moe_dense_debug": (i32, [vp, ctypes.POINTER(DenseDebugView)]),
             "moe_dense_destroy": (None, [vp]),
+            "moe_ctxkv_create": (i32, [ctypes.POINTER(CtxKvDims), ctypes.POINTER(CtxKvWeights),
+                                       ctypes.POINTER(vp)]),
+            "moe_ctxkv_project": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp, vp]),
+            "moe_ctxkv_profile": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp]),
+            "moe_ctxkv_debug": (i32, [vp, ctypes.POINTER(CtxKvDebugView)]),
+            "moe_ctxkv_last_error": (i32, [vp]),
+            "moe_ctxkv_destroy": (None, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -335,6 +358,64 @@ class DenseLayer:
     def close(self):
         if self.handle:
             _lib().moe_dense_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class ContextKV:
+    """The draft's context-KV projection (moe_ctxkv_*) over caller-owned device
+    tensors: w_hidden fp32 [H]; w_pre fp32 [L, H]; w_kv bf16 [L, 2*KVH*D, H]
+    (each layer's K rows, then V rows)."""
+
+    def __init__(self, hidden, n_layers, n_kv_heads, head_dim, max_ctx, w_hidden, w_pre, w_kv,
+                 eps=1e-6, qk_eps=1e-6, rope_theta=10000.0, max_position=0):
+        dims = CtxKvDims(hidden, n_layers, n_kv_heads, head_dim, max_ctx, max_position, eps, qk_eps,
+                         rope_theta)
+        self.dims = dims
+        self._keep = (w_hidden, w_pre, w_kv)
+        wts = CtxKvWeights(*[t.data_ptr() for t in self._keep])
+        out = ctypes.c_void_p()
+        _check(_lib().moe_ctxkv_create(ctypes.byref(dims), ctypes.byref(wts), ctypes.byref(out)),
+               "moe_ctxkv_create")
+        self.handle = out
+
+    @staticmethod
+    def _slot_args(slots, k_cache, v_cache):
+        if slots is None:
+            return None, 0, None, None, 0
+        stride = 0 if slots.dim() == 1 else slots.shape[1]
+        return _ptr(slots), stride, _ptr(k_cache), _ptr(v_cache), k_cache.shape[1]
+
+    def project(self, n_ctx, context, positions, slots=None, k_cache=None, v_cache=None,
+                k_out=None, v_out=None, stream=None):
+        sp, stride, kc, vc, n_slots = self._slot_args(slots, k_cache, v_cache)
+        _check(_lib().moe_ctxkv_project(self.handle, n_ctx, _ptr(context), _ptr(positions), sp, stride,
+                                        kc, vc, n_slots, _ptr(k_out), _ptr(v_out), _stream(stream)),
+               "moe_ctxkv_project")
+
+    def profile(self, n_ctx, context, positions, slots=None, k_cache=None, v_cache=None, stream=None):
+        sp, stride, kc, vc, n_slots = self._slot_args(slots, k_cache, v_cache)
+        ms = (ctypes.c_float * 3)()
+        _check(_lib().moe_ctxkv_profile(self.handle, n_ctx, _ptr(context), _ptr(positions), sp, stride,
+                                        kc, vc, n_slots, _stream(stream), ms), "moe_ctxkv_profile")
+        return list(ms)
+
+    def debug(self) -> CtxKvDebugView:
+        v = CtxKvDebugView()
+        _check(_lib().moe_ctxkv_debug(self.handle, ctypes.byref(v)), "moe_ctxkv_debug")
+        return v
+
+    def check(self):
+        _check(_lib().moe_ctxkv_last_error(self.handle), "moe_ctxkv_last_error")
+
+    def close(self):
+        if self.handle:
+            _lib().moe_ctxkv_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -6,7 +6,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_decode.so")
-SOURCES = ["boundary.cu", "router.cu", "experts.cu", "experts_tc.cu", "quant.cu", "quant_noalloc.cu", "dense.cu", "capi.cu"]
+SOURCES = ["boundary.cu", "router.cu", "experts.cu", "experts_tc.cu", "quant.cu", "quant_noalloc.cu", "dense.cu", "ctxkv.cu", "capi.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -1,0 +1,494 @@
+// The draft's context-KV projection: context rows -> every draft layer's keys
+// and values, written into the KV cache.
+//
+// Page: vllm.models.muse_spark.common.dspark, _project_muse_context_kv and
+// precompute_and_store_context_kv.  hidden_norm, then each layer's
+// pre_qkv_proj_norm (bf16 outputs); each layer's stacked K/V rows of
+// qkv_proj applied to its normalised rows (one batched bf16 GEMM, fp32
+// accumulation, bf16 out); every key head normalised in fp32 without a weight
+// and cast to bf16; the keys rotated by their positions (dimensions paired
+// (j, j + D/2), angle pos * theta^(-2j/D), bf16 out); values passed through;
+// keys and values scattered into the cache at their slots (negative = none).
+//
+// GB300 layout: three launches.  ctx_norm_kernel, one CTA per row, computes
+// both norms and writes the L layer inputs; the projection is a plain batched
+// GEMM over the stacked weights (cuBLAS, the weights streamed once);
+// kv_rope_kernel gives each (layer, row, head) one warp: the head's D values
+// sit D/32 to a lane, so the key norm is a warp sum and the rotation's
+// partner dimension (j + D/2) is 16 lanes away (one shuffle).  The rotation's
+// cosines and sines come from a table built once at create in fp64.
+#include <cublas_v2.h>
+
+#include <cmath>
+#include <cstdio>
+#include <vector>
+
+#include "../../include/moe_decode.h"
+#include "common.cuh"
+#include "moe_decode_internal.h"
+
+namespace moe {
+namespace {
+
+struct CtxNormParams {
+  int n, H, L;
+  float eps;
+  const __nv_bfloat16* ctx;  // [n][H]
+  const float* w_hidden;     // [H]
+  const float* w_pre;        // [L][H]
+  __nv_bfloat16* fc;         // [n][H]
+  __nv_bfloat16* u;          // [L][n][H]
+};
+
+// Sum over the block, the result in every thread; red holds 32 floats.
+__device__ float block_sum_all(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.0f;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  __syncthreads();  // red is reused by the next sum
+  return t;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 raw, float (&v)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA per context row; 8 columns per thread.
+__global__ void ctx_norm_kernel(CtxNormParams p) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int col = threadIdx.x * 8;
+  const bool live = col < p.H;
+  float c[8] = {};
+  if (live) unpack8(__ldg(reinterpret_cast<const uint4*>(p.ctx + (size_t)r * p.H + col)), c);
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss += c[i] * c[i];
+  const float inv_hidden = rsqrtf(block_sum_all(ss, red) / (float)p.H + p.eps);
+  float f[8] = {};
+  if (live) {
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.w_hidden + col));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.w_hidden + col + 4));
+    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __bfloat162float(__float2bfloat16_rn(c[i] * inv_hidden * w[i]));
+    *reinterpret_cast<uint4*>(p.fc + (size_t)r * p.H + col) = pack8(f);
+  }
+  float ss2 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss2 += f[i] * f[i];
+  const float inv_pre = rsqrtf(block_sum_all(ss2, red) / (float)p.H + p.eps);
+  if (!live) return;
+  for (int l = 0; l < p.L; ++l) {
+    const float* wl = p.w_pre + (size_t)l * p.H + col;
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(wl));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(wl + 4));
+    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = f[i] * inv_pre * w[i];
+    *reinterpret_cast<uint4*>(p.u + ((size_t)l * p.n + r) * p.H + col) = pack8(o);
+  }
+}
+
+struct KvRopeParams {
+  int n, L, KVH, D;
+  float qk_eps;
+  int max_pos;               // rows of the cos / sin table; 0 = no rotation
+  const float2* cs;          // [max_pos][D/2]: (cos, sin)
+  const int64_t* positions;  // [n]
+  const __nv_bfloat16* kv;   // [L][n][2 * KVH * D]: K heads, then V heads
+  __nv_bfloat16* k_out;      // [L][n][KVH][D]
+  __nv_bfloat16* v_out;
+  const int64_t* slots;      // [L][slot_stride] (stride 0: one map), or null
+  int slot_stride;
+  int64_t n_slots;
+  __nv_bfloat16* k_cache;  // [L][n_slots][KVH][D]
+  __nv_bfloat16* v_cache;
+  unsigned* err;
+};
+
+constexpr unsigned kErrPosition = 3;  // a position outside the rotary table
+constexpr unsigned kErrSlot = 4;      // a slot at or past n_slots
+
+template <int E>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&v)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + i));
+    v[i] = f.x;
+    v[i + 1] = f.y;
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float (&v)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; i += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
+}
+
+// One warp per (layer, row, head); E = D / 32 values per lane.
+template <int E>
+__global__ void kv_rope_kernel(KvRopeParams p) {
+  const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.L * p.n * p.KVH) return;
+  const int hd = warp % p.KVH;
+  const int r = (warp / p.KVH) % p.n;
+  const int l = warp / (p.KVH * p.n);
+  const int KD = p.KVH * p.D;
+  const __nv_bfloat16* row = p.kv + ((size_t)l * p.n + r) * 2 * KD;
+
+  float k[E], v[E];
+  load_bf16<E>(row + hd * p.D + lane * E, k);
+  load_bf16<E>(row + KD + hd * p.D + lane * E, v);
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) ss += k[i] * k[i];
+  const float inv = rsqrtf(warp_sum(ss) / (float)p.D + p.qk_eps);
+#pragma unroll
+  for (int i = 0; i < E; ++i) k[i] = __bfloat162float(__float2bfloat16_rn(k[i] * inv));
+
+  if (p.max_pos > 0) {
+    const int64_t pos = p.positions[r];
+    if (pos < 0 || pos >= p.max_pos) {
+      if (lane == 0) latch_error(p.err, kErrPosition);
+      return;
+    }
+    const float2* cs = p.cs + (size_t)pos * (p.D / 2) + (lane & 15) * E;
+    float y[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float partner = __shfl_xor_sync(0xffffffffu, k[i], 16);
+      const float2 t = __ldg(cs + i);
+      // first half: x1 cos - x2 sin; second half: x2 cos + x1 sin
+      y[i] = lane < 16 ? k[i] * t.x - partner * t.y : k[i] * t.x + partner * t.y;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) k[i] = y[i];
+  }
+
+  const size_t o = (((size_t)l * p.n + r) * p.KVH + hd) * p.D + lane * E;
+  store_bf16<E>(p.k_out + o, k);
+  store_bf16<E>(p.v_out + o, v);
+  if (p.slots) {
+    const int64_t slot = p.slots[(size_t)l * p.slot_stride + r];
+    if (slot >= p.n_slots) {
+      if (lane == 0) latch_error(p.err, kErrSlot);
+    } else if (slot >= 0) {
+      const size_t c = (((size_t)l * p.n_slots + slot) * p.KVH + hd) * p.D + lane * E;
+      store_bf16<E>(p.k_cache + c, k);
+      store_bf16<E>(p.v_cache + c, v);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+struct moe_ctxkv_s {
+  moe_ctxkv_dims d;
+  moe_ctxkv_weights w;
+  cublasHandle_t blas;
+  void* blas_ws;
+  void* base;                       // one allocation: the buffers below
+  __nv_bfloat16 *fc, *u, *kv, *k, *v;
+  float2* cs;                       // rotary table, or null
+  unsigned* err;
+};
+
+namespace {
+
+constexpr size_t kCtxBlasWorkspace = 8u << 20;
+
+bool ck_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int ck_cuda(cudaError_t e, const char* what) {
+  char buf[200];
+  snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
+  return moe::api_fail(MOE_ECUDA, buf);
+}
+
+int ck_blas(cublasStatus_t st, const char* what) {
+  char buf[160];
+  snprintf(buf, sizeof(buf), "%s: cuBLAS status %d", what, (int)st);
+  return moe::api_fail(MOE_ECUDA, buf);
+}
+
+struct ProjectArgs {
+  int n;
+  const uint16_t* context;
+  const int64_t* positions;
+  const int64_t* slots;
+  int slot_stride;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int64_t n_slots;
+  uint16_t* k_out;
+  uint16_t* v_out;
+};
+
+int check_project(const moe_ctxkv_t* h, const ProjectArgs& a) {
+  const moe_ctxkv_dims& d = h->d;
+  char buf[160];
+  if (a.n < 1 || a.n > d.max_ctx) {
+    snprintf(buf, sizeof(buf), "n_ctx %d outside [1, max_ctx=%d]", a.n, d.max_ctx);
+    return moe::api_fail(MOE_EINVAL, buf);
+  }
+  if (!a.context || !ck_aligned(a.context, 16))
+    return moe::api_fail(MOE_EINVAL, "context must be a 16-byte aligned device pointer");
+  if (d.rope_theta > 0.0 && (!a.positions || !ck_aligned(a.positions, 8)))
+    return moe::api_fail(MOE_EINVAL, "positions are required (8-byte aligned) with a rotary embedding");
+  if (a.slots) {
+    if (!ck_aligned(a.slots, 8)) return moe::api_fail(MOE_EINVAL, "slots must be 8-byte aligned");
+    if (a.slot_stride != 0 && a.slot_stride < a.n)
+      return moe::api_fail(MOE_EINVAL, "slot_stride must be 0 (one map) or at least n_ctx");
+    if (!a.k_cache || !a.v_cache || a.n_slots < 1 || !ck_aligned(a.k_cache, 16) || !ck_aligned(a.v_cache, 16))
+      return moe::api_fail(MOE_EINVAL, "slots need 16-byte aligned K and V caches and n_slots >= 1");
+  }
+  if ((a.k_out && !ck_aligned(a.k_out, 16)) || (a.v_out && !ck_aligned(a.v_out, 16)))
+    return moe::api_fail(MOE_EINVAL, "k_out and v_out must be 16-byte aligned");
+  return MOE_OK;
+}
+
+// The three launches on s; with ev, an event before each and after the last.
+int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEvent_t* ev) {
+  const moe_ctxkv_dims& d = h->d;
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  const int KD = d.n_kv_heads * d.head_dim;
+  mark(0);
+  moe::CtxNormParams np{};
+  np.n = a.n;
+  np.H = d.hidden;
+  np.L = d.n_layers;
+  np.eps = d.eps;
+  np.ctx = reinterpret_cast<const __nv_bfloat16*>(a.context);
+  np.w_hidden = h->w.w_hidden;
+  np.w_pre = h->w.w_pre;
+  np.fc = h->fc;
+  np.u = h->u;
+  const int threads = ((d.hidden / 8 + 31) / 32) * 32;
+  moe::ctx_norm_kernel<<<a.n, threads, 0, s>>>(np);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return ck_cuda(e, "context norm launch");
+  mark(1);
+  cublasStatus_t st = cublasSetStream(h->blas, s);
+  if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "cublasSetStream");
+  const float one = 1.0f, zero = 0.0f;
+  // kv[l] [n][2KD] = u[l] [n][H] . W_kv[l]^T  (column-major: W_kv[l] is H x 2KD)
+  st = cublasGemmStridedBatchedEx(
+      h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * KD, a.n, d.hidden, &one, h->w.w_kv, CUDA_R_16BF,
+      d.hidden, (long long)2 * KD * d.hidden, h->u, CUDA_R_16BF, d.hidden, (long long)a.n * d.hidden,
+      &zero, h->kv, CUDA_R_16BF, 2 * KD, (long long)a.n * 2 * KD, d.n_layers, CUBLAS_COMPUTE_32F,
+      CUBLAS_GEMM_DEFAULT);
+  if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "K/V projection GEMM");
+  mark(2);
+  moe::KvRopeParams kp{};
+  kp.n = a.n;
+  kp.L = d.n_layers;
+  kp.KVH = d.n_kv_heads;
+  kp.D = d.head_dim;
+  kp.qk_eps = d.qk_eps;
+  kp.max_pos = h->cs ? d.max_position : 0;
+  kp.cs = h->cs;
+  kp.positions = a.positions;
+  kp.kv = h->kv;
+  kp.k_out = a.k_out ? reinterpret_cast<__nv_bfloat16*>(a.k_out) : h->k;
+  kp.v_out = a.v_out ? reinterpret_cast<__nv_bfloat16*>(a.v_out) : h->v;
+  kp.slots = a.slots;
+  kp.slot_stride = a.slot_stride;
+  kp.n_slots = a.n_slots;
+  kp.k_cache = reinterpret_cast<__nv_bfloat16*>(a.k_cache);
+  kp.v_cache = reinterpret_cast<__nv_bfloat16*>(a.v_cache);
+  kp.err = h->err;
+  const long long warps = (long long)d.n_layers * a.n * d.n_kv_heads;
+  const int blocks = (int)((warps * 32 + 255) / 256);
+  switch (d.head_dim) {
+    case 64: moe::kv_rope_kernel<2><<<blocks, 256, 0, s>>>(kp); break;
+    case 128: moe::kv_rope_kernel<4><<<blocks, 256, 0, s>>>(kp); break;
+    default: moe::kv_rope_kernel<8><<<blocks, 256, 0, s>>>(kp); break;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return ck_cuda(e, "key norm / rotary launch");
+  mark(3);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe_ctxkv_t** out) {
+  if (!dims || !w || !out) return moe::api_fail(MOE_EINVAL, "dims, weights and out are required");
+  *out = nullptr;
+  const moe_ctxkv_dims d = *dims;
+  if (d.hidden < 8 || d.hidden % 8 || d.hidden > 8192)
+    return moe::api_fail(MOE_EUNSUPPORTED, "hidden must be a multiple of 8 in [8, 8192]");
+  if (d.n_layers < 1 || d.n_layers > 256) return moe::api_fail(MOE_EUNSUPPORTED, "n_layers must be in [1, 256]");
+  if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256)
+    return moe::api_fail(MOE_EUNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (d.n_kv_heads < 1 || d.n_kv_heads * d.head_dim > 32768)
+    return moe::api_fail(MOE_EUNSUPPORTED, "n_kv_heads * head_dim must be in [head_dim, 32768]");
+  if (d.max_ctx < 1 || d.max_ctx > 65536) return moe::api_fail(MOE_EUNSUPPORTED, "max_ctx must be in [1, 65536]");
+  if ((long long)d.n_layers * d.max_ctx * d.n_kv_heads * 32 >= (1ll << 31))
+    return moe::api_fail(MOE_EUNSUPPORTED, "n_layers * max_ctx * n_kv_heads must be below 2^26");
+  if (!(d.eps > 0.0f) || !(d.qk_eps > 0.0f)) return moe::api_fail(MOE_EINVAL, "eps and qk_eps must be positive");
+  if (!(d.rope_theta >= 0.0)) return moe::api_fail(MOE_EINVAL, "rope_theta must be >= 0 (0: no rotary embedding)");
+  if (d.rope_theta > 0.0 && (d.max_position < 1 || d.max_position > (1 << 20)))
+    return moe::api_fail(MOE_EUNSUPPORTED, "max_position must be in [1, 2^20] with a rotary embedding");
+  if (!w->w_hidden || !w->w_pre || !w->w_kv) return moe::api_fail(MOE_EINVAL, "a required weight pointer is NULL");
+  if (!ck_aligned(w->w_hidden, 16) || !ck_aligned(w->w_pre, 16) || !ck_aligned(w->w_kv, 16))
+    return moe::api_fail(MOE_EINVAL, "weight pointers must be 16-byte aligned");
+  int dev = 0, major = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e != cudaSuccess) return ck_cuda(e, "device query");
+  if (major != 10) return moe::api_fail(MOE_EUNSUPPORTED, "needs an SM 10.x GPU");
+
+  moe_ctxkv_t* h = new moe_ctxkv_t{};
+  h->d = d;
+  h->w = *w;
+  const size_t n = d.max_ctx, H = d.hidden, L = d.n_layers, KD = (size_t)d.n_kv_heads * d.head_dim;
+  const size_t table = d.rope_theta > 0.0 ? (size_t)d.max_position * (d.head_dim / 2) : 0;
+  auto up16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
+  const size_t b_fc = up16(2 * n * H), b_u = up16(2 * L * n * H), b_kv = up16(2 * L * n * 2 * KD),
+               b_k = up16(2 * L * n * KD), b_cs = table * sizeof(float2);
+  const size_t bytes = b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
+  uint8_t* base = nullptr;
+  e = cudaMalloc(&base, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kCtxBlasWorkspace);
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    moe_ctxkv_destroy(h);
+    return moe::api_fail(MOE_ENOMEM, "context-KV workspace");
+  }
+  h->base = base;
+  h->fc = reinterpret_cast<__nv_bfloat16*>(base);
+  h->u = reinterpret_cast<__nv_bfloat16*>(base + b_fc);
+  h->kv = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u);
+  h->k = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u + b_kv);
+  h->v = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u + b_kv + b_k);
+  h->cs = table ? reinterpret_cast<float2*>(base + b_fc + b_u + b_kv + 2 * b_k) : nullptr;
+  h->err = reinterpret_cast<unsigned*>(base + b_fc + b_u + b_kv + 2 * b_k + b_cs);
+  e = cudaMemset(h->err, 0, sizeof(unsigned));
+  if (e == cudaSuccess && table) {
+    // cos / sin of pos * theta^(-2j/D) in fp64, stored as fp32
+    const int half = d.head_dim / 2;
+    std::vector<double> freq(half);
+    for (int j = 0; j < half; ++j) freq[j] = std::pow(d.rope_theta, -2.0 * j / d.head_dim);
+    std::vector<float2> host(table);
+    for (size_t pos = 0; pos < (size_t)d.max_position; ++pos)
+      for (int j = 0; j < half; ++j) {
+        const double ang = (double)pos * freq[j];
+        host[pos * half + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    e = cudaMemcpy(h->cs, host.data(), b_cs, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    moe_ctxkv_destroy(h);
+    return ck_cuda(e, "context-KV set-up");
+  }
+  cublasStatus_t st = cublasCreate(&h->blas);
+  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, kCtxBlasWorkspace);
+  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);
+  if (st != CUBLAS_STATUS_SUCCESS) {
+    moe_ctxkv_destroy(h);
+    return ck_blas(st, "cuBLAS set-up");
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_ctxkv_project(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
+                      const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
+                      int64_t n_slots, uint16_t* k_out, uint16_t* v_out, void* cuda_stream) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  const ProjectArgs a{n_ctx, context, positions, slots, slot_stride, k_cache, v_cache, n_slots, k_out, v_out};
+  int rc = check_project(h, a);
+  if (rc) return rc;
+  return ctxkv_enqueue(h, a, static_cast<cudaStream_t>(cuda_stream), nullptr);
+}
+
+int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
+                      const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
+                      int64_t n_slots, void* cuda_stream, float* ms_host) {
+  if (!h || !ms_host) return moe::api_fail(MOE_EINVAL, "handle and ms_host are required");
+  const ProjectArgs a{n_ctx, context, positions, slots, slot_stride, k_cache, v_cache, n_slots, nullptr, nullptr};
+  int rc = check_project(h, a);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaEvent_t ev[4] = {};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  if (e == cudaSuccess) {
+    rc = ctxkv_enqueue(h, a, s, ev);
+    if (!rc) e = cudaEventSynchronize(ev[3]);
+    for (int i = 0; i < 3 && !rc && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms_host[i], ev[i], ev[i + 1]);
+  }
+  for (int i = 0; i < 4; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  if (rc) return rc;
+  if (e != cudaSuccess) return ck_cuda(e, "profile events");
+  return MOE_OK;
+}
+
+int moe_ctxkv_debug(moe_ctxkv_t* h, moe_ctxkv_debug_view* v) {
+  if (!h || !v) return moe::api_fail(MOE_EINVAL, "handle and view are required");
+  v->fc = h->fc;
+  v->u = h->u;
+  v->kv = h->kv;
+  v->k = h->k;
+  v->v = h->v;
+  return MOE_OK;
+}
+
+int moe_ctxkv_last_error(moe_ctxkv_t* h) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return ck_cuda(e, "device synchronize");
+  unsigned flag = 0;
+  e = cudaMemcpy(&flag, h->err, sizeof(flag), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return ck_cuda(e, "error flag read");
+  if (flag) {
+    cudaMemset(h->err, 0, sizeof(unsigned));
+    char buf[160];
+    snprintf(buf, sizeof(buf), "device-side error %u: %s", flag,
+             flag == moe::kErrPosition ? "a position outside [0, max_position)"
+             : flag == moe::kErrSlot   ? "a slot at or past n_slots"
+                                       : "unknown");
+    return moe::api_fail(MOE_EDEVICE, buf);
+  }
+  return MOE_OK;
+}
+
+void moe_ctxkv_destroy(moe_ctxkv_t* h) {
+  if (!h) return;
+  if (h->blas) cublasDestroy(h->blas);
+  cudaFree(h->blas_ws);
+  cudaFree(h->base);
+  delete h;
+}
+
+}  // extern "C"

@@ -42,6 +42,11 @@ KIND_W_FRONT = 13
 KIND_DENSE_W13 = 14
 KIND_DENSE_W2 = 15
 KIND_W_POST_FFN = 16
+KIND_CTX = 17
+KIND_W_HIDDEN = 18
+KIND_W_PRE_QKV = 19
+KIND_W_KV = 20
+KIND_CTX_PLACE = 21
 
 
 def tag(kind: int, layer: int = 0, index: int = 0) -> int:
@@ -295,3 +300,77 @@ def dev_dense_weights(w13, w2, w: Workload, layer: int, stream=None):
     dev_normal_bf16(w13, w.seed, tag(KIND_DENSE_W13, layer), *w.expert_dist, stream=stream)
     dev_normal_bf16(w2, w.seed, tag(KIND_DENSE_W2, layer), *w.expert_dist, stream=stream)
     return w13, w2
+
+
+# ----------------------------------------------------------------------------- draft context-KV
+
+
+@dataclass(frozen=True)
+class CtxKvWorkload:
+    """Shapes and value distributions of one context-KV projection."""
+
+    name: str
+    n_ctx: int           # context rows per call
+    hidden: int          # H
+    n_layers: int        # L: draft layers
+    n_kv_heads: int      # KVH
+    head_dim: int        # D
+    rope_theta: float = 10000.0
+    max_position: int = 32768
+    n_slots: int = 4096  # cache slots per layer (256 blocks of 16)
+    eps: float = 1e-6
+    qk_eps: float = 1e-6
+    seed: int = 0
+    ctx_dist: tuple = (0.0, 1.0)
+    norm_dist: tuple = (1.0, 0.1)
+    weight_dist: tuple = (0.0, 0.02)
+
+    def with_ctx(self, n_ctx: int) -> "CtxKvWorkload":
+        d = dict(self.__dict__)
+        d["n_ctx"] = n_ctx
+        return CtxKvWorkload(**d)
+
+
+# The pages give no draft geometry: hidden follows the target, eight KV heads
+# of 128, four draft layers (117 MB of K/V weights: under L2, so the bench
+# writes a buffer larger than L2 between timed steps).
+CTXKV_WORKLOADS = {
+    "draft_ctx_kv": CtxKvWorkload("draft_ctx_kv", n_ctx=8, hidden=7168, n_layers=4, n_kv_heads=8,
+                                  head_dim=128),
+    "draft_ctx_kv_small": CtxKvWorkload("draft_ctx_kv_small", n_ctx=8, hidden=256, n_layers=2,
+                                        n_kv_heads=2, head_dim=64, max_position=4096, n_slots=64),
+}
+
+
+def ctxkv_inputs(w: CtxKvWorkload, variant: int = 0):
+    """(context bf16 bits [n, H] ~ N(0, 1), positions int64 [n], slots int64 [n]).
+    The positions are consecutive from a seeded start; the slots are n distinct
+    seeded slots of the n_slots."""
+    ctx = normal_bf16((w.n_ctx, w.hidden), w.seed, tag(KIND_CTX, 0, variant), *w.ctx_dist)
+    words = philox_words(max(w.n_slots, 1), w.seed, tag(KIND_CTX_PLACE, 0, variant))
+    start = int(words[0, 1]) % max(w.max_position - w.n_ctx, 1)
+    positions = np.arange(start, start + w.n_ctx, dtype=np.int64)
+    slots = np.argsort(words[:, 0], kind="stable")[: w.n_ctx].astype(np.int64)
+    return ctx, positions, slots
+
+
+def ctxkv_norm_weights(w: CtxKvWorkload):
+    """(w_hidden fp32 [H], w_pre fp32 [L, H]), each 1 + 0.1 N(0, 1)."""
+    wh = normal_f32((w.hidden,), w.seed, tag(KIND_W_HIDDEN), *w.norm_dist)
+    wp = np.stack([normal_f32((w.hidden,), w.seed, tag(KIND_W_PRE_QKV, l), *w.norm_dist)
+                   for l in range(w.n_layers)])
+    return wh, wp
+
+
+def ctxkv_weights(w: CtxKvWorkload) -> np.ndarray:
+    """bf16 bits [L, 2*KVH*D, H]: each layer's K rows, then V rows, N(0, 0.02)."""
+    rows = 2 * w.n_kv_heads * w.head_dim
+    return np.stack([normal_bf16((rows, w.hidden), w.seed, tag(KIND_W_KV, l), *w.weight_dist)
+                     for l in range(w.n_layers)])
+
+
+def dev_ctxkv_weights(out, w: CtxKvWorkload, stream=None):
+    """Device twin of ctxkv_weights, into the bf16 CUDA tensor [L, 2*KVH*D, H]."""
+    for l in range(w.n_layers):
+        dev_normal_bf16(out[l], w.seed, tag(KIND_W_KV, l), *w.weight_dist, stream=stream)
+    return out

@@ -120,3 +120,50 @@ def test_dense_invalid_arguments():
     assert L.moe_dense_layer_profile(None, 1, None, None, None, ms) == moe.MOE_EINVAL
     assert L.moe_dense_debug(None, None) == moe.MOE_EINVAL
     L.moe_dense_destroy(None)
+
+
+def _ctxkv_create(null=None, shift=None, **kw):
+    d = dict(hidden=256, n_layers=2, n_kv_heads=2, head_dim=64, max_ctx=8, max_position=64,
+             eps=1e-6, qk_eps=1e-6, rope_theta=10000.0)
+    d.update(kw)
+    dims = moe.CtxKvDims(**d)
+    ptrs = [(1 << 20) + i * 256 for i in range(3)]
+    if null is not None:
+        ptrs[null] = None
+    if shift is not None:
+        ptrs[shift] += 8
+    h = ctypes.c_void_p()
+    rc = moe.lib().moe_ctxkv_create(ctypes.byref(dims), ctypes.byref(moe.CtxKvWeights(*ptrs)),
+                                    ctypes.byref(h))
+    return rc, moe.lib().moe_decode_error_message().decode()
+
+
+@pytest.mark.parametrize("kw", [dict(hidden=100), dict(hidden=8200), dict(n_layers=0),
+                                dict(n_layers=257), dict(head_dim=96), dict(n_kv_heads=0),
+                                dict(n_kv_heads=129, head_dim=256), dict(max_ctx=0),
+                                dict(max_ctx=65537), dict(max_position=0),
+                                dict(max_position=(1 << 20) + 1),
+                                dict(n_layers=256, max_ctx=65536, n_kv_heads=8)])
+def test_ctxkv_unsupported_shapes(kw):
+    rc, msg = _ctxkv_create(**kw)
+    assert rc == moe.MOE_EUNSUPPORTED, (kw, rc, msg)
+    assert msg
+
+
+def test_ctxkv_invalid_arguments():
+    for i in range(3):
+        rc, msg = _ctxkv_create(null=i)
+        assert rc == moe.MOE_EINVAL and "NULL" in msg
+        rc, msg = _ctxkv_create(shift=i)
+        assert rc == moe.MOE_EINVAL and "aligned" in msg
+    for kw in (dict(eps=0.0), dict(qk_eps=-1.0), dict(rope_theta=-1.0)):
+        rc, msg = _ctxkv_create(**kw)
+        assert rc == moe.MOE_EINVAL, kw
+    L = moe.lib()
+    assert L.moe_ctxkv_create(None, None, None) == moe.MOE_EINVAL
+    assert L.moe_ctxkv_project(None, 1, None, None, None, 0, None, None, 0, None, None, None) == moe.MOE_EINVAL
+    ms = (ctypes.c_float * 3)()
+    assert L.moe_ctxkv_profile(None, 1, None, None, None, 0, None, None, 0, None, ms) == moe.MOE_EINVAL
+    assert L.moe_ctxkv_debug(None, None) == moe.MOE_EINVAL
+    assert L.moe_ctxkv_last_error(None) == moe.MOE_EINVAL
+    L.moe_ctxkv_destroy(None)

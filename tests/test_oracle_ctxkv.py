@@ -49,7 +49,7 @@ def test_constant_rows_closed_form():
         cb = _f64(ctx[0, :1])[0]
         fc, u = np.zeros((1, H), np.uint16), np.zeros((L, 1, H), np.uint16)
         oracle.lib().oracle_ctx_norms(1, H, L, eps, oracle._p(ctx), oracle._p(np.ones(H, np.float32)),
-                                      oracle._p(w_pre), oracle._p(fc), oracle._p(u), None)
+                                      oracle._p(w_pre), oracle._p(fc), oracle._p(u), None, None)
         f_want = _bits_of(np.full(H, np.sign(cb) / math.sqrt(1.0 + eps / cb ** 2)))
         assert np.array_equal(fc[0], f_want)
         f = _f64(f_want[:1])[0]

@@ -118,13 +118,12 @@ MUTANTS = [
      "kn[i] = oracle_bf16_decode(oracle_bf16_from_double(oracle_bf16_decode(k[i]) * inv));",
      "kn[i] = oracle_bf16_decode(k[i]) * inv;",
      [("test_oracle_ctxkv", "test_one_hot_key_rotates_into_its_partner_dimension", {})]),
-    ("context KV: layer norms weighted by the hidden norm's weight",
+    ("context KV: every layer normalised with layer 0's weight",
      "double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_pre[(int64_t)l * H + h];",
-     "double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_hidden[h];",
+     "double v = oracle_bf16_decode(f[h]) * inv_pre * (double)w_pre[h];",
      [("test_oracle_ctxkv", "test_constant_rows_closed_form", {})]),
-    ("context KV: layer norms over the raw context",
-     "for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(f[h]) * oracle_bf16_decode(f[h]);",
-     "for (int h = 0; h < H; ++h) ms_fc += oracle_bf16_decode(c[h]) * oracle_bf16_decode(c[h]);",
+    ("context KV: layer norms' mean square not divided by H",
+     "double inv_pre = 1.0 / sqrt(ms_fc / H + eps);", "double inv_pre = 1.0 / sqrt(ms_fc + eps);",
      [("test_oracle_ctxkv", "test_constant_rows_closed_form", {})]),
     ("context KV: every layer's keys written to layer 0's cache",
      "memcpy(k_cache + ((int64_t)l * n_slots + slot) * KD,", "memcpy(k_cache + (slot) * KD,",
