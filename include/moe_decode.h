@@ -367,8 +367,10 @@ int moe_ctxkv_project(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const 
                       int64_t n_slots, uint16_t* k_out, uint16_t* v_out, void* cuda_stream);
 
 /* The same projection with CUDA events around its three launches (norms,
- * projection GEMM, key norm + rotation + cache write); synchronizes and
- * writes their durations (ms) to ms_host[0..2].  For measurement. */
+ * projection, key norm + rotation + cache write); synchronizes and writes
+ * their durations (ms) to ms_host[0..2].  For measurement.  Up to 8 rows
+ * (and H a multiple of 64) the projection is the library's split-K
+ * weight-streaming kernel, beyond that a batched cuBLAS GEMM. */
 int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
                       const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
                       int64_t n_slots, void* cuda_stream, float* ms_host);

@@ -11,9 +11,12 @@
 // keys and values scattered into the cache at their slots (negative = none).
 //
 // GB300 layout: three launches.  ctx_norm_kernel, one CTA per row, computes
-// both norms and writes the L layer inputs; the projection is a plain batched
-// GEMM over the stacked weights (cuBLAS, the weights streamed once);
-// kv_rope_kernel gives each (layer, row, head) one warp: the head's D values
+// both norms and writes the L layer inputs.  Up to 8 rows the projection is
+// the split-K weight-streaming kernel (gemv.cuh): fp32 partial sums per
+// K-split, launched with programmatic dependent launch so its first weight
+// loads overlap the norms; beyond 8 rows it is a batched bf16 GEMM (cuBLAS).
+// kv_rope_kernel gives each (layer, row, head) one warp: it sums the partials
+// in split order (or reads the GEMM's bf16 output), and the head's D values
 // sit D/32 to a lane, so the key norm is a warp sum and the rotation's
 // partner dimension (j + D/2) is 16 lanes away (one shuffle).  The rotation's
 // cosines and sines come from a table built once at create in fp64.
@@ -25,6 +28,7 @@
 
 #include "../../include/moe_decode.h"
 #include "common.cuh"
+#include "gemv.cuh"
 #include "moe_decode_internal.h"
 
 namespace moe {
@@ -74,6 +78,7 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 
 // One CTA per context row; 8 columns per thread.
 __global__ void ctx_norm_kernel(CtxNormParams p) {
+  grid_dep_launch();  // the projection may start streaming its weights
   __shared__ float red[32];
   const int r = blockIdx.x;
   const int col = threadIdx.x * 8;
@@ -116,7 +121,9 @@ struct KvRopeParams {
   int max_pos;               // rows of the cos / sin table; 0 = no rotation
   const float2* cs;          // [max_pos][D/2]: (cos, sin)
   const int64_t* positions;  // [n]
-  const __nv_bfloat16* kv;   // [L][n][2 * KVH * D]: K heads, then V heads
+  __nv_bfloat16* kv;         // [L][n][2 * KVH * D]: K heads, then V heads
+  const float* part;         // [S][L][n][2 * KVH * D] split-K partials, or null: read kv
+  int S;
   __nv_bfloat16* k_out;      // [L][n][KVH][D]
   __nv_bfloat16* v_out;
   const int64_t* slots;      // [L][slot_stride] (stride 0: one map), or null
@@ -147,7 +154,9 @@ __device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float (&v)[
     *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
 }
 
-// One warp per (layer, row, head); E = D / 32 values per lane.
+// One warp per (layer, row, head); E = D / 32 values per lane.  With
+// partials, the projection is their sum in split order, rounded to bf16 (and
+// kept in kv); otherwise kv holds it.
 template <int E>
 __global__ void kv_rope_kernel(KvRopeParams p) {
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -157,11 +166,45 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
   const int r = (warp / p.KVH) % p.n;
   const int l = warp / (p.KVH * p.n);
   const int KD = p.KVH * p.D;
-  const __nv_bfloat16* row = p.kv + ((size_t)l * p.n + r) * 2 * KD;
+  __nv_bfloat16* row = p.kv + ((size_t)l * p.n + r) * 2 * KD;
 
   float k[E], v[E];
-  load_bf16<E>(row + hd * p.D + lane * E, k);
-  load_bf16<E>(row + KD + hd * p.D + lane * E, v);
+  if (p.part) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) k[i] = v[i] = 0.0f;
+    grid_dep_wait();
+    const size_t split = (size_t)p.L * p.n * 2 * KD;
+    const float* src = p.part + ((size_t)l * p.n + r) * 2 * KD + hd * p.D + lane * E;
+    // eight splits' loads in flight at a time, summed in split order
+    for (int s0 = 0; s0 < p.S; s0 += 8) {
+      float pk[8][E], pv[8][E];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const bool in = s0 + j < p.S;
+          pk[j][i] = in ? __ldcg(src + (size_t)(s0 + j) * split + i) : 0.0f;
+          pv[j][i] = in ? __ldcg(src + (size_t)(s0 + j) * split + KD + i) : 0.0f;
+        }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          k[i] += pk[j][i];
+          v[i] += pv[j][i];
+        }
+    }
+    store_bf16<E>(row + hd * p.D + lane * E, k);
+    store_bf16<E>(row + KD + hd * p.D + lane * E, v);
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      k[i] = __bfloat162float(__float2bfloat16_rn(k[i]));
+      v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+    }
+  } else {
+    load_bf16<E>(row + hd * p.D + lane * E, k);
+    load_bf16<E>(row + KD + hd * p.D + lane * E, v);
+  }
   float ss = 0.0f;
 #pragma unroll
   for (int i = 0; i < E; ++i) ss += k[i] * k[i];
@@ -215,6 +258,9 @@ struct moe_ctxkv_s {
   __nv_bfloat16 *fc, *u, *kv, *k, *v;
   float2* cs;                       // rotary table, or null
   unsigned* err;
+  float* part;                      // split-K partials [S][L][8][2 * KVH * D], or null
+  int splits;                       // K-splits of the streaming projection; 0: none
+  int num_sms;
 };
 
 namespace {
@@ -289,21 +335,49 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   np.w_pre = h->w.w_pre;
   np.fc = h->fc;
   np.u = h->u;
-  const int threads = ((d.hidden / 8 + 31) / 32) * 32;
-  moe::ctx_norm_kernel<<<a.n, threads, 0, s>>>(np);
-  cudaError_t e = cudaGetLastError();
+  const bool stream_w = h->splits > 0 && a.n <= 8;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n, 1, 1);
+  cfg.blockDim = dim3(((d.hidden / 8 + 31) / 32) * 32, 1, 1);
+  cfg.stream = s;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe::ctx_norm_kernel, np);
   if (e != cudaSuccess) return ck_cuda(e, "context norm launch");
   mark(1);
-  cublasStatus_t st = cublasSetStream(h->blas, s);
-  if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "cublasSetStream");
-  const float one = 1.0f, zero = 0.0f;
-  // kv[l] [n][2KD] = u[l] [n][H] . W_kv[l]^T  (column-major: W_kv[l] is H x 2KD)
-  st = cublasGemmStridedBatchedEx(
-      h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * KD, a.n, d.hidden, &one, h->w.w_kv, CUDA_R_16BF,
-      d.hidden, (long long)2 * KD * d.hidden, h->u, CUDA_R_16BF, d.hidden, (long long)a.n * d.hidden,
-      &zero, h->kv, CUDA_R_16BF, 2 * KD, (long long)a.n * 2 * KD, d.n_layers, CUBLAS_COMPUTE_32F,
-      CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "K/V projection GEMM");
+  if (stream_w) {
+    moe::GemvParams gp{};
+    gp.W = reinterpret_cast<const __nv_bfloat16*>(h->w.w_kv);
+    gp.X = h->u;
+    gp.part = h->part;
+    gp.L = d.n_layers;
+    gp.R = 2 * KD;
+    gp.K = d.hidden;
+    gp.n = a.n;
+    gp.S = h->splits;
+    gp.KC = d.hidden / h->splits;
+    cudaLaunchConfig_t gc = {};
+    gc.gridDim = dim3(h->num_sms, 1, 1);
+    gc.blockDim = dim3(moe::kGemvThreads, 1, 1);
+    gc.dynamicSmemBytes = moe::kGemvSmem;
+    gc.stream = s;
+    gc.attrs = ev ? nullptr : &pdl;  // profiled launches are timed one at a time
+    gc.numAttrs = ev ? 0 : 1;
+    e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel, gp);
+    if (e != cudaSuccess) return ck_cuda(e, "K/V projection launch");
+  } else {
+    cublasStatus_t st = cublasSetStream(h->blas, s);
+    if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "cublasSetStream");
+    const float one = 1.0f, zero = 0.0f;
+    // kv[l] [n][2KD] = u[l] [n][H] . W_kv[l]^T  (column-major: W_kv[l] is H x 2KD)
+    st = cublasGemmStridedBatchedEx(
+        h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * KD, a.n, d.hidden, &one, h->w.w_kv, CUDA_R_16BF,
+        d.hidden, (long long)2 * KD * d.hidden, h->u, CUDA_R_16BF, d.hidden, (long long)a.n * d.hidden,
+        &zero, h->kv, CUDA_R_16BF, 2 * KD, (long long)a.n * 2 * KD, d.n_layers, CUBLAS_COMPUTE_32F,
+        CUBLAS_GEMM_DEFAULT);
+    if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "K/V projection GEMM");
+  }
   mark(2);
   moe::KvRopeParams kp{};
   kp.n = a.n;
@@ -315,6 +389,8 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   kp.cs = h->cs;
   kp.positions = a.positions;
   kp.kv = h->kv;
+  kp.part = stream_w ? h->part : nullptr;
+  kp.S = h->splits;
   kp.k_out = a.k_out ? reinterpret_cast<__nv_bfloat16*>(a.k_out) : h->k;
   kp.v_out = a.v_out ? reinterpret_cast<__nv_bfloat16*>(a.v_out) : h->v;
   kp.slots = a.slots;
@@ -324,13 +400,17 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   kp.v_cache = reinterpret_cast<__nv_bfloat16*>(a.v_cache);
   kp.err = h->err;
   const long long warps = (long long)d.n_layers * a.n * d.n_kv_heads;
-  const int blocks = (int)((warps * 32 + 255) / 256);
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3((unsigned)((warps * 32 + 255) / 256), 1, 1);
+  rc.blockDim = dim3(256, 1, 1);
+  rc.stream = s;
+  rc.attrs = (stream_w && !ev) ? &pdl : nullptr;
+  rc.numAttrs = (stream_w && !ev) ? 1 : 0;
   switch (d.head_dim) {
-    case 64: moe::kv_rope_kernel<2><<<blocks, 256, 0, s>>>(kp); break;
-    case 128: moe::kv_rope_kernel<4><<<blocks, 256, 0, s>>>(kp); break;
-    default: moe::kv_rope_kernel<8><<<blocks, 256, 0, s>>>(kp); break;
+    case 64: e = cudaLaunchKernelEx(&rc, moe::kv_rope_kernel<2>, kp); break;
+    case 128: e = cudaLaunchKernelEx(&rc, moe::kv_rope_kernel<4>, kp); break;
+    default: e = cudaLaunchKernelEx(&rc, moe::kv_rope_kernel<8>, kp); break;
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return ck_cuda(e, "key norm / rotary launch");
   mark(3);
   return MOE_OK;
@@ -372,10 +452,27 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   h->w = *w;
   const size_t n = d.max_ctx, H = d.hidden, L = d.n_layers, KD = (size_t)d.n_kv_heads * d.head_dim;
   const size_t table = d.rope_theta > 0.0 ? (size_t)d.max_position * (d.head_dim / 2) : 0;
+  int num_sms = 0;
+  e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    delete h;
+    return ck_cuda(e, "device query");
+  }
+  h->num_sms = num_sms;
+  h->splits = moe::gemv_splits(d.n_layers, 2 * d.n_kv_heads * d.head_dim, d.hidden, num_sms);
+  if (h->splits) {
+    e = cudaFuncSetAttribute(moe::gemv_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)moe::kGemvSmem);
+    if (e != cudaSuccess) {
+      delete h;
+      return ck_cuda(e, "streaming projection shared memory");
+    }
+  }
+  const size_t b_part = h->splits ? (size_t)h->splits * L * 8 * 2 * KD * sizeof(float) : 0;
   auto up16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
   const size_t b_fc = up16(2 * n * H), b_u = up16(2 * L * n * H), b_kv = up16(2 * L * n * 2 * KD),
                b_k = up16(2 * L * n * KD), b_cs = table * sizeof(float2);
-  const size_t bytes = b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
+  const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kCtxBlasWorkspace);
@@ -385,6 +482,8 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
     return moe::api_fail(MOE_ENOMEM, "context-KV workspace");
   }
   h->base = base;
+  h->part = h->splits ? reinterpret_cast<float*>(base) : nullptr;
+  base += b_part;
   h->fc = reinterpret_cast<__nv_bfloat16*>(base);
   h->u = reinterpret_cast<__nv_bfloat16*>(base + b_fc);
   h->kv = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u);
