@@ -67,17 +67,27 @@ __device__ __forceinline__ void route_finish(const RouterParams& p, int r, int n
   if (lane == 0) ws.flags[r] = (nsel > k) ? (uint8_t)((ek - ek1) / z < 1e-6f) : (uint8_t)0;
 }
 
+// Order-preserving 32-bit keys of fp32 logits (larger logit, larger key);
+// -0 is keyed as +0 so that equal logits tie.  Key 0 is below every logit.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // One row's routing for E <= 256: lane owns experts e = lane + 32 i (i < 8),
 // their logits in registers.  The slices' partial sums are all loaded at
-// once and added in slice order; the lane's 8 candidates are sorted once
-// (Batcher's odd-even merge network, 19 comparators) and each of the k + 1
-// selections is one warp arg-max of the lanes' heads, after which the
-// winning lane shifts its list.
+// once and added in slice order.  Each of the k + 1 selections is two warp
+// reductions: the largest key among the lanes' heads (redux.sync max), then
+// the lowest expert id among the lanes whose head has that key (redux.sync
+// min), so ties go to the lower id; the winning lane drops the expert and
+// rescans its 8 keys for its next head (largest key, lowest id).
 __device__ void route_row_small(const RouterParams& p, int r, int* sids) {
   const Workspace& ws = p.ws;
   const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
   float v[8];
-  int id[8];
   float part[8][8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
@@ -88,7 +98,7 @@ __device__ void route_row_small(const RouterParams& p, int r, int* sids) {
       part[s][i] = (s < p.S && e < E) ? __ldcg(src + e) : 0.0f;
     }
   }
-  float m = -INFINITY;
+  uint32_t key[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
@@ -99,63 +109,49 @@ __device__ void route_row_small(const RouterParams& p, int r, int* sids) {
     if (e < E) {
       if (p.bias) acc += __ldg(p.bias + e);
       ws.logits[(size_t)r * E + e] = acc;
-      m = fmaxf(m, acc);
-      v[i] = acc;
-      id[i] = e;
-    } else {
-      v[i] = -INFINITY;
-      id[i] = 0x7fffffff;
     }
+    v[i] = acc;
+    key[i] = (e < E) ? logit_key(acc) : 0u;
   }
-  m = warp_max(m);
+  uint32_t lk = key[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) lk = max(lk, key[i]);
+  const float m = key_logit(__reduce_max_sync(0xffffffffu, lk));
   float z = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     if (lane + 32 * i < E) z += expf(v[i] - m);
   z = warp_sum(z);
-  constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
-                               {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
-                               {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+  uint32_t hk = key[0];
+  int hi = 0;
 #pragma unroll
-  for (int c = 0; c < 19; ++c) {
-    const int a = kNet[c][0], b = kNet[c][1];
-    if (route_before(v[b], id[b], v[a], id[a])) {
-      const float tv = v[a];
-      v[a] = v[b];
-      v[b] = tv;
-      const int ti = id[a];
-      id[a] = id[b];
-      id[b] = ti;
+  for (int i = 1; i < 8; ++i)
+    if (key[i] > hk) {
+      hk = key[i];
+      hi = i;
     }
-  }
   const int nsel = (k < E) ? k + 1 : k;
   int sel_id = -1;
   float sel_v = 0.0f;
   for (int t = 0; t < nsel; ++t) {
-    float bv = v[0];
-    int bi = id[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (route_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t gid = __reduce_min_sync(0xffffffffu, hk == gk ? (uint32_t)(lane + 32 * hi) : 0xffffffffu);
     if (lane == t) {
-      sel_id = bi;
-      sel_v = bv;
+      sel_id = (int)gid;
+      sel_v = key_logit(gk);
     }
-    const bool won = (id[0] == bi);
+    if (lane == (int)(gid & 31u)) {
 #pragma unroll
-    for (int i = 0; i < 7; ++i) {
-      v[i] = won ? v[i + 1] : v[i];
-      id[i] = won ? id[i + 1] : id[i];
-    }
-    if (won) {
-      v[7] = -INFINITY;
-      id[7] = 0x7fffffff;
+      for (int i = 0; i < 8; ++i)
+        if (i == hi) key[i] = 0u;
+      hk = key[0];
+      hi = 0;
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+        if (key[i] > hk) {
+          hk = key[i];
+          hi = i;
+        }
     }
   }
   route_finish(p, r, nsel, sel_id, sel_v, m, z, sids);
@@ -240,7 +236,6 @@ struct RouteSmem {
   unsigned* mask;   // [E][RW]
   int* sids;        // [rows * k]
   int* wtot;        // [3][warps]
-  int* pk;          // [rows * k + 4]  pair's (expert | rank << 16), 16-byte aligned
 };
 
 __device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t* smem) {
@@ -252,8 +247,6 @@ __device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t*
   r.mask = reinterpret_cast<unsigned*>(r.off + p.E + 1);
   r.sids = reinterpret_cast<int*>(r.mask + p.E * RW);
   r.wtot = r.sids + p.rows * p.k;
-  r.pk = reinterpret_cast<int*>(
-      (reinterpret_cast<uintptr_t>(r.wtot + 3 * kRouterWarps) + 15) & ~static_cast<uintptr_t>(15));
   return r;
 }
 
@@ -283,63 +276,71 @@ __device__ void pool_reset(const RouterParams& p) {
   }
 }
 
-// Pooler for at most kRouterThreads pairs, without scans: each pair's rank
-// among its expert's pairs, then per expert one pass over the pairs (packed
-// as expert | rank << 16, four per load) for its offset, count, active index
-// and first virtual part (a part starts at every pair whose rank is a
-// multiple of kVirtualPairs).  The results equal the scanning pooler's.
+// Pooler for at most kRouterThreads pairs, one thread per pair.  A pair's
+// rank among its expert's pairs (pairs are in (row, slot) order, so they rank
+// by row) is its warp's match count below it plus the matches in earlier
+// warps; the counts come from shared-memory atomics.  One block-wide
+// exclusive scan over the experts of (count, active flag, work items)
+// packed 10 bits each (every field stays below 1024: at most 256 pairs)
+// gives each expert its offset, active index and first work item.  The
+// results equal the scanning pooler's.
 __device__ void pool_small(const RouterParams& p, uint8_t* smem, bool ids_in_smem) {
   const Workspace& ws = p.ws;
-  const int E = p.E, npairs = p.rows * p.k, tid = threadIdx.x;
+  const int E = p.E, npairs = p.rows * p.k, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RouteSmem rs = route_carve(p, smem);
   int* sids = rs.sids;
-  int* pk = rs.pk;
-  int* off = rs.off;
-  if (!ids_in_smem) {
+  int* cnt = rs.cnt;  // counts, then offsets
+  int* wtot = rs.wtot;
+  for (int e = tid; e < E; e += kRouterThreads) cnt[e] = 0;
+  if (!ids_in_smem)
     for (int q = tid; q < npairs; q += kRouterThreads) sids[q] = __ldcg(ws.ids + q);
-    __syncthreads();
-  }
-  // pairs are in (row, slot) order, so within an expert they rank by row
+  __syncthreads();
   const int eq = (tid < npairs) ? sids[tid] : -1;
   const bool valid = eq >= 0 && eq < E;
-  int rank = 0;
-  if (valid)
-    for (int q = 0; q < tid; ++q) rank += (sids[q] == eq);
-  if (tid < ((npairs + 3) & ~3)) pk[tid] = valid ? (eq | (rank << 16)) : -1;  // -1: no expert
-  const int n_valid = __syncthreads_count(valid);
-  const int n_act = __syncthreads_count(valid && rank == 0);
-  const int n_virt = __syncthreads_count(valid && (rank % kVirtualPairs) == 0);
-  const int4* pk4 = reinterpret_cast<const int4*>(pk);
-  for (int e = tid; e < E; e += kRouterThreads) {
-    int o = 0, c = 0, a = 0, v = 0;
-    for (int q4 = 0; q4 < (npairs + 3) / 4; ++q4) {
-      const int4 w = pk4[q4];
-      const int ws4[4] = {w.x, w.y, w.z, w.w};
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? eq : -1 - lane);
+  int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid) {
+    for (int q = 0; q < warp * 32; ++q) rank += (sids[q] == eq);
+    atomicAdd(&cnt[eq], 1);
+  }
+  __syncthreads();
+  const int per = (E + kRouterThreads - 1) / kRouterThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int loc = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt[e];
+    loc += c | ((c > 0) << 10) | (((c + kVirtualPairs - 1) / kVirtualPairs) << 20);
+  }
+  int inc = loc;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ex = ws4[i] & 0xFFFF, rq = ws4[i] >> 16;  // no expert: ex 0xFFFF
-        const int lt = ex < e;
-        o += lt;
-        a += lt & (rq == 0);
-        v += lt & ((rq & (kVirtualPairs - 1)) == 0);
-        c += (ex == e);
-      }
-    }
-    off[e] = o;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) wtot[warp] = inc;
+  __syncthreads();
+  int ex = inc - loc;
+  for (int w = 0; w < warp; ++w) ex += wtot[w];
+  int o = ex & 1023, a = (ex >> 10) & 1023, v = ex >> 20;
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt[e];
+    cnt[e] = o;
     ws.offset[e] = o;
     ws.count[e] = c;
-    if (c > 0) ws.active[a] = e;
+    if (c > 0) ws.active[a++] = e;
+    // the expert's work items: its pairs in groups of at most kVirtualPairs
     for (int g0 = 0; g0 < c; g0 += kVirtualPairs)
       ws.act_info[v++] = pack_expert(e, o + g0, min(kVirtualPairs, c - g0));
+    o += c;
   }
-  if (tid == 0) {
-    ws.offset[E] = n_valid;
-    ws.n_active[0] = n_act;
-    ws.n_virtual[0] = n_virt;
+  if (tid == kRouterThreads - 1) {
+    ws.offset[E] = o;
+    ws.n_active[0] = a;
+    ws.n_virtual[0] = v;
   }
   __syncthreads();
   if (valid) {
-    const int pos = off[eq] + rank;
+    const int pos = cnt[eq] + rank;
     ws.pair_order[pos] = tid;
     ws.pos_of_pair[tid] = pos;
   }
@@ -487,7 +488,7 @@ __device__ void quantize_share(const RouterParams& p, float sg) {
   if (cta == 0 && threadIdx.x == 0) ws.x_sg[0] = sg;
 }
 
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) {
+__global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
   const Workspace& ws = p.ws;
@@ -588,7 +589,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 size_t router_smem_bytes(int E, int rows) {
   const int RW = (rows + 31) / 32;
   const size_t route = (size_t)kRouterWarps * E * 4 + (size_t)E * 4 + (size_t)(E + 1) * 4 +
-                       (size_t)E * RW * 4 + 2 * (size_t)rows * kMaxTopK * 4 + 3 * kRouterWarps * 4 + 48;
+                       (size_t)E * RW * 4 + (size_t)rows * kMaxTopK * 4 + 3 * kRouterWarps * 4;
   const size_t xslice = (size_t)kRowBlock * kRouterChunks * 32 * 16;
   return route > xslice ? route : xslice;
 }
