@@ -586,7 +586,7 @@ def run_dense(args, w):
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT,
                 "h2d_bytes_per_step": rows * H * (4 + 2), "d2h_bytes_per_step": rows * H * 4},
         "gpu_launches": 3 * args.steps,
-        "library_launches": 2 * args.steps,
+        "library_launches": (dl.kernel_count(rows) - 3) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and ws == 1:
@@ -734,7 +734,7 @@ def run_ctxkv(args, w):
                 "h2d_bytes_per_step": n * H * 2 + n * 8 * 2,
                 "d2h_bytes_per_step": 2 * L * n * KVH * D * 2},
         "gpu_launches": (3 if streamed else 2) * args.steps,
-        "library_launches": 0 if streamed else args.steps,
+        "library_launches": (op.kernel_count(n) - (3 if streamed else 2)) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and ws == 1:

@@ -299,6 +299,12 @@ int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, 
 /* Workspace pointers of the last layer call (see moe_dense_debug_view). */
 int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
 
+/* Kernels one moe_dense_layer call of `rows` rows launches: the library's own
+ * three and the cuBLAS GEMMs' (whose count cuBLAS chooses per shape).
+ * Counted by capturing a call into a graph on a private stream (nothing
+ * runs).  Returns the count (> 0) or a negative MOE_E* code. */
+int moe_dense_kernel_count(moe_dense_t* h, int rows);
+
 void moe_dense_destroy(moe_dense_t* h);
 
 /* ------------------------------------------------------------------------
@@ -381,6 +387,12 @@ int moe_ctxkv_debug(moe_ctxkv_t* h, moe_ctxkv_debug_view* view);
 /* Synchronizes the device and returns MOE_EDEVICE if a projection latched a
  * device-side error since the last call (and clears it), else MOE_OK. */
 int moe_ctxkv_last_error(moe_ctxkv_t* h);
+
+/* Kernels one moe_ctxkv_project call of n_ctx rows launches (the library's
+ * three; with more than 8 rows the norm and key kernels plus cuBLAS's).
+ * Counted by capturing a call into a graph on a private stream (nothing
+ * runs).  Returns the count (> 0) or a negative MOE_E* code. */
+int moe_ctxkv_kernel_count(moe_ctxkv_t* h, int n_ctx);
 
 void moe_ctxkv_destroy(moe_ctxkv_t* h);
 

@@ -26,9 +26,9 @@ EXPORTS = (
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
-    "moe_dense_destroy",
+    "moe_dense_kernel_count", "moe_dense_destroy",
     "moe_ctxkv_create", "moe_ctxkv_project", "moe_ctxkv_profile", "moe_ctxkv_debug",
-    "moe_ctxkv_last_error", "moe_ctxkv_destroy",
+    "moe_ctxkv_last_error", "moe_ctxkv_kernel_count", "moe_ctxkv_destroy",
 )
 
 
@@ -119,6 +119,7 @@ def _lib():
             "moe_dense_layer": (i32, [vp, i32, vp, vp, vp]),
             "moe_dense_layer_profile": (i32, [vp, i32, vp, vp, vp, vp]),
             "moe_dense_debug": (i32, [vp, ctypes.POINTER(DenseDebugView)]),
+            "moe_dense_kernel_count": (i32, [vp, i32]),
             "moe_dense_destroy": (None, [vp]),
             "moe_ctxkv_create": (i32, [ctypes.POINTER(CtxKvDims), ctypes.POINTER(CtxKvWeights),
                                        ctypes.POINTER(vp)]),
@@ -126,6 +127,7 @@ def _lib():
             "moe_ctxkv_profile": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp]),
             "moe_ctxkv_debug": (i32, [vp, ctypes.POINTER(CtxKvDebugView)]),
             "moe_ctxkv_last_error": (i32, [vp]),
+            "moe_ctxkv_kernel_count": (i32, [vp, i32]),
             "moe_ctxkv_destroy": (None, [vp]),
         }
         for name, (res, args) in sig.items():
@@ -350,6 +352,11 @@ class DenseLayer:
                                               _stream(stream), ms), "moe_dense_layer_profile")
         return list(ms)
 
+    def kernel_count(self, rows):
+        n = _lib().moe_dense_kernel_count(self.handle, rows)
+        _check(min(n, 0), "moe_dense_kernel_count")
+        return n
+
     def debug(self) -> DenseDebugView:
         v = DenseDebugView()
         _check(_lib().moe_dense_debug(self.handle, ctypes.byref(v)), "moe_dense_debug")
@@ -404,6 +411,11 @@ class ContextKV:
         _check(_lib().moe_ctxkv_profile(self.handle, n_ctx, _ptr(context), _ptr(positions), sp, stride,
                                         kc, vc, n_slots, _stream(stream), ms), "moe_ctxkv_profile")
         return list(ms)
+
+    def kernel_count(self, n_ctx):
+        n = _lib().moe_ctxkv_kernel_count(self.handle, n_ctx)
+        _check(min(n, 0), "moe_ctxkv_kernel_count")
+        return n
 
     def debug(self) -> CtxKvDebugView:
         v = CtxKvDebugView()

@@ -553,6 +553,43 @@ int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const 
   return MOE_OK;
 }
 
+int moe_ctxkv_kernel_count(moe_ctxkv_t* h, int n_ctx) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  // capture one projection of n_ctx rows on a private stream (the handle's
+  // own buffers as inputs, no cache write; nothing runs) and count the
+  // graph's kernel nodes
+  const ProjectArgs a{n_ctx, reinterpret_cast<const uint16_t*>(h->fc), reinterpret_cast<const int64_t*>(h->k),
+                      nullptr, 0, nullptr, nullptr, 0, nullptr, nullptr};
+  int rc = check_project(h, a);
+  if (rc) return rc;
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return ck_cuda(e, "stream create");
+  cudaGraph_t g = nullptr;
+  e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    rc = ctxkv_enqueue(h, a, s, nullptr);
+    e = cudaStreamEndCapture(s, &g);
+  }
+  int count = 0;
+  size_t nn = 0;
+  if (e == cudaSuccess && !rc) e = cudaGraphGetNodes(g, nullptr, &nn);
+  if (e == cudaSuccess && !rc && nn) {
+    std::vector<cudaGraphNode_t> nodes(nn);
+    e = cudaGraphGetNodes(g, nodes.data(), &nn);
+    for (size_t i = 0; i < nn && e == cudaSuccess; ++i) {
+      cudaGraphNodeType t;
+      e = cudaGraphNodeGetType(nodes[i], &t);
+      count += (t == cudaGraphNodeTypeKernel);
+    }
+  }
+  if (g) cudaGraphDestroy(g);
+  cudaStreamDestroy(s);
+  if (rc) return rc;
+  if (e != cudaSuccess) return ck_cuda(e, "launch count capture");
+  return count;
+}
+
 int moe_ctxkv_debug(moe_ctxkv_t* h, moe_ctxkv_debug_view* v) {
   if (!h || !v) return moe::api_fail(MOE_EINVAL, "handle and view are required");
   v->fc = h->fc;

@@ -22,6 +22,7 @@
 #include <cublas_v2.h>
 
 #include <cstdio>
+#include <vector>
 
 #include "../../include/moe_decode.h"
 #include "common.cuh"
@@ -222,6 +223,40 @@ int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, 
   if (rc) return rc;
   if (e != cudaSuccess) return cuda_err(e, "profile events");
   return MOE_OK;
+}
+
+int moe_dense_kernel_count(moe_dense_t* h, int rows) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  int rc = check_rows_dense(h, rows);
+  if (rc) return rc;
+  // capture one layer on a private stream (inputs: the handle's own buffers,
+  // nothing runs) and count the graph's kernel nodes
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_err(e, "stream create");
+  cudaGraph_t g = nullptr;
+  e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    rc = dense_enqueue(h, rows, reinterpret_cast<const uint16_t*>(h->x), reinterpret_cast<float*>(h->gu), s, nullptr);
+    e = cudaStreamEndCapture(s, &g);
+  }
+  int count = 0;
+  size_t n = 0;
+  if (e == cudaSuccess && !rc) e = cudaGraphGetNodes(g, nullptr, &n);
+  if (e == cudaSuccess && !rc && n) {
+    std::vector<cudaGraphNode_t> nodes(n);
+    e = cudaGraphGetNodes(g, nodes.data(), &n);
+    for (size_t i = 0; i < n && e == cudaSuccess; ++i) {
+      cudaGraphNodeType t;
+      e = cudaGraphNodeGetType(nodes[i], &t);
+      count += (t == cudaGraphNodeTypeKernel);
+    }
+  }
+  if (g) cudaGraphDestroy(g);
+  cudaStreamDestroy(s);
+  if (rc) return rc;
+  if (e != cudaSuccess) return cuda_err(e, "launch count capture");
+  return count;
 }
 
 int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* v) {

@@ -181,6 +181,8 @@ def test_dense_layer_profile_and_row_limits():
         s_t, a_t = torch.from_numpy(stream).cuda(), _bf16_dev(attn)
         ms = case.layer.layer_profile(8, a_t, s_t)
         assert len(ms) == 5 and all(t > 0.0 for t in ms)
+        # the library's three kernels and at least one GEMM of the library's
+        assert case.layer.kernel_count(8) >= 4
         for rows in (0, 9):
             with pytest.raises(moe.MoeError):
                 case.layer.layer(rows, a_t, s_t)
