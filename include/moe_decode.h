@@ -169,12 +169,16 @@ int moe_decode_step(moe_decode_t* h, int rows, const uint16_t* branch, float* st
 int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
                           uint16_t* out, void* cuda_stream);
 
-/* End-to-end step on HOST buffers: copies branch and stream in (H2D), replays
- * the step graph, copies stream and out back (D2H) and synchronizes the
- * stream.  When all three buffers are page-locked, the copies and the step
- * are one library-owned graph (cached per rows and buffers, captured on the
- * first call), launched once per call; pageable buffers take separate copies
- * around the step graph. */
+/* End-to-end step on HOST buffers: brings branch and stream in, runs the
+ * step, returns stream and out, and synchronizes the stream.  When all three
+ * buffers are page-locked the step is one library-owned graph (cached per
+ * rows and buffers, captured on the first call), launched once per call; if
+ * the runtime also maps them into the device's address space (and stream is
+ * 16-byte, branch and out 8-byte aligned), the first boundary reads branch
+ * and stream from host memory and the final boundary writes stream and out
+ * there, so the graph holds no copy-engine copies, else it copies in and out
+ * around the step.  Pageable buffers take separate copies around the step
+ * graph. */
 int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
                          float* stream_host, uint16_t* out_host, void* cuda_stream);
 

@@ -106,7 +106,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
     for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss += *cluster.map_shared_rank(&part[0], q);
     const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
     if (live) {
-      s = __ldcg(reinterpret_cast<const float4*>(srow));
+      s = __ldcg(reinterpret_cast<const float4*>(p.stream_in ? p.stream_in + (size_t)r * p.H + col : srow));
       s.x += y.x * inv1 * wpost.x;
       s.y += y.y * inv1 * wpost.y;
       s.z += y.z * inv1 * wpost.z;

@@ -67,6 +67,17 @@ bool host_pinned(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
+// The address at which the current device may access pinned host memory p
+// (mapped into its address space), or null: the runtime reports none.
+void* host_mapped(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 struct GraphEntry {
   int rows;
   const void* branch;
@@ -358,7 +369,7 @@ int check_rows(const moe_decode_t* h, int rows) {
 }
 
 int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, float* stream,
-                 cudaStream_t s, cudaEvent_t* ev = nullptr) {
+                 cudaStream_t s, cudaEvent_t* ev = nullptr, const float* stream_in = nullptr) {
   const bool pdl = (ev == nullptr);
   auto mark = [&](int i) {
     if (ev) cudaEventRecord(ev[i], s);
@@ -376,6 +387,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   bp.o = h->ws.o;
   bp.gates = h->ws.gates;
   bp.stream = stream;
+  bp.stream_in = stream_in;
   bp.w_post = w.w_post;
   bp.w_pre = w.w_pre;
   bp.x_out = h->ws.x;
@@ -493,13 +505,16 @@ int check_step_args(moe_decode_t* h, int rows, const void* branch, const float* 
   return MOE_OK;
 }
 
+// stream_in: where the first layer reads the stream (null: stream itself);
+// aux: where the final boundary also writes the final stream (or null).
 int enqueue_step(moe_decode_t* h, int rows, const uint16_t* branch, float* stream, uint16_t* out,
-                 cudaStream_t s) {
+                 cudaStream_t s, const float* stream_in = nullptr, float* aux = nullptr) {
   for (int l = 0; l < h->d.n_layers; ++l) {
-    const int rc = launch_layer(h, l, rows, l == 0 ? branch : nullptr, stream, s);
+    const int rc = launch_layer(h, l, rows, l == 0 ? branch : nullptr, stream, s, nullptr,
+                                l == 0 ? stream_in : nullptr);
     if (rc) return rc;
   }
-  return launch_final(h, rows, stream, out, s);
+  return launch_final(h, rows, stream, out, s, aux);
 }
 
 }  // namespace
@@ -755,16 +770,30 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
         exec = g.exec;
     if (!exec) {
       cudaStream_t c = h->cap_stream;
+      // mapped pinned buffers: the first boundary reads the branch and the
+      // stream from host memory and the final boundary writes the output and
+      // the stream back there, so the kernels make the copies themselves;
+      // otherwise copy-engine copies around the step
+      const uint16_t* branch_d = static_cast<const uint16_t*>(host_mapped(branch_host));
+      float* stream_d = static_cast<float*>(host_mapped(stream_host));
+      uint16_t* out_d = static_cast<uint16_t*>(host_mapped(out_host));
+      const bool direct = branch_d && stream_d && out_d && aligned(stream_d, 16) && aligned(branch_d, 8) &&
+                          aligned(out_d, 8);
       cudaError_t e = cudaStreamBeginCapture(c, cudaStreamCaptureModeThreadLocal);
       if (e != cudaSuccess) return cuda_fail(e, "begin capture");
-      e = cudaMemcpyAsync(h->io_branch, branch_host, n * 2, cudaMemcpyHostToDevice, c);
-      if (e == cudaSuccess) e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, c);
-      int erc = (e == cudaSuccess) ? enqueue_step(h, rows, h->io_branch, h->io_stream, h->io_out, c)
-                                   : cuda_fail(e, "input copy");
-      if (!erc) {
-        e = cudaMemcpyAsync(stream_host, h->io_stream, n * 4, cudaMemcpyDeviceToHost, c);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, h->io_out, n * 2, cudaMemcpyDeviceToHost, c);
-        if (e != cudaSuccess) erc = cuda_fail(e, "output copy");
+      int erc = 0;
+      if (direct) {
+        erc = enqueue_step(h, rows, branch_d, h->io_stream, out_d, c, stream_d, stream_d);
+      } else {
+        e = cudaMemcpyAsync(h->io_branch, branch_host, n * 2, cudaMemcpyHostToDevice, c);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, c);
+        erc = (e == cudaSuccess) ? enqueue_step(h, rows, h->io_branch, h->io_stream, h->io_out, c)
+                                 : cuda_fail(e, "input copy");
+        if (!erc) {
+          e = cudaMemcpyAsync(stream_host, h->io_stream, n * 4, cudaMemcpyDeviceToHost, c);
+          if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, h->io_out, n * 2, cudaMemcpyDeviceToHost, c);
+          if (e != cudaSuccess) erc = cuda_fail(e, "output copy");
+        }
       }
       cudaGraph_t graph = nullptr;
       e = cudaStreamEndCapture(c, &graph);

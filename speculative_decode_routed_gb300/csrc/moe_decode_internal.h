@@ -78,6 +78,7 @@ struct BoundaryParams {
   const float* o;               // [rows*k][H]
   const float* gates;           // [rows][k]
   float* stream;                // [rows][H] in/out
+  const float* stream_in;       // [rows][H] read instead of stream when set (stream is still written)
   const float* w_post;          // [H]
   const float* w_pre;           // [H]
   __nv_bfloat16* x_out;         // [rows][H]
