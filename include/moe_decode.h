@@ -259,7 +259,9 @@ int moe_nvfp4_quantize_noalloc(const float* v, int64_t rows, int64_t cols, uint8
  *   g, u = bf16(W_gate x), bf16(W_up x)         gate_up_proj shards 0 / 1
  *   a  = bf16(silu(g) * u);  f = bf16(W_down a)
  *   s2 = s1 + rmsnorm(f) * w_post_ffn                      (fp32 stream)
- * The projections are plain bf16 GEMMs (cuBLAS, fp32 accumulation).
+ * Up to 8 rows with H and I multiples of 128 the projections are the
+ * library's own weight-streaming kernels (fp32 accumulation, SiLU * mul fused
+ * into gate/up); otherwise plain bf16 GEMMs (cuBLAS, fp32 accumulation).
  * ---------------------------------------------------------------------- */
 typedef struct moe_dense_s moe_dense_t;
 
@@ -303,8 +305,9 @@ int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, 
 /* Workspace pointers of the last layer call (see moe_dense_debug_view). */
 int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
 
-/* Kernels one moe_dense_layer call of `rows` rows launches: the library's own
- * three and the cuBLAS GEMMs' (whose count cuBLAS chooses per shape).
+/* Kernels one moe_dense_layer call of `rows` rows launches: four of the
+ * library's own on the streamed path, else its three and the cuBLAS GEMMs'
+ * (whose count cuBLAS chooses per shape).
  * Counted by capturing a call into a graph on a private stream (nothing
  * runs).  Returns the count (> 0) or a negative MOE_E* code. */
 int moe_dense_kernel_count(moe_dense_t* h, int rows);

@@ -70,6 +70,34 @@ __global__ void boundary_kernel(BoundaryParams p) {
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
       y = make_float4(a.x, a.y, b.x, b.y);
+    } else if (p.part) {
+      // the branch is the split-K partials' sum in split order, as bf16;
+      // eight splits' loads in flight at a time
+      const size_t split = (size_t)p.rows * p.H;
+      const float* src = p.part + (size_t)r * p.H + col;
+      for (int s0 = 0; s0 < p.part_S; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v[j] = (s0 + j < p.part_S) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(s0 + j) * split))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          y.x += v[j].x;
+          y.y += v[j].y;
+          y.z += v[j].z;
+          y.w += v[j].w;
+        }
+      }
+      const __nv_bfloat162 b01 = __floats2bfloat162_rn(y.x, y.y), b23 = __floats2bfloat162_rn(y.z, y.w);
+      if (p.part_out) {
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&b01);
+        packed.y = *reinterpret_cast<const uint32_t*>(&b23);
+        *reinterpret_cast<uint2*>(p.part_out + (size_t)r * p.H + col) = packed;
+      }
+      const float2 f01 = __bfloat1622float2(b01), f23 = __bfloat1622float2(b23);
+      y = make_float4(f01.x, f01.y, f23.x, f23.y);
     } else {
       // all slots' loads in flight at once (k <= 16), summed in slot order
       float g[16];

@@ -364,7 +364,7 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
     gc.stream = s;
     gc.attrs = ev ? nullptr : &pdl;  // profiled launches are timed one at a time
     gc.numAttrs = ev ? 0 : 1;
-    e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel, gp);
+    e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel<false>, gp);
     if (e != cudaSuccess) return ck_cuda(e, "K/V projection launch");
   } else {
     cublasStatus_t st = cublasSetStream(h->blas, s);
@@ -461,7 +461,7 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   h->num_sms = num_sms;
   h->splits = moe::gemv_splits(d.n_layers, 2 * d.n_kv_heads * d.head_dim, d.hidden, num_sms);
   if (h->splits) {
-    e = cudaFuncSetAttribute(moe::gemv_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(moe::gemv_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)moe::kGemvSmem);
     if (e != cudaSuccess) {
       delete h;

@@ -16,9 +16,15 @@
 //   f  = bf16(W_down a)
 //   s2 = s1 + rmsnorm(f) * w_post_ffn                        (fp32)
 //
-// GB300 layout: the norms run in the boundary kernel (cluster per row); the
-// two projections are plain bf16 GEMMs of a few rows (cuBLAS, fp32 compute,
-// bf16 out, weights streamed once); SiLU * mul is one elementwise kernel.
+// GB300 layout: the norms run in the boundary kernel (cluster per row).  Up
+// to 8 rows the projections are the library's weight-streaming kernel
+// (gemv.cuh): gate/up pairs each gate row with its up row in one task and
+// writes gu and SiLU * mul from its accumulators; the down projection leaves
+// fp32 split-K partials, which the output boundary sums in split order into
+// the bf16 branch.  Four launches chained by programmatic dependent launch.
+// Beyond 8 rows (or for widths the streamed kernels do not take) the
+// projections are plain bf16 GEMMs (cuBLAS, fp32 compute, bf16 out) and SiLU *
+// mul is one elementwise kernel.
 #include <cublas_v2.h>
 
 #include <cstdio>
@@ -26,6 +32,7 @@
 
 #include "../../include/moe_decode.h"
 #include "common.cuh"
+#include "gemv.cuh"
 #include "moe_decode_internal.h"
 
 namespace moe {
@@ -53,6 +60,9 @@ struct moe_dense_s {
   void* blas_ws;
   size_t blas_ws_bytes;
   __nv_bfloat16 *x, *gu, *a, *f;  // [R][H], [R][2I], [R][I], [R][H]
+  float* part;                     // down projection's split-K partials [S][8][H], or null
+  int down_splits;                 // K-splits of the streamed down projection; 0: no streaming
+  int num_sms;
 };
 
 namespace {
@@ -97,6 +107,64 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
   cudaError_t e = moe::launch_boundary(bp, h->cluster, s, false);
   if (e != cudaSuccess) return cuda_err(e, "pre-ffn boundary launch");
   mark(1);
+  if (h->down_splits && rows <= 8) {
+    // Up to 8 rows: the library's weight-streaming projections.  Gate/up
+    // pairs each gate row with its up row in one task and writes gu and
+    // SiLU * mul itself; the down projection leaves split-K partials that the
+    // output boundary sums.  Programmatic dependent launch between the four
+    // kernels (except when profiled, where each launch is timed alone).
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t gc = {};
+    gc.gridDim = dim3(h->num_sms, 1, 1);
+    gc.blockDim = dim3(moe::kGemvThreads, 1, 1);
+    gc.dynamicSmemBytes = moe::kGemvSmem;
+    gc.stream = s;
+    gc.attrs = ev ? nullptr : &pdl;
+    gc.numAttrs = ev ? 0 : 1;
+    moe::GemvParams gp{};
+    gp.W = reinterpret_cast<const __nv_bfloat16*>(h->w.w13);
+    gp.X = h->x;
+    gp.L = 1;
+    gp.R = 2 * d.inter;
+    gp.K = d.hidden;
+    gp.n = rows;
+    gp.S = 1;
+    gp.KC = d.hidden;
+    gp.I = d.inter;
+    gp.gu = h->gu;
+    gp.act = h->a;
+    e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel<true>, gp);
+    if (e != cudaSuccess) return cuda_err(e, "gate/up projection launch");
+    mark(2);
+    mark(3);  // SiLU * mul is part of the gate/up projection
+    moe::GemvParams dp{};
+    dp.W = reinterpret_cast<const __nv_bfloat16*>(h->w.w2);
+    dp.X = h->a;
+    dp.part = h->part;
+    dp.L = 1;
+    dp.R = d.hidden;
+    dp.K = d.inter;
+    dp.n = rows;
+    dp.S = h->down_splits;
+    dp.KC = d.inter / h->down_splits;
+    e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel<false>, dp);
+    if (e != cudaSuccess) return cuda_err(e, "down projection launch");
+    mark(4);
+    bp.branch = nullptr;
+    bp.part = h->part;
+    bp.part_S = h->down_splits;
+    bp.part_out = h->f;
+    bp.w_post = h->w.w_post_ffn;
+    bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
+    bp.x_out = nullptr;
+    bp.round_norm = 0;
+    e = moe::launch_boundary(bp, h->cluster, s, !ev);
+    if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
+    mark(5);
+    return MOE_OK;
+  }
   cublasStatus_t st = cublasSetStream(h->blas, s);
   if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "cublasSetStream");
   const float one = 1.0f, zero = 0.0f;
@@ -165,8 +233,30 @@ int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe
   h->d = d;
   h->w = *w;
   h->cluster = moe::boundary_cluster(d.hidden);
+  int num_sms = 0;
+  e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_err(e, "device query");
+  }
+  h->num_sms = num_sms;
+  // the streamed projections need H a multiple of 128 (gate/up K) and I one
+  // of 128 (down K; gate/up rows in groups of 16)
+  if (d.inter % 128 == 0) h->down_splits = moe::gemv_splits(1, d.hidden, d.inter, num_sms);
+  if (h->down_splits) {
+    e = cudaFuncSetAttribute(moe::gemv_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)moe::kGemvSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(moe::gemv_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)moe::kGemvSmem);
+    if (e != cudaSuccess) {
+      delete h;
+      return cuda_err(e, "streaming projection shared memory");
+    }
+  }
   const size_t R = (size_t)d.max_rows, H = (size_t)d.hidden, I = (size_t)d.inter;
-  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H);
+  const size_t part_bytes = h->down_splits ? (size_t)h->down_splits * 8 * H * sizeof(float) : 0;
+  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H) + part_bytes;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kBlasWorkspace);
@@ -180,6 +270,7 @@ int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe
   h->gu = h->x + R * H;
   h->a = h->gu + R * 2 * I;
   h->f = h->a + R * I;
+  h->part = h->down_splits ? reinterpret_cast<float*>(h->f + R * H) : nullptr;
   cublasStatus_t st = cublasCreate(&h->blas);
   if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, h->blas_ws_bytes);
   if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);

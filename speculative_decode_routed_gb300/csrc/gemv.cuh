@@ -28,8 +28,14 @@ namespace moe {
 struct GemvParams {
   const __nv_bfloat16* W;  // [L][R][K]
   const __nv_bfloat16* X;  // [L][n][K]
-  float* part;             // [S][L][n][R]
+  float* part;             // [S][L][n][R] (not gated)
   int L, R, K, n, S, KC;   // KC = K / S, a multiple of 128; R a multiple of 32
+  // Gated (a gate/up projection, R = 2I, S = 1): a task takes 16 gate rows
+  // j0.. and the matching 16 up rows I + j0.. as its two m-tiles and writes
+  // gu = bf16 of both and act = bf16(silu(gate) * up) instead of partials.
+  int I;
+  __nv_bfloat16* gu;   // [n][2I]
+  __nv_bfloat16* act;  // [n][I]
 };
 
 constexpr int kGemvWarps = 12;
@@ -59,6 +65,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+template <bool kGated>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p) {
   extern __shared__ uint4 gemv_ring[];
   // the dependents (the epilogue kernel) may launch now and wait for this grid
@@ -67,8 +74,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
   const int warp = threadIdx.x >> 5;
   const int wid = warp * (int)gridDim.x + (int)blockIdx.x;
   const int n_warps = kGemvWarps * (int)gridDim.x;
-  const int groups = p.R / kGemvRows;
+  const int groups = kGated ? p.I / 16 : p.R / kGemvRows;
   const int tasks = p.L * groups * p.S;
+  // rows of m-tile 1 relative to m-tile 0: the next 16 rows, or the up rows
+  const int mt1 = kGated ? p.I : 16;
   // this thread's pieces: slot st, piece j at ring[((warp * stages + st) * 16 + j) * 32 + lane]
   uint4* mine = gemv_ring + (size_t)warp * kGemvStages * kGemvPieces * 32 + lane;
   const uint32_t mine_s = smem_u32(mine);
@@ -77,8 +86,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
     const int s = task % p.S;
     const int mg = (task / p.S) % groups;
     const int l = task / (p.S * groups);
-    const __nv_bfloat16* w0 =
-        p.W + ((size_t)l * p.R + mg * kGemvRows + g) * p.K + (size_t)s * p.KC + t * 8;
+    const int row0 = kGated ? mg * 16 : mg * kGemvRows;
+    const __nv_bfloat16* w0 = p.W + ((size_t)l * p.R + row0 + g) * p.K + (size_t)s * p.KC + t * 8;
     const __nv_bfloat16* x0 = p.X + ((size_t)l * p.n + g) * p.K + (size_t)s * p.KC + t * 8;
     const int steps = p.KC / kGemvCols;
     // piece j: m-tile j >> 3, row g + 8 * ((j >> 2) & 1), 32-column block j & 3
@@ -88,7 +97,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
 #pragma unroll
         for (int j = 0; j < kGemvPieces; ++j)
           cp_async16(slot + j * 32 * 16,
-                     w0 + (size_t)((j >> 3) * 16 + ((j >> 2) & 1) * 8) * p.K + it * kGemvCols + (j & 3) * 32);
+                     w0 + (size_t)((j >> 3) * mt1 + ((j >> 2) & 1) * 8) * p.K + it * kGemvCols + (j & 3) * 32);
       }
       cp_async_commit();  // one group per step, empty past the end
     };
@@ -136,15 +145,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
       issue(it + kGemvStages);
     }
     cp_async_wait<0>();
-    float* out = p.part + ((size_t)s * p.L + l) * p.n * p.R + mg * kGemvRows;
+    if (kGated) {
+      // row j of the gate and of the up projection, context row i
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = mt * 16 + g + (j >> 1) * 8;
-        const int i = 2 * t + (j & 1);
-        if (i < p.n) out[(size_t)i * p.R + row] = acc[mt][j];
+      for (int q = 0; q < 4; ++q) {
+        const int j = row0 + g + (q >> 1) * 8;
+        const int i = 2 * t + (q & 1);
+        if (i < p.n) {
+          const __nv_bfloat16 gb = __float2bfloat16_rn(acc[0][q]), ub = __float2bfloat16_rn(acc[1][q]);
+          p.gu[(size_t)i * 2 * p.I + j] = gb;
+          p.gu[(size_t)i * 2 * p.I + p.I + j] = ub;
+          const float gv = __bfloat162float(gb), uv = __bfloat162float(ub);
+          p.act[(size_t)i * p.I + j] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+        }
       }
+    } else {
+      float* out = p.part + ((size_t)s * p.L + l) * p.n * p.R + mg * kGemvRows;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = mt * 16 + g + (q >> 1) * 8;
+          const int i = 2 * t + (q & 1);
+          if (i < p.n) out[(size_t)i * p.R + row] = acc[mt][q];
+        }
+    }
   }
 }
 

@@ -87,7 +87,11 @@ struct BoundaryParams {
                                 //    embedded tokens) itself, one norm (w_pre) into x_out
   float* aux;                   // [rows][H] copy of the updated stream, or null
   int round_norm;               // 1: the second norm reads the stream rounded to bf16
-};                              // (x_out may be null: no normalised output)
+                                // (x_out may be null: no normalised output)
+  const float* part;            // [part_S][rows][H] fp32 split-K partials of a bf16 branch,
+  int part_S;                   //   summed in split order and rounded to bf16 (when branch
+  __nv_bfloat16* part_out;      //   is null); the rounded branch also to part_out if set
+};
 
 // ------------------------------------------------------------- router (K2)
 struct RouterParams {
