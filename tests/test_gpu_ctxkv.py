@@ -156,6 +156,10 @@ def test_ragged_rows_with_per_layer_slots_and_skipped_rows():
           max_position=1 << 17, n_slots=40), 5),
     (dict(hidden=512, n_layers=1, n_kv_heads=1, head_dim=256, rope_theta=0.0, n_slots=16), 2),
     (dict(hidden=384, n_layers=2, n_kv_heads=4, head_dim=64, n_slots=300), 256),
+    # one 64-wide head over hidden 4096: the streamed projection in 32 K-splits,
+    # summed by the key kernel in four groups of eight
+    (dict(hidden=4096, n_layers=1, n_kv_heads=1, head_dim=64, n_slots=64), 8),
+    (dict(hidden=4096, n_layers=1, n_kv_heads=1, head_dim=64, n_slots=64), 3),
 ])
 def test_other_geometries(kw, n):
     w = _shape(SMALL, **kw)

@@ -126,7 +126,11 @@ def _check(case, rows, variant=0):
     return float(err.max()) / rms
 
 
-@pytest.mark.parametrize("hidden,inter,rows", [(256, 384, 8), (256, 384, 1), (1152, 520, 3),
+# (256, 384) and (256, 4096) take the streamed projections (the latter's down
+# projection in 16 K-splits, summed by the boundary in two groups of eight);
+# the others the library GEMMs
+@pytest.mark.parametrize("hidden,inter,rows", [(256, 384, 8), (256, 384, 1), (256, 4096, 8),
+                                               (256, 4096, 5), (1152, 520, 3),
                                                (1152, 520, 33), (384, 136, 128),
                                                (4224, 136, 2)])
 def test_dense_layer_matches_oracle(hidden, inter, rows):
