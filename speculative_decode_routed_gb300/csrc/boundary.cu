@@ -44,6 +44,9 @@ __device__ __forceinline__ void block_sum_to_slot(float v, float* warp_red, floa
   }
 }
 
+// KMAX: the most gather slots (k <= KMAX); 8 keeps the registers, and so
+// the CTAs per SM, of the common top-8 step.
+template <int KMAX>
 __global__ void boundary_kernel(BoundaryParams p) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float warp_red[32];
@@ -99,18 +102,18 @@ __global__ void boundary_kernel(BoundaryParams p) {
       const float2 f01 = __bfloat1622float2(b01), f23 = __bfloat1622float2(b23);
       y = make_float4(f01.x, f01.y, f23.x, f23.y);
     } else {
-      // all slots' loads in flight at once (k <= 16), summed in slot order
-      float g[16];
-      float4 o[16];
+      // all slots' loads in flight at once (k <= KMAX), summed in slot order
+      float g[KMAX];
+      float4 o[KMAX];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) {
+      for (int s = 0; s < KMAX; ++s) {
         if (s < p.k) {
           g[s] = __ldcg(p.gates + r * p.k + s);
           o[s] = __ldcg(reinterpret_cast<const float4*>(p.o + ((size_t)r * p.k + s) * p.H + col));
         }
       }
 #pragma unroll
-      for (int s = 0; s < 16; ++s) {
+      for (int s = 0; s < KMAX; ++s) {
         if (s < p.k) {
           y.x = fmaf(g[s], o[s].x, y.x);
           y.y = fmaf(g[s], o[s].y, y.y);
@@ -209,7 +212,7 @@ cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s
   attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, boundary_kernel, p);
+  return p.k <= 8 ? cudaLaunchKernelEx(&cfg, boundary_kernel<8>, p) : cudaLaunchKernelEx(&cfg, boundary_kernel<16>, p);
 }
 
 }  // namespace moe

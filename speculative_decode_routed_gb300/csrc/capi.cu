@@ -897,9 +897,13 @@ int moe_decode_last_error(moe_decode_t* h) {
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
 
 int moe_decode_step_kernel_count(const moe_decode_t* h) {
-  // the tensor-core build skips the pooler gather up to 32 rows
-  const int per_layer = (MOE_EXPERT_TC && h && h->d.max_rows <= 32) ? 3 : 4;
-  return h ? per_layer * h->d.n_layers + 1 : 0;
+  if (!h) return 0;
+  // boundary, router and the experts (or the CUDA-core build's gate/up and
+  // down), the routing kernel beyond 8 rows, and the tensor-core build's
+  // pooler gather beyond 32 rows; one final boundary per step
+  const int R = h->d.max_rows;
+  const int per_layer = (MOE_EXPERT_TC ? 3 + (R > 32) : 4) + (R > 8);
+  return per_layer * h->d.n_layers + 1;
 }
 
 void moe_decode_destroy(moe_decode_t* h) {

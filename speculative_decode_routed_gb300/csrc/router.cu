@@ -495,8 +495,6 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * p.EG + warp;
   const int sl = blockIdx.y;
-  const int rg = blockIdx.z;  // row group: rows [r0, r0 + nr)
-  const int r0 = rg * kRowBlock, nr = min(kRowBlock, p.rows - r0);
   const int nch = p.H / 8;
   const int c0 = sl * nch / p.S, c1 = (sl + 1) * nch / p.S;
 
@@ -512,18 +510,34 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
   grid_dep_wait();
   grid_dep_launch();
 
-  // this CTA's block of rows: the x slice is staged in shared memory with
-  // every load in flight at once, then each warp forms its expert's partial
+  // each block of 8 rows in turn: the x slice is staged in shared memory
+  // (every load in flight at once, the next block's already in registers
+  // while this one is multiplied), then each warp forms its expert's partial
   // dot products from registers and smem
   uint4* xs = reinterpret_cast<uint4*>(smem);  // [kRowBlock][kRouterChunks * 32]
   const int nc = c1 - c0;
-  {
-    for (int i = threadIdx.x; i < nr * nc; i += kRouterThreads) {
-      const int rr = i / nc, c = i % nc;
-      xs[rr * (kRouterChunks * 32) + c] =
-          __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)(r0 + rr) * p.H) + c0 + c);
+  const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
+  constexpr int kStage = kRowBlock * kRouterChunks * 32 / kRouterThreads;  // uint4 per thread
+  uint4 pre[kStage];
+  auto load_x = [&](int rb) {
+    const int r0 = rb * kRowBlock, nr = min(kRowBlock, p.rows - r0);
+#pragma unroll
+    for (int q = 0; q < kStage; ++q) {
+      const int i = threadIdx.x + q * kRouterThreads, rr = i / nc, c = i % nc;
+      pre[q] = (i < nr * nc) ? __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)(r0 + rr) * p.H) + c0 + c)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load_x(0);
+  for (int rb = 0; rb < nrb; ++rb) {
+    const int r0 = rb * kRowBlock, nr = min(kRowBlock, p.rows - r0);
+#pragma unroll
+    for (int q = 0; q < kStage; ++q) {
+      const int i = threadIdx.x + q * kRouterThreads;
+      if (i < nr * nc) xs[(i / nc) * (kRouterChunks * 32) + i % nc] = pre[q];
     }
     __syncthreads();
+    if (rb + 1 < nrb) load_x(rb + 1);
     if (warp < p.EG && e < p.E) {
       float acc[kRowBlock];
 #pragma unroll
@@ -537,51 +551,76 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
           }
         }
       }
+      // reduce-scatter over the lanes: each exchange halves the rows a lane
+      // keeps, so after three exchanges lanes 4m..4m+3 hold row m, and two
+      // more sum those four (9 shuffles for the 8 rows, not 40)
+      const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
+      float a4[4], a2[2];
 #pragma unroll
-      for (int rr = 0; rr < kRowBlock; ++rr) acc[rr] = warp_sum(acc[rr]);
-      if (lane < nr) {
-        float v = acc[0];
+      for (int j = 0; j < 4; ++j)
+        a4[j] = (h4 ? acc[j + 4] : acc[j]) + __shfl_xor_sync(0xffffffffu, h4 ? acc[j] : acc[j + 4], 16);
 #pragma unroll
-        for (int rr = 1; rr < kRowBlock; ++rr) v = (lane == rr) ? acc[rr] : v;
-        ws.logit_part[((size_t)sl * p.rows + r0 + lane) * p.E + e] = v;
-      }
+      for (int j = 0; j < 2; ++j)
+        a2[j] = (h3 ? a4[j + 2] : a4[j]) + __shfl_xor_sync(0xffffffffu, h3 ? a4[j] : a4[j + 2], 8);
+      float v = (h2 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? a2[0] : a2[1], 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      const int row = lane >> 2;
+      if ((lane & 3) == 0 && row < nr) ws.logit_part[((size_t)sl * p.rows + r0 + row) * p.E + e] = v;
     }
+    __syncthreads();  // the next block's staging reuses xs
   }
-  __syncthreads();
 
   // this CTA's share of the MoE input's quantization, before it arrives (the
   // pooler resets max |x| for the next layer once every CTA has arrived)
   quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
+  // beyond one block of rows, route_kernel routes the blocks in parallel
+  if (nrb > 1) return;
 
-  // the last CTA of this row group routes its rows; the last group to finish
-  // builds the pooler over every row
+  // one block of rows: the last CTA to finish routes them and builds the pooler
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned old = atomicAdd(ws.rg_count + rg, 1u);
+    const unsigned old = atomicAdd(ws.rg_count, 1u);
     s_last = (old == gridDim.x * gridDim.y - 1u);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   const RouteSmem rs = route_carve(p, smem);
+  route_rows(p, rs, 0, p.rows);
+  __syncthreads();
+  if (threadIdx.x == 0) ws.rg_count[0] = 0u;  // every CTA has arrived
+  if (p.rows * p.k <= kRouterThreads)
+    pool_small(p, smem, true);
+  else
+    pool_all(p, smem, true);
+}
+
+// Beyond one block of rows: after the router's dot products (programmatic
+// dependent launch), one CTA per block of 8 rows routes them, a warp per row;
+// the last CTA to finish builds the pooler over every row.
+__global__ void __launch_bounds__(kRouterThreads, 1) route_kernel(RouterParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+  grid_dep_wait();  // every block's logit partials
+  grid_dep_launch();
+  const int r0 = blockIdx.x * kRowBlock, nr = min(kRowBlock, p.rows - r0);
+  const RouteSmem rs = route_carve(p, smem);
   route_rows(p, rs, r0, nr);
   __syncthreads();
-  if (threadIdx.x == 0) ws.rg_count[rg] = 0u;  // every CTA of the block has arrived
-  if (gridDim.z > 1) {  // with one row block this CTA is already the last
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const unsigned old = atomicAdd(ws.counters, 1u);
-      s_last = (old == gridDim.z - 1u);
-    }
-    __syncthreads();
-    if (!s_last) return;
+  if (threadIdx.x == 0) {
     __threadfence();
+    const unsigned old = atomicAdd(p.ws.counters, 1u);
+    s_last = (old == gridDim.x - 1u);
   }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
   if (p.rows * p.k <= kRouterThreads)
-    pool_small(p, smem, gridDim.z == 1);
+    pool_small(p, smem, false);
   else
-    pool_all(p, smem, gridDim.z == 1);
+    pool_all(p, smem, false);
 }
 
 }  // namespace
@@ -598,7 +637,7 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   const size_t smem = router_smem_bytes(p.E, p.rows);
   static_assert(kMaxTopK <= 32, "one lane per selected expert");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_eg, p.S, (p.rows + kRowBlock - 1) / kRowBlock);
+  cfg.gridDim = dim3(p.n_eg, p.S, 1);
   cfg.blockDim = dim3(kRouterThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -607,12 +646,18 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, router_kernel, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, router_kernel, p);
+  const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
+  if (e != cudaSuccess || nrb == 1) return e;
+  cfg.gridDim = dim3(nrb, 1, 1);
+  return cudaLaunchKernelEx(&cfg, route_kernel, p);
 }
 
 cudaError_t router_set_smem(size_t bytes) {
-  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)bytes);
+  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return e;
 }
 
 }  // namespace moe
