@@ -19,6 +19,7 @@
 // top-k (one warp per row); the last row block to finish builds the pooler's
 // arrays over every row.
 #include "common.cuh"
+#include "gemv.cuh"
 
 namespace moe {
 namespace {
@@ -597,6 +598,76 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
     pool_all(p, smem, true);
 }
 
+// Beyond one block of rows the router's dot products are a GEMM (rows x E x H),
+// on the tensor cores: a CTA takes 16 experts and one of the S K-slices,
+// each of its 8 warps an eighth of the slice.  A warp keeps its 16 experts'
+// weights as mma.sync A fragments in registers for the whole launch (read
+// before the dependency wait), and per block of 8 rows loads that block's x
+// (the next block's loads in flight meanwhile) as B fragments, with the K
+// order permuted as in the streaming projections so each thread's pieces are
+// contiguous 16-byte runs; the 8 warps' 16 x 8 tiles are summed in warp order
+// through shared memory into the slice's partial logits.  Needs H / S a
+// multiple of 256 (a warp's columns in 32-column blocks, at most 4).
+__global__ void __launch_bounds__(kRouterThreads, 1) router_mma_kernel(RouterParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const Workspace& ws = p.ws;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  const int e0 = blockIdx.x * 16, sl = blockIdx.y;
+  const int W = p.H / p.S, CB = W / 256;
+  const int k0 = sl * W + warp * (W / 8) + t * 8;
+  uint4 a[2][4];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int e = e0 + g + 8 * hr;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      a[hr][c] = (c < CB && e < p.E) ? __ldg(reinterpret_cast<const uint4*>(p.wr + (size_t)e * p.H + k0 + c * 32))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  float* red = reinterpret_cast<float*>(smem);  // [8 warps][16 experts x 8 rows]
+  const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
+  uint4 bn[4];
+  auto load_x = [&](int rb) {
+    const int row = rb * kRowBlock + g;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      bn[c] = (c < CB && row < p.rows) ? __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)row * p.H + k0 + c * 32))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+  };
+  load_x(0);
+  for (int rb = 0; rb < nrb; ++rb) {
+    uint4 b[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) b[c] = bn[c];
+    if (rb + 1 < nrb) load_x(rb + 1);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c < CB) {
+        mma_16816_bf16(acc, a[0][c].x, a[1][c].x, a[0][c].y, a[1][c].y, b[c].x, b[c].y);
+        mma_16816_bf16(acc, a[0][c].z, a[1][c].z, a[0][c].w, a[1][c].w, b[c].z, b[c].w);
+      }
+    // acc: (expert g, rows 2t, 2t + 1), (expert g + 8, rows 2t, 2t + 1)
+    float* mine = red + warp * 128;
+    mine[g * 8 + 2 * t] = acc[0];
+    mine[g * 8 + 2 * t + 1] = acc[1];
+    mine[(g + 8) * 8 + 2 * t] = acc[2];
+    mine[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kRouterWarps; ++w) v += red[w * 128 + threadIdx.x];
+      const int e = e0 + (threadIdx.x >> 3), r = rb * kRowBlock + (threadIdx.x & 7);
+      if (e < p.E && r < p.rows) ws.logit_part[((size_t)sl * p.rows + r) * p.E + e] = v;
+    }
+    __syncthreads();
+  }
+  quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
+}
+
 // Beyond one block of rows: after the router's dot products (programmatic
 // dependent launch), one CTA per block of 8 rows routes them, a warp per row;
 // the last CTA to finish builds the pooler over every row.
@@ -646,8 +717,10 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, router_kernel, p);
   const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
+  const bool mma = nrb > 1 && p.H % (p.S * 256) == 0 && p.H / p.S <= 1024;
+  if (mma) cfg.gridDim = dim3((p.E + 15) / 16, p.S, 1);
+  cudaError_t e = mma ? cudaLaunchKernelEx(&cfg, router_mma_kernel, p) : cudaLaunchKernelEx(&cfg, router_kernel, p);
   if (e != cudaSuccess || nrb == 1) return e;
   cfg.gridDim = dim3(nrb, 1, 1);
   return cudaLaunchKernelEx(&cfg, route_kernel, p);
@@ -655,6 +728,8 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
 
 cudaError_t router_set_smem(size_t bytes) {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(router_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   return e;
