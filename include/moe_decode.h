@@ -205,7 +205,10 @@ int moe_decode_last_error(moe_decode_t* h);
 /* Bytes of device workspace the handle holds. */
 size_t moe_decode_workspace_bytes(const moe_decode_t* h);
 
-/* Number of kernels one moe_decode_step of max_rows rows launches. */
+/* Number of kernels one moe_decode_step of max_rows rows launches: per layer
+ * the boundary, the router and the experts, plus the routing kernel beyond 8
+ * rows and the pooler gather beyond 32 (the CUDA-core build: gate/up and
+ * down instead of the experts, no gather); one final boundary per step. */
 int moe_decode_step_kernel_count(const moe_decode_t* h);
 
 void moe_decode_destroy(moe_decode_t* h);
