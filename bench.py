@@ -542,19 +542,14 @@ def run_dense(args, w):
     dn_gbs = byt["down"] / (k_ms[3] * 1e-3) / 1e9
     step_gbs = byt["total"] / (ms * 1e-3) / 1e9 * ws
 
-    # end to end: pinned host inputs copied in, the layer, the stream copied out
+    # end to end through moe_dense_layer_host: the attention output and the
+    # stream in from page-locked host memory, the stream back out
     s_h, a_h = synth.step_inputs(w)
     sh = torch.from_numpy(s_h).pin_memory()
     ah = torch.from_numpy(a_h.view(np.int16)).view(torch.bfloat16).pin_memory()
-    oh = torch.empty_like(sh).pin_memory()
-    sd, ad = torch.empty_like(sh, device=device), torch.empty_like(ah, device=device)
 
     def host_step():
-        sd.copy_(sh, non_blocking=True)
-        ad.copy_(ah, non_blocking=True)
-        dl.layer(rows, ad, sd)
-        oh.copy_(sd, non_blocking=True)
-        torch.cuda.synchronize(device)
+        dl.layer_host(rows, ah, sh)
 
     for _ in range(3):
         host_step()
@@ -694,23 +689,17 @@ def run_ctxkv(args, w):
     gemm_gbs = byt["gemm"] / (k_ms[1] * 1e-3) / 1e9
     step_gbs = byt["total"] / (ms * 1e-3) / 1e9 * ws
 
-    # end to end: pinned context, positions and slots in; the keys and values out
+    # end to end through moe_ctxkv_project_host: context, positions and slots
+    # in from page-locked host memory, the keys and values out (the caches are
+    # device memory)
     ctx_h, pos_h, slots_h = synth.ctxkv_inputs(w)
     ch = torch.from_numpy(ctx_h.view(np.int16)).view(torch.bfloat16).pin_memory()
     ph, sh = torch.from_numpy(pos_h).pin_memory(), torch.from_numpy(slots_h).pin_memory()
     kh = torch.empty(L, n, KVH, D, dtype=torch.bfloat16).pin_memory()
     vh = torch.empty_like(kh).pin_memory()
-    cd, pd, sd = (torch.empty_like(t, device=device) for t in (ch, ph, sh))
-    kd, vd = torch.empty_like(kh, device=device), torch.empty_like(vh, device=device)
 
     def host_step():
-        cd.copy_(ch, non_blocking=True)
-        pd.copy_(ph, non_blocking=True)
-        sd.copy_(sh, non_blocking=True)
-        op.project(n, cd, pd, sd, kc, vc, k_out=kd, v_out=vd)
-        kh.copy_(kd, non_blocking=True)
-        vh.copy_(vd, non_blocking=True)
-        torch.cuda.synchronize(device)
+        op.project_host(n, ch, ph, kh, vh, slots=sh, k_cache=kc, v_cache=vc)
 
     for _ in range(3):
         host_step()

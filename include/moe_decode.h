@@ -308,6 +308,15 @@ int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, 
 /* Workspace pointers of the last layer call (see moe_dense_debug_view). */
 int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
 
+/* moe_dense_layer on HOST buffers: attn_host bf16 [rows][H] in, stream_host
+ * fp32 [rows][H] in/out; synchronizes cuda_stream.  Page-locked buffers that
+ * the runtime maps into the device's address space (attn 8-byte, stream
+ * 16-byte aligned) are read and written by the first and last boundaries
+ * themselves, the layer replayed from a graph cached per (rows, buffers);
+ * other buffers are copied in and out around the layer. */
+int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, float* stream_host,
+                         void* cuda_stream);
+
 /* Kernels one moe_dense_layer call of `rows` rows launches: four of the
  * library's own on the streamed path, else its three and the cuBLAS GEMMs'
  * (whose count cuBLAS chooses per shape).
@@ -381,6 +390,17 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
 int moe_ctxkv_project(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
                       const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
                       int64_t n_slots, uint16_t* k_out, uint16_t* v_out, void* cuda_stream);
+
+/* moe_ctxkv_project on HOST buffers for the context, positions, slot map and
+ * the keys and values out (k_out_host, v_out_host bf16 [L][n_ctx][KVH][D],
+ * required); the caches stay device memory.  Synchronizes cuda_stream.  When
+ * every given host buffer is page-locked and mapped into the device's
+ * address space, the kernels read and write them directly; otherwise they
+ * are copied in and out (a slot map of at most n_layers * max_ctx entries). */
+int moe_ctxkv_project_host(moe_ctxkv_t* h, int n_ctx, const uint16_t* context_host,
+                           const int64_t* positions_host, const int64_t* slots_host, int slot_stride,
+                           uint16_t* k_cache, uint16_t* v_cache, int64_t n_slots, uint16_t* k_out_host,
+                           uint16_t* v_out_host, void* cuda_stream);
 
 /* The same projection with CUDA events around its three launches (norms,
  * projection, key norm + rotation + cache write); synchronizes and writes

@@ -26,8 +26,8 @@ EXPORTS = (
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
-    "moe_dense_kernel_count", "moe_dense_destroy",
-    "moe_ctxkv_create", "moe_ctxkv_project", "moe_ctxkv_profile", "moe_ctxkv_debug",
+    "moe_dense_layer_host", "moe_dense_kernel_count", "moe_dense_destroy",
+    "moe_ctxkv_create", "moe_ctxkv_project", "moe_ctxkv_project_host", "moe_ctxkv_profile", "moe_ctxkv_debug",
     "moe_ctxkv_last_error", "moe_ctxkv_kernel_count", "moe_ctxkv_destroy",
 )
 
@@ -119,11 +119,13 @@ def _lib():
             "moe_dense_layer": (i32, [vp, i32, vp, vp, vp]),
             "moe_dense_layer_profile": (i32, [vp, i32, vp, vp, vp, vp]),
             "moe_dense_debug": (i32, [vp, ctypes.POINTER(DenseDebugView)]),
+            "moe_dense_layer_host": (i32, [vp, i32, vp, vp, vp]),
             "moe_dense_kernel_count": (i32, [vp, i32]),
             "moe_dense_destroy": (None, [vp]),
             "moe_ctxkv_create": (i32, [ctypes.POINTER(CtxKvDims), ctypes.POINTER(CtxKvWeights),
                                        ctypes.POINTER(vp)]),
             "moe_ctxkv_project": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp, vp]),
+            "moe_ctxkv_project_host": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp, vp]),
             "moe_ctxkv_profile": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp]),
             "moe_ctxkv_debug": (i32, [vp, ctypes.POINTER(CtxKvDebugView)]),
             "moe_ctxkv_last_error": (i32, [vp]),
@@ -346,6 +348,11 @@ class DenseLayer:
         _check(_lib().moe_dense_layer(self.handle, rows, _ptr(attn_out), _ptr(stream_buf),
                                       _stream(stream)), "moe_dense_layer")
 
+    def layer_host(self, rows, attn_host, stream_host, stream=None):
+        """The layer on host tensors (page-locked for the fastest path)."""
+        _check(_lib().moe_dense_layer_host(self.handle, rows, _ptr(attn_host), _ptr(stream_host),
+                                           _stream(stream)), "moe_dense_layer_host")
+
     def layer_profile(self, rows, attn_out, stream_buf, stream=None):
         ms = (ctypes.c_float * 5)()
         _check(_lib().moe_dense_layer_profile(self.handle, rows, _ptr(attn_out), _ptr(stream_buf),
@@ -404,6 +411,15 @@ class ContextKV:
         _check(_lib().moe_ctxkv_project(self.handle, n_ctx, _ptr(context), _ptr(positions), sp, stride,
                                         kc, vc, n_slots, _ptr(k_out), _ptr(v_out), _stream(stream)),
                "moe_ctxkv_project")
+
+    def project_host(self, n_ctx, context, positions, k_out, v_out, slots=None, k_cache=None, v_cache=None,
+                     stream=None):
+        """The projection with host tensors for the context, positions, slots and
+        outputs (page-locked for the fastest path); the caches are device tensors."""
+        sp, stride, kc, vc, n_slots = self._slot_args(slots, k_cache, v_cache)
+        _check(_lib().moe_ctxkv_project_host(self.handle, n_ctx, _ptr(context), _ptr(positions), sp, stride,
+                                             kc, vc, n_slots, _ptr(k_out), _ptr(v_out), _stream(stream)),
+               "moe_ctxkv_project_host")
 
     def profile(self, n_ctx, context, positions, slots=None, k_cache=None, v_cache=None, stream=None):
         sp, stride, kc, vc, n_slots = self._slot_args(slots, k_cache, v_cache)

@@ -261,6 +261,8 @@ struct moe_ctxkv_s {
   float* part;                      // split-K partials [S][L][8][2 * KVH * D], or null
   int splits;                       // K-splits of the streaming projection; 0: none
   int num_sms;
+  uint8_t* io;                      // host-buffer calls' copies: context [n][H] bf16,
+                                    // positions [n], slots [L][n] int64 (when not mapped)
 };
 
 namespace {
@@ -472,7 +474,8 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   auto up16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
   const size_t b_fc = up16(2 * n * H), b_u = up16(2 * L * n * H), b_kv = up16(2 * L * n * 2 * KD),
                b_k = up16(2 * L * n * KD), b_cs = table * sizeof(float2);
-  const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
+  const size_t b_io = up16(2 * n * H) + up16(8 * n) + up16(8 * L * n);
+  const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16 + b_io;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kCtxBlasWorkspace);
@@ -491,6 +494,7 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   h->v = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u + b_kv + b_k);
   h->cs = table ? reinterpret_cast<float2*>(base + b_fc + b_u + b_kv + 2 * b_k) : nullptr;
   h->err = reinterpret_cast<unsigned*>(base + b_fc + b_u + b_kv + 2 * b_k + b_cs);
+  h->io = base + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
   e = cudaMemset(h->err, 0, sizeof(unsigned));
   if (e == cudaSuccess && table) {
     // cos / sin of pos * theta^(-2j/D) in fp64, stored as fp32
@@ -528,6 +532,68 @@ int moe_ctxkv_project(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const 
   int rc = check_project(h, a);
   if (rc) return rc;
   return ctxkv_enqueue(h, a, static_cast<cudaStream_t>(cuda_stream), nullptr);
+}
+
+int moe_ctxkv_project_host(moe_ctxkv_t* h, int n_ctx, const uint16_t* context_host,
+                           const int64_t* positions_host, const int64_t* slots_host, int slot_stride,
+                           uint16_t* k_cache, uint16_t* v_cache, int64_t n_slots, uint16_t* k_out_host,
+                           uint16_t* v_out_host, void* cuda_stream) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  if (!context_host || !k_out_host || !v_out_host)
+    return moe::api_fail(MOE_EINVAL, "context_host, k_out_host and v_out_host are required");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const moe_ctxkv_dims& d = h->d;
+  const int n = n_ctx;
+  if (n < 1 || n > d.max_ctx) return moe::api_fail(MOE_EINVAL, "n_ctx outside [1, max_ctx]");
+  const size_t kv_bytes = (size_t)d.n_layers * n * d.n_kv_heads * d.head_dim * 2;
+  const size_t slot_count = slots_host ? (size_t)(slot_stride ? d.n_layers : 1) * (slot_stride ? slot_stride : n) : 0;
+  // mapped page-locked buffers are read and written by the kernels directly
+  auto mapped = [](const void* p) -> void* {
+    cudaPointerAttributes a{};
+    if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+  };
+  const uint16_t* ctx_d = static_cast<const uint16_t*>(mapped(context_host));
+  const int64_t* pos_d = static_cast<const int64_t*>(mapped(positions_host));
+  const int64_t* slots_d = static_cast<const int64_t*>(mapped(slots_host));
+  uint16_t* k_d = static_cast<uint16_t*>(mapped(k_out_host));
+  uint16_t* v_d = static_cast<uint16_t*>(mapped(v_out_host));
+  const bool direct = ctx_d && k_d && v_d && (!positions_host || pos_d) && (!slots_host || slots_d);
+  cudaError_t e = cudaSuccess;
+  if (!direct) {
+    // copies in: context, positions, slots into the handle's buffers
+    uint8_t* io = h->io;
+    const size_t b_ctx = ((size_t)2 * d.max_ctx * d.hidden + 15) & ~(size_t)15;
+    const size_t b_pos = ((size_t)8 * d.max_ctx + 15) & ~(size_t)15;
+    if ((size_t)slot_count > (size_t)d.n_layers * d.max_ctx)
+      return moe::api_fail(MOE_EINVAL, "slot map larger than n_layers * max_ctx");
+    ctx_d = reinterpret_cast<const uint16_t*>(io);
+    pos_d = positions_host ? reinterpret_cast<const int64_t*>(io + b_ctx) : nullptr;
+    slots_d = slots_host ? reinterpret_cast<const int64_t*>(io + b_ctx + b_pos) : nullptr;
+    e = cudaMemcpyAsync(io, context_host, (size_t)n * d.hidden * 2, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && positions_host)
+      e = cudaMemcpyAsync(io + b_ctx, positions_host, (size_t)n * 8, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && slots_host)
+      e = cudaMemcpyAsync(io + b_ctx + b_pos, slots_host, slot_count * 8, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return ck_cuda(e, "input copy");
+    k_d = nullptr;  // the workspace's keys and values, copied out below
+    v_d = nullptr;
+  }
+  const ProjectArgs a{n, ctx_d, pos_d, slots_d, slot_stride, k_cache, v_cache, n_slots, k_d, v_d};
+  int rc = check_project(h, a);
+  if (rc) return rc;
+  rc = ctxkv_enqueue(h, a, s, nullptr);
+  if (rc) return rc;
+  if (!direct) {
+    e = cudaMemcpyAsync(k_out_host, h->k, kv_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(v_out_host, h->v, kv_bytes, cudaMemcpyDeviceToHost, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return ck_cuda(e, "host-buffer projection");
+  return MOE_OK;
 }
 
 int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,

@@ -61,6 +61,15 @@ struct moe_dense_s {
   size_t blas_ws_bytes;
   __nv_bfloat16 *x, *gu, *a, *f;  // [R][H], [R][2I], [R][I], [R][H]
   float* part;                     // down projection's split-K partials [S][8][H], or null
+  float* io_stream;                // [R][H] the stream of a host-buffer call
+  __nv_bfloat16* io_attn;          // [R][H] its attention output (when copied in)
+  struct HostGraph {
+    int rows;
+    const void* attn;
+    const void* stream;
+    cudaGraphExec_t exec;
+  };
+  std::vector<HostGraph> host_graphs;
   int down_splits;                 // K-splits of the streamed down projection; 0: no streaming
   int num_sms;
 };
@@ -70,6 +79,16 @@ namespace {
 constexpr size_t kBlasWorkspace = 8u << 20;
 
 bool dense_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The device address of mapped page-locked host memory p, or null.
+void* dense_host_mapped(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 
 int blas_fail(cublasStatus_t st, const char* what) {
   char buf[160];
@@ -85,8 +104,10 @@ int cuda_err(cudaError_t e, const char* what) {
 
 // The dense layer's launches on s; with ev, an event before each and after
 // the last (boundary, gate/up, SiLU * mul, down, boundary).
+// stream_in: where the first boundary reads the stream (null: stream itself);
+// aux: where the output boundary also writes the new stream (or null).
 int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
-                  cudaStream_t s, cudaEvent_t* ev) {
+                  cudaStream_t s, cudaEvent_t* ev, const float* stream_in = nullptr, float* aux = nullptr) {
   const moe_dense_dims& d = h->d;
   auto mark = [&](int i) {
     if (ev) cudaEventRecord(ev[i], s);
@@ -100,6 +121,7 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
   bp.eps = d.eps;
   bp.branch = reinterpret_cast<const __nv_bfloat16*>(attn_out);
   bp.stream = stream;
+  bp.stream_in = stream_in;
   bp.w_post = h->w.w_post_attn;
   bp.w_pre = h->w.w_pre_ffn;
   bp.x_out = h->x;
@@ -160,6 +182,8 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
     bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
     bp.x_out = nullptr;
     bp.round_norm = 0;
+    bp.stream_in = nullptr;
+    bp.aux = aux;
     e = moe::launch_boundary(bp, h->cluster, s, !ev);
     if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
     mark(5);
@@ -190,6 +214,8 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
   bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
   bp.x_out = nullptr;
   bp.round_norm = 0;
+  bp.stream_in = nullptr;
+  bp.aux = aux;
   e = moe::launch_boundary(bp, h->cluster, s, false);
   if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
   mark(5);
@@ -256,7 +282,7 @@ int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe
   }
   const size_t R = (size_t)d.max_rows, H = (size_t)d.hidden, I = (size_t)d.inter;
   const size_t part_bytes = h->down_splits ? (size_t)h->down_splits * 8 * H * sizeof(float) : 0;
-  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H) + part_bytes;
+  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H) + part_bytes + R * H * (4 + 2);
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kBlasWorkspace);
@@ -271,6 +297,8 @@ int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe
   h->a = h->gu + R * 2 * I;
   h->f = h->a + R * I;
   h->part = h->down_splits ? reinterpret_cast<float*>(h->f + R * H) : nullptr;
+  h->io_stream = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(h->f + R * H) + part_bytes);
+  h->io_attn = reinterpret_cast<__nv_bfloat16*>(h->io_stream + R * H);
   cublasStatus_t st = cublasCreate(&h->blas);
   if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, h->blas_ws_bytes);
   if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);
@@ -290,6 +318,57 @@ int moe_dense_layer(moe_dense_t* h, int rows, const uint16_t* attn_out, float* s
   if (!attn_out || !stream || !dense_aligned(attn_out, 8) || !dense_aligned(stream, 16))
     return moe::api_fail(MOE_EINVAL, "attn_out (8-byte) and stream (16-byte) must be aligned device pointers");
   return dense_enqueue(h, rows, attn_out, stream, static_cast<cudaStream_t>(cuda_stream), nullptr);
+}
+
+int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, float* stream_host,
+                         void* cuda_stream) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  int rc = check_rows_dense(h, rows);
+  if (rc) return rc;
+  if (!attn_host || !stream_host) return moe::api_fail(MOE_EINVAL, "attn_host and stream_host are required");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const size_t n = (size_t)rows * h->d.hidden;
+  const uint16_t* attn_d = static_cast<const uint16_t*>(dense_host_mapped(attn_host));
+  float* stream_d = static_cast<float*>(dense_host_mapped(stream_host));
+  cudaError_t e = cudaSuccess;
+  if (attn_d && stream_d && dense_aligned(attn_d, 8) && dense_aligned(stream_d, 16)) {
+    // mapped page-locked buffers: the boundaries read and write host memory
+    // themselves; the layer is one cached graph per (rows, buffers)
+    cudaGraphExec_t exec = nullptr;
+    for (const auto& g : h->host_graphs)
+      if (g.rows == rows && g.attn == attn_host && g.stream == stream_host) exec = g.exec;
+    if (!exec) {
+      cudaStream_t c = nullptr;
+      e = cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking);
+      if (e != cudaSuccess) return cuda_err(e, "stream create");
+      cudaGraph_t graph = nullptr;
+      e = cudaStreamBeginCapture(c, cudaStreamCaptureModeThreadLocal);
+      if (e == cudaSuccess) {
+        rc = dense_enqueue(h, rows, attn_d, h->io_stream, c, nullptr, stream_d, stream_d);
+        e = cudaStreamEndCapture(c, &graph);
+      }
+      cudaStreamDestroy(c);
+      if (rc || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc ? rc : cuda_err(e, "host-buffer layer capture");
+      }
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return cuda_err(e, "graph instantiate");
+      h->host_graphs.push_back({rows, attn_host, stream_host, exec});
+    }
+    e = cudaGraphLaunch(exec, s);
+  } else {
+    e = cudaMemcpyAsync(h->io_attn, attn_host, n * 2, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->io_stream, stream_host, n * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_err(e, "input copy");
+    rc = dense_enqueue(h, rows, reinterpret_cast<const uint16_t*>(h->io_attn), h->io_stream, s, nullptr);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(stream_host, h->io_stream, n * 4, cudaMemcpyDeviceToHost, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_err(e, "host-buffer layer");
+  return MOE_OK;
 }
 
 int moe_dense_layer_profile(moe_dense_t* h, int rows, const uint16_t* attn_out, float* stream,
@@ -361,6 +440,7 @@ int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* v) {
 
 void moe_dense_destroy(moe_dense_t* h) {
   if (!h) return;
+  for (const auto& g : h->host_graphs) cudaGraphExecDestroy(g.exec);
   if (h->blas) cublasDestroy(h->blas);
   cudaFree(h->blas_ws);
   cudaFree(h->x);

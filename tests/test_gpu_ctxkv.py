@@ -240,3 +240,38 @@ def test_graph_replays_bitwise():
         case.op.check()
     finally:
         case.close()
+
+
+def test_host_buffers_match_the_device_call():
+    """moe_ctxkv_project_host: page-locked buffers (read and written by the
+    kernels) and pageable ones (copied) give the device call's keys, values and
+    caches bit for bit."""
+    case = _Case(SMALL, max_ctx=8)
+    try:
+        w = SMALL
+        L, KVH, D = w.n_layers, w.n_kv_heads, w.head_dim
+        ctx, pos, slots = synth.ctxkv_inputs(w, 5)
+        kc0, vc0 = case.caches(5)
+        kc, vc = _bf16_dev(kc0), _bf16_dev(vc0)
+        k_dev = torch.empty(L, 8, KVH, D, dtype=torch.bfloat16, device="cuda")
+        v_dev = torch.empty_like(k_dev)
+        case.op.project(8, _bf16_dev(ctx), torch.from_numpy(pos).cuda(), torch.from_numpy(slots).cuda(), kc, vc,
+                        k_out=k_dev, v_out=v_dev)
+        torch.cuda.synchronize()
+        want = [t.view(torch.int16).cpu().numpy() for t in (k_dev, v_dev, kc, vc)]
+        for pinned in (True, False):
+            c_h = torch.from_numpy(ctx.view(np.int16).copy()).view(torch.bfloat16)
+            p_h, s_h = torch.from_numpy(pos.copy()), torch.from_numpy(slots.copy())
+            k_h = torch.empty(L, 8, KVH, D, dtype=torch.bfloat16)
+            v_h = torch.empty_like(k_h)
+            if pinned:
+                c_h, p_h, s_h, k_h, v_h = (t.pin_memory() for t in (c_h, p_h, s_h, k_h, v_h))
+            kc2, vc2 = _bf16_dev(kc0), _bf16_dev(vc0)
+            case.op.project_host(8, c_h, p_h, k_h, v_h, slots=s_h, k_cache=kc2, v_cache=vc2)
+            got = [k_h.view(torch.int16).numpy(), v_h.view(torch.int16).numpy(),
+                   kc2.view(torch.int16).cpu().numpy(), vc2.view(torch.int16).cpu().numpy()]
+            for g_, w_, what in zip(got, want, ("keys", "values", "key cache", "value cache")):
+                assert np.array_equal(g_, w_), f"{what} differ ({'page-locked' if pinned else 'pageable'})"
+        case.op.check()
+    finally:
+        case.close()

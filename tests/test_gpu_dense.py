@@ -194,3 +194,27 @@ def test_dense_layer_profile_and_row_limits():
                 case.layer.layer(rows, a_t, s_t)
     finally:
         case.close()
+
+
+@pytest.mark.parametrize("hidden,inter", [(256, 384), (1152, 520)])
+def test_dense_layer_host_buffers_match_the_device_call(hidden, inter):
+    """moe_dense_layer_host: page-locked buffers (read and written by the
+    kernels, twice: captured, then replayed) and pageable ones (copied) give
+    the device call's stream bit for bit."""
+    case = _Case(_shape(SMALL, hidden, inter), max_rows=8)
+    try:
+        stream, attn = synth.step_inputs(case.w.with_rows(8), 4)
+        s_dev = torch.from_numpy(stream).cuda()
+        case.layer.layer(8, _bf16_dev(attn), s_dev)
+        want = s_dev.cpu().numpy()
+        a_pin = torch.from_numpy(attn.view(np.int16)).view(torch.bfloat16).pin_memory()
+        s_pin = torch.from_numpy(stream).pin_memory()
+        for _ in range(2):
+            s_pin.copy_(torch.from_numpy(stream))
+            case.layer.layer_host(8, a_pin, s_pin)
+            assert np.array_equal(s_pin.numpy(), want)
+        s_page = torch.from_numpy(stream.copy())
+        case.layer.layer_host(8, torch.from_numpy(attn.view(np.int16).copy()).view(torch.bfloat16), s_page)
+        assert np.array_equal(s_page.numpy(), want)
+    finally:
+        case.close()
