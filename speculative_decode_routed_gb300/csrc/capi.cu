@@ -67,16 +67,7 @@ bool host_pinned(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
-// The address at which the current device may access pinned host memory p
-// (mapped into its address space), or null: the runtime reports none.
-void* host_mapped(const void* p) {
-  cudaPointerAttributes a{};
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
-}
+
 
 struct GraphEntry {
   int rows;
@@ -92,6 +83,16 @@ namespace moe {
 // Records the reason of a failing call for moe_decode_error_message (entry
 // points defined outside this file).
 int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
+void* host_mapped(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // pageable memory may report an error on older drivers
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 }  // namespace moe
 
 struct moe_decode_s {
@@ -774,9 +775,9 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
       // stream from host memory and the final boundary writes the output and
       // the stream back there, so the kernels make the copies themselves;
       // otherwise copy-engine copies around the step
-      const uint16_t* branch_d = static_cast<const uint16_t*>(host_mapped(branch_host));
-      float* stream_d = static_cast<float*>(host_mapped(stream_host));
-      uint16_t* out_d = static_cast<uint16_t*>(host_mapped(out_host));
+      const uint16_t* branch_d = static_cast<const uint16_t*>(moe::host_mapped(branch_host));
+      float* stream_d = static_cast<float*>(moe::host_mapped(stream_host));
+      uint16_t* out_d = static_cast<uint16_t*>(moe::host_mapped(out_host));
       const bool direct = branch_d && stream_d && out_d && aligned(stream_d, 16) && aligned(branch_d, 8) &&
                           aligned(out_d, 8);
       cudaError_t e = cudaStreamBeginCapture(c, cudaStreamCaptureModeThreadLocal);

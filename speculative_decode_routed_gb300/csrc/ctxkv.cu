@@ -548,19 +548,11 @@ int moe_ctxkv_project_host(moe_ctxkv_t* h, int n_ctx, const uint16_t* context_ho
   const size_t kv_bytes = (size_t)d.n_layers * n * d.n_kv_heads * d.head_dim * 2;
   const size_t slot_count = slots_host ? (size_t)(slot_stride ? d.n_layers : 1) * (slot_stride ? slot_stride : n) : 0;
   // mapped page-locked buffers are read and written by the kernels directly
-  auto mapped = [](const void* p) -> void* {
-    cudaPointerAttributes a{};
-    if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
-  };
-  const uint16_t* ctx_d = static_cast<const uint16_t*>(mapped(context_host));
-  const int64_t* pos_d = static_cast<const int64_t*>(mapped(positions_host));
-  const int64_t* slots_d = static_cast<const int64_t*>(mapped(slots_host));
-  uint16_t* k_d = static_cast<uint16_t*>(mapped(k_out_host));
-  uint16_t* v_d = static_cast<uint16_t*>(mapped(v_out_host));
+  const uint16_t* ctx_d = static_cast<const uint16_t*>(moe::host_mapped(context_host));
+  const int64_t* pos_d = static_cast<const int64_t*>(moe::host_mapped(positions_host));
+  const int64_t* slots_d = static_cast<const int64_t*>(moe::host_mapped(slots_host));
+  uint16_t* k_d = static_cast<uint16_t*>(moe::host_mapped(k_out_host));
+  uint16_t* v_d = static_cast<uint16_t*>(moe::host_mapped(v_out_host));
   const bool direct = ctx_d && k_d && v_d && (!positions_host || pos_d) && (!slots_host || slots_d);
   cudaError_t e = cudaSuccess;
   if (!direct) {

@@ -80,15 +80,6 @@ constexpr size_t kBlasWorkspace = 8u << 20;
 
 bool dense_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The device address of mapped page-locked host memory p, or null.
-void* dense_host_mapped(const void* p) {
-  cudaPointerAttributes a{};
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
-}
 
 int blas_fail(cublasStatus_t st, const char* what) {
   char buf[160];
@@ -328,8 +319,8 @@ int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, fl
   if (!attn_host || !stream_host) return moe::api_fail(MOE_EINVAL, "attn_host and stream_host are required");
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const size_t n = (size_t)rows * h->d.hidden;
-  const uint16_t* attn_d = static_cast<const uint16_t*>(dense_host_mapped(attn_host));
-  float* stream_d = static_cast<float*>(dense_host_mapped(stream_host));
+  const uint16_t* attn_d = static_cast<const uint16_t*>(moe::host_mapped(attn_host));
+  float* stream_d = static_cast<float*>(moe::host_mapped(stream_host));
   cudaError_t e = cudaSuccess;
   if (attn_d && stream_d && dense_aligned(attn_d, 8) && dense_aligned(stream_d, 16)) {
     // mapped page-locked buffers: the boundaries read and write host memory

@@ -149,6 +149,10 @@ cudaError_t launch_nvfp4_encode(const float* v, int64_t nblocks, uint8_t* codes,
                                 const unsigned* amax, float* sg, cudaStream_t s);
 // Sets the calling thread's moe_decode_error_message; returns code.
 int api_fail(int code, const char* msg);
+// The address at which the current device may access page-locked host
+// memory p (mapped into its address space), or null: the runtime reports
+// none, p is not page-locked, or p is null.
+void* host_mapped(const void* p);
 
 size_t expert_smem_bytes(const ExpertParams& p);
 size_t expert_ctrl_bytes();

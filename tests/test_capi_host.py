@@ -120,6 +120,7 @@ def test_dense_invalid_arguments():
     assert L.moe_dense_layer_profile(None, 1, None, None, None, ms) == moe.MOE_EINVAL
     assert L.moe_dense_debug(None, None) == moe.MOE_EINVAL
     assert L.moe_dense_kernel_count(None, 1) == moe.MOE_EINVAL
+    assert L.moe_dense_layer_host(None, 1, None, None, None) == moe.MOE_EINVAL
     L.moe_dense_destroy(None)
 
 
@@ -168,4 +169,5 @@ def test_ctxkv_invalid_arguments():
     assert L.moe_ctxkv_debug(None, None) == moe.MOE_EINVAL
     assert L.moe_ctxkv_last_error(None) == moe.MOE_EINVAL
     assert L.moe_ctxkv_kernel_count(None, 1) == moe.MOE_EINVAL
+    assert L.moe_ctxkv_project_host(None, 1, None, None, None, 0, None, None, 0, None, None, None) == moe.MOE_EINVAL
     L.moe_ctxkv_destroy(None)
