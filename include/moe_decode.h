@@ -127,7 +127,13 @@ typedef struct {
 /* Validates the shapes, the device and every pointer, plans the kernels and
  * allocates the workspace.  `layers` points to dims->n_layers entries (copied).
  * w_post_final / w_final: [H] norm weights of the final boundary (may be
- * NULL if moe_decode_final / _step are never called). */
+ * NULL if moe_decode_final / _step are never called).  The tensor-core build
+ * also keeps, per layer, the weight scales rearranged for the tensor cores
+ * (1/8 of the code bytes) and, when the device memory is there, a copy of
+ * the expert codes in 16 KB tiles (as many bytes as the codes), which the
+ * experts kernel then streams instead of the row-major codes; the results
+ * are the same either way.  The caller keeps its weights alive until
+ * destroy. */
 int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* layers,
                       const float* w_post_final, const float* w_final, moe_decode_t** out);
 

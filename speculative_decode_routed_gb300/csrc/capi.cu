@@ -118,6 +118,8 @@ struct moe_decode_s {
   moe::TcParams tgu{}, tdn{};
   std::vector<CUtensorMap> tm_w13, tm_w2;
   std::vector<uint8_t*> sfa13, sfa2;   // weight scale atoms per layer (library-owned)
+  std::vector<uint8_t*> tiled13, tiled2;  // the expert codes in 16 KB tiles per layer (library-owned)
+  bool tiled = false;                  // the weight maps are over the tiles
   CUtensorMap tm_xpool{}, tm_xcodes{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
 };
 
@@ -288,6 +290,23 @@ int encode_rows_kb(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
   return MOE_OK;
 }
 
+// Tiled codes [tiles][128 rows][128 B]: boxes of kblocks consecutive whole
+// tiles, each one contiguous 16 KB read, landing 128B-swizzled.
+int encode_tiles(CUtensorMap* m, const void* base, uint64_t tiles, uint32_t kblocks) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {128, 128, tiles};
+  const cuuint64_t strides[2] = {128, 16384};
+  const cuuint32_t box[3] = {128, 128, kblocks};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "tensor map encode failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 // Scale lines [groups][rows][16 B]: boxes of 16 B x 32 rows x box_groups.
 int encode_lines(CUtensorMap* m, const void* base, uint64_t rows, uint64_t groups,
                  uint32_t box_groups = 4) {
@@ -433,11 +452,13 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   // gate/up and down in one persistent launch
   moe::TcParams tg = h->tgu;
   tg.sfa = h->sfa13[layer];
+  tg.tiled = h->tiled;
   tg.gscale = w.w_gscale;
   tg.ws = h->ws;
   tg.direct = direct ? 1 : 0;
   moe::TcParams td = h->tdn;
   td.sfa = h->sfa2[layer];
+  td.tiled = h->tiled;
   td.gscale = w.w_gscale;
   td.ws = h->ws;
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
@@ -654,6 +675,35 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
       if (!rc && moe::launch_sf_atoms(layers[l].w2_sf, (int64_t)E * H, (int)(I / 16), h->tdn.KBLK,
                                       h->sfa2[l], nullptr) != cudaSuccess)
         rc = fail(MOE_ECUDA, "scale atoms launch");
+    }
+    // the expert codes in 16 KB tiles, so that each TMA box is one contiguous
+    // read; when the memory is not there the row-major maps stay
+    if (!rc) {
+      const uint64_t n13 = E * (uint64_t)h->tgu.row_tiles * h->tgu.KBLK;
+      const uint64_t n2 = E * (uint64_t)h->tdn.row_tiles * h->tdn.KBLK;
+      h->tiled13.assign(d.n_layers, nullptr);
+      h->tiled2.assign(d.n_layers, nullptr);
+      bool ok = true;
+      for (int l = 0; l < d.n_layers && ok; ++l)
+        ok = cudaMalloc(&h->tiled13[l], n13 * 16384) == cudaSuccess &&
+             cudaMalloc(&h->tiled2[l], n2 * 16384) == cudaSuccess;
+      if (!ok) {
+        cudaGetLastError();
+        for (uint8_t* p : h->tiled13) cudaFree(p);
+        for (uint8_t* p : h->tiled2) cudaFree(p);
+        h->tiled13.clear();
+        h->tiled2.clear();
+      }
+      for (int l = 0; l < d.n_layers && ok && !rc; ++l) {
+        if (moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w13), (int64_t)E * 2 * I, (int)(H / 2),
+                                   h->tiled13[l], nullptr) != cudaSuccess ||
+            moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w2), (int64_t)E * H, (int)(I / 2),
+                                   h->tiled2[l], nullptr) != cudaSuccess)
+          rc = fail(MOE_ECUDA, "code tiling launch");
+        if (!rc) rc = encode_tiles(&h->tm_w13[l], h->tiled13[l], n13, 1);
+        if (!rc) rc = encode_tiles(&h->tm_w2[l], h->tiled2[l], n2, kps);
+      }
+      h->tiled = ok;
     }
     if (!rc && cudaDeviceSynchronize() != cudaSuccess) rc = fail(MOE_ECUDA, "scale atoms");
     if (rc) {
@@ -917,6 +967,8 @@ void moe_decode_destroy(moe_decode_t* h) {
   cudaFree(h->io_out);
   cudaFree(h->ws_mem);
   for (uint8_t* p : h->sfa13) cudaFree(p);
+  for (uint8_t* p : h->tiled13) cudaFree(p);
+  for (uint8_t* p : h->tiled2) cudaFree(p);
   for (uint8_t* p : h->sfa2) cudaFree(p);
   delete h;
 }

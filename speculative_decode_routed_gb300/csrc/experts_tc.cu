@@ -451,7 +451,9 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
                                  (uint32_t)(nt * KPS) * (4096u + 2048u);
           mbar_arrive_expect_tx(full, bytes);
           // gate rows (gate/up) or output rows (down) of this tile
-          if (KPS == 1)
+          if (p.tiled)  // tiles (e, tile, kb..kb+KPS-1) are contiguous
+            tma_3d_hint(st, tm_a, 0, 0, (e * p.row_tiles + tile) * KB + kb, full, pol);
+          else if (KPS == 1)
             tma_2d(st, tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
           else
             tma_3d_hint(st, tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
@@ -460,7 +462,10 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
                          full);
           if (kGU) {  // gate/up stages hold one K-block
             const int ru = p.I / 128 + tile;  // up rows follow the gate rows
-            tma_2d(st + 16384, tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
+            if (p.tiled)
+              tma_3d_hint(st + 16384, tm_a, 0, 0, (e * p.row_tiles + ru) * KB + kb, full, pol);
+            else
+              tma_2d(st + 16384, tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
             bulk_g2s_plain(st + p.off_sfa + 2048,
                            p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
                            full);
@@ -840,6 +845,28 @@ cudaError_t launch_tc_moe(const TcParams& gu, const CUtensorMap& gu_a, const CUt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc_moe_kernel, gu, gu_a, gu_b, gu_sfb, dn, dn_a, dn_b, dn_sfb);
+}
+
+// One CTA per 16 KB tile (row tile rt = t / KB, K-block kb = t % KB), 16
+// bytes per thread per step.
+__global__ void tile_codes_kernel(const uint8_t* __restrict__ src, int inner, int KB,
+                                  uint8_t* __restrict__ dst) {
+  const int64_t t = blockIdx.x;
+  const int64_t row0 = (t / KB) * 128;
+  const int kb = (int)(t % KB);
+  for (int q = threadIdx.x; q < 1024; q += blockDim.x) {
+    const int r = q >> 3, c = (q & 7) * 16;
+    const int col = kb * 128 + c;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (col + 16 <= inner) v = __ldg(reinterpret_cast<const uint4*>(src + (row0 + r) * inner + col));
+    *reinterpret_cast<uint4*>(dst + t * 16384 + r * 128 + c) = v;
+  }
+}
+
+cudaError_t launch_tile_codes(const uint8_t* src, int64_t rows, int inner, uint8_t* dst, cudaStream_t s) {
+  const int KB = (inner + 127) / 128;
+  tile_codes_kernel<<<(unsigned)(rows / 128 * KB), 256, 0, s>>>(src, inner, KB, dst);
+  return cudaGetLastError();
 }
 
 cudaError_t tc_set_smem(size_t bytes) {

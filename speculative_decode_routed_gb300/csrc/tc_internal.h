@@ -33,6 +33,8 @@ struct TcParams {
   int ws_pairs;             // rows * k of the workspace
   int direct;               // gate/up: B is the MoE input's rows themselves (rows <= 32), not
                             // its pooled copy; each pair reads the accumulator column of its row
+  int tiled;                // 1: the weight map is over the library's tiled copy of the codes,
+                            //    [E * row_tiles * KBLK][128 rows][128 B], each box contiguous
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
   Workspace ws;
@@ -51,6 +53,10 @@ cudaError_t launch_tc_moe(const TcParams& gu, const CUtensorMap& gu_a, const CUt
                           const CUtensorMap& dn_b, const CUtensorMap& dn_sfb, int grid,
                           cudaStream_t s, bool pdl);
 size_t tc_moe_smem_bytes(const TcParams& gu, const TcParams& dn);
+// Codes [rows][inner bytes] (rows a multiple of 128) into tiles
+// [rows / 128][ceil(inner / 128)][128][128 B], the missing part of a last
+// partial K-block zero.
+cudaError_t launch_tile_codes(const uint8_t* src, int64_t rows, int inner, uint8_t* dst, cudaStream_t s);
 cudaError_t launch_pool_gather(const PoolParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_sf_atoms(const uint8_t* sf, int64_t rows, int ks, int kblk, uint8_t* out,
                             cudaStream_t s);
