@@ -52,8 +52,8 @@ def _peaks():
 # one ncu capture at serving widths with 64 experts; valid only for the
 # kernel source it was taken on (profiles/expert_kernel_tc_fused_E64.md).
 EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu",
-                   "sha256_prefix": "de35a0fe07d72f35", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": 1075894080 / 43}
+                   "sha256_prefix": "75a309af2ce74a27", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": 1069186560 / 43}
 
 
 def _experts_traffic(w: synth.Workload, n_active: float):
