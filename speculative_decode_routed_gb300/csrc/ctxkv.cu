@@ -168,6 +168,24 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
   const int KD = p.KVH * p.D;
   __nv_bfloat16* row = p.kv + ((size_t)l * p.n + r) * 2 * KD;
 
+  // The caller's positions and slots and the rotary table do not come from
+  // the projection: read them before waiting for it.
+  int64_t pos = 0;
+  bool pos_ok = true;
+  float2 t[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) t[i] = make_float2(1.0f, 0.0f);
+  if (p.max_pos > 0) {
+    pos = p.positions[r];
+    pos_ok = pos >= 0 && pos < p.max_pos;
+    if (pos_ok) {
+      const float2* cs = p.cs + (size_t)pos * (p.D / 2) + (lane & 15) * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) t[i] = __ldg(cs + i);
+    }
+  }
+  const int64_t slot = p.slots ? p.slots[(size_t)l * p.slot_stride + r] : -1;
+
   float k[E], v[E];
   if (p.part) {
 #pragma unroll
@@ -213,19 +231,16 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
   for (int i = 0; i < E; ++i) k[i] = __bfloat162float(__float2bfloat16_rn(k[i] * inv));
 
   if (p.max_pos > 0) {
-    const int64_t pos = p.positions[r];
-    if (pos < 0 || pos >= p.max_pos) {
+    if (!pos_ok) {
       if (lane == 0) latch_error(p.err, kErrPosition);
       return;
     }
-    const float2* cs = p.cs + (size_t)pos * (p.D / 2) + (lane & 15) * E;
     float y[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) {
       const float partner = __shfl_xor_sync(0xffffffffu, k[i], 16);
-      const float2 t = __ldg(cs + i);
       // first half: x1 cos - x2 sin; second half: x2 cos + x1 sin
-      y[i] = lane < 16 ? k[i] * t.x - partner * t.y : k[i] * t.x + partner * t.y;
+      y[i] = lane < 16 ? k[i] * t[i].x - partner * t[i].y : k[i] * t[i].x + partner * t[i].y;
     }
 #pragma unroll
     for (int i = 0; i < E; ++i) k[i] = y[i];
@@ -235,7 +250,6 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
   store_bf16<E>(p.k_out + o, k);
   store_bf16<E>(p.v_out + o, v);
   if (p.slots) {
-    const int64_t slot = p.slots[(size_t)l * p.slot_stride + r];
     if (slot >= p.n_slots) {
       if (lane == 0) latch_error(p.err, kErrSlot);
     } else if (slot >= 0) {
