@@ -6,9 +6,11 @@ Staged checks feed each oracle piece the GPU's own output of the stage before
 and values into the cache scatter): projections and keys bit for bit except
 at bf16 rounding midpoints, values and caches bit for bit.  End to end the
 oracle runs on its own; a rounding taken the other way upstream may move a
-projection output by one bf16 step, which the key norm and the rotation carry
-into both keys of a rotated pair, so a key may differ by up to 2^-6 of its
-pair's norm and a value by 2^-7 of itself.
+projection output by one bf16 step (up to 2^-7 of it), which the key norm
+carries into the normalised key; the two casts before the rotation may then
+round apart by another step, the rotation keeps the pair's difference vector's
+length, and the two final casts may add a third: a key may differ by up to
+3 * 2^-7 of its pair's norm, and a value by 2^-7 of itself.
 """
 import numpy as np
 import pytest
@@ -18,6 +20,9 @@ import synth
 from helpers import bf16_near_tie, dev_array
 
 torch = pytest.importorskip("torch")
+
+# end-to-end key tolerance, relative to the pair's norm (three bf16 steps)
+KEY_TOL = 3 * 2.0 ** -7
 pytestmark = pytest.mark.gpu
 
 SMALL = synth.CTXKV_WORKLOADS["draft_ctx_kv_small"]
@@ -121,7 +126,7 @@ def _check(case, n, variant=0, slots=None, positions=None):
     rk = oracle.bf16_to_f64(ref["k"])
     pair = np.sqrt(rk[..., :h] ** 2 + rk[..., h:] ** 2)
     pair = np.concatenate([pair, pair], axis=-1)
-    assert np.all(dk <= 2.0 ** -6 * pair), f"keys: max excess {np.max(dk - 2.0 ** -6 * pair):.3e}"
+    assert np.all(dk <= KEY_TOL * pair), f"keys: max excess {np.max(dk - KEY_TOL * pair):.3e}"
     rv = oracle.bf16_to_f64(ref["v"])
     dv = np.abs(oracle.bf16_to_f64(got["v"]) - rv)
     rms_v = float(np.sqrt(np.mean(rv ** 2)))

@@ -172,3 +172,33 @@ def test_cache_scatter_by_brute_force():
                 if s >= 0:
                     wk[l, s], wv[l, s] = k[l, r], v[l, r]
         assert np.array_equal(kc, wk) and np.array_equal(vc, wv)
+
+
+def test_key_tolerance_covers_one_step_projection_differences():
+    """The end-to-end key tolerance of the GPU tests, 3 * 2^-7 of the pair's norm,
+    holds when projection outputs move by one bf16 step (the staged GEMM check's
+    allowance): the key norm carries the step, the casts before the rotation may
+    round apart, the rotation keeps the difference's length and the final casts
+    may add one more step.  Two steps (2^-6) do not suffice.  The differences are
+    a fifth of the outputs here, far more than the staged check lets through, and
+    still few enough that the head's RMS barely moves (a step in every output of
+    a head, in opposite directions, could move it by up to one more step)."""
+    rs = np.random.RandomState(6)
+    L, n, KVH, D = 2, 64, 8, 128
+    kv = _kv_rows(rs, L, n, KVH, D)
+    pos = rs.randint(0, 32768, n)
+    k0, _, _ = oracle.k_norm_rope(kv, pos, KVH, D, 1e-6, 10000.0)
+    a = _f64(k0)
+    h = D // 2
+    pair = np.sqrt(a[..., :h] ** 2 + a[..., h:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    worst = 0.0
+    for _ in range(20):
+        kv1 = kv.copy()
+        m = rs.rand(*kv.shape) < 0.2
+        step = rs.choice([-1, 1], kv.shape)
+        kv1[m] = (kv1[m].astype(np.int64) + step[m]).astype(np.uint16)
+        k1, _, _ = oracle.k_norm_rope(kv1, pos, KVH, D, 1e-6, 10000.0)
+        worst = max(worst, float(np.max(np.abs(_f64(k1) - a) / pair)))
+    assert worst <= 3 * 2.0 ** -7
+    assert worst > 2.0 ** -6
