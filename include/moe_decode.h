@@ -208,7 +208,10 @@ int moe_decode_debug(moe_decode_t* h, moe_decode_debug_view* out);
  * else MOE_OK. */
 int moe_decode_last_error(moe_decode_t* h);
 
-/* Bytes of device workspace the handle holds. */
+/* Bytes of device workspace (activations, routing and scratch) the handle
+ * holds.  The rearranged weight copies it also holds are not counted: the
+ * scale atoms, 1/8 of the expert code bytes, and the tiled codes, as many
+ * bytes as the codes when they could be allocated. */
 size_t moe_decode_workspace_bytes(const moe_decode_t* h);
 
 /* Number of kernels one moe_decode_step of max_rows rows launches: per layer
