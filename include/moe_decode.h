@@ -171,7 +171,11 @@ int moe_decode_step(moe_decode_t* h, int rows, const uint16_t* branch, float* st
 
 /* As moe_decode_step, replayed from a CUDA graph the library captures on the
  * first call for this (rows, branch, stream, out) and caches in the handle.
- * The first call for a new key must not itself be under stream capture. */
+ * The first call for a new key must not itself be under stream capture.
+ * Each of the library's graph caches (this one, the host-buffer step's and
+ * the dense layer's) keeps the 32 most recently used graphs; an older one is
+ * destroyed (freed by the runtime once it completes) and captured again if
+ * its key comes back. */
 int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, float* stream,
                           uint16_t* out, void* cuda_stream);
 

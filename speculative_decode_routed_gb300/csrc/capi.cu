@@ -779,9 +779,9 @@ int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, flo
                           uint16_t* out, void* cuda_stream) {
   int rc = check_step_args(h, rows, branch, stream, out);
   if (rc) return rc;
-  cudaGraphExec_t exec = nullptr;
-  for (const GraphEntry& g : h->graphs)
-    if (g.rows == rows && g.branch == branch && g.stream == stream && g.out == out) exec = g.exec;
+  cudaGraphExec_t exec = moe::graph_cache_find(h->graphs, [&](const GraphEntry& g) {
+    return g.rows == rows && g.branch == branch && g.stream == stream && g.out == out;
+  });
   if (!exec) {
     cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return cuda_fail(e, "begin capture");
@@ -796,7 +796,7 @@ int moe_decode_step_graph(moe_decode_t* h, int rows, const uint16_t* branch, flo
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
-    h->graphs.push_back(GraphEntry{rows, branch, stream, out, exec});
+    moe::graph_cache_insert(h->graphs, GraphEntry{rows, branch, stream, out, exec});
   }
   const cudaError_t e = cudaGraphLaunch(exec, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "graph launch");
@@ -815,10 +815,9 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
   // Pinned host buffers: the copies in, the step and the copies out as one
   // cached graph, so a call is one launch and one synchronization.
   if (host_pinned(branch_host) && host_pinned(stream_host) && host_pinned(out_host)) {
-    cudaGraphExec_t exec = nullptr;
-    for (const GraphEntry& g : h->host_graphs)
-      if (g.rows == rows && g.branch == branch_host && g.stream == stream_host && g.out == out_host)
-        exec = g.exec;
+    cudaGraphExec_t exec = moe::graph_cache_find(h->host_graphs, [&](const GraphEntry& g) {
+      return g.rows == rows && g.branch == branch_host && g.stream == stream_host && g.out == out_host;
+    });
     if (!exec) {
       cudaStream_t c = h->cap_stream;
       // mapped pinned buffers: the first boundary reads the branch and the
@@ -856,7 +855,7 @@ int moe_decode_step_host(moe_decode_t* h, int rows, const uint16_t* branch_host,
       e = cudaGraphInstantiate(&exec, graph, 0);
       cudaGraphDestroy(graph);
       if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
-      h->host_graphs.push_back(GraphEntry{rows, branch_host, stream_host, out_host, exec});
+      moe::graph_cache_insert(h->host_graphs, GraphEntry{rows, branch_host, stream_host, out_host, exec});
     }
     cudaError_t e = cudaGraphLaunch(exec, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);

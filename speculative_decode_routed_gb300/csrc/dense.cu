@@ -325,9 +325,9 @@ int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, fl
   if (attn_d && stream_d && dense_aligned(attn_d, 8) && dense_aligned(stream_d, 16)) {
     // mapped page-locked buffers: the boundaries read and write host memory
     // themselves; the layer is one cached graph per (rows, buffers)
-    cudaGraphExec_t exec = nullptr;
-    for (const auto& g : h->host_graphs)
-      if (g.rows == rows && g.attn == attn_host && g.stream == stream_host) exec = g.exec;
+    cudaGraphExec_t exec = moe::graph_cache_find(h->host_graphs, [&](const moe_dense_s::HostGraph& g) {
+      return g.rows == rows && g.attn == attn_host && g.stream == stream_host;
+    });
     if (!exec) {
       cudaStream_t c = nullptr;
       e = cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking);
@@ -346,7 +346,7 @@ int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, fl
       e = cudaGraphInstantiate(&exec, graph, 0);
       cudaGraphDestroy(graph);
       if (e != cudaSuccess) return cuda_err(e, "graph instantiate");
-      h->host_graphs.push_back({rows, attn_host, stream_host, exec});
+      moe::graph_cache_insert(h->host_graphs, moe_dense_s::HostGraph{rows, attn_host, stream_host, exec});
     }
     e = cudaGraphLaunch(exec, s);
   } else {

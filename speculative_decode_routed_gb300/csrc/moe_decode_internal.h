@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <vector>
+
 namespace moe {
 
 // Pairs of one virtual expert: an active expert's pooled pairs in groups of
@@ -156,5 +158,32 @@ void* host_mapped(const void* p);
 
 size_t expert_smem_bytes(const ExpertParams& p);
 size_t expert_ctrl_bytes();
+
+// The library-owned graph caches (one per entry point that keeps graphs)
+// hold at most kMaxCachedGraphs executables.  A lookup moves its hit to the
+// back; an insert past the bound destroys the least recently used, which the
+// runtime frees once it completes if it is still running.
+constexpr size_t kMaxCachedGraphs = 32;
+
+template <class Entry, class Match>
+cudaGraphExec_t graph_cache_find(std::vector<Entry>& cache, Match match) {
+  for (size_t i = 0; i < cache.size(); ++i)
+    if (match(cache[i])) {
+      const Entry hit = cache[i];
+      cache.erase(cache.begin() + (std::ptrdiff_t)i);
+      cache.push_back(hit);
+      return hit.exec;
+    }
+  return nullptr;
+}
+
+template <class Entry>
+void graph_cache_insert(std::vector<Entry>& cache, const Entry& entry) {
+  if (cache.size() >= kMaxCachedGraphs) {
+    cudaGraphExecDestroy(cache.front().exec);
+    cache.erase(cache.begin());
+  }
+  cache.push_back(entry);
+}
 
 }  // namespace moe

@@ -291,6 +291,30 @@ def test_repeated_replays_bitwise():
     dec.close()
 
 
+def test_graph_cache_evicts_and_recaptures():
+    """More distinct (branch, stream, out) buffer sets than the step-graph cache
+    keeps (32): every call gives the eager result bit for bit, including the
+    first sets again once their graphs were evicted and are captured anew."""
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    s0 = stream.clone()
+    out = torch.empty_like(branch)
+    dec.step(w.rows, branch, stream, out)
+    torch.cuda.synchronize()
+    dec.check()
+    ref_s, ref_o = stream.clone(), out.clone()
+    sets = [(branch.clone(), s0.clone(), torch.empty_like(out)) for _ in range(40)]
+    for b, s, o in sets + sets[:3]:
+        s.copy_(s0)
+        dec.step_graph(w.rows, b, s, o)
+        torch.cuda.synchronize()
+        assert torch.equal(s, ref_s) and torch.equal(o, ref_o)
+    dec.check()
+    dec.close()
+
+
 @pytest.mark.parametrize("H", [256, 7168])
 def test_front_and_aux_copies(H):
     """The first layer's front against the oracle (stream bit-exact, the
