@@ -56,19 +56,42 @@ EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu
                    "bytes_per_active_expert": 1069186560 / 43}
 
 
+# DRAM traffic (read + write) of one launch of the dense draft layer's
+# streamed gate/up projection at 8 rows, from one ncu capture
+# (profiles/dense_projections_streaming.md); valid only for the kernel
+# source it was taken on.
+DENSE_GATE_UP_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/gemv.cuh",
+                         "sha256_prefix": "a919c1e476a720c4", "hidden": 7168, "inter": 28672, "rows": 8,
+                         "bytes": 822260736 + 3262976}
+
+
+def _source_unchanged(t) -> bool:
+    """True if t["source"] still hashes to the source the capture was taken on."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, t["source"]), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest().startswith(t["sha256_prefix"])
+    except OSError:
+        return False
+
+
 def _experts_traffic(w: synth.Workload, n_active: float):
     """Bytes per launch of the experts kernel scaled from the ncu capture, or
     None if the kernel changed since or the widths differ."""
-    import hashlib
     t = EXPERTS_TRAFFIC
-    try:
-        with open(os.path.join(ROOT, t["source"]), "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-    except OSError:
-        return None
-    if not digest.startswith(t["sha256_prefix"]) or (w.hidden, w.inter) != (t["hidden"], t["inter"]):
+    if not _source_unchanged(t) or (w.hidden, w.inter) != (t["hidden"], t["inter"]):
         return None
     return int(round(t["bytes_per_active_expert"] * n_active))
+
+
+def _dense_traffic(hidden: int, inter: int, rows: int):
+    """Bytes per launch of the streamed gate/up projection from the ncu
+    capture, or None if the kernel changed since or the shape differs (the
+    capture is not scaled: its rows and widths are the bench's)."""
+    t = DENSE_GATE_UP_TRAFFIC
+    if not _source_unchanged(t) or (hidden, inter, rows) != (t["hidden"], t["inter"], t["rows"]):
+        return None
+    return int(t["bytes"])
 
 
 def _algorithmic_bytes(w: synth.Workload, n_active: int, rows: int):
@@ -579,7 +602,8 @@ def run_dense(args, w):
         "roofline": {"kernel": "gate/up projection + SiLU * mul (split-K weight-streaming kernel, bf16 mma.sync)"
                      if streamed else "gate/up projection (cuBLAS bf16 GEMM)", "bound": "hbm",
                      "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gu_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(gu_gbs / peak, 4),
+                     "traffic": _dense_traffic(H, I, rows) if streamed else None, "peak_kind": peak_kind,
                      "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gate_up"])},
         "kernels_us": dict({"boundary_attn": round(k_ms[0] * 1000, 2), "gate_up": round(k_ms[1] * 1000, 2)},
                            **({} if streamed else {"silu_mul": round(k_ms[2] * 1000, 2)}),

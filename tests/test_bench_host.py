@@ -61,3 +61,23 @@ def test_reference_arm_prints_once_under_two_ranks():
     rec = json.loads(lines[0][0])
     assert rec["impl"] == "reference" and rec["unit"] == "µs" and rec["higher_is_better"] is False
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_figures_are_gated_on_their_capture(monkeypatch):
+    """The ncu traffic figures are reported only for the kernel source and the
+    shape they were captured on, and each sits just above its kernel's
+    algorithmic bytes (every weight byte read once)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    wd = synth.DENSE_WORKLOADS["draft_dense"]
+    traffic = bench._dense_traffic(wd.hidden, wd.inter, 8)
+    if traffic is not None:   # the projection source is the captured one
+        ratio = traffic / bench._dense_bytes(wd, 8)["gate_up"]
+        assert 1.0 <= ratio < 1.01
+    assert bench._dense_traffic(wd.hidden, wd.inter, 4) is None
+    assert bench._dense_traffic(256, 384, 8) is None
+    monkeypatch.setitem(bench.DENSE_GATE_UP_TRAFFIC, "sha256_prefix", "0" * 16)
+    assert bench._dense_traffic(wd.hidden, wd.inter, 8) is None
+    monkeypatch.setitem(bench.EXPERTS_TRAFFIC, "sha256_prefix", "0" * 16)
+    assert bench._experts_traffic(synth.WORKLOADS["serving"], 60.0) is None
