@@ -22,9 +22,10 @@
  *    (FP4 E2M1: bias 1, max 6) and OCP 8-bit Floating Point (OFP8) v1.0
  *    (E4M3: bias 7, no infinities, max 448).
  *  - NVFP4 two-level scaling (e4m3 scale per 16 elements, fp32 per-tensor
- *    scale = amax / (6 * 448)) and the SiLU-gated expert MLP: the workload
- *    statement of this build; their order of operations is a reading
- *    recorded with the design notes.
+ *    scale = amax / (6 * 448)) and the SiLU-gated expert MLP: the stated
+ *    number format and block of the routed decode workload, which the pages
+ *    name but do not print; their order of operations is a reading recorded
+ *    with the design notes.
  */
 #include "oracle.h"
 
