@@ -174,6 +174,7 @@ int plan_experts(moe::ExpertParams& p, int mode, const moe_decode_dims& d) {
   return MOE_OK;
 }
 
+#if MOE_EXPERT_TC
 // Tile plan of the tensor-core path (see experts_tc.cu).
 int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
   p = moe::TcParams{};
@@ -323,6 +324,7 @@ int encode_lines(CUtensorMap* m, const void* base, uint64_t rows, uint64_t group
   if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "tensor map encode failed (%d)", (int)r);
   return MOE_OK;
 }
+#endif  // MOE_EXPERT_TC
 
 int check_layer(const moe_layer_weights& w, int i) {
   if (!w.w_post || !w.w_pre || !w.router_w || !w.w13 || !w.w13_sf || !w.w2 || !w.w2_sf ||
