@@ -128,6 +128,51 @@ MUTANTS = [
     ("context KV: every layer's keys written to layer 0's cache",
      "memcpy(k_cache + ((int64_t)l * n_slots + slot) * KD,", "memcpy(k_cache + (slot) * KD,",
      [("test_oracle_ctxkv", "test_cache_scatter_by_brute_force", {})]),
+    ("context KV: slot 0 skipped as if negative",
+     "if (slot < 0 || slot >= n_slots) continue;", "if (slot <= 0 || slot >= n_slots) continue;",
+     [("test_oracle_ctxkv", "test_cache_scatter_by_brute_force", {})]),
+    ("context KV: values copied from the key heads",
+     "memcpy(v_out + o, row + KD + hd * D, sizeof(uint16_t) * D);",
+     "memcpy(v_out + o, row + hd * D, sizeof(uint16_t) * D);",
+     [("test_oracle_ctxkv", "test_key_norm_of_constant_heads_and_values_pass_through", {})]),
+    ("context KV: keys rotated by the row index instead of the position",
+     "double ang = (double)positions[r] * pow(", "double ang = (double)r * pow(",
+     [("test_oracle_ctxkv", "test_one_hot_key_rotates_into_its_partner_dimension", {})]),
+    ("e4m3 subnormals decoded at half their value",
+     "mag = ldexp((double)m / 8.0, -6);", "mag = ldexp((double)m / 8.0, -7);",
+     [("test_oracle_formats", "test_e4m3_decode_matches_torch_and_golden", {})]),
+    ("e4m3 saturates to NaN instead of 448",
+     "if (a >= 448.0) return (uint8_t)(s | 0x7E);", "if (a >= 448.0) return (uint8_t)(s | 0x7F);",
+     [("test_oracle_formats", "test_e4m3_encode_matches_torch_in_range_and_saturates", {})]),
+    ("router bias subtracted",
+     "if (bias) acc += (double)bias[e];", "if (bias) acc -= (double)bias[e];",
+     [("test_oracle_step", "test_k_equals_E_is_the_full_softmax", {"bias": True})]),
+    ("softmax at temperature 2",
+     "p[e] = exp(logit[e] - m);", "p[e] = exp(0.5 * (logit[e] - m));",
+     [("test_oracle_step", "test_k_equals_E_is_the_full_softmax", {"bias": False})]),
+    ("pooler lists idle experts as active",
+     "if (count[e] > 0) active[na++] = e;", "if (count[e] >= 0) active[na++] = e;",
+     [("test_oracle_step", "test_pooler_invariants", {"rows": 2, "E": 9, "k": 2})]),
+    ("pooler orders an expert's pairs by descending row",
+     "for (int r = 0; r < rows; ++r)\n      for (int s = 0; s < k; ++s)\n        if (ids[r * k + s] == e)",
+     "for (int r = rows - 1; r >= 0; --r)\n      for (int s = 0; s < k; ++s)\n        if (ids[r * k + s] == e)",
+     [("test_oracle_step", "test_pooler_invariants", {"rows": 13, "E": 9, "k": 3})]),
+    ("h quantized from the first expert's rows",
+     "oracle_nvfp4_quantize(h + (int64_t)offset[e] * I, n, I,", "oracle_nvfp4_quantize(h, n, I,",
+     [("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {}),
+      ("test_oracle_step", "test_tiny_layer_statistics", {})]),
+    ("down dequantizes every h with expert 0's scale",
+     "h_sg[e], 1, I, hh + (int64_t)pos * I);", "h_sg[0], 1, I, hh + (int64_t)pos * I);",
+     [("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {})]),
+    ("gather reads the pairs slot-major",
+     "acc += gates[r * k + s] * (double)o[((int64_t)r * k + s) * H + hh];",
+     "acc += gates[r * k + s] * (double)o[((int64_t)s * rows + r) * H + hh];",
+     [("test_oracle_step", "test_every_expert_selected_matches_gated_dense_sum", {}),
+      ("test_oracle_step", "test_row_permutation_permutes_outputs", {})]),
+    ("dense: SiLU * mul takes the up value from the gate half",
+     "double u = oracle_bf16_decode(gu[(int64_t)r * 2 * I + I + j]);",
+     "double u = oracle_bf16_decode(gu[(int64_t)r * 2 * I + j]);",
+     [("test_oracle_dense", "test_single_entry_weights_name_each_product", {})]),
 ]
 
 
