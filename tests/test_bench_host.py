@@ -81,3 +81,27 @@ def test_traffic_figures_are_gated_on_their_capture(monkeypatch):
     assert bench._dense_traffic(wd.hidden, wd.inter, 8) is None
     monkeypatch.setitem(bench.EXPERTS_TRAFFIC, "sha256_prefix", "0" * 16)
     assert bench._experts_traffic(synth.WORKLOADS["serving"], 60.0) is None
+
+
+@pytest.mark.parametrize("workload", ["tiny", "draft_dense_small", "draft_ctx_kv_small"])
+def test_reference_arm_line_keeps_the_contract(workload):
+    """The oracle arm's one JSON line, for each kind of workload, carries the
+    keys the bench contract names, with a cpu_baseline describing the run
+    and an e2e of zero host bytes."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload,
+                        "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["steps"] == 1 and rec["warmup"] == 3
+    assert rec["value"] > 0 and rec["unit"] == "µs" and rec["higher_is_better"] is False
+    assert rec["config"]["workload"] == workload
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == rec["value"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
