@@ -190,3 +190,42 @@ def test_cuda_core_expert_variant_compiles_cleanly(tmp_path):
         r = subprocess.run(argv, capture_output=True, text=True, timeout=300)
         assert r.returncode == 0, r.stderr[-2000:]
         assert "warning" not in (r.stdout + r.stderr).lower(), (extra, r.stderr[-2000:])
+
+
+def test_weight_streaming_split_choice(tmp_path):
+    """gemv_splits (the split-K choice of the weight-streaming projection), run
+    as host code: no split when K is not a multiple of 128 or R of 32; else a
+    split count that divides K into 128-column steps, whose busiest-SM bytes
+    are within 3 % of the best choice keeping 8 warps busy on every SM, and
+    the fewest such splits."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc")
+                                    else None)
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    csrc = os.path.join(os.path.dirname(moe.__file__), "csrc")
+    cases = [(4, 2048, 7168, 152), (1, 7168, 28672, 152), (1, 4096, 1024, 152), (2, 512, 4096, 152),
+             (4, 2048, 7168, 148), (1, 256, 384, 152), (1, 7168, 7000, 152), (1, 7000, 7168, 152),
+             (8, 32, 128, 4)]
+    src = tmp_path / "splits.cu"
+    src.write_text('#include <cstdio>\n#include "gemv.cuh"\nint main() {\n' + "".join(
+        f'  std::printf("%d\\n", moe::gemv_splits({L}, {R}, {K}, {n}));\n' for L, R, K, n in cases)
+        + "  return 0;\n}\n")
+    exe = tmp_path / "splits"
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-I", csrc,
+                        str(src), "-o", str(exe)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          timeout=60).stdout.split()]
+    for (L, R, K, n), s in zip(cases, got):
+        if K % 128 or R % 32:
+            assert s == 0
+            continue
+        valid = [c for c in range(1, 33) if K % (128 * c) == 0]
+        cost = {c: -(-(L * (R // 32) * c) // n) * (K // c) for c in valid}
+        busy = [c for c in valid if L * (R // 32) * c >= 8 * n] or valid
+        best = min(cost[c] for c in busy)
+        assert s in busy and cost[s] * 100 <= best * 103, (L, R, K, n, s)
+        assert all(cost[c] * 100 > best * 103 for c in busy if c < s), (L, R, K, n, s)
+    assert got[0] == 7   # the context-KV projection: 4 layers of 2048 rows, K 7168
