@@ -52,7 +52,9 @@
  *  - Asynchrony: layer / final / step calls are asynchronous on the given CUDA
  *    stream (a cudaStream_t passed as void*; NULL = the legacy default
  *    stream), allocate nothing and never synchronize, so they can be
- *    captured into a CUDA graph.  A handle serves one stream at a time.
+ *    captured into a CUDA graph.  A handle serves one stream and one host
+ *    thread at a time: its workspace and graph caches are not locked.
+ *    Separate handles are independent.
  *  - Supported shapes: H and I multiples of 128, at most 8192;
  *    1 <= top_k <= min(E, 16); E <= 1024; 1 <= rows <= max_rows <= 128.
  *    The device must be of the SM 10.x family (built for sm_103a).
