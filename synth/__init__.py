@@ -206,7 +206,7 @@ SWEEP_ROWS = (1, 8, 32, 64, 128)
 
 # Dense draft layers (no experts: n_experts and top_k are 0).  The pages give
 # no draft widths; hidden follows the target and the MLP is four times as wide,
-# so one layer's bf16 weights (1.41 GB) dwarf the L2.
+# so one layer's bf16 weights (1.23 GB) dwarf the L2.
 DENSE_WORKLOADS = {
     "draft_dense": Workload("draft_dense", rows=8, hidden=7168, n_experts=0, top_k=0,
                             inter=28672),
