@@ -229,3 +229,29 @@ def test_weight_streaming_split_choice(tmp_path):
         assert s in busy and cost[s] * 100 <= best * 103, (L, R, K, n, s)
         assert all(cost[c] * 100 > best * 103 for c in busy if c < s), (L, R, K, n, s)
     assert got[0] == 7   # the context-KV projection: 4 layers of 2048 rows, K 7168
+
+
+def test_header_is_plain_c_and_a_c_program_links(tmp_path):
+    """include/moe_decode.h compiles as strict C11 (no C++ in the ABI), and a C
+    program links against the library and gets a validation error back from
+    moe_decode_create before any CUDA call."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(moe.LIB_PATH)
+    src = tmp_path / "c_abi.c"
+    src.write_text('#include "moe_decode.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n  moe_decode_dims d = {0};\n  moe_decode_t* h = NULL;\n"
+                   "  int rc = moe_decode_create(&d, NULL, NULL, NULL, &h);\n"
+                   '  printf("%d %s\\n", rc, moe_decode_strerror(rc));\n  return !(rc < 0 && h == NULL);\n}\n')
+    exe = tmp_path / "c_abi"
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(root, "include"), str(src), "-L", libdir, "-lmoe_decode",
+                        f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.split()[0] == str(moe.MOE_EINVAL)
