@@ -110,3 +110,17 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "libmoe_decode.so"))
     with pytest.raises(ImportError):
         moe.lib()
+
+
+def test_profile_summaries_name_their_commands():
+    """Every ncu summary under profiles/ is short text that gives the command
+    that made it: ncu with --clock-control none, running committed files only."""
+    pdir = os.path.join(ROOT, "profiles")
+    names = sorted(os.listdir(pdir))
+    assert names
+    for n in names:
+        assert n.endswith((".md", ".txt")), n
+        text = open(os.path.join(pdir, n)).read()
+        assert len(text) < 16000, n
+        assert "ncu " in text and "--clock-control none" in text, n
+        assert "_work/" not in text and "/root/" not in text, n
