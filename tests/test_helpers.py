@@ -1,0 +1,61 @@
+"""The test helpers that excuse GPU/oracle mismatches (no GPU).
+
+bf16_near_tie decides which bf16 differences the GPU parity tests accept, so a
+mistake in it would widen every staged check.  It must flag exact rounding
+midpoints, including the top of a binade, and must not flag values whose bf16
+rounding an fp32 evaluation cannot change.
+"""
+import numpy as np
+
+import oracle
+from helpers import bf16_near_tie
+
+
+def _bf16(x):
+    return np.array([oracle.bf16_from_double(float(v)) for v in np.ravel(x)], np.uint16)
+
+
+def test_midpoints_are_flagged_and_grid_points_are_not():
+    rs = np.random.RandomState(0)
+    grid = oracle.bf16_to_f64(_bf16(rs.standard_normal(2000) * np.exp2(rs.randint(-20, 20, 2000))))
+    grid = grid[grid != 0]
+    a = np.abs(grid)
+    q = np.exp2(np.floor(np.log2(a)) - 7)              # the bf16 quantum of each value's binade
+    mid = np.sign(grid) * (a + q / 2)                  # halfway to the next bf16 value up
+    assert np.all(bf16_near_tie(mid, abs_frac=0.0))
+    assert not np.any(bf16_near_tie(grid, abs_frac=0.0))
+
+
+def test_the_band_is_relative():
+    x = np.array([1.0 + 2.0 ** -8])                  # the midpoint between 1 and 1 + 2^-7
+    for rel_off, flagged in ((5e-6, True), (-5e-6, True), (3e-5, False), (-3e-5, False)):
+        assert bf16_near_tie(x * (1 + rel_off), abs_frac=0.0)[0] == flagged, rel_off
+
+
+def test_top_of_a_binade():
+    top = 2.0 - 2.0 ** -7                            # the largest bf16 value below 2
+    mid = (top + 2.0) / 2
+    assert bf16_near_tie(np.array([mid]), abs_frac=0.0)[0]
+    assert not bf16_near_tie(np.array([top, 2.0]), abs_frac=0.0).any()
+
+
+def test_outside_the_band_fp32_cannot_change_the_rounding():
+    """Away from the band, rounding the value to fp32 first (as a GPU stage
+    that computes in fp32 does) gives the same bf16 as rounding it once from
+    fp64: fp32's own error (2^-24 relative) is far inside the 1e-5 band."""
+    import torch
+    rs = np.random.RandomState(1)
+    x = rs.standard_normal(20000) * np.exp2(rs.randint(-10, 10, 20000))
+    keep = ~bf16_near_tie(x, abs_frac=0.0)
+    assert keep.mean() > 0.99
+    via32 = torch.from_numpy(x[keep].astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(via32.view(np.uint16), _bf16(x[keep]))
+
+
+def test_zero_and_the_absolute_term():
+    assert not bf16_near_tie(np.array([0.0]))[0]
+    # a value far below the tensor's rms is flagged through the absolute term,
+    # whose tolerance there exceeds the value's whole bf16 quantum (cancellation)
+    x = np.array([3e-6, 100.0, -100.0])
+    assert bf16_near_tie(x, rel=0.0, abs_frac=1e-5)[0]
+    assert not bf16_near_tie(x, rel=0.0, abs_frac=0.0)[0]
