@@ -109,6 +109,21 @@ def bf16_near_tie(exact, rel=1e-5, abs_frac=1e-5):
     return np.abs(frac - 0.5) * q <= tol
 
 
+def bits_match(got, ref, exact, what, slack=0, exclude=None):
+    """Assert that the bf16 bit patterns `got` equal `ref` except at rounding
+    midpoints of `exact` (bf16_near_tie) or where `exclude` is set, and at
+    most max(2, slack) further elements, each one bf16 step away."""
+    off = (got != ref) & ~bf16_near_tie(exact)
+    if exclude is not None:
+        off &= ~exclude
+    n_off = int(off.sum())
+    if n_off:
+        steps = np.abs(got.astype(np.int32) - ref.astype(np.int32))[off]
+        assert n_off <= max(2, slack) and steps.max() <= 1, \
+            f"{what}: {n_off} of {got.size} elements differ away from rounding midpoints " \
+            f"(max {steps.max()} steps)"
+
+
 def expert_subproblem(ow, e):
     """A one-expert oracle.LayerWeights holding expert e of `ow` as expert 0."""
     import oracle

@@ -17,7 +17,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import bf16_near_tie, dev_array
+from helpers import bf16_near_tie, bits_match, dev_array
 
 torch = pytest.importorskip("torch")
 
@@ -40,18 +40,7 @@ def _bf16_dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
 
-def _bits_match(got, ref, exact, what, slack=0, exclude=None):
-    """Equal bf16 bits except at rounding midpoints of `exact` or where `exclude`
-    is set (and at most max(2, slack) further elements, each one bf16 step away)."""
-    off = (got != ref) & ~bf16_near_tie(exact)
-    if exclude is not None:
-        off &= ~exclude
-    n_off = int(off.sum())
-    if n_off:
-        steps = np.abs(got.astype(np.int32) - ref.astype(np.int32))[off]
-        assert n_off <= max(2, slack) and steps.max() <= 1, \
-            f"{what}: {n_off} of {got.size} elements differ away from rounding midpoints " \
-            f"(max {steps.max()} steps)"
+_bits_match = bits_match     # equal bf16 bits away from rounding midpoints
 
 
 class _Case:

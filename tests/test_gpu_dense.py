@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import bf16_near_tie, dev_array
+from helpers import bits_match, dev_array
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -77,18 +77,7 @@ class _Case:
         self.layer.close()
 
 
-def _bits_match(got, ref, exact, what, slack=0):
-    """Equal bf16 bits except at rounding midpoints of `exact` (and at most
-    max(2, slack) further elements, each one bf16 step away)."""
-    diff = got != ref
-    off = diff & ~bf16_near_tie(exact)
-    n_off = int(off.sum())
-    if n_off:
-        steps = np.abs(got.astype(np.int32) - ref.astype(np.int32))[off]
-        assert n_off <= max(2, slack) and steps.max() <= 1, \
-            f"{what}: {n_off} of {got.size} elements differ away from rounding midpoints " \
-            f"(max {steps.max()} steps)"
-    return int(diff.sum())
+_bits_match = bits_match     # equal bf16 bits away from rounding midpoints
 
 
 def _check(case, rows, variant=0):

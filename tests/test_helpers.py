@@ -59,3 +59,47 @@ def test_zero_and_the_absolute_term():
     x = np.array([3e-6, 100.0, -100.0])
     assert bf16_near_tie(x, rel=0.0, abs_frac=1e-5)[0]
     assert not bf16_near_tie(x, rel=0.0, abs_frac=0.0)[0]
+
+
+def _case():
+    rs = np.random.RandomState(2)
+    exact = rs.standard_normal(4000)
+    ref = _bf16(exact)
+    return exact, ref
+
+
+def test_bits_match_accepts_equal_and_midpoint_differences():
+    from helpers import bits_match
+    exact, ref = _case()
+    bits_match(ref.copy(), ref, exact, "equal")
+    # move elements that sit on a midpoint by one step: excused however many
+    mid = exact.copy()
+    idx = np.arange(0, 4000, 7)
+    a = np.abs(exact[idx])
+    q = np.exp2(np.floor(np.log2(a)) - 7)
+    mid[idx] = np.sign(exact[idx]) * (np.floor(a / q) * q + q / 2)
+    ref_mid = _bf16(mid)
+    got = ref_mid.copy()
+    got[idx] = ref_mid[idx] ^ 1            # the other neighbour of each midpoint
+    bits_match(got, ref_mid, mid, "midpoints")
+
+
+def test_bits_match_counts_and_sizes_the_other_differences():
+    import pytest
+    from helpers import bits_match
+    exact, ref = _case()
+    away = np.flatnonzero(~bf16_near_tie(exact))[:10]
+    got = ref.copy()
+    got[away[:2]] += 1                      # two one-step differences: always allowed
+    bits_match(got, ref, exact, "two")
+    got[away[2]] += 1                       # a third needs slack
+    with pytest.raises(AssertionError):
+        bits_match(got, ref, exact, "three")
+    bits_match(got, ref, exact, "three with slack", slack=3)
+    got = ref.copy()
+    got[away[0]] += 2                       # two steps: never allowed
+    with pytest.raises(AssertionError):
+        bits_match(got, ref, exact, "two steps", slack=100)
+    excl = np.zeros(ref.shape, bool)
+    excl[away[0]] = True
+    bits_match(got, ref, exact, "excluded", exclude=excl)
