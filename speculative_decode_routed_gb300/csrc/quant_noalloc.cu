@@ -21,6 +21,8 @@
 // scales and tensor scale are bit for bit those of moe_nvfp4_quantize.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "../../include/moe_decode.h"
 #include "common.cuh"
 #include "moe_decode_internal.h"
@@ -81,9 +83,44 @@ __global__ void __launch_bounds__(kNoAllocThreads)
   }
 }
 
-// Device address of the scratch, looked up once per device.
+// Device address of the scratch, looked up once per device and context.  A
+// device reset (cudaDeviceReset, or a reset of the primary context) loads the
+// module again at a new address, so the cached address is kept together with
+// the unique ID of the context it was taken in (a context handle may be
+// reused after a reset; its ID never is) and looked up again when the current
+// context's ID differs.
 std::mutex g_setup_mu;
 unsigned char* g_scratch_addr[kNoAllocMaxDevices] = {};
+unsigned long long g_scratch_ctx_id[kNoAllocMaxDevices] = {};
+
+// The unique ID of the calling thread's current context (0: none yet), from
+// the driver's cuCtxGetCurrent and cuCtxGetId through the runtime's
+// entry-point query (the library does not link the driver library itself).
+CUresult current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* p1 = nullptr;
+    void* p2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 4000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return CUDA_ERROR_NOT_FOUND;
+    get_current = reinterpret_cast<GetCurrent>(p1);
+    get_id = reinterpret_cast<GetId>(p2);
+  }
+  CUcontext ctx = nullptr;
+  const CUresult r = get_current(&ctx);
+  if (r != CUDA_SUCCESS) return r;
+  *id = 0;
+  return ctx ? get_id(ctx, id) : CUDA_SUCCESS;
+}
 
 int scratch_address(unsigned char** out) {
   int dev = 0;
@@ -91,12 +128,17 @@ int scratch_address(unsigned char** out) {
   if (e != cudaSuccess) return api_fail(MOE_ECUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return api_fail(MOE_EUNSUPPORTED, "device ordinal beyond the no-alloc quantizer's table (64)");
+  unsigned long long id = 0;  // 0 before the runtime's first call on this thread
+  if (current_context_id(&id) != CUDA_SUCCESS) return api_fail(MOE_ECUDA, "context query failed");
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!id || !g_scratch_addr[dev] || g_scratch_ctx_id[dev] != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the primary context current
     if (e != cudaSuccess || !p) return api_fail(MOE_ECUDA, cudaGetErrorString(e));
+    if (!id && (current_context_id(&id) != CUDA_SUCCESS || !id))
+      return api_fail(MOE_ECUDA, "no current CUDA context");
     g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+    g_scratch_ctx_id[dev] = id;
   }
   *out = g_scratch_addr[dev];
   return MOE_OK;
@@ -117,7 +159,7 @@ extern "C" int moe_nvfp4_quantize_noalloc(const float* v, int64_t rows, int64_t 
                     "(16384 chunks of 65536); use moe_nvfp4_quantize");
   if (reinterpret_cast<uintptr_t>(v) % 16 || reinterpret_cast<uintptr_t>(codes) % 8 ||
       reinterpret_cast<uintptr_t>(sg) % 4)
-    return api_fail(MOE_EINVAL, "v must be 16-byte and codes 8-byte aligned");
+    return api_fail(MOE_EINVAL, "v must be 16-byte, codes 8-byte and sg 4-byte aligned");
   unsigned char* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != MOE_OK) return rc;

@@ -75,3 +75,43 @@ def test_noalloc_quantizer_rejects_tensors_beyond_its_scratch():
     assert rc == moe.MOE_OK
     torch.cuda.synchronize()
     assert float(sg.item()) == 0.0
+
+
+def test_noalloc_quantizer_many_chunks_ragged_tail():
+    """More chunks than the last CTA's threads (300 full chunks of 65536 and a
+    ragged 16-element tail): the final reduction's strided loop takes several
+    partials per thread.  Bit for bit with moe_nvfp4_quantize, twice in a row."""
+    import speculative_decode_routed_gb300 as moe
+    n = 300 * 65536 + 16
+    g = torch.Generator(device="cuda").manual_seed(11)
+    v = torch.randn(n // 16, 16, generator=g, device="cuda") * 3.0
+    v[-1, 5] = 77.0          # the tensor's max |v| sits in the ragged last chunk
+    for _ in range(2):
+        got = _with_noalloc(moe, v)
+        ref = _with_existing(moe, v)
+        torch.cuda.synchronize()
+        for a, b, what in zip(got, ref, ("codes", "block scales", "tensor scale")):
+            assert torch.equal(a, b), f"{what} differ from moe_nvfp4_quantize"
+    assert float(got[2].item()) == np.float32(77.0) / np.float32(2688.0)
+
+
+def test_noalloc_quantizer_rejects_misaligned_pointers():
+    """v off its 16-byte alignment, codes off 8 and sg off 4 are each rejected
+    before any launch with MOE_EINVAL."""
+    import speculative_decode_routed_gb300 as moe
+    v = torch.zeros(2, 64, dtype=torch.float32, device="cuda")
+    codes = torch.zeros(2 * 32 + 8, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(2 * 4, dtype=torch.uint8, device="cuda")
+    sg = torch.zeros(4, dtype=torch.float32, device="cuda")
+    lib = moe.lib()
+    vp = ctypes.c_void_p
+    base = (vp(v.data_ptr()), vp(codes.data_ptr()), vp(sf.data_ptr()), vp(sg.data_ptr()))
+    for i, shift in ((0, 4), (1, 4), (3, 2)):
+        args = list(base)
+        args[i] = vp(args[i].value + shift)
+        rc = lib.moe_nvfp4_quantize_noalloc(args[0], 1, 16, args[1], args[2], args[3], None)
+        assert rc == moe.MOE_EINVAL, f"pointer {i} off by {shift} bytes: rc {rc}"
+        assert b"aligned" in lib.moe_decode_error_message()
+    rc = lib.moe_nvfp4_quantize_noalloc(*base[:1], 1, 16, *base[1:], None)
+    assert rc == moe.MOE_OK
+    torch.cuda.synchronize()
