@@ -74,11 +74,27 @@ enum {
   MOE_EINVAL = -1,        /* a null / misaligned pointer or an out-of-range argument */
   MOE_EUNSUPPORTED = -2,  /* a shape or device this library does not serve */
   MOE_ECUDA = -3,         /* a CUDA runtime call failed */
-  MOE_ENOMEM = -4,        /* the workspace could not be allocated */
+  MOE_ENOMEM = -4,        /* device memory (workspace, weight copies) could not be allocated */
   MOE_EDEVICE = -5        /* a device-side check latched an error */
 };
 
 typedef struct moe_decode_s moe_decode_t;
+
+/* How a handle reads the expert codes (w13, w2) of moe_layer_weights.  The
+ * block scales (w13_sf, w2_sf) are row-major in every case.
+ *   MOE_CODES_ROW_MAJOR   the codes as laid out above, read in place.
+ *   MOE_CODES_TILED       the caller's w13 / w2 already hold the codes in
+ *                         16 KB tiles (moe_tile_codes), read in place: each
+ *                         TMA copy of the experts kernel is then one
+ *                         contiguous read (about 3 % faster at serving widths
+ *                         than the row-major codes).  Tensor-core build only.
+ *   MOE_CODES_TILED_COPY  the caller passes row-major codes and the handle
+ *                         makes and keeps its own tiled copy, as many bytes
+ *                         again as the codes; if that memory cannot be
+ *                         allocated, create fails with MOE_ENOMEM.
+ *                         Tensor-core build only.
+ * The results are the same, bit for bit, whichever layout is read. */
+enum { MOE_CODES_ROW_MAJOR = 0, MOE_CODES_TILED = 1, MOE_CODES_TILED_COPY = 2 };
 
 typedef struct {
   int hidden;     /* H */
@@ -88,6 +104,7 @@ typedef struct {
   int max_rows;   /* largest b any call will use */
   int n_layers;   /* L */
   float eps;      /* RMSNorm epsilon */
+  int code_layout; /* MOE_CODES_*: how w13 and w2 are laid out (0: row-major) */
 } moe_decode_dims;
 
 typedef struct {
@@ -95,9 +112,9 @@ typedef struct {
   const float* w_pre;         /* [H]  norm weight of the stream -> MoE input */
   const uint16_t* router_w;   /* bf16 [E][H] */
   const float* router_bias;   /* [E] additive logit bias, or NULL */
-  const uint8_t* w13;         /* e2m1x2 [E][2I][H/2] */
+  const uint8_t* w13;         /* e2m1x2 [E][2I][H/2], or its tiles (MOE_CODES_TILED) */
   const uint8_t* w13_sf;      /* e4m3 [E][2I][H/16] */
-  const uint8_t* w2;          /* e2m1x2 [E][H][I/2] */
+  const uint8_t* w2;          /* e2m1x2 [E][H][I/2], or its tiles (MOE_CODES_TILED) */
   const uint8_t* w2_sf;       /* e4m3 [E][H][I/16] */
   const float* w_gscale;      /* [E][3] */
 } moe_layer_weights;
@@ -131,11 +148,9 @@ typedef struct {
  * w_post_final / w_final: [H] norm weights of the final boundary (may be
  * NULL if moe_decode_final / _step are never called).  The tensor-core build
  * also keeps, per layer, the weight scales rearranged for the tensor cores
- * (1/8 of the code bytes) and, when the device memory is there, a copy of
- * the expert codes in 16 KB tiles (as many bytes as the codes), which the
- * experts kernel then streams instead of the row-major codes; the results
- * are the same either way.  The caller keeps its weights alive until
- * destroy. */
+ * (1/8 of the code bytes) and, with MOE_CODES_TILED_COPY, a tiled copy of
+ * the expert codes (as many bytes as the codes; MOE_ENOMEM if it cannot be
+ * allocated).  The caller keeps its weights alive until destroy. */
 int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* layers,
                       const float* w_post_final, const float* w_final, moe_decode_t** out);
 
@@ -214,11 +229,53 @@ int moe_decode_debug(moe_decode_t* h, moe_decode_debug_view* out);
  * else MOE_OK. */
 int moe_decode_last_error(moe_decode_t* h);
 
+/* The limit of every bounded wait in the handle's kernels (default 2 s):
+ * a wait that runs this long gives up, the kernel latches the wait-timeout
+ * code (moe_decode_last_error: MOE_EDEVICE, "device-side error 1"), lets its
+ * copies in flight land, frees its tensor memory and returns.  limit_ns in
+ * [1000, 6e10].  Synchronizes the device and drops the handle's cached
+ * graphs (they hold the old limit; they are captured again on next use).
+ * Not capturable. */
+int moe_decode_set_wait_limit(moe_decode_t* h, uint64_t limit_ns);
+
+/* Self-test of that give-up path, with no fault: one layer-step of layer 0
+ * (as moe_decode_layer) whose experts kernel never publishes a finished
+ * expert to its down phase, so every down item's wait for its expert runs
+ * to the wait limit and gives up.  The layer's expert outputs are then left
+ * unwritten; the stream is updated by the boundary as usual.  Expect
+ * moe_decode_last_error to report MOE_EDEVICE (wait timeout) afterwards;
+ * the handle stays usable and the next step computes normally.  Tensor-core
+ * build only (MOE_EUNSUPPORTED otherwise).  Asynchronous on cuda_stream. */
+int moe_decode_selftest_wait_timeout(moe_decode_t* h, int rows, const uint16_t* branch,
+                                     float* stream, void* cuda_stream);
+
 /* Bytes of device workspace (activations, routing and scratch) the handle
- * holds.  The rearranged weight copies it also holds are not counted: the
- * scale atoms, 1/8 of the expert code bytes, and the tiled codes, as many
- * bytes as the codes when they could be allocated. */
+ * holds.  The rearranged weight copies it also holds are not counted (see
+ * moe_decode_weight_copy_bytes). */
 size_t moe_decode_workspace_bytes(const moe_decode_t* h);
+
+/* Bytes of rearranged weight copies the handle holds: the scale atoms of the
+ * tensor-core build (1/8 of the expert code bytes) and, with
+ * MOE_CODES_TILED_COPY, the tiled copy of the codes (as many bytes as the
+ * codes).  0 for a null handle. */
+size_t moe_decode_weight_copy_bytes(const moe_decode_t* h);
+
+/* The tiled layout of expert codes (MOE_CODES_TILED).  A code tensor of
+ * `rows` rows of `row_bytes` bytes (w13: rows = E * 2I, row_bytes = H/2;
+ * w2: rows = E * H, row_bytes = I/2) becomes
+ *   tiles [rows / 128][ceil(row_bytes / 128)][128 rows][128 bytes]
+ * (row tile outermost, then the 128-byte K-block), the bytes of a last
+ * partial K-block beyond row_bytes zero.  Every expert's tiles are
+ * contiguous: expert e's start at e * (rows_per_expert / 128) *
+ * ceil(row_bytes / 128) * 16384 bytes.
+ * moe_tiled_code_bytes returns the tiled size in bytes, or a negative MOE_E*
+ * code if rows is not a positive multiple of 128 or row_bytes not a positive
+ * multiple of 16.  moe_tile_codes writes the tiles of src (row-major, 16-byte
+ * aligned) into dst (16-byte aligned, moe_tiled_code_bytes bytes, not
+ * overlapping src); asynchronous on cuda_stream. */
+int64_t moe_tiled_code_bytes(int64_t rows, int64_t row_bytes);
+int moe_tile_codes(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst,
+                   void* cuda_stream);
 
 /* Number of kernels one moe_decode_step of max_rows rows launches: per layer
  * the boundary, the router and the experts, plus the routing kernel beyond 8
@@ -256,7 +313,11 @@ int moe_nvfp4_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* code
  *     MOE_EUNSUPPORTED before anything is launched.
  *   - The first call on each device looks up the scratch's device address
  *     (with that device current); make that first call before any stream
- *     capture on the device.
+ *     capture on the device.  The address is kept with the unique ID of the
+ *     context it was taken in: after a device reset (cudaDeviceReset, or a
+ *     reset of the primary context) the next call looks it up again, and
+ *     that call too should come before any capture.
+ *   - v must be 16-byte, codes 8-byte and sg 4-byte aligned (MOE_EINVAL).
  *   - Every call on a device shares the one scratch array, which keeps the
  *     last call's contents (the call clears what must start at zero).  Calls
  *     that can overlap on the GPU -- on different streams, or from host

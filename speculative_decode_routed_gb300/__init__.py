@@ -17,12 +17,16 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
 
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOMEM, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
+# moe_decode_dims.code_layout
+MOE_CODES_ROW_MAJOR, MOE_CODES_TILED, MOE_CODES_TILED_COPY = 0, 1, 2
 
 # Every symbol include/moe_decode.h declares.
 EXPORTS = (
     "moe_decode_create", "moe_decode_layer", "moe_decode_final", "moe_decode_front", "moe_decode_step",
     "moe_decode_step_graph", "moe_decode_step_host", "moe_decode_layer_profile", "moe_decode_debug",
-    "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_step_kernel_count",
+    "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_weight_copy_bytes",
+    "moe_decode_step_kernel_count", "moe_tiled_code_bytes", "moe_tile_codes",
+    "moe_decode_set_wait_limit", "moe_decode_selftest_wait_timeout",
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
@@ -42,7 +46,7 @@ class MoeError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("inter", ctypes.c_int), ("max_rows", ctypes.c_int), ("n_layers", ctypes.c_int),
-                ("eps", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("code_layout", ctypes.c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -108,6 +112,11 @@ def _lib():
             "moe_decode_debug": (i32, [vp, ctypes.POINTER(DebugView)]),
             "moe_decode_last_error": (i32, [vp]),
             "moe_decode_workspace_bytes": (ctypes.c_size_t, [vp]),
+            "moe_decode_weight_copy_bytes": (ctypes.c_size_t, [vp]),
+            "moe_tiled_code_bytes": (i64, [i64, i64]),
+            "moe_tile_codes": (i32, [vp, i64, i64, vp, vp]),
+            "moe_decode_set_wait_limit": (i32, [vp, ctypes.c_uint64]),
+            "moe_decode_selftest_wait_timeout": (i32, [vp, i32, vp, vp, vp]),
             "moe_decode_step_kernel_count": (i32, [vp]),
             "moe_decode_destroy": (None, [vp]),
             "moe_decode_strerror": (ctypes.c_char_p, [i32]),
@@ -224,6 +233,24 @@ def moe_decode_workspace_bytes(h) -> int:
     return _lib().moe_decode_workspace_bytes(h)
 
 
+def moe_decode_weight_copy_bytes(h) -> int:
+    return _lib().moe_decode_weight_copy_bytes(h)
+
+
+def moe_tiled_code_bytes(rows, row_bytes) -> int:
+    n = _lib().moe_tiled_code_bytes(rows, row_bytes)
+    _check(min(n, 0), "moe_tiled_code_bytes")
+    return n
+
+
+def moe_tile_codes(src, dst, stream=None):
+    """src u8 CUDA tensor [rows, row_bytes] (row-major codes) -> dst u8 CUDA
+    tensor of moe_tiled_code_bytes(rows, row_bytes) bytes (the 16 KB tiles)."""
+    rows, row_bytes = src.shape
+    _check(_lib().moe_tile_codes(_ptr(src), rows, row_bytes, _ptr(dst), _stream(stream)),
+           "moe_tile_codes")
+
+
 def moe_decode_step_kernel_count(h) -> int:
     return _lib().moe_decode_step_kernel_count(h)
 
@@ -259,9 +286,9 @@ class LayerTensors:
     w_pre: object
     router_w: object          # bf16 [E, H]
     router_bias: object       # fp32 [E] or None
-    w13: object               # u8 [E, 2I, H/2]
+    w13: object               # u8 [E, 2I, H/2], or its 16 KB tiles (MOE_CODES_TILED)
     w13_sf: object            # u8 [E, 2I, H/16]
-    w2: object                # u8 [E, H, I/2]
+    w2: object                # u8 [E, H, I/2], or its 16 KB tiles (MOE_CODES_TILED)
     w2_sf: object             # u8 [E, H, I/16]
     w_gscale: object          # fp32 [E, 3]
 
@@ -275,8 +302,8 @@ class MoEDecode:
     """Owns a handle over caller-owned device weights (torch tensors)."""
 
     def __init__(self, hidden, n_experts, top_k, inter, max_rows, layers, w_post_final=None,
-                 w_final=None, eps=1e-6):
-        self.dims = Dims(hidden, n_experts, top_k, inter, max_rows, len(layers), eps)
+                 w_final=None, eps=1e-6, code_layout=MOE_CODES_ROW_MAJOR):
+        self.dims = Dims(hidden, n_experts, top_k, inter, max_rows, len(layers), eps, code_layout)
         self.layers = list(layers)
         self.w_post_final, self.w_final = w_post_final, w_final
         self.handle = moe_decode_create(self.dims, [l.struct() for l in self.layers],
@@ -305,6 +332,13 @@ class MoEDecode:
 
     def debug(self) -> DebugView:
         return moe_decode_debug(self.handle)
+
+    def set_wait_limit(self, limit_ns):
+        _check(_lib().moe_decode_set_wait_limit(self.handle, int(limit_ns)), "moe_decode_set_wait_limit")
+
+    def selftest_wait_timeout(self, rows, branch, stream_buf, stream=None):
+        _check(_lib().moe_decode_selftest_wait_timeout(self.handle, rows, _ptr(branch), _ptr(stream_buf),
+                                                       _stream(stream)), "moe_decode_selftest_wait_timeout")
 
     def last_error(self) -> int:
         return moe_decode_last_error(self.handle)

@@ -119,7 +119,8 @@ struct moe_decode_s {
   std::vector<CUtensorMap> tm_w13, tm_w2;
   std::vector<uint8_t*> sfa13, sfa2;   // weight scale atoms per layer (library-owned)
   std::vector<uint8_t*> tiled13, tiled2;  // the expert codes in 16 KB tiles per layer (library-owned)
-  bool tiled = false;                  // the weight maps are over the tiles
+  bool tiled = false;                  // the weight maps are over tiles (the caller's or the copy)
+  size_t copy_bytes = 0;               // rearranged weight copies held (scale atoms, tiled codes)
   CUtensorMap tm_xpool{}, tm_xcodes{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
 };
 
@@ -391,7 +392,8 @@ int check_rows(const moe_decode_t* h, int rows) {
 }
 
 int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, float* stream,
-                 cudaStream_t s, cudaEvent_t* ev = nullptr, const float* stream_in = nullptr) {
+                 cudaStream_t s, cudaEvent_t* ev = nullptr, const float* stream_in = nullptr,
+                 bool withhold_ready = false) {
   const bool pdl = (ev == nullptr);
   auto mark = [&](int i) {
     if (ev) cudaEventRecord(ev[i], s);
@@ -463,6 +465,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   td.tiled = h->tiled;
   td.gscale = w.w_gscale;
   td.ws = h->ws;
+  tg.withhold_ready = withhold_ready ? 1 : 0;
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
                          td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
@@ -578,6 +581,10 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
   if (d.n_layers < 1 || d.n_layers > 256)
     return fail(MOE_EUNSUPPORTED, "n_layers %d outside [1, 256]", d.n_layers);
   if (!(d.eps >= 0.0f)) return fail(MOE_EINVAL, "eps must be >= 0");
+  if (d.code_layout < MOE_CODES_ROW_MAJOR || d.code_layout > MOE_CODES_TILED_COPY)
+    return fail(MOE_EINVAL, "code_layout %d is not a MOE_CODES_* value", d.code_layout);
+  if (!MOE_EXPERT_TC && d.code_layout != MOE_CODES_ROW_MAJOR)
+    return fail(MOE_EUNSUPPORTED, "the CUDA-core expert build reads row-major codes only");
   for (int i = 0; i < d.n_layers; ++i) {
     const int rc = check_layer(layers[i], i);
     if (rc) return rc;
@@ -637,6 +644,7 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     return fail(MOE_ENOMEM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
   }
   layout_workspace(h->ws, static_cast<uint8_t*>(h->ws_mem), d, h->S);
+  h->ws.wait_ns = moe::kDefaultWaitNs;
   const size_t io = (size_t)d.max_rows * d.hidden;
   e = cudaMemset(h->ws_mem, 0, h->ws_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->io_branch, io * 2);
@@ -663,14 +671,14 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     h->tm_w2.resize(d.n_layers);
     h->sfa13.assign(d.n_layers, nullptr);
     h->sfa2.assign(d.n_layers, nullptr);
+    const uint64_t n13 = E * (uint64_t)h->tgu.row_tiles * h->tgu.KBLK;  // 16 KB tiles per layer
+    const uint64_t n2 = E * (uint64_t)h->tdn.row_tiles * h->tdn.KBLK;
     for (int l = 0; l < d.n_layers && !rc; ++l) {
-      rc = encode_rows(&h->tm_w13[l], layers[l].w13, H / 2, E * 2 * I, 128);
-      if (!rc) rc = kps == 1 ? encode_rows(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128)
-                             : encode_rows_kb(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128, kps);
       const size_t b13 = (size_t)E * h->tgu.row_tiles * h->tgu.KBLK * 2048;
       const size_t b2 = (size_t)E * h->tdn.row_tiles * h->tdn.KBLK * 2048;
       if (!rc && cudaMalloc(&h->sfa13[l], b13) != cudaSuccess) rc = fail(MOE_ENOMEM, "scale atoms");
       if (!rc && cudaMalloc(&h->sfa2[l], b2) != cudaSuccess) rc = fail(MOE_ENOMEM, "scale atoms");
+      if (!rc) h->copy_bytes += b13 + b2;
       if (!rc && moe::launch_sf_atoms(layers[l].w13_sf, (int64_t)E * 2 * I, (int)(H / 16),
                                       h->tgu.KBLK, h->sfa13[l], nullptr) != cudaSuccess)
         rc = fail(MOE_ECUDA, "scale atoms launch");
@@ -678,34 +686,44 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
                                       h->sfa2[l], nullptr) != cudaSuccess)
         rc = fail(MOE_ECUDA, "scale atoms launch");
     }
-    // the expert codes in 16 KB tiles, so that each TMA box is one contiguous
-    // read; when the memory is not there the row-major maps stay
-    if (!rc) {
-      const uint64_t n13 = E * (uint64_t)h->tgu.row_tiles * h->tgu.KBLK;
-      const uint64_t n2 = E * (uint64_t)h->tdn.row_tiles * h->tdn.KBLK;
+    // The weight maps, by the layout of the codes.  Row-major codes are read
+    // in place through 2D (or, two K-blocks per down stage, 3D) maps of
+    // 128-byte x 128-row boxes; tiled codes -- the caller's, or the handle's
+    // copy -- through 3D maps whose boxes are whole 16 KB tiles, each one
+    // contiguous read.
+    h->tiled = d.code_layout != MOE_CODES_ROW_MAJOR;
+    if (!rc && d.code_layout == MOE_CODES_TILED_COPY) {
       h->tiled13.assign(d.n_layers, nullptr);
       h->tiled2.assign(d.n_layers, nullptr);
-      bool ok = true;
-      for (int l = 0; l < d.n_layers && ok; ++l)
-        ok = cudaMalloc(&h->tiled13[l], n13 * 16384) == cudaSuccess &&
-             cudaMalloc(&h->tiled2[l], n2 * 16384) == cudaSuccess;
-      if (!ok) {
-        cudaGetLastError();
-        for (uint8_t* p : h->tiled13) cudaFree(p);
-        for (uint8_t* p : h->tiled2) cudaFree(p);
-        h->tiled13.clear();
-        h->tiled2.clear();
-      }
-      for (int l = 0; l < d.n_layers && ok && !rc; ++l) {
-        if (moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w13), (int64_t)E * 2 * I, (int)(H / 2),
-                                   h->tiled13[l], nullptr) != cudaSuccess ||
-            moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w2), (int64_t)E * H, (int)(I / 2),
-                                   h->tiled2[l], nullptr) != cudaSuccess)
+      for (int l = 0; l < d.n_layers && !rc; ++l) {
+        if (cudaMalloc(&h->tiled13[l], n13 * 16384) != cudaSuccess ||
+            cudaMalloc(&h->tiled2[l], n2 * 16384) != cudaSuccess) {
+          cudaGetLastError();
+          rc = fail(MOE_ENOMEM, "the tiled copy of layer %d's expert codes (%.2f GB): %s", l,
+                    (double)(n13 + n2) * 16384.0 / 1e9,
+                    "pass MOE_CODES_ROW_MAJOR, or tile the codes once (moe_tile_codes) and pass "
+                    "MOE_CODES_TILED");
+          break;
+        }
+        h->copy_bytes += (size_t)(n13 + n2) * 16384;
+        if (moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w13), (int64_t)E * 2 * I,
+                                   (int)(H / 2), h->tiled13[l], nullptr) != cudaSuccess ||
+            moe::launch_tile_codes(static_cast<const uint8_t*>(layers[l].w2), (int64_t)E * H,
+                                   (int)(I / 2), h->tiled2[l], nullptr) != cudaSuccess)
           rc = fail(MOE_ECUDA, "code tiling launch");
-        if (!rc) rc = encode_tiles(&h->tm_w13[l], h->tiled13[l], n13, 1);
-        if (!rc) rc = encode_tiles(&h->tm_w2[l], h->tiled2[l], n2, kps);
       }
-      h->tiled = ok;
+    }
+    for (int l = 0; l < d.n_layers && !rc; ++l) {
+      if (h->tiled) {
+        const void* c13 = d.code_layout == MOE_CODES_TILED ? layers[l].w13 : h->tiled13[l];
+        const void* c2 = d.code_layout == MOE_CODES_TILED ? layers[l].w2 : h->tiled2[l];
+        rc = encode_tiles(&h->tm_w13[l], c13, n13, 1);
+        if (!rc) rc = encode_tiles(&h->tm_w2[l], c2, n2, kps);
+      } else {
+        rc = encode_rows(&h->tm_w13[l], layers[l].w13, H / 2, E * 2 * I, 128);
+        if (!rc) rc = kps == 1 ? encode_rows(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128)
+                               : encode_rows_kb(&h->tm_w2[l], layers[l].w2, I / 2, E * H, 128, kps);
+      }
     }
     if (!rc && cudaDeviceSynchronize() != cudaSuccess) rc = fail(MOE_ECUDA, "scale atoms");
     if (rc) {
@@ -947,6 +965,60 @@ int moe_decode_last_error(moe_decode_t* h) {
 }
 
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }
+
+size_t moe_decode_weight_copy_bytes(const moe_decode_t* h) { return h ? h->copy_bytes : 0; }
+
+int moe_decode_set_wait_limit(moe_decode_t* h, uint64_t limit_ns) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  if (limit_ns < 1000ull || limit_ns > 60000000000ull)
+    return fail(MOE_EINVAL, "wait limit %llu ns outside [1 us, 60 s]", (unsigned long long)limit_ns);
+  // the kernels take the limit as a launch parameter: cached graphs hold the
+  // old one, so they are dropped and captured again on their next use
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  for (GraphEntry& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  for (GraphEntry& g : h->host_graphs) cudaGraphExecDestroy(g.exec);
+  h->graphs.clear();
+  h->host_graphs.clear();
+  h->ws.wait_ns = limit_ns;
+  return MOE_OK;
+}
+
+int moe_decode_selftest_wait_timeout(moe_decode_t* h, int rows, const uint16_t* branch,
+                                     float* stream, void* cuda_stream) {
+  if (!h) return fail(MOE_EINVAL, "null handle");
+  if (!MOE_EXPERT_TC)
+    return fail(MOE_EUNSUPPORTED, "the self-test withholds the tensor-core experts kernel's ready list");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!branch || !stream || !aligned(stream, 16) || !aligned(branch, 8))
+    return fail(MOE_EINVAL, "branch (8-byte) and stream (16-byte) aligned device pointers are required");
+  return launch_layer(h, 0, rows, branch, stream, static_cast<cudaStream_t>(cuda_stream), nullptr,
+                      nullptr, true);
+}
+
+int64_t moe_tiled_code_bytes(int64_t rows, int64_t row_bytes) {
+  if (rows <= 0 || rows % 128 || row_bytes <= 0 || row_bytes % 16)
+    return fail(MOE_EINVAL, "rows must be a positive multiple of 128 and row_bytes of 16");
+  if (row_bytes > (int64_t)1 << 30 || rows / 128 > ((int64_t)1 << 31) / ((row_bytes + 127) / 128))
+    return fail(MOE_EINVAL, "code tensor too large (2^31 tiles at most)");
+  return rows / 128 * ((row_bytes + 127) / 128) * 16384;
+}
+
+int moe_tile_codes(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst,
+                   void* cuda_stream) {
+  const int64_t bytes = moe_tiled_code_bytes(rows, row_bytes);
+  if (bytes < 0) return (int)bytes;
+  if (!src || !dst) return fail(MOE_EINVAL, "src and dst are required");
+  if (!aligned(src, 16) || !aligned(dst, 16)) return fail(MOE_EINVAL, "src and dst must be 16-byte aligned");
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (s0 < d0 + (uintptr_t)bytes && d0 < s0 + (uintptr_t)(rows * row_bytes))
+    return fail(MOE_EINVAL, "src and dst overlap");
+  const cudaError_t e = moe::launch_tile_codes(src, rows, (int)row_bytes, dst,
+                                               static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "code tiling launch");
+  return MOE_OK;
+}
 
 int moe_decode_step_kernel_count(const moe_decode_t* h) {
   if (!h) return 0;

@@ -71,17 +71,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity: gives up after
-// kWaitLimitNs of wall time and returns false (the caller latches an error
-// and winds down without touching the stage).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity: gives up after limit_ns
+// of wall time (the handle's wait limit, Workspace::wait_ns) and returns
+// false (the caller latches an error and winds down without touching the
+// stage).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 0u && global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(ExpertParams p) 
     // left behind at a later barrier.  Passing the barrier also proves every
     // thread is done with item n-1, so its stage is refilled right after.
     if (tid == 0) {
-      bool got = n < issued && mbar_wait(&sm.full[s], (n / p.NS) & 1);
+      bool got = n < issued && mbar_wait(&sm.full[s], (n / p.NS) & 1, ws.wait_ns);
       if (!got) latch_error(ws.err, kDevWaitTimeout);
       *sm.ok = got ? 1 : 0;
     }
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(ExpertParams p) 
   if (tid == 0) {
     for (int s = 0; s < p.NS && s < issued; ++s) {
       const int last = s + p.NS * ((issued - 1 - s) / p.NS);
-      (void)mbar_wait(&sm.full[s], (last / p.NS) & 1);
+      (void)mbar_wait(&sm.full[s], (last / p.NS) & 1, ws.wait_ns);
     }
   }
 }

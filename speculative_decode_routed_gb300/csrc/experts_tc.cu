@@ -273,7 +273,7 @@ __device__ __forceinline__ bool tc_resolve_down(const TcParams& p, int it, int4&
     for (uint32_t i = 1;; ++i) {
       w = ld_acquire_u32(slot);
       if (w) break;
-      if ((i & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+      if ((i & 63u) == 0u && global_ns() - t0 > p.ws.wait_ns) return false;
     }
   }
   fence_proxy_async_global();
@@ -282,9 +282,9 @@ __device__ __forceinline__ bool tc_resolve_down(const TcParams& p, int it, int4&
 }
 
 // Producer side of the item ring: publish item j (bounded wait for the slot).
-__device__ __forceinline__ bool ring_put(const TcSmem& sm, int j, int4 v) {
+__device__ __forceinline__ bool ring_put(const TcSmem& sm, int j, int4 v, uint64_t limit) {
   const int r = j % kItemRing;
-  if (j >= kItemRing && !mbar_wait(&sm.item_empty[r], (uint32_t)((j / kItemRing) - 1) & 1u))
+  if (j >= kItemRing && !mbar_wait(&sm.item_empty[r], (uint32_t)((j / kItemRing) - 1) & 1u, limit))
     return false;
   sm.items[r] = v;
   mbar_arrive(&sm.item_full[r]);
@@ -292,9 +292,9 @@ __device__ __forceinline__ bool ring_put(const TcSmem& sm, int j, int4 v) {
 }
 
 // One consumer thread's read of item j.
-__device__ __forceinline__ bool ring_get(const TcSmem& sm, int j, int4& v) {
+__device__ __forceinline__ bool ring_get(const TcSmem& sm, int j, int4& v, uint64_t limit) {
   const int r = j % kItemRing;
-  if (!mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u)) return false;
+  if (!mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u, limit)) return false;
   v = sm.items[r];
   mbar_arrive(&sm.item_empty[r]);
   return true;
@@ -372,7 +372,7 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
       ws.h_amax[e] = 0u;
       const unsigned slot = atomicAdd(ws.counters + 3, (unsigned)parts);
       const unsigned cap = (unsigned)virtual_slots(p.E, p.ws_pairs);
-      for (int g = 0; g < parts; ++g)
+      for (int g = 0; g < parts && !p.withhold_ready; ++g)
         if (slot + g < cap)
           st_release_u32(ws.ready_info + slot + g,
                          pack_expert(e, pos0 + kVirtualPairs * g, min(kVirtualPairs, ne - kVirtualPairs * g)));
@@ -392,6 +392,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
                                          const CUtensorMap* tm_b, const CUtensorMap* tm_sfb,
                                          const TcSmem& sm, uint32_t tmem, int n_items, int epi0) {
   const Workspace& ws = p.ws;
+  const uint64_t lim = ws.wait_ns;  // every wait's limit
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KB = p.KBLK;      // K-blocks of 256 per item
   const int KPS = p.KPS;      // K-blocks per stage
@@ -421,7 +422,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             live = ok = false;
           }
         }
-        if (!ring_put(sm, j, live ? make_int4(it, et.x, et.y, et.z) : make_int4(-1, 0, 0, 0))) {
+        if (!ring_put(sm, j, live ? make_int4(it, et.x, et.y, et.z) : make_int4(-1, 0, 0, 0), lim)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
         }
@@ -434,7 +435,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           const int kb = ks * KPS;  // first K-block of this stage
           const int nkb = min(KPS, KB - kb);
           const int s = g % p.NS;
-          if (g >= p.NS && !mbar_wait(&sm.empty[s], ((g / p.NS) - 1) & 1)) {
+          if (g >= p.NS && !mbar_wait(&sm.empty[s], ((g / p.NS) - 1) & 1, lim)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;
@@ -486,13 +487,13 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       for (int s = 0; s < p.NS && s < g; ++s) {
         const int last = s + p.NS * ((g - 1 - s) / p.NS);
         const int fb = s * p.Q + (last % KS) % p.Q;
-        if (!mbar_wait(&sm.full[fb], ((fbits >> fb) & 1u) ^ 1u)) latch_error(ws.err, kDevWaitTimeout);
+        if (!mbar_wait(&sm.full[fb], ((fbits >> fb) & 1u) ^ 1u, lim)) latch_error(ws.err, kDevWaitTimeout);
       }
       // and the issuers' releases of every stage have arrived (no commit may
       // land on a barrier after it is re-initialised for the next projection)
       if (ok)
         for (int s = 0; s < p.NS && s < g; ++s)
-          if (!mbar_wait(&sm.empty[s], (uint32_t)((g - 1 - s) / p.NS) & 1u))
+          if (!mbar_wait(&sm.empty[s], (uint32_t)((g - 1 - s) / p.NS) & 1u, lim))
             latch_error(ws.err, kDevWaitTimeout);
     }
   } else if (warp <= p.P) {
@@ -506,7 +507,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       bool ok = true;
       for (int j = 0; ok; ++j) {
         int4 v;
-        if (!ring_get(sm, j, v)) {
+        if (!ring_get(sm, j, v, lim)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
         }
@@ -514,7 +515,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
         const int nt = (v.w + 31) / 32;
         const int ab = (p.dbuf == 2) ? (j & 1) : 0;
         const int use = (p.dbuf == 2) ? (j >> 1) : j;
-        if (use >= 1 && !mbar_wait(&sm.acc_empty[ab], (use - 1) & 1)) {
+        if (use >= 1 && !mbar_wait(&sm.acc_empty[ab], (use - 1) & 1, lim)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
         }
@@ -527,14 +528,14 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           const int s = g % p.NS;
           const uint32_t par = (fpar >> s) & 1u;
           fpar ^= 1u << s;
-          if (!mbar_wait(&sm.full[s * p.Q + q], par)) {
+          if (!mbar_wait(&sm.full[s * p.Q + q], par, lim)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;
           }
           const int slot = c % p.sfslots;
           if (c >= p.sfslots &&
-              !mbar_wait(&sm.slot_free[i * 2 + slot], ((c / p.sfslots) - 1) & 1)) {
+              !mbar_wait(&sm.slot_free[i * 2 + slot], ((c / p.sfslots) - 1) & 1, lim)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;
@@ -569,10 +570,10 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       // everything this thread issued completes before the pipeline is torn
       // down, and the commits to its scale slots have arrived
       tc_commit(&sm.drain[i]);
-      if (!mbar_wait(&sm.drain[i], 0)) latch_error(ws.err, kDevWaitTimeout);
+      if (!mbar_wait(&sm.drain[i], 0, lim)) latch_error(ws.err, kDevWaitTimeout);
       if (ok)
         for (int sl = 0; sl < p.sfslots && sl < c; ++sl)
-          if (!mbar_wait(&sm.slot_free[i * 2 + sl], (uint32_t)((c - 1 - sl) / p.sfslots) & 1u))
+          if (!mbar_wait(&sm.slot_free[i * 2 + sl], (uint32_t)((c - 1 - sl) / p.sfslots) & 1u, lim))
             latch_error(ws.err, kDevWaitTimeout);
     }
   } else if (warp >= epi0) {
@@ -591,7 +592,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       // the next item (one thread waits, bounded; the barrier hands the slot
       // and the verdict to all four warps)
       const int r = j % kItemRing;
-      if (t == 0) *sm.flag = mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u) ? 1 : 0;
+      if (t == 0) *sm.flag = mbar_wait(&sm.item_full[r], (uint32_t)(j / kItemRing) & 1u, lim) ? 1 : 0;
       tc_named_sync();
       const bool have = *reinterpret_cast<volatile int*>(sm.flag) != 0;
       const int4 v = have ? sm.items[r] : make_int4(-1, 0, 0, 0);
@@ -626,7 +627,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       }
       const int ab = (p.dbuf == 2) ? (j & 1) : 0;
       const int use = (p.dbuf == 2) ? (j >> 1) : j;
-      if (t == 0) *sm.flag = mbar_wait(&sm.acc_full[ab], use & 1) ? 1 : 0;
+      if (t == 0) *sm.flag = mbar_wait(&sm.acc_full[ab], use & 1, lim) ? 1 : 0;
       tc_named_sync();
       const bool got = *reinterpret_cast<volatile int*>(sm.flag) != 0;
       tc_named_sync();

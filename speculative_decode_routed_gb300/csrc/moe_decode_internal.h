@@ -69,7 +69,11 @@ struct Workspace {
   unsigned* counters;    // [4]         [0] router row blocks routed, [1] gate/up item claims,
                          //             [2] down item claims, [3] experts ready
   unsigned* err;         // [1]         latched DeviceError
+  unsigned long long wait_ns;  // limit of every bounded wait in the kernels (a value, not a pointer)
 };
+
+// Default of Workspace::wait_ns.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // ----------------------------------------------------------- boundary (K1)
 struct BoundaryParams {

@@ -33,8 +33,11 @@ struct TcParams {
   int ws_pairs;             // rows * k of the workspace
   int direct;               // gate/up: B is the MoE input's rows themselves (rows <= 32), not
                             // its pooled copy; each pair reads the accumulator column of its row
-  int tiled;                // 1: the weight map is over the library's tiled copy of the codes,
-                            //    [E * row_tiles * KBLK][128 rows][128 B], each box contiguous
+  int tiled;                // 1: the weight map is over tiled codes (the caller's or the
+                            //    handle's copy), [E * row_tiles * KBLK][128 rows][128 B], each
+                            //    box contiguous
+  int withhold_ready;       // self-test of the bounded waits: completed experts are not
+                            // published to the down phase, whose waits then all run out
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
   Workspace ws;
