@@ -69,6 +69,7 @@ def lib():
             "oracle_gather": (None, [ctypes.c_int] * 3 + [_vp] * 3),
             "oracle_layer_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_f64, _vp, _vp, _vp, _vp, _vp]),
             "oracle_num_threads": (ctypes.c_int, []),
+            "oracle_set_num_threads": (None, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -410,3 +411,8 @@ def layer_step(w: LayerWeights, k, eps, branch, stream, forced_ids=None):
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Host threads of the oracle's parallel loops (timing only; results do not change)."""
+    lib().oracle_set_num_threads(int(n))

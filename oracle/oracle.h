@@ -168,6 +168,7 @@ int oracle_layer_step(int rows, int H, int E, int k, int I, double eps,
                       const int32_t* forced_ids, oracle_layer_out* out);
 
 /* Number of OpenMP threads the oracle uses (for reporting). */
+void oracle_set_num_threads(int n);
 int oracle_num_threads(void);
 
 #ifdef __cplusplus
