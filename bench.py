@@ -49,17 +49,18 @@ def _peaks():
 
 
 # DRAM traffic (read + write) of the experts kernel per active expert, from
-# one ncu capture at serving widths with 64 experts; valid only for the
-# kernel source it was taken on (profiles/expert_kernel_tc_fused_E64.md).
+# one full ncu capture of that kernel at serving widths with 64 experts
+# (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by its
+# active experts); valid only for the kernel source it was taken on.
 EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu",
                    "sha256_prefix": "75a309af2ce74a27", "hidden": 7168, "inter": 2048,
                    "bytes_per_active_expert": 1069186560 / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
-# streamed gate/up projection at 8 rows, from one ncu capture
-# (profiles/dense_projections_streaming.md); valid only for the kernel
-# source it was taken on.
+# streamed gate/up projection at 8 rows, from one full ncu capture of that
+# launch at the bench's widths; valid only for the kernel source it was taken
+# on.
 DENSE_GATE_UP_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/gemv.cuh",
                          "sha256_prefix": "a919c1e476a720c4", "hidden": 7168, "inter": 28672, "rows": 8,
                          "bytes": 822260736 + 3262976}
@@ -183,48 +184,111 @@ def _barrier(ws):
         dist.barrier()
 
 
-def cpu_baseline(w: synth.Workload, n_sample_experts: int = 4):
-    """The CPU oracle, as it stands, on a bounded sample of one layer-step:
-    the boundary, router and routing of every row, and the experts of
-    `n_sample_experts` activated experts (all their pairs); the expert time is
-    scaled to the step's activated experts.  -> (us per layer-step, info)."""
+def _expected_active(w: synth.Workload) -> float:
+    """Experts a layer-step activates on average under uniform routing:
+    E * (1 - (1 - k/E)^b) (the skewed sweep activates fewer)."""
+    return w.n_experts * (1.0 - (1.0 - w.top_k / w.n_experts) ** w.rows)
+
+
+def workload_config(w: synth.Workload, ws: int) -> dict:
+    """The `config` both arms print: the workload itself (its shapes, its
+    routing, how its inputs relate to L2), not how either arm runs it."""
+    H, I = w.hidden, w.inter
+    per_expert = 3 * H * I // 2 + 3 * H * I // 16
+    gb = _expected_active(w) * per_expert / 1e9
+    if gb * 1e9 < 129e6:
+        l2 = "L2-resident: the whole layer fits in the 129 MB L2 (a correctness configuration)"
+    else:
+        l2 = ("inputs larger than L2: each layer-step's activated experts hold about %.2f GB of "
+              "weights (uniform-routing estimate), far above the 129 MB L2; 4 input draws cycled" % gb)
+    return {"workload": w.name, "rows": w.rows, "hidden": H, "n_experts": w.n_experts,
+            "top_k": w.top_k, "inter": I, "n_layers": w.n_layers, "zipf_bias": w.zipf_bias,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2}
+
+
+def moe_cpu_baseline_modules():
+    """The CPU oracle and its test-side NVFP4 packing of the generators' raw
+    expert weights: the CPU-baseline leg and the reference arm are the only
+    parts of the bench that reach them."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
-    from helpers import oracle_weights
+    from helpers import quantize_expert
+    return oracle, quantize_expert
 
-    stream, branch = synth.step_inputs(w)
-    br = oracle.bf16_to_f64(branch)
-    w_post, w_pre = synth.norm_weights(w, 0)
-    rw = synth.router_weights(w, 0)
-    bias = synth.router_bias(w, 0)
-    t0 = time.perf_counter()
-    s1, x, _ = oracle.boundary(br, stream, w_post, w_pre, w.eps)
-    r = oracle.route(x, rw, bias, w.top_k)
-    pl = oracle.pool(r["ids"], w.n_experts)
-    xc, xs, xg, _ = oracle.nvfp4_quantize(oracle.bf16_to_f64(x).astype(np.float32))
-    t_front = time.perf_counter() - t0
-    act = list(pl["active"])
-    rs = np.random.RandomState(0)
-    sample = sorted(int(e) for e in rs.choice(act, size=min(n_sample_experts, len(act)), replace=False))
-    ow = oracle_weights(w, 0, experts=sample)          # input preparation, not timed
-    from helpers import expert_subproblem
-    t_exp = 0.0
-    for e in sample:
-        p0, p1 = pl["offset"][e], pl["offset"][e + 1]
-        pairs = pl["pair_order"][p0:p1]
-        n = p1 - p0
-        sub = expert_subproblem(ow, e)
-        zi, off, order = np.zeros((n, 1), np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32)
-        t1 = time.perf_counter()
-        h = oracle.gate_up(sub, 1, xc[pairs // w.top_k], xs[pairs // w.top_k], xg, zi, off, order)
-        hq = oracle.h_quant(1, w.inter, off, h)
-        oracle.down(sub, 1, zi, off, order, hq["h_codes"], hq["h_sf"], hq["h_sg"])
-        t_exp += time.perf_counter() - t1
-    t_step = t_front + t_exp * len(act) / len(sample)
-    info = {"kind": "oracle", "cores": oracle.num_threads(),
-            "sample": f"boundary+router+routing of all {w.rows} rows; experts of {len(sample)} of "
-                      f"{len(act)} activated experts (all their pairs), scaled to {len(act)}"}
-    return t_step * 1e6, info
+
+class OracleMoE:
+    """The CPU oracle, as it stands, over the workload's layer-steps.  The
+    experts a layer-step routes to are quantized by the oracle itself (its
+    own NVFP4 packing of the host generator's raw weights) and cached: that
+    is input preparation, outside the timed calls.  A probe of the boundary
+    and the routing (also untimed) tells which experts a layer-step needs
+    before the timed oracle.layer_step runs every stage over every row and
+    every activated expert."""
+
+    def __init__(self, w: synth.Workload):
+        self.oracle, self.quantize_expert = moe_cpu_baseline_modules()
+        self.w = w
+        self.experts = {}   # (layer, expert) -> packed tensors
+        self.dense = {}     # layer -> (w_post, w_pre, router_w, bias)
+
+    def _weights(self, layer, need):
+        quantize_expert = self.quantize_expert
+        w, E = self.w, self.w.n_experts
+        if layer not in self.dense:
+            self.dense[layer] = (*synth.norm_weights(w, layer), synth.router_weights(w, layer),
+                                 synth.router_bias(w, layer))
+        for e in need:
+            if (layer, e) not in self.experts:
+                self.experts[(layer, e)] = quantize_expert(w, layer, e)
+        w13, w13_sf, w2, w2_sf = {}, {}, {}, {}
+        gscale = np.zeros((E, 3), np.float32)
+        for e in need:
+            w13[e], w13_sf[e], w2[e], w2_sf[e], gscale[e] = self.experts[(layer, e)]
+        w_post, w_pre, rw, bias = self.dense[layer]
+        return self.oracle.LayerWeights(E, w.hidden, w.inter, w_post, w_pre, rw, bias, w13, w13_sf,
+                                        w2, w2_sf, gscale)
+
+    def layer(self, layer, branch, stream):
+        """(seconds of the timed oracle.layer_step, its outputs)."""
+        o, w = self.oracle, self.w
+        if layer not in self.dense:
+            self._weights(layer, [])
+        w_post, w_pre, rw, bias = self.dense[layer]
+        _, x, _ = o.boundary(branch, stream, w_post, w_pre, w.eps)       # probe, untimed
+        need = sorted(set(int(e) for e in o.route(x, rw, bias, w.top_k)["ids"].ravel()))
+        lw = self._weights(layer, need)
+        t0 = time.perf_counter()
+        out = o.layer_step(lw, w.top_k, w.eps, branch, stream)
+        return time.perf_counter() - t0, out
+
+    def step(self, variant, layers):
+        """One step over `layers` (then the final boundary) on input draw
+        `variant` -> (seconds of the layers, seconds of the final boundary)."""
+        o, w = self.oracle, self.w
+        stream, branch = synth.step_inputs(w, variant)
+        s, br = stream, o.bf16_to_f64(branch)
+        t_layers = 0.0
+        for l in layers:
+            dt, out = self.layer(l, br, s)
+            t_layers += dt
+            s, br = out["stream"], o.gather(out["gates"], out["o"], w.top_k)
+        wpf, wf = synth.final_norm_weights(w)
+        t0 = time.perf_counter()
+        o.boundary(br, s, wpf, wf, w.eps)
+        return t_layers, time.perf_counter() - t0
+
+
+def cpu_baseline(w: synth.Workload):
+    """The CPU oracle, as it stands, on one whole layer-step (every row, every
+    activated expert) of input draw 0, and the final boundary; the weights'
+    preparation is not timed.  -> (us per layer-step, info)."""
+    om = OracleMoE(w)
+    t_layer, t_final = om.step(0, [0])
+    info = {"kind": "oracle", "cores": om.oracle.num_threads(),
+            "sample": f"one whole layer-step (layer 0, input draw 0: boundary, router, routing, pooler, "
+                      f"x quantization, every activated expert, all {w.rows} rows), no extrapolation",
+            "final_boundary_us": round(t_final * 1e6, 1)}
+    return t_layer * 1e6, info
 
 
 DENSE_METRIC = "dense draft layer µs at b=8 and weight-stream HBM GB/s vs GB300 peak"
@@ -325,21 +389,34 @@ def run_reference(args, w):
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
-    times = []
-    info = None
+    om = OracleMoE(w)
+    if args.cpu_cores:
+        om.oracle.set_num_threads(args.cpu_cores)
+    # a step is the whole step (every layer, then the final boundary) up to 8
+    # layers, cycling 4 input draws; a deeper stack is sampled one layer-step
+    # per step (layer i mod L) on one draw, so the run ends within minutes
+    whole = w.n_layers <= 8
+    variants = 4 if w.n_layers == 1 else 1
+    lay_s, fin_s, steps_s = [], [], []
     for i in range(args.warmup + args.steps):
-        us, info = cpu_baseline(w, n_sample_experts=2)
+        layers = list(range(w.n_layers)) if whole else [i % w.n_layers]
+        tl, tf = om.step(i % variants, layers)
         if i >= args.warmup:
-            times.append(us)
-    v = float(np.mean(times))
+            lay_s.append(tl / len(layers))
+            fin_s.append(tf)
+            steps_s.append(tl + tf)
+    v = float(np.mean(lay_s)) * 1e6
+    sample = ("the whole step (every layer, every row, every activated expert, the final boundary) "
+              if whole else "one layer-step per step (layer i mod %d, every row and activated expert) "
+              "and the final boundary " % w.n_layers) + "of %d input draw(s), cycled" % variants
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(v / 1000.0 * w.n_layers, 3), "higher_is_better": False,
+            "ms_per_step": round(float(np.mean(steps_s)) * 1e3, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden,
-                       "n_experts": w.n_experts, "top_k": w.top_k, "inter": w.inter,
-                       "n_layers": w.n_layers},
-            "cpu_baseline": dict(info, value=round(v, 1), unit=UNIT),
+            "config": workload_config(w, args.gpus),
+            "final_boundary_us": round(float(np.mean(fin_s)) * 1e6, 1),
+            "cpu_baseline": {"kind": "oracle", "cores": om.oracle.num_threads(), "sample": sample,
+                             "value": round(v, 1), "unit": UNIT},
             "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -397,8 +474,42 @@ def run_native(args, w):
     dec.check()
     ms = ev0.elapsed_time(ev1) / args.steps
     ms = _max_over_ranks(ms, ws, device)
-    us_layer = ms * 1000.0 / w.n_layers
     clocks = clk.summary()
+
+    # The layer-step excludes the final boundary (which closes a whole step
+    # once): the layers alone and the final boundary alone, each captured in
+    # a graph of the library's calls per input draw and timed over K replays
+    # with CUDA events on the launching stream.
+    side = torch.cuda.Stream(device)
+    side.wait_stream(cs)
+    layer_graphs, final_graphs = [], []
+    for s, b, o in bufs:
+        gl, gf = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gl, stream=side):
+            for l in range(w.n_layers):
+                dec.layer(l, rows, b if l == 0 else None, s, stream=side)
+        with torch.cuda.graph(gf, stream=side):
+            dec.final(rows, s, o, stream=side)
+        layer_graphs.append(gl)
+        final_graphs.append(gf)
+    cs.wait_stream(side)
+
+    def timed(graphs):
+        for i in range(args.warmup):
+            graphs[i % V].replay()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(cs)
+        for i in range(args.steps):
+            graphs[i % V].replay()
+        z.record(cs)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(z) / args.steps
+
+    layers_ms = _max_over_ranks(timed(layer_graphs), ws, device)
+    final_ms = _max_over_ranks(timed(final_graphs), ws, device)
+    dec.check()
+    us_layer = layers_ms * 1000.0 / w.n_layers
 
     # per-kernel durations (events on the launching stream around each kernel)
     prof, prof_bytes = [], []
@@ -416,7 +527,7 @@ def run_native(args, w):
     exp_bytes = np.array([pb["gate_up"] + (pb["down"] if fused else 0) for pb in prof_bytes], float)
     exp_gbs = exp_bytes.sum() / (prof[:, 3].sum() * 1e-3) / 1e9
     dn_gbs = None if fused else (sum(pb["down"] for pb in prof_bytes) / (prof[:, 4].sum() * 1e-3) / 1e9)
-    step_gbs = byt["total"] * w.n_layers / (ms * 1e-3) / 1e9 * ws
+    step_gbs = byt["total"] * w.n_layers / (layers_ms * 1e-3) / 1e9 * ws
 
     # the first layer's front (embedded tokens -> stream + input norm), timed
     # alone: CUDA events around 50 launches on the launching stream
@@ -459,11 +570,13 @@ def run_native(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1",
         "data": "synthetic (seeded Philox / Irwin-Hall normals, NVFP4-packed on device)",
-        "config": {"workload": w.name, "rows": rows, "hidden": w.hidden, "n_experts": w.n_experts,
-                   "top_k": w.top_k, "inter": w.inter, "n_layers": w.n_layers,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "graph": "one CUDA graph per step (layers + final boundary)",
-                   "l2": "inputs larger than L2: ~%.2f GB of expert weights per step, 4 input draws cycled" % (byt["total"] / 1e9)},
+        "config": workload_config(w, ws),
+        "timing": {"value": "us per layer-step: a graph of the step's layers (no final boundary), "
+                            "K replays, divided by the layers",
+                   "ms_per_step": "the library's step graph (every layer and the final boundary), K replays",
+                   "step_us_per_layer": round(ms * 1000.0 / w.n_layers, 2),
+                   "final_boundary_us": round(final_ms * 1000.0, 2),
+                   "bytes_per_layer_step_measured": int(byt["total"])},
         "weight_stream_gbs": round(step_gbs, 1),
         "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
         "bytes_per_layer_step": int(byt["total"]), "n_active_mean": na,
@@ -475,13 +588,16 @@ def run_native(args, w):
                      "launch_us": round(k_ms[3] * 1000, 2),
                      "algorithmic_bytes": int(exp_bytes.mean())},
         "kernels_us": dict({"boundary": round(k_ms[0] * 1000, 2), "router": round(k_ms[1] * 1000, 2),
-                            "pool": round(k_ms[2] * 1000, 2), "front": round(front_us, 2)},
+                            "pool": round(k_ms[2] * 1000, 2), "front": round(front_us, 2),
+                            "final_boundary": round(final_ms * 1000.0, 2)},
                            **({"experts": round(k_ms[3] * 1000, 2)} if fused else
                               {"gate_up": round(k_ms[3] * 1000, 2), "down": round(k_ms[4] * 1000, 2),
                                "down_gbs": round(dn_gbs, 1)})),
         "e2e": {"value": round(e2e_ms * 1000.0 / w.n_layers, 2), "unit": UNIT,
                 "h2d_bytes_per_step": rows * w.hidden * (2 + 4),
-                "d2h_bytes_per_step": rows * w.hidden * (4 + 2)},
+                "d2h_bytes_per_step": rows * w.hidden * (4 + 2),
+                "includes": "moe_decode_step_host per call divided by the layers: the host transfers "
+                            "and the final boundary are inside"},
         "gpu_launches": moe.moe_decode_step_kernel_count(dec.handle) * args.steps,
         "clocks": clocks,
     }
@@ -794,6 +910,8 @@ def main():
                     + sorted(synth.CTXKV_WORKLOADS))
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-cores", type=int, default=0,
+                    help="host threads of the oracle in the reference arm (default: all)")
     args = ap.parse_args()
     w = (synth.WORKLOADS.get(args.workload) or synth.DENSE_WORKLOADS.get(args.workload)
          or synth.CTXKV_WORKLOADS[args.workload])

@@ -88,9 +88,12 @@ def test_reference_arm_line_keeps_the_contract(workload):
     """The oracle arm's one JSON line, for each kind of workload, carries the
     keys the bench contract names, with a cpu_baseline describing the run
     and an e2e of zero host bytes."""
+    import time
+    t0 = time.perf_counter()
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload,
-                        "--steps", "1", "--warmup", "3"],
+                        "--steps", "2", "--warmup", "3"],
                        cwd=ROOT, capture_output=True, text=True, timeout=300)
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
@@ -98,10 +101,33 @@ def test_reference_arm_line_keeps_the_contract(workload):
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in rec, key
-    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["steps"] == 1 and rec["warmup"] == 3
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["steps"] == 2 and rec["warmup"] == 3
+    # the steps it claims to have timed fit inside the run (nothing extrapolated)
+    assert rec["steps"] * rec["ms_per_step"] / 1000.0 <= wall
     assert rec["value"] > 0 and rec["unit"] == "µs" and rec["higher_is_better"] is False
     assert rec["config"]["workload"] == workload
     cb = rec["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == rec["value"]
     assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
+
+
+def test_both_arms_print_the_same_config():
+    """The native arm's config and the reference arm's are one function of the
+    workload, so the two lines compare; the reference arm's line carries it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    w = synth.WORKLOADS["tiny"]
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    rec = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][0])
+    assert rec["config"] == bench.workload_config(w, 1)
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    native = src[src.index("def run_native("):src.index("def run_dense(")]
+    assert '"config": workload_config(w, ws)' in native
+    serving = bench.workload_config(synth.WORKLOADS["serving"], 1)
+    assert serving["l2"].startswith("inputs larger than L2")
+    assert bench.workload_config(w, 1)["l2"].startswith("L2-resident")

@@ -27,7 +27,8 @@ def test_header_symbols_are_exported():
 
 
 def _dims(**kw):
-    d = dict(hidden=256, n_experts=8, top_k=2, inter=128, max_rows=8, n_layers=1, eps=1e-6)
+    d = dict(hidden=256, n_experts=8, top_k=2, inter=128, max_rows=8, n_layers=1, eps=1e-6,
+             code_layout=0)
     d.update(kw)
     return moe.Dims(**d)
 
@@ -67,6 +68,33 @@ def test_null_and_misaligned_pointers():
     assert rc == moe.MOE_EINVAL and "aligned" in msg
     rc = moe.lib().moe_decode_create(None, None, None, None, None)
     assert rc == moe.MOE_EINVAL
+
+
+def test_code_layout_is_validated():
+    rc, msg = _create(_dims(code_layout=3), [_fake_layer()])
+    assert rc == moe.MOE_EINVAL and "code_layout" in msg
+    rc, msg = _create(_dims(code_layout=-1), [_fake_layer()])
+    assert rc == moe.MOE_EINVAL and "code_layout" in msg
+
+
+def test_tiled_code_sizes_and_argument_checks():
+    """moe_tiled_code_bytes follows the header's layout (whole 16 KB tiles, a
+    partial last K-block padded) and rejects shapes it cannot tile; the tiling
+    call rejects bad pointers before any launch."""
+    L = moe.lib()
+    assert L.moe_tiled_code_bytes(256 * 4096, 3584) == 256 * 4096 * 3584      # H 7168: whole tiles
+    assert L.moe_tiled_code_bytes(128, 192) == 2 * 16384                      # H 384: one and a half
+    assert L.moe_tiled_code_bytes(384, 16) == 3 * 16384
+    for rows, rb in ((100, 64), (0, 64), (128, 8), (128, 0), (-128, 64), (1 << 40, 1 << 20)):
+        assert L.moe_tiled_code_bytes(rows, rb) == moe.MOE_EINVAL, (rows, rb)
+    base = 1 << 20
+    assert L.moe_tile_codes(None, 128, 64, base, None) == moe.MOE_EINVAL
+    assert L.moe_tile_codes(base, 128, 64, None, None) == moe.MOE_EINVAL
+    assert L.moe_tile_codes(base + 8, 128, 64, base << 4, None) == moe.MOE_EINVAL
+    assert L.moe_tile_codes(base, 128, 64, base + 4096, None) == moe.MOE_EINVAL   # overlapping
+    assert b"overlap" in L.moe_decode_error_message()
+    assert L.moe_tile_codes(base, 100, 64, base << 4, None) == moe.MOE_EINVAL
+    assert L.moe_decode_weight_copy_bytes(None) == 0
 
 
 def test_calls_on_a_null_handle_fail_cleanly():

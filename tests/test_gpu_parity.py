@@ -12,7 +12,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import (bf16_near_tie, dev_array, expert_subproblem, oracle_weights, read_debug)
+from helpers import (bf16_near_tie, check_gpu_weights, dev_array, expert_subproblem, gpu_layer_weights,
+                     oracle_weights, read_debug)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -100,37 +101,16 @@ def test_device_generator_bit_exact():
 # -------------------------------------------------------- staged layer check
 
 
-def _check_weights(dec, ow, layer, experts):
-    t = dec.layers[layer]
-    for e in experts:
-        assert np.array_equal(t.w13[e].cpu().numpy(), ow.w13[e]), f"w13 codes of expert {e}"
-        assert np.array_equal(t.w13_sf[e].cpu().numpy(), ow.w13_sf[e])
-        assert np.array_equal(t.w2[e].cpu().numpy(), ow.w2[e])
-        assert np.array_equal(t.w2_sf[e].cpu().numpy(), ow.w2_sf[e])
-        assert np.array_equal(t.w_gscale[e].cpu().numpy(), ow.gscale[e])
-
-
-def staged_layer(w, dec, ow, layer, rows, branch, stream, experts="all", prev=None):
-    """Run one layer on the GPU and check every stage.  branch: bf16 CUDA tensor,
-    or None (chained: the previous layer's unpooled output, from `prev`).
-    `ow` is oracle.LayerWeights, or a function of the GPU's debug data that
-    returns (LayerWeights, experts to check) -- for sampling at full size."""
+def check_stages(w, d, ow, experts, br, s_in, s_out, rows):
+    """Every stage of one layer the GPU ran, each against the oracle's stage on
+    the GPU's own input to it.  d: the layer's debug arrays (read_debug); ow:
+    oracle.LayerWeights holding at least `experts` ("all": every active one);
+    br: the branch (fp64) the layer's boundary added; s_in / s_out: the stream
+    before and after the layer."""
     k, E, I = w.top_k, w.n_experts, w.inter
-    s_in = stream.cpu().numpy().copy()
-    dec.layer(layer, rows, branch, stream)
-    torch.cuda.synchronize()
-    dec.check()
-    d = read_debug(dec, rows)
-    if callable(ow):
-        ow, experts = ow(d)
-
     # A: dual-norm boundary
-    if branch is not None:
-        br = oracle.bf16_to_f64(branch.view(torch.uint16).cpu().numpy())
-    else:
-        br = oracle.gather(prev["gates"].astype(np.float64), prev["o"], k)
     s_ref, x_ref, xe = oracle.boundary(br, s_in, ow.w_post, ow.w_pre, w.eps)
-    _close(stream.cpu().numpy(), s_ref, 1e-5, "stream after the boundary")
+    _close(s_out, s_ref, 1e-5, "stream after the boundary")
     diff = d["x"] != x_ref
     assert not np.any(diff & ~bf16_near_tie(xe)), "MoE input differs away from bf16 near-ties"
     assert np.mean(diff) < 1e-3
@@ -167,7 +147,27 @@ def staged_layer(w, dec, ow, layer, rows, branch, stream, experts="all", prev=No
         o_ref = oracle.down(sub, 1, zi, off, order, d["h_codes"][p0:p1], d["h_sf"][p0:p1],
                             np.array([d["h_sg"][e]], np.float32))
         _close(d["o"][pairs], o_ref, STAGE_TOL, f"o of expert {e}")
+
+
+def staged_layer(w, dec, ow, layer, rows, branch, stream, experts="all", prev=None):
+    """Run one layer on the GPU and check every stage.  branch: bf16 CUDA tensor,
+    or None (chained: the previous layer's unpooled output, from `prev`).
+    `ow` is oracle.LayerWeights, or a function of the GPU's debug data that
+    returns (LayerWeights, experts to check) -- for sampling at full size."""
+    k = w.top_k
+    s_in = stream.cpu().numpy().copy()
+    dec.layer(layer, rows, branch, stream)
+    torch.cuda.synchronize()
+    dec.check()
+    d = read_debug(dec, rows)
+    if callable(ow):
+        ow, experts = ow(d)
+    if branch is not None:
+        br = oracle.bf16_to_f64(branch.view(torch.uint16).cpu().numpy())
+    else:
+        br = oracle.gather(prev["gates"].astype(np.float64), prev["o"], k)
     d["stream"] = stream.cpu().numpy().copy()
+    check_stages(w, d, ow, experts, br, s_in, d["stream"], rows)
     return d
 
 
@@ -185,10 +185,152 @@ def _final_check(w, dec, d, rows, stream):
     assert np.mean(got != out_ref) < 1e-3
 
 
-def test_tiny_layer_staged():
+def _check_weights(dec, ow, layer, experts):
+    check_gpu_weights(dec, ow, layer, experts)
+
+
+# ---------------------------------------------------------------- end to end
+
+
+def run_step_layerwise(w, dec, rows, branch, stream, out, keep_debug=()):
+    """The step as moe_decode_step launches it -- every layer, then the final
+    boundary, the same kernels in the same order -- one layer call at a time,
+    keeping each layer's routing, MoE input, gates and unpooled outputs (and
+    the whole debug view of the layers in keep_debug, with the stream around
+    them)."""
+    k, H = w.top_k, w.hidden
+    per = []
+    for l in range(w.n_layers):
+        s_in = stream.cpu().numpy().copy() if l in keep_debug else None
+        dec.layer(l, rows, branch if l == 0 else None, stream)
+        torch.cuda.synchronize()
+        if l in keep_debug:
+            d = read_debug(dec, rows)
+            d["stream_in"], d["stream"] = s_in, stream.cpu().numpy().copy()
+        else:
+            v = dec.debug()
+            d = dict(ids=dev_array(v.ids, (rows, k), np.int32), x=dev_array(v.x, (rows, H), np.uint16),
+                     gates=dev_array(v.gates, (rows, k), np.float32),
+                     o=dev_array(v.o, (rows * k, H), np.float32),
+                     n_active=int(dev_array(v.n_active, (1,), np.int32)[0]))
+            d["active"] = dev_array(v.active, (w.n_experts,), np.int32)[: d["n_active"]]
+        per.append(d)
+    s_final_in = stream.cpu().numpy().copy()
+    dec.final(rows, stream, out)
+    torch.cuda.synchronize()
+    dec.check()
+    return per, s_final_in
+
+
+def final_output_band(s_got, s_ref, wf, eps):
+    """Per element of the final output, how far its unrounded value may move
+    given the measured stream error: out = s * w / sqrt(mean(s^2) + eps), so a
+    stream error of at most E in the row moves out_h by at most
+    |w_h| * inv * E * (1 + |s_h| * inv^2 * rms) to first order (the norm's own
+    change is at most E * rms / rms^2).  Doubled for the second-order terms."""
+    s_ref = np.asarray(s_ref, np.float64)
+    E = np.max(np.abs(np.asarray(s_got, np.float64) - s_ref), axis=1, keepdims=True)
+    ms = np.mean(s_ref ** 2, axis=1, keepdims=True)
+    inv = 1.0 / np.sqrt(ms + eps)
+    return 2.0 * np.abs(np.asarray(wf, np.float64))[None, :] * inv * E * (1.0 + np.abs(s_ref) * inv ** 2 * np.sqrt(ms))
+
+
+def check_final_output(got, out_ref, exact, band, what="final output"):
+    """bf16 output bits against the oracle's: equal except where the oracle's
+    unrounded value lies within R19's band plus `band` of a rounding midpoint,
+    and there by exactly one bf16 step."""
+    diff = got != out_ref
+    off = diff & ~bf16_near_tie(exact, band=band)
+    assert not np.any(off), f"{what}: {int(off.sum())} elements differ away from rounding midpoints"
+    steps = np.abs(got.astype(np.int32) - out_ref.astype(np.int32))[diff]
+    assert steps.size == 0 or steps.max() <= 1, f"{what}: a near-tie element is {steps.max()} steps off"
+
+
+def end_to_end(w, dec, rows, variant=0, sample_layers=None, n_sample=1, stage_layers=()):
+    """One whole step on the GPU (every layer and the final boundary) against
+    the oracle run layer by layer on its own stream with the GPU's expert ids
+    (R14), over every active expert, with the experts' NVFP4 weights as the
+    GPU packed them (a sample per layer checked bit for bit against the
+    oracle's own packing).  Asserts:
+      - at every layer, the oracle's routing of the GPU's MoE input gives the
+        GPU's ids on every unflagged row (bit for bit);
+      - the oracle's own routing of its own MoE input agrees with the GPU's
+        ids on every unflagged row whose input is bitwise the GPU's;
+      - the final fp32 stream within STREAM_TOL * rms(stream);
+      - the bf16 output equal except at rounding midpoints (the band derived
+        from the measured stream error), one step at most;
+      - the layers in stage_layers pass every staged check on a sample.
+    Returns the per-layer report (rows agreeing, flagged, inputs differing)."""
+    k = w.top_k
+    stream, branch = _sgpu().step_tensors(w.with_rows(rows) if rows != w.rows else w, variant)
+    out = torch.empty_like(branch)
+    per, s_final_in = run_step_layerwise(w, dec, rows, branch, stream, out, keep_debug=stage_layers)
+    s_host, b_host = synth.step_inputs(w.with_rows(rows) if rows != w.rows else w, variant)
+    s, br = s_host, oracle.bf16_to_f64(b_host)
+    report = []
+    sample_layers = range(w.n_layers) if sample_layers is None else sample_layers
+    for l in range(w.n_layers):
+        g = per[l]
+        ow = gpu_layer_weights(dec, w, l, g["active"])
+        if l in sample_layers:
+            hot = sorted(set(int(e) for e in g["active"][:: max(1, len(g["active"]) // n_sample)][:n_sample]))
+            check_gpu_weights(dec, oracle_weights(w, l, experts=hot), l, hot)
+        if l in stage_layers:
+            d = per[l]
+            prev_br = None if l == 0 else oracle.gather(per[l - 1]["gates"].astype(np.float64),
+                                                        per[l - 1]["o"], k)
+            picks = sorted(set([int(max(d["active"], key=lambda e: d["count"][e]))]
+                               + [int(e) for e in d["active"][:1]]))
+            check_gpu_weights(dec, oracle_weights(w, l, experts=picks), l, picks)
+            check_stages(w, d, ow, picks, oracle.bf16_to_f64(b_host) if l == 0 else prev_br,
+                         d["stream_in"], d["stream"], rows)
+        # the oracle's routing on the GPU's own MoE input: the GPU's ids (staged, bit for bit)
+        rg = oracle.route(g["x"], ow.router_w, ow.router_bias, k)
+        okg = rg["flags"] == 0
+        assert np.array_equal(rg["ids"][okg], g["ids"][okg]), f"layer {l}: ids on the GPU's input"
+        o = oracle.layer_step(ow, k, w.eps, br, s, forced_ids=g["ids"])
+        own = oracle.route(o["x"], ow.router_w, ow.router_bias, k)
+        same_x = np.all(o["x"] == g["x"], axis=1)
+        agree = np.all(own["ids"] == g["ids"], axis=1)
+        flagged = own["flags"] != 0
+        assert np.all(agree | flagged | ~same_x), f"layer {l}: ids differ on an unflagged row"
+        report.append(dict(layer=l, rows=rows, agree=int(agree.sum()), flagged=int(flagged.sum()),
+                           x_differs=int((~same_x).sum()), n_active=len(g["active"])))
+        s = o["stream"]
+        br = oracle.gather(o["gates"], o["o"], k)
+    wpf, wf = synth.final_norm_weights(w)
+    s_gpu = stream.cpu().numpy()
+    out_gpu = out.view(torch.uint16).cpu().numpy()
+    # the final boundary staged: the oracle's on the GPU's last gather and stream
+    y = oracle.gather(per[-1]["gates"].astype(np.float64), per[-1]["o"], k)
+    fs_ref, fo_ref, fe = oracle.boundary(y, s_final_in, wpf, wf, w.eps)
+    _close(s_gpu, fs_ref, 1e-5, "stream after the final boundary (staged)")
+    check_final_output(out_gpu, fo_ref, fe, None, "final output (staged)")
+    # end to end
+    s_ref, out_ref, oe = oracle.boundary(br, s, wpf, wf, w.eps)
+    err = float(np.max(np.abs(s_gpu.astype(np.float64) - s_ref)))
+    bound = STREAM_TOL * _rms(s_ref)
+    assert err <= bound, f"end-to-end stream max|err| {err:.3e} > {bound:.3e}"
+    check_final_output(out_gpu, out_ref, oe, final_output_band(s_gpu, s_ref, wf, w.eps))
+    for r in report:
+        r["stream_err_over_rms"] = err / _rms(s_ref)
+    print(f"{w.name} b={rows}: end-to-end stream max|err| / rms = {err / _rms(s_ref):.3e}; per layer "
+          + "; ".join(f"L{r['layer']}: {r['agree']}/{rows} ids agree, {r['flagged']} flagged, "
+                      f"{r['x_differs']} inputs differ, {r['n_active']} experts" for r in report))
+    return report, stream, out
+
+
+LAYOUTS = {"row_major": 0, "tiled": 1, "tiled_copy": 2}   # moe_decode_dims.code_layout
+
+
+@pytest.mark.parametrize("layout", sorted(LAYOUTS))
+def test_tiny_layer_staged(layout):
+    """Every stage of one tiny layer, with the expert codes read in each
+    layout: row-major in place, the caller's tiles in place, the handle's
+    tiled copy."""
     w = synth.WORKLOADS["tiny"]
     sgpu = _sgpu()
-    dec = sgpu.build(w)
+    dec = sgpu.build(w, layout=LAYOUTS[layout])
     ow = oracle_weights(w, 0)
     _check_weights(dec, ow, 0, range(w.n_experts))
     stream, branch = sgpu.step_tensors(w)
@@ -209,8 +351,8 @@ def _oracle_step(w, variant=0, experts_needed=None):
         s = o["stream"]
         br = oracle.gather(o["gates"], o["o"], w.top_k)
     wpf, wf = synth.final_norm_weights(w)
-    s, out, _ = oracle.boundary(br, s, wpf, wf, w.eps)
-    return s, out, outs
+    s, out, oe = oracle.boundary(br, s, wpf, wf, w.eps)
+    return s, out, oe, outs
 
 
 def test_tiny_step_end_to_end_graph_and_host():
@@ -218,7 +360,7 @@ def test_tiny_step_end_to_end_graph_and_host():
     w = synth.WORKLOADS["tiny"]
     sgpu = _sgpu()
     dec = sgpu.build(w)
-    s_ref, out_ref, outs = _oracle_step(w)
+    s_ref, out_ref, oe, outs = _oracle_step(w)
     # eager
     stream, branch = sgpu.step_tensors(w)
     out = torch.empty_like(branch)
@@ -231,7 +373,8 @@ def test_tiny_step_end_to_end_graph_and_host():
     eager_stream, eager_out = stream.cpu().numpy(), out.view(torch.uint16).cpu().numpy()
     err = np.abs(eager_stream - s_ref).max()
     assert err <= STREAM_TOL * _rms(s_ref), f"end-to-end stream max|err| {err:.3e}"
-    assert np.mean(eager_out != out_ref) < 0.02
+    check_final_output(eager_out, out_ref, oe,
+                       final_output_band(eager_stream, s_ref, synth.final_norm_weights(w)[1], w.eps))
     # graph replay is bitwise the eager result, twice in a row
     for _ in range(2):
         stream2, branch2 = sgpu.step_tensors(w)
@@ -289,6 +432,69 @@ def test_repeated_replays_bitwise():
     dec.check()
     assert bad == 0, f"{bad} replays differ from the eager result"
     dec.close()
+
+
+def test_bounded_wait_gives_up_and_the_handle_recovers():
+    """The experts kernel's give-up path, with no fault: with a 1 ms wait
+    limit, a layer whose completed experts are never published to the down
+    phase makes every down item's wait run out.  The call returns within the
+    limit's order (the default 2 s would not have given up yet), the latched
+    code reads as a wait timeout and is cleared by reading it, and the next
+    steps -- eager and graph, under the short limit and the default -- give
+    the reference result bit for bit."""
+    import time
+
+    import speculative_decode_routed_gb300 as moe
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    s0 = stream.clone()
+    out = torch.empty_like(branch)
+    dec.step(w.rows, branch, stream, out)
+    torch.cuda.synchronize()
+    dec.check()
+    ref_s, ref_o = stream.clone(), out.clone()
+    dec.set_wait_limit(1_000_000)
+    s1 = s0.clone()
+    t0 = time.perf_counter()
+    dec.selftest_wait_timeout(w.rows, branch, s1)
+    rc = dec.last_error()
+    elapsed = time.perf_counter() - t0
+    assert rc == moe.MOE_EDEVICE, f"expected a latched wait timeout, got {rc}"
+    assert b"error 1 " in moe.lib().moe_decode_error_message()
+    assert elapsed < 1.0, f"the self-test took {elapsed:.3f} s"
+    assert dec.last_error() == moe.MOE_OK
+    for limit in (1_000_000, 2_000_000_000):
+        dec.set_wait_limit(limit)
+        for call in (dec.step, dec.step_graph):
+            stream.copy_(s0)
+            out.zero_()
+            call(w.rows, branch, stream, out)
+            torch.cuda.synchronize()
+            dec.check()
+            assert torch.equal(stream, ref_s) and torch.equal(out, ref_o)
+    with pytest.raises(moe.MoeError):
+        dec.set_wait_limit(10)
+    dec.close()
+
+
+def test_tile_codes_matches_the_layout():
+    """moe_tile_codes against the layout its header states (untiled on the
+    host), the bytes of a partial last K-block zero."""
+    import speculative_decode_routed_gb300 as moe
+    from helpers import untile_codes
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for rows, rb in ((256, 3584), (384, 192), (128, 64), (256, 1024)):
+        src = torch.randint(0, 256, (rows, rb), dtype=torch.uint8, device="cuda", generator=g)
+        dst = torch.full((moe.moe_tiled_code_bytes(rows, rb),), 0xEE, dtype=torch.uint8, device="cuda")
+        moe.moe_tile_codes(src, dst)
+        torch.cuda.synchronize()
+        t = dst.cpu().numpy()
+        assert np.array_equal(untile_codes(t, rows, rb), src.cpu().numpy())
+        kb = -(-rb // 128)
+        tail = t.reshape(rows // 128, kb, 128, 128)[:, -1, :, rb - (kb - 1) * 128:]
+        assert not tail.any(), "bytes beyond the row in the last K-block must be zero"
 
 
 def test_graph_cache_evicts_and_recaptures():
@@ -366,9 +572,20 @@ ODD_SHAPES = [
 
 @pytest.mark.parametrize("rows,H,E,k,I", ODD_SHAPES)
 def test_odd_shapes_staged(rows, H, E, k, I):
+    _odd_shape(rows, H, E, k, I, LAYOUTS["tiled"])
+
+
+@pytest.mark.parametrize("rows,H,E,k,I", [ODD_SHAPES[0], ODD_SHAPES[4], ODD_SHAPES[5]])
+def test_odd_shapes_row_major_codes(rows, H, E, k, I):
+    """The row-major weight maps (read in place) on a ragged H and I (a last
+    K-block half filled) and on experts split into several 32-pair parts."""
+    _odd_shape(rows, H, E, k, I, LAYOUTS["row_major"])
+
+
+def _odd_shape(rows, H, E, k, I, layout):
     w = synth.Workload(f"odd{H}", rows=rows, hidden=H, n_experts=E, top_k=k, inter=I)
     sgpu = _sgpu()
-    dec = sgpu.build(w)
+    dec = sgpu.build(w, layout=layout)
     ow = oracle_weights(w, 0)
     stream, branch = sgpu.step_tensors(w)
     d = staged_layer(w, dec, ow, 0, rows, branch, stream)
@@ -416,58 +633,72 @@ def _staged_full(w, dec, layer, rows, branch, stream, n_extra=2, prev=None):
     return staged_layer(w, dec, pick, layer, rows, branch, stream, prev=prev)
 
 
-@pytest.mark.slow
-def test_serving_width_layer_sampled():
-    """One layer at serving width (H 7168, 256 experts, top-8, I 2048, b 8): the
-    bench's configuration and launch path."""
-    w = synth.WORKLOADS["serving"]
+def _graph_equals_eager(w, dec, rows, variant=1):
+    """The library's captured step replays bit for bit what the eager step computes."""
     sgpu = _sgpu()
-    dec = sgpu.build(w)
-    stream, branch = sgpu.step_tensors(w)
-    d = _staged_full(w, dec, 0, w.rows, branch, stream)
-    _final_check(w, dec, d, w.rows, stream)
-    # the graph-replayed step matches the eager step bit for bit
-    s1, b1 = sgpu.step_tensors(w, variant=1)
+    wr = w.with_rows(rows) if rows != w.rows else w
+    s1, b1 = sgpu.step_tensors(wr, variant=variant)
     o1 = torch.empty_like(b1)
-    dec.step(w.rows, b1, s1, o1)
-    s2, b2 = sgpu.step_tensors(w, variant=1)
+    dec.step(rows, b1, s1, o1)
+    s2, b2 = sgpu.step_tensors(wr, variant=variant)
     o2 = torch.empty_like(b2)
-    dec.step_graph(w.rows, b2, s2, o2)
+    dec.step_graph(rows, b2, s2, o2)
     torch.cuda.synchronize()
-    assert torch.equal(s1, s2) and torch.equal(o1, o2)
+    dec.check()
+    assert torch.equal(s1, s2) and torch.equal(o1, o2), "graph replay differs from the eager step"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("layout", ["tiled", "row_major"])
+def test_serving_end_to_end(layout):
+    """One layer at serving width (H 7168, 256 experts, top-8, I 2048, b 8), the
+    bench's configuration and launch path: every active expert end to end
+    against the oracle, the layer's stages on a sample, the final boundary,
+    and the graph replay against the eager step."""
+    w = synth.WORKLOADS["serving"]
+    dec = _sgpu().build(w, layout=LAYOUTS[layout])
+    end_to_end(w, dec, w.rows, stage_layers=(0,))
+    _graph_equals_eager(w, dec, w.rows)
     dec.close()
 
 
 @pytest.mark.slow
-def test_chained_layers_sampled():
-    """Eight chained layers (H 5120, 128 experts, top-8, I 1536): each layer's
-    stages checked on a sample, the chained gather included, then the graph."""
+def test_chained_layers_end_to_end():
+    """Eight chained layers (H 5120, 128 experts, top-8, I 1536): the whole
+    step end to end against the oracle, every layer's stages on a sample (the
+    chained gather included), and the graph."""
     w = synth.WORKLOADS["chained8"]
-    sgpu = _sgpu()
-    dec = sgpu.build(w)
-    stream, branch = sgpu.step_tensors(w)
-    prev = None
-    for l in range(w.n_layers):
-        prev = _staged_full(w, dec, l, w.rows, branch if l == 0 else None, stream, n_extra=1,
-                            prev=prev)
-    _final_check(w, dec, prev, w.rows, stream)
-    eager_stream = stream.clone()
-    s2, b2 = sgpu.step_tensors(w)
-    o2 = torch.empty_like(b2)
-    dec.step_graph(w.rows, b2, s2, o2)
-    torch.cuda.synchronize()
-    assert torch.equal(s2, eager_stream)
+    dec = _sgpu().build(w)
+    end_to_end(w, dec, w.rows, stage_layers=tuple(range(w.n_layers)))
+    _graph_equals_eager(w, dec, w.rows)
     dec.close()
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("rows", synth.SWEEP_ROWS)
-def test_batch_skew_sweep_sampled(rows):
+def test_batch_skew_sweep_end_to_end(rows):
     """H 7168, 256 experts, top-8, I 2048 with a Zipf(1.1) logit bias, b in
-    {1, 8, 32, 64, 128}; the hottest expert (most rows) is always checked."""
+    {1, 8, 32, 64, 128}: end to end over every active expert, the stages on a
+    sample (the hottest expert included)."""
     w = synth.WORKLOADS["sweep"].with_rows(rows)
-    sgpu = _sgpu()
-    dec = sgpu.build(w)
-    stream, branch = sgpu.step_tensors(w)
-    _staged_full(w, dec, 0, rows, branch, stream, n_extra=1)
+    dec = _sgpu().build(w)
+    end_to_end(w, dec, rows, stage_layers=(0,))
+    dec.close()
+
+
+@pytest.mark.slow
+def test_stack16_end_to_end():
+    """The 16-layer stack at serving widths (about 101.5 GB of NVFP4 weights,
+    generated on the device), b 8, the codes held once in tiles: the whole
+    step end to end against the oracle, three layers' stages on a sample, and
+    the graph replay against the eager step."""
+    import speculative_decode_routed_gb300 as moe
+    w = synth.WORKLOADS["stack16"]
+    dec = _sgpu().build(w)
+    H, I, E = w.hidden, w.inter, w.n_experts
+    codes = E * (2 * I * H // 2 + H * I // 2)
+    # the handle holds only the scale atoms (1/8 of the code bytes), no copy of the codes
+    assert moe.moe_decode_weight_copy_bytes(dec.handle) <= w.n_layers * codes // 8 + (1 << 20)
+    end_to_end(w, dec, w.rows, sample_layers=(0, 8, 15), stage_layers=(0, 8, 15))
+    _graph_equals_eager(w, dec, w.rows)
     dec.close()

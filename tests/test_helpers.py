@@ -103,3 +103,34 @@ def test_bits_match_counts_and_sizes_the_other_differences():
     excl = np.zeros(ref.shape, bool)
     excl[away[0]] = True
     bits_match(got, ref, exact, "excluded", exclude=excl)
+
+
+def test_untile_inverts_the_documented_tiling():
+    """untile_codes against the tiled layout written out element by element:
+    byte (r, c) of a [rows][row_bytes] code tensor sits in tile
+    (r / 128) * ceil(row_bytes / 128) + c / 128, at row r % 128, byte c % 128;
+    tile bytes beyond row_bytes are zero."""
+    from helpers import tiled_expert_bytes, untile_codes
+    rs = np.random.RandomState(0)
+    for rows, rb in ((256, 448), (128, 192), (384, 64), (128, 128)):
+        src = rs.randint(0, 256, size=(rows, rb)).astype(np.uint8)
+        kb = -(-rb // 128)
+        tiles = np.zeros(rows // 128 * kb * 16384, np.uint8)
+        for r in range(rows):
+            for c in range(rb):
+                t = (r // 128) * kb + c // 128
+                tiles[t * 16384 + (r % 128) * 128 + c % 128] = src[r, c]
+        assert np.array_equal(untile_codes(tiles, rows, rb), src)
+        assert tiles.size == tiled_expert_bytes(rows, rb)
+        # a plausible mistake -- K-block outermost -- does not pass
+        wrong = tiles.reshape(rows // 128, kb, 128, 128).transpose(1, 0, 2, 3).reshape(-1)
+        if kb > 1 and rows > 128:
+            assert not np.array_equal(untile_codes(wrong, rows, rb), src)
+
+
+def test_band_widens_the_near_tie_test():
+    from helpers import bf16_near_tie
+    x = np.array([1.0 + 2.0 ** -8 + 1e-4, 1.0 + 2.0 ** -8 + 1e-6])   # above a midpoint by 1e-4, 1e-6
+    assert list(bf16_near_tie(x)) == [False, True]
+    assert list(bf16_near_tie(x, band=np.array([2e-4, 0.0]))) == [True, True]
+    assert list(bf16_near_tie(x, band=np.array([5e-5, 0.0]))) == [False, True]
