@@ -195,18 +195,16 @@ def _check_weights(dec, ow, layer, experts):
 def run_step_layerwise(w, dec, rows, branch, stream, out, keep_debug=()):
     """The step as moe_decode_step launches it -- every layer, then the final
     boundary, the same kernels in the same order -- one layer call at a time,
-    keeping each layer's routing, MoE input, gates and unpooled outputs (and
-    the whole debug view of the layers in keep_debug, with the stream around
-    them)."""
+    keeping each layer's routing, MoE input, gates, unpooled outputs and the
+    stream around it (and the whole debug view of the layers in keep_debug)."""
     k, H = w.top_k, w.hidden
     per = []
     for l in range(w.n_layers):
-        s_in = stream.cpu().numpy().copy() if l in keep_debug else None
+        s_in = stream.cpu().numpy().copy()
         dec.layer(l, rows, branch if l == 0 else None, stream)
         torch.cuda.synchronize()
         if l in keep_debug:
             d = read_debug(dec, rows)
-            d["stream_in"], d["stream"] = s_in, stream.cpu().numpy().copy()
         else:
             v = dec.debug()
             d = dict(ids=dev_array(v.ids, (rows, k), np.int32), x=dev_array(v.x, (rows, H), np.uint16),
@@ -214,6 +212,7 @@ def run_step_layerwise(w, dec, rows, branch, stream, out, keep_debug=()):
                      o=dev_array(v.o, (rows * k, H), np.float32),
                      n_active=int(dev_array(v.n_active, (1,), np.int32)[0]))
             d["active"] = dev_array(v.active, (w.n_experts,), np.int32)[: d["n_active"]]
+        d["stream_in"], d["stream"] = s_in, stream.cpu().numpy().copy()
         per.append(d)
     s_final_in = stream.cpu().numpy().copy()
     dec.final(rows, stream, out)
@@ -237,86 +236,119 @@ def final_output_band(s_got, s_ref, wf, eps):
 
 def check_final_output(got, out_ref, exact, band, what="final output"):
     """bf16 output bits against the oracle's: equal except where the oracle's
-    unrounded value lies within R19's band plus `band` of a rounding midpoint,
-    and there by exactly one bf16 step."""
+    unrounded value lies within R19's band plus `band` (an array, or None) of
+    a rounding midpoint; there the GPU's value may have rounded the other
+    way, so it lies within half its own quantum plus that band of the
+    oracle's unrounded value."""
+    x = np.asarray(exact, np.float64)
+    tol = 1e-5 * np.abs(x) + 1e-5 * np.sqrt(np.mean(x ** 2))
+    if band is not None:
+        tol = tol + band
     diff = got != out_ref
-    off = diff & ~bf16_near_tie(exact, band=band)
+    off = diff & ~bf16_near_tie(x, band=band)
     assert not np.any(off), f"{what}: {int(off.sum())} elements differ away from rounding midpoints"
-    steps = np.abs(got.astype(np.int32) - out_ref.astype(np.int32))[diff]
-    assert steps.size == 0 or steps.max() <= 1, f"{what}: a near-tie element is {steps.max()} steps off"
+    g = oracle.bf16_to_f64(got)
+    a = np.maximum(np.abs(g), np.abs(x))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    half_q = np.exp2(np.maximum(e, -126) - 8)
+    far = diff & (np.abs(g - x) > half_q + tol)
+    assert not np.any(far), f"{what}: {int(far.sum())} elements round beyond the band"
 
 
-def end_to_end(w, dec, rows, variant=0, sample_layers=None, n_sample=1, stage_layers=()):
+def end_to_end(w, dec, rows, variant=0, sample_layers=None, n_sample=1, stage_layers=(), chain_report=None):
     """One whole step on the GPU (every layer and the final boundary) against
-    the oracle run layer by layer on its own stream with the GPU's expert ids
-    (R14), over every active expert, with the experts' NVFP4 weights as the
-    GPU packed them (a sample per layer checked bit for bit against the
-    oracle's own packing).  Asserts:
+    the oracle, over every active expert, with the experts' NVFP4 weights as
+    the GPU packed them (a sample per layer checked bit for bit against the
+    oracle's own packing).  Each layer is recomputed by the oracle as a whole
+    -- boundary, router, routing, pooler, both quantizations, the experts,
+    the gather into the next boundary -- from the GPU's state at that
+    layer's entry (its stream and branch), with the GPU's expert ids (R14);
+    a single-layer workload is therefore checked end to end from the step's
+    inputs.  Asserts:
       - at every layer, the oracle's routing of the GPU's MoE input gives the
         GPU's ids on every unflagged row (bit for bit);
       - the oracle's own routing of its own MoE input agrees with the GPU's
         ids on every unflagged row whose input is bitwise the GPU's;
-      - the final fp32 stream within STREAM_TOL * rms(stream);
-      - the bf16 output equal except at rounding midpoints (the band derived
-        from the measured stream error), one step at most;
+      - after each layer, the stream at the next boundary (the next layer's,
+        or the final) within STREAM_TOL * rms(stream), and the next bf16
+        output (the next MoE input, or the final output) equal except at
+        rounding midpoints, the band derived from that stream error;
       - the layers in stage_layers pass every staged check on a sample.
-    Returns the per-layer report (rows agreeing, flagged, inputs differing)."""
+    Over several layers the stream is not compared from the step's inputs
+    alone: the chain is ill-conditioned (R32), a one-ulp change of its input
+    grows past the tolerance within a few layers in the oracle itself.  With
+    chain_report (a list), the oracle is also run freely from the step's
+    inputs (the GPU's ids forced) and its per-layer divergence is appended.
+    Returns the per-layer report."""
     k = w.top_k
-    stream, branch = _sgpu().step_tensors(w.with_rows(rows) if rows != w.rows else w, variant)
+    wr = w.with_rows(rows) if rows != w.rows else w
+    stream, branch = _sgpu().step_tensors(wr, variant)
     out = torch.empty_like(branch)
     per, s_final_in = run_step_layerwise(w, dec, rows, branch, stream, out, keep_debug=stage_layers)
-    s_host, b_host = synth.step_inputs(w.with_rows(rows) if rows != w.rows else w, variant)
-    s, br = s_host, oracle.bf16_to_f64(b_host)
-    report = []
+    s_host, b_host = synth.step_inputs(wr, variant)
+    s_gpu = stream.cpu().numpy()
+    out_gpu = out.view(torch.uint16).cpu().numpy()
+    wpf, wf = synth.final_norm_weights(w)
     sample_layers = range(w.n_layers) if sample_layers is None else sample_layers
+    report = []
+    free_s, free_br = s_host, oracle.bf16_to_f64(b_host)
     for l in range(w.n_layers):
         g = per[l]
+        # the GPU's branch into layer l: the step's, or its gather of layer l - 1
+        br = oracle.bf16_to_f64(b_host) if l == 0 else \
+            oracle.gather(per[l - 1]["gates"].astype(np.float64), per[l - 1]["o"], k)
         ow = gpu_layer_weights(dec, w, l, g["active"])
         if l in sample_layers:
             hot = sorted(set(int(e) for e in g["active"][:: max(1, len(g["active"]) // n_sample)][:n_sample]))
             check_gpu_weights(dec, oracle_weights(w, l, experts=hot), l, hot)
         if l in stage_layers:
             d = per[l]
-            prev_br = None if l == 0 else oracle.gather(per[l - 1]["gates"].astype(np.float64),
-                                                        per[l - 1]["o"], k)
             picks = sorted(set([int(max(d["active"], key=lambda e: d["count"][e]))]
                                + [int(e) for e in d["active"][:1]]))
             check_gpu_weights(dec, oracle_weights(w, l, experts=picks), l, picks)
-            check_stages(w, d, ow, picks, oracle.bf16_to_f64(b_host) if l == 0 else prev_br,
-                         d["stream_in"], d["stream"], rows)
+            check_stages(w, d, ow, picks, br, d["stream_in"], d["stream"], rows)
         # the oracle's routing on the GPU's own MoE input: the GPU's ids (staged, bit for bit)
         rg = oracle.route(g["x"], ow.router_w, ow.router_bias, k)
         okg = rg["flags"] == 0
         assert np.array_equal(rg["ids"][okg], g["ids"][okg]), f"layer {l}: ids on the GPU's input"
-        o = oracle.layer_step(ow, k, w.eps, br, s, forced_ids=g["ids"])
+        # the whole layer from the GPU's entry state, then the next boundary
+        o = oracle.layer_step(ow, k, w.eps, br, g["stream_in"], forced_ids=g["ids"])
         own = oracle.route(o["x"], ow.router_w, ow.router_bias, k)
         same_x = np.all(o["x"] == g["x"], axis=1)
         agree = np.all(own["ids"] == g["ids"], axis=1)
         flagged = own["flags"] != 0
         assert np.all(agree | flagged | ~same_x), f"layer {l}: ids differ on an unflagged row"
+        y = oracle.gather(o["gates"], o["o"], k)
+        last = l == w.n_layers - 1
+        nxt_w = (wpf, wf) if last else synth.norm_weights(w, l + 1)
+        s_ref, b_ref, b_exact = oracle.boundary(y, o["stream"], nxt_w[0], nxt_w[1], w.eps)
+        s_got = s_gpu if last else per[l + 1]["stream"]
+        b_got = out_gpu if last else per[l + 1]["x"]
+        err = float(np.max(np.abs(s_got.astype(np.float64) - s_ref)))
+        bound = STREAM_TOL * _rms(s_ref)
+        assert err <= bound, f"layer {l}: stream at the next boundary max|err| {err:.3e} > {bound:.3e}"
+        check_final_output(b_got, b_ref, b_exact, final_output_band(s_got, s_ref, nxt_w[1], w.eps),
+                           "final output" if last else f"layer {l + 1}'s MoE input")
         report.append(dict(layer=l, rows=rows, agree=int(agree.sum()), flagged=int(flagged.sum()),
-                           x_differs=int((~same_x).sum()), n_active=len(g["active"])))
-        s = o["stream"]
-        br = oracle.gather(o["gates"], o["o"], k)
-    wpf, wf = synth.final_norm_weights(w)
-    s_gpu = stream.cpu().numpy()
-    out_gpu = out.view(torch.uint16).cpu().numpy()
+                           x_differs=int((~same_x).sum()), n_active=len(g["active"]),
+                           err_over_rms=err / _rms(s_ref)))
+        if chain_report is not None and w.n_layers > 1:
+            of = oracle.layer_step(ow, k, w.eps, free_br, free_s, forced_ids=g["ids"])
+            free_s, free_br = of["stream"], oracle.gather(of["gates"], of["o"], k)
+            gs = per[l]["stream"].astype(np.float64)
+            chain_report.append(float(np.max(np.abs(gs - free_s)) / _rms(free_s)))
     # the final boundary staged: the oracle's on the GPU's last gather and stream
     y = oracle.gather(per[-1]["gates"].astype(np.float64), per[-1]["o"], k)
     fs_ref, fo_ref, fe = oracle.boundary(y, s_final_in, wpf, wf, w.eps)
     _close(s_gpu, fs_ref, 1e-5, "stream after the final boundary (staged)")
     check_final_output(out_gpu, fo_ref, fe, None, "final output (staged)")
-    # end to end
-    s_ref, out_ref, oe = oracle.boundary(br, s, wpf, wf, w.eps)
-    err = float(np.max(np.abs(s_gpu.astype(np.float64) - s_ref)))
-    bound = STREAM_TOL * _rms(s_ref)
-    assert err <= bound, f"end-to-end stream max|err| {err:.3e} > {bound:.3e}"
-    check_final_output(out_gpu, out_ref, oe, final_output_band(s_gpu, s_ref, wf, w.eps))
-    for r in report:
-        r["stream_err_over_rms"] = err / _rms(s_ref)
-    print(f"{w.name} b={rows}: end-to-end stream max|err| / rms = {err / _rms(s_ref):.3e}; per layer "
-          + "; ".join(f"L{r['layer']}: {r['agree']}/{rows} ids agree, {r['flagged']} flagged, "
-                      f"{r['x_differs']} inputs differ, {r['n_active']} experts" for r in report))
+    print(f"{w.name} b={rows}: per layer "
+          + "; ".join(f"L{r['layer']}: max|err|/rms {r['err_over_rms']:.2e}, {r['agree']}/{rows} ids agree, "
+                      f"{r['flagged']} flagged, {r['x_differs']} inputs differ, {r['n_active']} experts"
+                      for r in report)
+          + ("" if not chain_report else "; free-running chain max|err|/rms per layer: "
+             + " ".join(f"{x:.1e}" for x in chain_report)))
     return report, stream, out
 
 
@@ -664,12 +696,13 @@ def test_serving_end_to_end(layout):
 
 @pytest.mark.slow
 def test_chained_layers_end_to_end():
-    """Eight chained layers (H 5120, 128 experts, top-8, I 1536): the whole
-    step end to end against the oracle, every layer's stages on a sample (the
-    chained gather included), and the graph."""
+    """Eight chained layers (H 5120, 128 experts, top-8, I 1536): every layer
+    end to end against the oracle from the GPU's state at its entry (R32),
+    every layer's stages on a sample (the chained gather included), the
+    final boundary, and the graph."""
     w = synth.WORKLOADS["chained8"]
     dec = _sgpu().build(w)
-    end_to_end(w, dec, w.rows, stage_layers=tuple(range(w.n_layers)))
+    end_to_end(w, dec, w.rows, stage_layers=tuple(range(w.n_layers)), chain_report=[])
     _graph_equals_eager(w, dec, w.rows)
     dec.close()
 
@@ -689,9 +722,10 @@ def test_batch_skew_sweep_end_to_end(rows):
 @pytest.mark.slow
 def test_stack16_end_to_end():
     """The 16-layer stack at serving widths (about 101.5 GB of NVFP4 weights,
-    generated on the device), b 8, the codes held once in tiles: the whole
-    step end to end against the oracle, three layers' stages on a sample, and
-    the graph replay against the eager step."""
+    generated on the device), b 8, the codes held once in tiles: every layer
+    end to end against the oracle from the GPU's state at its entry (R32),
+    three layers' stages on a sample, the final boundary, and the graph
+    replay against the eager step."""
     import speculative_decode_routed_gb300 as moe
     w = synth.WORKLOADS["stack16"]
     dec = _sgpu().build(w)
@@ -699,6 +733,6 @@ def test_stack16_end_to_end():
     codes = E * (2 * I * H // 2 + H * I // 2)
     # the handle holds only the scale atoms (1/8 of the code bytes), no copy of the codes
     assert moe.moe_decode_weight_copy_bytes(dec.handle) <= w.n_layers * codes // 8 + (1 << 20)
-    end_to_end(w, dec, w.rows, sample_layers=(0, 8, 15), stage_layers=(0, 8, 15))
+    end_to_end(w, dec, w.rows, sample_layers=(0, 8, 15), stage_layers=(0, 8, 15), chain_report=[])
     _graph_equals_eager(w, dec, w.rows)
     dec.close()

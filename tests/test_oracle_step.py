@@ -302,3 +302,44 @@ def test_tiny_layer_statistics():
     # every pair's h tensor scale is that expert's amax / 2688
     for e in out["active"]:
         assert out["h_sg"][e] == np.float32(out["h_amax"][e] / np.float32(2688.0))
+
+
+def test_chained_layers_amplify_a_one_ulp_input_change():
+    """Why a chained step is checked layer by layer from the GPU's own state
+    at each layer's entry, not end to end from the step's inputs (R32): the
+    chain is ill-conditioned.  The oracle run twice over the same eight
+    chained layers (H 1024, 16 experts, top-8, I 256), the second time from a
+    stream one fp32 ulp up and with the first run's expert ids forced, agrees
+    with itself after the first layer to about 1e-6 of the stream's rms, yet
+    ends far more than the end-to-end tolerance (2e-3 * rms) apart after the
+    eighth: each NVFP4 quantization -- a code, a block scale, and above all a
+    per-expert tensor scale of h -- turns a sub-ulp difference into a whole
+    quantization step, and the next boundary's rmsnorm(y) carries it into the
+    stream at full size.  An fp32 evaluation differs from the fp64 oracle by
+    at least one ulp, so the tolerance can hold per layer, not over the
+    chain."""
+    w = synth.Workload("chain8_small", rows=8, hidden=1024, n_experts=16, top_k=8, inter=256,
+                       n_layers=8)
+    ows = [oracle_weights(w, l) for l in range(w.n_layers)]
+    s0, b0 = synth.step_inputs(w, 0)
+
+    def run(s, forced=None):
+        br, outs = oracle.bf16_to_f64(b0), []
+        for l in range(w.n_layers):
+            o = oracle.layer_step(ows[l], w.top_k, w.eps, br, s,
+                                  forced_ids=None if forced is None else forced[l])
+            outs.append(o)
+            s, br = o["stream"], oracle.gather(o["gates"], o["o"], w.top_k)
+        return outs
+
+    a = run(s0)
+    b = run(np.nextafter(s0, np.float32(np.inf)).astype(np.float32), [o["ids"] for o in a])
+
+    def rel(l):
+        sa = a[l]["stream"].astype(np.float64)
+        return np.max(np.abs(sa - b[l]["stream"])) / np.sqrt(np.mean(sa ** 2))
+
+    assert rel(0) < 1e-5
+    assert rel(w.n_layers - 1) > 10 * 2e-3
+    # the growth passes through a changed h tensor scale on the way
+    assert any(not np.array_equal(a[l]["h_sg"], b[l]["h_sg"]) for l in range(w.n_layers))
