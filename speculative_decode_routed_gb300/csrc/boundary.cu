@@ -44,6 +44,21 @@ __device__ __forceinline__ void block_sum_to_slot(float v, float* warp_red, floa
   }
 }
 
+// The cluster-wide sum of one shared-memory slot: every peer's value read at
+// once (at most 8 CTAs), then added in rank order, so every CTA forms the same
+// total bit for bit.
+__device__ __forceinline__ float cluster_slot_sum(cg::cluster_group& cluster, float* slot) {
+  const unsigned n = cluster.num_blocks();
+  float v[8];
+#pragma unroll
+  for (unsigned q = 0; q < 8; ++q) v[q] = q < n ? *cluster.map_shared_rank(slot, q) : 0.0f;
+  float t = 0.0f;
+#pragma unroll
+  for (unsigned q = 0; q < 8; ++q)
+    if (q < n) t += v[q];
+  return t;
+}
+
 // KMAX: the most gather slots (k <= KMAX); 8 keeps the registers, and so
 // the CTAs per SM, of the common top-8 step.
 template <int KMAX>
@@ -130,14 +145,15 @@ __global__ void boundary_kernel(BoundaryParams p) {
     // the first layer's front: the embedded tokens are the stream
     s = y;
   } else {
+    // the stream's load in flight with the branch's
+    if (live)
+      s = __ldcg(reinterpret_cast<const float4*>(p.stream_in ? p.stream_in + (size_t)r * p.H + col : srow));
     // rms of the branch over the whole row (cluster-wide)
     block_sum_to_slot(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, warp_red, &part[0]);
     cluster.sync();
-    float ss = 0.0f;
-    for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss += *cluster.map_shared_rank(&part[0], q);
+    const float ss = cluster_slot_sum(cluster, &part[0]);
     const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
     if (live) {
-      s = __ldcg(reinterpret_cast<const float4*>(p.stream_in ? p.stream_in + (size_t)r * p.H + col : srow));
       s.x += y.x * inv1 * wpost.x;
       s.y += y.y * inv1 * wpost.y;
       s.z += y.z * inv1 * wpost.z;
@@ -159,8 +175,11 @@ __global__ void boundary_kernel(BoundaryParams p) {
   }
   block_sum_to_slot(s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w, warp_red, &part[1]);
   cluster.sync();
-  float ss2 = 0.0f;
-  for (unsigned q = 0; q < cluster.num_blocks(); ++q) ss2 += *cluster.map_shared_rank(&part[1], q);
+  const float ss2 = cluster_slot_sum(cluster, &part[1]);
+  // this CTA has read its peers' shared memory for the last time: arrive now,
+  // and wait only before exiting, so the barrier's latency hides behind the
+  // stores below
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const float inv2 = rsqrtf(ss2 / (float)p.H + p.eps);
 
   float m = 0.0f;
@@ -185,7 +204,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
     }
   }
   // keep this CTA's shared memory alive until every peer has read it
-  cluster.sync();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace

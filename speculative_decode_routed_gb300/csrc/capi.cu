@@ -432,6 +432,10 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   rp.wr = reinterpret_cast<const __nv_bfloat16*>(w.router_w);
   rp.bias = w.router_bias;
   rp.line_rows = d.max_rows * d.top_k;
+  // up to 8 rows the tensor-core experts kernel routes and pools itself
+  const bool local_route = MOE_EXPERT_TC && rows <= 8;
+  rp.route_in_experts = local_route ? 1 : 0;
+  rp.cluster_sum = rows <= 8 ? 1 : 0;  // one block of rows: the slices are summed in the router
   rp.ws = h->ws;
   e = moe::launch_router(rp, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
@@ -466,6 +470,10 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   td.gscale = w.w_gscale;
   td.ws = h->ws;
   tg.withhold_ready = withhold_ready ? 1 : 0;
+  tg.local_route = td.local_route = local_route ? 1 : 0;
+  tg.rows = td.rows = rows;
+  tg.S = td.S = 1;  // the router summed its slices (cluster_sum)
+  tg.rbias = td.rbias = w.router_bias;
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
                          td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);

@@ -30,6 +30,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "routing.cuh"
 #include "tc_internal.h"
 
 namespace moe {
@@ -166,6 +167,8 @@ struct TcSmem {
   int* pairs;            // [kMaxPairsTc]
   int* flag;
   uint32_t* tmem_base;
+  unsigned* act;         // [kMaxPairsTc]  local routing: packed work item per active expert
+  int* porder;           // [kMaxPairsTc]  local routing: pair id at each pooled position
   uint8_t* stages;
 };
 
@@ -183,6 +186,8 @@ __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
   s.pairs = reinterpret_cast<int*>(base + 640);
   s.flag = s.pairs + kMaxPairsTc;
   s.tmem_base = reinterpret_cast<uint32_t*>(s.flag + 4);
+  s.act = reinterpret_cast<unsigned*>(base + 1280);
+  s.porder = reinterpret_cast<int*>(base + 1280 + 4 * kMaxPairsTc);
   s.stages = base + kTcCtrl;
   return s;
 }
@@ -256,10 +261,144 @@ __device__ __forceinline__ bool tc_item_ok(const TcParams& p, int4 et) {
 }
 
 // Gate/up item it: tile it % tiles of virtual expert it / tiles (an active
-// expert's pairs in groups of at most 32).
-__device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, int it) {
-  const unsigned w = __ldcg(p.ws.act_info + it / p.tiles);
+// expert's pairs in groups of at most 32), from this CTA's own pooler when it
+// routed the rows itself.
+__device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, const TcSmem& sm, int it) {
+  const unsigned w = p.local_route ? sm.act[it / p.tiles] : __ldcg(p.ws.act_info + it / p.tiles);
   return w ? unpack_expert(w) : make_int4(-1, 0, 0, 0);
+}
+
+// In-kernel routing and pooler (at most 8 rows, so at most 128 pairs and at
+// most 8 pairs per expert: one work item per active expert).  Every CTA
+// routes the rows itself, one warp per row, from the router's logits, then
+// pools the pairs in shared memory with bitmaps: each pair sets its expert's
+// bit in an E-bit map and its row's bit in the expert's row mask; one warp
+// scan of the map's population counts numbers the active experts (ascending),
+// a second scan over the active experts' pair counts gives each one's first
+// pooled position, and a pair's position is that plus the number of earlier
+// rows routed to the same expert -- experts ascend and rows ascend within an
+// expert, as the pooler defines.  Every CTA computes the same result.  The
+// first CTA also writes the workspace copies -- ids, gates, flags, logits,
+// count, offset, pair order, active list, work items -- that the next
+// boundary's gather and the staged checks read, and resets max |x| (every
+// router CTA has read it).  The transient arrays live in the stage ring,
+// which no copy has touched yet.  Returns the number of work items.
+__device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
+  const Workspace& ws = p.ws;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int k = p.k, E = p.E, rows = p.rows, npairs = rows * k;
+  const int EW = (E + 31) >> 5;                                // words of the expert map (<= 32)
+  const bool lead = blockIdx.x == 0;
+  int* sids = reinterpret_cast<int*>(sm.stages);               // [128] the routed ids
+  unsigned* emap = reinterpret_cast<unsigned*>(sids + kMaxPairsTc);  // [32] bit e: expert e is active
+  int* wbase = reinterpret_cast<int*>(emap + 32);              // [32] active experts below each map word
+  int* aoff = wbase + 32;                                      // [129] first pooled position per active index
+  unsigned* rmask = reinterpret_cast<unsigned*>(aoff + kMaxPairsTc + 1);  // [E] rows routed to each expert
+  float* lg = reinterpret_cast<float*>(rmask + 1024);          // [rows][E] scratch above 256 experts
+  for (int i = tid; i < EW; i += blockDim.x) emap[i] = 0u;
+  for (int i = tid; i < E; i += blockDim.x) rmask[i] = 0u;
+  if (warp < rows) {
+    const RouteRow rr{ws.logit_part, p.S, rows, E, k, p.rbias,
+                      lead ? ws.logits : nullptr, lead ? ws.ids : nullptr,
+                      lead ? ws.gates : nullptr, lead ? ws.flags : nullptr, ws.err, sids};
+    route_row(rr, warp, lg + warp * E);
+  }
+  __syncthreads();
+  int e = -1, r = 0;
+  if (tid < npairs) {
+    e = sids[tid];
+    r = tid / k;
+    if (e >= 0 && e < E) {
+      atomicOr(&emap[e >> 5], 1u << (e & 31));
+      atomicOr(&rmask[e], 1u << r);
+    } else {
+      e = -1;                      // out of range: latched by the routing, not pooled
+    }
+  }
+  __syncthreads();
+  // the active experts below each map word (warp 0: one word per lane)
+  if (warp == 0) {
+    const int c = lane < EW ? __popc(emap[lane]) : 0;
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane < EW) wbase[lane] = inc - c;
+  }
+  __syncthreads();
+  const bool valid = e >= 0;
+  int a = 0, rank = 0, cnt = 0;
+  if (valid) {
+    a = wbase[e >> 5] + __popc(emap[e >> 5] & ((1u << (e & 31)) - 1u));  // active index of e
+    const unsigned m = rmask[e];
+    rank = __popc(m & ((1u << r) - 1u));                                   // earlier rows of e
+    cnt = __popc(m);
+    if (rank == 0) aoff[a] = cnt;
+  }
+  const int n_items = __syncthreads_count(valid && rank == 0);
+  // first pooled position of each active expert: a scan of the pair counts
+  // in active order (warp 0, four per lane)
+  if (warp == 0) {
+    int v[4], c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[j] = 4 * lane + j < n_items ? aoff[4 * lane + j] : 0;
+      c += v[j];
+    }
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    int run = inc - c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (4 * lane + j < n_items) aoff[4 * lane + j] = run;
+      run += v[j];
+    }
+    if (lane == 31) aoff[kMaxPairsTc] = inc;                   // every pooled pair
+  }
+  __syncthreads();
+  const int n_valid = aoff[kMaxPairsTc];
+  if (valid) {
+    const int pos = aoff[a] + rank;
+    sm.porder[pos] = tid;
+    if (rank == 0) {
+      const unsigned wi = pack_expert(e, aoff[a], cnt);
+      sm.act[a] = wi;
+      if (lead) {
+        ws.active[a] = e;
+        ws.act_info[a] = wi;
+      }
+    }
+    if (lead) {
+      ws.pair_order[pos] = tid;
+      ws.pos_of_pair[tid] = pos;
+    }
+  }
+  if (lead) {
+    // every expert's count and first pooled position (that of the first
+    // active expert at or above it)
+    for (int x = tid; x < E; x += blockDim.x) {
+      const int ax = wbase[x >> 5] + __popc(emap[x >> 5] & ((1u << (x & 31)) - 1u));
+      ws.count[x] = __popc(rmask[x]);
+      ws.offset[x] = ax < n_items ? aoff[ax] : n_valid;
+    }
+    if (tid == 0) {
+      ws.offset[E] = n_valid;
+      ws.n_active[0] = n_items;
+      ws.n_virtual[0] = n_items;
+      ws.x_amax[0] = 0u;
+    }
+  }
+  // the scratch was written through the generic proxy; the stage ring is
+  // next written by the TMA (async proxy)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  return n_items;
 }
 
 // Down item it: tile it % tiles of the (it / tiles)-th virtual expert whose h
@@ -348,9 +487,11 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
 // completes the expert -- every tile of every part -- quantizes all of the
 // expert's h rows and publishes its parts to the down projection.
 __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int tiles,
-                                 float amax_part, int t) {
+                                 float amax_part, int t, int pos0_local, int ne_local) {
   const Workspace& ws = p.ws;
-  const int pos0 = __ldcg(ws.offset + e), ne = __ldcg(ws.offset + e + 1) - pos0;
+  // under local routing an expert is one work item: its pooled rows are the item's
+  const int pos0 = p.local_route ? pos0_local : __ldcg(ws.offset + e);
+  const int ne = p.local_route ? ne_local : __ldcg(ws.offset + e + 1) - pos0;
   const int parts = (ne + kVirtualPairs - 1) / kVirtualPairs;
   const float am = warp_max(amax_part);
   if ((t & 31) == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + e, am);
@@ -390,7 +531,8 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
 template <bool kGU>
 __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* tm_a,
                                          const CUtensorMap* tm_b, const CUtensorMap* tm_sfb,
-                                         const TcSmem& sm, uint32_t tmem, int n_items, int epi0) {
+                                         const TcSmem& sm, uint32_t tmem, int n_items, int epi0,
+                                         int first_claim = -1) {
   const Workspace& ws = p.ws;
   const uint64_t lim = ws.wait_ns;  // every wait's limit
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -406,13 +548,14 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       int g = 0;           // stages issued = item * KS + ks
       uint32_t fbits = 0;  // per (stage, group) full barrier: parity of fills issued
       bool ok = true;
-      int it = (int)atomicAdd(claim, 1u);
+      // the first claim may have been made already (its latency hidden under the routing)
+      int it = first_claim >= 0 ? first_claim : (int)atomicAdd(claim, 1u);
       for (int j = 0;; ++j) {
         int4 et = make_int4(-1, 0, 0, 0);
         bool live = ok && it < n_items;
         if (live) {
           if (kGU) {
-            et = tc_resolve_gate_up(p, it);
+            et = tc_resolve_gate_up(p, sm, it);
           } else if (!tc_resolve_down(p, it, et)) {
             latch_error(ws.err, kDevWaitTimeout);
             live = ok = false;
@@ -586,7 +729,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
     // h and o are read back soon (the h quantization and the next boundary's
     // gather): keep them in L2 while the weights stream through it
     const uint64_t keep = l2_evict_last_policy();
-    int cur_e = -1, cur_pos0 = -1, cur_tiles = 0;
+    int cur_e = -1, cur_pos0 = -1, cur_ne = 0, cur_tiles = 0;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
     for (int j = 0;; ++j) {
       // the next item (one thread waits, bounded; the barrier hands the slot
@@ -607,13 +750,15 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       // gate/up accumulates per expert (over its virtual parts); down and
       // direct gate/up keep the pair ids of the current virtual part
       const bool new_e = (e != cur_e), new_part = new_e || pos0 != cur_pos0;
-      if (new_e && kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
+      if (new_e && kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne);
       if (new_part && (!kGU || p.direct)) {
         tc_named_sync();  // nobody still reads the previous part's pair ids
-        for (int jj = t; jj < ne; jj += kEpiThreads) sm.pairs[jj] = __ldcg(ws.pair_order + pos0 + jj);
+        for (int jj = t; jj < ne; jj += kEpiThreads)
+          sm.pairs[jj] = p.local_route ? sm.porder[pos0 + jj] : __ldcg(ws.pair_order + pos0 + jj);
         tc_named_sync();
       }
       cur_pos0 = pos0;
+      cur_ne = ne;
       if (new_e) {
         cur_e = e;
         cur_tiles = 0;
@@ -707,7 +852,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
       ++cur_tiles;
     }
-    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t);
+    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne);
   }
 }
 
@@ -757,7 +902,9 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   // kernels before
   grid_dep_wait();
   grid_dep_launch();
-  const int na = __ldcg(pg.ws.n_virtual);
+  // the producer's first gate/up claim, in flight while the CTA routes
+  const int first_claim = tid == 0 ? (int)atomicAdd(pg.ws.counters + 1, 1u) : -1;
+  const int na = pg.local_route ? tc_local_route(pg, sm) : __ldcg(pg.ws.n_virtual);
   const bool na_ok = na >= 0 && na <= virtual_slots(pg.E, pg.ws_pairs);
   tc_fence_before();
   __syncthreads();
@@ -766,7 +913,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   if (!na_ok && tid == 0) latch_error(pg.ws.err, kDevBadRouting);
   const int n_act = na_ok ? na : 0;
 
-  tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0);
+  tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0, first_claim);
 
   // this CTA's gate/up copies have landed, its MMAs completed and its
   // accumulators been read: the shared memory takes the down layout

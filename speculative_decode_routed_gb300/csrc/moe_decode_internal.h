@@ -109,6 +109,13 @@ struct RouterParams {
   const __nv_bfloat16* wr;      // [E][H]
   const float* bias;            // [E] or null
   int line_rows;                // row stride of the scale lines (max_rows * k)
+  int cluster_sum;              // 1 (at most 8 rows): the S slice CTAs of an expert group form a
+                                // cluster whose first CTA sums their partials in slice order into
+                                // logit_part's first slice (the logits without bias), so routing
+                                // reads one slice
+  int route_in_experts;         // 1 (at most 8 rows, tensor-core experts): the experts kernel
+                                // routes the rows and pools the pairs itself; the router only
+                                // writes the partial logits and the MoE input's quantization
   Workspace ws;
 };
 

@@ -18,8 +18,13 @@
 // counter, no spin) sums its rows' partials in slice order and selects their
 // top-k (one warp per row); the last row block to finish builds the pooler's
 // arrays over every row.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "gemv.cuh"
+#include "routing.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
@@ -40,193 +45,6 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
     acc = fmaf(fa.y, fb.y, acc);
   }
   return acc;
-}
-
-// Comparator of the routing order: higher logit first, ties to the lower id.
-__device__ __forceinline__ bool route_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// Shared tail of one row's routing (lane t < nsel holds the t-th selection):
-// renormalised gates in slot order, the near-tie flag, ids to global and to
-// shared memory for the pooler.
-__device__ __forceinline__ void route_finish(const RouterParams& p, int r, int nsel, int sel_id,
-                                             float sel_v, float m, float z, int* sids) {
-  const Workspace& ws = p.ws;
-  const int k = p.k, lane = threadIdx.x & 31;
-  const float ex = (lane < nsel) ? expf(sel_v - m) : 0.0f;
-  float den = 0.0f;
-  for (int t = 0; t < k; ++t) den += __shfl_sync(0xffffffffu, ex, t);
-  const float ek = __shfl_sync(0xffffffffu, ex, k - 1);
-  const float ek1 = __shfl_sync(0xffffffffu, ex, (nsel > k) ? k : 0);
-  if (lane < k) {
-    ws.ids[r * k + lane] = sel_id;
-    sids[r * k + lane] = sel_id;
-    ws.gates[r * k + lane] = ex / den;
-    if (sel_id < 0 || sel_id >= p.E) latch_error(ws.err, kDevBadRouting);
-  }
-  if (lane == 0) ws.flags[r] = (nsel > k) ? (uint8_t)((ek - ek1) / z < 1e-6f) : (uint8_t)0;
-}
-
-// Order-preserving 32-bit keys of fp32 logits (larger logit, larger key);
-// -0 is keyed as +0 so that equal logits tie.  Key 0 is below every logit.
-__device__ __forceinline__ uint32_t logit_key(float f) {
-  const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_logit(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// One row's routing for E <= 256: lane owns experts e = lane + 32 i (i < 8),
-// their logits in registers.  The slices' partial sums are all loaded at
-// once and added in slice order.  Each of the k + 1 selections is two warp
-// reductions: the largest key among the lanes' heads (redux.sync max), then
-// the lowest expert id among the lanes whose head has that key (redux.sync
-// min), so ties go to the lower id; the winning lane drops the expert and
-// rescans its 8 keys for its next head (largest key, lowest id).
-__device__ void route_row_small(const RouterParams& p, int r, int* sids) {
-  const Workspace& ws = p.ws;
-  const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
-  float v[8];
-  float part[8][8];
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      part[s][i] = (s < p.S && e < E) ? __ldcg(src + e) : 0.0f;
-    }
-  }
-  uint32_t key[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    float acc = 0.0f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < p.S) acc += part[s][i];
-    if (e < E) {
-      if (p.bias) acc += __ldg(p.bias + e);
-      ws.logits[(size_t)r * E + e] = acc;
-    }
-    v[i] = acc;
-    key[i] = (e < E) ? logit_key(acc) : 0u;
-  }
-  uint32_t lk = key[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) lk = max(lk, key[i]);
-  const float m = key_logit(__reduce_max_sync(0xffffffffu, lk));
-  float z = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (lane + 32 * i < E) z += expf(v[i] - m);
-  z = warp_sum(z);
-  uint32_t hk = key[0];
-  int hi = 0;
-#pragma unroll
-  for (int i = 1; i < 8; ++i)
-    if (key[i] > hk) {
-      hk = key[i];
-      hi = i;
-    }
-  const int nsel = (k < E) ? k + 1 : k;
-  int sel_id = -1;
-  float sel_v = 0.0f;
-  for (int t = 0; t < nsel; ++t) {
-    const uint32_t gk = __reduce_max_sync(0xffffffffu, hk);
-    const uint32_t gid = __reduce_min_sync(0xffffffffu, hk == gk ? (uint32_t)(lane + 32 * hi) : 0xffffffffu);
-    if (lane == t) {
-      sel_id = (int)gid;
-      sel_v = key_logit(gk);
-    }
-    if (lane == (int)(gid & 31u)) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i == hi) key[i] = 0u;
-      hk = key[0];
-      hi = 0;
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (key[i] > hk) {
-          hk = key[i];
-          hi = i;
-        }
-    }
-  }
-  route_finish(p, r, nsel, sel_id, sel_v, m, z, sids);
-}
-
-// One row's routing for any E (up to 1024): logits staged in shared memory,
-// each selection a scan of the lane's experts and a warp arg-max.
-__device__ void route_row_any(const RouterParams& p, int r, float* l, int* sids) {
-  const Workspace& ws = p.ws;
-  const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  // the lane's experts e = lane + 32 i, in groups of 8 so that the loads of
-  // a slice are all in flight together; slices are summed in order
-  for (int i0 = 0; i0 * 32 < E; i0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    for (int s = 0; s < p.S; ++s) {
-      const float* src = ws.logit_part + ((size_t)s * rows + r) * E;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * (i0 + i);
-        if (e < E) v[i] += __ldcg(src + e);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * (i0 + i);
-      if (e < E) {
-        const float vb = p.bias ? v[i] + __ldg(p.bias + e) : v[i];
-        l[e] = vb;
-        ws.logits[(size_t)r * E + e] = vb;
-        m = fmaxf(m, vb);
-      }
-    }
-  }
-  m = warp_max(m);
-  float z = 0.0f;
-  for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
-  z = warp_sum(z);
-  __syncwarp();
-  // top-(k+1) by logit (monotone in probability), ties to the lower id
-  const int nsel = (k < E) ? k + 1 : k;
-  int sel_id = -1;      // lane t keeps the t-th selection
-  float sel_v = 0.0f;
-  for (int t = 0; t < nsel; ++t) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = l[e];
-      if (route_before(v, e, bv, bi)) {
-        bv = v;
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (route_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == t) {
-      sel_id = bi;
-      sel_v = bv;
-    }
-    __syncwarp();
-    if (lane == 0) l[bi] = -INFINITY;  // taken
-    __syncwarp();
-  }
-  route_finish(p, r, nsel, sel_id, sel_v, m, z, sids);
-  __syncwarp();
 }
 
 // Shared-memory carve of the routing and pooler tails.
@@ -255,10 +73,10 @@ __device__ __forceinline__ RouteSmem route_carve(const RouterParams& p, uint8_t*
 __device__ void route_rows(const RouterParams& p, const RouteSmem& rs, int r0, int nr) {
   const int warp = threadIdx.x >> 5;
   if (warp < nr) {
-    if (p.E <= 256)
-      route_row_small(p, r0 + warp, rs.sids);
-    else
-      route_row_any(p, r0 + warp, rs.lg + warp * p.E, rs.sids);
+    const Workspace& ws = p.ws;
+    const RouteRow rr{ws.logit_part, p.cluster_sum ? 1 : p.S, p.rows, p.E, p.k, p.bias, ws.logits,
+                      ws.ids, ws.gates, ws.flags, ws.err, rs.sids};
+    route_row(rr, r0 + warp, rs.lg + warp * p.E);
   }
 }
 
@@ -445,23 +263,35 @@ __device__ void pool_all(const RouterParams& p, uint8_t* smem, bool ids_in_smem)
   pool_reset(p);
 }
 
+// This CTA's range of the MoE input's 16-element blocks.
+__device__ __forceinline__ void quant_range(const RouterParams& p, int& b0, int& b1) {
+  const int ncta = gridDim.x * gridDim.y * gridDim.z;
+  const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  const int nblk = p.rows * (p.H / 16);
+  b0 = (int)((long long)cta * nblk / ncta);
+  b1 = (int)((long long)(cta + 1) * nblk / ncta);
+}
+
 // This CTA's share of the MoE input's NVFP4 quantization (sg: its tensor
-// scale).
-__device__ void quantize_share(const RouterParams& p, float sg) {
+// scale).  pre0 / pre1: the thread's first block, already loaded (or
+// loaded here when has_pre is false).
+__device__ void quantize_share(const RouterParams& p, float sg, bool has_pre = false,
+                               uint4 pre0 = make_uint4(0u, 0u, 0u, 0u),
+                               uint4 pre1 = make_uint4(0u, 0u, 0u, 0u)) {
   // the MoE input as one NVFP4 tensor: this CTA's share of the 16-blocks,
   // one per thread.  Each block's scale also goes into its 16-byte scale
   // line ([H/64][line_rows][16]: bytes 0-3 the four scales of 64 elements,
   // the rest zero) that the tensor-core experts read when the rows
   // themselves are the MMA's N.
   const Workspace& ws = p.ws;
-  const int ncta = gridDim.x * gridDim.y * gridDim.z;
   const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   const int bpr = p.H / 16;
-  const int nblk = p.rows * bpr;
-  const int b0 = (int)((long long)cta * nblk / ncta), b1 = (int)((long long)(cta + 1) * nblk / ncta);
+  int b0, b1;
+  quant_range(p, b0, b1);
   for (int b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
-    const uint4 q0 = __ldcg(src), q1 = __ldcg(src + 1);
+    const bool first = has_pre && b == b0 + (int)threadIdx.x;
+    const uint4 q0 = first ? pre0 : __ldcg(src), q1 = first ? pre1 : __ldcg(src + 1);
     float v[16];
     const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
     const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
@@ -492,6 +322,7 @@ __device__ void quantize_share(const RouterParams& p, float sg) {
 __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
+  __shared__ float s_part[kRowBlock * kRouterWarps];  // cluster sum: this CTA's [row][expert] partials
   const Workspace& ws = p.ws;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * p.EG + warp;
@@ -510,6 +341,20 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
   }
   grid_dep_wait();
   grid_dep_launch();
+  // this CTA's first quantization block and max |x| (written by the
+  // boundary): loads in flight while the dot products run
+  uint4 qpre0 = make_uint4(0u, 0u, 0u, 0u), qpre1 = qpre0;
+  {
+    int qb0, qb1;
+    quant_range(p, qb0, qb1);
+    const int b = qb0 + threadIdx.x;
+    if (b < qb1) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)b * 16);
+      qpre0 = __ldcg(src);
+      qpre1 = __ldcg(src + 1);
+    }
+  }
+  const unsigned amax_bits = __ldcg(ws.x_amax);
 
   // each block of 8 rows in turn: the x slice is staged in shared memory
   // (every load in flight at once, the next block's already in registers
@@ -567,16 +412,50 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       const int row = lane >> 2;
-      if ((lane & 3) == 0 && row < nr) ws.logit_part[((size_t)sl * p.rows + r0 + row) * p.E + e] = v;
+      if ((lane & 3) == 0 && row < nr) {
+        if (p.cluster_sum)
+          s_part[row * kRouterWarps + warp] = v;
+        else
+          ws.logit_part[((size_t)sl * p.rows + r0 + row) * p.E + e] = v;
+      }
     }
     __syncthreads();  // the next block's staging reuses xs
   }
 
+  // cluster sum (one block of rows): the partials are published to the
+  // cluster, and the barrier's wait hides behind this CTA's quantization
+  if (p.cluster_sum) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   // this CTA's share of the MoE input's quantization, before it arrives (the
   // pooler resets max |x| for the next layer once every CTA has arrived)
-  quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
+  quantize_share(p, __fdiv_rn(__uint_as_float(amax_bits), 2688.0f), true, qpre0, qpre1);
+  if (p.cluster_sum) {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    // the slice-0 CTA sums the S slices' partials in slice order (the cluster
+    // rank is the slice) into the first slice of logit_part
+    cg::cluster_group cluster = cg::this_cluster();
+    if (sl == 0 && (int)threadIdx.x < p.rows * kRouterWarps) {
+      const int r = threadIdx.x / kRouterWarps, wi = threadIdx.x % kRouterWarps;
+      const int ee = blockIdx.x * p.EG + wi;
+      float acc = 0.0f;
+      for (int q = 0; q < p.S; ++q) acc += *cluster.map_shared_rank(&s_part[r * kRouterWarps + wi], q);
+      if (wi < p.EG && ee < p.E) ws.logit_part[(size_t)r * p.E + ee] = acc;
+    }
+    // every peer keeps its partials until the sums are read
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
   // beyond one block of rows, route_kernel routes the blocks in parallel
   if (nrb > 1) return;
+  if (p.route_in_experts) {
+    // the experts kernel routes and pools (and resets max |x| once every
+    // router CTA has read it); its item claims and ready list start empty
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      const int V = virtual_slots(p.E, p.rows * p.k);
+      for (int v = threadIdx.x; v < V; v += kRouterThreads) ws.ready_info[v] = 0u;
+      if (threadIdx.x < 4) ws.counters[threadIdx.x] = 0u;
+    }
+    return;
+  }
 
   // one block of rows: the last CTA to finish routes them and builds the pooler
   __syncthreads();
@@ -712,16 +591,22 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   cfg.blockDim = dim3(kRouterThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = (unsigned)p.S;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
+  if (p.cluster_sum && (nrb != 1 || p.S > 8 || p.EG != kRouterWarps)) return cudaErrorInvalidValue;
+  cfg.numAttrs = p.cluster_sum ? 2 : 1;
   const bool mma = nrb > 1 && p.H % (p.S * 256) == 0 && p.H / p.S <= 1024;
   if (mma) cfg.gridDim = dim3((p.E + 15) / 16, p.S, 1);
   cudaError_t e = mma ? cudaLaunchKernelEx(&cfg, router_mma_kernel, p) : cudaLaunchKernelEx(&cfg, router_kernel, p);
   if (e != cudaSuccess || nrb == 1) return e;
+  cfg.numAttrs = 1;
   cfg.gridDim = dim3(nrb, 1, 1);
   return cudaLaunchKernelEx(&cfg, route_kernel, p);
 }
