@@ -53,8 +53,8 @@ def _peaks():
 # (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by its
 # active experts); valid only for the kernel source it was taken on.
 EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu",
-                   "sha256_prefix": "75a309af2ce74a27", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": 1069186560 / 43}
+                   "sha256_prefix": "89efa5d83b31eaac", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": (1065518848 + 3387648) / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
