@@ -226,8 +226,20 @@ int moe_decode_debug(moe_decode_t* h, moe_decode_debug_view* out);
 
 /* Synchronizes the device, then returns MOE_EDEVICE if a device-side check
  * latched an error since create (and clears it), MOE_ECUDA on a CUDA error,
- * else MOE_OK. */
+ * else MOE_OK.  The codes (in moe_decode_error_message): 1 a bounded wait
+ * gave up, 2 routing produced an out-of-range value, 3 a data-dependent
+ * index was out of range (bounds-check builds only; the access was
+ * skipped), 4 a workspace guard changed.  Every region of the workspace is
+ * followed by a 256-byte guard whose first 16 bytes hold a pattern written
+ * at create; this call checks every guard, so a write past a region's end
+ * is reported with the region's name (and the guard is rewritten). */
 int moe_decode_last_error(moe_decode_t* h);
+
+/* How this library was built: bit 0 set in a bounds-check build (compiled
+ * with MOE_BOUNDS_CHECK: every index that comes from data is tested before
+ * it addresses memory, latching code 3 instead of faulting); bit 1 set in
+ * the CUDA-core expert build. */
+int moe_decode_build_info(void);
 
 /* The limit of every bounded wait in the handle's kernels (default 2 s):
  * a wait that runs this long gives up, the kernel latches the wait-timeout

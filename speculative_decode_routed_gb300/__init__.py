@@ -14,7 +14,9 @@ import os
 from dataclasses import dataclass
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
+# MOE_DECODE_LIB may name another build of the library (the bounds-check
+# variant, libmoe_decode_bounds.so, beside this file)
+LIB_PATH = os.environ.get("MOE_DECODE_LIB") or os.path.join(_HERE, "libmoe_decode.so")
 
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ENOMEM, MOE_EDEVICE = 0, -1, -2, -3, -4, -5
 # moe_decode_dims.code_layout
@@ -26,7 +28,7 @@ EXPORTS = (
     "moe_decode_step_graph", "moe_decode_step_host", "moe_decode_layer_profile", "moe_decode_debug",
     "moe_decode_last_error", "moe_decode_workspace_bytes", "moe_decode_weight_copy_bytes",
     "moe_decode_step_kernel_count", "moe_tiled_code_bytes", "moe_tile_codes",
-    "moe_decode_set_wait_limit", "moe_decode_selftest_wait_timeout",
+    "moe_decode_set_wait_limit", "moe_decode_selftest_wait_timeout", "moe_decode_build_info",
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
@@ -116,6 +118,7 @@ def _lib():
             "moe_tiled_code_bytes": (i64, [i64, i64]),
             "moe_tile_codes": (i32, [vp, i64, i64, vp, vp]),
             "moe_decode_set_wait_limit": (i32, [vp, ctypes.c_uint64]),
+            "moe_decode_build_info": (i32, []),
             "moe_decode_selftest_wait_timeout": (i32, [vp, i32, vp, vp, vp]),
             "moe_decode_step_kernel_count": (i32, [vp]),
             "moe_decode_destroy": (None, [vp]),

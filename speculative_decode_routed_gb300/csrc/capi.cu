@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/moe_decode.h"
+#include "common.cuh"
 #include "moe_decode_internal.h"
 #include "tc_internal.h"
 
@@ -69,6 +70,12 @@ bool host_pinned(const void* p) {
 
 
 
+// A guard of the workspace: 16 pattern bytes after a region (see Carver).
+struct Guard {
+  size_t offset;     // from the workspace base
+  const char* name;  // the region it follows
+};
+
 struct GraphEntry {
   int rows;
   const void* branch;
@@ -119,6 +126,8 @@ struct moe_decode_s {
   std::vector<CUtensorMap> tm_w13, tm_w2;
   std::vector<uint8_t*> sfa13, sfa2;   // weight scale atoms per layer (library-owned)
   std::vector<uint8_t*> tiled13, tiled2;  // the expert codes in 16 KB tiles per layer (library-owned)
+  std::vector<Guard> guards;           // the workspace's guards (offset, region)
+  unsigned long long* guard_offsets = nullptr;  // device copy of their offsets
   bool tiled = false;                  // the weight maps are over tiles (the caller's or the copy)
   size_t copy_bytes = 0;               // rearranged weight copies held (scale atoms, tiled codes)
   CUtensorMap tm_xpool{}, tm_xcodes{}, tm_xlines{}, tm_hcodes{}, tm_hlines{};
@@ -339,50 +348,90 @@ int check_layer(const moe_layer_weights& w, int i) {
   return MOE_OK;
 }
 
-template <typename T>
-T* carve(uint8_t*& cur, size_t count) {
-  T* p = reinterpret_cast<T*>(cur);
-  cur += (count * sizeof(T) + 255) / 256 * 256;
-  return p;
+// Every region of the workspace is followed by a 256-byte guard whose first
+// 16 bytes hold a pattern written at create; moe_decode_last_error checks
+// them, so a kernel writing past a region's end is caught (a substitute for
+// a memory sanitizer).
+constexpr size_t kGuardBytes = 256;
+
+// Region allocator over the workspace: 256-byte aligned regions, each followed
+// by a guard (recorded when guards is given).
+struct Carver {
+  uint8_t* base;
+  uint8_t* cur;
+  std::vector<Guard>* guards;
+  template <typename T>
+  T* take(size_t count, const char* name) {
+    T* p = reinterpret_cast<T*>(cur);
+    cur += (count * sizeof(T) + 255) / 256 * 256;
+    if (guards) guards->push_back(Guard{(size_t)(cur - base), name});
+    cur += kGuardBytes;
+    return p;
+  }
+};
+
+__global__ void guard_kernel(uint8_t* base, const unsigned long long* offsets, int n, int check,
+                             unsigned* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  uint4* g = reinterpret_cast<uint4*>(base + offsets[i]);
+  const uint4 want = make_uint4(0xC0DE0000u ^ (unsigned)i, 0x5AFE0000u ^ (unsigned)i, ~(unsigned)i,
+                                (unsigned)i * 2654435761u);
+  if (!check) {
+    *g = want;
+    return;
+  }
+  const uint4 v = *g;
+  if (v.x != want.x || v.y != want.y || v.z != want.z || v.w != want.w) {
+    atomicCAS(err, 0u, (unsigned)moe::kDevCanary);
+    atomicMin(err + 1, (unsigned)i);
+  }
 }
 
-size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims& d, int S) {
+size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims& d, int S,
+                        std::vector<Guard>* guards = nullptr,
+                        unsigned long long** guard_offsets = nullptr) {
   const size_t R = d.max_rows, H = d.hidden, E = d.n_experts, k = d.top_k, I = d.inter;
-  uint8_t* cur = base;
-  ws.x = carve<__nv_bfloat16>(cur, R * H);
-  ws.x_codes = carve<uint8_t>(cur, R * H / 2);
-  ws.x_sf = carve<uint8_t>(cur, R * H / 16);
-  ws.x_sg = carve<float>(cur, 1);
-  ws.x_amax = carve<unsigned>(cur, 1);
-  ws.logit_part = carve<float>(cur, (size_t)S * R * E);
-  ws.logits = carve<float>(cur, R * E);
-  ws.ids = carve<int>(cur, R * k);
-  ws.gates = carve<float>(cur, R * k);
-  ws.flags = carve<uint8_t>(cur, R);
-  ws.count = carve<int>(cur, E);
-  ws.offset = carve<int>(cur, E + 1);
-  ws.pair_order = carve<int>(cur, R * k);
-  ws.pos_of_pair = carve<int>(cur, R * k);
-  ws.active = carve<int>(cur, E);
-  ws.n_active = carve<int>(cur, 1);
-  ws.h = carve<float>(cur, R * k * I);
-  ws.h_amax = carve<unsigned>(cur, E);
-  ws.h_sg = carve<float>(cur, E);
-  ws.h_codes = carve<uint8_t>(cur, R * k * I / 2);
-  ws.h_sf = carve<uint8_t>(cur, R * k * I / 16);
-  ws.done = carve<unsigned>(cur, E);
-  ws.o = carve<float>(cur, R * k * H);
-  ws.x_pool = carve<uint8_t>(cur, R * k * H / 2);
-  ws.x_lines = carve<uint8_t>(cur, R * k * (H / 64) * 16);
-  ws.h_lines = carve<uint8_t>(cur, R * k * (I / 64) * 16);
+  Carver cv{base, base, guards};
+  ws.x = cv.take<__nv_bfloat16>(R * H, "x");
+  ws.x_codes = cv.take<uint8_t>(R * H / 2, "x_codes");
+  ws.x_sf = cv.take<uint8_t>(R * H / 16, "x_sf");
+  ws.x_sg = cv.take<float>(1, "x_sg");
+  ws.x_amax = cv.take<unsigned>(1, "x_amax");
+  ws.logit_part = cv.take<float>((size_t)S * R * E, "logit_part");
+  ws.logits = cv.take<float>(R * E, "logits");
+  ws.ids = cv.take<int>(R * k, "ids");
+  ws.gates = cv.take<float>(R * k, "gates");
+  ws.flags = cv.take<uint8_t>(R, "flags");
+  ws.count = cv.take<int>(E, "count");
+  ws.offset = cv.take<int>(E + 1, "offset");
+  ws.pair_order = cv.take<int>(R * k, "pair_order");
+  ws.pos_of_pair = cv.take<int>(R * k, "pos_of_pair");
+  ws.active = cv.take<int>(E, "active");
+  ws.n_active = cv.take<int>(1, "n_active");
+  ws.h = cv.take<float>(R * k * I, "h");
+  ws.h_amax = cv.take<unsigned>(E, "h_amax");
+  ws.h_sg = cv.take<float>(E, "h_sg");
+  ws.h_codes = cv.take<uint8_t>(R * k * I / 2, "h_codes");
+  ws.h_sf = cv.take<uint8_t>(R * k * I / 16, "h_sf");
+  ws.done = cv.take<unsigned>(E, "done");
+  ws.o = cv.take<float>(R * k * H, "o");
+  ws.x_pool = cv.take<uint8_t>(R * k * H / 2, "x_pool");
+  ws.x_lines = cv.take<uint8_t>(R * k * (H / 64) * 16, "x_lines");
+  ws.h_lines = cv.take<uint8_t>(R * k * (I / 64) * 16, "h_lines");
   const size_t V = (size_t)moe::virtual_slots((int)E, (int)(R * k));
-  ws.act_info = carve<unsigned>(cur, V);
-  ws.ready_info = carve<unsigned>(cur, V);
-  ws.n_virtual = carve<int>(cur, 1);
-  ws.rg_count = carve<unsigned>(cur, 16);
-  ws.counters = carve<unsigned>(cur, 4);
-  ws.err = carve<unsigned>(cur, 1);
-  return (size_t)(cur - base);
+  ws.act_info = cv.take<unsigned>(V, "act_info");
+  ws.ready_info = cv.take<unsigned>(V, "ready_info");
+  ws.n_virtual = cv.take<int>(1, "n_virtual");
+  ws.rg_count = cv.take<unsigned>(16, "rg_count");
+  ws.counters = cv.take<unsigned>(4, "counters");
+  ws.err = cv.take<unsigned>(2, "err");
+  // the guards' offsets, for the fill and check kernels (no guard after them)
+  const size_t n_guards = guards ? guards->size() : 64;
+  unsigned long long* offs = reinterpret_cast<unsigned long long*>(cv.cur);
+  cv.cur += (n_guards * sizeof(unsigned long long) + 255) / 256 * 256;
+  if (guard_offsets) *guard_offsets = offs;
+  return (size_t)(cv.cur - base);
 }
 
 int check_rows(const moe_decode_t* h, int rows) {
@@ -473,7 +522,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   tg.local_route = td.local_route = local_route ? 1 : 0;
   tg.rows = td.rows = rows;
   tg.S = td.S = 1;  // the router summed its slices (cluster_sum)
-  tg.rbias = td.rbias = w.router_bias;
+  tg.rbias = td.rbias = nullptr;  // the router's cluster sum added it
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
                          td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);
@@ -651,10 +700,25 @@ int moe_decode_create(const moe_decode_dims* dims, const moe_layer_weights* laye
     delete h;
     return fail(MOE_ENOMEM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
   }
-  layout_workspace(h->ws, static_cast<uint8_t*>(h->ws_mem), d, h->S);
+  layout_workspace(h->ws, static_cast<uint8_t*>(h->ws_mem), d, h->S, &h->guards, &h->guard_offsets);
   h->ws.wait_ns = moe::kDefaultWaitNs;
   const size_t io = (size_t)d.max_rows * d.hidden;
   e = cudaMemset(h->ws_mem, 0, h->ws_bytes);
+  // the guards: their offsets to the device, their patterns written, and the
+  // error word's second slot (the first changed guard) set to "none"
+  if (e == cudaSuccess) {
+    std::vector<unsigned long long> offs;
+    for (const Guard& g : h->guards) offs.push_back(g.offset);
+    e = cudaMemcpy(h->guard_offsets, offs.data(), offs.size() * sizeof(unsigned long long),
+                   cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaMemset(h->ws.err + 1, 0xFF, sizeof(unsigned));
+  if (e == cudaSuccess) {
+    const int n = (int)h->guards.size();
+    guard_kernel<<<(n + 127) / 128, 128>>>(static_cast<uint8_t*>(h->ws_mem), h->guard_offsets, n, 0,
+                                           h->ws.err);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = cudaMalloc(&h->io_branch, io * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->io_stream, io * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h->io_out, io * 2);
@@ -961,15 +1025,36 @@ int moe_decode_last_error(moe_decode_t* h) {
   if (!h) return fail(MOE_EINVAL, "null handle");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
-  unsigned flag = 0;
-  e = cudaMemcpy(&flag, h->ws.err, sizeof(flag), cudaMemcpyDeviceToHost);
+  // the workspace guards: a changed one latches kDevCanary and its index
+  const int n = (int)h->guards.size();
+  guard_kernel<<<(n + 127) / 128, 128>>>(static_cast<uint8_t*>(h->ws_mem), h->guard_offsets, n, 1,
+                                         h->ws.err);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "workspace guard check");
+  unsigned flag[2] = {0u, 0u};
+  e = cudaMemcpy(flag, h->ws.err, sizeof(flag), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "error flag read");
-  if (flag) {
+  if (flag[0]) {
+    const unsigned none = 0xFFFFFFFFu;
     cudaMemset(h->ws.err, 0, sizeof(unsigned));
-    return fail(MOE_EDEVICE, "device-side error %u (1 = bounded wait gave up, 2 = bad routing)",
-                flag);
+    cudaMemcpy(h->ws.err + 1, &none, sizeof(none), cudaMemcpyHostToDevice);
+    if (flag[0] == moe::kDevCanary && flag[1] < h->guards.size()) {
+      // the guard is rewritten: the next check reports only new damage
+      guard_kernel<<<(n + 127) / 128, 128>>>(static_cast<uint8_t*>(h->ws_mem), h->guard_offsets, n, 0,
+                                             h->ws.err);
+      cudaDeviceSynchronize();
+      return fail(MOE_EDEVICE, "device-side error 4: the workspace guard after region '%s' changed "
+                  "(a write past that region's end)", h->guards[flag[1]].name);
+    }
+    return fail(MOE_EDEVICE, "device-side error %u (1 = bounded wait gave up, 2 = bad routing, "
+                "3 = an index out of range in a bounds-check build)", flag[0]);
   }
   return MOE_OK;
+}
+
+int moe_decode_build_info(void) {
+  return (moe::kBoundsCheck ? 1 : 0) | (MOE_EXPERT_TC ? 0 : 2);
 }
 
 size_t moe_decode_workspace_bytes(const moe_decode_t* h) { return h ? h->ws_bytes : 0; }

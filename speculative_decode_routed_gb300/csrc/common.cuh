@@ -20,6 +20,20 @@ __device__ __forceinline__ void latch_error(unsigned* err, unsigned code) {
   if (err) atomicCAS(err, 0u, code);
 }
 
+// Bounds-check builds (-DMOE_BOUNDS_CHECK) test every index that comes from
+// data -- a pair id, a pooled position, a routed row -- before it addresses
+// memory: a bad one latches kDevBadIndex and the access is skipped, where
+// the normal build (in which the routing makes the indexes valid) compiles
+// the test away.  A substitute for a memory sanitizer, which this device's
+// pool does not offer.
+#ifdef MOE_BOUNDS_CHECK
+#define MOE_IN_BOUNDS(cond, err_word) ((cond) ? true : (latch_error((err_word), kDevBadIndex), false))
+constexpr bool kBoundsCheck = true;
+#else
+#define MOE_IN_BOUNDS(cond, err_word) true
+constexpr bool kBoundsCheck = false;
+#endif
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

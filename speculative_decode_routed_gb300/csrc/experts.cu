@@ -149,7 +149,8 @@ __device__ __forceinline__ void load_act(const ExpertParams& p, bool gate_up, in
   for (int a = 0; a < RB; ++a) {
     if (a < rb && live) {
       const int pos = pos0 + a;
-      const int row = gate_up ? __ldcg(ws.pair_order + pos) / p.k : pos;
+      int row = gate_up ? __ldcg(ws.pair_order + pos) / p.k : pos;
+      if (!MOE_IN_BOUNDS(row >= 0 && row < p.ws_pairs, ws.err)) row = 0;
       const uint4 c = __ldcg(reinterpret_cast<const uint4*>(codes + (size_t)row * p.KB) + cc);
       if (kF16)
         chunk_to_f16(c, av + a * W);
@@ -275,7 +276,8 @@ __device__ __forceinline__ void run_group(const ExpertParams& p, const Smem& sm,
       float acc_o = 0.0f;
       for (int i = 0; i < wpg; ++i) acc_o += red[((w / TW) * wpg + i) * V + (w % TW) * RB + a];
       const int pair = sm.pairs[a0 + a];
-      ws.o[(size_t)pair * p.H + tile * p.T + w] = acc_o * sc0;
+      if (MOE_IN_BOUNDS(pair >= 0 && pair < p.ws_pairs, ws.err))
+        ws.o[(size_t)pair * p.H + tile * p.T + w] = acc_o * sc0;
     }
   }
 }

@@ -330,7 +330,7 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   __syncthreads();
   const bool valid = e >= 0;
   int a = 0, rank = 0, cnt = 0;
-  if (valid) {
+  if (valid && MOE_IN_BOUNDS(r < 32, ws.err)) {
     a = wbase[e >> 5] + __popc(emap[e >> 5] & ((1u << (e & 31)) - 1u));  // active index of e
     const unsigned m = rmask[e];
     rank = __popc(m & ((1u << r) - 1u));                                   // earlier rows of e
@@ -363,7 +363,7 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   }
   __syncthreads();
   const int n_valid = aoff[kMaxPairsTc];
-  if (valid) {
+  if (valid && MOE_IN_BOUNDS(a < kMaxPairsTc && aoff[a] + rank < npairs, ws.err)) {
     const int pos = aoff[a] + rank;
     sm.porder[pos] = tid;
     if (rank == 0) {
@@ -491,7 +491,8 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
   const Workspace& ws = p.ws;
   // under local routing an expert is one work item: its pooled rows are the item's
   const int pos0 = p.local_route ? pos0_local : __ldcg(ws.offset + e);
-  const int ne = p.local_route ? ne_local : __ldcg(ws.offset + e + 1) - pos0;
+  int ne = p.local_route ? ne_local : __ldcg(ws.offset + e + 1) - pos0;
+  if (!MOE_IN_BOUNDS(pos0 >= 0 && ne >= 1 && pos0 + ne <= p.ws_pairs, ws.err)) ne = 0;
   const int parts = (ne + kVirtualPairs - 1) / kVirtualPairs;
   const float am = warp_max(amax_part);
   if ((t & 31) == 0 && am > 0.0f) atomic_max_nonneg(ws.h_amax + e, am);
@@ -753,8 +754,10 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (new_e && kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne);
       if (new_part && (!kGU || p.direct)) {
         tc_named_sync();  // nobody still reads the previous part's pair ids
-        for (int jj = t; jj < ne; jj += kEpiThreads)
-          sm.pairs[jj] = p.local_route ? sm.porder[pos0 + jj] : __ldcg(ws.pair_order + pos0 + jj);
+        for (int jj = t; jj < ne; jj += kEpiThreads) {
+          const int pr = p.local_route ? sm.porder[pos0 + jj] : __ldcg(ws.pair_order + pos0 + jj);
+          sm.pairs[jj] = MOE_IN_BOUNDS(pr >= 0 && pr < p.ws_pairs, ws.err) ? pr : -1;
+        }
         tc_named_sync();
       }
       cur_pos0 = pos0;
@@ -786,7 +789,9 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (kGU && p.direct) {
         // the B columns are the rows: pair jj reads the column of its row
         for (int jj = 0; jj < ne; ++jj) {
-          const uint32_t col = (uint32_t)(sm.pairs[jj] / p.k);
+          const int pr = sm.pairs[jj];
+          if (kBoundsCheck && !MOE_IN_BOUNDS(pr >= 0 && pr / p.k < kVirtualPairs, ws.err)) continue;
+          const uint32_t col = (uint32_t)(pr / p.k);
           float g = 0.0f, u = 0.0f;
           for (int qq = 0; qq < nparts; ++qq) {
             uint32_t ra, rb;
@@ -841,7 +846,8 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             for (int n = 0; n < 16; ++n) {
               if (n < cnt) {
                 const int pair = sm.pairs[c0 + n];
-                st_keep(ws.o + (size_t)pair * p.H + (size_t)tile * 128 + m, acc0[n] * sc0, keep);
+                if (MOE_IN_BOUNDS(pair >= 0 && pair < p.ws_pairs, ws.err))
+                  st_keep(ws.o + (size_t)pair * p.H + (size_t)tile * 128 + m, acc0[n] * sc0, keep);
               }
             }
           }
@@ -949,6 +955,7 @@ __global__ void pool_gather_kernel(PoolParams p) {
   const int pos = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (pos >= p.rows * p.k) return;
   const int row = __ldcg(ws.pair_order + pos) / p.k;
+  if (!MOE_IN_BOUNDS(row >= 0 && row < p.rows, ws.err)) return;
   const uint4* src = reinterpret_cast<const uint4*>(ws.x_codes + (size_t)row * (p.H / 2));
   uint4* dst = reinterpret_cast<uint4*>(ws.x_pool + (size_t)pos * (p.H / 2));
   for (int c = lane; c < p.H / 32; c += 32) dst[c] = __ldcg(src + c);

@@ -30,6 +30,8 @@ enum DeviceError : unsigned {
   kDevOk = 0,
   kDevWaitTimeout = 1,    // a bounded mbarrier wait gave up
   kDevBadRouting = 2,     // routing produced an out-of-range id / count
+  kDevBadIndex = 3,       // bounds-check builds: a data-dependent index out of range (skipped)
+  kDevCanary = 4,         // a workspace guard word changed (a write past a region's end)
 };
 
 // Library-owned scratch, sized at create for max_rows rows.
@@ -68,7 +70,7 @@ struct Workspace {
   unsigned* rg_count;    // [16]        router CTA arrivals per block of 8 rows
   unsigned* counters;    // [4]         [0] router row blocks routed, [1] gate/up item claims,
                          //             [2] down item claims, [3] experts ready
-  unsigned* err;         // [1]         latched DeviceError
+  unsigned* err;         // [1]         latched DeviceError; [1]: the first changed guard's index
   unsigned long long wait_ns;  // limit of every bounded wait in the kernels (a value, not a pointer)
 };
 
@@ -110,9 +112,9 @@ struct RouterParams {
   const float* bias;            // [E] or null
   int line_rows;                // row stride of the scale lines (max_rows * k)
   int cluster_sum;              // 1 (at most 8 rows): the S slice CTAs of an expert group form a
-                                // cluster whose first CTA sums their partials in slice order into
-                                // logit_part's first slice (the logits without bias), so routing
-                                // reads one slice
+                                // cluster whose first CTA sums their partials in slice order, then
+                                // adds the bias, into logit_part's first slice (the logits), so
+                                // routing reads one slice and no bias
   int route_in_experts;         // 1 (at most 8 rows, tensor-core experts): the experts kernel
                                 // routes the rows and pools the pairs itself; the router only
                                 // writes the partial logits and the MoE input's quantization

@@ -74,8 +74,10 @@ __device__ void route_rows(const RouterParams& p, const RouteSmem& rs, int r0, i
   const int warp = threadIdx.x >> 5;
   if (warp < nr) {
     const Workspace& ws = p.ws;
-    const RouteRow rr{ws.logit_part, p.cluster_sum ? 1 : p.S, p.rows, p.E, p.k, p.bias, ws.logits,
-                      ws.ids, ws.gates, ws.flags, ws.err, rs.sids};
+    // with the cluster sum the first slice holds the logits, bias included
+    const RouteRow rr{ws.logit_part, p.cluster_sum ? 1 : p.S, p.rows, p.E, p.k,
+                      p.cluster_sum ? nullptr : p.bias, ws.logits, ws.ids, ws.gates, ws.flags, ws.err,
+                      rs.sids};
     route_row(rr, r0 + warp, rs.lg + warp * p.E);
   }
 }
@@ -158,7 +160,7 @@ __device__ void pool_small(const RouterParams& p, uint8_t* smem, bool ids_in_sme
     ws.n_virtual[0] = v;
   }
   __syncthreads();
-  if (valid) {
+  if (valid && MOE_IN_BOUNDS(cnt[eq] + rank < npairs, ws.err)) {
     const int pos = cnt[eq] + rank;
     ws.pair_order[pos] = tid;
     ws.pos_of_pair[tid] = pos;
@@ -257,6 +259,7 @@ __device__ void pool_all(const RouterParams& p, uint8_t* smem, bool ids_in_smem)
     for (int w = 0; w < (r >> 5); ++w) rank += __popc(mask[e * RW + w]);
     rank += __popc(mask[e * RW + (r >> 5)] & ((1u << (r & 31)) - 1u));
     const int pos = off[e] + rank;
+    if (!MOE_IN_BOUNDS(pos < npairs, ws.err)) continue;
     ws.pair_order[pos] = q;
     ws.pos_of_pair[q] = pos;
   }
@@ -330,6 +333,9 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
   const int nch = p.H / 8;
   const int c0 = sl * nch / p.S, c1 = (sl + 1) * nch / p.S;
 
+  // the slice-0 CTA's bias for its cluster sum (static): before the wait
+  const int bias_e = blockIdx.x * p.EG + (int)(threadIdx.x % kRouterWarps);
+  const float bias_v = (p.cluster_sum && p.bias && sl == 0 && bias_e < p.E) ? __ldg(p.bias + bias_e) : 0.0f;
   // the expert's slice of the router weights (static): before the wait
   uint4 wv[kRouterChunks];
 #pragma unroll
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
       const int ee = blockIdx.x * p.EG + wi;
       float acc = 0.0f;
       for (int q = 0; q < p.S; ++q) acc += *cluster.map_shared_rank(&s_part[r * kRouterWarps + wi], q);
+      if (p.bias) acc += bias_v;  // the same fp32 sum, then the bias, as the routing would add it
       if (wi < p.EG && ee < p.E) ws.logit_part[(size_t)r * p.E + ee] = acc;
     }
     // every peer keeps its partials until the sums are read

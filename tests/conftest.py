@@ -41,7 +41,8 @@ def _ensure_cuda_lib():
     from speculative_decode_routed_gb300 import _build as pb
     srcs = [os.path.join(pb.CSRC, f) for f in os.listdir(pb.CSRC)]
     srcs.append(os.path.join(ROOT, "include", "moe_decode.h"))
-    if os.path.exists(pb.LIB) and all(os.path.getmtime(s) <= os.path.getmtime(pb.LIB) for s in srcs):
+    if all(os.path.exists(lib) and all(os.path.getmtime(s) <= os.path.getmtime(lib) for s in srcs)
+           for lib in (pb.LIB, pb.LIB_BOUNDS)):
         return
     if shutil.which("nvcc") is None:
         return  # the tests that load the library then fail loudly

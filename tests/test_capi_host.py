@@ -283,3 +283,13 @@ def test_header_is_plain_c_and_a_c_program_links(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.split()[0] == str(moe.MOE_EINVAL)
+
+
+def test_build_info_names_each_variant():
+    """The default library is the tensor-core build without bounds checks; the
+    bounds-check variant that build() makes beside it says so."""
+    from speculative_decode_routed_gb300 import _build as pb
+    assert moe.lib().moe_decode_build_info() == 0
+    b = ctypes.CDLL(pb.LIB_BOUNDS)
+    b.moe_decode_build_info.restype = ctypes.c_int
+    assert b.moe_decode_build_info() == 1

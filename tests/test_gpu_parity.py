@@ -511,6 +511,47 @@ def test_bounded_wait_gives_up_and_the_handle_recovers():
     dec.close()
 
 
+def test_workspace_guards_catch_a_stray_write():
+    """A write past the end of a workspace region lands in the guard after it,
+    and the next error check reports the region by name (then the guard is
+    rewritten, so a later check is clean).  The write is made here, by the
+    host, into the guard that follows the MoE input x: every region is
+    followed by a 256-byte guard, and x holds max_rows * H bf16 values."""
+    import speculative_decode_routed_gb300 as moe
+    from helpers import _CudaArray
+    w = synth.WORKLOADS["tiny"]
+    sgpu = _sgpu()
+    dec = sgpu.build(w)
+    stream, branch = sgpu.step_tensors(w)
+    out = torch.empty_like(branch)
+    dec.step(w.rows, branch, stream, out)
+    torch.cuda.synchronize()
+    dec.check()                                     # every guard intact after a step
+    x_bytes = dec.dims.max_rows * dec.dims.hidden * 2
+    guard = dec.debug().x + (x_bytes + 255) // 256 * 256
+    torch.as_tensor(_CudaArray(guard, (4,), "|u1"), device="cuda").fill_(0x77)
+    torch.cuda.synchronize()
+    with pytest.raises(moe.MoeError) as err:
+        dec.check()
+    assert err.value.code == moe.MOE_EDEVICE and "region 'x'" in str(err.value)
+    dec.check()
+    dec.step(w.rows, branch, stream, out)
+    dec.check()
+    dec.close()
+
+
+def test_loaded_library_variant():
+    """The library the tests run against: the bounds-check variant when the
+    environment asks for it (the bounds-check run of this file), else the
+    default build."""
+    import os
+
+    import speculative_decode_routed_gb300 as moe
+    info = moe.lib().moe_decode_build_info()
+    want = 1 if os.environ.get("MOE_DECODE_EXPECT_BOUNDS") == "1" else 0
+    assert info & 1 == want
+
+
 def test_tile_codes_matches_the_layout():
     """moe_tile_codes against the layout its header states (untiled on the
     host), the bytes of a partial last K-block zero."""
