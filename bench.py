@@ -638,7 +638,7 @@ def run_dense(args, w):
         bufs.append((torch.from_numpy(s).to(device),
                      torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)))
     cs = torch.cuda.current_stream(device)
-    for s, a in bufs:                                 # eager first calls set cuBLAS up
+    for s, a in bufs:                                 # eager first calls, outside capture
         dl.layer(rows, a, s.clone())
     torch.cuda.synchronize(device)
     graphs = []
@@ -676,7 +676,7 @@ def run_dense(args, w):
     # up to 8 rows (H and I multiples of 128) the library streams both
     # projections itself: four kernels of its own, SiLU * mul inside gate/up
     streamed = rows <= 8 and H % 128 == 0 and I % 128 == 0
-    own = 4 if streamed else 3
+    own = 4                                           # every kernel the library's own
     gu_gbs = byt["gate_up"] / (k_ms[1] * 1e-3) / 1e9
     dn_gbs = byt["down"] / (k_ms[3] * 1e-3) / 1e9
     step_gbs = byt["total"] / (ms * 1e-3) / 1e9 * ws
@@ -716,19 +716,19 @@ def run_dense(args, w):
         "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
         "bytes_per_layer_step": int(byt["total"]),
         "roofline": {"kernel": "gate/up projection + SiLU * mul (split-K weight-streaming kernel, bf16 mma.sync)"
-                     if streamed else "gate/up projection (cuBLAS bf16 GEMM)", "bound": "hbm",
+                     if streamed else "gate/up projection + SiLU * mul (tcgen05 bf16 projection kernel)",
+                     "bound": "hbm",
                      "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gu_gbs / peak, 4),
                      "traffic": _dense_traffic(H, I, rows) if streamed else None, "peak_kind": peak_kind,
                      "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gate_up"])},
-        "kernels_us": dict({"boundary_attn": round(k_ms[0] * 1000, 2), "gate_up": round(k_ms[1] * 1000, 2)},
-                           **({} if streamed else {"silu_mul": round(k_ms[2] * 1000, 2)}),
-                           down=round(k_ms[3] * 1000, 2), boundary_ffn=round(k_ms[4] * 1000, 2),
-                           down_gbs=round(dn_gbs, 1)),
+        "kernels_us": {"boundary_attn": round(k_ms[0] * 1000, 2), "gate_up": round(k_ms[1] * 1000, 2),
+                       "down": round(k_ms[3] * 1000, 2), "boundary_ffn": round(k_ms[4] * 1000, 2),
+                       "down_gbs": round(dn_gbs, 1)},
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT,
                 "h2d_bytes_per_step": rows * H * (4 + 2), "d2h_bytes_per_step": rows * H * 4},
         "gpu_launches": own * args.steps,
-        "library_launches": (dl.kernel_count(rows) - own) * args.steps,
+        "library_launches": (dl.kernel_count(rows) - own) * args.steps,   # 0: no library kernels
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and ws == 1:
@@ -870,7 +870,7 @@ def run_ctxkv(args, w):
         "weight_stream_frac_of_peak": round(step_gbs / (peak * ws), 4),
         "bytes_per_step": int(byt["total"]),
         "roofline": {"kernel": "K/V projection (split-K weight-streaming kernel, bf16 mma.sync)" if streamed
-                     else "K/V projection (cuBLAS strided-batched bf16 GEMM)", "bound": "hbm",
+                     else "K/V projection (tcgen05 bf16 projection kernel)", "bound": "hbm",
                      "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gemm_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
                      "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gemm"])},
@@ -879,8 +879,8 @@ def run_ctxkv(args, w):
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT,
                 "h2d_bytes_per_step": n * H * 2 + n * 8 * 2,
                 "d2h_bytes_per_step": 2 * L * n * KVH * D * 2},
-        "gpu_launches": (3 if streamed else 2) * args.steps,
-        "library_launches": (op.kernel_count(n) - (3 if streamed else 2)) * args.steps,
+        "gpu_launches": 3 * args.steps,
+        "library_launches": (op.kernel_count(n) - 3) * args.steps,   # 0: no library kernels
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and ws == 1:

@@ -351,8 +351,11 @@ int moe_nvfp4_quantize_noalloc(const float* v, int64_t rows, int64_t cols, uint8
  *   a  = bf16(silu(g) * u);  f = bf16(W_down a)
  *   s2 = s1 + rmsnorm(f) * w_post_ffn                      (fp32 stream)
  * Up to 8 rows with H and I multiples of 128 the projections are the
- * library's own weight-streaming kernels (fp32 accumulation, SiLU * mul fused
- * into gate/up); otherwise plain bf16 GEMMs (cuBLAS, fp32 accumulation).
+ * library's own weight-streaming kernels; otherwise its tensor-core
+ * projection kernel (tcgen05, bf16 operands).  Either way fp32 accumulation,
+ * SiLU * mul fused into gate/up, and the down projection's split-K partials
+ * summed in split order by the output boundary: four launches, all the
+ * library's own.
  * ---------------------------------------------------------------------- */
 typedef struct moe_dense_s moe_dense_t;
 
@@ -378,7 +381,7 @@ typedef struct {                 /* device pointers into the handle's workspace 
   void* f;                       /* bf16 [rows][H]  the feed-forward output */
 } moe_dense_debug_view;
 
-/* Validates the shapes, allocates the workspace and a cuBLAS handle. */
+/* Validates the shapes and allocates the workspace. */
 int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe_dense_t** out);
 
 /* One layer's MLP block for `rows` rows: attn_out bf16 [rows][H] (8-byte
@@ -405,12 +408,16 @@ int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* out);
 int moe_dense_layer_host(moe_dense_t* h, int rows, const uint16_t* attn_host, float* stream_host,
                          void* cuda_stream);
 
-/* Kernels one moe_dense_layer call of `rows` rows launches: four of the
- * library's own on the streamed path, else its three and the cuBLAS GEMMs'
- * (whose count cuBLAS chooses per shape).
+/* Kernels one moe_dense_layer call of `rows` rows launches: four, all the
+ * library's own.
  * Counted by capturing a call into a graph on a private stream (nothing
  * runs).  Returns the count (> 0) or a negative MOE_E* code. */
 int moe_dense_kernel_count(moe_dense_t* h, int rows);
+
+/* Synchronizes the device and returns MOE_EDEVICE if a projection latched a
+ * device-side error (code 1: a bounded wait gave up) since the last call (and
+ * clears it), else MOE_OK. */
+int moe_dense_last_error(moe_dense_t* h);
 
 void moe_dense_destroy(moe_dense_t* h);
 
@@ -494,7 +501,7 @@ int moe_ctxkv_project_host(moe_ctxkv_t* h, int n_ctx, const uint16_t* context_ho
  * projection, key norm + rotation + cache write); synchronizes and writes
  * their durations (ms) to ms_host[0..2].  For measurement.  Up to 8 rows
  * (and H a multiple of 64) the projection is the library's split-K
- * weight-streaming kernel, beyond that a batched cuBLAS GEMM. */
+ * weight-streaming kernel, beyond that its tensor-core projection kernel. */
 int moe_ctxkv_profile(moe_ctxkv_t* h, int n_ctx, const uint16_t* context, const int64_t* positions,
                       const int64_t* slots, int slot_stride, uint16_t* k_cache, uint16_t* v_cache,
                       int64_t n_slots, void* cuda_stream, float* ms_host);
@@ -507,7 +514,7 @@ int moe_ctxkv_debug(moe_ctxkv_t* h, moe_ctxkv_debug_view* view);
 int moe_ctxkv_last_error(moe_ctxkv_t* h);
 
 /* Kernels one moe_ctxkv_project call of n_ctx rows launches (the library's
- * three; with more than 8 rows the norm and key kernels plus cuBLAS's).
+ * three, all its own). 
  * Counted by capturing a call into a graph on a private stream (nothing
  * runs).  Returns the count (> 0) or a negative MOE_E* code. */
 int moe_ctxkv_kernel_count(moe_ctxkv_t* h, int n_ctx);

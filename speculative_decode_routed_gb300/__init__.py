@@ -32,7 +32,7 @@ EXPORTS = (
     "moe_decode_destroy", "moe_decode_strerror", "moe_decode_error_message",
     "moe_nvfp4_quantize", "moe_nvfp4_quantize_noalloc",
     "moe_dense_create", "moe_dense_layer", "moe_dense_layer_profile", "moe_dense_debug",
-    "moe_dense_layer_host", "moe_dense_kernel_count", "moe_dense_destroy",
+    "moe_dense_layer_host", "moe_dense_kernel_count", "moe_dense_last_error", "moe_dense_destroy",
     "moe_ctxkv_create", "moe_ctxkv_project", "moe_ctxkv_project_host", "moe_ctxkv_profile", "moe_ctxkv_debug",
     "moe_ctxkv_last_error", "moe_ctxkv_kernel_count", "moe_ctxkv_destroy",
 )
@@ -133,6 +133,7 @@ def _lib():
             "moe_dense_debug": (i32, [vp, ctypes.POINTER(DenseDebugView)]),
             "moe_dense_layer_host": (i32, [vp, i32, vp, vp, vp]),
             "moe_dense_kernel_count": (i32, [vp, i32]),
+            "moe_dense_last_error": (i32, [vp]),
             "moe_dense_destroy": (None, [vp]),
             "moe_ctxkv_create": (i32, [ctypes.POINTER(CtxKvDims), ctypes.POINTER(CtxKvWeights),
                                        ctypes.POINTER(vp)]),
@@ -405,6 +406,9 @@ class DenseLayer:
         v = DenseDebugView()
         _check(_lib().moe_dense_debug(self.handle, ctypes.byref(v)), "moe_dense_debug")
         return v
+
+    def check(self):
+        _check(_lib().moe_dense_last_error(self.handle), "moe_dense_last_error")
 
     def close(self):
         if self.handle:

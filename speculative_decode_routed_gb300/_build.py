@@ -11,7 +11,8 @@ LIB = os.path.join(HERE, "libmoe_decode.so")
 # when MOE_DECODE_LIB names it
 BUILD_BOUNDS = os.path.join(HERE, "_build_bounds")
 LIB_BOUNDS = os.path.join(HERE, "libmoe_decode_bounds.so")
-SOURCES = ["boundary.cu", "router.cu", "experts.cu", "experts_tc.cu", "quant.cu", "quant_noalloc.cu", "dense.cu", "ctxkv.cu", "capi.cu"]
+SOURCES = ["boundary.cu", "router.cu", "experts.cu", "experts_tc.cu", "tc_gemm.cu", "quant.cu", "quant_noalloc.cu",
+           "dense.cu", "ctxkv.cu", "capi.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -29,4 +30,4 @@ def compile_commands(nvcc="nvcc", extra=(), build_dir=BUILD):
 
 
 def link_command(objects, nvcc="nvcc", lib=LIB):
-    return [nvcc, *ARCH, "-shared", "-o", lib, *objects, "-lcublas"]
+    return [nvcc, *ARCH, "-shared", "-o", lib, *objects]

@@ -14,13 +14,14 @@
 // both norms and writes the L layer inputs.  Up to 8 rows the projection is
 // the split-K weight-streaming kernel (gemv.cuh): fp32 partial sums per
 // K-split, launched with programmatic dependent launch so its first weight
-// loads overlap the norms; beyond 8 rows it is a batched bf16 GEMM (cuBLAS).
+// loads overlap the norms; beyond 8 rows it is the library's tensor-core
+// projection kernel (tc_gemm.cu), split-K partials while they fit the
+// handle's buffer (summed here like the streaming kernel's), else bf16 K/V.
 // kv_rope_kernel gives each (layer, row, head) one warp: it sums the partials
 // in split order (or reads the GEMM's bf16 output), and the head's D values
 // sit D/32 to a lane, so the key norm is a warp sum and the rotation's
 // partner dimension (j + D/2) is 16 lanes away (one shuffle).  The rotation's
 // cosines and sines come from a table built once at create in fp64.
-#include <cublas_v2.h>
 
 #include <cmath>
 #include <cstdio>
@@ -29,6 +30,7 @@
 #include "../../include/moe_decode.h"
 #include "common.cuh"
 #include "gemv.cuh"
+#include "tc_gemm.h"
 #include "moe_decode_internal.h"
 
 namespace moe {
@@ -266,13 +268,14 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
 struct moe_ctxkv_s {
   moe_ctxkv_dims d;
   moe_ctxkv_weights w;
-  cublasHandle_t blas;
-  void* blas_ws;
+  moe::GemmMaps maps;               // the tensor-core projection's tensor maps (W_kv over u)
+  int tc_part_rows;                 // up to this many rows its split-K partials fit the buffer
+  int tc_max_splits;                // and this many splits; beyond, it writes bf16 kv directly
   void* base;                       // one allocation: the buffers below
   __nv_bfloat16 *fc, *u, *kv, *k, *v;
   float2* cs;                       // rotary table, or null
   unsigned* err;
-  float* part;                      // split-K partials [S][L][8][2 * KVH * D], or null
+  float* part;                      // split-K partials [S][L][rows][2 * KVH * D]
   int splits;                       // K-splits of the streaming projection; 0: none
   int num_sms;
   uint8_t* io;                      // host-buffer calls' copies: context [n][H] bf16,
@@ -281,19 +284,13 @@ struct moe_ctxkv_s {
 
 namespace {
 
-constexpr size_t kCtxBlasWorkspace = 8u << 20;
+constexpr size_t kCtxPartBudget = 64u << 20;  // bytes of split-K partials the handle keeps
 
 bool ck_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int ck_cuda(cudaError_t e, const char* what) {
   char buf[200];
   snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
-  return moe::api_fail(MOE_ECUDA, buf);
-}
-
-int ck_blas(cublasStatus_t st, const char* what) {
-  char buf[160];
-  snprintf(buf, sizeof(buf), "%s: cuBLAS status %d", what, (int)st);
   return moe::api_fail(MOE_ECUDA, buf);
 }
 
@@ -352,6 +349,8 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   np.fc = h->fc;
   np.u = h->u;
   const bool stream_w = h->splits > 0 && a.n <= 8;
+  moe::GemmParams gp_tc;
+  int tc_S = 0;  // the tensor-core projection's splits when it left partials
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -383,16 +382,18 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
     e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel<false>, gp);
     if (e != cudaSuccess) return ck_cuda(e, "K/V projection launch");
   } else {
-    cublasStatus_t st = cublasSetStream(h->blas, s);
-    if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "cublasSetStream");
-    const float one = 1.0f, zero = 0.0f;
-    // kv[l] [n][2KD] = u[l] [n][H] . W_kv[l]^T  (column-major: W_kv[l] is H x 2KD)
-    st = cublasGemmStridedBatchedEx(
-        h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * KD, a.n, d.hidden, &one, h->w.w_kv, CUDA_R_16BF,
-        d.hidden, (long long)2 * KD * d.hidden, h->u, CUDA_R_16BF, d.hidden, (long long)a.n * d.hidden,
-        &zero, h->kv, CUDA_R_16BF, 2 * KD, (long long)a.n * 2 * KD, d.n_layers, CUBLAS_COMPUTE_32F,
-        CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return ck_blas(st, "K/V projection GEMM");
+    // the tensor-core projection: split-K partials while they fit the
+    // handle's buffer, else the bf16 projection itself
+    const bool partial = a.n <= h->tc_part_rows;
+    if (!moe::plan_gemm(gp_tc, partial ? moe::kGemmPartial : moe::kGemmBf16, d.n_layers, 2 * KD, d.hidden,
+                        a.n, 0, a.n, h->num_sms, partial ? h->tc_max_splits : 1))
+      return moe::api_fail(MOE_EUNSUPPORTED, "no tensor-core plan for the K/V projection");
+    gp_tc.part = h->part;
+    gp_tc.out = h->kv;
+    gp_tc.err = h->err;
+    e = moe::launch_gemm(gp_tc, h->maps, h->num_sms, s, !ev);
+    if (e != cudaSuccess) return ck_cuda(e, "K/V projection launch");
+    tc_S = partial ? gp_tc.S : 0;
   }
   mark(2);
   moe::KvRopeParams kp{};
@@ -405,8 +406,8 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   kp.cs = h->cs;
   kp.positions = a.positions;
   kp.kv = h->kv;
-  kp.part = stream_w ? h->part : nullptr;
-  kp.S = h->splits;
+  kp.part = (stream_w || tc_S) ? h->part : nullptr;
+  kp.S = stream_w ? h->splits : tc_S;
   kp.k_out = a.k_out ? reinterpret_cast<__nv_bfloat16*>(a.k_out) : h->k;
   kp.v_out = a.v_out ? reinterpret_cast<__nv_bfloat16*>(a.v_out) : h->v;
   kp.slots = a.slots;
@@ -484,7 +485,20 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
       return ck_cuda(e, "streaming projection shared memory");
     }
   }
-  const size_t b_part = h->splits ? (size_t)h->splits * L * 8 * 2 * KD * sizeof(float) : 0;
+  e = moe::gemm_set_smem();
+  if (e != cudaSuccess) {
+    delete h;
+    return ck_cuda(e, "tensor-core projection shared memory");
+  }
+  // the tensor-core projection's partials: up to 128 rows and 8 splits,
+  // fewer splits (or none: bf16 output) when the budget does not hold them
+  h->tc_part_rows = (int)(n < 128 ? n : 128);
+  const size_t per_split = L * (size_t)h->tc_part_rows * 2 * KD * sizeof(float);
+  h->tc_max_splits = (int)(kCtxPartBudget / per_split < 8 ? kCtxPartBudget / per_split : 8);
+  if (h->tc_max_splits == 0) h->tc_part_rows = 0;
+  const size_t part_stream = h->splits ? (size_t)h->splits * L * 8 * 2 * KD * sizeof(float) : 0;
+  const size_t part_tc = (size_t)h->tc_max_splits * per_split;
+  const size_t b_part = part_stream > part_tc ? part_stream : part_tc;
   auto up16 = [](size_t b) { return (b + 15) & ~(size_t)15; };
   const size_t b_fc = up16(2 * n * H), b_u = up16(2 * L * n * H), b_kv = up16(2 * L * n * 2 * KD),
                b_k = up16(2 * L * n * KD), b_cs = table * sizeof(float2);
@@ -492,14 +506,13 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16 + b_io;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kCtxBlasWorkspace);
   if (e != cudaSuccess) {
     cudaFree(base);
     moe_ctxkv_destroy(h);
     return moe::api_fail(MOE_ENOMEM, "context-KV workspace");
   }
   h->base = base;
-  h->part = h->splits ? reinterpret_cast<float*>(base) : nullptr;
+  h->part = b_part ? reinterpret_cast<float*>(base) : nullptr;
   base += b_part;
   h->fc = reinterpret_cast<__nv_bfloat16*>(base);
   h->u = reinterpret_cast<__nv_bfloat16*>(base + b_fc);
@@ -527,12 +540,11 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
     moe_ctxkv_destroy(h);
     return ck_cuda(e, "context-KV set-up");
   }
-  cublasStatus_t st = cublasCreate(&h->blas);
-  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, kCtxBlasWorkspace);
-  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);
-  if (st != CUBLAS_STATUS_SUCCESS) {
+  // W_kv [L * 2KD][H] over u [L * max_ctx][H]
+  e = moe::encode_gemm_maps(h->maps, h->w.w_kv, (int64_t)L * 2 * KD, h->u, (int64_t)L * n, (int)H);
+  if (e != cudaSuccess) {
     moe_ctxkv_destroy(h);
-    return ck_blas(st, "cuBLAS set-up");
+    return ck_cuda(e, "K/V projection tensor maps");
   }
   *out = h;
   return MOE_OK;
@@ -693,8 +705,6 @@ int moe_ctxkv_last_error(moe_ctxkv_t* h) {
 
 void moe_ctxkv_destroy(moe_ctxkv_t* h) {
   if (!h) return;
-  if (h->blas) cublasDestroy(h->blas);
-  cudaFree(h->blas_ws);
   cudaFree(h->base);
   delete h;
 }

@@ -21,12 +21,11 @@
 // (gemv.cuh): gate/up pairs each gate row with its up row in one task and
 // writes gu and SiLU * mul from its accumulators; the down projection leaves
 // fp32 split-K partials, which the output boundary sums in split order into
-// the bf16 branch.  Four launches chained by programmatic dependent launch.
-// Beyond 8 rows (or for widths the streamed kernels do not take) the
-// projections are plain bf16 GEMMs (cuBLAS, fp32 compute, bf16 out) and SiLU *
-// mul is one elementwise kernel.
-#include <cublas_v2.h>
-
+// the bf16 branch.  Beyond 8 rows (or for widths the streaming kernel does
+// not take) the projections are the library's tensor-core projection kernel
+// (tc_gemm.cu): gate/up with SiLU * mul from its two accumulators, down as
+// split-K partials the output boundary sums the same way.  Four launches
+// chained by programmatic dependent launch either way.
 #include <cstdio>
 #include <vector>
 
@@ -34,33 +33,20 @@
 #include "common.cuh"
 #include "gemv.cuh"
 #include "moe_decode_internal.h"
+#include "tc_gemm.h"
 
-namespace moe {
 namespace {
-
-__global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int I, int n,
-                                __nv_bfloat16* __restrict__ a) {
-  // gu: [rows][2I] (gate columns, then up columns); a: [rows][I]; n = rows * I
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const int r = i / I, j = i % I;
-    const float g = __bfloat162float(gu[(size_t)r * 2 * I + j]);
-    const float u = __bfloat162float(gu[(size_t)r * 2 * I + I + j]);
-    a[i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
-  }
+constexpr int kDenseMaxSplits = 8;  // K-splits of the tensor-core down projection
 }
-
-}  // namespace
-}  // namespace moe
 
 struct moe_dense_s {
   moe_dense_dims d;
   moe_dense_weights w;
   int cluster;
-  cublasHandle_t blas;
-  void* blas_ws;
-  size_t blas_ws_bytes;
+  moe::GemmMaps gu_maps, dn_maps;  // the tensor-core projections' tensor maps
+  unsigned* err;                   // [2] latched device error (a bounded wait that gave up)
   __nv_bfloat16 *x, *gu, *a, *f;  // [R][H], [R][2I], [R][I], [R][H]
-  float* part;                     // down projection's split-K partials [S][8][H], or null
+  float* part;                     // down projection's split-K partials [S][rows][H]
   float* io_stream;                // [R][H] the stream of a host-buffer call
   __nv_bfloat16* io_attn;          // [R][H] its attention output (when copied in)
   struct HostGraph {
@@ -76,16 +62,7 @@ struct moe_dense_s {
 
 namespace {
 
-constexpr size_t kBlasWorkspace = 8u << 20;
-
 bool dense_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-
-int blas_fail(cublasStatus_t st, const char* what) {
-  char buf[160];
-  snprintf(buf, sizeof(buf), "%s: cuBLAS status %d", what, (int)st);
-  return moe::api_fail(MOE_ECUDA, buf);
-}
 
 int cuda_err(cudaError_t e, const char* what) {
   char buf[200];
@@ -120,15 +97,16 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
   cudaError_t e = moe::launch_boundary(bp, h->cluster, s, false);
   if (e != cudaSuccess) return cuda_err(e, "pre-ffn boundary launch");
   mark(1);
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  int part_S = 0;
   if (h->down_splits && rows <= 8) {
     // Up to 8 rows: the library's weight-streaming projections.  Gate/up
     // pairs each gate row with its up row in one task and writes gu and
     // SiLU * mul itself; the down projection leaves split-K partials that the
     // output boundary sums.  Programmatic dependent launch between the four
     // kernels (except when profiled, where each launch is timed alone).
-    cudaLaunchAttribute pdl;
-    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t gc = {};
     gc.gridDim = dim3(h->num_sms, 1, 1);
     gc.blockDim = dim3(moe::kGemvThreads, 1, 1);
@@ -164,50 +142,41 @@ int dense_enqueue(moe_dense_t* h, int rows, const uint16_t* attn_out, float* str
     dp.KC = d.inter / h->down_splits;
     e = cudaLaunchKernelEx(&gc, moe::gemv_bf16_kernel<false>, dp);
     if (e != cudaSuccess) return cuda_err(e, "down projection launch");
-    mark(4);
-    bp.branch = nullptr;
-    bp.part = h->part;
-    bp.part_S = h->down_splits;
-    bp.part_out = h->f;
-    bp.w_post = h->w.w_post_ffn;
-    bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
-    bp.x_out = nullptr;
-    bp.round_norm = 0;
-    bp.stream_in = nullptr;
-    bp.aux = aux;
-    e = moe::launch_boundary(bp, h->cluster, s, !ev);
-    if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
-    mark(5);
-    return MOE_OK;
+    part_S = h->down_splits;
+  } else {
+    // Beyond: the tensor-core projection kernel, gate/up with SiLU * mul from
+    // its two accumulators, then down as split-K partials.
+    moe::GemmParams gp;
+    if (!moe::plan_gemm(gp, moe::kGemmGated, 1, 2 * d.inter, d.hidden, rows, d.inter, 0, h->num_sms, 1))
+      return moe::api_fail(MOE_EUNSUPPORTED, "no tensor-core plan for the gate/up projection");
+    gp.gu = h->gu;
+    gp.act = h->a;
+    gp.err = h->err;
+    e = moe::launch_gemm(gp, h->gu_maps, h->num_sms, s, !ev);
+    if (e != cudaSuccess) return cuda_err(e, "gate/up projection launch");
+    mark(2);
+    mark(3);  // SiLU * mul is part of the gate/up projection
+    moe::GemmParams dp;
+    if (!moe::plan_gemm(dp, moe::kGemmPartial, 1, d.hidden, d.inter, rows, 0, 0, h->num_sms, kDenseMaxSplits))
+      return moe::api_fail(MOE_EUNSUPPORTED, "no tensor-core plan for the down projection");
+    dp.part = h->part;
+    dp.err = h->err;
+    e = moe::launch_gemm(dp, h->dn_maps, h->num_sms, s, !ev);
+    if (e != cudaSuccess) return cuda_err(e, "down projection launch");
+    part_S = dp.S;
   }
-  cublasStatus_t st = cublasSetStream(h->blas, s);
-  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "cublasSetStream");
-  const float one = 1.0f, zero = 0.0f;
-  // gu [rows][2I] = x [rows][H] . W13^T  (column-major: W13 is H x 2I)
-  st = cublasGemmEx(h->blas, CUBLAS_OP_T, CUBLAS_OP_N, 2 * d.inter, rows, d.hidden, &one,
-                    h->w.w13, CUDA_R_16BF, d.hidden, h->x, CUDA_R_16BF, d.hidden, &zero, h->gu,
-                    CUDA_R_16BF, 2 * d.inter, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "gate/up GEMM");
-  mark(2);
-  const int n = rows * d.inter;
-  moe::silu_mul_kernel<<<(n + 255) / 256, 256, 0, s>>>(h->gu, d.inter, n, h->a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_err(e, "SiLU * mul launch");
-  mark(3);
-  // f [rows][H] = a [rows][I] . W2^T  (column-major: W2 is I x H)
-  st = cublasGemmEx(h->blas, CUBLAS_OP_T, CUBLAS_OP_N, d.hidden, rows, d.inter, &one, h->w.w2,
-                    CUDA_R_16BF, d.inter, h->a, CUDA_R_16BF, d.inter, &zero, h->f, CUDA_R_16BF,
-                    d.hidden, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) return blas_fail(st, "down GEMM");
   mark(4);
-  bp.branch = h->f;
+  bp.branch = nullptr;
+  bp.part = h->part;
+  bp.part_S = part_S;
+  bp.part_out = h->f;
   bp.w_post = h->w.w_post_ffn;
   bp.w_pre = h->w.w_post_ffn;  // read but unused: no normalised output
   bp.x_out = nullptr;
   bp.round_norm = 0;
   bp.stream_in = nullptr;
   bp.aux = aux;
-  e = moe::launch_boundary(bp, h->cluster, s, false);
+  e = moe::launch_boundary(bp, h->cluster, s, !ev);
   if (e != cudaSuccess) return cuda_err(e, "post-ffn boundary launch");
   mark(5);
   return MOE_OK;
@@ -271,31 +240,41 @@ int moe_dense_create(const moe_dense_dims* dims, const moe_dense_weights* w, moe
       return cuda_err(e, "streaming projection shared memory");
     }
   }
+  e = moe::gemm_set_smem();
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_err(e, "tensor-core projection shared memory");
+  }
   const size_t R = (size_t)d.max_rows, H = (size_t)d.hidden, I = (size_t)d.inter;
-  const size_t part_bytes = h->down_splits ? (size_t)h->down_splits * 8 * H * sizeof(float) : 0;
-  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H) + part_bytes + R * H * (4 + 2);
+  // the down projection's partials: the streamed path's [S][8][H] or the
+  // tensor-core path's [S][R][H], whichever is larger
+  const size_t part_stream = h->down_splits ? (size_t)h->down_splits * 8 * H : 0;
+  const size_t part_tc = (size_t)kDenseMaxSplits * R * H;
+  const size_t part_bytes = (part_stream > part_tc ? part_stream : part_tc) * sizeof(float);
+  const size_t bytes = 2 * (R * H + R * 2 * I + R * I + R * H) + part_bytes + R * H * (4 + 2) + 16;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->blas_ws, kBlasWorkspace);
   if (e != cudaSuccess) {
     moe_dense_destroy(h);
-    cudaFree(base);
     return moe::api_fail(MOE_ENOMEM, "dense layer workspace");
   }
-  h->blas_ws_bytes = kBlasWorkspace;
   h->x = reinterpret_cast<__nv_bfloat16*>(base);
   h->gu = h->x + R * H;
   h->a = h->gu + R * 2 * I;
   h->f = h->a + R * I;
-  h->part = h->down_splits ? reinterpret_cast<float*>(h->f + R * H) : nullptr;
+  h->part = reinterpret_cast<float*>(h->f + R * H);
   h->io_stream = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(h->f + R * H) + part_bytes);
   h->io_attn = reinterpret_cast<__nv_bfloat16*>(h->io_stream + R * H);
-  cublasStatus_t st = cublasCreate(&h->blas);
-  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetWorkspace(h->blas, h->blas_ws, h->blas_ws_bytes);
-  if (st == CUBLAS_STATUS_SUCCESS) st = cublasSetMathMode(h->blas, CUBLAS_DEFAULT_MATH);
-  if (st != CUBLAS_STATUS_SUCCESS) {
+  h->err = reinterpret_cast<unsigned*>(h->io_attn + R * H);
+  e = cudaMemset(h->err, 0, 2 * sizeof(unsigned));
+  // the tensor-core projections' tensor maps: W13 [2I][H] over x [R][H], W2
+  // [H][I] over a [R][I]
+  if (e == cudaSuccess)
+    e = moe::encode_gemm_maps(h->gu_maps, h->w.w13, 2 * (int64_t)I, h->x, (int64_t)R, (int)H);
+  if (e == cudaSuccess) e = moe::encode_gemm_maps(h->dn_maps, h->w.w2, (int64_t)H, h->a, (int64_t)R, (int)I);
+  if (e != cudaSuccess) {
     moe_dense_destroy(h);
-    return blas_fail(st, "cuBLAS set-up");
+    return cuda_err(e, "dense layer set-up");
   }
   *out = h;
   return MOE_OK;
@@ -429,11 +408,24 @@ int moe_dense_debug(moe_dense_t* h, moe_dense_debug_view* v) {
   return MOE_OK;
 }
 
+int moe_dense_last_error(moe_dense_t* h) {
+  if (!h) return moe::api_fail(MOE_EINVAL, "null handle");
+  cudaError_t e = cudaDeviceSynchronize();
+  unsigned flag = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, h->err, sizeof(flag), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(e, "dense layer error word");
+  if (flag) {
+    cudaMemset(h->err, 0, sizeof(unsigned));
+    char buf[96];
+    snprintf(buf, sizeof(buf), "device-side error %u (1 = a bounded wait gave up)", flag);
+    return moe::api_fail(MOE_EDEVICE, buf);
+  }
+  return MOE_OK;
+}
+
 void moe_dense_destroy(moe_dense_t* h) {
   if (!h) return;
   for (const auto& g : h->host_graphs) cudaGraphExecDestroy(g.exec);
-  if (h->blas) cublasDestroy(h->blas);
-  cudaFree(h->blas_ws);
   cudaFree(h->x);
   delete h;
 }

@@ -89,8 +89,8 @@ def _check(case, rows, variant=0):
     # differ in its last bit; where that bit moves bf16(s1) across a midpoint
     # one element of x moves by one step
     _bits_match(got["x"], ref["x"], ref["x_exact"], "x", slack=got["x"].size // 10000)
-    # the projections: the library GEMM's fp32 summation (order and tensor-core
-    # accumulation unspecified) strays past the 1e-5 midpoint band now and then
+    # the projections: the tensor-core kernel's fp32 summation (the MMA's
+    # internal accumulation order is unspecified) strays past the 1e-5 midpoint band now and then
     # at K in the thousands; those results are one bf16 step away, and rare
     gu, gu_ex = oracle.bf16_linear(got["x"], case.w13_h)
     _bits_match(got["gu"], gu, gu_ex, "gate/up", slack=GEMM_SLACK * gu.size)
@@ -117,7 +117,7 @@ def _check(case, rows, variant=0):
 
 # (256, 384) and (256, 4096) take the streamed projections (the latter's down
 # projection in 16 K-splits, summed by the boundary in two groups of eight);
-# the others the library GEMMs
+# the others the tensor-core projection kernel
 @pytest.mark.parametrize("hidden,inter,rows", [(256, 384, 8), (256, 384, 1), (256, 4096, 8),
                                                (256, 4096, 5), (1152, 520, 3),
                                                (1152, 520, 33), (384, 136, 128),
@@ -143,7 +143,8 @@ def test_dense_layer_full_width():
 @pytest.mark.parametrize("hidden,inter", [(1152, 520), (256, 384)])
 def test_dense_layer_graph_replays_bitwise(hidden, inter):
     """A captured layer replays to the eager result bit for bit (the library
-    GEMM path, and the streamed path with its programmatic dependent launches)."""
+    tensor-core path and the streamed path, both with programmatic dependent
+    launches)."""
     case = _Case(_shape(SMALL, hidden, inter), max_rows=8)
     try:
         stream, attn = synth.step_inputs(case.w.with_rows(8), 2)
@@ -153,7 +154,7 @@ def test_dense_layer_graph_replays_bitwise(hidden, inter):
         s_graph = torch.from_numpy(stream).cuda()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):          # a first call outside capture sets cuBLAS up
+        with torch.cuda.stream(side):          # a first call outside capture
             case.layer.layer(8, a_t, s_graph.clone())
         torch.cuda.current_stream().wait_stream(side)
         g = torch.cuda.CUDAGraph()
@@ -176,7 +177,7 @@ def test_dense_layer_profile_and_row_limits():
         s_t, a_t = torch.from_numpy(stream).cuda(), _bf16_dev(attn)
         ms = case.layer.layer_profile(8, a_t, s_t)
         assert len(ms) == 5 and all(t > 0.0 for t in ms)
-        # up to 8 rows (H and I multiples of 128) four kernels, all the library's own
+        # four kernels, all the library's own, streamed (up to 8 rows) or not
         assert case.layer.kernel_count(8) == 4
         for rows in (0, 9):
             with pytest.raises(moe.MoeError):
