@@ -52,9 +52,10 @@ def _peaks():
 # one full ncu capture of that kernel at serving widths with 64 experts
 # (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by its
 # active experts); valid only for the kernel source it was taken on.
-EXPERTS_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/experts_tc.cu",
-                   "sha256_prefix": "89efa5d83b31eaac", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": (1065518848 + 3387648) / 43}
+EXPERTS_TRAFFIC = {"source": ["speculative_decode_routed_gb300/csrc/experts_tc.cu",
+                              "speculative_decode_routed_gb300/csrc/tc_ptx.cuh"],
+                   "sha256_prefix": "3c743dae3816b010", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": (1065534208 + 3768576) / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
@@ -67,13 +68,18 @@ DENSE_GATE_UP_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/gemv.cu
 
 
 def _source_unchanged(t) -> bool:
-    """True if t["source"] still hashes to the source the capture was taken on."""
+    """True if the kernel's sources (t["source"], one path or several, hashed
+    in order as one stream) still hash to those the capture was taken on."""
     import hashlib
+    paths = t["source"] if isinstance(t["source"], (list, tuple)) else [t["source"]]
+    h = hashlib.sha256()
     try:
-        with open(os.path.join(ROOT, t["source"]), "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest().startswith(t["sha256_prefix"])
+        for path in paths:
+            with open(os.path.join(ROOT, path), "rb") as f:
+                h.update(f.read())
     except OSError:
         return False
+    return h.hexdigest().startswith(t["sha256_prefix"])
 
 
 def _experts_traffic(w: synth.Workload, n_active: float):

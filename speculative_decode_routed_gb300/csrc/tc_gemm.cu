@@ -10,7 +10,10 @@
 // Swap-AB, as in the routed experts: the weight rows fill the MMA's M = 128
 // (operand A, streamed from HBM through a TMA ring, 128-byte swizzle) and the
 // activation rows fill N (operand B, 16..128 rows per tile); K advances in
-// blocks of 64 elements (128 bytes), four K = 16 MMAs each.  A task is one
+// boxes of 64 elements (128 bytes), four K = 16 MMAs each, and a pipeline
+// stage holds KX consecutive boxes, so every weight row is requested in runs
+// of KX * 128 contiguous bytes (with one box per stage the next 128 bytes of a
+// row came a stage later, and DRAM ran half idle).  A task is one
 // 128-row weight tile (of one layer; gated: 128 gate rows and the matching
 // 128 up rows, two accumulators), one activation tile and one K-split; one
 // persistent CTA per SM takes tasks b, b + grid, ... and keeps its ring
@@ -84,7 +87,7 @@ __device__ __forceinline__ GmSmem gm_carve(uint8_t* base) {
 
 // Task t -> (layer, weight tile, split, activation tile).
 struct GmTask {
-  int l, m, s, nt, kb0, kb1;
+  int l, m, s, nt, st0, st1;  // stages [st0, st1) along K
 };
 
 __device__ __forceinline__ GmTask gm_task(const GemmParams& p, int t) {
@@ -93,8 +96,8 @@ __device__ __forceinline__ GmTask gm_task(const GemmParams& p, int t) {
   k.s = (t / p.n_tiles) % p.S;
   k.m = (t / (p.n_tiles * p.S)) % p.m_tiles;
   k.l = t / (p.n_tiles * p.S * p.m_tiles);
-  k.kb0 = k.s * p.KBS;
-  k.kb1 = min(p.KB, k.kb0 + p.KBS);
+  k.st0 = k.s * p.KBS;
+  k.st1 = min(p.KST, k.st0 + p.KBS);
   return k;
 }
 
@@ -135,34 +138,38 @@ __global__ void __launch_bounds__(kGmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_base;
-  const uint32_t bytes = p.a_bytes + (uint32_t)p.NT * 128u;
+  const uint32_t bytes = p.a_bytes + (uint32_t)p.KX * p.b_box;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      auto issue_w = [&](uint8_t* st, uint64_t* full, const GmTask& k, int kb) {
+      auto issue_w = [&](uint8_t* st, uint64_t* full, const GmTask& k, int sk) {
         mbar_arrive_expect_tx(full, bytes);
-        if (gated) {
-          tma_2d(st, &mw, kb * 64, k.m * 128, full, pol);
-          tma_2d(st + 16384, &mw, kb * 64, p.I + k.m * 128, full, pol);
-        } else {
-          tma_2d(st, &mw, kb * 64, k.l * p.R + k.m * 128, full, pol);
+        for (int b = 0; b < p.KX; ++b) {
+          const int x = (sk * p.KX + b) * 64;
+          uint8_t* dst = st + (size_t)b * p.a_box;
+          if (gated) {
+            tma_2d(dst, &mw, x, k.m * 128, full, pol);
+            tma_2d(dst + 16384, &mw, x, p.I + k.m * 128, full, pol);
+          } else {
+            tma_2d(dst, &mw, x, k.l * p.R + k.m * 128, full, pol);
+          }
         }
       };
       // the first stages' weights, before the dependency wait
       int pre = 0;
       for (int t = blockIdx.x; t < tasks && pre < p.NS; t += gridDim.x) {
         const GmTask k = gm_task(p, t);
-        for (int kb = k.kb0; kb < k.kb1 && pre < p.NS; ++kb, ++pre)
-          issue_w(sm.stages + (size_t)pre * p.stage_stride, &sm.full[pre], k, kb);
+        for (int sk = k.st0; sk < k.st1 && pre < p.NS; ++sk, ++pre)
+          issue_w(sm.stages + (size_t)pre * p.stage_stride, &sm.full[pre], k, sk);
       }
       grid_dep_wait();
       int g = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tasks && ok; t += gridDim.x) {
         const GmTask k = gm_task(p, t);
-        for (int kb = k.kb0; kb < k.kb1; ++kb, ++g) {
+        for (int sk = k.st0; sk < k.st1; ++sk, ++g) {
           const int s = g % p.NS;
           uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
           if (g >= pre) {
@@ -171,9 +178,11 @@ __global__ void __launch_bounds__(kGmThreads, 1)
               ok = false;
               break;
             }
-            issue_w(st, &sm.full[s], k, kb);
+            issue_w(st, &sm.full[s], k, sk);
           }
-          tma_2d_plain(st + p.a_bytes, &mx, kb * 64, k.l * p.x_layer_rows + k.nt * p.NT, &sm.full[s]);
+          for (int b = 0; b < p.KX; ++b)
+            tma_2d_plain(st + p.a_bytes + (size_t)b * p.b_box, &mx, (sk * p.KX + b) * 64,
+                         k.l * p.x_layer_rows + k.nt * p.NT, &sm.full[s]);
         }
       }
       // every issued copy lands before the CTA exits: the last fill of each
@@ -200,7 +209,7 @@ __global__ void __launch_bounds__(kGmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)buf * kGmAccCols;
-        for (int kb = k.kb0; kb < k.kb1; ++kb, ++g) {
+        for (int sk = k.st0; sk < k.st1; ++sk, ++g) {
           const int s = g % p.NS;
           if (!mbar_wait(&sm.full[s], (uint32_t)(g / p.NS) & 1u, lim)) {
             latch_error(p.err, kDevWaitTimeout);
@@ -208,14 +217,17 @@ __global__ void __launch_bounds__(kGmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sm.stages + (size_t)s * p.stage_stride);
-          const uint32_t b0 = a0 + p.a_bytes;
+          const uint32_t st = smem_u32(sm.stages + (size_t)s * p.stage_stride);
+          for (int b = 0; b < p.KX; ++b) {
+            const uint32_t a0 = st + (uint32_t)b * p.a_box;
+            const uint32_t b0 = st + p.a_bytes + (uint32_t)b * p.b_box;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint64_t bd = smem_desc(b0 + 32u * q, 16, 1024, 2);
-            const bool acc = !(kb == k.kb0 && q == 0);
-            gm_mma(d0, smem_desc(a0 + 32u * q, 16, 1024, 2), bd, idesc, acc);
-            if (gated) gm_mma(d0 + 128u, smem_desc(a0 + 16384u + 32u * q, 16, 1024, 2), bd, idesc, acc);
+            for (int q = 0; q < 4; ++q) {
+              const uint64_t bd = smem_desc(b0 + 32u * q, 16, 1024, 2);
+              const bool acc = !(sk == k.st0 && b == 0 && q == 0);
+              gm_mma(d0, smem_desc(a0 + 32u * q, 16, 1024, 2), bd, idesc, acc);
+              if (gated) gm_mma(d0 + 128u, smem_desc(a0 + 16384u + 32u * q, 16, 1024, 2), bd, idesc, acc);
+            }
           }
           tc_commit(&sm.empty[s]);
         }
@@ -313,7 +325,7 @@ cudaError_t encode_bf16_rows(CUtensorMap* m, const void* base, int64_t rows, int
 }  // namespace
 
 bool plan_gemm(GemmParams& p, int mode, int L, int R, int K, int n, int I, int x_layer_rows,
-               int num_sms, int max_splits) {
+               int num_sms, int max_splits, int kx) {
   if (K < 8 || K % 8 || n < 1 || L < 1 || R < 1) return false;
   p = GemmParams{};
   p.mode = mode;
@@ -327,16 +339,32 @@ bool plan_gemm(GemmParams& p, int mode, int L, int R, int K, int n, int I, int x
   p.n_tiles = (n + p.NT - 1) / p.NT;
   p.KB = (K + 63) / 64;
   p.m_tiles = mode == kGemmGated ? (I + 127) / 128 : (R + 127) / 128;
-  // K-splits (partials only): the busiest SM's K-blocks, ceil(tasks / SMs) *
-  // K-blocks per split, as small as it gets; among counts within 3 % of the
+  p.a_box = mode == kGemmGated ? 32768u : 16384u;
+  p.b_box = (uint32_t)p.NT * 128u;
+  const uint32_t budget = 227u * 1024u - 1024u - (uint32_t)kGmCtrl;
+  auto stride_of = [&](int x) { return ((uint32_t)x * (p.a_box + p.b_box) + 1023u) / 1024u * 1024u; };
+  if (kx <= 0) {
+    // the widest stage (up to 8 boxes, 1 KB of each weight row) that leaves
+    // two in the ring and does not read far past K: measured on 33- to
+    // 128-row projections at K 7168 and 28672, longer runs per row beat a
+    // deeper ring (K 28672, 33 rows: 1, 2, 4 boxes at 0.58, 0.72, 0.77 of the
+    // copy bandwidth with 8, 5, 2 stages)
+    kx = 8;
+    while (kx > 1 && kx / 2 >= p.KB) kx /= 2;
+    while (kx > 1 && budget / stride_of(kx) < 2) kx /= 2;
+  }
+  p.KX = kx;
+  p.KST = (p.KB + kx - 1) / kx;
+  // K-splits (partials only): the busiest SM's stages, ceil(tasks / SMs) *
+  // stages per split, as small as it gets; among counts within 3 % of the
   // best, the fewest (the caller sums the partials)
   int S = 1;
   if (mode == kGemmPartial) {
     const long long base = (long long)L * p.m_tiles * p.n_tiles;
     long long best = -1;
     for (int pass = 0; pass < 2; ++pass)
-      for (int s = 1; s <= max_splits && s <= p.KB; ++s) {
-        const int kbs = (p.KB + s - 1) / s;
+      for (int s = 1; s <= max_splits && s <= p.KST; ++s) {
+        const int kbs = (p.KST + s - 1) / s;
         const long long cost = ((base * s + num_sms - 1) / num_sms) * kbs;
         if (pass == 0 && (best < 0 || cost < best)) best = cost;
         if (pass == 1 && cost * 100 <= best * 103) {
@@ -346,11 +374,11 @@ bool plan_gemm(GemmParams& p, int mode, int L, int R, int K, int n, int I, int x
         }
       }
   }
-  p.KBS = (p.KB + S - 1) / S;
-  p.S = (p.KB + p.KBS - 1) / p.KBS;  // every split has at least one K-block
-  p.a_bytes = mode == kGemmGated ? 32768u : 16384u;
-  p.stage_stride = (p.a_bytes + (uint32_t)p.NT * 128u + 1023u) / 1024u * 1024u;
-  int ns = (int)((227 * 1024 - 1024 - kGmCtrl) / p.stage_stride);
+  p.KBS = (p.KST + S - 1) / S;
+  p.S = (p.KST + p.KBS - 1) / p.KBS;  // every split has at least one stage
+  p.a_bytes = (uint32_t)kx * p.a_box;
+  p.stage_stride = stride_of(kx);
+  const int ns = (int)(budget / p.stage_stride);
   p.NS = ns > kGmMaxStages ? kGmMaxStages : ns;
   p.wait_ns = kDefaultWaitNs;
   return p.NS >= 2;

@@ -22,14 +22,18 @@ struct GemmParams {
   int L, R, K, n;    // layers, weight rows per layer, reduction length, activation rows
   int I;             // gated: gate rows 0..I-1, up rows I..2I-1 of W
   int S;             // K-splits (partials), else 1
-  int KB;            // K-blocks of 64 elements: ceil(K / 64)
-  int KBS;           // K-blocks per split (every split has at least one)
+  int KB;            // K-boxes of 64 elements: ceil(K / 64)
+  int KX;            // K-boxes per pipeline stage (consecutive in K; boxes past K read zeros)
+  int KST;           // stages along K: ceil(KB / KX)
+  int KBS;           // stages per split (every split has at least one)
   int NT;            // activation rows per MMA tile: a multiple of 16, at most 128
   int n_tiles;       // ceil(n / NT)
   int m_tiles;       // 128-row weight tiles per layer: ceil(R / 128), gated ceil(I / 128)
   int x_layer_rows;  // rows between layers in X's map (X[l][i] is row l * x_layer_rows + i)
   int NS;            // pipeline stages
-  uint32_t a_bytes;  // weight bytes per stage (16 KB, gated 32 KB)
+  uint32_t a_box;    // weight bytes per K-box (16 KB; gated 32 KB: gate tile, then up tile)
+  uint32_t a_bytes;  // weight bytes per stage: KX * a_box
+  uint32_t b_box;    // activation bytes per K-box: NT * 128
   uint32_t stage_stride;
   float* part;           // kGemmPartial
   __nv_bfloat16* out;    // kGemmBf16
@@ -47,10 +51,11 @@ struct GemmMaps {
 };
 
 // Plans mode, shapes and splits for num_sms SMs (the K-splits of a partial
-// projection chosen so the busiest SM streams the fewest K-blocks).
-// Returns false if the shape is not served (K not a multiple of 8).
+// projection chosen so the busiest SM streams the fewest stages).  kx > 0
+// fixes the K-boxes per stage, else the plan picks them.  Returns false if
+// the shape is not served (K not a multiple of 8).
 bool plan_gemm(GemmParams& p, int mode, int L, int R, int K, int n, int I, int x_layer_rows,
-               int num_sms, int max_splits);
+               int num_sms, int max_splits, int kx = 0);
 // Encodes the weight map over W [L * R][K] and the activation maps over X
 // [x_rows][K] (bf16, row-major, 16-byte aligned, K a multiple of 8).
 cudaError_t encode_gemm_maps(GemmMaps& m, const void* W, int64_t w_rows, const void* X,
