@@ -80,6 +80,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
   }
   grid_dep_wait();
   grid_dep_launch();
+  if (p.sig_reset && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.sig_reset = 0u;
 
   float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
   if (live) {

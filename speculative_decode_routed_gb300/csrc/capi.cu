@@ -424,7 +424,7 @@ size_t layout_workspace(moe::Workspace& ws, uint8_t* base, const moe_decode_dims
   ws.ready_info = cv.take<unsigned>(V, "ready_info");
   ws.n_virtual = cv.take<int>(1, "n_virtual");
   ws.rg_count = cv.take<unsigned>(16, "rg_count");
-  ws.counters = cv.take<unsigned>(4, "counters");
+  ws.counters = cv.take<unsigned>(8, "counters");
   ws.err = cv.take<unsigned>(2, "err");
   // the guards' offsets, for the fill and check kernels (no guard after them)
   const size_t n_guards = guards ? guards->size() : 64;
@@ -465,6 +465,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   bp.w_pre = w.w_pre;
   bp.x_out = h->ws.x;
   bp.x_amax = h->ws.x_amax;
+  bp.sig_reset = h->ws.counters + 4;  // the previous experts kernel has read it
   cudaError_t e = moe::launch_boundary(bp, h->cluster, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "boundary launch");
   mark(1);
@@ -521,6 +522,7 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   tg.withhold_ready = withhold_ready ? 1 : 0;
   tg.local_route = td.local_route = local_route ? 1 : 0;
   tg.rows = td.rows = rows;
+  tg.n_leaders = td.n_leaders = h->n_eg;
   tg.S = td.S = 1;  // the router summed its slices (cluster_sum)
   tg.rbias = td.rbias = nullptr;  // the router's cluster sum added it
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,

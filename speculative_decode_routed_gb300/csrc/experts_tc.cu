@@ -286,7 +286,6 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
       ws.offset[E] = n_valid;
       ws.n_active[0] = n_items;
       ws.n_virtual[0] = n_items;
-      ws.x_amax[0] = 0u;
     }
   }
   // the scratch was written through the generic proxy; the stage ring is
@@ -296,9 +295,11 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   return n_items;
 }
 
-// Down item it: tile it % tiles of the (it / tiles)-th virtual expert whose h
-// became ready.  Waits (bounded) until that expert is published; the acquire and the
-// proxy fence make its h codes and scale lines visible to the TMA.
+// Down item it: tile it % tiles of virtual expert it / tiles -- under
+// in-kernel routing the active expert of that index, else the one whose h
+// became ready in that place.  Waits (bounded) until that expert is
+// published; the acquire and the proxy fence make its h codes and scale
+// lines visible to the TMA.
 __device__ __forceinline__ bool tc_resolve_down(const TcParams& p, int it, int4& et) {
   const unsigned* slot = p.ws.ready_info + it / p.tiles;
   unsigned w = ld_acquire_u32(slot);
@@ -382,7 +383,7 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
 // completes the expert -- every tile of every part -- quantizes all of the
 // expert's h rows and publishes its parts to the down projection.
 __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int tiles,
-                                 float amax_part, int t, int pos0_local, int ne_local) {
+                                 float amax_part, int t, int pos0_local, int ne_local, int a_local) {
   const Workspace& ws = p.ws;
   // under local routing an expert is one work item: its pooled rows are the item's
   const int pos0 = p.local_route ? pos0_local : __ldcg(ws.offset + e);
@@ -407,12 +408,19 @@ __device__ void tc_finish_expert(const TcParams& p, const TcSmem& sm, int e, int
     if (t == 0) {
       ws.done[e] = 0u;
       ws.h_amax[e] = 0u;
-      const unsigned slot = atomicAdd(ws.counters + 3, (unsigned)parts);
-      const unsigned cap = (unsigned)virtual_slots(p.E, p.ws_pairs);
-      for (int g = 0; g < parts && !p.withhold_ready; ++g)
-        if (slot + g < cap)
-          st_release_u32(ws.ready_info + slot + g,
-                         pack_expert(e, pos0 + kVirtualPairs * g, min(kVirtualPairs, ne - kVirtualPairs * g)));
+      if (p.local_route) {
+        // one part per expert (at most 8 pairs), published at its active
+        // index: the down items are numbered in active order
+        if (!p.withhold_ready && MOE_IN_BOUNDS(a_local >= 0 && a_local < p.E && parts == 1, ws.err))
+          st_release_u32(ws.ready_info + a_local, pack_expert(e, pos0, ne));
+      } else {
+        const unsigned slot = atomicAdd(ws.counters + 3, (unsigned)parts);
+        const unsigned cap = (unsigned)virtual_slots(p.E, p.ws_pairs);
+        for (int g = 0; g < parts && !p.withhold_ready; ++g)
+          if (slot + g < cap)
+            st_release_u32(ws.ready_info + slot + g,
+                           pack_expert(e, pos0 + kVirtualPairs * g, min(kVirtualPairs, ne - kVirtualPairs * g)));
+      }
     }
   }
   tc_named_sync();
@@ -428,7 +436,8 @@ template <bool kGU>
 __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* tm_a,
                                          const CUtensorMap* tm_b, const CUtensorMap* tm_sfb,
                                          const TcSmem& sm, uint32_t tmem, int n_items, int epi0,
-                                         int first_claim = -1) {
+                                         int first_claim = -1, const TcParams* pdn = nullptr,
+                                         int* dn_claim = nullptr) {
   const Workspace& ws = p.ws;
   const uint64_t lim = ws.wait_ns;  // every wait's limit
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -445,43 +454,29 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       uint32_t fbits = 0;  // per (stage, group) full barrier: parity of fills issued
       bool ok = true;
       // the first claim may have been made already (its latency hidden under the routing)
-      int it = first_claim >= 0 ? first_claim : (int)atomicAdd(claim, 1u);
-      for (int j = 0;; ++j) {
-        int4 et = make_int4(-1, 0, 0, 0);
-        bool live = ok && it < n_items;
-        if (live) {
-          if (kGU) {
-            et = tc_resolve_gate_up(p, sm, it);
-          } else if (!tc_resolve_down(p, it, et)) {
-            latch_error(ws.err, kDevWaitTimeout);
-            live = ok = false;
-          }
-          if (live && !tc_item_ok(p, et)) {
-            latch_error(ws.err, kDevBadRouting);
-            live = ok = false;
-          }
-        }
-        if (!ring_put(sm, j, live ? make_int4(it, et.x, et.y, et.z) : make_int4(-1, 0, 0, 0), lim)) {
-          latch_error(ws.err, kDevWaitTimeout);
-          break;
-        }
-        if (!live) break;
-        const int nxt = (int)atomicAdd(claim, 1u);  // its latency hides under this item
-        const int e = et.x, tile = it % p.tiles, pos0 = et.y, ne = et.z;
-        const int nt = (ne + 31) / 32;
-        const int brow = (kGU && p.direct) ? 0 : pos0;  // first B row
-        for (int ks = 0; ks < KS; ++ks, ++g) {
-          const int kb = ks * KPS;  // first K-block of this stage
-          const int nkb = min(KPS, KB - kb);
-          const int s = g % p.NS;
-          if (g >= p.NS && !mbar_wait(&sm.empty[s], ((g / p.NS) - 1) & 1, lim)) {
-            latch_error(ws.err, kDevWaitTimeout);
-            ok = false;
-            break;
-          }
-          uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
-          const int fb = s * p.Q + ks % p.Q;
-          uint64_t* full = &sm.full[fb];
+      // gate/up items below the grid size are taken statically (item b by CTA b)
+      const int cbase = kGU ? (int)gridDim.x : 0;
+      int it = first_claim >= 0 ? first_claim : (int)atomicAdd(claim, 1u) + cbase;
+      // Down items under in-kernel routing are numbered in active order, so
+      // the expert is known at the claim: the stages' weights (and their
+      // scale atoms) go out before the expert's h is published, and only the
+      // h tiles wait for it.  Elsewhere down items are numbered in the order
+      // the experts' h became ready.
+      const bool early = !kGU && p.local_route;
+      int e = 0, tile = 0, nt = 0, brow = 0;
+      // Stage ks of the current item as the g-th stage through the ring:
+      // wts arms its full barrier for every byte and issues the weight tiles
+      // and scale atoms (waiting, bounded, for the slot); acts issues the
+      // activation (gate/up) or h (down) tiles and scale lines.
+      auto stage = [&](int ks, int gg, bool wts, bool acts) -> bool {
+        const int kb = ks * KPS;  // first K-block of this stage
+        const int nkb = min(KPS, KB - kb);
+        const int s = gg % p.NS;
+        uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
+        const int fb = s * p.Q + ks % p.Q;
+        uint64_t* full = &sm.full[fb];
+        if (wts) {
+          if (gg >= p.NS && !mbar_wait(&sm.empty[s], ((gg / p.NS) - 1) & 1, lim)) return false;
           fbits ^= 1u << fb;
           // weight tiles (a missing second K-block of a stage is zero filled
           // and counts in full), the present K-blocks' scale atoms, and per
@@ -510,6 +505,8 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
                            p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
                            full);
           }
+        }
+        if (acts) {
           for (int t = 0; t < nt; ++t) {
             if (KPS == 1)
               tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, brow + 32 * t, full);
@@ -518,6 +515,80 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
             tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, brow + 32 * t, kb * 4, full);
           }
         }
+        return true;
+      };
+      for (int j = 0;; ++j) {
+        int4 et = make_int4(-1, 0, 0, 0);
+        bool live = ok && it < n_items;
+        int npre = 0;  // stages whose weights went out before the item was ready
+        if (live) {
+          if (kGU || early) {
+            et = kGU ? tc_resolve_gate_up(p, sm, it) : unpack_expert(sm.act[it / p.tiles]);
+          } else if (!tc_resolve_down(p, it, et)) {
+            latch_error(ws.err, kDevWaitTimeout);
+            live = ok = false;
+          }
+          if (live && !tc_item_ok(p, et)) {
+            latch_error(ws.err, kDevBadRouting);
+            live = ok = false;
+          }
+        }
+        if (live) {
+          e = et.x;
+          tile = it % p.tiles;
+          nt = (et.z + 31) / 32;
+          brow = (kGU && p.direct) ? 0 : et.y;  // first B row
+        }
+        if (live && early) {
+          // A ready expert takes the usual path (its stages' weights and h
+          // tiles together).  Until it is ready, the weights of its stages go
+          // out as ring slots come free -- only slots that earlier items
+          // release: a slot this item itself holds would wait on its own h.
+          const unsigned* slot = ws.ready_info + it / p.tiles;
+          const int cap = min(KS, p.NS);
+          unsigned w = ld_acquire_u32(slot);
+          const uint64_t t0 = global_ns();
+          for (uint32_t i = 1; !w; ++i) {
+            for (int gg = g + npre;
+                 npre < cap && (gg < p.NS || mbar_test(&sm.empty[gg % p.NS], ((gg / p.NS) - 1) & 1));
+                 ++gg) {
+              stage(npre, gg, true, false);  // its slot is free: no wait
+              ++npre;
+            }
+            w = ld_acquire_u32(slot);
+            if (!w && (i & 63u) == 0u && global_ns() - t0 > lim) break;
+          }
+          g += npre;
+          if (!w) {
+            latch_error(ws.err, kDevWaitTimeout);
+            live = ok = false;
+          } else {
+            fence_proxy_async_global();
+            const int4 wt = unpack_expert(w);
+            if (!MOE_IN_BOUNDS(wt.x == et.x && wt.y == et.y && wt.z == et.z, ws.err)) live = ok = false;
+          }
+        }
+        // the item is handed to the issuers and the epilogue only once it is
+        // ready (the epilogue reads the expert's h scale)
+        if (!ring_put(sm, j, live ? make_int4(it, et.x, et.y, et.z) : make_int4(-1, 0, 0, 0), lim)) {
+          latch_error(ws.err, kDevWaitTimeout);
+          break;
+        }
+        if (!live) {
+          // gate/up claims ran out (in-kernel routing): claim this CTA's first
+          // down item now -- every gate/up item is claimed -- so the claim's
+          // latency hides under the CTA's last gate/up stages and epilogue
+          if (kGU && ok && pdn && pdn->local_route && dn_claim) *dn_claim = (int)atomicAdd(ws.counters + 2, 1u);
+          break;
+        }
+        const int nxt = (int)atomicAdd(claim, 1u) + cbase;  // its latency hides under this item
+        for (int ks = 0; ks < npre; ++ks) stage(ks, g - npre + ks, false, true);
+        for (int ks = npre; ks < KS; ++ks, ++g)
+          if (!stage(ks, g, true, true)) {
+            latch_error(ws.err, kDevWaitTimeout);
+            ok = false;
+            break;
+          }
         it = nxt;
       }
       // every issued copy lands before the pipeline is torn down: the last
@@ -625,7 +696,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
     // h and o are read back soon (the h quantization and the next boundary's
     // gather): keep them in L2 while the weights stream through it
     const uint64_t keep = l2_evict_last_policy();
-    int cur_e = -1, cur_pos0 = -1, cur_ne = 0, cur_tiles = 0;
+    int cur_e = -1, cur_pos0 = -1, cur_ne = 0, cur_tiles = 0, cur_a = -1;
     float cur_amax = 0.0f, sc0 = 0.0f, sc1 = 0.0f;
     for (int j = 0;; ++j) {
       // the next item (one thread waits, bounded; the barrier hands the slot
@@ -646,7 +717,8 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       // gate/up accumulates per expert (over its virtual parts); down and
       // direct gate/up keep the pair ids of the current virtual part
       const bool new_e = (e != cur_e), new_part = new_e || pos0 != cur_pos0;
-      if (new_e && kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne);
+      if (new_e && kGU && cur_e >= 0)
+        tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne, cur_a);
       if (new_part && (!kGU || p.direct)) {
         tc_named_sync();  // nobody still reads the previous part's pair ids
         for (int jj = t; jj < ne; jj += kEpiThreads) {
@@ -659,6 +731,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       cur_ne = ne;
       if (new_e) {
         cur_e = e;
+        cur_a = v.x / p.tiles;
         cur_tiles = 0;
         cur_amax = 0.0f;
         if (kGU) {
@@ -753,7 +826,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
       ++cur_tiles;
     }
-    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne);
+    if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne, cur_a);
   }
 }
 
@@ -761,11 +834,16 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
 
 // ======================================================================
 // Routed experts of one layer in one persistent launch: every CTA claims
-// gate/up items until they run out, then down items.  An expert's down items
-// are handed out in the order experts' h became ready, so CTAs that finish
-// gate/up early stream down weights instead of idling.  A CTA only ever
-// waits for gate/up work that running CTAs have already claimed, and gate/up
-// work waits for nothing, so the launch needs no co-residency guarantee.
+// gate/up items until they run out, then down items.  Under in-kernel
+// routing (at most 8 rows) the down items follow the active order, which is
+// also the order the gate/up items were claimed in, and a CTA streams a down
+// item's weights before the expert's h is ready; beyond, an expert's down
+// items are handed out in the order experts' h became ready.  Either way
+// CTAs that finish gate/up early stream down weights instead of idling.  A
+// CTA only ever waits for gate/up work that running CTAs have already
+// claimed (no CTA claims a down item before every gate/up item is claimed),
+// and gate/up work waits for nothing, so the launch needs no co-residency
+// guarantee.
 __global__ void __launch_bounds__(kTcMaxThreads, 1)
     tc_moe_kernel(const __grid_constant__ TcParams pg, const __grid_constant__ CUtensorMap g_a,
                   const __grid_constant__ CUtensorMap g_b, const __grid_constant__ CUtensorMap g_sfb,
@@ -799,13 +877,40 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
                  "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // the routing, the pooled MoE input and the item counters come from the
-  // kernels before
-  grid_dep_wait();
-  grid_dep_launch();
-  // the producer's first gate/up claim, in flight while the CTA routes
-  const int first_claim = tid == 0 ? (int)atomicAdd(pg.ws.counters + 1, 1u) : -1;
-  const int na = pg.local_route ? tc_local_route(pg, sm) : __ldcg(pg.ws.n_virtual);
+  int na;
+  if (pg.local_route) {
+    // The router's expert groups count their finished logits: the CTA
+    // routes as soon as every group's are written, while the router's grid
+    // still quantizes the MoE input (bounded wait).  The quantized input,
+    // the item counters and the ready list come with the router's end.
+    if (tid == 0) {
+      const unsigned* cnt = pg.ws.counters + 4;
+      bool got = ld_acquire_u32(cnt) >= (unsigned)pg.n_leaders;
+      const uint64_t t0 = global_ns();
+      for (uint32_t i = 1; !got; ++i) {
+        got = ld_acquire_u32(cnt) >= (unsigned)pg.n_leaders;
+        if (!got && (i & 63u) == 0u && global_ns() - t0 > pg.ws.wait_ns) break;
+      }
+      if (!got) latch_error(pg.ws.err, kDevWaitTimeout);
+      *sm.flag = got ? 1 : 0;
+    }
+    __syncthreads();
+    const bool got = *reinterpret_cast<volatile int*>(sm.flag) != 0;
+    na = got ? tc_local_route(pg, sm) : -1;
+    grid_dep_wait();
+    grid_dep_launch();
+    // every router CTA has read max |x|: reset for the next layer's boundary
+    if (blockIdx.x == 0 && tid == 0) pg.ws.x_amax[0] = 0u;
+  } else {
+    // the routing, the pooled MoE input and the item counters come from the
+    // kernels before
+    grid_dep_wait();
+    grid_dep_launch();
+    na = __ldcg(pg.ws.n_virtual);
+  }
+  // the first gate/up item of CTA b is item b; later claims count from the
+  // grid size
+  const int first_claim = tid == 0 ? (int)blockIdx.x : -1;
   const bool na_ok = na >= 0 && na <= virtual_slots(pg.E, pg.ws_pairs);
   tc_fence_before();
   __syncthreads();
@@ -814,7 +919,8 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   if (!na_ok && tid == 0) latch_error(pg.ws.err, kDevBadRouting);
   const int n_act = na_ok ? na : 0;
 
-  tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0, first_claim);
+  int dn_claim = -1;  // the producer's first down claim, made when gate/up claims run out
+  tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0, first_claim, &pd, &dn_claim);
 
   // this CTA's gate/up copies have landed, its MMAs completed and its
   // accumulators been read: the shared memory takes the down layout
@@ -828,7 +934,7 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   }
   __syncthreads();
 
-  tc_phase<false>(pd, &d_a, &d_b, &d_sfb, sm, tmem, n_act * pd.tiles, epi0);
+  tc_phase<false>(pd, &d_a, &d_b, &d_sfb, sm, tmem, n_act * pd.tiles, epi0, dn_claim);
 
   tc_fence_before();
   __syncthreads();

@@ -447,6 +447,14 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
       if (p.bias) acc += bias_v;  // the same fp32 sum, then the bias, as the routing would add it
       if (wi < p.EG && ee < p.E) ws.logit_part[(size_t)r * p.E + ee] = acc;
     }
+    if (p.route_in_experts && sl == 0) {
+      // this expert group's logits are final: counted for the experts
+      // kernel, which routes as soon as every group's are (while the rest of
+      // this grid quantizes x)
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) atomicAdd(ws.counters + 4, 1u);
+    }
     // every peer keeps its partials until the sums are read
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
