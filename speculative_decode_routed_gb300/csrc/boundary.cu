@@ -80,7 +80,10 @@ __global__ void boundary_kernel(BoundaryParams p) {
   }
   grid_dep_wait();
   grid_dep_launch();
-  if (p.sig_reset && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.sig_reset = 0u;
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int i = threadIdx.x; i < p.n_reset0; i += blockDim.x) p.reset0[i] = 0u;
+    for (int i = threadIdx.x; i < p.n_reset1; i += blockDim.x) p.reset1[i] = 0u;
+  }
 
   float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
   if (live) {

@@ -465,7 +465,16 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   bp.w_pre = w.w_pre;
   bp.x_out = h->ws.x;
   bp.x_amax = h->ws.x_amax;
-  bp.sig_reset = h->ws.counters + 4;  // the previous experts kernel has read it
+  // Up to 8 rows the tensor-core experts kernel routes and pools itself from
+  // the router's logits.  Its item counters and ready list start at zero:
+  // the boundary clears them once the previous experts kernel has finished.
+  const bool local_route = MOE_EXPERT_TC && rows <= 8;
+  if (local_route) {
+    bp.reset0 = h->ws.counters;
+    bp.n_reset0 = 8;
+    bp.reset1 = h->ws.ready_info;
+    bp.n_reset1 = moe::virtual_slots(d.n_experts, d.max_rows * d.top_k);
+  }
   cudaError_t e = moe::launch_boundary(bp, h->cluster, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "boundary launch");
   mark(1);
@@ -482,10 +491,8 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   rp.wr = reinterpret_cast<const __nv_bfloat16*>(w.router_w);
   rp.bias = w.router_bias;
   rp.line_rows = d.max_rows * d.top_k;
-  // up to 8 rows the tensor-core experts kernel routes and pools itself
-  const bool local_route = MOE_EXPERT_TC && rows <= 8;
-  rp.route_in_experts = local_route ? 1 : 0;
   rp.cluster_sum = rows <= 8 ? 1 : 0;  // one block of rows: the slices are summed in the router
+  rp.route_in_experts = local_route ? 1 : 0;
   rp.ws = h->ws;
   e = moe::launch_router(rp, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
@@ -522,9 +529,6 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   tg.withhold_ready = withhold_ready ? 1 : 0;
   tg.local_route = td.local_route = local_route ? 1 : 0;
   tg.rows = td.rows = rows;
-  tg.n_leaders = td.n_leaders = h->n_eg;
-  tg.S = td.S = 1;  // the router summed its slices (cluster_sum)
-  tg.rbias = td.rbias = nullptr;  // the router's cluster sum added it
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
                          td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);

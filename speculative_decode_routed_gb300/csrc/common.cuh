@@ -237,6 +237,19 @@ __device__ __forceinline__ void atomic_max_nonneg(unsigned* addr, float v) {
   atomicMax(addr, __float_as_uint(v));
 }
 
+// fp32 dot product of eight bf16 pairs, accumulated in element order.
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
+  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -163,6 +163,70 @@ __device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, const TcSm
   return w ? unpack_expert(w) : make_int4(-1, 0, 0, 0);
 }
 
+// An item's K order: stage ks of item it reads K-stage (ks + rot) mod KSTEPS,
+// rot = it mod KSTEPS -- a function of the item, so every run sums its
+// products in the same order.
+__device__ __forceinline__ int tc_item_rot(const TcParams& p, int it) { return it % p.KSTEPS; }
+__device__ __forceinline__ int tc_stage_k(const TcParams& p, int ks, int rot) {
+  const int k = ks + rot;
+  return k >= p.KSTEPS ? k - p.KSTEPS : k;
+}
+
+// Stage ks of an item (expert e, output tile, nt activation tiles from row
+// brow) as the gg-th stage through the ring, its slot already free; the item
+// streams its K-blocks from stage rot on (tc_stage_k), so that CTAs which
+// start items together do not all read the same offsets.  wts
+// arms the stage's full barrier for every byte (toggling its bit in fbits)
+// and issues the weight tiles and scale atoms; acts issues the activation
+// (gate/up) or h (down) tiles and scale lines.
+__device__ __forceinline__ void tc_issue_stage(const TcParams& p, const TcSmem& sm, const CUtensorMap* tm_a,
+                                               const CUtensorMap* tm_b, const CUtensorMap* tm_sfb,
+                                               uint64_t pol, bool kGU, int e, int tile, int nt, int brow,
+                                               int ks, int gg, int rot, bool wts, bool acts, uint32_t& fbits) {
+  const int KB = p.KBLK, KPS = p.KPS;
+  const int kb = tc_stage_k(p, ks, rot) * KPS;  // first K-block of this stage
+  const int nkb = min(KPS, KB - kb);
+  const int s = gg % p.NS;
+  uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
+  const int fb = s * p.Q + ks % p.Q;
+  uint64_t* full = &sm.full[fb];
+  if (wts) {
+    fbits ^= 1u << fb;
+    // weight tiles (a missing second K-block of a stage is zero filled and
+    // counts in full), the present K-blocks' scale atoms, and per N-tile the
+    // activation tiles and scale lines
+    const uint32_t sfa_b = 2048u * (uint32_t)nkb;
+    const uint32_t bytes = p.a_bytes + sfa_b * (uint32_t)p.T + (uint32_t)(nt * KPS) * (4096u + 2048u);
+    mbar_arrive_expect_tx(full, bytes);
+    // gate rows (gate/up) or output rows (down) of this tile
+    if (p.tiled)  // tiles (e, tile, kb..kb+KPS-1) are contiguous
+      tma_3d_hint(st, tm_a, 0, 0, (e * p.row_tiles + tile) * KB + kb, full, pol);
+    else if (KPS == 1)
+      tma_2d(st, tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
+    else
+      tma_3d_hint(st, tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
+    bulk_g2s_plain(st + p.off_sfa, p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, sfa_b, full);
+    if (kGU) {  // gate/up stages hold one K-block
+      const int ru = p.I / 128 + tile;  // up rows follow the gate rows
+      if (p.tiled)
+        tma_3d_hint(st + 16384, tm_a, 0, 0, (e * p.row_tiles + ru) * KB + kb, full, pol);
+      else
+        tma_2d(st + 16384, tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
+      bulk_g2s_plain(st + p.off_sfa + 2048, p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
+                     full);
+    }
+  }
+  if (acts) {
+    for (int t = 0; t < nt; ++t) {
+      if (KPS == 1)
+        tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, brow + 32 * t, full);
+      else
+        tma_3d(st + p.off_b + t * 4096 * KPS, tm_b, 0, brow + 32 * t, kb, full);
+      tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, brow + 32 * t, kb * 4, full);
+    }
+  }
+}
+
 // In-kernel routing and pooler (at most 8 rows, so at most 128 pairs and at
 // most 8 pairs per expert: one work item per active expert).  Every CTA
 // routes the rows itself, one warp per row, from the router's logits, then
@@ -175,9 +239,9 @@ __device__ __forceinline__ int4 tc_resolve_gate_up(const TcParams& p, const TcSm
 // expert, as the pooler defines.  Every CTA computes the same result.  The
 // first CTA also writes the workspace copies -- ids, gates, flags, logits,
 // count, offset, pair order, active list, work items -- that the next
-// boundary's gather and the staged checks read, and resets max |x| (every
-// router CTA has read it).  The transient arrays live in the stage ring,
-// which no copy has touched yet.  Returns the number of work items.
+// boundary's gather and the staged checks read.  The transient arrays live
+// in the stage ring, which no copy has touched yet.  Returns the number of
+// work items.
 __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   const Workspace& ws = p.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -193,7 +257,7 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   for (int i = tid; i < EW; i += blockDim.x) emap[i] = 0u;
   for (int i = tid; i < E; i += blockDim.x) rmask[i] = 0u;
   if (warp < rows) {
-    const RouteRow rr{ws.logit_part, p.S, rows, E, k, p.rbias,
+    const RouteRow rr{ws.logit_part, 1, rows, E, k, nullptr,
                       lead ? ws.logits : nullptr, lead ? ws.ids : nullptr,
                       lead ? ws.gates : nullptr, lead ? ws.flags : nullptr, ws.err, sids};
     route_row(rr, warp, lg + warp * E);
@@ -457,64 +521,22 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       // gate/up items below the grid size are taken statically (item b by CTA b)
       const int cbase = kGU ? (int)gridDim.x : 0;
       int it = first_claim >= 0 ? first_claim : (int)atomicAdd(claim, 1u) + cbase;
+      int nxt = 0;  // the next claim (raw: the grid offset is added only at its use)
       // Down items under in-kernel routing are numbered in active order, so
       // the expert is known at the claim: the stages' weights (and their
       // scale atoms) go out before the expert's h is published, and only the
       // h tiles wait for it.  Elsewhere down items are numbered in the order
       // the experts' h became ready.
       const bool early = !kGU && p.local_route;
-      int e = 0, tile = 0, nt = 0, brow = 0;
+      int e = 0, tile = 0, nt = 0, brow = 0, rot = 0;
       // Stage ks of the current item as the g-th stage through the ring:
       // wts arms its full barrier for every byte and issues the weight tiles
       // and scale atoms (waiting, bounded, for the slot); acts issues the
       // activation (gate/up) or h (down) tiles and scale lines.
       auto stage = [&](int ks, int gg, bool wts, bool acts) -> bool {
-        const int kb = ks * KPS;  // first K-block of this stage
-        const int nkb = min(KPS, KB - kb);
         const int s = gg % p.NS;
-        uint8_t* st = sm.stages + (size_t)s * p.stage_stride;
-        const int fb = s * p.Q + ks % p.Q;
-        uint64_t* full = &sm.full[fb];
-        if (wts) {
-          if (gg >= p.NS && !mbar_wait(&sm.empty[s], ((gg / p.NS) - 1) & 1, lim)) return false;
-          fbits ^= 1u << fb;
-          // weight tiles (a missing second K-block of a stage is zero filled
-          // and counts in full), the present K-blocks' scale atoms, and per
-          // N-tile the activation tiles and scale lines
-          const uint32_t sfa_b = 2048u * (uint32_t)nkb;
-          const uint32_t bytes = p.a_bytes + sfa_b * (uint32_t)p.T +
-                                 (uint32_t)(nt * KPS) * (4096u + 2048u);
-          mbar_arrive_expect_tx(full, bytes);
-          // gate rows (gate/up) or output rows (down) of this tile
-          if (p.tiled)  // tiles (e, tile, kb..kb+KPS-1) are contiguous
-            tma_3d_hint(st, tm_a, 0, 0, (e * p.row_tiles + tile) * KB + kb, full, pol);
-          else if (KPS == 1)
-            tma_2d(st, tm_a, kb * 128, e * p.RE + tile * 128, full, pol);
-          else
-            tma_3d_hint(st, tm_a, 0, e * p.RE + tile * 128, kb, full, pol);
-          bulk_g2s_plain(st + p.off_sfa,
-                         p.sfa + (((size_t)e * p.row_tiles + tile) * KB + kb) * 2048u, sfa_b,
-                         full);
-          if (kGU) {  // gate/up stages hold one K-block
-            const int ru = p.I / 128 + tile;  // up rows follow the gate rows
-            if (p.tiled)
-              tma_3d_hint(st + 16384, tm_a, 0, 0, (e * p.row_tiles + ru) * KB + kb, full, pol);
-            else
-              tma_2d(st + 16384, tm_a, kb * 128, e * p.RE + ru * 128, full, pol);
-            bulk_g2s_plain(st + p.off_sfa + 2048,
-                           p.sfa + (((size_t)e * p.row_tiles + ru) * KB + kb) * 2048u, 2048u,
-                           full);
-          }
-        }
-        if (acts) {
-          for (int t = 0; t < nt; ++t) {
-            if (KPS == 1)
-              tma_2d_plain(st + p.off_b + t * 4096, tm_b, kb * 128, brow + 32 * t, full);
-            else
-              tma_3d(st + p.off_b + t * 4096 * KPS, tm_b, 0, brow + 32 * t, kb, full);
-            tma_3d(st + p.off_sfb + t * 2048 * KPS, tm_sfb, 0, brow + 32 * t, kb * 4, full);
-          }
-        }
+        if (wts && gg >= p.NS && !mbar_wait(&sm.empty[s], ((gg / p.NS) - 1) & 1, lim)) return false;
+        tc_issue_stage(p, sm, tm_a, tm_b, tm_sfb, pol, kGU, e, tile, nt, brow, ks, gg, rot, wts, acts, fbits);
         return true;
       };
       for (int j = 0;; ++j) {
@@ -538,6 +560,7 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           tile = it % p.tiles;
           nt = (et.z + 31) / 32;
           brow = (kGU && p.direct) ? 0 : et.y;  // first B row
+          rot = tc_item_rot(p, it);
         }
         if (live && early) {
           // A ready expert takes the usual path (its stages' weights and h
@@ -581,15 +604,27 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           if (kGU && ok && pdn && pdn->local_route && dn_claim) *dn_claim = (int)atomicAdd(ws.counters + 2, 1u);
           break;
         }
-        const int nxt = (int)atomicAdd(claim, 1u) + cbase;  // its latency hides under this item
         for (int ks = 0; ks < npre; ++ks) stage(ks, g - npre + ks, false, true);
-        for (int ks = npre; ks < KS; ++ks, ++g)
+        // the next claim goes out once this item's first copies are issued
+        // (its latency then hides under the item)
+        bool claimed = false;
+        if (npre > 0) {
+          nxt = (int)atomicAdd(claim, 1u);
+          claimed = true;
+        }
+        for (int ks = npre; ks < KS; ++ks, ++g) {
           if (!stage(ks, g, true, true)) {
             latch_error(ws.err, kDevWaitTimeout);
             ok = false;
             break;
           }
-        it = nxt;
+          if (!claimed) {
+            nxt = (int)atomicAdd(claim, 1u);
+            claimed = true;
+          }
+        }
+        if (!claimed) nxt = (int)atomicAdd(claim, 1u);
+        it = nxt + cbase;
       }
       // every issued copy lands before the pipeline is torn down: the last
       // fill of a stage was issued only after every earlier fill of it had
@@ -632,9 +667,10 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
         tc_fence_after();
         const uint32_t dcol = ibase + (uint32_t)ab * p.acc_cols;
         bool first = true;
+        const int rot = tc_item_rot(p, v.x);
         for (int ks = q; ks < KS; ks += p.Q, ++c) {
           const int g = j * KS + ks;
-          const int nkb = min(KPS, KB - ks * KPS);
+          const int nkb = min(KPS, KB - tc_stage_k(p, ks, rot) * KPS);
           const int s = g % p.NS;
           const uint32_t par = (fpar >> s) & 1u;
           fpar ^= 1u << s;
@@ -877,35 +913,16 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
                  "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // the logits (or the routing and pooled MoE input), the quantized input
+  // and the zeroed item counters come from the kernels before
+  grid_dep_wait();
+  grid_dep_launch();
   int na;
   if (pg.local_route) {
-    // The router's expert groups count their finished logits: the CTA
-    // routes as soon as every group's are written, while the router's grid
-    // still quantizes the MoE input (bounded wait).  The quantized input,
-    // the item counters and the ready list come with the router's end.
-    if (tid == 0) {
-      const unsigned* cnt = pg.ws.counters + 4;
-      bool got = ld_acquire_u32(cnt) >= (unsigned)pg.n_leaders;
-      const uint64_t t0 = global_ns();
-      for (uint32_t i = 1; !got; ++i) {
-        got = ld_acquire_u32(cnt) >= (unsigned)pg.n_leaders;
-        if (!got && (i & 63u) == 0u && global_ns() - t0 > pg.ws.wait_ns) break;
-      }
-      if (!got) latch_error(pg.ws.err, kDevWaitTimeout);
-      *sm.flag = got ? 1 : 0;
-    }
-    __syncthreads();
-    const bool got = *reinterpret_cast<volatile int*>(sm.flag) != 0;
-    na = got ? tc_local_route(pg, sm) : -1;
-    grid_dep_wait();
-    grid_dep_launch();
+    na = tc_local_route(pg, sm);
     // every router CTA has read max |x|: reset for the next layer's boundary
     if (blockIdx.x == 0 && tid == 0) pg.ws.x_amax[0] = 0u;
   } else {
-    // the routing, the pooled MoE input and the item counters come from the
-    // kernels before
-    grid_dep_wait();
-    grid_dep_launch();
     na = __ldcg(pg.ws.n_virtual);
   }
   // the first gate/up item of CTA b is item b; later claims count from the

@@ -69,9 +69,7 @@ struct Workspace {
   int* n_virtual;        // [1]         virtual experts of the step (V = E + rows*k/32 + 1 slots)
   unsigned* rg_count;    // [16]        router CTA arrivals per block of 8 rows
   unsigned* counters;    // [8]         [0] router row blocks routed, [1] gate/up item claims,
-                         //             [2] down item claims, [3] experts ready, [4] router expert
-                         //             groups whose summed logits are written (at most 8 rows;
-                         //             reset by the boundary before the router), [5..7] unused
+                         //             [2] down item claims, [3] experts ready, [4..7] unused
   unsigned* err;         // [1]         latched DeviceError; [1]: the first changed guard's index
   unsigned long long wait_ns;  // limit of every bounded wait in the kernels (a value, not a pointer)
 };
@@ -96,8 +94,10 @@ struct BoundaryParams {
   int front;                    // 1: the first layer's front -- the stream is the branch (the
                                 //    embedded tokens) itself, one norm (w_pre) into x_out
   float* aux;                   // [rows][H] copy of the updated stream, or null
-  unsigned* sig_reset;          // a signal word zeroed once the kernel before has finished, or
-                                // null (the router's logit count, Workspace::counters[4])
+  unsigned* reset0;             // words zeroed once the kernel before has finished (the experts
+  int n_reset0;                 //   kernel's counters and ready list when it routes itself), or
+  unsigned* reset1;             //   null
+  int n_reset1;
   int round_norm;               // 1: the second norm reads the stream rounded to bf16
                                 // (x_out may be null: no normalised output)
   const float* part;            // [part_S][rows][H] fp32 split-K partials of a bf16 branch,
@@ -121,7 +121,7 @@ struct RouterParams {
                                 // routing reads one slice and no bias
   int route_in_experts;         // 1 (at most 8 rows, tensor-core experts): the experts kernel
                                 // routes the rows and pools the pairs itself; the router only
-                                // writes the partial logits and the MoE input's quantization
+                                // writes the logits and the MoE input's quantization
   Workspace ws;
 };
 

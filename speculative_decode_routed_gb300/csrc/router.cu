@@ -35,18 +35,6 @@ constexpr int kRouterChunks = 4;   // 8-element chunks per lane per slice: slice
 constexpr int kMaxTopK = 16;
 constexpr int kRowBlock = 8;       // rows whose x slice is staged at once
 
-__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
-  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
-    acc = fmaf(fa.x, fb.x, acc);
-    acc = fmaf(fa.y, fb.y, acc);
-  }
-  return acc;
-}
-
 // Shared-memory carve of the routing and pooler tails.
 struct RouteSmem {
   float* lg;        // [warps][E]
@@ -447,30 +435,16 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
       if (p.bias) acc += bias_v;  // the same fp32 sum, then the bias, as the routing would add it
       if (wi < p.EG && ee < p.E) ws.logit_part[(size_t)r * p.E + ee] = acc;
     }
-    if (p.route_in_experts && sl == 0) {
-      // this expert group's logits are final: counted for the experts
-      // kernel, which routes as soon as every group's are (while the rest of
-      // this grid quantizes x)
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(ws.counters + 4, 1u);
-    }
     // every peer keeps its partials until the sums are read
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
   // beyond one block of rows, route_kernel routes the blocks in parallel
   if (nrb > 1) return;
-  if (p.route_in_experts) {
-    // the experts kernel routes and pools (and resets max |x| once every
-    // router CTA has read it); its item claims and ready list start empty
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
-      const int V = virtual_slots(p.E, p.rows * p.k);
-      for (int v = threadIdx.x; v < V; v += kRouterThreads) ws.ready_info[v] = 0u;
-      if (threadIdx.x < 4) ws.counters[threadIdx.x] = 0u;
-    }
-    return;
-  }
+  // the experts kernel routes and pools (and resets max |x| once every
+  // router CTA has read it); the boundary cleared its item claims and ready
+  // list
+  if (p.route_in_experts) return;
 
   // one block of rows: the last CTA to finish routes them and builds the pooler
   __syncthreads();

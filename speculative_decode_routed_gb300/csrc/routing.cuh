@@ -64,11 +64,11 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 
 // One row's routing for E <= 256: lane owns experts e = lane + 32 i (i < 8),
 // their logits in registers.  The slices' partial sums are all loaded at
-// once and added in slice order.  Each of the k + 1 selections is two warp
-// reductions: the largest key among the lanes' heads (redux.sync max), then
-// the lowest expert id among the lanes whose head has that key (redux.sync
-// min), so ties go to the lower id; the winning lane drops the expert and
-// rescans its 8 keys for its next head (largest key, lowest id).
+// once and added in slice order.  Each lane sorts its 8 keys once; each of
+// the k + 1 selections is then two warp reductions: the largest key among
+// the lanes' heads (redux.sync max), then the lowest expert id among the
+// lanes whose head has that key (redux.sync min), so ties go to the lower
+// id; the winning lane shifts its sorted keys to the next.
 __device__ inline void route_row_small(const RouteRow& p, int r) {
   const int E = p.E, k = p.k, rows = p.rows, lane = threadIdx.x & 31;
   float v[8];
@@ -106,36 +106,49 @@ __device__ inline void route_row_small(const RouteRow& p, int r) {
   for (int i = 0; i < 8; ++i)
     if (lane + 32 * i < E) z += expf(v[i] - m);
   z = warp_sum(z);
-  uint32_t hk = key[0];
-  int hi = 0;
+  // the lane's 8 keys sorted (largest first, ties to the lower expert id) by
+  // a 19-comparator odd-even merge network; the head is then the lane's best
+  uint32_t sk[8];
+  int si[8];
 #pragma unroll
-  for (int i = 1; i < 8; ++i)
-    if (key[i] > hk) {
-      hk = key[i];
-      hi = i;
-    }
+  for (int i = 0; i < 8; ++i) {
+    sk[i] = key[i];
+    si[i] = i;
+  }
+  constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                               {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                               {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const int a = kNet[c][0], b = kNet[c][1];
+    const bool keep = sk[a] > sk[b] || (sk[a] == sk[b] && si[a] < si[b]);
+    const uint32_t ka = sk[a], kb = sk[b];
+    const int ia = si[a], ib = si[b];
+    sk[a] = keep ? ka : kb;
+    sk[b] = keep ? kb : ka;
+    si[a] = keep ? ia : ib;
+    si[b] = keep ? ib : ia;
+  }
   const int nsel = (k < E) ? k + 1 : k;
   int sel_id = -1;
   float sel_v = 0.0f;
   for (int t = 0; t < nsel; ++t) {
-    const uint32_t gk = __reduce_max_sync(0xffffffffu, hk);
-    const uint32_t gid = __reduce_min_sync(0xffffffffu, hk == gk ? (uint32_t)(lane + 32 * hi) : 0xffffffffu);
+    // the largest head key, then the lowest expert id among the lanes whose
+    // head has it; the winning lane moves on to its next key
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, sk[0]);
+    const uint32_t gid =
+        __reduce_min_sync(0xffffffffu, sk[0] == gk ? (uint32_t)(lane + 32 * si[0]) : 0xffffffffu);
     if (lane == t) {
       sel_id = (int)gid;
       sel_v = key_logit(gk);
     }
     if (lane == (int)(gid & 31u)) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i == hi) key[i] = 0u;
-      hk = key[0];
-      hi = 0;
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (key[i] > hk) {
-          hk = key[i];
-          hi = i;
-        }
+      for (int i = 0; i < 7; ++i) {
+        sk[i] = sk[i + 1];
+        si[i] = si[i + 1];
+      }
+      sk[7] = 0u;
     }
   }
   route_finish(p, r, nsel, sel_id, sel_v, m, z);

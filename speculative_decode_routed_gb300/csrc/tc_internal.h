@@ -39,12 +39,8 @@ struct TcParams {
   int withhold_ready;       // self-test of the bounded waits: completed experts are not
                             // published to the down phase, whose waits then all run out
   int local_route;          // 1 (at most 8 rows): every CTA routes the rows from the router's
-                            // partial logits and pools their pairs in shared memory
+                            // logits and pools their pairs in shared memory
   int rows;                 // rows of the step (local routing)
-  int n_leaders;            // local routing: the router's expert groups, each of which counts
-                            // its finished logits in Workspace::counters[4]
-  int S;                    // the router's split-K slices: partials [S][rows][E]
-  const float* rbias;       // the router's logit bias [E], or null
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
   Workspace ws;
