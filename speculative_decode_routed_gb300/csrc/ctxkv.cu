@@ -78,42 +78,78 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One CTA per context row; 8 columns per thread.
-__global__ void ctx_norm_kernel(CtxNormParams p) {
+constexpr int kNormChunks = 2;      // 8-column chunks per thread
+constexpr int kNormPreLayers = 4;   // layers whose norm weights a thread loads up front
+
+// One CTA per context row; chunks of 8 columns, kNormChunks per thread (thread
+// t takes chunks t + j * blockDim).  Every load the thread needs -- its
+// context columns, the hidden norm's weights and the first layers'
+// pre-projection weights -- is issued at once, before the two reductions, so
+// the kernel's latency is one memory round trip plus the reductions.
+__global__ void __launch_bounds__(512, 1) ctx_norm_kernel(CtxNormParams p) {
   grid_dep_launch();  // the projection may start streaming its weights
   __shared__ float red[32];
   const int r = blockIdx.x;
-  const int col = threadIdx.x * 8;
-  const bool live = col < p.H;
-  float c[8] = {};
-  if (live) unpack8(__ldg(reinterpret_cast<const uint4*>(p.ctx + (size_t)r * p.H + col)), c);
+  const int nch = p.H / 8;
+  uint4 craw[kNormChunks];
+  float4 wh[kNormChunks][2];
+  float4 wp[kNormPreLayers][kNormChunks][2];
+#pragma unroll
+  for (int j = 0; j < kNormChunks; ++j) {
+    const int ch = threadIdx.x + j * blockDim.x, col = ch * 8;
+    const bool live = ch < nch;
+    craw[j] = live ? __ldg(reinterpret_cast<const uint4*>(p.ctx + (size_t)r * p.H + col)) : make_uint4(0u, 0u, 0u, 0u);
+    wh[j][0] = live ? __ldg(reinterpret_cast<const float4*>(p.w_hidden + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    wh[j][1] = live ? __ldg(reinterpret_cast<const float4*>(p.w_hidden + col + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int l = 0; l < kNormPreLayers; ++l)
+      if (live && l < p.L) {
+        wp[l][j][0] = __ldg(reinterpret_cast<const float4*>(p.w_pre + (size_t)l * p.H + col));
+        wp[l][j][1] = __ldg(reinterpret_cast<const float4*>(p.w_pre + (size_t)l * p.H + col + 4));
+      }
+  }
+  float c[kNormChunks][8];
   float ss = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ss += c[i] * c[i];
-  const float inv_hidden = rsqrtf(block_sum_all(ss, red) / (float)p.H + p.eps);
-  float f[8] = {};
-  if (live) {
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.w_hidden + col));
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.w_hidden + col + 4));
-    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  for (int j = 0; j < kNormChunks; ++j) {
+    unpack8(craw[j], c[j]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = __bfloat162float(__float2bfloat16_rn(c[i] * inv_hidden * w[i]));
-    *reinterpret_cast<uint4*>(p.fc + (size_t)r * p.H + col) = pack8(f);
+    for (int i = 0; i < 8; ++i) ss += c[j][i] * c[j][i];
   }
+  const float inv_hidden = rsqrtf(block_sum_all(ss, red) / (float)p.H + p.eps);
+  float f[kNormChunks][8];
   float ss2 = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ss2 += f[i] * f[i];
+  for (int j = 0; j < kNormChunks; ++j) {
+    const int ch = threadIdx.x + j * blockDim.x;
+    const float w[8] = {wh[j][0].x, wh[j][0].y, wh[j][0].z, wh[j][0].w,
+                        wh[j][1].x, wh[j][1].y, wh[j][1].z, wh[j][1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[j][i] = __bfloat162float(__float2bfloat16_rn(c[j][i] * inv_hidden * w[i]));
+      ss2 += f[j][i] * f[j][i];
+    }
+    if (ch < nch) *reinterpret_cast<uint4*>(p.fc + (size_t)r * p.H + ch * 8) = pack8(f[j]);
+  }
   const float inv_pre = rsqrtf(block_sum_all(ss2, red) / (float)p.H + p.eps);
-  if (!live) return;
-  for (int l = 0; l < p.L; ++l) {
-    const float* wl = p.w_pre + (size_t)l * p.H + col;
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(wl));
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(wl + 4));
+  auto write_layer = [&](int l, int j, float4 w0, float4 w1) {
     const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = f[i] * inv_pre * w[i];
+    for (int i = 0; i < 8; ++i) o[i] = f[j][i] * inv_pre * w[i];
+    const int col = (threadIdx.x + j * blockDim.x) * 8;
     *reinterpret_cast<uint4*>(p.u + ((size_t)l * p.n + r) * p.H + col) = pack8(o);
+  };
+#pragma unroll
+  for (int j = 0; j < kNormChunks; ++j) {
+    if (threadIdx.x + j * blockDim.x >= nch) continue;
+#pragma unroll
+    for (int l = 0; l < kNormPreLayers; ++l)
+      if (l < p.L) write_layer(l, j, wp[l][j][0], wp[l][j][1]);
+    for (int l = kNormPreLayers; l < p.L; ++l) {
+      const float* wl = p.w_pre + (size_t)l * p.H + (threadIdx.x + j * blockDim.x) * 8;
+      write_layer(l, j, __ldg(reinterpret_cast<const float4*>(wl)), __ldg(reinterpret_cast<const float4*>(wl + 4)));
+    }
   }
 }
 
@@ -356,7 +392,7 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   pdl.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n, 1, 1);
-  cfg.blockDim = dim3(((d.hidden / 8 + 31) / 32) * 32, 1, 1);
+  cfg.blockDim = dim3(((d.hidden / 8 + moe::kNormChunks - 1) / moe::kNormChunks + 31) / 32 * 32, 1, 1);
   cfg.stream = s;
   cudaError_t e = cudaLaunchKernelEx(&cfg, moe::ctx_norm_kernel, np);
   if (e != cudaSuccess) return ck_cuda(e, "context norm launch");
