@@ -54,8 +54,8 @@ def _peaks():
 # active experts); valid only for the kernel source it was taken on.
 EXPERTS_TRAFFIC = {"source": ["speculative_decode_routed_gb300/csrc/experts_tc.cu",
                               "speculative_decode_routed_gb300/csrc/tc_ptx.cuh"],
-                   "sha256_prefix": "3c743dae3816b010", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": (1065534208 + 3768576) / 43}
+                   "sha256_prefix": "ee23f2db1005b57b", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": (1065511168 + 3129856) / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
