@@ -68,6 +68,7 @@ def lib():
             "oracle_down": (ctypes.c_int, [ctypes.c_int] * 5 + [_vp] * 8),
             "oracle_gather": (None, [ctypes.c_int] * 3 + [_vp] * 3),
             "oracle_layer_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_f64, _vp, _vp, _vp, _vp, _vp]),
+            "oracle_moe_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_vp, _vp, _vp]),
             "oracle_num_threads": (ctypes.c_int, []),
             "oracle_set_num_threads": (None, [ctypes.c_int]),
         }
@@ -375,15 +376,9 @@ def gather(gates, o, k):
     return y
 
 
-def layer_step(w: LayerWeights, k, eps, branch, stream, forced_ids=None):
-    """One layer: boundary, routing, pooler, NVFP4 experts.  Returns a dict with
-    the new fp32 stream and every intermediate."""
-    branch = _c(branch, np.float64)
-    s = np.array(stream, dtype=np.float32, copy=True, order="C")
-    rows, H = s.shape
-    E, I = w.E, w.I
+def _layer_outputs(rows, H, E, k, I):
     n = rows * k
-    o = dict(
+    return dict(
         x=np.zeros((rows, H), np.uint16), x_exact=np.zeros((rows, H)),
         x_codes=np.zeros((rows, H // 2), np.uint8), x_sf=np.zeros((rows, H // 16), np.uint8),
         x_sg=np.zeros(1, np.float32), x_amax=np.zeros(1, np.float32),
@@ -395,18 +390,48 @@ def layer_step(w: LayerWeights, k, eps, branch, stream, forced_ids=None):
         h=np.zeros((n, I), np.float32), h_codes=np.zeros((n, I // 2), np.uint8),
         h_sf=np.zeros((n, I // 16), np.uint8), h_sg=np.zeros(E, np.float32),
         h_amax=np.zeros(E, np.float32), o=np.zeros((n, H), np.float32))
-    st = _LayerOut(**{name: _p(a) for name, a in o.items()})
-    fi = None if forced_ids is None else _c(forced_ids, np.int32)
-    rc = lib().oracle_layer_step(rows, H, E, k, I, eps, ctypes.byref(w.struct()), _p(branch),
-                                 _p(s), _p(fi), ctypes.byref(st))
-    if rc:
-        raise ValueError("oracle_layer_step: an active expert's weights were not given")
-    o["stream"] = s
+
+
+def _finish(o):
     o["x_sg"] = np.float32(o["x_sg"][0])
     o["x_amax"] = np.float32(o["x_amax"][0])
     o["n_active"] = int(o["n_active"][0])
     o["active"] = o["active"][: o["n_active"]]
     return o
+
+
+def layer_step(w: LayerWeights, k, eps, branch, stream, forced_ids=None):
+    """One layer: boundary, routing, pooler, NVFP4 experts.  Returns a dict with
+    the new fp32 stream and every intermediate."""
+    branch = _c(branch, np.float64)
+    s = np.array(stream, dtype=np.float32, copy=True, order="C")
+    rows, H = s.shape
+    o = _layer_outputs(rows, H, w.E, k, w.I)
+    st = _LayerOut(**{name: _p(a) for name, a in o.items()})
+    fi = None if forced_ids is None else _c(forced_ids, np.int32)
+    rc = lib().oracle_layer_step(rows, H, w.E, k, w.I, eps, ctypes.byref(w.struct()), _p(branch),
+                                 _p(s), _p(fi), ctypes.byref(st))
+    if rc:
+        raise ValueError("oracle_layer_step: an active expert's weights were not given")
+    o["stream"] = s
+    return _finish(o)
+
+
+def moe_step(w: LayerWeights, k, x, forced_ids=None):
+    """A layer's MoE part alone from its bf16 MoE input x (uint16 [rows, H]):
+    routing (forced_ids as in layer_step), pooler, the input's NVFP4
+    quantization and the experts.  The same arithmetic as layer_step after its
+    boundary."""
+    x = _c(x, np.uint16)
+    rows, H = x.shape
+    o = _layer_outputs(rows, H, w.E, k, w.I)
+    o["x"][...] = x
+    st = _LayerOut(**{name: _p(a) for name, a in o.items()})
+    fi = None if forced_ids is None else _c(forced_ids, np.int32)
+    rc = lib().oracle_moe_step(rows, H, w.E, k, w.I, ctypes.byref(w.struct()), _p(fi), ctypes.byref(st))
+    if rc:
+        raise ValueError("oracle_moe_step: an active expert's weights were not given")
+    return _finish(o)
 
 
 def num_threads() -> int:

@@ -591,10 +591,11 @@ void oracle_gather(int rows, int H, int k, const double* gates, const float* o, 
 
 /* ---------------------------------------------------------------- one layer */
 
-int oracle_layer_step(int rows, int H, int E, int k, int I, double eps,
-                      const oracle_layer_weights* w, const double* branch, float* stream,
-                      const int32_t* forced_ids, oracle_layer_out* out) {
-  oracle_boundary(rows, H, eps, branch, stream, w->w_post, w->w_pre, out->x, out->x_exact);
+/* The MoE part of a layer from its bf16 input out->x (already filled): the
+   routing (optionally with the given ids), the pooler, the input's NVFP4
+   quantization and the experts. */
+int oracle_moe_step(int rows, int H, int E, int k, int I, const oracle_layer_weights* w,
+                    const int32_t* forced_ids, oracle_layer_out* out) {
   double* p = (double*)malloc(sizeof(double) * (size_t)rows * E);
   oracle_route(rows, H, E, k, out->x, w->router_w, w->router_bias, NULL, p, out->ids, out->gates,
                out->flags, out->gap);
@@ -626,6 +627,13 @@ int oracle_layer_step(int rows, int H, int E, int k, int I, double eps,
                   out->h_sf, out->h_sg, out->o))
     return -1;
   return 0;
+}
+
+int oracle_layer_step(int rows, int H, int E, int k, int I, double eps,
+                      const oracle_layer_weights* w, const double* branch, float* stream,
+                      const int32_t* forced_ids, oracle_layer_out* out) {
+  oracle_boundary(rows, H, eps, branch, stream, w->w_post, w->w_pre, out->x, out->x_exact);
+  return oracle_moe_step(rows, H, E, k, I, w, forced_ids, out);
 }
 
 /* Host threads the oracle's parallel loops use (n >= 1); for timing it on a

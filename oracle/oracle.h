@@ -167,6 +167,13 @@ int oracle_layer_step(int rows, int H, int E, int k, int I, double eps,
                       const oracle_layer_weights* w, const double* branch, float* stream,
                       const int32_t* forced_ids, oracle_layer_out* out);
 
+/* The same layer's MoE part alone, from the bf16 MoE input already in
+ * out->x (x_exact is not touched): routing, pooler, the input's NVFP4
+ * quantization and the experts, with forced_ids as above.  oracle_layer_step
+ * is the boundary followed by this. */
+int oracle_moe_step(int rows, int H, int E, int k, int I, const oracle_layer_weights* w,
+                    const int32_t* forced_ids, oracle_layer_out* out);
+
 /* Number of OpenMP threads the oracle uses (for reporting). */
 void oracle_set_num_threads(int n);
 int oracle_num_threads(void);

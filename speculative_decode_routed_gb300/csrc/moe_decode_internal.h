@@ -159,6 +159,9 @@ constexpr int kSmemBudget = 226 * 1024;  // of the 227 KB a CTA may use
 int boundary_cluster(int H);
 cudaError_t launch_boundary(const BoundaryParams& p, int cluster, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl);
+// Whether the tensor-core router's K-slices fit H (H a multiple of 256 S,
+// slices at most 1024 wide).
+bool router_mma_fits(const RouterParams& p);
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_quantize(const float* v, int64_t rows, int64_t cols, uint8_t* codes,
                             uint8_t* sf, float* sg, float* amax, cudaStream_t s);

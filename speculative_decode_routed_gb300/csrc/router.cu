@@ -572,6 +572,8 @@ size_t router_smem_bytes(int E, int rows) {
   return route > xslice ? route : xslice;
 }
 
+bool router_mma_fits(const RouterParams& p) { return p.H % (p.S * 256) == 0 && p.H / p.S <= 1024; }
+
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   const size_t smem = router_smem_bytes(p.E, p.rows);
   static_assert(kMaxTopK <= 32, "one lane per selected expert");
@@ -591,10 +593,13 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
   if (p.cluster_sum && (nrb != 1 || p.S > 8 || p.EG != kRouterWarps)) return cudaErrorInvalidValue;
   cfg.numAttrs = p.cluster_sum ? 2 : 1;
-  const bool mma = nrb > 1 && p.H % (p.S * 256) == 0 && p.H / p.S <= 1024;
+  // the tensor-core dot products beyond one block of rows, and for one block
+  // when the experts kernel routes (it sums the slices' partials itself)
+  const bool mma = !p.cluster_sum && (nrb > 1 || p.route_in_experts) && router_mma_fits(p);
+  if (p.route_in_experts && !mma && !p.cluster_sum) return cudaErrorInvalidValue;
   if (mma) cfg.gridDim = dim3((p.E + 15) / 16, p.S, 1);
   cudaError_t e = mma ? cudaLaunchKernelEx(&cfg, router_mma_kernel, p) : cudaLaunchKernelEx(&cfg, router_kernel, p);
-  if (e != cudaSuccess || nrb == 1) return e;
+  if (e != cudaSuccess || nrb == 1 || p.route_in_experts) return e;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(nrb, 1, 1);
   return cudaLaunchKernelEx(&cfg, route_kernel, p);

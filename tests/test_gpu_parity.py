@@ -277,7 +277,9 @@ def end_to_end(w, dec, rows, variant=0, sample_layers=None, n_sample=1, stage_la
       - the layers in stage_layers pass every staged check on a sample.
     Over several layers the stream is not compared from the step's inputs
     alone: the chain is ill-conditioned (R32), a one-ulp change of its input
-    grows past the tolerance within a few layers in the oracle itself.  With
+    grows past the tolerance within a few layers in the oracle itself.  Within
+    a layer, where the oracle's MoE input differs from the GPU's at a bf16
+    midpoint, the MoE part runs from the GPU's input (R34).  With
     chain_report (a list), the oracle is also run freely from the step's
     inputs (the GPU's ids forced) and its per-layer divergence is appended.
     Returns the per-layer report."""
@@ -319,7 +321,12 @@ def end_to_end(w, dec, rows, variant=0, sample_layers=None, n_sample=1, stage_la
         agree = np.all(own["ids"] == g["ids"], axis=1)
         flagged = own["flags"] != 0
         assert np.all(agree | flagged | ~same_x), f"layer {l}: ids differ on an unflagged row"
-        y = oracle.gather(o["gates"], o["o"], k)
+        # where the oracle's MoE input differs from the GPU's (at a bf16
+        # rounding midpoint: the previous boundary's check bounds that), the
+        # MoE part continues from the GPU's input: one ulp at an NVFP4 code
+        # boundary moves the experts' outputs by whole quantization steps (R34)
+        moe = o if np.all(same_x) else oracle.moe_step(ow, k, g["x"], forced_ids=g["ids"])
+        y = oracle.gather(moe["gates"], moe["o"], k)
         last = l == w.n_layers - 1
         nxt_w = (wpf, wf) if last else synth.norm_weights(w, l + 1)
         s_ref, b_ref, b_exact = oracle.boundary(y, o["stream"], nxt_w[0], nxt_w[1], w.eps)

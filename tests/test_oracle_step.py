@@ -343,3 +343,49 @@ def test_chained_layers_amplify_a_one_ulp_input_change():
     assert rel(w.n_layers - 1) > 10 * 2e-3
     # the growth passes through a changed h tensor scale on the way
     assert any(not np.array_equal(a[l]["h_sg"], b[l]["h_sg"]) for l in range(w.n_layers))
+
+
+def test_moe_step_is_layer_step_after_its_boundary():
+    """The MoE part alone, from the boundary's bf16 output, reproduces every
+    intermediate of the whole layer bit for bit (the same arithmetic)."""
+    w = synth.Workload("moe_part", rows=6, hidden=512, n_experts=12, top_k=3, inter=256)
+    ow = oracle_weights(w, 0)
+    s0, b0 = synth.step_inputs(w, 0)
+    full = oracle.layer_step(ow, w.top_k, w.eps, oracle.bf16_to_f64(b0), s0)
+    part = oracle.moe_step(ow, w.top_k, full["x"])
+    for name in ("ids", "gates", "flags", "x_codes", "x_sf", "x_sg", "count", "offset", "pair_order",
+                 "active", "h", "h_codes", "h_sf", "h_sg", "o"):
+        assert np.array_equal(np.asarray(full[name]), np.asarray(part[name])), name
+    forced = np.roll(full["ids"], 1, axis=1)
+    a = oracle.layer_step(ow, w.top_k, w.eps, oracle.bf16_to_f64(b0), s0, forced_ids=forced)
+    b = oracle.moe_step(ow, w.top_k, a["x"], forced_ids=forced)
+    assert np.array_equal(a["gates"], b["gates"]) and np.array_equal(a["o"], b["o"])
+
+
+def test_one_ulp_moe_input_change_moves_the_experts_past_the_tolerance():
+    """Why a layer's end-to-end check continues from the GPU's MoE input where
+    the oracle's differs from it at a bf16 rounding midpoint (R34): one
+    element of x moved by one bf16 ulp -- the size of such a difference --
+    flips its NVFP4 code when it sits at a code boundary, and that moves the
+    layer's expert outputs by far more than the end-to-end tolerance
+    (2e-3 * rms): h changes, its per-expert NVFP4 tensor is re-quantized, and
+    whole quantization steps follow."""
+    w = synth.Workload("moe_ulp", rows=4, hidden=1024, n_experts=8, top_k=2, inter=256)
+    ow = oracle_weights(w, 0)
+    s0, b0 = synth.step_inputs(w, 0)
+    a = oracle.layer_step(ow, w.top_k, w.eps, oracle.bf16_to_f64(b0), s0)
+    rms = np.sqrt(np.mean(a["o"].astype(np.float64) ** 2))
+    worst, flips = 0.0, 0
+    for r in range(w.rows):
+        for col in range(0, w.hidden, 3):
+            x = a["x"].copy()
+            x[r, col] = np.uint16(x[r, col] + 1)  # one bf16 ulp (away from zero)
+            b = oracle.moe_step(ow, w.top_k, x, forced_ids=a["ids"])
+            if np.array_equal(a["x_codes"], b["x_codes"]) and np.array_equal(a["x_sf"], b["x_sf"]):
+                continue                           # most such changes leave every code alone
+            flips += 1
+            worst = max(worst, float(np.max(np.abs(a["o"].astype(np.float64) - b["o"]))) / rms)
+        if flips >= 6:
+            break
+    assert flips >= 3
+    assert worst > 5 * 2e-3
