@@ -492,11 +492,10 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   rp.bias = w.router_bias;
   rp.line_rows = d.max_rows * d.top_k;
   rp.route_in_experts = local_route ? 1 : 0;
-  // one block of rows: the tensor-core router's slice partials, summed (in
-  // slice order) by the experts kernel's routing when it routes; else the
-  // CUDA-core router summing its slices in a thread-block cluster
-  const bool mma_route = local_route && moe::router_mma_fits(rp);
-  rp.cluster_sum = (rows <= 8 && !mma_route) ? 1 : 0;
+  // one block of rows: the router's slice CTAs sum their partials in a
+  // thread-block cluster (the tensor-core router's when the experts kernel
+  // routes and H splits into its slices)
+  rp.cluster_sum = rows <= 8 ? 1 : 0;
   rp.ws = h->ws;
   e = moe::launch_router(rp, s, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
@@ -533,8 +532,6 @@ int launch_layer(moe_decode_t* h, int layer, int rows, const uint16_t* branch, f
   tg.withhold_ready = withhold_ready ? 1 : 0;
   tg.local_route = td.local_route = local_route ? 1 : 0;
   tg.rows = td.rows = rows;
-  tg.S = td.S = mma_route ? rp.S : 1;
-  tg.rbias = td.rbias = mma_route ? w.router_bias : nullptr;
   e = moe::launch_tc_moe(tg, h->tm_w13[layer], direct ? h->tm_xcodes : h->tm_xpool, h->tm_xlines,
                          td, h->tm_w2[layer],
                          h->tm_hcodes, h->tm_hlines, h->num_sms, s, pdl);

@@ -257,7 +257,7 @@ __device__ int tc_local_route(const TcParams& p, const TcSmem& sm) {
   for (int i = tid; i < EW; i += blockDim.x) emap[i] = 0u;
   for (int i = tid; i < E; i += blockDim.x) rmask[i] = 0u;
   if (warp < rows) {
-    const RouteRow rr{ws.logit_part, p.S, rows, E, k, p.rbias,
+    const RouteRow rr{ws.logit_part, 1, rows, E, k, nullptr,
                       lead ? ws.logits : nullptr, lead ? ws.ids : nullptr,
                       lead ? ws.gates : nullptr, lead ? ws.flags : nullptr, ws.err, sids};
     route_row(rr, warp, lg + warp * E);

@@ -478,6 +478,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(RouterParams 
 // multiple of 256 (a warp's columns in 32-column blocks, at most 4).
 __global__ void __launch_bounds__(kRouterThreads, 1) router_mma_kernel(RouterParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float s_tile[128];  // cluster sum: this slice's [16 experts][8 rows] partials
   const Workspace& ws = p.ws;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
   const int e0 = blockIdx.x * 16, sl = blockIdx.y;
@@ -529,11 +530,42 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_mma_kernel(RouterPar
 #pragma unroll
       for (int w = 0; w < kRouterWarps; ++w) v += red[w * 128 + threadIdx.x];
       const int e = e0 + (threadIdx.x >> 3), r = rb * kRowBlock + (threadIdx.x & 7);
-      if (e < p.E && r < p.rows) ws.logit_part[((size_t)sl * p.rows + r) * p.E + e] = v;
+      if (p.cluster_sum)
+        s_tile[threadIdx.x] = v;
+      else if (e < p.E && r < p.rows)
+        ws.logit_part[((size_t)sl * p.rows + r) * p.E + e] = v;
     }
     __syncthreads();
   }
+  if (!p.cluster_sum) {
+    quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
+    return;
+  }
+  // one block of rows: the S slice CTAs of this group of 16 experts form a
+  // cluster; its first CTA sums their [16 experts x 8 rows] tiles in slice
+  // order and adds the bias, into logit_part's first slice (the logits), and
+  // the barrier's wait hides behind this CTA's share of the quantization
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   quantize_share(p, __fdiv_rn(__uint_as_float(__ldcg(ws.x_amax)), 2688.0f));
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (sl == 0 && threadIdx.x < 128) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int e = e0 + (threadIdx.x >> 3), r = threadIdx.x & 7;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = q < p.S ? *cluster.map_shared_rank(&s_tile[threadIdx.x], q) : 0.0f;
+    float acc = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < p.S) acc += v[q];
+    if (e < p.E && r < p.rows) {
+      if (p.bias) acc += __ldg(p.bias + e);
+      ws.logit_part[(size_t)r * p.E + e] = acc;
+    }
+  }
+  // every peer keeps its tile until the sums are read
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Beyond one block of rows: after the router's dot products (programmatic
@@ -591,12 +623,11 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   const int nrb = (p.rows + kRowBlock - 1) / kRowBlock;
-  if (p.cluster_sum && (nrb != 1 || p.S > 8 || p.EG != kRouterWarps)) return cudaErrorInvalidValue;
   cfg.numAttrs = p.cluster_sum ? 2 : 1;
   // the tensor-core dot products beyond one block of rows, and for one block
-  // when the experts kernel routes (it sums the slices' partials itself)
-  const bool mma = !p.cluster_sum && (nrb > 1 || p.route_in_experts) && router_mma_fits(p);
-  if (p.route_in_experts && !mma && !p.cluster_sum) return cudaErrorInvalidValue;
+  // when the experts kernel routes (then summed in a cluster as well)
+  const bool mma = (nrb > 1 || p.route_in_experts) && router_mma_fits(p);
+  if (p.cluster_sum && (nrb != 1 || p.S > 8 || (!mma && p.EG != kRouterWarps))) return cudaErrorInvalidValue;
   if (mma) cfg.gridDim = dim3((p.E + 15) / 16, p.S, 1);
   cudaError_t e = mma ? cudaLaunchKernelEx(&cfg, router_mma_kernel, p) : cudaLaunchKernelEx(&cfg, router_kernel, p);
   if (e != cudaSuccess || nrb == 1 || p.route_in_experts) return e;

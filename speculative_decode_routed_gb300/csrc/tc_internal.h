@@ -41,8 +41,6 @@ struct TcParams {
   int local_route;          // 1 (at most 8 rows): every CTA routes the rows from the router's
                             // logits and pools their pairs in shared memory
   int rows;                 // rows of the step (local routing)
-  int S;                    // local routing: the router's K-slice partials to sum [S][rows][E]
-  const float* rbias;       // local routing: the router's logit bias [E] to add, or null
   const uint8_t* sfa;       // weight scale atoms [E][row_tiles][KBLK][2048]
   const float* gscale;      // [E][3]
   Workspace ws;
