@@ -44,19 +44,25 @@ __device__ __forceinline__ void block_sum_to_slot(float v, float* warp_red, floa
   }
 }
 
-// The cluster-wide sum of one shared-memory slot: every peer's value read at
-// once (at most 8 CTAs), then added in rank order, so every CTA forms the same
-// total bit for bit.
-__device__ __forceinline__ float cluster_slot_sum(cg::cluster_group& cluster, float* slot) {
-  const unsigned n = cluster.num_blocks();
-  float v[8];
+// The cluster-wide sum of one shared-memory slot (after a cluster barrier):
+// lanes 0..7 of warp 0 read one peer's value each (at most 8 CTAs), lane 0
+// adds them in rank order -- so every CTA forms the same total bit for bit --
+// and the block reads the total from its own shared memory (*total).  One
+// remote read per peer and CTA, not one per thread.
+__device__ __forceinline__ float cluster_slot_sum(cg::cluster_group& cluster, float* slot, float* total) {
+  if (threadIdx.x < 32) {
+    const unsigned n = cluster.num_blocks(), lane = threadIdx.x;
+    const float v = lane < n ? *cluster.map_shared_rank(slot, lane) : 0.0f;
+    float t = 0.0f;
 #pragma unroll
-  for (unsigned q = 0; q < 8; ++q) v[q] = q < n ? *cluster.map_shared_rank(slot, q) : 0.0f;
-  float t = 0.0f;
-#pragma unroll
-  for (unsigned q = 0; q < 8; ++q)
-    if (q < n) t += v[q];
-  return t;
+    for (unsigned q = 0; q < 8; ++q) {
+      const float vq = __shfl_sync(0xffffffffu, v, q);
+      if (q < n) t += vq;
+    }
+    if (lane == 0) *total = t;
+  }
+  __syncthreads();
+  return *total;
 }
 
 // KMAX: the most gather slots (k <= KMAX); 8 keeps the registers, and so
@@ -66,6 +72,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float warp_red[32];
   __shared__ float part[2];
+  __shared__ float part_total[2];
   __shared__ float amax_red[32];
 
   const int r = blockIdx.y;
@@ -155,7 +162,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
     // rms of the branch over the whole row (cluster-wide)
     block_sum_to_slot(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w, warp_red, &part[0]);
     cluster.sync();
-    const float ss = cluster_slot_sum(cluster, &part[0]);
+    const float ss = cluster_slot_sum(cluster, &part[0], &part_total[0]);
     const float inv1 = rsqrtf(ss / (float)p.H + p.eps);
     if (live) {
       s.x += y.x * inv1 * wpost.x;
@@ -179,7 +186,7 @@ __global__ void boundary_kernel(BoundaryParams p) {
   }
   block_sum_to_slot(s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w, warp_red, &part[1]);
   cluster.sync();
-  const float ss2 = cluster_slot_sum(cluster, &part[1]);
+  const float ss2 = cluster_slot_sum(cluster, &part[1], &part_total[1]);
   // this CTA has read its peers' shared memory for the last time: arrive now,
   // and wait only before exiting, so the barrier's latency hides behind the
   // stores below
