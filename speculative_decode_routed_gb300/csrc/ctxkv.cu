@@ -21,7 +21,11 @@
 // in split order (or reads the GEMM's bf16 output), and the head's D values
 // sit D/32 to a lane, so the key norm is a warp sum and the rotation's
 // partner dimension (j + D/2) is 16 lanes away (one shuffle).  The rotation's
-// cosines and sines come from a table built once at create in fp64.
+// cosines and sines come from a table built once at create in fp64.  After
+// the streaming projection it does not wait for the whole grid: each task
+// counts itself done per (layer, head) once its partials are stored, and a
+// head's warps start when its count is complete (ctx_norm_kernel resets the
+// counts each call, before the projection counts).
 
 #include <cmath>
 #include <cstdio>
@@ -31,6 +35,7 @@
 #include "common.cuh"
 #include "gemv.cuh"
 #include "tc_gemm.h"
+#include "tc_ptx.cuh"
 #include "moe_decode_internal.h"
 
 namespace moe {
@@ -44,6 +49,8 @@ struct CtxNormParams {
   const float* w_pre;        // [L][H]
   __nv_bfloat16* fc;         // [n][H]
   __nv_bfloat16* u;          // [L][n][H]
+  unsigned* done;            // the projection's per-head completion counters, reset here
+  int n_done;
 };
 
 // Sum over the block, the result in every thread; red holds 32 floats.
@@ -88,6 +95,10 @@ constexpr int kNormPreLayers = 4;   // layers whose norm weights a thread loads 
 // the kernel's latency is one memory round trip plus the reductions.
 __global__ void __launch_bounds__(512, 1) ctx_norm_kernel(CtxNormParams p) {
   grid_dep_launch();  // the projection may start streaming its weights
+  // this step's counters start from zero: the projection counts only after
+  // this grid has completed, and its consumer launches only after that
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.n_done; i += blockDim.x) p.done[i] = 0u;
   __shared__ float red[32];
   const int r = blockIdx.x;
   const int nch = p.H / 8;
@@ -170,6 +181,13 @@ struct KvRopeParams {
   __nv_bfloat16* k_cache;  // [L][n_slots][KVH][D]
   __nv_bfloat16* v_cache;
   unsigned* err;
+  // The streaming projection's per-(layer, head) completion counters, or
+  // null (then the whole projection grid is waited for): a head's partials
+  // are complete when its counter reaches done_target (its K and V row
+  // groups times the splits).  The wait gives up after wait_ns.
+  const unsigned* done;
+  unsigned done_target;
+  unsigned long long wait_ns;
 };
 
 constexpr unsigned kErrPosition = 3;  // a position outside the rotary table
@@ -228,7 +246,27 @@ __global__ void kv_rope_kernel(KvRopeParams p) {
   if (p.part) {
 #pragma unroll
     for (int i = 0; i < E; ++i) k[i] = v[i] = 0.0f;
-    grid_dep_wait();
+    if (p.done) {
+      // this head's tasks (every split of its K and V rows) have stored
+      // their partials: a bounded wait on its counter, then every lane reads
+      bool ok = true;
+      if (lane == 0) {
+        const unsigned* c = p.done + (size_t)l * p.KVH + hd;
+        const uint64_t t0 = global_ns();
+        while (tc::ld_acquire_u32(c) < p.done_target) {
+          if (global_ns() - t0 > p.wait_ns) {
+            latch_error(p.err, kDevWaitTimeout);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
+    } else {
+      grid_dep_wait();
+    }
     const size_t split = (size_t)p.L * p.n * 2 * KD;
     const float* src = p.part + ((size_t)l * p.n + r) * 2 * KD + hd * p.D + lane * E;
     // eight splits' loads in flight at a time, summed in split order
@@ -311,6 +349,7 @@ struct moe_ctxkv_s {
   __nv_bfloat16 *fc, *u, *kv, *k, *v;
   float2* cs;                       // rotary table, or null
   unsigned* err;
+  unsigned* done;                   // [L][KVH] the streaming projection's completion counters
   float* part;                      // split-K partials [S][L][rows][2 * KVH * D]
   int splits;                       // K-splits of the streaming projection; 0: none
   int num_sms;
@@ -384,6 +423,8 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   np.w_pre = h->w.w_pre;
   np.fc = h->fc;
   np.u = h->u;
+  np.done = h->done;
+  np.n_done = d.n_layers * d.n_kv_heads;
   const bool stream_w = h->splits > 0 && a.n <= 8;
   moe::GemmParams gp_tc;
   int tc_S = 0;  // the tensor-core projection's splits when it left partials
@@ -408,6 +449,9 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
     gp.n = a.n;
     gp.S = h->splits;
     gp.KC = d.hidden / h->splits;
+    gp.done = h->done;
+    gp.done_mod = KD;
+    gp.done_div = d.head_dim;
     cudaLaunchConfig_t gc = {};
     gc.gridDim = dim3(h->num_sms, 1, 1);
     gc.blockDim = dim3(moe::kGemvThreads, 1, 1);
@@ -452,10 +496,15 @@ int ctxkv_enqueue(moe_ctxkv_t* h, const ProjectArgs& a, cudaStream_t s, cudaEven
   kp.k_cache = reinterpret_cast<__nv_bfloat16*>(a.k_cache);
   kp.v_cache = reinterpret_cast<__nv_bfloat16*>(a.v_cache);
   kp.err = h->err;
+  kp.done = stream_w ? h->done : nullptr;
+  kp.done_target = (unsigned)(2 * (d.head_dim / 32) * h->splits);
+  kp.wait_ns = moe::kDefaultWaitNs;
   const long long warps = (long long)d.n_layers * a.n * d.n_kv_heads;
+  // CTAs of 4 warps, small enough to be resident beside a streaming
+  // projection CTA, so that a head's warps start as its counter completes
   cudaLaunchConfig_t rc = {};
-  rc.gridDim = dim3((unsigned)((warps * 32 + 255) / 256), 1, 1);
-  rc.blockDim = dim3(256, 1, 1);
+  rc.gridDim = dim3((unsigned)((warps * 32 + 127) / 128), 1, 1);
+  rc.blockDim = dim3(128, 1, 1);
   rc.stream = s;
   rc.attrs = (stream_w && !ev) ? &pdl : nullptr;
   rc.numAttrs = (stream_w && !ev) ? 1 : 0;
@@ -539,7 +588,8 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   const size_t b_fc = up16(2 * n * H), b_u = up16(2 * L * n * H), b_kv = up16(2 * L * n * 2 * KD),
                b_k = up16(2 * L * n * KD), b_cs = table * sizeof(float2);
   const size_t b_io = up16(2 * n * H) + up16(8 * n) + up16(8 * L * n);
-  const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16 + b_io;
+  const size_t b_done = up16(sizeof(unsigned) * L * d.n_kv_heads);
+  const size_t bytes = b_part + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16 + b_done + b_io;
   uint8_t* base = nullptr;
   e = cudaMalloc(&base, bytes);
   if (e != cudaSuccess) {
@@ -557,8 +607,10 @@ int moe_ctxkv_create(const moe_ctxkv_dims* dims, const moe_ctxkv_weights* w, moe
   h->v = reinterpret_cast<__nv_bfloat16*>(base + b_fc + b_u + b_kv + b_k);
   h->cs = table ? reinterpret_cast<float2*>(base + b_fc + b_u + b_kv + 2 * b_k) : nullptr;
   h->err = reinterpret_cast<unsigned*>(base + b_fc + b_u + b_kv + 2 * b_k + b_cs);
-  h->io = base + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16;
+  h->done = reinterpret_cast<unsigned*>(base + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16);
+  h->io = base + b_fc + b_u + b_kv + 2 * b_k + b_cs + 16 + b_done;
   e = cudaMemset(h->err, 0, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(h->done, 0, b_done);
   if (e == cudaSuccess && table) {
     // cos / sin of pos * theta^(-2j/D) in fp64, stored as fp32
     const int half = d.head_dim / 2;
@@ -731,9 +783,10 @@ int moe_ctxkv_last_error(moe_ctxkv_t* h) {
     cudaMemset(h->err, 0, sizeof(unsigned));
     char buf[160];
     snprintf(buf, sizeof(buf), "device-side error %u: %s", flag,
-             flag == moe::kErrPosition ? "a position outside [0, max_position)"
-             : flag == moe::kErrSlot   ? "a slot at or past n_slots"
-                                       : "unknown");
+             flag == moe::kErrPosition     ? "a position outside [0, max_position)"
+             : flag == moe::kErrSlot       ? "a slot at or past n_slots"
+             : flag == moe::kDevWaitTimeout ? "a bounded wait gave up"
+                                           : "unknown");
     return moe::api_fail(MOE_EDEVICE, buf);
   }
   return MOE_OK;

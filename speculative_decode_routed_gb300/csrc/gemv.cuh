@@ -36,6 +36,14 @@ struct GemvParams {
   int I;
   __nv_bfloat16* gu;   // [n][2I]
   __nv_bfloat16* act;  // [n][I]
+  // Completion counters (not gated; null: none).  Once a task's partials are
+  // stored, done[l * (done_mod / done_div) + (row0 % done_mod) / done_div] is
+  // incremented after a fence, so that a consumer can start on a group of
+  // rows as soon as all of its tasks have finished.  With counters the
+  // dependent grid is let launch only after this grid's dependency wait (so
+  // that it never sees the counters before the predecessor has reset them).
+  unsigned* done;
+  int done_mod, done_div;
 };
 
 constexpr int kGemvWarps = 12;
@@ -69,7 +77,7 @@ template <bool kGated>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p) {
   extern __shared__ uint4 gemv_ring[];
   // the dependents (the epilogue kernel) may launch now and wait for this grid
-  grid_dep_launch();
+  if (!p.done) grid_dep_launch();
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int warp = threadIdx.x >> 5;
   const int wid = warp * (int)gridDim.x + (int)blockIdx.x;
@@ -106,6 +114,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
     // the weights do not depend on the previous kernel; X does
     if (!waited) {
       grid_dep_wait();
+      if (p.done) grid_dep_launch();
       waited = true;
     }
     auto load_x = [&](int it, uint4 (&b)[4]) {
@@ -169,6 +178,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_bf16_kernel(GemvParams p
           const int i = 2 * t + (q & 1);
           if (i < p.n) out[(size_t)i * p.R + row] = acc[mt][q];
         }
+      if (p.done) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          atomicAdd(p.done + (size_t)l * (p.done_mod / p.done_div) + (row0 % p.done_mod) / p.done_div, 1u);
+      }
     }
   }
 }
