@@ -43,6 +43,10 @@ constexpr int kTcMaxThreads = 32 * (1 + 4 + 4);  // producer, up to 4 MMA issuer
 constexpr int kEpiThreads = 128;
 constexpr int kMaxPairsTc = 128;
 constexpr int kTcCtrl = 4096;             // barriers, tables, flags
+// Named barriers of the switch from gate/up to down (2 is the epilogue's own)
+constexpr int kBarSwitch = 3;    // every warp: the epilogue has read its last accumulators
+constexpr int kBarDownInit = 4;  // producer and issuers: the down barriers are initialised
+constexpr int kBarDownEpi = 5;   // the producer warp to the epilogue: the same
 
 // kind::mxf4nvf4 instruction descriptor: A, B e2m1 (1), K-major, scales
 // ue4m3 (0), M = 128, N = 32, dense.
@@ -412,6 +416,10 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
   const float amax = __uint_as_float(__ldcg(ws.h_amax + e));
   const float sg = __fdiv_rn(amax, 2688.0f);
   const int bpr = p.I / 16;
+  // blocks 4m..4m+3 of a row sit in four adjacent lanes (bpr and the stride
+  // are multiples of 4, so the four are active together): the lane of block
+  // 4m gathers their scales into the row's scale line m (one 16-byte line per
+  // row and MMA of 64: bytes 0-3 the four block scales, the rest zero)
   for (int b = t; b < ne * bpr; b += kEpiThreads) {
     const int row = pos0 + b / bpr, blk = b % bpr;
     const float4* src = reinterpret_cast<const float4*>(ws.h + (size_t)row * p.I + blk * 16);
@@ -428,16 +436,12 @@ __device__ void tc_quantize_expert_h(const TcParams& p, int e, int pos0, int ne,
     quant_block16(v, sg, lo, hi, sb);
     *reinterpret_cast<uint2*>(ws.h_codes + (size_t)row * (p.I / 2) + blk * 8) = make_uint2(lo, hi);
     ws.h_sf[(size_t)row * bpr + blk] = (uint8_t)sb;
-  }
-  tc_named_sync();
-  // scale lines: one 16-byte line per (row, MMA of 64): bytes 0-3 = its four
-  // block scales, the rest zero
-  const int lpr = p.I / 64;
-  for (int l = t; l < ne * lpr; l += kEpiThreads) {
-    const int row = pos0 + l / lpr, m = l % lpr;
-    const uint32_t w = __ldcg(reinterpret_cast<const uint32_t*>(ws.h_sf + (size_t)row * bpr) + m);
-    *reinterpret_cast<uint4*>(ws.h_lines + ((size_t)m * p.ws_pairs + row) * 16) =
-        make_uint4(w, 0u, 0u, 0u);
+    const unsigned mask = __activemask();
+    const uint32_t s1 = __shfl_down_sync(mask, sb, 1), s2 = __shfl_down_sync(mask, sb, 2),
+                   s3 = __shfl_down_sync(mask, sb, 3);
+    if ((blk & 3) == 0)
+      *reinterpret_cast<uint4*>(ws.h_lines + ((size_t)(blk >> 2) * p.ws_pairs + row) * 16) =
+          make_uint4(sb | (s1 << 8) | (s2 << 16) | (s3 << 24), 0u, 0u, 0u);
   }
   if (t == 0) ws.h_sg[e] = sg;
 }
@@ -862,6 +866,13 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
       if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
       ++cur_tiles;
     }
+    if (kGU) {
+      // its last accumulators are read: the other warps may switch the CTA to
+      // the down projection while this expert's publication runs
+      tc_fence_before();
+      __syncwarp();
+      named_bar_arrive(kBarSwitch, (int)blockDim.x);
+    }
     if (kGU && cur_e >= 0) tc_finish_expert(p, sm, cur_e, cur_tiles, cur_amax, t, cur_pos0, cur_ne, cur_a);
   }
 }
@@ -939,17 +950,28 @@ __global__ void __launch_bounds__(kTcMaxThreads, 1)
   int dn_claim = -1;  // the producer's first down claim, made when gate/up claims run out
   tc_phase<true>(pg, &g_a, &g_b, &g_sfb, sm, tmem, n_act * pg.tiles, epi0, first_claim, &pd, &dn_claim);
 
-  // this CTA's gate/up copies have landed, its MMAs completed and its
-  // accumulators been read: the shared memory takes the down layout
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) {
-    tc_barriers(pg, sm, false, tid);
+  // Once this CTA's gate/up copies have landed, its MMAs completed and its
+  // epilogue has read the last accumulators, the shared memory takes the down
+  // layout, and the producer and issuers start on the down items while the
+  // epilogue publishes its last expert (it joins the down phase after).
+  if (warp < epi0) {
+    tc_fence_before();
     __syncwarp();
-    tc_barriers(pd, sm, true, tid);
+    named_bar(kBarSwitch, (int)blockDim.x);
+    tc_fence_after();
+    if (warp == 0) {
+      tc_barriers(pg, sm, false, tid);
+      __syncwarp();
+      tc_barriers(pd, sm, true, tid);
+    }
+    __syncwarp();
+    named_bar(kBarDownInit, 32 * epi0);
+    if (warp == 0) named_bar_arrive(kBarDownEpi, 32 + kEpiThreads);
+  } else {
+    __syncwarp();
+    named_bar(kBarDownEpi, 32 + kEpiThreads);
+    tc_fence_after();
   }
-  __syncthreads();
 
   tc_phase<false>(pd, &d_a, &d_b, &d_sfb, sm, tmem, n_act * pd.tiles, epi0, dn_claim);
 
