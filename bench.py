@@ -54,8 +54,8 @@ def _peaks():
 # active experts); valid only for the kernel source it was taken on.
 EXPERTS_TRAFFIC = {"source": ["speculative_decode_routed_gb300/csrc/experts_tc.cu",
                               "speculative_decode_routed_gb300/csrc/tc_ptx.cuh"],
-                   "sha256_prefix": "ee23f2db1005b57b", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": (1065511168 + 3129856) / 43}
+                   "sha256_prefix": "9b7046dacea0ef0a", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": (1065513984 + 3333120) / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
@@ -63,8 +63,23 @@ EXPERTS_TRAFFIC = {"source": ["speculative_decode_routed_gb300/csrc/experts_tc.c
 # launch at the bench's widths; valid only for the kernel source it was taken
 # on.
 DENSE_GATE_UP_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/gemv.cuh",
-                         "sha256_prefix": "a919c1e476a720c4", "hidden": 7168, "inter": 28672, "rows": 8,
-                         "bytes": 822260736 + 3262976}
+                         "sha256_prefix": "2557b235656f8a67", "hidden": 7168, "inter": 28672, "rows": 8,
+                         "bytes": 822262784 + 3353600}
+
+# The same for one launch of the context-KV projection's streaming kernel at
+# 8 rows (hidden 7168, 4 layers of 8 KV heads of 128).
+CTXKV_PROJ_TRAFFIC = {"source": "speculative_decode_routed_gb300/csrc/gemv.cuh",
+                      "sha256_prefix": "2557b235656f8a67", "shape": (7168, 4, 8, 128, 8),
+                      "bytes": 117915392 + 3609088}
+
+
+def _ctxkv_traffic(hidden: int, layers: int, kv_heads: int, head_dim: int, rows: int):
+    """Bytes per launch of the context-KV streaming projection from the ncu
+    capture, or None if the kernel changed since or the shape differs."""
+    t = CTXKV_PROJ_TRAFFIC
+    if not _source_unchanged(t) or (hidden, layers, kv_heads, head_dim, rows) != t["shape"]:
+        return None
+    return int(t["bytes"])
 
 
 def _source_unchanged(t) -> bool:
@@ -901,7 +916,8 @@ def run_ctxkv(args, w):
         "roofline": {"kernel": "K/V projection (split-K weight-streaming kernel, bf16 mma.sync)" if streamed
                      else "K/V projection (tcgen05 bf16 projection kernel)", "bound": "hbm",
                      "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gemm_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(gemm_gbs / peak, 4), "traffic": _ctxkv_traffic(H, L, KVH, D, n) if streamed
+                     else None, "peak_kind": peak_kind,
                      "launch_us": round(k_ms[1] * 1000, 2), "algorithmic_bytes": int(byt["gemm"])},
         "kernels_us": {"norms": round(k_ms[0] * 1000, 2), "projection": round(k_ms[1] * 1000, 2),
                        "key_norm_rope_cache": round(k_ms[2] * 1000, 2)},
