@@ -217,6 +217,26 @@ int plan_tc(moe::TcParams& p, int mode, const moe_decode_dims& d) {
   const int kps_opts[2] = {2, 1};
   const int kps_first = (!gu && d.inter % 256 == 0) ? 0 : 1;
   const int modes[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
+  if (!gu && kps_first == 0 && (p.KBLK + 1) / 2 <= 3) {
+    // down items of at most three stages (two K-blocks each): three issuers
+    // with three accumulator buffers each, so that three items are in flight
+    // between the MMAs and the epilogue (with two, a down item's epilogue
+    // latency paced the phase, and a fourth issuer had no stage to take).
+    // Measured: 8 chained layers of intermediate 1536, 133.2 against 134.4
+    // µs per layer-step; with four stages per item (intermediate 2048) the
+    // uneven split over three issuers cost 16 µs, so those keep four.
+    const uint32_t sfc = 16u * 2u * (1u + (uint32_t)p.nt_max);
+    const uint32_t cols = 3u * p.acc_cols + sfc;
+    if (3u * cols <= 512u) {
+      p.Q = 3;
+      p.P = 3;
+      p.KPS = 2;
+      p.dbuf = 3;
+      p.sfslots = 1;
+      p.sf_cols = sfc;
+      p.issuer_cols = cols;
+    }
+  }
   for (int qi = 0; qi < nq && !p.P; ++qi)
     for (int ki = kps_first; ki < 2 && !p.P; ++ki)
       for (int mi = 0; mi < 4 && !p.P; ++mi) {

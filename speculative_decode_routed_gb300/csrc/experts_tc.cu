@@ -75,8 +75,8 @@ constexpr int kItemRing = 4;  // items published ahead by the producer
 struct TcSmem {
   uint64_t* full;        // [NS][Q]   TMA bytes landed, one barrier per stage and K-phase group
   uint64_t* empty;       // [NS]      every issuer that reads the stage is done (T arrivals)
-  uint64_t* acc_full;    // [2]       accumulators ready for the epilogue (P arrivals)
-  uint64_t* acc_empty;   // [2]       epilogue done reading them (4 arrivals)
+  uint64_t* acc_full;    // [4]       accumulator buffer ready for the epilogue (P arrivals)
+  uint64_t* acc_empty;   // [4]       epilogue done reading it (4 arrivals)
   uint64_t* slot_free;   // [4][2]    an issuer's scale slot may be overwritten
   uint64_t* drain;       // [4]       every MMA of an issuer done
   uint64_t* item_full;   // [kItemRing]  an item published by the producer
@@ -95,13 +95,13 @@ __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
   s.full = reinterpret_cast<uint64_t*>(base);
   s.empty = s.full + 32;
   s.acc_full = s.empty + 16;
-  s.acc_empty = s.acc_full + 2;
-  s.slot_free = s.acc_empty + 2;
-  s.drain = s.slot_free + 8;                 // 64 barriers: 512 bytes
-  s.item_full = reinterpret_cast<uint64_t*>(base + 512);
+  s.acc_empty = s.acc_full + 4;
+  s.slot_free = s.acc_empty + 4;
+  s.drain = s.slot_free + 8;                 // 68 barriers: 544 bytes
+  s.item_full = reinterpret_cast<uint64_t*>(base + 576);
   s.item_empty = s.item_full + kItemRing;
-  s.items = reinterpret_cast<int4*>(base + 576);
-  s.pairs = reinterpret_cast<int*>(base + 640);
+  s.items = reinterpret_cast<int4*>(base + 640);
+  s.pairs = reinterpret_cast<int*>(base + 704);
   s.flag = s.pairs + kMaxPairsTc;
   s.tmem_base = reinterpret_cast<uint32_t*>(s.flag + 4);
   s.act = reinterpret_cast<unsigned*>(base + 1280);
@@ -115,7 +115,7 @@ __device__ __forceinline__ TcSmem tc_carve(uint8_t* base) {
 // shared memory takes the other projection's layout), spread over the lanes
 // of one warp: lane l takes the barriers j = l mod 32 of the list below.
 __device__ void tc_barriers(const TcParams& p, const TcSmem& sm, bool init, int lane) {
-  const int nfull = p.NS * p.Q, nb = nfull + p.NS + 4 + 8 + 4 + 2 * kItemRing;
+  const int nfull = p.NS * p.Q, nb = nfull + p.NS + 8 + 8 + 4 + 2 * kItemRing;
   for (int j = lane; j < nb; j += 32) {
     uint64_t* b;
     uint32_t count = 1;
@@ -125,13 +125,13 @@ __device__ void tc_barriers(const TcParams& p, const TcSmem& sm, bool init, int 
     } else if ((i -= nfull) < p.NS) {
       b = &sm.empty[i];
       count = (uint32_t)p.T;
-    } else if ((i -= p.NS) < 2) {
+    } else if ((i -= p.NS) < 4) {
       b = &sm.acc_full[i];
       count = (uint32_t)p.P;
-    } else if ((i -= 2) < 2) {
+    } else if ((i -= 4) < 4) {
       b = &sm.acc_empty[i];
       count = kEpiThreads / 32;
-    } else if ((i -= 2) < 8) {
+    } else if ((i -= 4) < 8) {
       b = &sm.slot_free[i];
     } else if ((i -= 8) < 4) {
       b = &sm.drain[i];
@@ -662,8 +662,8 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
         }
         if (v.x < 0) break;
         const int nt = (v.w + 31) / 32;
-        const int ab = (p.dbuf == 2) ? (j & 1) : 0;
-        const int use = (p.dbuf == 2) ? (j >> 1) : j;
+        const int ab = j % p.dbuf;  // accumulator buffer of item j
+        const int use = j / p.dbuf;
         if (use >= 1 && !mbar_wait(&sm.acc_empty[ab], (use - 1) & 1, lim)) {
           latch_error(ws.err, kDevWaitTimeout);
           break;
@@ -781,8 +781,8 @@ __device__ __forceinline__ void tc_phase(const TcParams& p, const CUtensorMap* t
           sc0 = __ldg(p.gscale + 3 * e + 2) * __ldcg(ws.h_sg + e);
         }
       }
-      const int ab = (p.dbuf == 2) ? (j & 1) : 0;
-      const int use = (p.dbuf == 2) ? (j >> 1) : j;
+      const int ab = j % p.dbuf;
+      const int use = j / p.dbuf;
       if (t == 0) *sm.flag = mbar_wait(&sm.acc_full[ab], use & 1, lim) ? 1 : 0;
       tc_named_sync();
       const bool got = *reinterpret_cast<volatile int*>(sm.flag) != 0;
