@@ -54,8 +54,8 @@ def _peaks():
 # active experts); valid only for the kernel source it was taken on.
 EXPERTS_TRAFFIC = {"source": ["speculative_decode_routed_gb300/csrc/experts_tc.cu",
                               "speculative_decode_routed_gb300/csrc/tc_ptx.cuh"],
-                   "sha256_prefix": "9b7046dacea0ef0a", "hidden": 7168, "inter": 2048,
-                   "bytes_per_active_expert": (1065513984 + 3333120) / 43}
+                   "sha256_prefix": "93a95c69758f057c", "hidden": 7168, "inter": 2048,
+                   "bytes_per_active_expert": (1065521920 + 3277568) / 43}
 
 
 # DRAM traffic (read + write) of one launch of the dense draft layer's
