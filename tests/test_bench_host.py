@@ -81,6 +81,17 @@ def test_traffic_figures_are_gated_on_their_capture(monkeypatch):
     assert bench._dense_traffic(wd.hidden, wd.inter, 8) is None
     monkeypatch.setitem(bench.EXPERTS_TRAFFIC, "sha256_prefix", "0" * 16)
     assert bench._experts_traffic(synth.WORKLOADS["serving"], 60.0) is None
+    # the context-KV projection's: the fp32 partials and the per-head counts
+    # come on top of the weights and activations
+    wc = synth.CTXKV_WORKLOADS["draft_ctx_kv"]
+    shape = (wc.hidden, wc.n_layers, wc.n_kv_heads, wc.head_dim, 8)
+    traffic = bench._ctxkv_traffic(*shape)
+    if traffic is not None:
+        ratio = traffic / bench._ctxkv_bytes(wc, 8)["gemm"]
+        assert 1.0 <= ratio < 1.04
+    assert bench._ctxkv_traffic(*shape[:4], 128) is None
+    monkeypatch.setitem(bench.CTXKV_PROJ_TRAFFIC, "sha256_prefix", "0" * 16)
+    assert bench._ctxkv_traffic(*shape) is None
 
 
 @pytest.mark.parametrize("workload", ["tiny", "draft_dense_small", "draft_ctx_kv_small"])
